@@ -1,0 +1,236 @@
+"""chunked_gated_delta_04_gb300 -- the chunked gated delta rule on GB300 (sm_103a).
+
+A thin ctypes binding over ``libgdr.so`` (C ABI in ``include/gdr.h``).  The entry
+points keep the C names (``gdr_fwd``, ``gdr_bwd``, ...) and only marshal
+arguments: every step of the computation runs in the library's CUDA kernels.
+PyTorch supplies device memory and the current stream.  There is no CPU path:
+if the library cannot be loaded, every call raises.
+
+Operator (FlashQLA PR #34, "SM120/121: Add support for fused backward kernel",
+Summary and "Current status"): S_t = exp(g_t) S_{t-1}(I - beta_t k_t k_t^T) +
+beta_t v_t k_t^T, o_t = scale * S_t q_t, evaluated in 64-token chunks, with its
+backward (dq, dk, dv, dg, dbeta, dS0 from dO and dS_T).
+
+High-level helpers: ``forward`` / ``backward`` allocate outputs and workspace with
+torch; ``chunk_gated_delta_rule`` is the autograd entry point.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdr.so")
+
+GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_ALIGNMENT, GDR_ERR_CUDA, GDR_ERR_TIMEOUT, \
+    GDR_ERR_WORKSPACE = range(7)
+GDR_DTYPE_F32, GDR_DTYPE_BF16 = 0, 1
+GDR_STATE_KV, GDR_STATE_VK = 0, 1
+CHUNK = 64
+
+
+class gdr_problem(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("Hk", ctypes.c_int), ("Hv", ctypes.c_int),
+                ("DK", ctypes.c_int), ("DV", ctypes.c_int), ("num_seqs", ctypes.c_int),
+                ("cu_seqlens", ctypes.c_void_p), ("dtype", ctypes.c_int), ("layout", ctypes.c_int),
+                ("scale", ctypes.c_float)]
+
+
+class GDRError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib_handle().gdr_status_string(status).decode() if _LIB is not None else str(status)
+        super().__init__(f"{where}: {msg}")
+
+
+_LIB = None
+
+EXPORTS = ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes", "gdr_bwd_workspace_bytes",
+           "gdr_fwd", "gdr_bwd", "gdr_workspace_status", "gdr_status_string", "gdr_path"]
+
+
+def _lib_handle():
+    """Load libgdr.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libgdr.so not built ({LIB_PATH}); run `python -m chunked_gated_delta_04_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER(gdr_problem)
+        vp, sz, i, u32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)
+        for name in ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes",
+                     "gdr_bwd_workspace_bytes"]:
+            getattr(lib, name).argtypes = [P]
+            getattr(lib, name).restype = sz
+        lib.gdr_path.argtypes = [P]
+        lib.gdr_path.restype = i
+        lib.gdr_fwd.argtypes = [P] + [vp] * 9 + [vp, sz, vp]
+        lib.gdr_fwd.restype = i
+        lib.gdr_bwd.argtypes = [P] + [vp] * 14 + [vp, sz, vp]
+        lib.gdr_bwd.restype = i
+        lib.gdr_workspace_status.argtypes = [vp, vp, u32p]
+        lib.gdr_workspace_status.restype = i
+        lib.gdr_status_string.argtypes = [i]
+        lib.gdr_status_string.restype = ctypes.c_char_p
+        _LIB = lib
+    return _LIB
+
+
+def load():
+    return _lib_handle()
+
+
+# ------------------------------------------------------------------ marshalling helpers
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_problem(B, T, Hk, Hv, DK, DV, dtype, layout="KV", cu_seqlens=None, num_seqs=None, scale=None):
+    """Build a gdr_problem.  dtype: torch.float32/bfloat16; layout "KV"/"VK"."""
+    p = gdr_problem()
+    p.B, p.T, p.Hk, p.Hv, p.DK, p.DV = B, T, Hk, Hv, DK, DV
+    if cu_seqlens is not None:
+        p.cu_seqlens = _ptr(cu_seqlens)
+        p.num_seqs = (cu_seqlens.numel() - 1) if num_seqs is None else num_seqs
+    else:
+        p.cu_seqlens = None
+        p.num_seqs = B if num_seqs is None else num_seqs
+    p.dtype = GDR_DTYPE_BF16 if dtype == torch.bfloat16 else (GDR_DTYPE_F32 if dtype == torch.float32 else 99)
+    p.layout = {"KV": GDR_STATE_KV, "VK": GDR_STATE_VK}.get(layout, 99) if isinstance(layout, str) else layout
+    p.scale = 0.0 if scale is None else float(scale)
+    return p
+
+
+def gdr_max_chunks(p) -> int:
+    return _lib_handle().gdr_max_chunks(ctypes.byref(p))
+
+
+def gdr_saved_states_bytes(p) -> int:
+    return _lib_handle().gdr_saved_states_bytes(ctypes.byref(p))
+
+
+def gdr_fwd_workspace_bytes(p) -> int:
+    return _lib_handle().gdr_fwd_workspace_bytes(ctypes.byref(p))
+
+
+def gdr_bwd_workspace_bytes(p) -> int:
+    return _lib_handle().gdr_bwd_workspace_bytes(ctypes.byref(p))
+
+
+def gdr_path(p) -> int:
+    return _lib_handle().gdr_path(ctypes.byref(p))
+
+
+def gdr_fwd(p, q, k, v, g, beta, S0, o, S_T, h_saved, workspace, workspace_bytes=None, stream=None) -> int:
+    """C gdr_fwd on tensors / raw device pointers; returns the status code."""
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    return _lib_handle().gdr_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(S0),
+                                 _ptr(o), _ptr(S_T), _ptr(h_saved), _ptr(workspace), wb, _stream_ptr(stream))
+
+
+def gdr_bwd(p, q, k, v, g, beta, h_saved, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, workspace,
+            workspace_bytes=None, stream=None) -> int:
+    """C gdr_bwd on tensors / raw device pointers; returns the status code."""
+    wb = workspace.numel() * workspace.element_size() if workspace_bytes is None else workspace_bytes
+    return _lib_handle().gdr_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                 _ptr(h_saved), _ptr(dO), _ptr(dS_T), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
+                                 _ptr(dbeta), _ptr(dS0), _ptr(workspace), wb, _stream_ptr(stream))
+
+
+def gdr_workspace_status(workspace, stream=None):
+    """Synchronises the stream; returns (status, raw flag bits)."""
+    flags = ctypes.c_uint32(0)
+    st = _lib_handle().gdr_workspace_status(_ptr(workspace), _stream_ptr(stream), ctypes.byref(flags))
+    return st, flags.value
+
+
+def gdr_status_string(s: int) -> str:
+    return _lib_handle().gdr_status_string(s).decode()
+
+
+def _check(st, where):
+    if st != GDR_OK:
+        raise GDRError(st, where)
+
+
+def _problem_for(q, v, cu_seqlens, layout, scale):
+    B, T, Hk, DK = q.shape
+    Hv, DV = v.shape[2], v.shape[3]
+    return make_problem(B, T, Hk, Hv, DK, DV, q.dtype, layout, cu_seqlens, scale=scale)
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's allocator returns 512-byte aligned blocks, which covers the 256-byte requirement
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------ allocating helpers
+def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, layout="KV", scale=None, output_final_state=True,
+            workspace=None, stream=None):
+    """Run gdr_fwd; returns (o, S_T or None, h_saved)."""
+    p = _problem_for(q, v, cu_seqlens, layout, scale)
+    dev = q.device
+    N = p.num_seqs
+    o = torch.empty_like(v)
+    sshape = (N, p.Hv, p.DK, p.DV) if layout == "KV" else (N, p.Hv, p.DV, p.DK)
+    S_T = torch.empty(sshape, dtype=torch.float32, device=dev) if output_final_state else None
+    h_saved = torch.empty((gdr_max_chunks(p), p.Hv, p.DK, p.DV), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(gdr_fwd_workspace_bytes(p), dev)
+    _check(gdr_fwd(p, q, k, v, g, beta, S0, o, S_T, h_saved, workspace, stream=stream), "gdr_fwd")
+    return o, S_T, h_saved
+
+
+def backward(q, k, v, g, beta, h_saved, dO, dS_T=None, cu_seqlens=None, layout="KV", scale=None,
+             want_dS0=True, workspace=None, stream=None):
+    """Run gdr_bwd; returns (dq, dk, dv, dg, dbeta, dS0 or None)."""
+    p = _problem_for(q, v, cu_seqlens, layout, scale)
+    dev = q.device
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg = torch.empty_like(g)
+    dbeta = torch.empty_like(beta)
+    N = p.num_seqs
+    sshape = (N, p.Hv, p.DK, p.DV) if layout == "KV" else (N, p.Hv, p.DV, p.DK)
+    dS0 = torch.empty(sshape, dtype=torch.float32, device=dev) if want_dS0 else None
+    if workspace is None:
+        workspace = alloc_workspace(gdr_bwd_workspace_bytes(p), dev)
+    _check(gdr_bwd(p, q, k, v, g, beta, h_saved, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, workspace, stream=stream),
+           "gdr_bwd")
+    return dq, dk, dv, dg, dbeta, dS0
+
+
+class _GDRFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, S0, cu_seqlens, layout, scale):
+        o, S_T, h_saved = forward(q, k, v, g, beta, S0, cu_seqlens, layout, scale)
+        ctx.save_for_backward(q, k, v, g, beta, h_saved, cu_seqlens)
+        ctx.layout, ctx.scale, ctx.has_S0 = layout, scale, S0 is not None
+        return o, S_T
+
+    @staticmethod
+    def backward(ctx, do, dS_T):
+        q, k, v, g, beta, h_saved, cu_seqlens = ctx.saved_tensors
+        dq, dk, dv, dg, dbeta, dS0 = backward(q, k, v, g, beta, h_saved, do.contiguous(),
+                                              None if dS_T is None else dS_T.contiguous(), cu_seqlens,
+                                              ctx.layout, ctx.scale, want_dS0=ctx.has_S0)
+        return dq, dk, dv, dg, dbeta, dS0, None, None, None
+
+
+def chunk_gated_delta_rule(q, k, v, g, beta, initial_state=None, cu_seqlens=None, layout="KV", scale=None):
+    """Autograd entry point: returns (o, final_state).  Tensors as in include/gdr.h."""
+    return _GDRFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, layout, scale)

@@ -1,0 +1,197 @@
+// gdr_api.cu -- the C ABI (include/gdr.h): validation, workspace layout, dispatch.
+//
+// Host code only.  It never reads tensor contents, never allocates device memory
+// and never synchronises, except gdr_workspace_status (documented to synchronise).
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "gdr_internal.h"
+
+namespace gdr {
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Fills *d from *p; returns GDR_OK or the reason the problem is rejected.
+gdr_status resolve(const gdr_problem* p, Dims* d) {
+  if (p == nullptr) return GDR_ERR_INVALID_ARG;
+  if (p->B < 0 || p->T < 0 || p->Hk <= 0 || p->Hv <= 0 || p->DK <= 0 || p->DV <= 0 || p->num_seqs < 0)
+    return GDR_ERR_INVALID_ARG;
+  if (p->Hv % p->Hk != 0) return GDR_ERR_INVALID_ARG;
+  if (p->dtype != GDR_DTYPE_F32 && p->dtype != GDR_DTYPE_BF16) return GDR_ERR_INVALID_ARG;
+  if (p->layout != GDR_STATE_KV && p->layout != GDR_STATE_VK) return GDR_ERR_INVALID_ARG;
+  if (p->cu_seqlens != nullptr) {
+    if (p->B != 1) return GDR_ERR_INVALID_ARG;
+  } else if (p->num_seqs != p->B) {
+    return GDR_ERR_INVALID_ARG;
+  }
+  if (p->DK % 16 != 0 || p->DV % 16 != 0 || p->DK > 128 || p->DV > 128) return GDR_ERR_UNSUPPORTED;
+  const long long T_total = (long long)p->B * p->T;
+  if (T_total >= (1ll << 31) / (p->Hv > p->Hk ? p->Hv : p->Hk)) return GDR_ERR_UNSUPPORTED;
+  long long maxc = p->cu_seqlens ? (long long)p->T / kChunk + p->num_seqs
+                                 : (long long)p->B * ((p->T + kChunk - 1) / kChunk);
+  if (maxc >= (1ll << 31) / p->Hv) return GDR_ERR_UNSUPPORTED;
+  d->B = p->B;
+  d->T = p->T;
+  d->Hk = p->Hk;
+  d->Hv = p->Hv;
+  d->DK = p->DK;
+  d->DV = p->DV;
+  d->G = p->Hv / p->Hk;
+  d->num_seqs = p->num_seqs;
+  d->T_total = T_total;
+  d->max_chunks = (int)maxc;
+  d->scale = p->scale > 0.f ? p->scale : (float)(1.0 / sqrt((double)p->DK));
+  d->dtype = p->dtype;
+  d->layout = p->layout;
+  d->cu = p->cu_seqlens;
+  d->path = (p->dtype == GDR_DTYPE_BF16 && p->DK == 128 && p->DV == 128 && tc_available()) ? 1 : 0;
+  return GDR_OK;
+}
+
+}  // namespace
+
+size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws) {
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> char* {
+    char* p = base ? base + off : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  Workspace w;
+  memset(&w, 0, sizeof(w));
+  const size_t chH = (size_t)d.max_chunks * d.Hv;
+  const size_t el = d.path == 1 ? 2 : 4;  // intermediates: bf16 on the tensor-core path
+  w.status = (uint32_t*)take(256);
+  w.chunks = (int4*)take(sizeof(int4) * (size_t)d.max_chunks);
+  w.seq_chunk_off = (int*)take(sizeof(int) * ((size_t)d.num_seqs + 1));
+  w.seq_order = (int*)take(sizeof(int) * ((size_t)d.num_seqs + 1));
+  w.gam = (float*)take(sizeof(float) * chH * kChunk);
+  w.W = take(el * chH * kChunk * d.DK);
+  w.U = take(el * chH * kChunk * d.DV);
+  w.Vn = take(el * chH * kChunk * d.DV);
+  if (d.path == 1) w.P = take(el * chH * kChunk * kChunk);
+  if (backward) {
+    if (d.path == 0) w.Tm = (float*)take(sizeof(float) * chH * kChunk * kChunk);
+    w.dhp = (float*)take(sizeof(float) * chH * d.DK * d.DV);
+    if (d.G > 1) {
+      w.dq_part = (float*)take(sizeof(float) * (size_t)d.T_total * d.Hv * d.DK);
+      w.dk_part = (float*)take(sizeof(float) * (size_t)d.T_total * d.Hv * d.DK);
+    }
+  }
+  if (ws) *ws = w;
+  return off;
+}
+
+}  // namespace gdr
+
+using namespace gdr;
+
+extern "C" {
+
+size_t gdr_max_chunks(const gdr_problem* p) {
+  Dims d;
+  return resolve(p, &d) == GDR_OK ? (size_t)d.max_chunks : 0;
+}
+
+size_t gdr_saved_states_bytes(const gdr_problem* p) {
+  Dims d;
+  if (resolve(p, &d) != GDR_OK) return 0;
+  return (size_t)d.max_chunks * d.Hv * d.DK * d.DV * sizeof(float);
+}
+
+size_t gdr_fwd_workspace_bytes(const gdr_problem* p) {
+  Dims d;
+  if (resolve(p, &d) != GDR_OK) return 0;
+  return layout_workspace(d, false, nullptr, nullptr);
+}
+
+size_t gdr_bwd_workspace_bytes(const gdr_problem* p) {
+  Dims d;
+  if (resolve(p, &d) != GDR_OK) return 0;
+  return layout_workspace(d, true, nullptr, nullptr);
+}
+
+int gdr_path(const gdr_problem* p) {
+  Dims d;
+  return resolve(p, &d) == GDR_OK ? d.path : -1;
+}
+
+gdr_status gdr_fwd(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                   const void* beta, const float* S0, void* o, float* S_T, float* h_saved, void* workspace,
+                   size_t workspace_bytes, gdr_stream_t stream) {
+  Dims d;
+  gdr_status st = resolve(p, &d);
+  if (st != GDR_OK) return st;
+  const bool any_tokens = d.T_total > 0;
+  if (any_tokens && (!q || !k || !v || !g || !beta || !o || !h_saved)) return GDR_ERR_INVALID_ARG;
+  if (!workspace) return GDR_ERR_WORKSPACE;
+  const void* ptrs[] = {q, k, v, g, beta, S0, o, S_T, h_saved, p->cu_seqlens};
+  for (const void* x : ptrs)
+    if (x && !aligned16(x)) return GDR_ERR_ALIGNMENT;
+  if (((uintptr_t)workspace & 255u) != 0) return GDR_ERR_ALIGNMENT;
+  Workspace ws;
+  const size_t need = layout_workspace(d, false, (char*)workspace, &ws);
+  if (workspace_bytes < need) return GDR_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  FwdArgs a{q, k, v, g, beta, S0, o, S_T, h_saved};
+  cudaError_t e = launch_index(d, ws, s);
+  if (e == cudaSuccess) e = d.path == 1 ? tc_forward(d, a, ws, s) : simt_forward(d, a, ws, s);
+  return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                   const void* beta, const float* h_saved, const void* dO, const float* dS_T, void* dq,
+                   void* dk, void* dv, float* dg, void* dbeta, float* dS0, void* workspace,
+                   size_t workspace_bytes, gdr_stream_t stream) {
+  Dims d;
+  gdr_status st = resolve(p, &d);
+  if (st != GDR_OK) return st;
+  const bool any_tokens = d.T_total > 0;
+  if (any_tokens && (!q || !k || !v || !g || !beta || !h_saved || !dO || !dq || !dk || !dv || !dg || !dbeta))
+    return GDR_ERR_INVALID_ARG;
+  if (!workspace) return GDR_ERR_WORKSPACE;
+  const void* ptrs[] = {q, k, v, g, beta, h_saved, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, p->cu_seqlens};
+  for (const void* x : ptrs)
+    if (x && !aligned16(x)) return GDR_ERR_ALIGNMENT;
+  if (((uintptr_t)workspace & 255u) != 0) return GDR_ERR_ALIGNMENT;
+  Workspace ws;
+  const size_t need = layout_workspace(d, true, (char*)workspace, &ws);
+  if (workspace_bytes < need) return GDR_ERR_WORKSPACE;
+  cudaStream_t s = (cudaStream_t)stream;
+  BwdArgs a{q, k, v, g, beta, h_saved, dO, dS_T, dq, dk, dv, dg, dbeta, dS0};
+  cudaError_t e = launch_index(d, ws, s);
+  if (e == cudaSuccess) e = d.path == 1 ? tc_backward(d, a, ws, s) : simt_backward(d, a, ws, s);
+  return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_workspace_status(const void* workspace, gdr_stream_t stream, uint32_t* flags) {
+  if (!workspace) return GDR_ERR_WORKSPACE;
+  uint32_t word = 0;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GDR_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDR_ERR_CUDA;
+  if (flags) *flags = word;
+  if (word & kDevErrBadCuSeqlens) return GDR_ERR_INVALID_ARG;
+  if (word & (kDevErrTimeoutFwd | kDevErrTimeoutBwd | kDevErrTimeoutPrep)) return GDR_ERR_TIMEOUT;
+  return GDR_OK;
+}
+
+const char* gdr_status_string(gdr_status s) {
+  switch (s) {
+    case GDR_OK: return "GDR_OK";
+    case GDR_ERR_INVALID_ARG: return "GDR_ERR_INVALID_ARG: invalid argument";
+    case GDR_ERR_UNSUPPORTED: return "GDR_ERR_UNSUPPORTED: unsupported shape or dtype";
+    case GDR_ERR_ALIGNMENT: return "GDR_ERR_ALIGNMENT: pointer not 16-byte aligned (workspace: 256)";
+    case GDR_ERR_CUDA: return "GDR_ERR_CUDA: a CUDA call failed";
+    case GDR_ERR_TIMEOUT: return "GDR_ERR_TIMEOUT: a kernel's bounded wait ran out";
+    case GDR_ERR_WORKSPACE: return "GDR_ERR_WORKSPACE: workspace missing or too small";
+  }
+  return "unknown gdr_status";
+}
+
+}  // extern "C"

@@ -1,0 +1,128 @@
+// gdr_index.cu -- K0: the chunk index of a (possibly variable-length) batch.
+//
+// Chunks restart at every sequence start (chunked gated delta rule, FlashQLA PR
+// #34, "Current status": fixed-length and variable-length inputs).  For sequence n
+// of length L_n the index holds chunk_offset[n] = sum_{n'<n} ceil(L_n'/64) and, per
+// global chunk c, {seq, first packed token, length (1..64), chunk index within the
+// sequence}.  Slots past the last real chunk get length 0 (no work).  The order
+// of sequences for the sequential kernels is longest first.  Everything is
+// computed on the device from cu_seqlens, so the host never reads tensor data.
+#include "gdr_device.cuh"
+#include "gdr_internal.h"
+
+namespace gdr {
+
+constexpr int kIndexThreads = 1024;
+constexpr int kMaxOrderedSeqs = 8192;  // above this the order is the identity
+
+__global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t* __restrict__ cu,
+                                                                  int num_seqs, int T, int max_chunks,
+                                                                  int4* __restrict__ chunks,
+                                                                  int* __restrict__ off,
+                                                                  int* __restrict__ order,
+                                                                  uint32_t* __restrict__ status) {
+  __shared__ int warp_tot[32];
+  __shared__ int s_bad;
+  __shared__ int s_carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int w = 0; w < 64; ++w) status[w] = 0u;  // fresh status for this call
+    s_bad = 0;
+    s_carry = 0;
+  }
+  __syncthreads();
+  // validate cu_seqlens: cu[0] == 0, non-decreasing, cu[num_seqs] == T
+  if (cu != nullptr) {
+    for (int n = tid; n < num_seqs; n += kIndexThreads) {
+      const int a = cu[n], b = cu[n + 1];
+      if (b < a || a < 0 || b > T) s_bad = 1;
+    }
+    if (tid == 0 && (cu[0] != 0 || cu[num_seqs] != T)) s_bad = 1;
+  }
+  __syncthreads();
+  const bool bad = s_bad != 0;
+  if (bad && tid == 0) status[0] |= kDevErrBadCuSeqlens;
+
+  // exclusive scan of ceil(L/64) over sequences, in tiles of kIndexThreads
+  for (int base = 0; base < num_seqs; base += kIndexThreads) {
+    const int n = base + tid;
+    int nc = 0;
+    if (n < num_seqs && !bad) {
+      const int L = cu ? cu[n + 1] - cu[n] : T;
+      nc = (L + kChunk - 1) / kChunk;
+    }
+    int x = nc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int t = warp_tot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, t, o);
+        if (lane >= o) t += y;
+      }
+      warp_tot[lane] = t;  // inclusive prefix over warps
+    }
+    __syncthreads();
+    const int carry = s_carry;
+    const int incl = x + (warp > 0 ? warp_tot[warp - 1] : 0);
+    if (n < num_seqs) off[n] = carry + incl - nc;
+    __syncthreads();
+    if (tid == kIndexThreads - 1) s_carry = carry + incl;
+    __syncthreads();
+  }
+  int total = s_carry;
+  if (total > max_chunks) {  // only reachable with an inconsistent cu_seqlens
+    if (tid == 0) status[0] |= kDevErrBadCuSeqlens;
+    total = 0;
+  }
+  if (tid == 0) off[num_seqs] = total;
+  __syncthreads();
+
+  for (int c = tid; c < max_chunks; c += kIndexThreads) {
+    int4 ci = make_int4(-1, 0, 0, 0);
+    if (c < total) {
+      int lo = 0, hi = num_seqs - 1;  // last n with off[n] <= c
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= c) lo = mid; else hi = mid - 1;
+      }
+      const int n = lo;
+      const int start = cu ? cu[n] : n * T;
+      const int L = cu ? cu[n + 1] - cu[n] : T;
+      const int local = c - off[n];
+      const int len = min(kChunk, L - local * kChunk);
+      ci = make_int4(n, start + local * kChunk, len, local);
+    }
+    chunks[c] = ci;
+  }
+
+  // longest-first order (stable: ties keep index order)
+  if (num_seqs <= kMaxOrderedSeqs && !bad) {
+    for (int n = tid; n < num_seqs; n += kIndexThreads) {
+      const int Ln = cu ? cu[n + 1] - cu[n] : T;
+      int rank = 0;
+      for (int m = 0; m < num_seqs; ++m) {
+        const int Lm = cu ? cu[m + 1] - cu[m] : T;
+        rank += (Lm > Ln) || (Lm == Ln && m < n);
+      }
+      order[rank] = n;
+    }
+  } else {
+    for (int n = tid; n < num_seqs; n += kIndexThreads) order[n] = n;
+  }
+}
+
+cudaError_t launch_index(const Dims& d, const Workspace& ws, cudaStream_t s) {
+  gdr_index_kernel<<<1, kIndexThreads, 0, s>>>(d.cu, d.num_seqs, d.cu ? (int)d.T_total : d.T,
+                                               d.max_chunks, ws.chunks, ws.seq_chunk_off, ws.seq_order,
+                                               ws.status);
+  return cudaGetLastError();
+}
+
+}  // namespace gdr

@@ -1,0 +1,92 @@
+// gdr_internal.h -- declarations shared by the library's translation units
+// (host API, index kernel, SIMT kernels, tcgen05 kernels).  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gdr.h"
+
+namespace gdr {
+
+constexpr int kChunk = 64;  // chunk length of the chunked method (tokens)
+
+// Status-word bits written by kernels (workspace header, word 0).
+enum : uint32_t {
+  kDevErrBadCuSeqlens = 1u << 0,  // cu_seqlens not 0..T non-decreasing: nothing computed
+  kDevErrTimeoutFwd = 1u << 1,    // a bounded wait in a forward kernel ran out
+  kDevErrTimeoutBwd = 1u << 2,    // a bounded wait in a backward kernel ran out
+  kDevErrTimeoutPrep = 1u << 3,   // a bounded wait in the chunk-prep kernel ran out
+};
+
+// Resolved problem.
+struct Dims {
+  int B, T, Hk, Hv, DK, DV, G, num_seqs;
+  long long T_total;  // B * T
+  int max_chunks;
+  float scale;
+  int dtype;   // gdr_dtype
+  int layout;  // gdr_state_layout
+  const int32_t* cu;  // device cu_seqlens or nullptr
+  int path;    // 1 = tcgen05, 0 = SIMT
+};
+
+// Pointers into the caller's workspace.  Every region starts 256-byte aligned.
+struct Workspace {
+  uint32_t* status;    // [64] words; word 0 = status bits above
+  int4* chunks;        // [max_chunks] {seq, t0 (packed token index), len, local chunk index}
+  int* seq_chunk_off;  // [num_seqs + 1]
+  int* seq_order;      // [num_seqs] sequences, longest first
+  // intermediates (fp32 on the SIMT path, bf16 on the tensor-core path)
+  void* W;       // [max_chunks][Hv][64][DK]
+  void* U;       // [max_chunks][Hv][64][DV]
+  void* P;       // tensor-core path: [max_chunks][Hv][64][64]
+  float* gam;    // [max_chunks][Hv][64] in-chunk cumsum of g
+  void* Vn;      // [max_chunks][Hv][64][DV]
+  float* Tm;     // SIMT backward: [max_chunks][Hv][64][64]
+  float* dhp;    // backward: [max_chunks][Hv][DK][DV] state gradient at each chunk's end
+  float* dq_part;  // backward, Hv > Hk: [T_total][Hv][DK]
+  float* dk_part;  // backward, Hv > Hk: [T_total][Hv][DK]
+};
+
+// Computes the workspace layout; with base == nullptr only the size is returned.
+size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws);
+
+struct FwdArgs {
+  const void *q, *k, *v;
+  const float* g;
+  const void* beta;
+  const float* S0;
+  void* o;
+  float* S_T;
+  float* h_saved;
+};
+
+struct BwdArgs {
+  const void *q, *k, *v;
+  const float* g;
+  const void* beta;
+  const float* h_saved;
+  const void* dO;
+  const float* dS_T;
+  void *dq, *dk, *dv;
+  float* dg;
+  void* dbeta;
+  float* dS0;
+};
+
+// K0: chunk index (chunks, seq offsets, longest-first order) and status reset.
+cudaError_t launch_index(const Dims& d, const Workspace& ws, cudaStream_t s);
+
+// fp32 SIMT kernels (any supported shape and dtype).
+cudaError_t simt_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s);
+cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cudaStream_t s);
+
+// tcgen05 kernels (bf16, DK = DV = 128).  tc_available() is false when this build
+// leaves them out.
+bool tc_available();
+cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s);
+cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cudaStream_t s);
+
+}  // namespace gdr

@@ -1,0 +1,136 @@
+/*
+ * gdr.h -- C ABI of the GB300 (sm_103a) chunked gated delta rule library (libgdr.so).
+ *
+ * The operator (FlashQLA PR #34, "SM120/121: Add support for fused backward
+ * kernel", Summary: the forward and the fused backward "fused_gdr_bwd" of the
+ * chunked gated delta rule; "Current status": fixed-length and variable-length
+ * inputs, KV/VK state layouts, initial/final states, autograd).  The pages do not
+ * write the recurrence out; it is fixed as
+ *
+ *     S_t = exp(g_t) S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T,
+ *     o_t = scale * S_t q_t,        S in R^{DV x DK},  scale = 1/sqrt(DK) by default,
+ *
+ * evaluated in 64-token chunks that restart at every sequence start.  The
+ * backward takes dL/do and dL/dS_T and returns dq, dk, dv, dg, dbeta, dS0.
+ *
+ * Conventions shared by every entry point
+ *  - Ownership: the caller allocates every buffer (device memory unless stated)
+ *    and keeps it alive until the work on `stream` has finished.  The library
+ *    never allocates device memory, keeps no device state between calls and
+ *    never synchronises the stream (except gdr_workspace_status, which says so).
+ *  - Asynchrony: all work is enqueued on `stream`; a GDR_OK return means the
+ *    launches were enqueued, not that they finished.
+ *  - Validation: arguments are checked on the host before anything is launched,
+ *    without reading any tensor contents.  On an error nothing is launched and
+ *    the outputs are untouched.
+ *  - Tensor layouts (all contiguous, row-major, base pointers 16-byte aligned):
+ *      q, k, dq, dk       [B, T, Hk, DK]     dtype
+ *      v, o, dO, dv       [B, T, Hv, DV]     dtype
+ *      g, dg              [B, T, Hv]         float32 (log decay, usually <= 0)
+ *      beta, dbeta        [B, T, Hv]         dtype
+ *      S0, S_T, dS_T, dS0 [num_seqs, Hv, DK, DV] float32 for GDR_STATE_KV (stores S^T),
+ *                         [num_seqs, Hv, DV, DK] float32 for GDR_STATE_VK (stores S)
+ *      h_saved            [max_chunks, Hv, DK, DV] float32: S^T at the START of every
+ *                         64-token chunk, whatever the state layout; chunk c of sequence
+ *                         n sits at index chunk_offset[n] + c with
+ *                         chunk_offset[n] = sum_{n' < n} ceil(L_n' / 64).  Slots past
+ *                         the last real chunk (varlen upper bound) are left untouched.
+ *    Variable length: B = 1, T = total tokens, cu_seqlens (device, int32,
+ *    num_seqs + 1 entries, cu_seqlens[0] = 0, non-decreasing, last = T) delimits the
+ *    sequences; empty sequences are allowed (S_T = S0, dS0 = dS_T).
+ *  - Heads: v-head j uses q/k head j / (Hv / Hk); g and beta are per v-head.
+ *  - Supported shapes: Hv % Hk == 0; DK, DV in {16, 32, 48, ..., 128} (multiples of
+ *    16).  dtype BF16 with DK = DV = 128 runs the tcgen05 tensor-core kernels; every
+ *    other supported case runs the fp32 SIMT kernels (fp32 arithmetic throughout).
+ *  - Errors inside a kernel (a bounded wait that ran out) are recorded in the
+ *    workspace's status word and the kernel returns early without trapping; read
+ *    it with gdr_workspace_status.
+ */
+#ifndef GDR_H_
+#define GDR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gdr_stream_t; /* = cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  GDR_OK = 0,
+  GDR_ERR_INVALID_ARG = 1, /* null required pointer, bad shape, bad enum value */
+  GDR_ERR_UNSUPPORTED = 2, /* a shape/dtype combination this build does not implement */
+  GDR_ERR_ALIGNMENT = 3,   /* a base pointer is not 16-byte aligned */
+  GDR_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, tensor map, ...) */
+  GDR_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out (see gdr_workspace_status) */
+  GDR_ERR_WORKSPACE = 6    /* workspace missing or smaller than the size query returned */
+} gdr_status;
+
+typedef enum { GDR_DTYPE_F32 = 0, GDR_DTYPE_BF16 = 1 } gdr_dtype;
+
+typedef enum { GDR_STATE_KV = 0, GDR_STATE_VK = 1 } gdr_state_layout;
+
+typedef struct {
+  int B, T;                  /* fixed length: B sequences of T tokens; varlen: B = 1, T = total */
+  int Hk, Hv, DK, DV;        /* q/k heads, v heads (Hv % Hk == 0), key and value widths */
+  int num_seqs;              /* fixed length: = B; varlen: number of sequences */
+  const int32_t* cu_seqlens; /* device pointer (varlen) or NULL (fixed length) */
+  gdr_dtype dtype;           /* dtype of q, k, v, beta, o, dO, dq, dk, dv, dbeta */
+  gdr_state_layout layout;   /* orientation of S0, S_T, dS_T, dS0 */
+  float scale;               /* output scale; <= 0 selects 1/sqrt(DK) */
+} gdr_problem;
+
+/* Upper bound on the number of 64-token chunks: B * ceil(T/64) for fixed length,
+ * floor(T/64) + num_seqs for varlen.  Returns 0 for an invalid problem. */
+size_t gdr_max_chunks(const gdr_problem* p);
+
+/* Bytes of h_saved: gdr_max_chunks(p) * Hv * DK * DV * 4. */
+size_t gdr_saved_states_bytes(const gdr_problem* p);
+
+/* Bytes of the scratch workspace that gdr_fwd / gdr_bwd need (device memory,
+ * 256-byte aligned).  Its contents need not be initialised and are not meaningful
+ * after the call, except the status word read by gdr_workspace_status. */
+size_t gdr_fwd_workspace_bytes(const gdr_problem* p);
+size_t gdr_bwd_workspace_bytes(const gdr_problem* p);
+
+/* Forward (chunked gated delta rule, FlashQLA PR #34 Summary).
+ *   in : q, k, v, g, beta; S0 (nullable: zero initial state)
+ *   out: o; S_T (nullable: final state not written); h_saved (required: the
+ *        chunk-start states that gdr_bwd consumes)
+ * workspace/workspace_bytes: see gdr_fwd_workspace_bytes. */
+gdr_status gdr_fwd(const gdr_problem* p, const void* q, const void* k, const void* v,
+                   const float* g, const void* beta, const float* S0, void* o, float* S_T,
+                   float* h_saved, void* workspace, size_t workspace_bytes, gdr_stream_t stream);
+
+/* Backward (the fused backward "fused_gdr_bwd" of FlashQLA PR #34: walks the chunks
+ * in reverse carrying the state gradient dh).
+ *   in : q, k, v, g, beta, h_saved (as written by gdr_fwd for the same inputs and S0),
+ *        dO, dS_T (nullable: zero)
+ *   out: dq, dk (summed over the Hv/Hk v-heads of each q/k head), dv, dg, dbeta;
+ *        dS0 (nullable: not written).  All outputs are overwritten.
+ * The result is bitwise deterministic: no floating-point atomics. */
+gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const void* v,
+                   const float* g, const void* beta, const float* h_saved, const void* dO,
+                   const float* dS_T, void* dq, void* dk, void* dv, float* dg, void* dbeta,
+                   float* dS0, void* workspace, size_t workspace_bytes, gdr_stream_t stream);
+
+/* Synchronises `stream`, then reads the status word that the kernels of the last
+ * gdr_fwd / gdr_bwd using `workspace` left there: GDR_OK, or GDR_ERR_TIMEOUT if a
+ * bounded wait ran out (the kernel returned early; its outputs are invalid).
+ * *flags (nullable) receives the raw bit set (bit i = kernel role i). */
+gdr_status gdr_workspace_status(const void* workspace, gdr_stream_t stream, uint32_t* flags);
+
+/* Human-readable name of a status code (static storage). */
+const char* gdr_status_string(gdr_status s);
+
+/* Which kernel family a problem runs on: 1 = tcgen05 tensor-core kernels,
+ * 0 = fp32 SIMT kernels, -1 = invalid or unsupported problem. */
+int gdr_path(const gdr_problem* p);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_H_ */

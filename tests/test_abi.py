@@ -1,0 +1,99 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads, exports every
+function declared in include/gdr.h, sizes its buffers correctly and rejects bad
+arguments with a status code before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import chunked_gated_delta_04_gb300 as gdr
+from chunked_gated_delta_04_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdr.load()
+
+
+def declared_functions():
+    hdr = open(os.path.join(ROOT, "include", "gdr.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdr_[a-z0-9_]+)\s*\(", hdr)))
+
+
+def test_library_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert "gdr_fwd" in names and "gdr_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(gdr.EXPORTS)
+
+
+def prob(**kw):
+    args = dict(B=2, T=130, Hk=2, Hv=4, DK=64, DV=32, dtype=torch.bfloat16, layout="KV")
+    args.update(kw)
+    return gdr.make_problem(**args)
+
+
+def test_size_queries(lib):
+    p = prob()
+    assert gdr.gdr_max_chunks(p) == 2 * 3
+    assert gdr.gdr_saved_states_bytes(p) == 6 * 4 * 64 * 32 * 4
+    assert gdr.gdr_fwd_workspace_bytes(p) > 0
+    assert gdr.gdr_bwd_workspace_bytes(p) > gdr.gdr_fwd_workspace_bytes(p)
+    # varlen bound: floor(T/64) + num_seqs
+    cu = torch.tensor([0, 1, 65, 300], dtype=torch.int32)
+    pv = gdr.make_problem(1, 300, 1, 1, 32, 32, torch.float32, "VK", cu_seqlens=cu)
+    assert gdr.gdr_max_chunks(pv) == 300 // 64 + 3
+    assert gdr.gdr_path(prob(DK=128, DV=128)) in (0, 1)
+    assert gdr.gdr_path(prob(dtype=torch.float32)) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hv=3), gdr.GDR_ERR_INVALID_ARG),          # Hv % Hk != 0
+    (dict(DK=72), gdr.GDR_ERR_UNSUPPORTED),         # not a multiple of 16
+    (dict(DV=256), gdr.GDR_ERR_UNSUPPORTED),        # wider than 128
+    (dict(layout=7), gdr.GDR_ERR_INVALID_ARG),
+    (dict(dtype=torch.float16), gdr.GDR_ERR_INVALID_ARG),
+    (dict(T=-1), gdr.GDR_ERR_INVALID_ARG),
+])
+def test_bad_problems_are_rejected(lib, kw, code):
+    p = prob(**kw)
+    fake = 1 << 20  # never dereferenced: validation fails first
+    st = gdr.gdr_fwd(p, fake, fake, fake, fake, fake, None, fake, None, fake, fake, workspace_bytes=1 << 30,
+                     stream=0)
+    assert st == code
+    assert gdr.gdr_max_chunks(p) == 0
+
+
+def test_pointer_and_workspace_checks(lib):
+    p = prob()
+    a = 1 << 20
+    ws_bytes = gdr.gdr_fwd_workspace_bytes(p)
+    # null required pointer
+    assert gdr.gdr_fwd(p, None, a, a, a, a, None, a, None, a, a, ws_bytes, 0) == gdr.GDR_ERR_INVALID_ARG
+    # misaligned pointer
+    assert gdr.gdr_fwd(p, a + 4, a, a, a, a, None, a, None, a, a, ws_bytes, 0) == gdr.GDR_ERR_ALIGNMENT
+    # workspace too small / missing / misaligned
+    assert gdr.gdr_fwd(p, a, a, a, a, a, None, a, None, a, a, ws_bytes - 1, 0) == gdr.GDR_ERR_WORKSPACE
+    assert gdr.gdr_fwd(p, a, a, a, a, a, None, a, None, a, None, ws_bytes, 0) == gdr.GDR_ERR_WORKSPACE
+    assert gdr.gdr_fwd(p, a, a, a, a, a, None, a, None, a, a + 128, ws_bytes, 0) == gdr.GDR_ERR_ALIGNMENT
+    wb = gdr.gdr_bwd_workspace_bytes(p)
+    args = [a] * 6 + [a, None] + [a] * 5 + [None]
+    assert gdr.gdr_bwd(p, *args, a, wb - 1, 0) == gdr.GDR_ERR_WORKSPACE
+    args[6] = None  # dO
+    assert gdr.gdr_bwd(p, *args, a, wb, 0) == gdr.GDR_ERR_INVALID_ARG
+    # varlen needs B == 1
+    cu = torch.tensor([0, 5, 10], dtype=torch.int32)
+    pv = gdr.make_problem(2, 10, 1, 1, 32, 32, torch.float32, "KV", cu_seqlens=cu)
+    assert gdr.gdr_fwd(pv, a, a, a, a, a, None, a, None, a, a, 1 << 30, 0) == gdr.GDR_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert gdr.gdr_status_string(s).startswith("GDR_")

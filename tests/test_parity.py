@@ -1,0 +1,145 @@
+"""GPU parity: the CUDA path against the fp64 oracle, element by element.
+
+Bar: max|got - ref| / max|ref| per output tensor (o, S_T, h_saved, dq, dk, dv, dg,
+dbeta, dS0) <= 1e-4 for fp32 inputs and <= 2e-2 for bf16 inputs; the oracle runs on
+the exact (rounded) inputs the GPU sees.  Small cases span several chunks and a
+ragged tail; the named full-size workloads are checked on sampled heads (all
+tokens, all chunks of the sampled heads) in the same launch configuration the
+benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+from chunked_gated_delta_04_gb300.inputs import WORKLOADS, make_inputs, small_workload
+from gdr_testlib import compare, head_slice, reference, run_gpu, slice_result, tol_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(w, heads=None):
+    inp = make_inputs(w)
+    res = run_gpu(inp)
+    torch.cuda.synchronize()
+    if heads is not None:
+        sub, vh = head_slice(inp, heads)
+        ref = reference(sub)
+        res = slice_result(res, heads, vh)
+    else:
+        ref = reference(inp)
+    return compare(res, ref, tol_for(w.dtype))
+
+
+SMALL = [
+    # name, dtype, B, T, Hk, Hv, D, layout, S0, dST
+    ("f32_t1", torch.float32, 1, 1, 1, 1, 32, "KV", True, True),
+    ("f32_t63", torch.float32, 1, 63, 1, 1, 64, "KV", False, False),
+    ("f32_t64", torch.float32, 2, 64, 1, 1, 16, "VK", True, True),
+    ("f32_t65", torch.float32, 1, 65, 1, 2, 32, "KV", True, True),
+    ("f32_t130_gva", torch.float32, 2, 130, 2, 4, 32, "VK", True, False),
+    ("f32_d128", torch.float32, 1, 200, 1, 1, 128, "KV", True, True),
+    ("bf16_t129", torch.bfloat16, 1, 129, 1, 1, 128, "KV", True, True),
+    ("bf16_t300_b2", torch.bfloat16, 2, 300, 2, 2, 128, "VK", True, True),
+    ("bf16_gva", torch.bfloat16, 1, 192, 1, 2, 128, "KV", False, False),
+    ("bf16_d64", torch.bfloat16, 1, 100, 1, 1, 64, "KV", True, True),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_shapes(case):
+    name, dt, B, T, Hk, Hv, D, layout, s0, dst = case
+    _check(small_workload(name, dt, B, T, Hk, Hv, D, D, layout, s0, dst))
+
+
+@pytest.mark.parametrize("dt,D", [(torch.float32, 32), (torch.bfloat16, 128)])
+def test_varlen_ragged(dt, D):
+    # lengths: empty, 1, exactly one chunk, a ragged tail, several chunks
+    w = small_workload("varlen", dt, Hk=1, Hv=2, DK=D, DV=D, seqlens=[0, 1, 64, 77, 200], layout="VK")
+    _check(w)
+
+
+def test_tiny_fp32_workload():
+    _check(WORKLOADS["tiny_fp32"])
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,heads", [("b2_t4096", [0, 15]), ("varlen8", [3]), ("long_t65536", [7]),
+                                        ("gva_b4_t8192", [0])])
+def test_named_workloads_sampled_heads(name, heads):
+    errs = _check(WORKLOADS[name], heads)
+    print(name, errs)
+
+
+def test_varlen_matches_separate_fixed_length_runs():
+    """Packing sequences with cu_seqlens gives bitwise the same results as separate runs."""
+    lens = [70, 130]
+    w = small_workload("vl", torch.bfloat16, Hk=1, Hv=1, DK=128, DV=128, seqlens=lens)
+    inp = make_inputs(w)
+    res = run_gpu(inp)
+    cu = [0, 70, 200]
+    for n, L in enumerate(lens):
+        sub = dict(inp)
+        for key in ["q", "k", "v", "dO", "g", "beta"]:
+            sub[key] = inp[key][:, cu[n]:cu[n + 1]].contiguous()
+        for key in ["S0", "dS_T"]:
+            sub[key] = inp[key][n:n + 1].contiguous()
+        sub["cu_seqlens"] = None
+        r1 = run_gpu(sub)
+        for key in ["o", "dq", "dk", "dv", "dg", "dbeta"]:
+            assert torch.equal(r1[key], res[key][:, cu[n]:cu[n + 1]]), key
+        for key in ["S_T", "dS0"]:
+            assert torch.equal(r1[key][0], res[key][n]), key
+
+
+def test_null_states_equal_zero_states():
+    w = small_workload("z", torch.bfloat16, T=150, DK=128, DV=128, with_S0=False, with_dST=False)
+    inp = make_inputs(w)
+    r0 = run_gpu(inp)
+    inp2 = dict(inp)
+    inp2["S0"] = torch.zeros(1, 1, 128, 128)
+    inp2["dS_T"] = torch.zeros(1, 1, 128, 128)
+    r1 = run_gpu(inp2)
+    for key in r0:
+        if r0[key] is not None:
+            assert torch.equal(r0[key], r1[key]), key
+
+
+def test_kv_and_vk_layouts_are_transposes():
+    w = small_workload("kv", torch.bfloat16, T=140, DK=128, DV=128, layout="KV")
+    inp = make_inputs(w)
+    rk = run_gpu(inp)
+    inp2 = dict(inp)
+    inp2["layout"] = "VK"
+    inp2["S0"] = inp["S0"].transpose(-1, -2).contiguous()
+    inp2["dS_T"] = inp["dS_T"].transpose(-1, -2).contiguous()
+    rv = run_gpu(inp2)
+    for key in ["o", "h_saved", "dq", "dk", "dv", "dg", "dbeta"]:
+        assert torch.equal(rk[key], rv[key]), key
+    assert torch.equal(rk["S_T"], rv["S_T"].transpose(-1, -2))
+    assert torch.equal(rk["dS0"], rv["dS0"].transpose(-1, -2))
+
+
+def test_runs_are_bitwise_deterministic():
+    w = small_workload("det", torch.bfloat16, B=2, T=257, Hk=1, Hv=2, DK=128, DV=128)
+    inp = make_inputs(w)
+    r1, r2 = run_gpu(inp), run_gpu(inp)
+    for key in r1:
+        if r1[key] is not None:
+            assert torch.equal(r1[key], r2[key]), key
+
+
+def test_autograd_function_matches_oracle():
+    import chunked_gated_delta_04_gb300 as gdr
+
+    w = small_workload("ag", torch.bfloat16, T=100, DK=128, DV=128)
+    inp = make_inputs(w)
+    dev = {k_: (v_.cuda() if isinstance(v_, torch.Tensor) else v_) for k_, v_ in inp.items()}
+    leaves = {k_: dev[k_].clone().requires_grad_(True) for k_ in ["q", "k", "v", "g", "beta", "S0"]}
+    o, ST = gdr.chunk_gated_delta_rule(leaves["q"], leaves["k"], leaves["v"], leaves["g"], leaves["beta"],
+                                       leaves["S0"], None, "KV")
+    loss = (o.float() * dev["dO"].float()).sum() + (ST * dev["dS_T"]).sum()
+    loss.backward()
+    ref = reference(inp)
+    got = {"o": o, "S_T": ST, "dq": leaves["q"].grad, "dk": leaves["k"].grad, "dv": leaves["v"].grad,
+           "dg": leaves["g"].grad, "dbeta": leaves["beta"].grad, "dS0": leaves["S0"].grad}
+    compare(got, ref, tol_for(torch.bfloat16))
