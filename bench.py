@@ -1,0 +1,477 @@
+#!/usr/bin/env python
+"""Benchmark of the chunked gated delta rule (forward + backward) on GB300.
+
+One step = gdr_fwd followed by gdr_bwd over one batch of the named workload
+(default: bf16, B=2, T=4096, H=16, DK=DV=128, "KV" states, S0 and dS_T given), with
+the inputs already resident in HBM.  An L2 flush (a 512 MB write, > 2x the 129 MB
+L2) runs between timed steps, outside the timed intervals.  Prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the workload
+(weak scaling, no collective on the data path); the time is the max over ranks.
+``--impl reference`` times the fp64 CPU oracle (the baseline arm) on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDR fwd+bwd tokens/s & % of roofline at B=2 T=4096 H=16 DK=DV=128 bf16"
+UNIT = "tokens/s"
+FLUSH_BYTES = 512 << 20
+CHUNK = 64
+
+# Which of the operator's own tensors each kernel stage reads (r) or writes (w): its
+# algorithmic bytes are the compulsory bytes of those tensors (workspace traffic is
+# not algorithmic and shows up only in the ncu "traffic" figure).
+STAGE_IO = {
+    "index": ("", ""),
+    "fwd_prep": ("k v g beta", ""),
+    "fwd_state": ("S0", "h_saved S_T"),
+    "fwd_out": ("q", "o"),
+    "fwd_main": ("q k v g beta S0", "o h_saved S_T"),
+    "bwd_prep": ("k v g beta", ""),
+    "bwd_vn": ("h_saved", ""),
+    "bwd_walk": ("dO dS_T", "dS0"),
+    "bwd_grad": ("q k v dO beta h_saved", "dq dk dv dg dbeta"),
+    "bwd_group_reduce": ("", "dq dk"),
+}
+
+
+def rank_info():
+    r = int(os.environ.get("RANK", "0"))
+    w = int(os.environ.get("WORLD_SIZE", "1"))
+    lr = int(os.environ.get("LOCAL_RANK", "0"))
+    return r, w, lr
+
+
+# ----------------------------------------------------------------------------- work model
+def chunk_lengths(seqlens):
+    out = []
+    for L in seqlens:
+        out += [min(CHUNK, L - s) for s in range(0, L, CHUNK)]
+    return out
+
+
+def tensor_bytes(inp, w):
+    """Bytes of every operator-level tensor of one fwd+bwd call."""
+    el = 2 if w.dtype.itemsize == 2 else 4
+    tok = sum(inp["seqlens"])
+    N = inp["num_seqs"]
+    nch = len(chunk_lengths(inp["seqlens"]))
+    st = N * w.Hv * w.DK * w.DV * 4
+    qk = tok * w.Hk * w.DK * el
+    vv = tok * w.Hv * w.DV * el
+    return {
+        "q": qk, "k": qk, "dq": qk, "dk": qk, "v": vv, "o": vv, "dO": vv, "dv": vv,
+        "g": tok * w.Hv * 4, "dg": tok * w.Hv * 4, "beta": tok * w.Hv * el, "dbeta": tok * w.Hv * el,
+        "S0": st if inp["S0"] is not None else 0, "S_T": st, "dS_T": st if inp["dS_T"] is not None else 0,
+        "dS0": st, "h_saved": nch * w.Hv * w.DK * w.DV * 4,
+    }
+
+
+def work_model(inp, w):
+    """Algorithmic FLOPs (the chunked method's GEMMs, C x C products dense, the T inverse
+    as C^3/3) and compulsory HBM bytes of the forward and the backward."""
+    G = w.Hv // w.Hk
+    DK, DV = w.DK, w.DV
+    ff = fb = 0.0
+    for c in chunk_lengths(inp["seqlens"]):
+        ff += 4 * c * c * DK / G + 2 * c * c * DK + 4 * c * c * DV + 6 * c * DK * DV + c ** 3 / 3
+        fb += 14 * c * DK * DV + 2 * c * c * DK * (7 + 2 / G) + 10 * c * c * DV + 4 * c ** 3 + c ** 3 / 3
+    ff *= w.Hv
+    fb *= w.Hv
+    tb = tensor_bytes(inp, w)
+    bf = sum(tb[k] for k in ["q", "k", "v", "g", "beta", "o", "h_saved", "S0", "S_T"])
+    bb = sum(tb[k] for k in ["q", "k", "v", "dO", "g", "beta", "h_saved", "dq", "dk", "dv", "dg", "dbeta",
+                             "dS_T", "dS0"])
+    return {"flops_fwd": ff, "flops_bwd": fb, "bytes_fwd": bf, "bytes_bwd": bb, "tensor_bytes": tb}
+
+
+def stage_alg_bytes(stage, tb):
+    r, wr = STAGE_IO.get(stage, ("", ""))
+    return sum(tb[k] for k in (r + " " + wr).split() if k)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), float(pk.get("bf16_tflops_sustained", 0)), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def ncu_traffic(stage):
+    """dram bytes per launch of a stage from profiles/ncu_traffic.txt, or None when the
+    kernel's source has changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        parts = line.split()
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == stage:
+            src = os.path.join(ROOT, "chunked_gated_delta_04_gb300", "csrc", parts[3])
+            if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != parts[2]:
+                return None
+            return float(parts[1])
+    return None
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names[1:], p[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- oracle arms
+def _head_slice(inp, qk_heads):
+    Hk = inp["q"].shape[2]
+    Hv = inp["v"].shape[2]
+    G = Hv // Hk
+    vh = [i * G + jj for i in qk_heads for jj in range(G)]
+    out = dict(inp)
+    out["q"] = inp["q"][:, :, qk_heads]
+    out["k"] = inp["k"][:, :, qk_heads]
+    for key in ["v", "dO", "g", "beta"]:
+        out[key] = inp[key][:, :, vh]
+    for key in ["S0", "dS_T"]:
+        if inp[key] is not None:
+            out[key] = inp[key][:, vh]
+    return out
+
+
+def time_oracle(inp, w, n_qk_heads, nthreads):
+    """Times the fp64 oracle (fwd + bwd) on the first n_qk_heads q/k heads of every
+    sequence; returns (seconds, tokens-equivalent of the full workload processed)."""
+    import oracle
+
+    sub = _head_slice(inp, list(range(n_qk_heads)))
+    t0 = time.perf_counter()
+    oracle.reference(sub, inp["layout"], backward=True, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    tokens = sum(inp["seqlens"]) * n_qk_heads / w.Hk
+    return dt, tokens
+
+
+def reference_arm(args, w, inp):
+    r, world, _ = rank_info()
+    if r != 0:
+        return 0
+    nthreads = os.cpu_count() or 1
+    # per step: as many q/k heads (with their v-heads) of every sequence as there are host cores
+    n_heads = max(1, min(w.Hk, nthreads // max(1, inp["num_seqs"])))
+    for _ in range(args.warmup):
+        time_oracle(inp, w, n_heads, nthreads)
+    total_t, total_tok = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, tok = time_oracle(inp, w, n_heads, nthreads)
+        total_t += dt
+        total_tok += tok
+    value = total_tok / total_t
+    units = inp["num_seqs"] * n_heads
+    sample = (f"per step: fp64 oracle fwd+bwd on {n_heads} of {w.Hk} q/k heads (with its {w.Hv // w.Hk} v-heads) "
+              f"of all {inp['num_seqs']} sequences ({sum(inp['seqlens'])} tokens); tokens scaled by {n_heads}/{w.Hk}")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, inp),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(nthreads, units), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(w, inp):
+    return {"workload": w.name, "B": w.B if inp["cu_seqlens"] is None else 1, "T": int(sum(inp["seqlens"])) if
+            inp["cu_seqlens"] is not None else w.T, "Hk": w.Hk, "Hv": w.Hv, "DK": w.DK, "DV": w.DV,
+            "layout": w.layout, "num_seqs": inp["num_seqs"], "chunk": CHUNK,
+            "varlen": inp["cu_seqlens"] is not None, "S0": inp["S0"] is not None,
+            "dS_T": inp["dS_T"] is not None, "l2": "flushed (512 MB write) between timed steps",
+            "parallelism": "replicas"}
+
+
+# ----------------------------------------------------------------------------- our arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="b2_t4096")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+
+    from chunked_gated_delta_04_gb300.inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w)
+    if args.impl == "reference":
+        return reference_arm(args, w, inp)
+
+    import chunked_gated_delta_04_gb300 as gdr
+
+    rank, world, local_rank = rank_info()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    dev = torch.device("cuda", local_rank)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    B, T, Hk, DK = d["q"].shape
+    Hv, DV = d["v"].shape[2], d["v"].shape[3]
+    p = gdr.make_problem(B, T, Hk, Hv, DK, DV, d["q"].dtype, w.layout, d["cu_seqlens"])
+    stream = torch.cuda.current_stream()
+    N = p.num_seqs
+    sshape = (N, Hv, DK, DV) if w.layout == "KV" else (N, Hv, DV, DK)
+    o = torch.empty_like(d["v"])
+    S_T = torch.empty(sshape, dtype=torch.float32, device=dev)
+    h_saved = torch.empty((gdr.gdr_max_chunks(p), Hv, DK, DV), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+    dg, dbeta = torch.empty_like(d["g"]), torch.empty_like(d["beta"])
+    dS0 = torch.empty(sshape, dtype=torch.float32, device=dev)
+    ws_bytes = max(gdr.gdr_fwd_workspace_bytes(p), gdr.gdr_bwd_workspace_bytes(p))
+    ws = gdr.alloc_workspace(ws_bytes, dev)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def fwd(src=d):
+        st = gdr.gdr_fwd(p, src["q"], src["k"], src["v"], src["g"], src["beta"], src["S0"], o, S_T, h_saved, ws,
+                         ws_bytes, stream)
+        if st != 0:
+            raise RuntimeError(f"gdr_fwd: {gdr.gdr_status_string(st)}")
+
+    def bwd(src=d):
+        st = gdr.gdr_bwd(p, src["q"], src["k"], src["v"], src["g"], src["beta"], h_saved, src["dO"], src["dS_T"],
+                         dq, dk, dv, dg, dbeta, dS0, ws, ws_bytes, stream)
+        if st != 0:
+            raise RuntimeError(f"gdr_bwd: {gdr.gdr_status_string(st)}")
+
+    def step():
+        fwd()
+        bwd()
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def timed(fn, n):
+        """Device time (ms) of n calls of fn, each after an L2 flush, via CUDA events."""
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            flush()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    st, flags = gdr.gdr_workspace_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {gdr.gdr_status_string(st)} (flags {flags:#x})")
+
+    # ---- main timed region: exactly K steps
+    launches0 = gdr.gdr_debug_launch_count()
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        step_ms = timed(step, args.steps)
+        torch.cuda.synchronize()
+        barrier()
+    launches = gdr.gdr_debug_launch_count() - launches0
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens = float(sum(inp["seqlens"]))
+    value = world * tokens * args.steps / (total_ms / 1e3)
+    ms_per_step = total_ms / args.steps
+
+    # ---- fwd / bwd separately (informational)
+    fwd_ms = statistics.median(timed(fwd, max(5, args.steps // 2)))
+    bwd_ms = statistics.median(timed(bwd, max(5, args.steps // 2)))
+
+    # ---- per-kernel times with stage events (separate pass; the main loop has no hooks)
+    nev = 16
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+    gdr.gdr_debug_set_stage_events(events)
+    stage_tot = {}
+    reps = max(5, args.steps // 2)
+    for _ in range(reps):
+        for fn in (fwd, bwd):
+            flush()
+            fn()
+            torch.cuda.synchronize()
+            names = gdr.gdr_debug_stage_names()
+            for i, nm in enumerate(names):
+                stage_tot.setdefault(nm, []).append(events[i].elapsed_time(events[i + 1]))
+    gdr.gdr_debug_set_stage_events(None)
+    stage_ms = {k: statistics.mean(v) for k, v in stage_tot.items()}
+
+    wm = work_model(inp, w)
+    hbm, bf16_burst, bf16_sus, peak_src = load_peaks()
+    dom = max(stage_ms, key=stage_ms.get)
+    alg = stage_alg_bytes(dom, wm["tensor_bytes"])
+    achieved = alg / (stage_ms[dom] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": ncu_traffic(dom), "alg_bytes": alg,
+                "avg_launch_ms": stage_ms[dom], "peak_source": f"{peak_src} hbm_gbs (copy bandwidth)"}
+    t_hbm_step = (wm["bytes_fwd"] + wm["bytes_bwd"]) / (hbm * 1e9) * 1e3
+    t_flop_step = (wm["flops_fwd"] + wm["flops_bwd"]) / (bf16_sus * 1e12) * 1e3
+    step_roof = max(t_hbm_step, t_flop_step)
+
+    def dir_obj(ms, flops, nbytes):
+        t_roof = max(nbytes / (hbm * 1e9), flops / (bf16_sus * 1e12)) * 1e3
+        return {"ms": ms, "tokens_per_s": tokens / (ms / 1e3), "tflops": flops / (ms / 1e3) / 1e12,
+                "gbs": nbytes / (ms / 1e3) / 1e9, "roofline_ms": t_roof, "roofline_frac": t_roof / ms}
+
+    # ---- end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    in_keys = ["q", "k", "v", "g", "beta", "S0", "dO", "dS_T"]
+    host_in = {k: inp[k].pin_memory() for k in in_keys if inp[k] is not None}
+    dev_in = {k: torch.empty_like(d[k]) for k in host_in}
+    dev_in["cu_seqlens"] = d["cu_seqlens"]
+    for k in in_keys:
+        dev_in.setdefault(k, None)
+    outs = [o, S_T, dq, dk, dv, dg, dbeta, dS0]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for k, t in host_in.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        fwd(dev_in)
+        bwd(dev_in)
+        for h, t in zip(host_out, outs):
+            h.copy_(t, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = timed(e2e_step, args.steps)
+    torch.cuda.synchronize()
+    e2e_total = sum(e2e_ms)
+    if dist is not None:
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = world * tokens * args.steps / (e2e_total / 1e3)
+
+    # ---- oracle on host cores (rank 0, N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nthreads = os.cpu_count() or 1
+        n_heads = max(1, min(w.Hk, 4))
+        dt, tok = time_oracle(inp, w, n_heads, nthreads)
+        cpu = {"value": tok / dt, "unit": UNIT, "cores": min(nthreads, inp["num_seqs"] * n_heads), "kind": "oracle",
+               "sample": f"fp64 oracle fwd+bwd on {n_heads} of {w.Hk} q/k heads of all {inp['num_seqs']} sequences "
+                         f"({dt:.1f} s); tokens scaled by {n_heads}/{w.Hk}"}
+
+    clocks = clk.summary()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
+            "data": "synthetic (seeded; see chunked_gated_delta_04_gb300/inputs.py)",
+            "config": config_dict(w, inp),
+            "roofline": roofline,
+            "step_roofline": {"ms": step_roof, "frac": step_roof / ms_per_step, "bound": "hbm" if
+                              t_hbm_step >= t_flop_step else "tensor", "bytes": wm["bytes_fwd"] + wm["bytes_bwd"],
+                              "flops": wm["flops_fwd"] + wm["flops_bwd"]},
+            "fwd": dir_obj(fwd_ms, wm["flops_fwd"], wm["bytes_fwd"]),
+            "bwd": dir_obj(bwd_ms, wm["flops_bwd"], wm["bytes_bwd"]),
+            "stages_ms": stage_ms,
+            "path": "tcgen05" if gdr.gdr_path(p) == 1 else "simt",
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -47,9 +47,12 @@ class GDRError(RuntimeError):
 
 
 _LIB = None
+_STAGE_ARR = None
 
 EXPORTS = ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes", "gdr_bwd_workspace_bytes",
-           "gdr_fwd", "gdr_bwd", "gdr_workspace_status", "gdr_status_string", "gdr_path"]
+           "gdr_fwd", "gdr_bwd", "gdr_workspace_status", "gdr_status_string", "gdr_path",
+           "gdr_debug_set_stage_events", "gdr_debug_stage_count", "gdr_debug_stage_name",
+           "gdr_debug_launch_count"]
 
 
 def _lib_handle():
@@ -75,6 +78,14 @@ def _lib_handle():
         lib.gdr_workspace_status.restype = i
         lib.gdr_status_string.argtypes = [i]
         lib.gdr_status_string.restype = ctypes.c_char_p
+        lib.gdr_debug_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i]
+        lib.gdr_debug_set_stage_events.restype = None
+        lib.gdr_debug_stage_count.argtypes = []
+        lib.gdr_debug_stage_count.restype = i
+        lib.gdr_debug_stage_name.argtypes = [i]
+        lib.gdr_debug_stage_name.restype = ctypes.c_char_p
+        lib.gdr_debug_launch_count.argtypes = []
+        lib.gdr_debug_launch_count.restype = ctypes.c_ulonglong
         _LIB = lib
     return _LIB
 
@@ -161,6 +172,30 @@ def gdr_workspace_status(workspace, stream=None):
 
 def gdr_status_string(s: int) -> str:
     return _lib_handle().gdr_status_string(s).decode()
+
+
+def gdr_debug_set_stage_events(events) -> None:
+    """events: list of torch.cuda.Event (created with enable_timing=True) or None to switch off."""
+    lib = _lib_handle()
+    if events is None:
+        lib.gdr_debug_set_stage_events(None, 0)
+        return
+    global _STAGE_ARR
+    for e in events:  # torch creates the cudaEvent_t handle lazily, at the first record
+        e.record()
+    torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _STAGE_ARR = arr  # keep the handle array alive while the library may use it
+    lib.gdr_debug_set_stage_events(arr, len(events))
+
+
+def gdr_debug_stage_names() -> list:
+    lib = _lib_handle()
+    return [lib.gdr_debug_stage_name(i).decode() for i in range(lib.gdr_debug_stage_count())]
+
+
+def gdr_debug_launch_count() -> int:
+    return _lib_handle().gdr_debug_launch_count()
 
 
 def _check(st, where):

@@ -7,8 +7,34 @@
 #include <string.h>
 
 #include "gdr_internal.h"
+#include "../../include/gdr_debug.h"
+#include <atomic>
 
 namespace gdr {
+
+namespace {
+constexpr int kMaxStages = 32;
+cudaEvent_t* g_stage_events = nullptr;
+int g_stage_n = 0;
+int g_stage_i = 0;
+const char* g_stage_names[kMaxStages];
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+void stage_begin(cudaStream_t s) {
+  g_stage_i = 0;
+  if (g_stage_events && g_stage_n > 0) cudaEventRecord(g_stage_events[0], s);
+}
+
+void stage_mark(cudaStream_t s, const char* stage) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (g_stage_events && g_stage_i + 1 < g_stage_n && g_stage_i < kMaxStages) {
+    g_stage_names[g_stage_i] = stage;
+    cudaEventRecord(g_stage_events[g_stage_i + 1], s);
+    ++g_stage_i;
+  }
+}
+
 namespace {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -138,6 +164,7 @@ gdr_status gdr_fwd(const gdr_problem* p, const void* q, const void* k, const voi
   if (workspace_bytes < need) return GDR_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
   FwdArgs a{q, k, v, g, beta, S0, o, S_T, h_saved};
+  stage_begin(s);
   cudaError_t e = launch_index(d, ws, s);
   if (e == cudaSuccess) e = d.path == 1 ? tc_forward(d, a, ws, s) : simt_forward(d, a, ws, s);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
@@ -163,6 +190,7 @@ gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const voi
   if (workspace_bytes < need) return GDR_ERR_WORKSPACE;
   cudaStream_t s = (cudaStream_t)stream;
   BwdArgs a{q, k, v, g, beta, h_saved, dO, dS_T, dq, dk, dv, dg, dbeta, dS0};
+  stage_begin(s);
   cudaError_t e = launch_index(d, ws, s);
   if (e == cudaSuccess) e = d.path == 1 ? tc_backward(d, a, ws, s) : simt_backward(d, a, ws, s);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
@@ -180,6 +208,18 @@ gdr_status gdr_workspace_status(const void* workspace, gdr_stream_t stream, uint
   if (word & (kDevErrTimeoutFwd | kDevErrTimeoutBwd | kDevErrTimeoutPrep)) return GDR_ERR_TIMEOUT;
   return GDR_OK;
 }
+
+void gdr_debug_set_stage_events(void** events, int n) {
+  g_stage_events = (cudaEvent_t*)events;
+  g_stage_n = events ? n : 0;
+  g_stage_i = 0;
+}
+
+int gdr_debug_stage_count(void) { return g_stage_i; }
+
+const char* gdr_debug_stage_name(int i) { return (i >= 0 && i < g_stage_i) ? g_stage_names[i] : ""; }
+
+unsigned long long gdr_debug_launch_count(void) { return g_launches.load(); }
 
 const char* gdr_status_string(gdr_status s) {
   switch (s) {

@@ -122,6 +122,7 @@ cudaError_t launch_index(const Dims& d, const Workspace& ws, cudaStream_t s) {
   gdr_index_kernel<<<1, kIndexThreads, 0, s>>>(d.cu, d.num_seqs, d.cu ? (int)d.T_total : d.T,
                                                d.max_chunks, ws.chunks, ws.seq_chunk_off, ws.seq_order,
                                                ws.status);
+  stage_mark(s, "index");
   return cudaGetLastError();
 }
 

@@ -76,6 +76,12 @@ struct BwdArgs {
   float* dS0;
 };
 
+// Marks the end of one kernel launch named `stage` on `s`: counts the launch and,
+// when stage events are on (include/gdr_debug.h), records the next event.
+void stage_mark(cudaStream_t s, const char* stage);
+// Called at the start of every gdr_fwd / gdr_bwd (records event 0 when enabled).
+void stage_begin(cudaStream_t s);
+
 // K0: chunk index (chunks, seq offsets, longest-first order) and status reset.
 cudaError_t launch_index(const Dims& d, const Workspace& ws, cudaStream_t s);
 

@@ -586,6 +586,7 @@ cudaError_t simt_forward_t(const Dims& d, const FwdArgs& a, const Workspace& ws,
     cudaFuncSetAttribute(simt_prep_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
     simt_prep_kernel<IT><<<gc, kThreads, smp, s>>>(d, (const IT*)a.k, (const IT*)a.v, a.g,
                                                    (const IT*)a.beta, ws);
+    stage_mark(s, "fwd_prep");
   }
   if (d.num_seqs > 0) {
     const int dvs = dv_slice(d);
@@ -593,12 +594,14 @@ cudaError_t simt_forward_t(const Dims& d, const FwdArgs& a, const Workspace& ws,
     size_t sms = sizeof(float) * (d.DK * dvs + kChunk * dvs + kChunk);
     cudaFuncSetAttribute(simt_state_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
     simt_state_kernel<IT><<<gs, kThreads, sms, s>>>(d, (const IT*)a.k, a.S0, a.S_T, a.h_saved, ws, dvs);
+    stage_mark(s, "fwd_state");
   }
   if (d.max_chunks > 0) {
     const dim3 gc(d.max_chunks, d.Hv);
     size_t smo = sizeof(float) * (2 * kChunk * d.DK + kChunk * kLd + kChunk);
     cudaFuncSetAttribute(simt_out_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo);
     simt_out_kernel<IT><<<gc, kThreads, smo, s>>>(d, (const IT*)a.q, (const IT*)a.k, a.h_saved, (IT*)a.o, ws);
+    stage_mark(s, "fwd_out");
   }
   return cudaGetLastError();
 }
@@ -611,7 +614,9 @@ cudaError_t simt_backward_t(const Dims& d, const BwdArgs& a, const Workspace& ws
     cudaFuncSetAttribute(simt_prep_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
     simt_prep_kernel<IT><<<gc, kThreads, smp, s>>>(d, (const IT*)a.k, (const IT*)a.v, a.g,
                                                    (const IT*)a.beta, ws);
+    stage_mark(s, "bwd_prep");
     simt_vn_kernel<<<gc, kThreads, 0, s>>>(d, a.h_saved, ws);
+    stage_mark(s, "bwd_vn");
   }
   if (d.num_seqs > 0) {
     const int dvs = dv_slice(d);
@@ -620,6 +625,7 @@ cudaError_t simt_backward_t(const Dims& d, const BwdArgs& a, const Workspace& ws
     cudaFuncSetAttribute(simt_walk_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smw);
     simt_walk_kernel<IT><<<gs, kThreads, smw, s>>>(d, (const IT*)a.q, (const IT*)a.k, (const IT*)a.dO,
                                                    a.dS_T, a.dS0, ws, dvs);
+    stage_mark(s, "bwd_walk");
   }
   if (d.max_chunks > 0) {
     const dim3 gc(d.max_chunks, d.Hv);
@@ -628,9 +634,11 @@ cudaError_t simt_backward_t(const Dims& d, const BwdArgs& a, const Workspace& ws
     simt_grad_kernel<IT><<<gc, kThreads, smg, s>>>(d, (const IT*)a.q, (const IT*)a.k, (const IT*)a.v,
                                                    (const IT*)a.beta, a.h_saved, (const IT*)a.dO,
                                                    (IT*)a.dq, (IT*)a.dk, (IT*)a.dv, a.dg, (IT*)a.dbeta, ws);
+    stage_mark(s, "bwd_grad");
   }
   if (d.G > 1 && d.T_total > 0) {
     simt_group_reduce_kernel<IT><<<1024, kThreads, 0, s>>>(d, (IT*)a.dq, (IT*)a.dk, ws);
+    stage_mark(s, "bwd_group_reduce");
   }
   return cudaGetLastError();
 }

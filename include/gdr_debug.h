@@ -1,0 +1,35 @@
+/*
+ * gdr_debug.h -- benchmark instrumentation of libgdr.so (not needed to use the
+ * operator; no counterpart on the pages).
+ *
+ * Stage events: after gdr_debug_set_stage_events(events, n) with n >= 1 caller-
+ * created cudaEvent_t handles, every following gdr_fwd / gdr_bwd records
+ * events[0] on its stream before its first kernel and events[i + 1] right after
+ * its i-th kernel launch (at most n - 1 kernels are bracketed).  The elapsed
+ * time between events[i] and events[i + 1] is then kernel i's device time on
+ * that stream.  gdr_debug_stage_count() gives the number of kernels the last call
+ * bracketed and gdr_debug_stage_name(i) a stable stage name ("fwd_prep",
+ * "bwd_grad", ...).  Pass events = NULL to switch it off.  The setting is
+ * process-global host state and not thread-safe; the events stay owned by the
+ * caller.
+ *
+ * Launch counter: gdr_debug_launch_count() returns how many kernels this process
+ * has launched through the library so far.
+ */
+#ifndef GDR_DEBUG_H_
+#define GDR_DEBUG_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+void gdr_debug_set_stage_events(void** events, int n);
+int gdr_debug_stage_count(void);
+const char* gdr_debug_stage_name(int i);
+unsigned long long gdr_debug_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDR_DEBUG_H_ */
