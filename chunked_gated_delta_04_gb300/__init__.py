@@ -52,7 +52,7 @@ _STAGE_ARR = None
 EXPORTS = ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes", "gdr_bwd_workspace_bytes",
            "gdr_fwd", "gdr_bwd", "gdr_workspace_status", "gdr_status_string", "gdr_path",
            "gdr_debug_set_stage_events", "gdr_debug_stage_count", "gdr_debug_stage_name",
-           "gdr_debug_launch_count"]
+           "gdr_debug_launch_count", "gdr_fwd_noalloc"]
 
 
 def _lib_handle():
@@ -74,6 +74,8 @@ def _lib_handle():
         lib.gdr_fwd.restype = i
         lib.gdr_bwd.argtypes = [P] + [vp] * 14 + [vp, sz, vp]
         lib.gdr_bwd.restype = i
+        lib.gdr_fwd_noalloc.argtypes = [P] + [vp] * 9 + [vp]
+        lib.gdr_fwd_noalloc.restype = i
         lib.gdr_workspace_status.argtypes = [vp, vp, u32p]
         lib.gdr_workspace_status.restype = i
         lib.gdr_status_string.argtypes = [i]
@@ -161,6 +163,16 @@ def gdr_bwd(p, q, k, v, g, beta, h_saved, dO, dS_T, dq, dk, dv, dg, dbeta, dS0, 
     return _lib_handle().gdr_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                  _ptr(h_saved), _ptr(dO), _ptr(dS_T), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg),
                                  _ptr(dbeta), _ptr(dS0), _ptr(workspace), wb, _stream_ptr(stream))
+
+
+def gdr_fwd_noalloc(p, q, k, v, g, beta, S0, o, S_T, h_saved, stream=None) -> int:
+    """C gdr_fwd_noalloc (the forward with library-owned scratch, for callers that
+    cannot allocate); returns the status code."""
+    return _lib_handle().gdr_fwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                         _ptr(S0), _ptr(o), _ptr(S_T), _ptr(h_saved), _stream_ptr(stream))
+
+
+NOALLOC_MAX_WORKSPACE_BYTES = 64 << 20
 
 
 def gdr_workspace_status(workspace, stream=None):

@@ -80,6 +80,8 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
 
 }  // namespace
 
+gdr_status resolve_problem(const gdr_problem* p, Dims* d) { return resolve(p, d); }
+
 size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws) {
   size_t off = 0;
   auto take = [&](size_t bytes) -> char* {

@@ -50,6 +50,9 @@ struct Workspace {
   float* dk_part;  // backward, Hv > Hk: [T_total][Hv][DK]
 };
 
+// Validates *p and fills *d (the checks of gdr_fwd / gdr_bwd on the problem itself).
+gdr_status resolve_problem(const gdr_problem* p, Dims* d);
+
 // Computes the workspace layout; with base == nullptr only the size is returned.
 size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws);
 

@@ -116,6 +116,31 @@ gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const voi
                    const float* dS_T, void* dq, void* dk, void* dv, float* dg, void* dbeta,
                    float* dS0, void* workspace, size_t workspace_bytes, gdr_stream_t stream);
 
+/* Forward without a workspace argument (no counterpart on the pages: it is a
+ * convenience of this library).  For callers that cannot give the library scratch
+ * memory and cannot allocate any themselves: e.g. a plugin whose host framework
+ * owns all device memory and forbids side allocations, or a latency-critical loop
+ * where a cudaMalloc, which may synchronise the whole device, is not acceptable.
+ * Same arguments, results and errors as gdr_fwd, minus the workspace.
+ *  - Its scratch is one array of GDR_NOALLOC_MAX_WORKSPACE_BYTES in device memory,
+ *    owned by the library: every GPU that loads this part of the library keeps that
+ *    much memory until the process exits (with CUDA's default lazy module loading,
+ *    only GPUs on which this entry point has run).  It allocates nothing, ever.
+ *  - A problem whose gdr_fwd_workspace_bytes exceeds the limit is refused with
+ *    GDR_ERR_WORKSPACE before anything is launched.
+ *  - It runs on the current device.  The first call on each device looks up the
+ *    array's device address (cudaGetSymbolAddress) and caches it, so make that first
+ *    call before any stream capture begins.
+ *  - Every call uses the same array and leaves its contents behind; nothing needs
+ *    clearing between calls.  Calls whose GPU work can overlap (e.g. on two
+ *    unordered streams) race on the array and corrupt each other's results:
+ *    serialise them.  The array's status word is not readable through
+ *    gdr_workspace_status. */
+#define GDR_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)64 << 20)
+gdr_status gdr_fwd_noalloc(const gdr_problem* p, const void* q, const void* k, const void* v,
+                           const float* g, const void* beta, const float* S0, void* o, float* S_T,
+                           float* h_saved, gdr_stream_t stream);
+
 /* Synchronises `stream`, then reads the status word that the kernels of the last
  * gdr_fwd / gdr_bwd using `workspace` left there: GDR_OK, or GDR_ERR_TIMEOUT if a
  * bounded wait ran out (the kernel returned early; its outputs are invalid).
