@@ -52,7 +52,7 @@ _STAGE_ARR = None
 EXPORTS = ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes", "gdr_bwd_workspace_bytes",
            "gdr_fwd", "gdr_bwd", "gdr_workspace_status", "gdr_status_string", "gdr_path",
            "gdr_debug_set_stage_events", "gdr_debug_stage_count", "gdr_debug_stage_name",
-           "gdr_debug_launch_count", "gdr_fwd_noalloc"]
+           "gdr_debug_launch_count", "gdr_fwd_noalloc", "gdr_debug_tc_gemm"]
 
 
 def _lib_handle():
@@ -88,6 +88,8 @@ def _lib_handle():
         lib.gdr_debug_stage_name.restype = ctypes.c_char_p
         lib.gdr_debug_launch_count.argtypes = []
         lib.gdr_debug_launch_count.restype = ctypes.c_ulonglong
+        lib.gdr_debug_tc_gemm.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
+        lib.gdr_debug_tc_gemm.restype = i
         _LIB = lib
     return _LIB
 
@@ -204,6 +206,11 @@ def gdr_debug_set_stage_events(events) -> None:
 def gdr_debug_stage_names() -> list:
     lib = _lib_handle()
     return [lib.gdr_debug_stage_name(i).decode() for i in range(lib.gdr_debug_stage_count())]
+
+
+def gdr_debug_tc_gemm(A, B, D, N, K, a_mn, b_mn, status, stream=None) -> int:
+    return _lib_handle().gdr_debug_tc_gemm(_ptr(A), _ptr(B), _ptr(D), N, K, a_mn, b_mn, _ptr(status),
+                                           _stream_ptr(stream))
 
 
 def gdr_debug_launch_count() -> int:

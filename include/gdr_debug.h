@@ -28,6 +28,15 @@ int gdr_debug_stage_count(void);
 const char* gdr_debug_stage_name(int i);
 unsigned long long gdr_debug_launch_count(void);
 
+/* Device self-test of the tensor-core operand layouts: one tcgen05 GEMM on one CTA,
+ * D[m][n] = sum_k Amat[m][k] Bmat[k][n] (M = 128, N in {64, 128}, K in {64, 128}),
+ * A and B bf16 row-major device buffers, Amat = A ([128][K], a_mn = 0) or A^T ([K][128],
+ * a_mn = 1), Bmat = B^T ([N][K], b_mn = 0) or B ([K][N], b_mn = 1); D fp32 [128][N].
+ * status: device uint32 that receives a timeout bit if the MMA never completes.
+ * Returns 0 when launched, non-zero for bad sizes or a launch error. */
+int gdr_debug_tc_gemm(const void* A, const void* B, float* D, int N, int K, int a_mn, int b_mn,
+                      unsigned int* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
