@@ -74,7 +74,10 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
   d->dtype = p->dtype;
   d->layout = p->layout;
   d->cu = p->cu_seqlens;
-  d->path = (p->dtype == GDR_DTYPE_BF16 && p->DK == 128 && p->DV == 128 && tc_available()) ? 1 : 0;
+  d->path = (p->dtype == GDR_DTYPE_BF16 && p->DK == 128 && p->DV == 128 && maxc * p->Hv * kChunk < (1ll << 31) &&
+             tc_available())
+                ? 1
+                : 0;
   return GDR_OK;
 }
 
@@ -140,6 +143,7 @@ size_t gdr_fwd_workspace_bytes(const gdr_problem* p) {
 size_t gdr_bwd_workspace_bytes(const gdr_problem* p) {
   Dims d;
   if (resolve(p, &d) != GDR_OK) return 0;
+  if (d.path == 1 && !tc_bwd_available()) d.path = 0;
   return layout_workspace(d, true, nullptr, nullptr);
 }
 
@@ -179,6 +183,7 @@ gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const voi
   Dims d;
   gdr_status st = resolve(p, &d);
   if (st != GDR_OK) return st;
+  if (d.path == 1 && !tc_bwd_available()) d.path = 0;
   const bool any_tokens = d.T_total > 0;
   if (any_tokens && (!q || !k || !v || !g || !beta || !h_saved || !dO || !dq || !dk || !dv || !dg || !dbeta))
     return GDR_ERR_INVALID_ARG;

@@ -95,6 +95,7 @@ cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, 
 // tcgen05 kernels (bf16, DK = DV = 128).  tc_available() is false when this build
 // leaves them out.
 bool tc_available();
+bool tc_bwd_available();  // the tensor-core backward is built
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s);
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cudaStream_t s);
 

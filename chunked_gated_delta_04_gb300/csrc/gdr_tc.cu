@@ -1,14 +1,508 @@
-// gdr_tc.cu -- tcgen05 tensor-core kernels (bf16, DK = DV = 128).
-#include "gdr_device.cuh"
+// gdr_tc.cu -- tcgen05 tensor-core kernels of the chunked gated delta rule
+// (bf16 inputs, DK = DV = 128, fp32 state), chunk = 64 tokens.
+//
+// Notation per chunk (FlashQLA PR #34, Summary: the chunked gated delta rule), with
+// h := S^T (DK x DV) the state at the chunk start, gamma the in-chunk cumsum of g,
+// Gam[r,s] = exp(gamma_r - gamma_s) for r >= s:
+//   A  = strict-lower(diag(beta) K K^T * Gam),  T = (I + A)^{-1}
+//   T' = T diag(beta e^gamma),  T'' = T diag(beta),  W = T' K,  U = T'' V
+//   P  = (Q K^T) * Gam (lower incl. diagonal)
+//   Vn = U - W h
+//   O  = scale (diag(e^gamma) Q h + P Vn)
+//   h <- e^{gamma_C} h + K^T diag(e^{gamma_C - gamma}) Vn
+//
+// Kernels
+//   tc_prep   one CTA per (chunk, v-head): [K;Q] K^T on the tensor core (one M = 128
+//             MMA gives K K^T and Q K^T), the 64 x 64 unit-lower solve on CUDA cores
+//             (one thread per column of T, the column in registers), then
+//             [T';T''] K and [T';T''] V (two M = 128 MMAs: W lands in TMEM lanes 0-63,
+//             U in lanes 64-127).  Writes W, U, P (bf16) and gamma to the workspace.
+//   tc_fwd_state  one CTA per (sequence, v-head, 64-column slice of DV), sequential
+//             over the chunks: h stays in registers (thread t = row t of h); per
+//             chunk [W;Q] h (M = 128), then P Vn and K^T Vn~; TMA prefetches the next
+//             chunk's tiles into the other stage while the current chunk computes.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/gdr_debug.h"
 #include "gdr_internal.h"
+#include "tc_primitives.cuh"
 
 namespace gdr {
 
-bool tc_available() { return false; }
+namespace {
 
-cudaError_t tc_forward(const Dims&, const FwdArgs&, const Workspace&, cudaStream_t) {
-  return cudaErrorNotSupported;
+using bf16 = __nv_bfloat16;
+constexpr int kTcThreads = 128;
+constexpr uint32_t kSlab = 64 * 128;  // bytes of one 64-row x 128-byte slab
+
+// ---------------------------------------------------------------------------------
+// host: tensor maps
+// ---------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+  });
+  return g_encode != nullptr;
 }
+
+// 3D map over a [rows][heads][cols] bf16 tensor, box = 64 columns x 1 head x 64 rows.
+bool map_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t heads, uint64_t rows) {
+  cuuint64_t dims[3] = {cols, heads, rows};
+  cuuint64_t strides[2] = {cols * 2, heads * cols * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D map over a [rows][cols] bf16 matrix, box = 64 columns x 64 rows.
+bool map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
+  return (unsigned char*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
+}
+
+// Store 64 fp32 values as bf16 into row `row` of a 64-column swizzled slab.
+__device__ __forceinline__ void st_row_bf16(unsigned char* slab, int row, const float* v) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    uint4 w;
+    uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[ch * 8 + 2 * e], v[ch * 8 + 2 * e + 1]);
+      wp[e] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(slab + row * 128 + (((ch ^ (row & 7)) & 7) << 4)) = w;
+  }
+}
+
+// Load row `row` (64 bf16) of a 64-column swizzled slab as fp32.
+__device__ __forceinline__ void ld_row_bf16(const unsigned char* slab, int row, float* v) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    const uint4 w = *reinterpret_cast<const uint4*>(slab + row * 128 + (((ch ^ (row & 7)) & 7) << 4));
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&wp[e]);
+      const float2 f = __bfloat1622float2(b);
+      v[ch * 8 + 2 * e] = f.x;
+      v[ch * 8 + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+// 64 fp32 -> 64 bf16 in global memory (128 bytes, 16-byte aligned).
+__device__ __forceinline__ void st_global_bf16x64(bf16* dst, const float* v) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    uint4 w;
+    uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[ch * 8 + 2 * e], v[ch * 8 + 2 * e + 1]);
+      wp[e] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    reinterpret_cast<uint4*>(dst)[ch] = w;
+  }
+}
+
+// Loads 64 TMEM columns [col, col + 64) of this thread's lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t tbase, int warp, int col, float* v) {
+  tc::tmem_ld32(tc::tmem_lane_addr(tbase, warp, col), v);
+  tc::tmem_ld32(tc::tmem_lane_addr(tbase, warp, col + 32), v + 32);
+  tc::tmem_wait_ld();
+}
+
+// In-chunk inclusive cumsum of g over 64 rows (threads 0-63 hold row tid);
+// returns gamma_r for r = tid < 64.  `scratch` holds 1 float.
+__device__ __forceinline__ float chunk_cumsum64(float x, int tid, float* scratch) {
+  const int lane = tid & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (tid == 31) *scratch = x;
+  __syncthreads();
+  if (tid >= 32 && tid < 64) x += *scratch;
+  return x;
+}
+
+// ---------------------------------------------------------------------------------
+// tc_prep: W, U, P, gamma of one (chunk, v-head)
+// ---------------------------------------------------------------------------------
+struct PrepSmem {
+  static constexpr uint32_t KQ = 0;              // [K | Q] x 2 slabs: 32 KB
+  static constexpr uint32_t V = 32768;           // 2 slabs: 16 KB
+  static constexpr uint32_t TT = V + 16384;      // [T' | T''] bf16: 16 KB
+  static constexpr uint32_t A = TT + 16384;      // fp32 [64][64]: 16 KB
+  static constexpr uint32_t BYTES = A + 16384;   // 80 KB
+};
+
+__global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                             const __grid_constant__ CUtensorMap tm_k,
+                                                             const __grid_constant__ CUtensorMap tm_v, Dims d,
+                                                             const float* __restrict__ g,
+                                                             const bf16* __restrict__ beta, Workspace ws) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = align1024(smem_raw);
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tmem_slot;
+  __shared__ float s_gam[64], s_beta[64], s_carry;
+  const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int4 ci = ws.chunks[c];
+  const int len = ci.z, t0 = ci.y;
+  if (len <= 0) return;
+  const int Hv = d.Hv;
+  const size_t ch = (size_t)c * Hv + j;
+
+  if (tid == 0) {
+    tc::mbar_init(&bar_tma, 1);
+    tc::mbar_init(&bar_mma, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tbase = tmem_slot;
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&bar_tma, 6 * kSlab);
+    tc::tma_load_3d(sm + PrepSmem::KQ, &tm_k, &bar_tma, 0, i, t0);
+    tc::tma_load_3d(sm + PrepSmem::KQ + 2 * kSlab, &tm_k, &bar_tma, 64, i, t0);
+    tc::tma_load_3d(sm + PrepSmem::KQ + kSlab, &tm_q, &bar_tma, 0, i, t0);
+    tc::tma_load_3d(sm + PrepSmem::KQ + 3 * kSlab, &tm_q, &bar_tma, 64, i, t0);
+    tc::tma_load_3d(sm + PrepSmem::V, &tm_v, &bar_tma, 0, j, t0);
+    tc::tma_load_3d(sm + PrepSmem::V + kSlab, &tm_v, &bar_tma, 64, j, t0);
+  }
+  // gamma (in-chunk cumsum of g) and beta, zero past the chunk end
+  {
+    float x = 0.f, b = 0.f;
+    if (tid < 64 && tid < len) {
+      x = g[(size_t)(t0 + tid) * Hv + j];
+      b = __bfloat162float(beta[(size_t)(t0 + tid) * Hv + j]);
+    }
+    x = chunk_cumsum64(x, tid, &s_carry);
+    if (tid < 64) {
+      s_gam[tid] = x;
+      s_beta[tid] = b;
+    }
+  }
+  bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma, 0, ws.status, kDevErrTimeoutPrep));
+  const uint32_t s_kq = tc::smem_u32(sm + PrepSmem::KQ), s_v = tc::smem_u32(sm + PrepSmem::V);
+  const uint32_t s_tt = tc::smem_u32(sm + PrepSmem::TT);
+  if (ok && tid == 0) {
+    tc::tc_fence_after();
+    const uint32_t id = tc::idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      tc::mma_bf16(tbase, tc::kmajor_step_desc(s_kq, 2 * kSlab, kk), tc::kmajor_step_desc(s_kq, 2 * kSlab, kk), id,
+                   kk > 0);
+    tc::mma_commit(&bar_mma);
+  }
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutPrep));
+  tc::tc_fence_after();
+  float* sA = reinterpret_cast<float*>(sm + PrepSmem::A);
+  if (ok) {
+    float row[64];
+    tmem_ld64(tbase, warp, 0, row);
+    const int r = tid & 63;
+    const float gr = s_gam[r];
+    if (tid < 64) {  // A row r
+      const float br = s_beta[r];
+#pragma unroll
+      for (int s = 0; s < 64; ++s) sA[r * 64 + s] = (s < r && r < len) ? br * __expf(gr - s_gam[s]) * row[s] : 0.f;
+    } else {  // P row r
+#pragma unroll
+      for (int s = 0; s < 64; ++s) row[s] = (s <= r && r < len) ? row[s] * __expf(gr - s_gam[s]) : 0.f;
+      st_global_bf16x64((bf16*)ws.P + (ch * 64 + r) * 64, row);
+    }
+  }
+  __syncthreads();
+  // T = (I + A)^{-1}: thread s < 64 owns column s of T in registers
+  if (ok && tid < 64) {
+    const int s = tid;
+    float tcol[64];
+#pragma unroll
+    for (int r = 0; r < 64; ++r) {
+      float acc0 = (r == s) ? 1.f : 0.f, acc1 = 0.f;
+      const float* Ar = sA + r * 64;
+#pragma unroll
+      for (int m = 0; m + 1 < r; m += 2) {
+        acc0 -= Ar[m] * tcol[m];
+        acc1 -= Ar[m + 1] * tcol[m + 1];
+      }
+      if (r & 1) acc0 -= Ar[r - 1] * tcol[r - 1];
+      tcol[r] = acc0 + acc1;
+    }
+    const float bs = s_beta[s], es = bs * __expf(s_gam[s]);
+    unsigned char* tt = sm + PrepSmem::TT;
+#pragma unroll
+    for (int r = 0; r < 64; ++r) {
+      *reinterpret_cast<bf16*>(tt + tc::sw128_off(r, s, 64)) = __float2bfloat16_rn(tcol[r] * es);          // T'
+      *reinterpret_cast<bf16*>(tt + kSlab + tc::sw128_off(r, s, 64)) = __float2bfloat16_rn(tcol[r] * bs);  // T''
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  if (ok && tid == 0) {
+    tc::tc_fence_after();
+    // W = T' K (lanes 0-63 of cols [0,128)), U = T'' V (lanes 64-127 of cols [128,256))
+    const uint32_t id = tc::idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t a = tc::kmajor_step_desc(s_tt, kSlab, kk);
+      tc::mma_bf16(tbase, a, tc::mnmajor_step_desc(s_kq, 2 * kSlab, kk), id, kk > 0);
+      tc::mma_bf16(tbase + 128, a, tc::mnmajor_step_desc(s_v, kSlab, kk), id, kk > 0);
+    }
+    tc::mma_commit(&bar_mma);
+  }
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutPrep));
+  tc::tc_fence_after();
+  if (ok) {
+    const int r = tid & 63;
+    bf16* dst = (tid < 64 ? (bf16*)ws.W : (bf16*)ws.U) + (ch * 64 + r) * 128;
+    const int col = tid < 64 ? 0 : 128;
+    float v[64];
+    tmem_ld64(tbase, warp, col, v);
+    st_global_bf16x64(dst, v);
+    tmem_ld64(tbase, warp, col + 64, v);
+    st_global_bf16x64(dst + 64, v);
+    if (tid < 64) ws.gam[ch * 64 + tid] = s_gam[tid];
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tbase, 256);
+}
+
+// ---------------------------------------------------------------------------------
+// tc_fwd_state: sequential chunk walk of one (sequence, v-head, 64-wide DV slice)
+// ---------------------------------------------------------------------------------
+struct StateSmem {
+  // per stage: [W|Q] x 2 slabs (32 KB), K 2 slabs (16 KB), [U | P] (16 KB)
+  static constexpr uint32_t STAGE = 65536;
+  static constexpr uint32_t WQ = 0, K = 32768, U = 49152, P = 57344;
+  static constexpr uint32_t H = 2 * STAGE;        // h as bf16 B operand: 128 rows x 128 B = 16 KB
+  static constexpr uint32_t VN = H + 16384;       // Vn (8 KB)
+  static constexpr uint32_t VT = VN + 8192;       // Vn scaled by e^{gamma_C - gamma} (8 KB)
+  static constexpr uint32_t BYTES = VT + 8192;    // 160 KB
+};
+
+__global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
+    const __grid_constant__ CUtensorMap tm_p, Dims d, const float* __restrict__ S0, float* __restrict__ S_T,
+    float* __restrict__ h_saved, bf16* __restrict__ o, Workspace ws) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = align1024(smem_raw);
+  __shared__ uint64_t bar_load[2], bar_mma;
+  __shared__ uint32_t tmem_slot;
+  const int n = ws.seq_order[blockIdx.x], j = blockIdx.y, i = j / d.G;
+  const int dv0 = blockIdx.z * 64;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int Hv = d.Hv;
+  const int c_begin = ws.seq_chunk_off[n], c_end = ws.seq_chunk_off[n + 1];
+
+  if (tid == 0) {
+    tc::mbar_init(&bar_load[0], 1);
+    tc::mbar_init(&bar_load[1], 1);
+    tc::mbar_init(&bar_mma, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tbase = tmem_slot;
+  const uint32_t D1 = tbase, D2 = tbase + 64, D3 = tbase + 128;
+
+  // h row `tid` (dk = tid), columns dv0 .. dv0 + 63
+  float h[64];
+  {
+    const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
+#pragma unroll
+    for (int b = 0; b < 64; ++b)
+      h[b] = S0 ? S0[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] : 0.f;
+  }
+  auto issue_loads = [&](int c, int st) {
+    const int4 cc = ws.chunks[c];
+    const size_t chh = (size_t)c * Hv + j;
+    unsigned char* base = sm + st * StateSmem::STAGE;
+    tc::mbar_arrive_expect_tx(&bar_load[st], 8 * kSlab);
+    tc::tma_load_2d(base + StateSmem::WQ, &tm_w, &bar_load[st], 0, (int)(chh * 64));
+    tc::tma_load_2d(base + StateSmem::WQ + 2 * kSlab, &tm_w, &bar_load[st], 64, (int)(chh * 64));
+    tc::tma_load_3d(base + StateSmem::WQ + kSlab, &tm_q, &bar_load[st], 0, i, cc.y);
+    tc::tma_load_3d(base + StateSmem::WQ + 3 * kSlab, &tm_q, &bar_load[st], 64, i, cc.y);
+    tc::tma_load_3d(base + StateSmem::K, &tm_k, &bar_load[st], 0, i, cc.y);
+    tc::tma_load_3d(base + StateSmem::K + kSlab, &tm_k, &bar_load[st], 64, i, cc.y);
+    tc::tma_load_2d(base + StateSmem::U, &tm_u, &bar_load[st], dv0, (int)(chh * 64));
+    tc::tma_load_2d(base + StateSmem::P, &tm_p, &bar_load[st], 0, (int)(chh * 64));
+  };
+  if (tid == 0 && c_begin < c_end) issue_loads(c_begin, 0);
+
+  bool ok = true;
+  uint32_t mma_phase = 0;
+  const uint32_t s_h = tc::smem_u32(sm + StateSmem::H), s_vn = tc::smem_u32(sm + StateSmem::VN);
+  const uint32_t s_vt = tc::smem_u32(sm + StateSmem::VT);
+  for (int c = c_begin; c < c_end && ok; ++c) {
+    const int it = c - c_begin, st = it & 1;
+    const uint32_t ld_phase = (it >> 1) & 1;
+    const int4 cc = ws.chunks[c];
+    const int len = cc.z, t0 = cc.y;
+    const size_t chh = (size_t)c * Hv + j;
+    if (tid == 0 && c + 1 < c_end) issue_loads(c + 1, st ^ 1);
+    // save the chunk-start state and stage h as the bf16 B operand
+    {
+      float* hs = h_saved + chh * 128 * 128 + (size_t)tid * 128 + dv0;
+#pragma unroll
+      for (int b = 0; b < 64; b += 4) *reinterpret_cast<float4*>(hs + b) = make_float4(h[b], h[b + 1], h[b + 2], h[b + 3]);
+      st_row_bf16(sm + StateSmem::H, tid, h);
+    }
+    const int r = tid & 63;
+    const float gC = ws.gam[chh * 64 + len - 1];
+    const float gr = ws.gam[chh * 64 + r];
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    ok = __syncthreads_and(tc::mbar_wait(&bar_load[st], ld_phase, ws.status, kDevErrTimeoutFwd));
+    unsigned char* stg = sm + st * StateSmem::STAGE;
+    const uint32_t s_wq = tc::smem_u32(stg + StateSmem::WQ), s_k = tc::smem_u32(stg + StateSmem::K);
+    const uint32_t s_up = tc::smem_u32(stg + StateSmem::U);
+    if (ok && tid == 0) {
+      tc::tc_fence_after();
+      const uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // [W;Q] h
+        tc::mma_bf16(D1, tc::kmajor_step_desc(s_wq, 2 * kSlab, kk), tc::mnmajor_step_desc(s_h, 16384, kk), id, kk > 0);
+      tc::mma_commit(&bar_mma);
+    }
+    ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutFwd));
+    mma_phase ^= 1;
+    tc::tc_fence_after();
+    float x[64];
+    if (ok) {
+      tmem_ld64(tbase, warp, 0, x);
+      if (tid < 64) {  // Vn = U - W h
+        float u[64];
+        ld_row_bf16(stg + StateSmem::U, r, u);
+#pragma unroll
+        for (int b = 0; b < 64; ++b) u[b] -= x[b];
+        st_row_bf16(sm + StateSmem::VN, r, u);
+        const float dec = __expf(gC - gr);
+#pragma unroll
+        for (int b = 0; b < 64; ++b) u[b] *= dec;
+        st_row_bf16(sm + StateSmem::VT, r, u);
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (ok && tid == 0) {
+      tc::tc_fence_after();
+      const uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
+      const uint32_t idt = tc::idesc_bf16(128, 64, 1, 1);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        // rows 64-127 of this A operand are P (rows 0-63 are the U tile: unused lanes)
+        tc::mma_bf16(D2, tc::kmajor_step_desc(s_up, kSlab, kk), tc::mnmajor_step_desc(s_vn, kSlab, kk), id, kk > 0);
+        // K^T Vn~: A = K^T (MN-major view of the K tile)
+        tc::mma_bf16(D3, tc::mnmajor_step_desc(s_k, kSlab, kk), tc::mnmajor_step_desc(s_vt, kSlab, kk), idt, kk > 0);
+      }
+      tc::mma_commit(&bar_mma);
+    }
+    ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutFwd));
+    mma_phase ^= 1;
+    tc::tc_fence_after();
+    if (ok) {
+      float y[64];
+      if (tid >= 64) {  // O rows: x holds (Q h)[r], D2 lanes 64-127 hold (P Vn)[r]
+        tmem_ld64(tbase, warp, 64, y);
+        if (r < len) {
+          const float eg = __expf(gr);
+#pragma unroll
+          for (int b = 0; b < 64; ++b) y[b] = d.scale * (eg * x[b] + y[b]);
+          st_global_bf16x64(o + ((size_t)(t0 + r) * Hv + j) * 128 + dv0, y);
+        }
+      }
+      tmem_ld64(tbase, warp, 128, y);
+      const float eC = __expf(gC);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) h[b] = eC * h[b] + y[b];
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+  }
+  if (ok && S_T) {
+    const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
+#pragma unroll
+    for (int b = 0; b < 64; ++b)
+      S_T[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] = h[b];
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tbase, 256);
+}
+
+}  // namespace
+
+bool tc_available() { return get_encoder(); }
+
+bool tc_bwd_available() { return false; }
+
+cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s) {
+  if (!get_encoder()) return cudaErrorNotSupported;
+  CUtensorMap tq, tk, tv, tw, tu, tp;
+  const uint64_t Tt = (uint64_t)d.T_total;
+  const uint64_t rows = (uint64_t)d.max_chunks * d.Hv * 64;
+  if (Tt == 0 && d.num_seqs == 0) return cudaSuccess;
+  const uint64_t Tmap = Tt > 0 ? Tt : 1;
+  if (!map_3d(&tq, a.q, 128, d.Hk, Tmap) || !map_3d(&tk, a.k, 128, d.Hk, Tmap) ||
+      !map_3d(&tv, a.v, 128, d.Hv, Tmap))
+    return cudaErrorInvalidValue;
+  if (rows > 0 && (!map_2d(&tw, ws.W, 128, rows) || !map_2d(&tu, ws.U, 128, rows) || !map_2d(&tp, ws.P, 64, rows)))
+    return cudaErrorInvalidValue;
+  if (d.max_chunks > 0 && Tt > 0) {
+    const size_t smp = PrepSmem::BYTES + 1024;
+    cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
+    tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, d, a.g, (const bf16*)a.beta, ws);
+    stage_mark(s, "fwd_prep");
+  }
+  if (d.num_seqs > 0) {
+    const size_t sms = StateSmem::BYTES + 1024;
+    cudaFuncSetAttribute(tc_fwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
+    tc_fwd_state_kernel<<<dim3(d.num_seqs, d.Hv, 2), kTcThreads, sms, s>>>(tq, tk, tw, tu, tp, d, a.S0, a.S_T,
+                                                                         a.h_saved, (bf16*)a.o, ws);
+    stage_mark(s, "fwd_state");
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t tc_backward(const Dims&, const BwdArgs&, const Workspace&, cudaStream_t) {
   return cudaErrorNotSupported;
 }

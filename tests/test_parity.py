@@ -143,3 +143,12 @@ def test_autograd_function_matches_oracle():
     got = {"o": o, "S_T": ST, "dq": leaves["q"].grad, "dk": leaves["k"].grad, "dv": leaves["v"].grad,
            "dg": leaves["g"].grad, "dbeta": leaves["beta"].grad, "dS0": leaves["S0"].grad}
     compare(got, ref, tol_for(torch.bfloat16))
+
+
+def test_tensor_core_path_is_selected_for_bf16_d128():
+    import chunked_gated_delta_04_gb300 as gdr
+
+    p = gdr.make_problem(2, 4096, 16, 16, 128, 128, torch.bfloat16, "KV")
+    assert gdr.gdr_path(p) == 1
+    p32 = gdr.make_problem(1, 128, 1, 1, 64, 64, torch.float32, "KV")
+    assert gdr.gdr_path(p32) == 0
