@@ -38,14 +38,15 @@ CHUNK = 64
 # not algorithmic and shows up only in the ncu "traffic" figure).
 STAGE_IO = {
     "index": ("", ""),
-    "fwd_prep": ("k v g beta", ""),
-    "fwd_state": ("S0", "h_saved S_T"),
+    "fwd_prep": ("q k v g beta", ""),
+    "fwd_state": ("q k S0", "o h_saved S_T"),
     "fwd_out": ("q", "o"),
-    "fwd_main": ("q k v g beta S0", "o h_saved S_T"),
-    "bwd_prep": ("k v g beta", ""),
+    "bwd_prep": ("q k v g beta", ""),
     "bwd_vn": ("h_saved", ""),
     "bwd_walk": ("dO dS_T", "dS0"),
     "bwd_grad": ("q k v dO beta h_saved", "dq dk dv dg dbeta"),
+    "bwd_gradA": ("q k dO h_saved", "dq"),
+    "bwd_gradB": ("k v beta", "dk dv dg dbeta"),
     "bwd_group_reduce": ("", "dq dk"),
 }
 

@@ -103,11 +103,18 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
   w.gam = (float*)take(sizeof(float) * chH * kChunk);
   w.W = take(el * chH * kChunk * d.DK);
   w.U = take(el * chH * kChunk * d.DV);
-  w.Vn = take(el * chH * kChunk * d.DV);
+  if (d.path == 0) w.Vn = take(el * chH * kChunk * d.DV);
   if (d.path == 1) w.P = take(el * chH * kChunk * kChunk);
   if (backward) {
     if (d.path == 0) w.Tm = (float*)take(sizeof(float) * chH * kChunk * kChunk);
-    w.dhp = (float*)take(sizeof(float) * chH * d.DK * d.DV);
+    w.dhp = take(el * chH * d.DK * d.DV);
+    if (d.path == 1) {
+      w.Tb = take(el * chH * kChunk * kChunk);
+      w.dVn = take(el * chH * kChunk * d.DV);
+      w.dWb = take(el * chH * kChunk * d.DK);
+      w.dKA = take(el * chH * kChunk * d.DK);
+      w.dgamA = (float*)take(sizeof(float) * chH * kChunk);
+    }
     if (d.G > 1) {
       w.dq_part = (float*)take(sizeof(float) * (size_t)d.T_total * d.Hv * d.DK);
       w.dk_part = (float*)take(sizeof(float) * (size_t)d.T_total * d.Hv * d.DK);

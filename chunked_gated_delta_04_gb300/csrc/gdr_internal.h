@@ -2,6 +2,7 @@
 // (host API, index kernel, SIMT kernels, tcgen05 kernels).  Not part of the ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -45,7 +46,13 @@ struct Workspace {
   float* gam;    // [max_chunks][Hv][64] in-chunk cumsum of g
   void* Vn;      // [max_chunks][Hv][64][DV]
   float* Tm;     // SIMT backward: [max_chunks][Hv][64][64]
-  float* dhp;    // backward: [max_chunks][Hv][DK][DV] state gradient at each chunk's end
+  void* dhp;     // backward: [max_chunks][Hv][DK][DV] state gradient at each chunk's end
+                 // (fp32 on the SIMT path, bf16 on the tensor-core path)
+  void* Tb;      // tensor-core backward: T = (I + A)^{-1}, bf16 [max_chunks][Hv][64][64]
+  void* dVn;     // tensor-core backward: dL/dVn, bf16 [max_chunks][Hv][64][DV]
+  void* dWb;     // tensor-core backward: dL/dW, bf16 [max_chunks][Hv][64][DK]
+  void* dKA;     // tensor-core backward: dk terms from the output/state path, bf16 [..][64][DK]
+  float* dgamA;  // tensor-core backward: d gamma terms from the output/state path, [..][64]
   float* dq_part;  // backward, Hv > Hk: [T_total][Hv][DK]
   float* dk_part;  // backward, Hv > Hk: [T_total][Hv][DK]
 };
@@ -92,10 +99,21 @@ cudaError_t launch_index(const Dims& d, const Workspace& ws, cudaStream_t s);
 cudaError_t simt_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s);
 cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cudaStream_t s);
 
+// Sums dq_part / dk_part over the v-heads of each q/k head into dq / dk (dtype).
+cudaError_t launch_group_reduce(const Dims& d, void* dq, void* dk, const Workspace& ws, cudaStream_t s);
+
 // tcgen05 kernels (bf16, DK = DV = 128).  tc_available() is false when this build
 // leaves them out.
 bool tc_available();
+// Tensor maps (host): 3D over [rows][heads][cols] with a 64 x 1 x 64 box, 2D over
+// [rows][cols] with a 64 x 64 box; bf16, 128-byte swizzle.
+bool get_encoder();
+bool map_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t heads, uint64_t rows);
+bool map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows);
 bool tc_bwd_available();  // the tensor-core backward is built
+// The chunk-prep kernel (W, U, P, gamma; with write_T also T) on the tensor cores.
+cudaError_t tc_launch_prep(const Dims& d, const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, const Workspace& ws, int write_T, cudaStream_t s, const char* stage);
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s);
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cudaStream_t s);
 

@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) simt_walk_kernel(Dims d, const IT* _
     const size_t ch = (size_t)c * Hv + j;
     for (int e = tid; e < DK * dvs; e += kThreads) {
       const int a = e / dvs, b = e % dvs;
-      ws.dhp[ch * DK * DV + (size_t)a * DV + dv0 + b] = sdh[e];
+      ((float*)ws.dhp)[ch * DK * DV + (size_t)a * DV + dv0 + b] = sdh[e];
     }
     for (int r = tid; r < kChunk; r += kThreads) sg[r] = ws.gam[ch * kChunk + r];
     __syncthreads();
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kThreads) simt_grad_kernel(Dims d, const IT* _
   float* sred = skdv + kChunk;      // [32] block reduction scratch
   const size_t ch = (size_t)c * Hv + j;
   const float* h = h_saved + ch * DK * DV;
-  const float* dhp = ws.dhp + ch * DK * DV;
+  const float* dhp = (const float*)ws.dhp + ch * DK * DV;
   const float* Vn = (const float*)ws.Vn + ch * kChunk * DV;
   const float* Tg = ws.Tm + ch * kChunk * kChunk;
   auto Q = [&](int r, int x) { return ldf(q + ((size_t)(t0 + r) * Hk + i) * DK + x); };
@@ -575,6 +575,19 @@ __global__ void __launch_bounds__(kThreads) simt_group_reduce_kernel(Dims d, IT*
     dk[e] = from_f32<IT>(sk);
   }
 }
+
+}  // namespace
+
+cudaError_t launch_group_reduce(const Dims& d, void* dq, void* dk, const Workspace& ws, cudaStream_t s) {
+  if (d.dtype == GDR_DTYPE_F32)
+    simt_group_reduce_kernel<float><<<1024, kThreads, 0, s>>>(d, (float*)dq, (float*)dk, ws);
+  else
+    simt_group_reduce_kernel<__nv_bfloat16><<<1024, kThreads, 0, s>>>(d, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, ws);
+  stage_mark(s, "bwd_group_reduce");
+  return cudaGetLastError();
+}
+
+namespace {
 
 inline int dv_slice(const Dims& d) { return d.DV % 32 == 0 ? 32 : 16; }
 

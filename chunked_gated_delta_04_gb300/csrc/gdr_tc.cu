@@ -27,21 +27,22 @@
 
 #include "../../include/gdr_debug.h"
 #include "gdr_internal.h"
+#include "tc_common.cuh"
 #include "tc_primitives.cuh"
 
 namespace gdr {
 
 namespace {
 
-using bf16 = __nv_bfloat16;
-constexpr int kTcThreads = 128;
-constexpr uint32_t kSlab = 64 * 128;  // bytes of one 64-row x 128-byte slab
+using namespace tcx;
 
 // ---------------------------------------------------------------------------------
 // host: tensor maps
 // ---------------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+
+}  // namespace
 
 bool get_encoder() {
   std::call_once(g_encode_once, [] {
@@ -77,80 +78,7 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// ---------------------------------------------------------------------------------
-// device helpers
-// ---------------------------------------------------------------------------------
-__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
-  return (unsigned char*)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);
-}
-
-// Store 64 fp32 values as bf16 into row `row` of a 64-column swizzled slab.
-__device__ __forceinline__ void st_row_bf16(unsigned char* slab, int row, const float* v) {
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    uint4 w;
-    uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(v[ch * 8 + 2 * e], v[ch * 8 + 2 * e + 1]);
-      wp[e] = *reinterpret_cast<uint32_t*>(&b);
-    }
-    *reinterpret_cast<uint4*>(slab + row * 128 + (((ch ^ (row & 7)) & 7) << 4)) = w;
-  }
-}
-
-// Load row `row` (64 bf16) of a 64-column swizzled slab as fp32.
-__device__ __forceinline__ void ld_row_bf16(const unsigned char* slab, int row, float* v) {
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    const uint4 w = *reinterpret_cast<const uint4*>(slab + row * 128 + (((ch ^ (row & 7)) & 7) << 4));
-    const uint32_t* wp = reinterpret_cast<const uint32_t*>(&w);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&wp[e]);
-      const float2 f = __bfloat1622float2(b);
-      v[ch * 8 + 2 * e] = f.x;
-      v[ch * 8 + 2 * e + 1] = f.y;
-    }
-  }
-}
-
-// 64 fp32 -> 64 bf16 in global memory (128 bytes, 16-byte aligned).
-__device__ __forceinline__ void st_global_bf16x64(bf16* dst, const float* v) {
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    uint4 w;
-    uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      __nv_bfloat162 b = __floats2bfloat162_rn(v[ch * 8 + 2 * e], v[ch * 8 + 2 * e + 1]);
-      wp[e] = *reinterpret_cast<uint32_t*>(&b);
-    }
-    reinterpret_cast<uint4*>(dst)[ch] = w;
-  }
-}
-
-// Loads 64 TMEM columns [col, col + 64) of this thread's lane.
-__device__ __forceinline__ void tmem_ld64(uint32_t tbase, int warp, int col, float* v) {
-  tc::tmem_ld32(tc::tmem_lane_addr(tbase, warp, col), v);
-  tc::tmem_ld32(tc::tmem_lane_addr(tbase, warp, col + 32), v + 32);
-  tc::tmem_wait_ld();
-}
-
-// In-chunk inclusive cumsum of g over 64 rows (threads 0-63 hold row tid);
-// returns gamma_r for r = tid < 64.  `scratch` holds 1 float.
-__device__ __forceinline__ float chunk_cumsum64(float x, int tid, float* scratch) {
-  const int lane = tid & 31;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (tid == 31) *scratch = x;
-  __syncthreads();
-  if (tid >= 32 && tid < 64) x += *scratch;
-  return x;
-}
+namespace {
 
 // ---------------------------------------------------------------------------------
 // tc_prep: W, U, P, gamma of one (chunk, v-head)
@@ -167,7 +95,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
                                                              const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v, Dims d,
                                                              const float* __restrict__ g,
-                                                             const bf16* __restrict__ beta, Workspace ws) {
+                                                             const bf16* __restrict__ beta, Workspace ws,
+                                                             int write_T) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint64_t bar_tma, bar_mma;
@@ -261,6 +190,11 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
       tcol[r] = acc0 + acc1;
     }
     const float bs = s_beta[s], es = bs * __expf(s_gam[s]);
+    if (write_T) {  // T itself, for the backward (row r, column s)
+      bf16* Tg = (bf16*)ws.Tb + ch * 64 * 64 + s;
+#pragma unroll
+      for (int r = 0; r < 64; ++r) Tg[r * 64] = __float2bfloat16_rn(tcol[r]);
+    }
     unsigned char* tt = sm + PrepSmem::TT;
 #pragma unroll
     for (int r = 0; r < 64; ++r) {
@@ -311,7 +245,8 @@ struct StateSmem {
   static constexpr uint32_t H = 2 * STAGE;        // h as bf16 B operand: 128 rows x 128 B = 16 KB
   static constexpr uint32_t VN = H + 16384;       // Vn (8 KB)
   static constexpr uint32_t VT = VN + 8192;       // Vn scaled by e^{gamma_C - gamma} (8 KB)
-  static constexpr uint32_t BYTES = VT + 8192;    // 160 KB
+  static constexpr uint32_t GAM = VT + 8192;      // gamma of each stage: 2 x 256 B
+  static constexpr uint32_t BYTES = GAM + 512;
 };
 
 __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
@@ -328,6 +263,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
   const int tid = threadIdx.x, warp = tid >> 5;
   const int Hv = d.Hv;
   const int c_begin = ws.seq_chunk_off[n], c_end = ws.seq_chunk_off[n + 1];
+  const int t_seq = d.cu ? d.cu[n] : n * d.T;        // first token of the sequence
+  const int L = d.cu ? d.cu[n + 1] - t_seq : d.T;     // its length
 
   if (tid == 0) {
     tc::mbar_init(&bar_load[0], 1);
@@ -351,16 +288,17 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
       h[b] = S0 ? S0[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] : 0.f;
   }
   auto issue_loads = [&](int c, int st) {
-    const int4 cc = ws.chunks[c];
+    const int tc0 = t_seq + (c - c_begin) * 64;
     const size_t chh = (size_t)c * Hv + j;
     unsigned char* base = sm + st * StateSmem::STAGE;
-    tc::mbar_arrive_expect_tx(&bar_load[st], 8 * kSlab);
+    tc::mbar_arrive_expect_tx(&bar_load[st], 8 * kSlab + 256);
+    tc::bulk_load(sm + StateSmem::GAM + st * 256, ws.gam + chh * 64, 256, &bar_load[st]);
     tc::tma_load_2d(base + StateSmem::WQ, &tm_w, &bar_load[st], 0, (int)(chh * 64));
     tc::tma_load_2d(base + StateSmem::WQ + 2 * kSlab, &tm_w, &bar_load[st], 64, (int)(chh * 64));
-    tc::tma_load_3d(base + StateSmem::WQ + kSlab, &tm_q, &bar_load[st], 0, i, cc.y);
-    tc::tma_load_3d(base + StateSmem::WQ + 3 * kSlab, &tm_q, &bar_load[st], 64, i, cc.y);
-    tc::tma_load_3d(base + StateSmem::K, &tm_k, &bar_load[st], 0, i, cc.y);
-    tc::tma_load_3d(base + StateSmem::K + kSlab, &tm_k, &bar_load[st], 64, i, cc.y);
+    tc::tma_load_3d(base + StateSmem::WQ + kSlab, &tm_q, &bar_load[st], 0, i, tc0);
+    tc::tma_load_3d(base + StateSmem::WQ + 3 * kSlab, &tm_q, &bar_load[st], 64, i, tc0);
+    tc::tma_load_3d(base + StateSmem::K, &tm_k, &bar_load[st], 0, i, tc0);
+    tc::tma_load_3d(base + StateSmem::K + kSlab, &tm_k, &bar_load[st], 64, i, tc0);
     tc::tma_load_2d(base + StateSmem::U, &tm_u, &bar_load[st], dv0, (int)(chh * 64));
     tc::tma_load_2d(base + StateSmem::P, &tm_p, &bar_load[st], 0, (int)(chh * 64));
   };
@@ -373,8 +311,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
   for (int c = c_begin; c < c_end && ok; ++c) {
     const int it = c - c_begin, st = it & 1;
     const uint32_t ld_phase = (it >> 1) & 1;
-    const int4 cc = ws.chunks[c];
-    const int len = cc.z, t0 = cc.y;
+    const int t0 = t_seq + it * 64;
+    const int len = min(64, L - it * 64);
     const size_t chh = (size_t)c * Hv + j;
     if (tid == 0 && c + 1 < c_end) issue_loads(c + 1, st ^ 1);
     // save the chunk-start state and stage h as the bf16 B operand
@@ -385,12 +323,13 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
       st_row_bf16(sm + StateSmem::H, tid, h);
     }
     const int r = tid & 63;
-    const float gC = ws.gam[chh * 64 + len - 1];
-    const float gr = ws.gam[chh * 64 + r];
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     ok = __syncthreads_and(tc::mbar_wait(&bar_load[st], ld_phase, ws.status, kDevErrTimeoutFwd));
+    const float* sgam = reinterpret_cast<const float*>(sm + StateSmem::GAM + st * 256);
+    const float gC = sgam[len - 1];
+    const float gr = sgam[r];
     unsigned char* stg = sm + st * StateSmem::STAGE;
     const uint32_t s_wq = tc::smem_u32(stg + StateSmem::WQ), s_k = tc::smem_u32(stg + StateSmem::K);
     const uint32_t s_up = tc::smem_u32(stg + StateSmem::U);
@@ -473,8 +412,6 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
 
 bool tc_available() { return get_encoder(); }
 
-bool tc_bwd_available() { return false; }
-
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s) {
   if (!get_encoder()) return cudaErrorNotSupported;
   CUtensorMap tq, tk, tv, tw, tu, tp;
@@ -490,7 +427,8 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
   if (d.max_chunks > 0 && Tt > 0) {
     const size_t smp = PrepSmem::BYTES + 1024;
     cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
-    tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, d, a.g, (const bf16*)a.beta, ws);
+    tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, d, a.g, (const bf16*)a.beta, ws,
+                                                                      0);
     stage_mark(s, "fwd_prep");
   }
   if (d.num_seqs > 0) {
@@ -503,8 +441,19 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
   return cudaGetLastError();
 }
 
-cudaError_t tc_backward(const Dims&, const BwdArgs&, const Workspace&, cudaStream_t) {
-  return cudaErrorNotSupported;
+cudaError_t tc_launch_prep(const Dims& d, const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, const Workspace& ws, int write_T, cudaStream_t s, const char* stage) {
+  if (d.max_chunks == 0 || d.T_total == 0) return cudaSuccess;
+  CUtensorMap tq, tk, tv;
+  const uint64_t Tt = (uint64_t)d.T_total;
+  if (!map_3d(&tq, q, 128, d.Hk, Tt) || !map_3d(&tk, k, 128, d.Hk, Tt) || !map_3d(&tv, v, 128, d.Hv, Tt))
+    return cudaErrorInvalidValue;
+  const size_t smp = PrepSmem::BYTES + 1024;
+  cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
+  tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, d, g, (const bf16*)beta, ws,
+                                                                    write_T);
+  stage_mark(s, stage);
+  return cudaGetLastError();
 }
 
 }  // namespace gdr

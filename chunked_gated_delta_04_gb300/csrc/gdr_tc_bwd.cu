@@ -1,0 +1,716 @@
+// gdr_tc_bwd.cu -- tcgen05 backward of the chunked gated delta rule (bf16, DK = DV = 128).
+//
+// The backward (the fused backward of FlashQLA PR #34, which walks the chunks in
+// reverse carrying the state gradient dh) runs as four stages here:
+//   prep   (gdr_tc.cu) W, U, P, gamma and T of every chunk, chunk-parallel.
+//   walk   one CTA per (sequence, v-head, 64-wide DV slice), chunks in reverse; dh
+//          (dL/dh at the chunk end, "dh'") stays in registers:
+//            dVn = scale P^T dO + diag(e^{gamma_C - gamma}) K dh'
+//            dh  = e^{gamma_C} dh' + scale Q^T diag(e^gamma) dO - W^T dVn
+//          writes dh' and dVn of every chunk (bf16) and dS0.
+//   gradA  one CTA per (chunk, v-head): the terms that need h and dh':
+//            Vn = U - W h,  dP = scale (dO Vn^T) * Gam,
+//            dq = scale diag(e^gamma) dO h^T + dP K,
+//            dk_A = dP^T Q + diag(e^{gamma_C - gamma}) Vn dh'^T,  dW = -dVn h^T,
+//          and the gate-gradient terms of the output and state paths.
+//   gradB  one CTA per (chunk, v-head): the WY backward through W = T' K, U = T'' V,
+//          T = (I + A)^{-1}:  dT = dW B_k^T + dVn B_v^T, dB_k = T^T dW, dB_v = T^T dVn,
+//          dA = -strict-lower(T^T dT T^T); then dv, dk, dbeta and dg (in-chunk
+//          reverse cumsum of d gamma).
+// No floating-point atomics anywhere: every reduction has a fixed order, so the
+// backward is bitwise deterministic.
+#include <cudaTypedefs.h>
+
+#include "gdr_internal.h"
+#include "tc_common.cuh"
+#include "tc_primitives.cuh"
+
+namespace gdr {
+namespace {
+
+using namespace tcx;
+using tc::kmaj;
+using tc::mnmaj;
+
+__device__ __forceinline__ void ld_row_bf16_g(const bf16* src, float* v) {  // 64 bf16 from global
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    const uint4 w = reinterpret_cast<const uint4*>(src)[ch];
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wp[e]));
+      v[ch * 8 + 2 * e] = f.x;
+      v[ch * 8 + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+__device__ __forceinline__ float block_sum128(float x, float* red) {  // fixed-order sum over 128 threads
+  x = warp_sum(x);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+  __syncthreads();
+  const float s = (red[0] + red[1]) + (red[2] + red[3]);
+  __syncthreads();
+  return s;
+}
+
+// ---------------------------------------------------------------------------------
+// walk
+// ---------------------------------------------------------------------------------
+struct WalkSmem {
+  static constexpr uint32_t STAGE = 66560;  // KQ 32 KB | W 16 KB | P 8 KB | dO 8 KB | gamma 256 B (+pad)
+  static constexpr uint32_t KQ = 0, W = 32768, P = 49152, DO = 57344, GAM = 65536;
+  static constexpr uint32_t DH = 2 * STAGE;       // dh' as bf16 B operand: 128 rows x 128 B
+  static constexpr uint32_t DVN = DH + 16384;     // dVn bf16 [64][64]
+  static constexpr uint32_t DOS = DVN + 8192;     // diag(e^gamma) dO bf16 [64][64]
+  static constexpr uint32_t BYTES = DOS + 8192;
+};
+
+__global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
+    const __grid_constant__ CUtensorMap tm_do, Dims d, const float* __restrict__ dS_T, float* __restrict__ dS0,
+    Workspace ws) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = align1024(smem_raw);
+  __shared__ uint64_t bar_load[2], bar_mma;
+  __shared__ uint32_t tmem_slot;
+  const int n = ws.seq_order[blockIdx.x], j = blockIdx.y, i = j / d.G;
+  const int dv0 = blockIdx.z * 64;
+  const int tid = threadIdx.x, warp = tid >> 5, r = tid & 63;
+  const int Hv = d.Hv;
+  const int c_begin = ws.seq_chunk_off[n], c_end = ws.seq_chunk_off[n + 1];
+  const int t_seq = d.cu ? d.cu[n] : n * d.T;
+  const int L = d.cu ? d.cu[n + 1] - t_seq : d.T;
+
+  if (tid == 0) {
+    tc::mbar_init(&bar_load[0], 1);
+    tc::mbar_init(&bar_load[1], 1);
+    tc::mbar_init(&bar_mma, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tb = tmem_slot;
+  const uint32_t Da = tb, Db = tb + 64, Dc = tb + 128, Dd = tb + 192;
+
+  float dh[64];  // dL/dh at the end of the current chunk, row dk = tid, columns dv0..dv0+63
+  {
+    const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
+#pragma unroll
+    for (int b = 0; b < 64; ++b)
+      dh[b] = dS_T ? dS_T[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] : 0.f;
+  }
+  auto issue_loads = [&](int c, int st) {
+    const int tc0 = t_seq + (c - c_begin) * 64;
+    const size_t chh = (size_t)c * Hv + j;
+    unsigned char* base = sm + st * WalkSmem::STAGE;
+    uint64_t* bar = &bar_load[st];
+    tc::mbar_arrive_expect_tx(bar, 8 * kSlab + 256);
+    tc::bulk_load(base + WalkSmem::GAM, ws.gam + chh * 64, 256, bar);
+    tc::tma_load_3d(base + WalkSmem::KQ, &tm_k, bar, 0, i, tc0);
+    tc::tma_load_3d(base + WalkSmem::KQ + 2 * kSlab, &tm_k, bar, 64, i, tc0);
+    tc::tma_load_3d(base + WalkSmem::KQ + kSlab, &tm_q, bar, 0, i, tc0);
+    tc::tma_load_3d(base + WalkSmem::KQ + 3 * kSlab, &tm_q, bar, 64, i, tc0);
+    tc::tma_load_2d(base + WalkSmem::W, &tm_w, bar, 0, (int)(chh * 64));
+    tc::tma_load_2d(base + WalkSmem::W + kSlab, &tm_w, bar, 64, (int)(chh * 64));
+    tc::tma_load_2d(base + WalkSmem::P, &tm_p, bar, 0, (int)(chh * 64));
+    tc::tma_load_3d(base + WalkSmem::DO, &tm_do, bar, dv0, j, tc0);
+  };
+  if (tid == 0 && c_begin < c_end) issue_loads(c_end - 1, 0);
+
+  bool ok = true;
+  uint32_t mma_phase = 0;
+  for (int it = 0; c_end - 1 - it >= c_begin && ok; ++it) {
+    const int c = c_end - 1 - it, st = it & 1;
+    const uint32_t ld_phase = (it >> 1) & 1;
+    const int t0 = t_seq + (c - c_begin) * 64;
+    const int len = min(64, L - (c - c_begin) * 64);
+    (void)t0;
+    const size_t chh = (size_t)c * Hv + j;
+    if (tid == 0 && c - 1 >= c_begin) issue_loads(c - 1, st ^ 1);
+    st_global_bf16x64((bf16*)ws.dhp + (chh * 128 + tid) * 128 + dv0, dh);
+    st_row_bf16(sm + WalkSmem::DH, tid, dh);
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    ok = __syncthreads_and(tc::mbar_wait(&bar_load[st], ld_phase, ws.status, kDevErrTimeoutBwd));
+    unsigned char* stg = sm + st * WalkSmem::STAGE;
+    const float* sgam = reinterpret_cast<const float*>(stg + WalkSmem::GAM);
+    const float gC = sgam[len - 1], gr = sgam[r];
+    if (ok && tid >= 64) {  // diag(e^gamma) dO, zero past the chunk end
+      float x[64];
+      ld_row_bf16(stg + WalkSmem::DO, r, x);
+      const float e = r < len ? __expf(gr) : 0.f;
+#pragma unroll
+      for (int b = 0; b < 64; ++b) x[b] *= e;
+      st_row_bf16(sm + WalkSmem::DOS, r, x);
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (ok && tid == 0) {
+      tc::tc_fence_after();
+      tc::gemm(Da, kmaj(stg + WalkSmem::KQ, 2 * kSlab), mnmaj(sm + WalkSmem::DH, 16384), 64, 8, false);  // K dh'
+      tc::gemm(Db, mnmaj(stg + WalkSmem::P, kSlab), mnmaj(stg + WalkSmem::DO, kSlab), 64, 4, false);     // P^T dO
+      tc::gemm(Dd, mnmaj(stg + WalkSmem::KQ + kSlab, 2 * kSlab), mnmaj(sm + WalkSmem::DOS, kSlab), 64, 4,
+               false);  // Q^T diag(e^gamma) dO
+      tc::mma_commit(&bar_mma);
+    }
+    ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutBwd));
+    mma_phase ^= 1;
+    tc::tc_fence_after();
+    if (ok && tid < 64) {
+      float x[64], y[64];
+      tmem_ld64(tb, warp, 0, x);
+      tmem_ld64(tb, warp, 64, y);
+      const float dec = __expf(gC - gr);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) y[b] = r < len ? d.scale * y[b] + dec * x[b] : 0.f;
+      st_row_bf16(sm + WalkSmem::DVN, r, y);
+      st_global_bf16x64((bf16*)ws.dVn + (chh * 64 + r) * 128 + dv0, y);
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (ok && tid == 0) {
+      tc::tc_fence_after();
+      tc::gemm(Dc, mnmaj(stg + WalkSmem::W, kSlab), mnmaj(sm + WalkSmem::DVN, kSlab), 64, 4, false);  // W^T dVn
+      tc::mma_commit(&bar_mma);
+    }
+    ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutBwd));
+    mma_phase ^= 1;
+    tc::tc_fence_after();
+    if (ok) {
+      float x[64], y[64];
+      tmem_ld64(tb, warp, 128, x);
+      tmem_ld64(tb, warp, 192, y);
+      const float eC = __expf(gC);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) dh[b] = eC * dh[b] + d.scale * y[b] - x[b];
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+  }
+  if (ok && dS0) {
+    const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
+#pragma unroll
+    for (int b = 0; b < 64; ++b)
+      dS0[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] = dh[b];
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tb, 256);
+}
+
+// ---------------------------------------------------------------------------------
+// gradA
+// ---------------------------------------------------------------------------------
+struct GradASmem {
+  static constexpr uint32_t KQ = 0;             // [K | Q] x 2 slabs (32 KB)
+  static constexpr uint32_t DO = 32768;         // dO, 2 slabs (16 KB)
+  static constexpr uint32_t W = 49152;          // W (16 KB); later Vn~ = diag(e^{gC-gamma}) Vn
+  static constexpr uint32_t DVN = 65536;        // dVn (16 KB)
+  static constexpr uint32_t DH = 81920;         // dh' bf16, rows dk, 2 slabs of 16 KB (32 KB)
+  static constexpr uint32_t H = 114688;         // h bf16, rows dk, 2 slabs of 16 KB (32 KB); later dP
+  static constexpr uint32_t VN = 147456;        // Vn (16 KB)
+  static constexpr uint32_t OH = 163840;        // scale diag(e^gamma) dO (16 KB)
+  static constexpr uint32_t SCR = 180224;       // fp32 [64][65]
+  static constexpr uint32_t GAM = SCR + 16640;  // gamma (256 B)
+  static constexpr uint32_t BYTES = GAM + 256;
+};
+
+template <bool kGroup>
+__global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_w,
+    const __grid_constant__ CUtensorMap tm_dvn, const __grid_constant__ CUtensorMap tm_dh, Dims d,
+    const float* __restrict__ h_saved, bf16* __restrict__ dq, Workspace ws) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = align1024(smem_raw);
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tmem_slot;
+  __shared__ float s_rowpp[64], s_colpp[64], s_qh[64], s_kdv[64], s_red[4];
+  const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
+  const int tid = threadIdx.x, warp = tid >> 5, r = tid & 63;
+  const int4 ci = ws.chunks[c];
+  const int len = ci.z, t0 = ci.y;
+  if (len <= 0) return;
+  const int Hv = d.Hv;
+  const size_t ch = (size_t)c * Hv + j;
+
+  if (tid == 0) {
+    tc::mbar_init(&bar_tma, 1);
+    tc::mbar_init(&bar_mma, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tb = tmem_slot;
+  if (tid == 0) {
+    uint64_t* bar = &bar_tma;
+    tc::mbar_arrive_expect_tx(bar, 14 * kSlab + 256);
+    tc::bulk_load(sm + GradASmem::GAM, ws.gam + ch * 64, 256, bar);
+    tc::tma_load_3d(sm + GradASmem::KQ, &tm_k, bar, 0, i, t0);
+    tc::tma_load_3d(sm + GradASmem::KQ + 2 * kSlab, &tm_k, bar, 64, i, t0);
+    tc::tma_load_3d(sm + GradASmem::KQ + kSlab, &tm_q, bar, 0, i, t0);
+    tc::tma_load_3d(sm + GradASmem::KQ + 3 * kSlab, &tm_q, bar, 64, i, t0);
+    tc::tma_load_3d(sm + GradASmem::DO, &tm_do, bar, 0, j, t0);
+    tc::tma_load_3d(sm + GradASmem::DO + kSlab, &tm_do, bar, 64, j, t0);
+    tc::tma_load_2d(sm + GradASmem::W, &tm_w, bar, 0, (int)(ch * 64));
+    tc::tma_load_2d(sm + GradASmem::W + kSlab, &tm_w, bar, 64, (int)(ch * 64));
+    tc::tma_load_2d(sm + GradASmem::DVN, &tm_dvn, bar, 0, (int)(ch * 64));
+    tc::tma_load_2d(sm + GradASmem::DVN + kSlab, &tm_dvn, bar, 64, (int)(ch * 64));
+    for (int q4 = 0; q4 < 4; ++q4)  // dh' rows (q4 & 1) * 64.., columns (q4 >> 1) * 64..
+      tc::tma_load_2d(sm + GradASmem::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
+                      (int)(ch * 128 + (q4 & 1) * 64));
+  }
+  // h row `tid` (fp32) -> bf16 operand tile
+  const float* hrow = h_saved + ch * 128 * 128 + (size_t)tid * 128;
+  {
+    float hv[64];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int b = 0; b < 64; b += 4) {
+        const float4 f = *reinterpret_cast<const float4*>(hrow + half * 64 + b);
+        hv[b] = f.x; hv[b + 1] = f.y; hv[b + 2] = f.z; hv[b + 3] = f.w;
+      }
+      st_row_bf16(sm + GradASmem::H + half * 16384, tid, hv);
+    }
+  }
+  bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma, 0, ws.status, kDevErrTimeoutBwd));
+  const float* sgam = reinterpret_cast<const float*>(sm + GradASmem::GAM);
+  const float gC = sgam[len - 1], gr = sgam[r];
+  const float dec = __expf(gC - gr), eg = __expf(gr);
+  // <dh', h> over the whole state (fixed-order reduction)
+  float hdh = 0.f;
+  if (ok) {
+    float a[64];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      ld_row_bf16(sm + GradASmem::DH + half * 16384, tid, a);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) hdh += a[b] * hrow[half * 64 + b];
+    }
+  }
+  hdh = block_sum128(hdh, s_red);
+  if (ok && tid < 64) {  // O-hat = scale diag(e^gamma) dO, zero past the chunk end
+    float x[64];
+    const float e = r < len ? d.scale * eg : 0.f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      ld_row_bf16(sm + GradASmem::DO + half * kSlab, r, x);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) x[b] *= e;
+      st_row_bf16(sm + GradASmem::OH + half * kSlab, r, x);
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  // Ph2: [KK;QK] (cols 0-63), W h (64-191), O-hat h^T (192-319), dVn h^T (320-447)
+  if (ok && tid == 0) {
+    tc::tc_fence_after();
+    tc::gemm(tb, kmaj(sm + GradASmem::KQ, 2 * kSlab), kmaj(sm + GradASmem::KQ, 2 * kSlab), 64, 8, false);
+    tc::gemm(tb + 64, kmaj(sm + GradASmem::W, kSlab), mnmaj(sm + GradASmem::H, 16384), 128, 8, false);
+    tc::gemm(tb + 192, kmaj(sm + GradASmem::OH, kSlab), kmaj(sm + GradASmem::H, 16384), 128, 8, false);
+    tc::gemm(tb + 320, kmaj(sm + GradASmem::DVN, kSlab), kmaj(sm + GradASmem::H, 16384), 128, 8, false);
+    tc::mma_commit(&bar_mma);
+  }
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
+  tc::tc_fence_after();
+  float* scr = reinterpret_cast<float*>(sm + GradASmem::SCR);
+  if (ok) {
+    if (tid < 64) {
+      float x[64], u[64];
+      float qh = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld64(tb, warp, 64 + half * 64, x);  // (W h)[r]
+        ld_row_bf16_g((const bf16*)ws.U + (ch * 64 + r) * 128 + half * 64, u);
+#pragma unroll
+        for (int b = 0; b < 64; ++b) u[b] = r < len ? u[b] - x[b] : 0.f;
+        st_row_bf16(sm + GradASmem::VN + half * kSlab, r, u);
+#pragma unroll
+        for (int b = 0; b < 64; ++b) u[b] *= dec;
+        st_row_bf16(sm + GradASmem::W + half * kSlab, r, u);  // Vn~ (W no longer needed)
+        tmem_ld64(tb, warp, 192 + half * 64, x);            // (O-hat h^T)[r]
+        ld_row_bf16(sm + GradASmem::KQ + kSlab + half * 2 * kSlab, r, u);  // q_r
+#pragma unroll
+        for (int b = 0; b < 64; ++b) qh += x[b] * u[b];
+        tmem_ld64(tb, warp, 320 + half * 64, x);  // (dVn h^T)[r] = -dW[r]
+#pragma unroll
+        for (int b = 0; b < 64; ++b) x[b] = -x[b];
+        st_global_bf16x64((bf16*)ws.dWb + (ch * 64 + r) * 128 + half * 64, x);
+      }
+      s_qh[r] = qh;
+    } else {  // Q K^T rows -> scratch (fp32)
+      float x[64];
+      tmem_ld64(tb, warp, 0, x);
+#pragma unroll
+      for (int s = 0; s < 64; ++s) scr[r * 65 + s] = x[s];
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  // Ph4: dO Vn^T (cols 0-63), K dh' (64-191), Vn~ dh'^T (320-447); dq stays in 192-319
+  if (ok && tid == 0) {
+    tc::tc_fence_after();
+    tc::gemm(tb, kmaj(sm + GradASmem::DO, kSlab), kmaj(sm + GradASmem::VN, kSlab), 64, 8, false);
+    tc::gemm(tb + 64, kmaj(sm + GradASmem::KQ, 2 * kSlab), mnmaj(sm + GradASmem::DH, 16384), 128, 8, false);
+    tc::gemm(tb + 320, kmaj(sm + GradASmem::W, kSlab), kmaj(sm + GradASmem::DH, 16384), 128, 8, false);
+    tc::mma_commit(&bar_mma);
+  }
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
+  tc::tc_fence_after();
+  if (ok && tid < 64) {
+    float x[64], v[64];
+    tmem_ld64(tb, warp, 0, x);  // (dO Vn^T)[r]
+    float rowpp = 0.f;
+#pragma unroll
+    for (int s = 0; s < 64; ++s) {
+      const float dp = (s <= r && r < len) ? d.scale * x[s] * __expf(gr - sgam[s]) : 0.f;
+      x[s] = dp;
+      const float pp = dp * scr[r * 65 + s];
+      scr[r * 65 + s] = pp;
+      rowpp += pp;
+    }
+    s_rowpp[r] = rowpp;
+    st_row_bf16(sm + GradASmem::H, r, x);  // dP (h no longer needed)
+    float kdv = 0.f;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      tmem_ld64(tb, warp, 64 + half * 64, x);  // (K dh')[r]
+      ld_row_bf16(sm + GradASmem::VN + half * kSlab, r, v);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) kdv += x[b] * v[b];
+    }
+    s_kdv[r] = r < len ? kdv : 0.f;
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  if (ok && tid < 64) {
+    float cs = 0.f;
+    for (int rr = 0; rr < 64; ++rr) cs += scr[rr * 65 + tid];
+    s_colpp[tid] = cs;
+  }
+  // Ph6: dq += dP K (cols 192-319), dk_A += dP^T Q (cols 320-447)
+  if (ok && tid == 0) {
+    tc::tc_fence_after();
+    tc::gemm(tb + 192, kmaj(sm + GradASmem::H, kSlab), mnmaj(sm + GradASmem::KQ, 2 * kSlab), 128, 4, true);
+    tc::gemm(tb + 320, mnmaj(sm + GradASmem::H, kSlab), mnmaj(sm + GradASmem::KQ + kSlab, 2 * kSlab), 128, 4, true);
+    tc::mma_commit(&bar_mma);
+  }
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
+  tc::tc_fence_after();
+  if (ok && tid < 64) {
+    float x[64];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      tmem_ld64(tb, warp, 192 + half * 64, x);
+      if (r < len) {
+        if (kGroup) {
+          float* dst = ws.dq_part + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64;
+#pragma unroll
+          for (int b = 0; b < 64; b += 4) *reinterpret_cast<float4*>(dst + b) = make_float4(x[b], x[b + 1], x[b + 2], x[b + 3]);
+        } else {
+          st_global_bf16x64(dq + ((size_t)(t0 + r) * d.Hk + i) * 128 + half * 64, x);
+        }
+      }
+      tmem_ld64(tb, warp, 320 + half * 64, x);
+      st_global_bf16x64((bf16*)ws.dKA + (ch * 64 + r) * 128 + half * 64, x);
+    }
+    float dga = 0.f;
+    if (r < len) {
+      dga = s_rowpp[r] - s_colpp[r] + s_qh[r] - dec * s_kdv[r];
+      if (r == len - 1) {
+        float sk = 0.f;
+        for (int s = 0; s < len; ++s) sk += __expf(gC - sgam[s]) * s_kdv[s];
+        dga += __expf(gC) * hdh + sk;
+      }
+    }
+    ws.dgamA[ch * 64 + r] = dga;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tb, 512);
+}
+
+// ---------------------------------------------------------------------------------
+// gradB
+// ---------------------------------------------------------------------------------
+struct GradBSmem {
+  static constexpr uint32_t K = 0;         // K, 2 slabs (16 KB)
+  static constexpr uint32_t V = 16384;     // V, 2 slabs (16 KB)
+  static constexpr uint32_t T = 32768;     // T bf16 [64][64] (8 KB)
+  static constexpr uint32_t TP = 40960;    // T' = T diag(beta e^gamma) (8 KB)
+  static constexpr uint32_t DW = 49152;    // dW, 2 slabs (16 KB)
+  static constexpr uint32_t DVN = 65536;   // dVn, 2 slabs (16 KB)
+  static constexpr uint32_t DT = 81920;    // dT (8 KB)
+  static constexpr uint32_t X = 90112;     // T^T dT (8 KB)
+  static constexpr uint32_t DAG = 98304;   // diag(beta) (dA * Gam) (8 KB)
+  static constexpr uint32_t SCR = 106496;  // fp32 [64][65]
+  static constexpr uint32_t GAM = SCR + 16640;
+  static constexpr uint32_t BYTES = GAM + 256;
+};
+
+template <bool kGroup>
+__global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_dw,
+    const __grid_constant__ CUtensorMap tm_dvn, Dims d, const bf16* __restrict__ beta, bf16* __restrict__ dk,
+    bf16* __restrict__ dv, float* __restrict__ dg, bf16* __restrict__ dbeta, Workspace ws) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = align1024(smem_raw);
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tmem_slot;
+  __shared__ float s_beta[64], s_dgam[64], s_colaa[64];
+  const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
+  const int tid = threadIdx.x, warp = tid >> 5, r = tid & 63;
+  const int4 ci = ws.chunks[c];
+  const int len = ci.z, t0 = ci.y;
+  if (len <= 0) return;
+  const int Hv = d.Hv;
+  const size_t ch = (size_t)c * Hv + j;
+
+  if (tid == 0) {
+    tc::mbar_init(&bar_tma, 1);
+    tc::mbar_init(&bar_mma, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tb = tmem_slot;
+  if (tid == 0) {
+    uint64_t* bar = &bar_tma;
+    tc::mbar_arrive_expect_tx(bar, 9 * kSlab + 256);
+    tc::bulk_load(sm + GradBSmem::GAM, ws.gam + ch * 64, 256, bar);
+    tc::tma_load_3d(sm + GradBSmem::K, &tm_k, bar, 0, i, t0);
+    tc::tma_load_3d(sm + GradBSmem::K + kSlab, &tm_k, bar, 64, i, t0);
+    tc::tma_load_3d(sm + GradBSmem::V, &tm_v, bar, 0, j, t0);
+    tc::tma_load_3d(sm + GradBSmem::V + kSlab, &tm_v, bar, 64, j, t0);
+    tc::tma_load_2d(sm + GradBSmem::T, &tm_t, bar, 0, (int)(ch * 64));
+    tc::tma_load_2d(sm + GradBSmem::DW, &tm_dw, bar, 0, (int)(ch * 64));
+    tc::tma_load_2d(sm + GradBSmem::DW + kSlab, &tm_dw, bar, 64, (int)(ch * 64));
+    tc::tma_load_2d(sm + GradBSmem::DVN, &tm_dvn, bar, 0, (int)(ch * 64));
+    tc::tma_load_2d(sm + GradBSmem::DVN + kSlab, &tm_dvn, bar, 64, (int)(ch * 64));
+  }
+  if (tid < 64) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * Hv + j]) : 0.f;
+  bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma, 0, ws.status, kDevErrTimeoutBwd));
+  const float* sgam = reinterpret_cast<const float*>(sm + GradBSmem::GAM);
+  const float gr = sgam[r], eg = __expf(gr), br = s_beta[r];
+  if (ok && tid < 64) {  // T' row r = T[r][:] * beta e^gamma (per column)
+    float x[64];
+    ld_row_bf16(sm + GradBSmem::T, r, x);
+#pragma unroll
+    for (int s = 0; s < 64; ++s) x[s] *= s_beta[s] * __expf(sgam[s]);
+    st_row_bf16(sm + GradBSmem::TP, r, x);
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  // R1: K K^T (0-63), dW K^T (64-127), dVn V^T (128-191), T^T dW (192-319), T^T dVn (320-447)
+  if (ok && tid == 0) {
+    tc::tc_fence_after();
+    tc::gemm(tb, kmaj(sm + GradBSmem::K, kSlab), kmaj(sm + GradBSmem::K, kSlab), 64, 8, false);
+    tc::gemm(tb + 64, kmaj(sm + GradBSmem::DW, kSlab), kmaj(sm + GradBSmem::K, kSlab), 64, 8, false);
+    tc::gemm(tb + 128, kmaj(sm + GradBSmem::DVN, kSlab), kmaj(sm + GradBSmem::V, kSlab), 64, 8, false);
+    tc::gemm(tb + 192, mnmaj(sm + GradBSmem::T, kSlab), mnmaj(sm + GradBSmem::DW, kSlab), 128, 4, false);
+    tc::gemm(tb + 320, mnmaj(sm + GradBSmem::T, kSlab), mnmaj(sm + GradBSmem::DVN, kSlab), 128, 4, false);
+    tc::mma_commit(&bar_mma);
+  }
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
+  tc::tc_fence_after();
+  float* scr = reinterpret_cast<float*>(sm + GradBSmem::SCR);
+  float dbk = 0.f, dbv = 0.f;
+  if (ok && tid < 64) {
+    float x[64], y[64];
+    tmem_ld64(tb, warp, 0, x);  // K K^T row r
+#pragma unroll
+    for (int s = 0; s < 64; ++s) scr[r * 65 + s] = x[s];
+    tmem_ld64(tb, warp, 64, x);   // (dW K^T)[r]
+    tmem_ld64(tb, warp, 128, y);  // (dVn V^T)[r]
+#pragma unroll
+    for (int s = 0; s < 64; ++s)
+      x[s] = (r < len && s < len) ? s_beta[s] * (__expf(sgam[s]) * x[s] + y[s]) : 0.f;
+    st_row_bf16(sm + GradBSmem::DT, r, x);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      tmem_ld64(tb, warp, 192 + half * 64, x);  // dB_k[r]
+      ld_row_bf16(sm + GradBSmem::K + half * kSlab, r, y);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) dbk += x[b] * y[b];
+      tmem_ld64(tb, warp, 320 + half * 64, x);  // dB_v[r]
+      ld_row_bf16(sm + GradBSmem::V + half * kSlab, r, y);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) {
+        dbv += x[b] * y[b];
+        x[b] *= br;
+      }
+      if (r < len) st_global_bf16x64(dv + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64, x);
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  // R2: X = T^T dT (cols 448-511)
+  if (ok && tid == 0) {
+    tc::tc_fence_after();
+    tc::gemm(tb + 448, mnmaj(sm + GradBSmem::T, kSlab), mnmaj(sm + GradBSmem::DT, kSlab), 64, 4, false);
+    tc::mma_commit(&bar_mma);
+  }
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
+  tc::tc_fence_after();
+  if (ok && tid < 64) {
+    float x[64];
+    tmem_ld64(tb, warp, 448, x);
+    st_row_bf16(sm + GradBSmem::X, r, x);
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  // R3: X T^T (cols 0-63)
+  if (ok && tid == 0) {
+    tc::tc_fence_after();
+    tc::gemm(tb, kmaj(sm + GradBSmem::X, kSlab), kmaj(sm + GradBSmem::T, kSlab), 64, 4, false);
+    tc::mma_commit(&bar_mma);
+  }
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
+  tc::tc_fence_after();
+  float akk = 0.f, rowaa = 0.f;
+  if (ok && tid < 64) {
+    float x[64];
+    tmem_ld64(tb, warp, 0, x);
+#pragma unroll
+    for (int s = 0; s < 64; ++s) {
+      const float da = (s < r && r < len) ? -x[s] : 0.f;
+      const float dag = da * __expf(gr - sgam[s]);
+      const float kk = scr[r * 65 + s];
+      akk += dag * kk;
+      x[s] = br * dag;
+      const float aa = x[s] * kk;  // dA * A with A = beta_r Gam K K^T
+      rowaa += aa;
+      scr[r * 65 + s] = aa;
+    }
+    st_row_bf16(sm + GradBSmem::DAG, r, x);
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  if (ok && tid < 64) {
+    float cs = 0.f;
+    for (int rr = 0; rr < 64; ++rr) cs += scr[rr * 65 + tid];
+    s_colaa[tid] = cs;
+  }
+  // R4: dk_B = T'^T dW + dAGb K + dAGb^T K (cols 64-191)
+  if (ok && tid == 0) {
+    tc::tc_fence_after();
+    tc::gemm(tb + 64, mnmaj(sm + GradBSmem::TP, kSlab), mnmaj(sm + GradBSmem::DW, kSlab), 128, 4, false);
+    tc::gemm(tb + 64, kmaj(sm + GradBSmem::DAG, kSlab), mnmaj(sm + GradBSmem::K, kSlab), 128, 4, true);
+    tc::gemm(tb + 64, mnmaj(sm + GradBSmem::DAG, kSlab), mnmaj(sm + GradBSmem::K, kSlab), 128, 4, true);
+    tc::mma_commit(&bar_mma);
+  }
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
+  tc::tc_fence_after();
+  if (ok && tid < 64) {
+    float x[64], y[64];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      tmem_ld64(tb, warp, 64 + half * 64, x);
+      ld_row_bf16_g((const bf16*)ws.dKA + (ch * 64 + r) * 128 + half * 64, y);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) x[b] += y[b];
+      if (r < len) {
+        if (kGroup) {
+          float* dst = ws.dk_part + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64;
+#pragma unroll
+          for (int b = 0; b < 64; b += 4) *reinterpret_cast<float4*>(dst + b) = make_float4(x[b], x[b + 1], x[b + 2], x[b + 3]);
+        } else {
+          st_global_bf16x64(dk + ((size_t)(t0 + r) * d.Hk + i) * 128 + half * 64, x);
+        }
+      }
+    }
+    if (r < len) dbeta[(size_t)(t0 + r) * Hv + j] = __float2bfloat16_rn(eg * dbk + dbv + akk);
+    s_dgam[r] = r < len ? ws.dgamA[ch * 64 + r] + br * eg * dbk + rowaa - s_colaa[r] : 0.f;
+  }
+  __syncthreads();
+  if (ok && tid == 0) {  // dg = in-chunk reverse cumsum of d gamma
+    float run = 0.f;
+    for (int rr = len - 1; rr >= 0; --rr) {
+      run += s_dgam[rr];
+      dg[(size_t)(t0 + rr) * Hv + j] = run;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tb, 512);
+}
+
+}  // namespace
+
+bool tc_bwd_available() { return get_encoder(); }
+
+cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cudaStream_t s) {
+  if (!get_encoder()) return cudaErrorNotSupported;
+  const uint64_t Tt = (uint64_t)d.T_total;
+  const uint64_t rows = (uint64_t)d.max_chunks * d.Hv * 64;
+  if (Tt == 0 && d.num_seqs == 0) return cudaSuccess;
+  cudaError_t e = tc_launch_prep(d, a.q, a.k, a.v, a.g, a.beta, ws, 1, s, "bwd_prep");
+  if (e != cudaSuccess) return e;
+  const uint64_t Tmap = Tt > 0 ? Tt : 1;
+  const uint64_t rmap = rows > 0 ? rows : 64;
+  CUtensorMap tq, tk, tv, tdo, tw, tp, tdvn, tdh, tt, tdw;
+  if (!map_3d(&tq, a.q, 128, d.Hk, Tmap) || !map_3d(&tk, a.k, 128, d.Hk, Tmap) ||
+      !map_3d(&tv, a.v, 128, d.Hv, Tmap) || !map_3d(&tdo, a.dO, 128, d.Hv, Tmap) ||
+      !map_2d(&tw, ws.W, 128, rmap) || !map_2d(&tp, ws.P, 64, rmap) || !map_2d(&tdvn, ws.dVn, 128, rmap) ||
+      !map_2d(&tdh, ws.dhp, 128, rmap * 2) || !map_2d(&tt, ws.Tb, 64, rmap) || !map_2d(&tdw, ws.dWb, 128, rmap))
+    return cudaErrorInvalidValue;
+  if (d.num_seqs > 0) {
+    const size_t sm = WalkSmem::BYTES + 1024;
+    cudaFuncSetAttribute(tc_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    tc_bwd_walk_kernel<<<dim3(d.num_seqs, d.Hv, 2), kTcThreads, sm, s>>>(tq, tk, tw, tp, tdo, d, a.dS_T, a.dS0,
+                                                                        ws);
+    stage_mark(s, "bwd_walk");
+  }
+  if (d.max_chunks > 0 && Tt > 0) {
+    const dim3 grid(d.max_chunks, d.Hv);
+    const size_t sma = GradASmem::BYTES + 1024, smb = GradBSmem::BYTES + 1024;
+    if (d.G > 1) {
+      cudaFuncSetAttribute(tc_bwd_gradA_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sma);
+      tc_bwd_gradA_kernel<true><<<grid, kTcThreads, sma, s>>>(tq, tk, tdo, tw, tdvn, tdh, d, a.h_saved,
+                                                               (bf16*)a.dq, ws);
+    } else {
+      cudaFuncSetAttribute(tc_bwd_gradA_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sma);
+      tc_bwd_gradA_kernel<false><<<grid, kTcThreads, sma, s>>>(tq, tk, tdo, tw, tdvn, tdh, d, a.h_saved,
+                                                                (bf16*)a.dq, ws);
+    }
+    stage_mark(s, "bwd_gradA");
+    if (d.G > 1) {
+      cudaFuncSetAttribute(tc_bwd_gradB_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smb);
+      tc_bwd_gradB_kernel<true><<<grid, kTcThreads, smb, s>>>(tk, tv, tt, tdw, tdvn, d, (const bf16*)a.beta,
+                                                               (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
+    } else {
+      cudaFuncSetAttribute(tc_bwd_gradB_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smb);
+      tc_bwd_gradB_kernel<false><<<grid, kTcThreads, smb, s>>>(tk, tv, tt, tdw, tdvn, d, (const bf16*)a.beta,
+                                                                (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
+    }
+    stage_mark(s, "bwd_gradB");
+    if (d.G > 1) {
+      e = launch_group_reduce(d, a.dq, a.dk, ws, s);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gdr

@@ -105,6 +105,14 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Plain bulk copy global -> shared (16-byte aligned addresses, size multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // ------------------------------------------------------------------ TMEM
 // Allocation is warp-wide (one warp calls it); writes the TMEM base address to *slot.
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
@@ -200,6 +208,28 @@ __device__ __forceinline__ uint64_t kmajor_step_desc(uint32_t tile_saddr, uint32
 
 __device__ __forceinline__ uint64_t mnmajor_step_desc(uint32_t tile_saddr, uint32_t slab_bytes, int kk) {
   return sdesc_sw128(tile_saddr + (uint32_t)kk * 2048u, slab_bytes, 1024u);
+}
+
+// A shared-memory operand of a GEMM: base address, its slab stride (K-major) or its
+// M/N atom stride (MN-major), and which of the two it is.
+struct Opnd {
+  uint32_t base;
+  uint32_t stride;
+  int mn;
+};
+
+__device__ __forceinline__ Opnd kmaj(const void* p, uint32_t slab) { return Opnd{smem_u32(p), slab, 0}; }
+__device__ __forceinline__ Opnd mnmaj(const void* p, uint32_t lbo) { return Opnd{smem_u32(p), lbo, 1}; }
+
+__device__ __forceinline__ uint64_t step_desc(const Opnd& o, int kk) {
+  return o.mn ? mnmajor_step_desc(o.base, o.stride, kk) : kmajor_step_desc(o.base, o.stride, kk);
+}
+
+// D (+)= A * B with M = 128, K = 16 * ksteps.  Issued by one thread.
+__device__ __forceinline__ void gemm(uint32_t d_tmem, const Opnd& a, const Opnd& b, int N, int ksteps,
+                                     bool accumulate) {
+  const uint32_t id = idesc_bf16(128, N, a.mn, b.mn);
+  for (int kk = 0; kk < ksteps; ++kk) mma_bf16(d_tmem, step_desc(a, kk), step_desc(b, kk), id, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 }  // namespace tc
