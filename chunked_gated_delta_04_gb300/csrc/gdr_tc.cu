@@ -67,6 +67,19 @@ bool map_3d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t heads, uin
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D map over a [rows][cols] matrix of `dt` (element size esz) with a box of
+// box_cols x box_rows, 128-byte swizzle (box_cols * esz must be 128).
+bool map_2d_box(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32_t esz, uint64_t cols,
+                uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * esz};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2D map over a [rows][cols] bf16 matrix, box = 64 columns x 64 rows.
 bool map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
   cuuint64_t dims[2] = {cols, rows};
@@ -88,12 +101,16 @@ struct PrepSmem {
   static constexpr uint32_t V = 32768;           // 2 slabs: 16 KB
   static constexpr uint32_t TT = V + 16384;      // [T' | T''] bf16: 16 KB
   static constexpr uint32_t A = TT + 16384;      // fp32 [64][64]: 16 KB
-  static constexpr uint32_t BYTES = A + 16384;   // 80 KB
+  static constexpr uint32_t PS = A + 16384;      // P staged for its TMA store: 8 KB
+  static constexpr uint32_t BYTES = PS + 8192;   // 88 KB (two CTAs per SM)
 };
 
 __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                              const __grid_constant__ CUtensorMap tm_k,
-                                                             const __grid_constant__ CUtensorMap tm_v, Dims d,
+                                                             const __grid_constant__ CUtensorMap tm_v,
+                                                             const __grid_constant__ CUtensorMap tm_w,
+                                                             const __grid_constant__ CUtensorMap tm_u,
+                                                             const __grid_constant__ CUtensorMap tm_p, Dims d,
                                                              const float* __restrict__ g,
                                                              const bf16* __restrict__ beta, Workspace ws,
                                                              int write_T) {
@@ -169,10 +186,15 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
     } else {  // P row r
 #pragma unroll
       for (int s = 0; s < 64; ++s) row[s] = (s <= r && r < len) ? row[s] * __expf(gr - s_gam[s]) : 0.f;
-      st_global_bf16x64((bf16*)ws.P + (ch * 64 + r) * 64, row);
+      st_row_bf16(sm + PrepSmem::PS, r, row);
     }
   }
+  tc::fence_proxy_async_smem();
   __syncthreads();
+  if (ok && tid == 0) {
+    tc::tma_store_2d(&tm_p, sm + PrepSmem::PS, 0, (int)(ch * 64));
+    tc::bulk_commit();
+  }
   // T = (I + A)^{-1}: thread s < 64 owns column s of T in registers
   if (ok && tid < 64) {
     const int s = tid;
@@ -219,19 +241,28 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutPrep));
   tc::tc_fence_after();
-  if (ok) {
+  if (ok) {  // W rows (threads 0-63) and U rows (threads 64-127) staged in the free K/Q tiles
     const int r = tid & 63;
-    bf16* dst = (tid < 64 ? (bf16*)ws.W : (bf16*)ws.U) + (ch * 64 + r) * 128;
     const int col = tid < 64 ? 0 : 128;
+    unsigned char* stg = sm + PrepSmem::KQ + (tid < 64 ? 0 : 2 * kSlab);
     float v[64];
     tmem_ld64(tbase, warp, col, v);
-    st_global_bf16x64(dst, v);
+    st_row_bf16(stg, r, v);
     tmem_ld64(tbase, warp, col + 64, v);
-    st_global_bf16x64(dst + 64, v);
+    st_row_bf16(stg + kSlab, r, v);
     if (tid < 64) ws.gam[ch * 64 + tid] = s_gam[tid];
   }
+  tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
+  if (ok && tid == 0) {
+    tc::tma_store_2d(&tm_w, sm + PrepSmem::KQ, 0, (int)(ch * 64));
+    tc::tma_store_2d(&tm_w, sm + PrepSmem::KQ + kSlab, 64, (int)(ch * 64));
+    tc::tma_store_2d(&tm_u, sm + PrepSmem::KQ + 2 * kSlab, 0, (int)(ch * 64));
+    tc::tma_store_2d(&tm_u, sm + PrepSmem::KQ + 3 * kSlab, 64, (int)(ch * 64));
+    tc::bulk_commit();
+  }
+  if (tid == 0) tc::bulk_wait_all();
   if (warp == 0) tc::tmem_dealloc(tbase, 256);
 }
 
@@ -245,15 +276,18 @@ struct StateSmem {
   static constexpr uint32_t H = 2 * STAGE;        // h as bf16 B operand: 128 rows x 128 B = 16 KB
   static constexpr uint32_t VN = H + 16384;       // Vn (8 KB)
   static constexpr uint32_t VT = VN + 8192;       // Vn scaled by e^{gamma_C - gamma} (8 KB)
-  static constexpr uint32_t GAM = VT + 8192;      // gamma of each stage: 2 x 256 B
+  static constexpr uint32_t HS = VT + 8192;       // h (fp32) staged for the TMA store: 2 x 16 KB
+  static constexpr uint32_t OS = HS + 32768;      // o rows (bf16) staged for the TMA store (8 KB)
+  static constexpr uint32_t GAM = OS + 8192;      // gamma of each stage: 2 x 256 B
   static constexpr uint32_t BYTES = GAM + 512;
 };
 
 __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
-    const __grid_constant__ CUtensorMap tm_p, Dims d, const float* __restrict__ S0, float* __restrict__ S_T,
-    float* __restrict__ h_saved, bf16* __restrict__ o, Workspace ws) {
+    const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_hs,
+    const __grid_constant__ CUtensorMap tm_o, Dims d, const float* __restrict__ S0, float* __restrict__ S_T,
+    bf16* __restrict__ o, Workspace ws) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint64_t bar_load[2], bar_mma;
@@ -315,17 +349,19 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     const int len = min(64, L - it * 64);
     const size_t chh = (size_t)c * Hv + j;
     if (tid == 0 && c + 1 < c_end) issue_loads(c + 1, st ^ 1);
-    // save the chunk-start state and stage h as the bf16 B operand
-    {
-      float* hs = h_saved + chh * 128 * 128 + (size_t)tid * 128 + dv0;
-#pragma unroll
-      for (int b = 0; b < 64; b += 4) *reinterpret_cast<float4*>(hs + b) = make_float4(h[b], h[b + 1], h[b + 2], h[b + 3]);
-      st_row_bf16(sm + StateSmem::H, tid, h);
-    }
+    // stage the chunk-start state (fp32, for h_saved) and h as the bf16 B operand
+    st_row_f32x32(sm + StateSmem::HS, tid, h);
+    st_row_f32x32(sm + StateSmem::HS + 16384, tid, h + 32);
+    st_row_bf16(sm + StateSmem::H, tid, h);
     const int r = tid & 63;
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
+    if (tid == 0) {  // h_saved[chunk] rows 0..127, columns dv0..dv0+63
+      tc::tma_store_2d(&tm_hs, sm + StateSmem::HS, dv0, (int)(chh * 128));
+      tc::tma_store_2d(&tm_hs, sm + StateSmem::HS + 16384, dv0 + 32, (int)(chh * 128));
+      tc::bulk_commit();
+    }
     ok = __syncthreads_and(tc::mbar_wait(&bar_load[st], ld_phase, ws.status, kDevErrTimeoutFwd));
     const float* sgam = reinterpret_cast<const float*>(sm + StateSmem::GAM + st * 256);
     const float gC = sgam[len - 1];
@@ -375,6 +411,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
       }
       tc::mma_commit(&bar_mma);
     }
+    if (tid == 0) tc::bulk_wait_read<1>();  // the previous chunk's o store has left the staging tile
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutFwd));
     mma_phase ^= 1;
     tc::tc_fence_after();
@@ -386,7 +423,10 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
           const float eg = __expf(gr);
 #pragma unroll
           for (int b = 0; b < 64; ++b) y[b] = d.scale * (eg * x[b] + y[b]);
-          st_global_bf16x64(o + ((size_t)(t0 + r) * Hv + j) * 128 + dv0, y);
+          if (len == 64)
+            st_row_bf16(sm + StateSmem::OS, r, y);  // full chunk: one TMA store below
+          else
+            st_global_bf16x64(o + ((size_t)(t0 + r) * Hv + j) * 128 + dv0, y);
         }
       }
       tmem_ld64(tbase, warp, 128, y);
@@ -394,9 +434,16 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
 #pragma unroll
       for (int b = 0; b < 64; ++b) h[b] = eC * h[b] + y[b];
     }
+    if (tid == 0) tc::bulk_wait_read<0>();  // h staging free for the next chunk
+    tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
+    if (ok && tid == 0 && len == 64) {
+      tc::tma_store_3d(&tm_o, sm + StateSmem::OS, dv0, j, t0);
+      tc::bulk_commit();
+    }
   }
+  if (tid == 0) tc::bulk_wait_all();
   if (ok && S_T) {
     const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
 #pragma unroll
@@ -414,28 +461,31 @@ bool tc_available() { return get_encoder(); }
 
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s) {
   if (!get_encoder()) return cudaErrorNotSupported;
-  CUtensorMap tq, tk, tv, tw, tu, tp;
+  // Maps are built only when there are tokens; with none, no kernel reads them (every
+  // chunk slot is empty and the state kernel only copies S0 to S_T).
+  CUtensorMap tq{}, tk{}, tv{}, tw{}, tu{}, tp{}, ths{}, tov{};
   const uint64_t Tt = (uint64_t)d.T_total;
   const uint64_t rows = (uint64_t)d.max_chunks * d.Hv * 64;
   if (Tt == 0 && d.num_seqs == 0) return cudaSuccess;
-  const uint64_t Tmap = Tt > 0 ? Tt : 1;
-  if (!map_3d(&tq, a.q, 128, d.Hk, Tmap) || !map_3d(&tk, a.k, 128, d.Hk, Tmap) ||
-      !map_3d(&tv, a.v, 128, d.Hv, Tmap))
-    return cudaErrorInvalidValue;
-  if (rows > 0 && (!map_2d(&tw, ws.W, 128, rows) || !map_2d(&tu, ws.U, 128, rows) || !map_2d(&tp, ws.P, 64, rows)))
-    return cudaErrorInvalidValue;
+  if (Tt > 0) {
+    if (!map_3d(&tq, a.q, 128, d.Hk, Tt) || !map_3d(&tk, a.k, 128, d.Hk, Tt) || !map_3d(&tv, a.v, 128, d.Hv, Tt) ||
+        !map_3d(&tov, a.o, 128, d.Hv, Tt) || !map_2d(&tw, ws.W, 128, rows) || !map_2d(&tu, ws.U, 128, rows) ||
+        !map_2d(&tp, ws.P, 64, rows) ||
+        !map_2d_box(&ths, a.h_saved, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, rows * 2, 32, 128))
+      return cudaErrorInvalidValue;
+  }
   if (d.max_chunks > 0 && Tt > 0) {
     const size_t smp = PrepSmem::BYTES + 1024;
     cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
-    tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, d, a.g, (const bf16*)a.beta, ws,
-                                                                      0);
+    tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, d, a.g,
+                                                                      (const bf16*)a.beta, ws, 0);
     stage_mark(s, "fwd_prep");
   }
   if (d.num_seqs > 0) {
     const size_t sms = StateSmem::BYTES + 1024;
     cudaFuncSetAttribute(tc_fwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
-    tc_fwd_state_kernel<<<dim3(d.num_seqs, d.Hv, 2), kTcThreads, sms, s>>>(tq, tk, tw, tu, tp, d, a.S0, a.S_T,
-                                                                         a.h_saved, (bf16*)a.o, ws);
+    tc_fwd_state_kernel<<<dim3(d.num_seqs, d.Hv, 2), kTcThreads, sms, s>>>(tq, tk, tw, tu, tp, ths, tov, d, a.S0,
+                                                                         a.S_T, (bf16*)a.o, ws);
     stage_mark(s, "fwd_state");
   }
   return cudaGetLastError();
@@ -444,14 +494,16 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
 cudaError_t tc_launch_prep(const Dims& d, const void* q, const void* k, const void* v, const float* g,
                            const void* beta, const Workspace& ws, int write_T, cudaStream_t s, const char* stage) {
   if (d.max_chunks == 0 || d.T_total == 0) return cudaSuccess;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, tw, tu, tp;
   const uint64_t Tt = (uint64_t)d.T_total;
-  if (!map_3d(&tq, q, 128, d.Hk, Tt) || !map_3d(&tk, k, 128, d.Hk, Tt) || !map_3d(&tv, v, 128, d.Hv, Tt))
+  const uint64_t rows = (uint64_t)d.max_chunks * d.Hv * 64;
+  if (!map_3d(&tq, q, 128, d.Hk, Tt) || !map_3d(&tk, k, 128, d.Hk, Tt) || !map_3d(&tv, v, 128, d.Hv, Tt) ||
+      !map_2d(&tw, ws.W, 128, rows) || !map_2d(&tu, ws.U, 128, rows) || !map_2d(&tp, ws.P, 64, rows))
     return cudaErrorInvalidValue;
   const size_t smp = PrepSmem::BYTES + 1024;
   cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
-  tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, d, g, (const bf16*)beta, ws,
-                                                                    write_T);
+  tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, d, g, (const bf16*)beta,
+                                                                    ws, write_T);
   stage_mark(s, stage);
   return cudaGetLastError();
 }

@@ -70,7 +70,8 @@ struct WalkSmem {
 __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
-    const __grid_constant__ CUtensorMap tm_do, Dims d, const float* __restrict__ dS_T, float* __restrict__ dS0,
+    const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dhs,
+    const __grid_constant__ CUtensorMap tm_dvs, Dims d, const float* __restrict__ dS_T, float* __restrict__ dS0,
     Workspace ws) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
@@ -132,11 +133,14 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
     (void)t0;
     const size_t chh = (size_t)c * Hv + j;
     if (tid == 0 && c - 1 >= c_begin) issue_loads(c - 1, st ^ 1);
-    st_global_bf16x64((bf16*)ws.dhp + (chh * 128 + tid) * 128 + dv0, dh);
     st_row_bf16(sm + WalkSmem::DH, tid, dh);
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
+    if (tid == 0) {  // dh' of this chunk -> workspace, straight from the operand tile
+      tc::tma_store_2d(&tm_dhs, sm + WalkSmem::DH, dv0, (int)(chh * 128));
+      tc::bulk_commit();
+    }
     ok = __syncthreads_and(tc::mbar_wait(&bar_load[st], ld_phase, ws.status, kDevErrTimeoutBwd));
     unsigned char* stg = sm + st * WalkSmem::STAGE;
     const float* sgam = reinterpret_cast<const float*>(stg + WalkSmem::GAM);
@@ -160,6 +164,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
                false);  // Q^T diag(e^gamma) dO
       tc::mma_commit(&bar_mma);
     }
+    if (tid == 0) tc::bulk_wait_read<1>();  // the previous chunk's dVn store has left its tile
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutBwd));
     mma_phase ^= 1;
     tc::tc_fence_after();
@@ -171,12 +176,13 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
 #pragma unroll
       for (int b = 0; b < 64; ++b) y[b] = r < len ? d.scale * y[b] + dec * x[b] : 0.f;
       st_row_bf16(sm + WalkSmem::DVN, r, y);
-      st_global_bf16x64((bf16*)ws.dVn + (chh * 64 + r) * 128 + dv0, y);
     }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     if (ok && tid == 0) {
+      tc::tma_store_2d(&tm_dvs, sm + WalkSmem::DVN, dv0, (int)(chh * 64));
+      tc::bulk_commit();
       tc::tc_fence_after();
       tc::gemm(Dc, mnmaj(stg + WalkSmem::W, kSlab), mnmaj(sm + WalkSmem::DVN, kSlab), 64, 4, false);  // W^T dVn
       tc::mma_commit(&bar_mma);
@@ -192,9 +198,11 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
 #pragma unroll
       for (int b = 0; b < 64; ++b) dh[b] = eC * dh[b] + d.scale * y[b] - x[b];
     }
+    if (tid == 0) tc::bulk_wait_read<1>();  // this chunk's dh' store has left the operand tile
     tc::tc_fence_before();
     __syncthreads();
   }
+  if (tid == 0) tc::bulk_wait_all();
   if (ok && dS0) {
     const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
 #pragma unroll
@@ -218,17 +226,21 @@ struct GradASmem {
   static constexpr uint32_t H = 114688;         // h bf16, rows dk, 2 slabs of 16 KB (32 KB); later dP
   static constexpr uint32_t VN = 147456;        // Vn (16 KB)
   static constexpr uint32_t OH = 163840;        // scale diag(e^gamma) dO (16 KB)
-  static constexpr uint32_t SCR = 180224;       // fp32 [64][65]
+  static constexpr uint32_t UT = 180224;        // U (16 KB)
+  static constexpr uint32_t SCR = UT + 16384;   // fp32 [64][65]
   static constexpr uint32_t GAM = SCR + 16640;  // gamma (256 B)
   static constexpr uint32_t BYTES = GAM + 256;
+  // stores are staged in tiles that are free by then: dW -> DVN, dk_A -> VN, dq -> OH
 };
 
 template <bool kGroup>
 __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_w,
-    const __grid_constant__ CUtensorMap tm_dvn, const __grid_constant__ CUtensorMap tm_dh, Dims d,
-    const float* __restrict__ h_saved, bf16* __restrict__ dq, Workspace ws) {
+    const __grid_constant__ CUtensorMap tm_dvn, const __grid_constant__ CUtensorMap tm_dh,
+    const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dwb,
+    const __grid_constant__ CUtensorMap tm_dka, const __grid_constant__ CUtensorMap tm_dq,
+    const __grid_constant__ CUtensorMap tm_h, Dims d, bf16* __restrict__ dq, Workspace ws) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint64_t bar_tma, bar_mma;
@@ -254,8 +266,14 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
   const uint32_t tb = tmem_slot;
   if (tid == 0) {
     uint64_t* bar = &bar_tma;
-    tc::mbar_arrive_expect_tx(bar, 14 * kSlab + 256);
+    tc::mbar_arrive_expect_tx(bar, 24 * kSlab + 256);
+    // h (fp32) as four 32-column slabs of 128 rows over the H, VN and OH tiles (64 KB),
+    // converted to the bf16 operand in place below
+    for (int q4 = 0; q4 < 4; ++q4)
+      tc::tma_load_2d(sm + GradASmem::H + q4 * 16384, &tm_h, bar, q4 * 32, (int)(ch * 128));
     tc::bulk_load(sm + GradASmem::GAM, ws.gam + ch * 64, 256, bar);
+    tc::tma_load_2d(sm + GradASmem::UT, &tm_u, bar, 0, (int)(ch * 64));
+    tc::tma_load_2d(sm + GradASmem::UT + kSlab, &tm_u, bar, 64, (int)(ch * 64));
     tc::tma_load_3d(sm + GradASmem::KQ, &tm_k, bar, 0, i, t0);
     tc::tma_load_3d(sm + GradASmem::KQ + 2 * kSlab, &tm_k, bar, 64, i, t0);
     tc::tma_load_3d(sm + GradASmem::KQ + kSlab, &tm_q, bar, 0, i, t0);
@@ -270,34 +288,34 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
       tc::tma_load_2d(sm + GradASmem::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
                       (int)(ch * 128 + (q4 & 1) * 64));
   }
-  // h row `tid` (fp32) -> bf16 operand tile
-  const float* hrow = h_saved + ch * 128 * 128 + (size_t)tid * 128;
-  {
-    float hv[64];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-      for (int b = 0; b < 64; b += 4) {
-        const float4 f = *reinterpret_cast<const float4*>(hrow + half * 64 + b);
-        hv[b] = f.x; hv[b + 1] = f.y; hv[b + 2] = f.z; hv[b + 3] = f.w;
-      }
-      st_row_bf16(sm + GradASmem::H + half * 16384, tid, hv);
-    }
-  }
   bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma, 0, ws.status, kDevErrTimeoutBwd));
   const float* sgam = reinterpret_cast<const float*>(sm + GradASmem::GAM);
   const float gC = sgam[len - 1], gr = sgam[r];
   const float dec = __expf(gC - gr), eg = __expf(gr);
-  // <dh', h> over the whole state (fixed-order reduction)
+  // h row `tid`: fp32 slabs (32 columns each) -> bf16 operand slabs (64 columns each).
+  // bf16 slab s overwrites fp32 slab s, so each half is read completely (and the
+  // barrier passed) before it is written.  <dh', h> is accumulated on the way.
   float hdh = 0.f;
-  if (ok) {
-    float a[64];
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      ld_row_bf16(sm + GradASmem::DH + half * 16384, tid, a);
+  for (int half = 0; half < 2; ++half) {
+    float hv[64], dv_[64];
+    if (ok) {
 #pragma unroll
-      for (int b = 0; b < 64; ++b) hdh += a[b] * hrow[half * 64 + b];
+      for (int q = 0; q < 2; ++q) {
+        const unsigned char* src = sm + GradASmem::H + (2 * half + q) * 16384 + tid * 128;
+#pragma unroll
+        for (int ch4 = 0; ch4 < 8; ++ch4) {
+          const float4 f = *reinterpret_cast<const float4*>(src + (((ch4 ^ (tid & 7)) & 7) << 4));
+          hv[q * 32 + 4 * ch4] = f.x; hv[q * 32 + 4 * ch4 + 1] = f.y;
+          hv[q * 32 + 4 * ch4 + 2] = f.z; hv[q * 32 + 4 * ch4 + 3] = f.w;
+        }
+      }
+      ld_row_bf16(sm + GradASmem::DH + half * 16384, tid, dv_);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) hdh += hv[b] * dv_[b];
     }
+    __syncthreads();
+    if (ok) st_row_bf16(sm + GradASmem::H + half * 16384, tid, hv);
   }
   hdh = block_sum128(hdh, s_red);
   if (ok && tid < 64) {  // O-hat = scale diag(e^gamma) dO, zero past the chunk end
@@ -333,7 +351,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         tmem_ld64(tb, warp, 64 + half * 64, x);  // (W h)[r]
-        ld_row_bf16_g((const bf16*)ws.U + (ch * 64 + r) * 128 + half * 64, u);
+        ld_row_bf16(sm + GradASmem::UT + half * kSlab, r, u);
 #pragma unroll
         for (int b = 0; b < 64; ++b) u[b] = r < len ? u[b] - x[b] : 0.f;
         st_row_bf16(sm + GradASmem::VN + half * kSlab, r, u);
@@ -347,7 +365,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
         tmem_ld64(tb, warp, 320 + half * 64, x);  // (dVn h^T)[r] = -dW[r]
 #pragma unroll
         for (int b = 0; b < 64; ++b) x[b] = -x[b];
-        st_global_bf16x64((bf16*)ws.dWb + (ch * 64 + r) * 128 + half * 64, x);
+        st_row_bf16(sm + GradASmem::DVN + half * kSlab, r, x);  // dVn tile is free after Ph2
       }
       s_qh[r] = qh;
     } else {  // Q K^T rows -> scratch (fp32)
@@ -362,6 +380,9 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
   __syncthreads();
   // Ph4: dO Vn^T (cols 0-63), K dh' (64-191), Vn~ dh'^T (320-447); dq stays in 192-319
   if (ok && tid == 0) {
+    tc::tma_store_2d(&tm_dwb, sm + GradASmem::DVN, 0, (int)(ch * 64));
+    tc::tma_store_2d(&tm_dwb, sm + GradASmem::DVN + kSlab, 64, (int)(ch * 64));
+    tc::bulk_commit();
     tc::tc_fence_after();
     tc::gemm(tb, kmaj(sm + GradASmem::DO, kSlab), kmaj(sm + GradASmem::VN, kSlab), 64, 8, false);
     tc::gemm(tb + 64, kmaj(sm + GradASmem::KQ, 2 * kSlab), mnmaj(sm + GradASmem::DH, 16384), 128, 8, false);
@@ -416,17 +437,19 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       tmem_ld64(tb, warp, 192 + half * 64, x);
-      if (r < len) {
-        if (kGroup) {
+      if (kGroup) {
+        if (r < len) {
           float* dst = ws.dq_part + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64;
 #pragma unroll
           for (int b = 0; b < 64; b += 4) *reinterpret_cast<float4*>(dst + b) = make_float4(x[b], x[b + 1], x[b + 2], x[b + 3]);
-        } else {
-          st_global_bf16x64(dq + ((size_t)(t0 + r) * d.Hk + i) * 128 + half * 64, x);
         }
+      } else if (len == 64) {
+        st_row_bf16(sm + GradASmem::OH + half * kSlab, r, x);  // full chunk: TMA store below
+      } else if (r < len) {
+        st_global_bf16x64(dq + ((size_t)(t0 + r) * d.Hk + i) * 128 + half * 64, x);
       }
       tmem_ld64(tb, warp, 320 + half * 64, x);
-      st_global_bf16x64((bf16*)ws.dKA + (ch * 64 + r) * 128 + half * 64, x);
+      st_row_bf16(sm + GradASmem::VN + half * kSlab, r, x);
     }
     float dga = 0.f;
     if (r < len) {
@@ -439,8 +462,19 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
     }
     ws.dgamA[ch * 64 + r] = dga;
   }
+  tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
+  if (ok && tid == 0) {
+    tc::tma_store_2d(&tm_dka, sm + GradASmem::VN, 0, (int)(ch * 64));
+    tc::tma_store_2d(&tm_dka, sm + GradASmem::VN + kSlab, 64, (int)(ch * 64));
+    if (!kGroup && len == 64) {
+      tc::tma_store_3d(&tm_dq, sm + GradASmem::OH, 0, i, t0);
+      tc::tma_store_3d(&tm_dq, sm + GradASmem::OH + kSlab, 64, i, t0);
+    }
+    tc::bulk_commit();
+  }
+  if (tid == 0) tc::bulk_wait_all();
   if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
@@ -457,16 +491,20 @@ struct GradBSmem {
   static constexpr uint32_t DT = 81920;    // dT (8 KB)
   static constexpr uint32_t X = 90112;     // T^T dT (8 KB)
   static constexpr uint32_t DAG = 98304;   // diag(beta) (dA * Gam) (8 KB)
-  static constexpr uint32_t SCR = 106496;  // fp32 [64][65]
+  static constexpr uint32_t KA = 106496;   // dk_A from gradA (16 KB)
+  static constexpr uint32_t SCR = 122880;  // fp32 [64][65]
   static constexpr uint32_t GAM = SCR + 16640;
   static constexpr uint32_t BYTES = GAM + 256;
+  // dv rows are staged in the V tile and dk rows in the K tile once those are consumed
 };
 
 template <bool kGroup>
 __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_dw,
-    const __grid_constant__ CUtensorMap tm_dvn, Dims d, const bf16* __restrict__ beta, bf16* __restrict__ dk,
+    const __grid_constant__ CUtensorMap tm_dvn, const __grid_constant__ CUtensorMap tm_dka,
+    const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_dk, Dims d,
+    const bf16* __restrict__ beta, bf16* __restrict__ dk,
     bf16* __restrict__ dv, float* __restrict__ dg, bf16* __restrict__ dbeta, Workspace ws) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
@@ -493,8 +531,10 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
   const uint32_t tb = tmem_slot;
   if (tid == 0) {
     uint64_t* bar = &bar_tma;
-    tc::mbar_arrive_expect_tx(bar, 9 * kSlab + 256);
+    tc::mbar_arrive_expect_tx(bar, 11 * kSlab + 256);
     tc::bulk_load(sm + GradBSmem::GAM, ws.gam + ch * 64, 256, bar);
+    tc::tma_load_2d(sm + GradBSmem::KA, &tm_dka, bar, 0, (int)(ch * 64));
+    tc::tma_load_2d(sm + GradBSmem::KA + kSlab, &tm_dka, bar, 64, (int)(ch * 64));
     tc::tma_load_3d(sm + GradBSmem::K, &tm_k, bar, 0, i, t0);
     tc::tma_load_3d(sm + GradBSmem::K + kSlab, &tm_k, bar, 64, i, t0);
     tc::tma_load_3d(sm + GradBSmem::V, &tm_v, bar, 0, j, t0);
@@ -557,7 +597,10 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
         dbv += x[b] * y[b];
         x[b] *= br;
       }
-      if (r < len) st_global_bf16x64(dv + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64, x);
+      if (len == 64)
+        st_row_bf16(sm + GradBSmem::V + half * kSlab, r, x);  // own row of V already consumed
+      else if (r < len)
+        st_global_bf16x64(dv + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64, x);
     }
   }
   tc::fence_proxy_async_smem();
@@ -565,6 +608,11 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
   __syncthreads();
   // R2: X = T^T dT (cols 448-511)
   if (ok && tid == 0) {
+    if (len == 64) {
+      tc::tma_store_3d(&tm_dv, sm + GradBSmem::V, 0, j, t0);
+      tc::tma_store_3d(&tm_dv, sm + GradBSmem::V + kSlab, 64, j, t0);
+      tc::bulk_commit();
+    }
     tc::tc_fence_after();
     tc::gemm(tb + 448, mnmaj(sm + GradBSmem::T, kSlab), mnmaj(sm + GradBSmem::DT, kSlab), 64, 4, false);
     tc::mma_commit(&bar_mma);
@@ -627,30 +675,39 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       tmem_ld64(tb, warp, 64 + half * 64, x);
-      ld_row_bf16_g((const bf16*)ws.dKA + (ch * 64 + r) * 128 + half * 64, y);
+      ld_row_bf16(sm + GradBSmem::KA + half * kSlab, r, y);
 #pragma unroll
       for (int b = 0; b < 64; ++b) x[b] += y[b];
-      if (r < len) {
-        if (kGroup) {
+      if (kGroup) {
+        if (r < len) {
           float* dst = ws.dk_part + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64;
 #pragma unroll
           for (int b = 0; b < 64; b += 4) *reinterpret_cast<float4*>(dst + b) = make_float4(x[b], x[b + 1], x[b + 2], x[b + 3]);
-        } else {
-          st_global_bf16x64(dk + ((size_t)(t0 + r) * d.Hk + i) * 128 + half * 64, x);
         }
+      } else if (len == 64) {
+        st_row_bf16(sm + GradBSmem::K + half * kSlab, r, x);  // K tile is free after R4
+      } else if (r < len) {
+        st_global_bf16x64(dk + ((size_t)(t0 + r) * d.Hk + i) * 128 + half * 64, x);
       }
     }
     if (r < len) dbeta[(size_t)(t0 + r) * Hv + j] = __float2bfloat16_rn(eg * dbk + dbv + akk);
     s_dgam[r] = r < len ? ws.dgamA[ch * 64 + r] + br * eg * dbk + rowaa - s_colaa[r] : 0.f;
   }
+  tc::fence_proxy_async_smem();
   __syncthreads();
-  if (ok && tid == 0) {  // dg = in-chunk reverse cumsum of d gamma
-    float run = 0.f;
+  if (ok && tid == 0) {
+    if (!kGroup && len == 64) {
+      tc::tma_store_3d(&tm_dk, sm + GradBSmem::K, 0, i, t0);
+      tc::tma_store_3d(&tm_dk, sm + GradBSmem::K + kSlab, 64, i, t0);
+      tc::bulk_commit();
+    }
+    float run = 0.f;  // dg = in-chunk reverse cumsum of d gamma
     for (int rr = len - 1; rr >= 0; --rr) {
       run += s_dgam[rr];
       dg[(size_t)(t0 + rr) * Hv + j] = run;
     }
   }
+  if (tid == 0) tc::bulk_wait_all();
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, 512);
@@ -667,19 +724,24 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
   if (Tt == 0 && d.num_seqs == 0) return cudaSuccess;
   cudaError_t e = tc_launch_prep(d, a.q, a.k, a.v, a.g, a.beta, ws, 1, s, "bwd_prep");
   if (e != cudaSuccess) return e;
-  const uint64_t Tmap = Tt > 0 ? Tt : 1;
-  const uint64_t rmap = rows > 0 ? rows : 64;
-  CUtensorMap tq, tk, tv, tdo, tw, tp, tdvn, tdh, tt, tdw;
-  if (!map_3d(&tq, a.q, 128, d.Hk, Tmap) || !map_3d(&tk, a.k, 128, d.Hk, Tmap) ||
-      !map_3d(&tv, a.v, 128, d.Hv, Tmap) || !map_3d(&tdo, a.dO, 128, d.Hv, Tmap) ||
-      !map_2d(&tw, ws.W, 128, rmap) || !map_2d(&tp, ws.P, 64, rmap) || !map_2d(&tdvn, ws.dVn, 128, rmap) ||
-      !map_2d(&tdh, ws.dhp, 128, rmap * 2) || !map_2d(&tt, ws.Tb, 64, rmap) || !map_2d(&tdw, ws.dWb, 128, rmap))
-    return cudaErrorInvalidValue;
+  CUtensorMap tq{}, tk{}, tv{}, tdo{}, tw{}, tp{}, tdvn{}, tdh{}, tt{}, tdw{}, tdhs{}, tu{}, tka{}, tdq{}, tdk{}, tdv{},
+      thf{};
+  if (Tt > 0) {  // with no tokens no kernel reads the maps (see tc_forward)
+    if (!map_3d(&tq, a.q, 128, d.Hk, Tt) || !map_3d(&tk, a.k, 128, d.Hk, Tt) || !map_3d(&tv, a.v, 128, d.Hv, Tt) ||
+        !map_3d(&tdo, a.dO, 128, d.Hv, Tt) || !map_2d(&tw, ws.W, 128, rows) || !map_2d(&tp, ws.P, 64, rows) ||
+        !map_2d(&tdvn, ws.dVn, 128, rows) || !map_2d(&tdh, ws.dhp, 128, rows * 2) || !map_2d(&tt, ws.Tb, 64, rows) ||
+        !map_2d(&tdw, ws.dWb, 128, rows) ||
+        !map_2d_box(&tdhs, ws.dhp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, rows * 2, 64, 128) ||
+        !map_2d(&tu, ws.U, 128, rows) || !map_2d(&tka, ws.dKA, 128, rows) || !map_3d(&tdq, a.dq, 128, d.Hk, Tt) ||
+        !map_3d(&tdk, a.dk, 128, d.Hk, Tt) || !map_3d(&tdv, a.dv, 128, d.Hv, Tt) ||
+        !map_2d_box(&thf, a.h_saved, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, rows * 2, 32, 128))
+      return cudaErrorInvalidValue;
+  }
   if (d.num_seqs > 0) {
     const size_t sm = WalkSmem::BYTES + 1024;
     cudaFuncSetAttribute(tc_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    tc_bwd_walk_kernel<<<dim3(d.num_seqs, d.Hv, 2), kTcThreads, sm, s>>>(tq, tk, tw, tp, tdo, d, a.dS_T, a.dS0,
-                                                                        ws);
+    tc_bwd_walk_kernel<<<dim3(d.num_seqs, d.Hv, 2), kTcThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, d, a.dS_T,
+                                                                        a.dS0, ws);
     stage_mark(s, "bwd_walk");
   }
   if (d.max_chunks > 0 && Tt > 0) {
@@ -687,21 +749,23 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     const size_t sma = GradASmem::BYTES + 1024, smb = GradBSmem::BYTES + 1024;
     if (d.G > 1) {
       cudaFuncSetAttribute(tc_bwd_gradA_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sma);
-      tc_bwd_gradA_kernel<true><<<grid, kTcThreads, sma, s>>>(tq, tk, tdo, tw, tdvn, tdh, d, a.h_saved,
+      tc_bwd_gradA_kernel<true><<<grid, kTcThreads, sma, s>>>(tq, tk, tdo, tw, tdvn, tdh, tu, tdw, tka, tdq, thf, d,
                                                                (bf16*)a.dq, ws);
     } else {
       cudaFuncSetAttribute(tc_bwd_gradA_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sma);
-      tc_bwd_gradA_kernel<false><<<grid, kTcThreads, sma, s>>>(tq, tk, tdo, tw, tdvn, tdh, d, a.h_saved,
-                                                                (bf16*)a.dq, ws);
+      tc_bwd_gradA_kernel<false><<<grid, kTcThreads, sma, s>>>(tq, tk, tdo, tw, tdvn, tdh, tu, tdw, tka, tdq, thf,
+                                                                d, (bf16*)a.dq, ws);
     }
     stage_mark(s, "bwd_gradA");
     if (d.G > 1) {
       cudaFuncSetAttribute(tc_bwd_gradB_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smb);
-      tc_bwd_gradB_kernel<true><<<grid, kTcThreads, smb, s>>>(tk, tv, tt, tdw, tdvn, d, (const bf16*)a.beta,
+      tc_bwd_gradB_kernel<true><<<grid, kTcThreads, smb, s>>>(tk, tv, tt, tdw, tdvn, tka, tdv, tdk, d,
+                                                               (const bf16*)a.beta,
                                                                (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
     } else {
       cudaFuncSetAttribute(tc_bwd_gradB_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smb);
-      tc_bwd_gradB_kernel<false><<<grid, kTcThreads, smb, s>>>(tk, tv, tt, tdw, tdvn, d, (const bf16*)a.beta,
+      tc_bwd_gradB_kernel<false><<<grid, kTcThreads, smb, s>>>(tk, tv, tt, tdw, tdvn, tka, tdv, tdk, d,
+                                                                (const bf16*)a.beta,
                                                                 (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
     }
     stage_mark(s, "bwd_gradB");

@@ -85,5 +85,13 @@ __device__ __forceinline__ float chunk_cumsum64(float x, int tid, float* scratch
   return x;
 }
 
+// Store 32 fp32 values into row `row` of a 128-byte-swizzled fp32 slab (32 columns).
+__device__ __forceinline__ void st_row_f32x32(unsigned char* slab, int row, const float* v) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch)
+    *reinterpret_cast<float4*>(slab + row * 128 + (((ch ^ (row & 7)) & 7) << 4)) =
+        make_float4(v[4 * ch], v[4 * ch + 1], v[4 * ch + 2], v[4 * ch + 3]);
+}
+
 }  // namespace tcx
 }  // namespace gdr
