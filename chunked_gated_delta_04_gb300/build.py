@@ -54,6 +54,7 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
                        "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
     if debug:
         flags += ["-DGDR_DEBUG_DELAY=1"]
+    flags += os.environ.get("GDR_NVCC_EXTRA", "").split()
     if verbose:
         flags += ["-Xptxas", "-v"]
 

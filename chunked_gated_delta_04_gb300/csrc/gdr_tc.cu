@@ -100,17 +100,141 @@ struct PrepSmem {
   static constexpr uint32_t KQ = 0;              // [K | Q] x 2 slabs: 32 KB
   static constexpr uint32_t V = 32768;           // 2 slabs: 16 KB
   static constexpr uint32_t TT = V + 16384;      // [T' | T''] bf16: 16 KB
-  static constexpr uint32_t A = TT + 16384;      // fp32 [64][64]: 16 KB
-  static constexpr uint32_t PS = A + 16384;      // P staged for its TMA store: 8 KB
-  static constexpr uint32_t BYTES = PS + 8192;   // 88 KB (two CTAs per SM)
+  static constexpr uint32_t A = TT + 16384;      // fp32 A [64][65]
+  static constexpr uint32_t TF = A + 17408;      // fp32 T [64][65]
+  static constexpr uint32_t Y = TF + 17408;      // fp32 3 x [16][16] block products
+  static constexpr uint32_t PS = Y + 4096;       // P (then T) staged for TMA stores: 8 KB
+  static constexpr uint32_t BYTES = PS + 8192;   // 110 KB (two CTAs per SM)
 };
+
+// T = (I + A)^{-1} for strictly lower-triangular A (fp32, row stride 65) by recursive
+// 2 x 2 block inversion: with L = [[L11, 0], [L21, L22]], L^{-1} = [[L11^{-1}, 0],
+// [-L22^{-1} L21 L11^{-1}, L22^{-1}]].  Steps: the four 16 x 16 diagonal inverses by
+// forward substitution (one thread per column); the two 16 x 16 off-diagonal blocks
+// of the 32 x 32 diagonal halves; the 32 x 32 lower-left block.  Every product is
+// register-tiled (all loads of a thread before its stores).  Writes the full T
+// (zeros above the diagonal) into sT (row stride 65).  All 128 threads take part.
+__device__ __forceinline__ void solve_unit_lower64(const float* __restrict__ sA, float* __restrict__ sT,
+                                                   float* __restrict__ sY, int tid) {
+#ifdef GDR_TRACE
+  unsigned long long ts_ = clock64();
+#define SOLVE_MARK(k)                                                   \
+  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) {                 \
+    const unsigned long long n_ = clock64();                            \
+    g_gdr_trace[0][16 + (k)] += n_ - ts_;                               \
+    ts_ = n_;                                                           \
+  }
+#else
+#define SOLVE_MARK(k)
+#endif
+  for (int e = tid; e < 64 * 65; e += kTcThreads) sT[e] = 0.f;
+  __syncthreads();
+  SOLVE_MARK(0);
+  if (tid < 64) {  // diagonal 16 x 16 blocks
+    const int b = tid >> 4, c = tid & 15;
+    const float* Ab = sA + (16 * b) * 65 + 16 * b;
+    float col[16];
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) {
+      float acc = (rr == c) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < rr; ++m) acc -= Ab[rr * 65 + m] * col[m];
+      col[rr] = acc;
+    }
+#pragma unroll
+    for (int rr = 0; rr < 16; ++rr) sT[(16 * b + rr) * 65 + 16 * b + c] = col[rr];
+  }
+  __syncthreads();
+  SOLVE_MARK(1);
+  {  // T_{2b+1,2b} = -T_{2b+1,2b+1} A_{2b+1,2b} T_{2b,2b}, b = 0, 1; thread: 1 row x 4 columns
+    const int b = tid >> 6, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
+    const int r0 = 16 * (2 * b + 1), c0 = 16 * (2 * b);
+    float x[16], z[16][4], o[4];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      x[k] = sA[(r0 + rr) * 65 + c0 + k];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) z[k][q] = sT[(c0 + k) * 65 + c0 + c4 + q];
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      o[q] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) o[q] += x[k] * z[k][q];
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sY[b * 256 + rr * 16 + c4 + q] = o[q];
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      x[k] = sT[(r0 + rr) * 65 + r0 + k];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) z[k][q] = sY[b * 256 + k * 16 + c4 + q];
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      o[q] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) o[q] += x[k] * z[k][q];
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sT[(r0 + rr) * 65 + c0 + c4 + q] = -o[q];
+  }
+  __syncthreads();
+  SOLVE_MARK(2);
+  {  // T_[23][01] = -T_[23][23] A_[23][01] T_[01][01] (32 x 32); thread: 1 row x 8 columns
+    const int rr = tid >> 2, c8 = (tid & 3) * 8;
+    float o[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = 0.f;
+#pragma unroll
+    for (int kh = 0; kh < 32; kh += 16) {
+      float x[16], z[16][8];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        x[k] = sA[(32 + rr) * 65 + kh + k];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) z[k][q] = sT[(kh + k) * 65 + c8 + q];
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) o[q] += x[k] * z[k][q];
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) sY[rr * 32 + c8 + q] = o[q];
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < 8; ++q) o[q] = 0.f;
+#pragma unroll
+    for (int kh = 0; kh < 32; kh += 16) {
+      float x[16], z[16][8];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        x[k] = sT[(32 + rr) * 65 + 32 + kh + k];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) z[k][q] = sY[(kh + k) * 32 + c8 + q];
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+#pragma unroll
+        for (int k = 0; k < 16; ++k) o[q] += x[k] * z[k][q];
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) sT[(32 + rr) * 65 + c8 + q] = -o[q];
+  }
+  __syncthreads();
+  SOLVE_MARK(3);
+#undef SOLVE_MARK
+}
 
 __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                              const __grid_constant__ CUtensorMap tm_k,
                                                              const __grid_constant__ CUtensorMap tm_v,
                                                              const __grid_constant__ CUtensorMap tm_w,
                                                              const __grid_constant__ CUtensorMap tm_u,
-                                                             const __grid_constant__ CUtensorMap tm_p, Dims d,
+                                                             const __grid_constant__ CUtensorMap tm_p,
+                                                             const __grid_constant__ CUtensorMap tm_t, Dims d,
                                                              const float* __restrict__ g,
                                                              const bf16* __restrict__ beta, Workspace ws,
                                                              int write_T) {
@@ -118,7 +242,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_slot;
-  __shared__ float s_gam[64], s_beta[64], s_carry;
+  __shared__ float s_gam[64], s_beta[64], s_bexp[64], s_carry;
   const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int4 ci = ws.chunks[c];
@@ -137,6 +261,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tbase = tmem_slot;
+  GDR_TRACE_INIT();
   if (tid == 0) {
     tc::mbar_arrive_expect_tx(&bar_tma, 6 * kSlab);
     tc::tma_load_3d(sm + PrepSmem::KQ, &tm_k, &bar_tma, 0, i, t0);
@@ -157,9 +282,11 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
     if (tid < 64) {
       s_gam[tid] = x;
       s_beta[tid] = b;
+      s_bexp[tid] = b * fexp(x);  // beta_s e^{gamma_s}
     }
   }
   bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma, 0, ws.status, kDevErrTimeoutPrep));
+  GDR_TRACE_MARK(0, 0);
   const uint32_t s_kq = tc::smem_u32(sm + PrepSmem::KQ), s_v = tc::smem_u32(sm + PrepSmem::V);
   const uint32_t s_tt = tc::smem_u32(sm + PrepSmem::TT);
   if (ok && tid == 0) {
@@ -172,6 +299,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutPrep));
+  GDR_TRACE_MARK(0, 1);
   tc::tc_fence_after();
   float* sA = reinterpret_cast<float*>(sm + PrepSmem::A);
   if (ok) {
@@ -179,13 +307,18 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
     tmem_ld64(tbase, warp, 0, row);
     const int r = tid & 63;
     const float gr = s_gam[r];
-    if (tid < 64) {  // A row r
+    if (tid < 64) {  // A row r (all loads before the stores: smem pointers may alias)
       const float br = s_beta[r];
+      float gs[64];
 #pragma unroll
-      for (int s = 0; s < 64; ++s) sA[r * 64 + s] = (s < r && r < len) ? br * __expf(gr - s_gam[s]) * row[s] : 0.f;
+      for (int s = 0; s < 64; ++s) gs[s] = s_gam[s];
+#pragma unroll
+      for (int s = 0; s < 64; ++s) row[s] = (s < r && r < len) ? br * fexp(gr - gs[s]) * row[s] : 0.f;
+#pragma unroll
+      for (int s = 0; s < 64; ++s) sA[r * 65 + s] = row[s];
     } else {  // P row r
 #pragma unroll
-      for (int s = 0; s < 64; ++s) row[s] = (s <= r && r < len) ? row[s] * __expf(gr - s_gam[s]) : 0.f;
+      for (int s = 0; s < 64; ++s) row[s] = (s <= r && r < len) ? row[s] * fexp(gr - s_gam[s]) : 0.f;
       st_row_bf16(sm + PrepSmem::PS, r, row);
     }
   }
@@ -195,39 +328,37 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
     tc::tma_store_2d(&tm_p, sm + PrepSmem::PS, 0, (int)(ch * 64));
     tc::bulk_commit();
   }
-  // T = (I + A)^{-1}: thread s < 64 owns column s of T in registers
-  if (ok && tid < 64) {
-    const int s = tid;
-    float tcol[64];
+  GDR_TRACE_MARK(0, 2);
+  // T = (I + A)^{-1}
+  if (tid == 0) tc::bulk_wait_read<0>();  // P has left its staging tile (reused for T below)
+  GDR_TRACE_MARK(0, 8);
+  float* sT = reinterpret_cast<float*>(sm + PrepSmem::TF);
+  solve_unit_lower64(sA, sT, reinterpret_cast<float*>(sm + PrepSmem::Y), tid);
+  GDR_TRACE_MARK(0, 9);
+  if (ok) {  // rows of T' = T diag(beta e^gamma) (threads 0-63), T'' = T diag(beta) (64-127)
+    const int r = tid & 63;
+    float x[64];
 #pragma unroll
-    for (int r = 0; r < 64; ++r) {
-      float acc0 = (r == s) ? 1.f : 0.f, acc1 = 0.f;
-      const float* Ar = sA + r * 64;
-#pragma unroll
-      for (int m = 0; m + 1 < r; m += 2) {
-        acc0 -= Ar[m] * tcol[m];
-        acc1 -= Ar[m + 1] * tcol[m + 1];
-      }
-      if (r & 1) acc0 -= Ar[r - 1] * tcol[r - 1];
-      tcol[r] = acc0 + acc1;
+    for (int s2 = 0; s2 < 64; ++s2) {
+      const float t = sT[r * 65 + s2];
+      x[s2] = t * (tid < 64 ? s_bexp[s2] : s_beta[s2]);
     }
-    const float bs = s_beta[s], es = bs * __expf(s_gam[s]);
-    if (write_T) {  // T itself, for the backward (row r, column s)
-      bf16* Tg = (bf16*)ws.Tb + ch * 64 * 64 + s;
+    st_row_bf16(sm + PrepSmem::TT + (tid < 64 ? 0 : kSlab), r, x);
+    if (write_T && tid < 64) {  // T itself for the backward
 #pragma unroll
-      for (int r = 0; r < 64; ++r) Tg[r * 64] = __float2bfloat16_rn(tcol[r]);
-    }
-    unsigned char* tt = sm + PrepSmem::TT;
-#pragma unroll
-    for (int r = 0; r < 64; ++r) {
-      *reinterpret_cast<bf16*>(tt + tc::sw128_off(r, s, 64)) = __float2bfloat16_rn(tcol[r] * es);          // T'
-      *reinterpret_cast<bf16*>(tt + kSlab + tc::sw128_off(r, s, 64)) = __float2bfloat16_rn(tcol[r] * bs);  // T''
+      for (int s2 = 0; s2 < 64; ++s2) x[s2] = sT[r * 65 + s2];
+      st_row_bf16(sm + PrepSmem::PS, r, x);
     }
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
+  GDR_TRACE_MARK(0, 3);
   if (ok && tid == 0) {
+    if (write_T) {
+      tc::tma_store_2d(&tm_t, sm + PrepSmem::PS, 0, (int)(ch * 64));
+      tc::bulk_commit();
+    }
     tc::tc_fence_after();
     // W = T' K (lanes 0-63 of cols [0,128)), U = T'' V (lanes 64-127 of cols [128,256))
     const uint32_t id = tc::idesc_bf16(128, 128, 0, 1);
@@ -240,6 +371,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutPrep));
+  GDR_TRACE_MARK(0, 4);
   tc::tc_fence_after();
   if (ok) {  // W rows (threads 0-63) and U rows (threads 64-127) staged in the free K/Q tiles
     const int r = tid & 63;
@@ -262,7 +394,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
     tc::tma_store_2d(&tm_u, sm + PrepSmem::KQ + 3 * kSlab, 64, (int)(ch * 64));
     tc::bulk_commit();
   }
-  if (tid == 0) tc::bulk_wait_all();
+  if (tid == 0) tc::bulk_wait_read<0>();  // smem sources read before exit
+  GDR_TRACE_MARK(0, 5);
   if (warp == 0) tc::tmem_dealloc(tbase, 256);
 }
 
@@ -337,9 +470,11 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     tc::tma_load_2d(base + StateSmem::P, &tm_p, &bar_load[st], 0, (int)(chh * 64));
   };
   if (tid == 0 && c_begin < c_end) issue_loads(c_begin, 0);
+  st_row_bf16(sm + StateSmem::H, tid, h);
 
   bool ok = true;
   uint32_t mma_phase = 0;
+  GDR_TRACE_INIT();
   const uint32_t s_h = tc::smem_u32(sm + StateSmem::H), s_vn = tc::smem_u32(sm + StateSmem::VN);
   const uint32_t s_vt = tc::smem_u32(sm + StateSmem::VT);
   for (int c = c_begin; c < c_end && ok; ++c) {
@@ -348,21 +483,14 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     const int t0 = t_seq + it * 64;
     const int len = min(64, L - it * 64);
     const size_t chh = (size_t)c * Hv + j;
-    if (tid == 0 && c + 1 < c_end) issue_loads(c + 1, st ^ 1);
-    // stage the chunk-start state (fp32, for h_saved) and h as the bf16 B operand
-    st_row_f32x32(sm + StateSmem::HS, tid, h);
-    st_row_f32x32(sm + StateSmem::HS + 16384, tid, h + 32);
-    st_row_bf16(sm + StateSmem::H, tid, h);
+    // h (bf16 B operand) was written at the end of the previous chunk / before the loop
     const int r = tid & 63;
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // h_saved[chunk] rows 0..127, columns dv0..dv0+63
-      tc::tma_store_2d(&tm_hs, sm + StateSmem::HS, dv0, (int)(chh * 128));
-      tc::tma_store_2d(&tm_hs, sm + StateSmem::HS + 16384, dv0 + 32, (int)(chh * 128));
-      tc::bulk_commit();
-    }
+    GDR_TRACE_MARK(1, 0);
     ok = __syncthreads_and(tc::mbar_wait(&bar_load[st], ld_phase, ws.status, kDevErrTimeoutFwd));
+    GDR_TRACE_MARK(1, 1);
     const float* sgam = reinterpret_cast<const float*>(sm + StateSmem::GAM + st * 256);
     const float gC = sgam[len - 1];
     const float gr = sgam[r];
@@ -377,9 +505,20 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
         tc::mma_bf16(D1, tc::kmajor_step_desc(s_wq, 2 * kSlab, kk), tc::mnmajor_step_desc(s_h, 16384, kk), id, kk > 0);
       tc::mma_commit(&bar_mma);
     }
+    if (tid == 0 && c + 1 < c_end) issue_loads(c + 1, st ^ 1);  // overlaps the MMA
+    // while [W;Q] h runs: stage the chunk-start state (fp32) for its h_saved store
+    st_row_f32x32(sm + StateSmem::HS, tid, h);
+    st_row_f32x32(sm + StateSmem::HS + 16384, tid, h + 32);
+    tc::fence_proxy_async_smem();
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutFwd));
     mma_phase ^= 1;
     tc::tc_fence_after();
+    if (tid == 0) {  // h_saved[chunk] rows 0..127, columns dv0..dv0+63
+      tc::tma_store_2d(&tm_hs, sm + StateSmem::HS, dv0, (int)(chh * 128));
+      tc::tma_store_2d(&tm_hs, sm + StateSmem::HS + 16384, dv0 + 32, (int)(chh * 128));
+      tc::bulk_commit();
+    }
+    GDR_TRACE_MARK(1, 2);
     float x[64];
     if (ok) {
       tmem_ld64(tbase, warp, 0, x);
@@ -389,7 +528,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
 #pragma unroll
         for (int b = 0; b < 64; ++b) u[b] -= x[b];
         st_row_bf16(sm + StateSmem::VN, r, u);
-        const float dec = __expf(gC - gr);
+        const float dec = fexp(gC - gr);
 #pragma unroll
         for (int b = 0; b < 64; ++b) u[b] *= dec;
         st_row_bf16(sm + StateSmem::VT, r, u);
@@ -398,6 +537,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
+    GDR_TRACE_MARK(1, 3);
     if (ok && tid == 0) {
       tc::tc_fence_after();
       const uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
@@ -415,12 +555,18 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutFwd));
     mma_phase ^= 1;
     tc::tc_fence_after();
+    GDR_TRACE_MARK(1, 4);
     if (ok) {
       float y[64];
+      tmem_ld64(tbase, warp, 128, y);  // h <- e^{gamma_C} h + K^T Vn~, then stage it for the next chunk
+      const float eC = fexp(gC);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) h[b] = eC * h[b] + y[b];
+      st_row_bf16(sm + StateSmem::H, tid, h);
       if (tid >= 64) {  // O rows: x holds (Q h)[r], D2 lanes 64-127 hold (P Vn)[r]
         tmem_ld64(tbase, warp, 64, y);
         if (r < len) {
-          const float eg = __expf(gr);
+          const float eg = fexp(gr);
 #pragma unroll
           for (int b = 0; b < 64; ++b) y[b] = d.scale * (eg * x[b] + y[b]);
           if (len == 64)
@@ -429,10 +575,6 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
             st_global_bf16x64(o + ((size_t)(t0 + r) * Hv + j) * 128 + dv0, y);
         }
       }
-      tmem_ld64(tbase, warp, 128, y);
-      const float eC = __expf(gC);
-#pragma unroll
-      for (int b = 0; b < 64; ++b) h[b] = eC * h[b] + y[b];
     }
     if (tid == 0) tc::bulk_wait_read<0>();  // h staging free for the next chunk
     tc::fence_proxy_async_smem();
@@ -442,8 +584,9 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
       tc::tma_store_3d(&tm_o, sm + StateSmem::OS, dv0, j, t0);
       tc::bulk_commit();
     }
+    GDR_TRACE_MARK(1, 5);
   }
-  if (tid == 0) tc::bulk_wait_all();
+  if (tid == 0) tc::bulk_wait_read<0>();  // smem sources read before exit
   if (ok && S_T) {
     const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
 #pragma unroll
@@ -458,6 +601,12 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
 }  // namespace
 
 bool tc_available() { return get_encoder(); }
+
+#ifdef GDR_TRACE
+extern "C" int gdr_debug_trace_fwd(unsigned long long* out) {
+  return cudaMemcpyFromSymbol(out, tcx::g_gdr_trace, sizeof(tcx::g_gdr_trace)) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s) {
   if (!get_encoder()) return cudaErrorNotSupported;
@@ -477,7 +626,7 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
   if (d.max_chunks > 0 && Tt > 0) {
     const size_t smp = PrepSmem::BYTES + 1024;
     cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
-    tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, d, a.g,
+    tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, tp, d, a.g,
                                                                       (const bf16*)a.beta, ws, 0);
     stage_mark(s, "fwd_prep");
   }
@@ -494,16 +643,17 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
 cudaError_t tc_launch_prep(const Dims& d, const void* q, const void* k, const void* v, const float* g,
                            const void* beta, const Workspace& ws, int write_T, cudaStream_t s, const char* stage) {
   if (d.max_chunks == 0 || d.T_total == 0) return cudaSuccess;
-  CUtensorMap tq, tk, tv, tw, tu, tp;
+  CUtensorMap tq, tk, tv, tw, tu, tp, tt{};
   const uint64_t Tt = (uint64_t)d.T_total;
   const uint64_t rows = (uint64_t)d.max_chunks * d.Hv * 64;
   if (!map_3d(&tq, q, 128, d.Hk, Tt) || !map_3d(&tk, k, 128, d.Hk, Tt) || !map_3d(&tv, v, 128, d.Hv, Tt) ||
       !map_2d(&tw, ws.W, 128, rows) || !map_2d(&tu, ws.U, 128, rows) || !map_2d(&tp, ws.P, 64, rows))
     return cudaErrorInvalidValue;
+  if (write_T && !map_2d(&tt, ws.Tb, 64, rows)) return cudaErrorInvalidValue;
   const size_t smp = PrepSmem::BYTES + 1024;
   cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
-  tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, d, g, (const bf16*)beta,
-                                                                    ws, write_T);
+  tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, tt, d, g,
+                                                                    (const bf16*)beta, ws, write_T);
   stage_mark(s, stage);
   return cudaGetLastError();
 }

@@ -132,7 +132,6 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
     const int len = min(64, L - (c - c_begin) * 64);
     (void)t0;
     const size_t chh = (size_t)c * Hv + j;
-    if (tid == 0 && c - 1 >= c_begin) issue_loads(c - 1, st ^ 1);
     st_row_bf16(sm + WalkSmem::DH, tid, dh);
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
@@ -148,7 +147,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
     if (ok && tid >= 64) {  // diag(e^gamma) dO, zero past the chunk end
       float x[64];
       ld_row_bf16(stg + WalkSmem::DO, r, x);
-      const float e = r < len ? __expf(gr) : 0.f;
+      const float e = r < len ? fexp(gr) : 0.f;
 #pragma unroll
       for (int b = 0; b < 64; ++b) x[b] *= e;
       st_row_bf16(sm + WalkSmem::DOS, r, x);
@@ -164,6 +163,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
                false);  // Q^T diag(e^gamma) dO
       tc::mma_commit(&bar_mma);
     }
+    if (tid == 0 && c - 1 >= c_begin) issue_loads(c - 1, st ^ 1);  // overlaps the MMAs
     if (tid == 0) tc::bulk_wait_read<1>();  // the previous chunk's dVn store has left its tile
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutBwd));
     mma_phase ^= 1;
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
       float x[64], y[64];
       tmem_ld64(tb, warp, 0, x);
       tmem_ld64(tb, warp, 64, y);
-      const float dec = __expf(gC - gr);
+      const float dec = fexp(gC - gr);
 #pragma unroll
       for (int b = 0; b < 64; ++b) y[b] = r < len ? d.scale * y[b] + dec * x[b] : 0.f;
       st_row_bf16(sm + WalkSmem::DVN, r, y);
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
       float x[64], y[64];
       tmem_ld64(tb, warp, 128, x);
       tmem_ld64(tb, warp, 192, y);
-      const float eC = __expf(gC);
+      const float eC = fexp(gC);
 #pragma unroll
       for (int b = 0; b < 64; ++b) dh[b] = eC * dh[b] + d.scale * y[b] - x[b];
     }
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
     tc::tc_fence_before();
     __syncthreads();
   }
-  if (tid == 0) tc::bulk_wait_all();
+  if (tid == 0) tc::bulk_wait_read<0>();  // smem sources read before exit
   if (ok && dS0) {
     const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
 #pragma unroll
@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tb = tmem_slot;
+  GDR_TRACE_INIT();
   if (tid == 0) {
     uint64_t* bar = &bar_tma;
     tc::mbar_arrive_expect_tx(bar, 24 * kSlab + 256);
@@ -289,9 +290,10 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
                       (int)(ch * 128 + (q4 & 1) * 64));
   }
   bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma, 0, ws.status, kDevErrTimeoutBwd));
+  GDR_TRACE_MARK(2, 0);
   const float* sgam = reinterpret_cast<const float*>(sm + GradASmem::GAM);
   const float gC = sgam[len - 1], gr = sgam[r];
-  const float dec = __expf(gC - gr), eg = __expf(gr);
+  const float dec = fexp(gC - gr), eg = fexp(gr);
   // h row `tid`: fp32 slabs (32 columns each) -> bf16 operand slabs (64 columns each).
   // bf16 slab s overwrites fp32 slab s, so each half is read completely (and the
   // barrier passed) before it is written.  <dh', h> is accumulated on the way.
@@ -318,6 +320,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
     if (ok) st_row_bf16(sm + GradASmem::H + half * 16384, tid, hv);
   }
   hdh = block_sum128(hdh, s_red);
+  GDR_TRACE_MARK(2, 1);
   if (ok && tid < 64) {  // O-hat = scale diag(e^gamma) dO, zero past the chunk end
     float x[64];
     const float e = r < len ? d.scale * eg : 0.f;
@@ -342,6 +345,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
+  GDR_TRACE_MARK(2, 2);
   tc::tc_fence_after();
   float* scr = reinterpret_cast<float*>(sm + GradASmem::SCR);
   if (ok) {
@@ -378,6 +382,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
+  GDR_TRACE_MARK(2, 3);
   // Ph4: dO Vn^T (cols 0-63), K dh' (64-191), Vn~ dh'^T (320-447); dq stays in 192-319
   if (ok && tid == 0) {
     tc::tma_store_2d(&tm_dwb, sm + GradASmem::DVN, 0, (int)(ch * 64));
@@ -390,20 +395,32 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
+  GDR_TRACE_MARK(2, 4);
   tc::tc_fence_after();
   if (ok && tid < 64) {
     float x[64], v[64];
+    GDR_TRACE_MARK(2, 10);
     tmem_ld64(tb, warp, 0, x);  // (dO Vn^T)[r]
+    GDR_TRACE_MARK(2, 11);
     float rowpp = 0.f;
+    float gs[64], qk[64];  // all smem loads first: the compiler cannot prove the tiles do not alias
 #pragma unroll
     for (int s = 0; s < 64; ++s) {
-      const float dp = (s <= r && r < len) ? d.scale * x[s] * __expf(gr - sgam[s]) : 0.f;
-      x[s] = dp;
-      const float pp = dp * scr[r * 65 + s];
-      scr[r * 65 + s] = pp;
-      rowpp += pp;
+      gs[s] = sgam[s];
+      qk[s] = scr[r * 65 + s];
     }
+#pragma unroll
+    for (int s = 0; s < 64; ++s) {
+      const float dp = (s <= r && r < len) ? d.scale * x[s] * fexp(gr - gs[s]) : 0.f;
+      x[s] = dp;
+      qk[s] *= dp;
+      rowpp += qk[s];
+    }
+    GDR_TRACE_MARK(2, 12);
+#pragma unroll
+    for (int s = 0; s < 64; ++s) scr[r * 65 + s] = qk[s];
     s_rowpp[r] = rowpp;
+    GDR_TRACE_MARK(2, 13);
     st_row_bf16(sm + GradASmem::H, r, x);  // dP (h no longer needed)
     float kdv = 0.f;
 #pragma unroll
@@ -414,15 +431,20 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
       for (int b = 0; b < 64; ++b) kdv += x[b] * v[b];
     }
     s_kdv[r] = r < len ? kdv : 0.f;
+    const float part = warp_sum(r < len ? dec * kdv : 0.f);  // e^{gC - g_r} k_r^T dh' vn_r
+    if ((tid & 31) == 0) s_red[tid >> 5] = part;
+    GDR_TRACE_MARK(2, 14);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
+  GDR_TRACE_MARK(2, 15);
   if (ok && tid < 64) {
     float cs = 0.f;
     for (int rr = 0; rr < 64; ++rr) cs += scr[rr * 65 + tid];
     s_colpp[tid] = cs;
   }
+  GDR_TRACE_MARK(2, 5);
   // Ph6: dq += dP K (cols 192-319), dk_A += dP^T Q (cols 320-447)
   if (ok && tid == 0) {
     tc::tc_fence_after();
@@ -431,6 +453,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
+  GDR_TRACE_MARK(2, 6);
   tc::tc_fence_after();
   if (ok && tid < 64) {
     float x[64];
@@ -454,11 +477,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
     float dga = 0.f;
     if (r < len) {
       dga = s_rowpp[r] - s_colpp[r] + s_qh[r] - dec * s_kdv[r];
-      if (r == len - 1) {
-        float sk = 0.f;
-        for (int s = 0; s < len; ++s) sk += __expf(gC - sgam[s]) * s_kdv[s];
-        dga += __expf(gC) * hdh + sk;
-      }
+      if (r == len - 1) dga += fexp(gC) * hdh + (s_red[0] + s_red[1]);
     }
     ws.dgamA[ch * 64 + r] = dga;
   }
@@ -474,7 +493,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
     }
     tc::bulk_commit();
   }
-  if (tid == 0) tc::bulk_wait_all();
+  if (tid == 0) tc::bulk_wait_read<0>();  // smem sources read before exit
+  GDR_TRACE_MARK(2, 7);
   if (warp == 0) tc::tmem_dealloc(tb, 512);
 }
 
@@ -510,7 +530,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_slot;
-  __shared__ float s_beta[64], s_dgam[64], s_colaa[64];
+  __shared__ float s_beta[64], s_dgam[64], s_colaa[64], s_eg[64];
   const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
   const int tid = threadIdx.x, warp = tid >> 5, r = tid & 63;
   const int4 ci = ws.chunks[c];
@@ -529,6 +549,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tb = tmem_slot;
+  GDR_TRACE_INIT();
   if (tid == 0) {
     uint64_t* bar = &bar_tma;
     tc::mbar_arrive_expect_tx(bar, 11 * kSlab + 256);
@@ -547,18 +568,22 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
   }
   if (tid < 64) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * Hv + j]) : 0.f;
   bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma, 0, ws.status, kDevErrTimeoutBwd));
+  GDR_TRACE_MARK(3, 0);
   const float* sgam = reinterpret_cast<const float*>(sm + GradBSmem::GAM);
-  const float gr = sgam[r], eg = __expf(gr), br = s_beta[r];
+  if (tid < 64) s_eg[tid] = fexp(sgam[tid]);
+  __syncthreads();
+  const float gr = sgam[r], eg = s_eg[r], br = s_beta[r];
   if (ok && tid < 64) {  // T' row r = T[r][:] * beta e^gamma (per column)
     float x[64];
     ld_row_bf16(sm + GradBSmem::T, r, x);
 #pragma unroll
-    for (int s = 0; s < 64; ++s) x[s] *= s_beta[s] * __expf(sgam[s]);
+    for (int s = 0; s < 64; ++s) x[s] *= s_beta[s] * s_eg[s];
     st_row_bf16(sm + GradBSmem::TP, r, x);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
+  GDR_TRACE_MARK(3, 1);
   // R1: K K^T (0-63), dW K^T (64-127), dVn V^T (128-191), T^T dW (192-319), T^T dVn (320-447)
   if (ok && tid == 0) {
     tc::tc_fence_after();
@@ -570,6 +595,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
+  GDR_TRACE_MARK(3, 2);
   tc::tc_fence_after();
   float* scr = reinterpret_cast<float*>(sm + GradBSmem::SCR);
   float dbk = 0.f, dbv = 0.f;
@@ -582,7 +608,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
     tmem_ld64(tb, warp, 128, y);  // (dVn V^T)[r]
 #pragma unroll
     for (int s = 0; s < 64; ++s)
-      x[s] = (r < len && s < len) ? s_beta[s] * (__expf(sgam[s]) * x[s] + y[s]) : 0.f;
+      x[s] = (r < len && s < len) ? s_beta[s] * (s_eg[s] * x[s] + y[s]) : 0.f;
     st_row_bf16(sm + GradBSmem::DT, r, x);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -606,6 +632,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
+  GDR_TRACE_MARK(3, 3);
   // R2: X = T^T dT (cols 448-511)
   if (ok && tid == 0) {
     if (len == 64) {
@@ -618,6 +645,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
+  GDR_TRACE_MARK(3, 4);
   tc::tc_fence_after();
   if (ok && tid < 64) {
     float x[64];
@@ -627,6 +655,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
+  GDR_TRACE_MARK(3, 5);
   // R3: X T^T (cols 0-63)
   if (ok && tid == 0) {
     tc::tc_fence_after();
@@ -634,22 +663,30 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
+  GDR_TRACE_MARK(3, 6);
   tc::tc_fence_after();
   float akk = 0.f, rowaa = 0.f;
   if (ok && tid < 64) {
     float x[64];
     tmem_ld64(tb, warp, 0, x);
+    float gs[64], kk[64];  // all smem loads first: the compiler cannot prove the tiles do not alias
 #pragma unroll
     for (int s = 0; s < 64; ++s) {
-      const float da = (s < r && r < len) ? -x[s] : 0.f;
-      const float dag = da * __expf(gr - sgam[s]);
-      const float kk = scr[r * 65 + s];
-      akk += dag * kk;
-      x[s] = br * dag;
-      const float aa = x[s] * kk;  // dA * A with A = beta_r Gam K K^T
-      rowaa += aa;
-      scr[r * 65 + s] = aa;
+      gs[s] = sgam[s];
+      kk[s] = scr[r * 65 + s];
     }
+#pragma unroll
+    for (int s = 0; s < 64; ++s) {
+      // exp(gamma_r - gamma_s) only below the diagonal: above it the exponent is
+      // positive and can overflow, and 0 * inf would give NaN
+      const float dag = (s < r && r < len) ? -x[s] * fexp(gr - gs[s]) : 0.f;
+      akk += dag * kk[s];
+      x[s] = br * dag;
+      kk[s] *= x[s];  // dA * A with A = beta_r Gam K K^T
+      rowaa += kk[s];
+    }
+#pragma unroll
+    for (int s = 0; s < 64; ++s) scr[r * 65 + s] = kk[s];
     st_row_bf16(sm + GradBSmem::DAG, r, x);
   }
   tc::fence_proxy_async_smem();
@@ -660,6 +697,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
     for (int rr = 0; rr < 64; ++rr) cs += scr[rr * 65 + tid];
     s_colaa[tid] = cs;
   }
+  GDR_TRACE_MARK(3, 7);
   // R4: dk_B = T'^T dW + dAGb K + dAGb^T K (cols 64-191)
   if (ok && tid == 0) {
     tc::tc_fence_after();
@@ -669,6 +707,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
+  GDR_TRACE_MARK(3, 8);
   tc::tc_fence_after();
   if (ok && tid < 64) {
     float x[64], y[64];
@@ -701,13 +740,25 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
       tc::tma_store_3d(&tm_dk, sm + GradBSmem::K + kSlab, 64, i, t0);
       tc::bulk_commit();
     }
-    float run = 0.f;  // dg = in-chunk reverse cumsum of d gamma
-    for (int rr = len - 1; rr >= 0; --rr) {
-      run += s_dgam[rr];
-      dg[(size_t)(t0 + rr) * Hv + j] = run;
-    }
   }
-  if (tid == 0) tc::bulk_wait_all();
+  if (ok && tid < 64) {  // dg = in-chunk reverse cumsum of d gamma (rows >= len hold 0)
+    const int lane = tid & 31;
+    float x = s_dgam[63 - tid];  // reversed order: prefix sums become suffix sums
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    s_colaa[tid] = x;  // s_colaa is free again: reuse it for the warp totals
+  }
+  __syncthreads();
+  if (ok && tid < 64) {
+    const int rr = 63 - tid;
+    const float v = s_colaa[tid] + (tid >= 32 ? s_colaa[31] : 0.f);
+    if (rr < len) dg[(size_t)(t0 + rr) * Hv + j] = v;
+  }
+  if (tid == 0) tc::bulk_wait_read<0>();  // smem sources read before exit
+  GDR_TRACE_MARK(3, 9);
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, 512);
@@ -716,6 +767,12 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
 }  // namespace
 
 bool tc_bwd_available() { return get_encoder(); }
+
+#ifdef GDR_TRACE
+extern "C" int gdr_debug_trace_bwd(unsigned long long* out) {
+  return cudaMemcpyFromSymbol(out, tcx::g_gdr_trace, sizeof(tcx::g_gdr_trace)) == cudaSuccess ? 0 : 1;
+}
+#endif
 
 cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cudaStream_t s) {
   if (!get_encoder()) return cudaErrorNotSupported;

@@ -9,6 +9,28 @@
 namespace gdr {
 namespace tcx {
 
+// Opt-in phase trace (-DGDR_TRACE): thread 0 of CTA (0,0,0) adds the clock64() cycles
+// spent between consecutive marks into a per-translation-unit table [kernel][mark].
+#ifdef GDR_TRACE
+static __device__ unsigned long long g_gdr_trace[8][32];
+#define GDR_TRACE_INIT() unsigned long long gdr_tprev_ = clock64()
+#define GDR_TRACE_MARK(kid, slot)                                                                  \
+  do {                                                                                             \
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {               \
+      const unsigned long long now_ = clock64();                                                   \
+      g_gdr_trace[kid][slot] += now_ - gdr_tprev_;                                                 \
+      gdr_tprev_ = now_;                                                                           \
+    }                                                                                              \
+  } while (0)
+#else
+#define GDR_TRACE_INIT() \
+  do {                   \
+  } while (0)
+#define GDR_TRACE_MARK(kid, slot) \
+  do {                            \
+  } while (0)
+#endif
+
 using bf16 = __nv_bfloat16;
 constexpr int kTcThreads = 128;
 constexpr uint32_t kSlab = 64 * 128;  // bytes of one 64-row x 128-byte slab
@@ -83,6 +105,14 @@ __device__ __forceinline__ float chunk_cumsum64(float x, int tid, float* scratch
   __syncthreads();
   if (tid >= 32 && tid < 64) x += *scratch;
   return x;
+}
+
+// e^x as 2^(x log2 e) on the hardware exp2 unit (about 2 ulp; results below 2^-126
+// flush to zero).  In the epilogue loops it is several times faster than __expf.
+__device__ __forceinline__ float fexp(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+  return y;
 }
 
 // Store 32 fp32 values into row `row` of a 128-byte-swizzled fp32 slab (32 columns).

@@ -45,6 +45,13 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("dt,D", [(torch.float32, 32), (torch.bfloat16, 128)])
+def test_strong_decay_gates(dt, D):
+    # g = logsigmoid(N(-4, 1)) ~ -4 per token: in-chunk cumsums reach ~ -250, so any
+    # exp(gamma_r - gamma_s) evaluated above the diagonal would overflow to inf
+    _check(small_workload("strong_decay", dt, B=1, T=192, Hk=1, Hv=1, DK=D, DV=D, g_shift=-4.0))
+
+
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
 def test_small_shapes(case):
     name, dt, B, T, Hk, Hv, D, layout, s0, dst = case
