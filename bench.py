@@ -45,8 +45,7 @@ STAGE_IO = {
     "bwd_vn": ("h_saved", ""),
     "bwd_walk": ("dO dS_T", "dS0"),
     "bwd_grad": ("q k v dO beta h_saved", "dq dk dv dg dbeta"),
-    "bwd_gradA": ("q k dO h_saved", "dq"),
-    "bwd_gradB": ("k v beta", "dk dv dg dbeta"),
+
     "bwd_group_reduce": ("", "dq dk"),
 }
 

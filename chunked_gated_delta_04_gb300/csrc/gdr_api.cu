@@ -111,9 +111,6 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
     if (d.path == 1) {
       w.Tb = take(el * chH * kChunk * kChunk);
       w.dVn = take(el * chH * kChunk * d.DV);
-      w.dWb = take(el * chH * kChunk * d.DK);
-      w.dKA = take(el * chH * kChunk * d.DK);
-      w.dgamA = (float*)take(sizeof(float) * chH * kChunk);
     }
     if (d.G > 1) {
       w.dq_part = (float*)take(sizeof(float) * (size_t)d.T_total * d.Hv * d.DK);

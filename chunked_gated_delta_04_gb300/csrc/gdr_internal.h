@@ -50,9 +50,6 @@ struct Workspace {
                  // (fp32 on the SIMT path, bf16 on the tensor-core path)
   void* Tb;      // tensor-core backward: T = (I + A)^{-1}, bf16 [max_chunks][Hv][64][64]
   void* dVn;     // tensor-core backward: dL/dVn, bf16 [max_chunks][Hv][64][DV]
-  void* dWb;     // tensor-core backward: dL/dW, bf16 [max_chunks][Hv][64][DK]
-  void* dKA;     // tensor-core backward: dk terms from the output/state path, bf16 [..][64][DK]
-  float* dgamA;  // tensor-core backward: d gamma terms from the output/state path, [..][64]
   float* dq_part;  // backward, Hv > Hk: [T_total][Hv][DK]
   float* dk_part;  // backward, Hv > Hk: [T_total][Hv][DK]
 };

@@ -1,22 +1,23 @@
 // gdr_tc_bwd.cu -- tcgen05 backward of the chunked gated delta rule (bf16, DK = DV = 128).
 //
 // The backward (the fused backward of FlashQLA PR #34, which walks the chunks in
-// reverse carrying the state gradient dh) runs as four stages here:
+// reverse carrying the state gradient dh) runs as three stages here:
 //   prep   (gdr_tc.cu) W, U, P, gamma and T of every chunk, chunk-parallel.
 //   walk   one CTA per (sequence, v-head, 64-wide DV slice), chunks in reverse; dh
 //          (dL/dh at the chunk end, "dh'") stays in registers:
 //            dVn = scale P^T dO + diag(e^{gamma_C - gamma}) K dh'
 //            dh  = e^{gamma_C} dh' + scale Q^T diag(e^gamma) dO - W^T dVn
 //          writes dh' and dVn of every chunk (bf16) and dS0.
-//   gradA  one CTA per (chunk, v-head): the terms that need h and dh':
+//   grad   one CTA per (chunk, v-head), everything on chip:
 //            Vn = U - W h,  dP = scale (dO Vn^T) * Gam,
 //            dq = scale diag(e^gamma) dO h^T + dP K,
-//            dk_A = dP^T Q + diag(e^{gamma_C - gamma}) Vn dh'^T,  dW = -dVn h^T,
-//          and the gate-gradient terms of the output and state paths.
-//   gradB  one CTA per (chunk, v-head): the WY backward through W = T' K, U = T'' V,
-//          T = (I + A)^{-1}:  dT = dW B_k^T + dVn B_v^T, dB_k = T^T dW, dB_v = T^T dVn,
-//          dA = -strict-lower(T^T dT T^T); then dv, dk, dbeta and dg (in-chunk
-//          reverse cumsum of d gamma).
+//            dk = dP^T Q + diag(e^{gamma_C - gamma}) Vn dh'^T + ...,  dW = -dVn h^T,
+//          then the WY backward through W = T' K, U = T'' V, T = (I + A)^{-1}:
+//            dT = dW B_k^T + dVn B_v^T, dB_v = T^T dVn, dA = -strict-lower(T^T dT T^T),
+//            <dB_k[s], k_s> = sum_m T[m][s] (dW K^T)[m][s],
+//            dk += T'^T dW + diag(beta)(dA * Gam) K + (dA * Gam)^T diag(beta) K,
+//          and dv, dbeta, dg (in-chunk reverse cumsum of d gamma).  dk stays in TMEM
+//          from its first term to its last.
 // No floating-point atomics anywhere: every reduction has a fixed order, so the
 // backward is bitwise deterministic.
 #include <cudaTypedefs.h>
@@ -215,47 +216,52 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
 }
 
 // ---------------------------------------------------------------------------------
-// gradA
+// grad: all gradients of one (chunk, v-head)
 // ---------------------------------------------------------------------------------
-struct GradASmem {
-  static constexpr uint32_t KQ = 0;             // [K | Q] x 2 slabs (32 KB)
-  static constexpr uint32_t DO = 32768;         // dO, 2 slabs (16 KB)
-  static constexpr uint32_t W = 49152;          // W (16 KB); later Vn~ = diag(e^{gC-gamma}) Vn
-  static constexpr uint32_t DVN = 65536;        // dVn (16 KB)
-  static constexpr uint32_t DH = 81920;         // dh' bf16, rows dk, 2 slabs of 16 KB (32 KB)
-  static constexpr uint32_t H = 114688;         // h bf16, rows dk, 2 slabs of 16 KB (32 KB); later dP
-  static constexpr uint32_t VN = 147456;        // Vn (16 KB)
-  static constexpr uint32_t OH = 163840;        // scale diag(e^gamma) dO (16 KB)
-  static constexpr uint32_t UT = 180224;        // U (16 KB)
-  static constexpr uint32_t SCR = UT + 16384;   // fp32 [64][65]
+// Shared memory (1024-aligned tiles; later users of a tile noted after the arrow).
+struct GradSmem {
+  static constexpr uint32_t KQ = 0;             // [K | Q] x 2 slabs (32 KB), to the end
+  static constexpr uint32_t DO = 32768;         // dO (16 KB) -> dk staging
+  static constexpr uint32_t W = 49152;          // W (16 KB) -> Vn~ -> dv staging
+  static constexpr uint32_t DVN = 65536;        // dVn (16 KB), to the WY backward
+  static constexpr uint32_t DH = 81920;         // dh' (32 KB) -> dq staging
+  static constexpr uint32_t H = 114688;         // h fp32 lands in H|VN|OH (64 KB); h bf16 (32 KB)
+                                                //   -> dP | dT | X | dAGb (8 KB each)
+  static constexpr uint32_t VN = 147456;        // Vn (16 KB) -> T'
+  static constexpr uint32_t OH = 163840;        // scale diag(e^gamma) dO (16 KB) -> V
+  static constexpr uint32_t UT = 180224;        // U (16 KB) -> dW
+  static constexpr uint32_t SCR = 196608;       // fp32 [64][65] scratch for row/column sums
   static constexpr uint32_t GAM = SCR + 16640;  // gamma (256 B)
   static constexpr uint32_t BYTES = GAM + 256;
-  // stores are staged in tiles that are free by then: dW -> DVN, dk_A -> VN, dq -> OH
+  // V and T are fetched right after P2 into the O-hat tile and the last 8 KB of H (T is
+  // last read by the X T^T product, before dAGb is written there)
+  static constexpr uint32_t V = OH, T = H + 24576, DP = H, DT = H + 8192, XT = H + 16384, DAG = H + 24576;
+  static constexpr uint32_t TP = VN, DQS = DH, DVS = W, DKS = DO, DW = UT;
 };
 
 template <bool kGroup>
-__global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
+__global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_w,
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
     const __grid_constant__ CUtensorMap tm_dvn, const __grid_constant__ CUtensorMap tm_dh,
-    const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_dwb,
-    const __grid_constant__ CUtensorMap tm_dka, const __grid_constant__ CUtensorMap tm_dq,
-    const __grid_constant__ CUtensorMap tm_h, Dims d, bf16* __restrict__ dq, Workspace ws) {
+    const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_t,
+    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+    const __grid_constant__ CUtensorMap tm_dv, Dims d, const bf16* __restrict__ beta, bf16* __restrict__ dq,
+    bf16* __restrict__ dk, bf16* __restrict__ dv, float* __restrict__ dg, bf16* __restrict__ dbeta,
+    Workspace ws) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
-  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint64_t bar_tma, bar_tma2, bar_mma;
   __shared__ uint32_t tmem_slot;
-  __shared__ float s_rowpp[64], s_colpp[64], s_qh[64], s_kdv[64], s_red[4];
-  const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
+  __shared__ float s_beta[64], s_eg[64], s_dgam[64], s_colpp[64], s_colbk[64], s_colaa[64], s_red[4];
   const int tid = threadIdx.x, warp = tid >> 5, r = tid & 63;
-  const int4 ci = ws.chunks[c];
-  const int len = ci.z, t0 = ci.y;
-  if (len <= 0) return;
   const int Hv = d.Hv;
-  const size_t ch = (size_t)c * Hv + j;
+  using S = GradSmem;
 
   if (tid == 0) {
     tc::mbar_init(&bar_tma, 1);
+    tc::mbar_init(&bar_tma2, 1);
     tc::mbar_init(&bar_mma, 1);
     tc::fence_barrier_init();
   }
@@ -264,39 +270,53 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tb = tmem_slot;
+  // TMEM columns: [K K^T ; Q K^T] 0-63 (K K^T kept to the end); dq 256-383; dk 384-511.
+  const uint32_t C_KK = tb, C_DQ = tb + 256, C_DK = tb + 384;
   GDR_TRACE_INIT();
+  // Persistent: each CTA walks the (chunk, v-head) items w = blockIdx.x + k * gridDim.x,
+  // keeping its barriers, TMEM and (warm) instruction cache across items.
+  bool ok = true;
+  uint32_t item_par = 0;  // phase parity of bar_tma / bar_tma2 for the current item
+  const int n_items = d.max_chunks * Hv;
+  for (int witem = blockIdx.x; witem < n_items && ok; witem += gridDim.x) {
+  const int c = witem / Hv, j = witem % Hv, i = j / d.G;
+  const int4 ci = ws.chunks[c];
+  const int len = ci.z, t0 = ci.y;
+  if (len <= 0) continue;  // empty chunk slot (uniform across the CTA)
+  const size_t ch = (size_t)c * Hv + j;
   if (tid == 0) {
     uint64_t* bar = &bar_tma;
     tc::mbar_arrive_expect_tx(bar, 24 * kSlab + 256);
-    // h (fp32) as four 32-column slabs of 128 rows over the H, VN and OH tiles (64 KB),
-    // converted to the bf16 operand in place below
-    for (int q4 = 0; q4 < 4; ++q4)
-      tc::tma_load_2d(sm + GradASmem::H + q4 * 16384, &tm_h, bar, q4 * 32, (int)(ch * 128));
-    tc::bulk_load(sm + GradASmem::GAM, ws.gam + ch * 64, 256, bar);
-    tc::tma_load_2d(sm + GradASmem::UT, &tm_u, bar, 0, (int)(ch * 64));
-    tc::tma_load_2d(sm + GradASmem::UT + kSlab, &tm_u, bar, 64, (int)(ch * 64));
-    tc::tma_load_3d(sm + GradASmem::KQ, &tm_k, bar, 0, i, t0);
-    tc::tma_load_3d(sm + GradASmem::KQ + 2 * kSlab, &tm_k, bar, 64, i, t0);
-    tc::tma_load_3d(sm + GradASmem::KQ + kSlab, &tm_q, bar, 0, i, t0);
-    tc::tma_load_3d(sm + GradASmem::KQ + 3 * kSlab, &tm_q, bar, 64, i, t0);
-    tc::tma_load_3d(sm + GradASmem::DO, &tm_do, bar, 0, j, t0);
-    tc::tma_load_3d(sm + GradASmem::DO + kSlab, &tm_do, bar, 64, j, t0);
-    tc::tma_load_2d(sm + GradASmem::W, &tm_w, bar, 0, (int)(ch * 64));
-    tc::tma_load_2d(sm + GradASmem::W + kSlab, &tm_w, bar, 64, (int)(ch * 64));
-    tc::tma_load_2d(sm + GradASmem::DVN, &tm_dvn, bar, 0, (int)(ch * 64));
-    tc::tma_load_2d(sm + GradASmem::DVN + kSlab, &tm_dvn, bar, 64, (int)(ch * 64));
-    for (int q4 = 0; q4 < 4; ++q4)  // dh' rows (q4 & 1) * 64.., columns (q4 >> 1) * 64..
-      tc::tma_load_2d(sm + GradASmem::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
+    tc::bulk_load(sm + S::GAM, ws.gam + ch * 64, 256, bar);
+    tc::tma_load_3d(sm + S::KQ, &tm_k, bar, 0, i, t0);
+    tc::tma_load_3d(sm + S::KQ + 2 * kSlab, &tm_k, bar, 64, i, t0);
+    tc::tma_load_3d(sm + S::KQ + kSlab, &tm_q, bar, 0, i, t0);
+    tc::tma_load_3d(sm + S::KQ + 3 * kSlab, &tm_q, bar, 64, i, t0);
+    tc::tma_load_3d(sm + S::DO, &tm_do, bar, 0, j, t0);
+    tc::tma_load_3d(sm + S::DO + kSlab, &tm_do, bar, 64, j, t0);
+    tc::tma_load_2d(sm + S::W, &tm_w, bar, 0, (int)(ch * 64));
+    tc::tma_load_2d(sm + S::W + kSlab, &tm_w, bar, 64, (int)(ch * 64));
+    tc::tma_load_2d(sm + S::DVN, &tm_dvn, bar, 0, (int)(ch * 64));
+    tc::tma_load_2d(sm + S::DVN + kSlab, &tm_dvn, bar, 64, (int)(ch * 64));
+    tc::tma_load_2d(sm + S::UT, &tm_u, bar, 0, (int)(ch * 64));
+    tc::tma_load_2d(sm + S::UT + kSlab, &tm_u, bar, 64, (int)(ch * 64));
+    for (int q4 = 0; q4 < 4; ++q4) {  // dh' rows (q4 & 1) * 64.., columns (q4 >> 1) * 64..
+      tc::tma_load_2d(sm + S::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
                       (int)(ch * 128 + (q4 & 1) * 64));
+      // h (fp32) as four 32-column slabs of 128 rows over H|VN|OH, converted in place below
+      tc::tma_load_2d(sm + S::H + q4 * 16384, &tm_h, bar, q4 * 32, (int)(ch * 128));
+    }
   }
-  bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma, 0, ws.status, kDevErrTimeoutBwd));
-  GDR_TRACE_MARK(2, 0);
-  const float* sgam = reinterpret_cast<const float*>(sm + GradASmem::GAM);
+  if (tid < 64) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * Hv + j]) : 0.f;
+  ok = __syncthreads_and(tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutBwd));
+  const float* sgam = reinterpret_cast<const float*>(sm + S::GAM);
+  if (tid < 64) s_eg[tid] = fexp(sgam[tid]);
   const float gC = sgam[len - 1], gr = sgam[r];
-  const float dec = fexp(gC - gr), eg = fexp(gr);
-  // h row `tid`: fp32 slabs (32 columns each) -> bf16 operand slabs (64 columns each).
-  // bf16 slab s overwrites fp32 slab s, so each half is read completely (and the
-  // barrier passed) before it is written.  <dh', h> is accumulated on the way.
+  const float dec = fexp(gC - gr);
+  GDR_TRACE_MARK(2, 0);
+
+  // h row `tid`: fp32 slabs (32 columns) -> bf16 operand slabs (64 columns) in place;
+  // <dh', h> accumulated on the way.
   float hdh = 0.f;
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
@@ -304,74 +324,79 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
     if (ok) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const unsigned char* src = sm + GradASmem::H + (2 * half + q) * 16384 + tid * 128;
+        const unsigned char* src = sm + S::H + (2 * half + q) * 16384 + tid * 128;
 #pragma unroll
-        for (int ch4 = 0; ch4 < 8; ++ch4) {
-          const float4 f = *reinterpret_cast<const float4*>(src + (((ch4 ^ (tid & 7)) & 7) << 4));
-          hv[q * 32 + 4 * ch4] = f.x; hv[q * 32 + 4 * ch4 + 1] = f.y;
-          hv[q * 32 + 4 * ch4 + 2] = f.z; hv[q * 32 + 4 * ch4 + 3] = f.w;
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 f = *reinterpret_cast<const float4*>(src + (((c4 ^ (tid & 7)) & 7) << 4));
+          hv[q * 32 + 4 * c4] = f.x; hv[q * 32 + 4 * c4 + 1] = f.y;
+          hv[q * 32 + 4 * c4 + 2] = f.z; hv[q * 32 + 4 * c4 + 3] = f.w;
         }
       }
-      ld_row_bf16(sm + GradASmem::DH + half * 16384, tid, dv_);
+      ld_row_bf16(sm + S::DH + half * 16384, tid, dv_);
 #pragma unroll
       for (int b = 0; b < 64; ++b) hdh += hv[b] * dv_[b];
     }
     __syncthreads();
-    if (ok) st_row_bf16(sm + GradASmem::H + half * 16384, tid, hv);
+    if (ok) st_row_bf16(sm + S::H + half * 16384, tid, hv);
   }
   hdh = block_sum128(hdh, s_red);
-  GDR_TRACE_MARK(2, 1);
   if (ok && tid < 64) {  // O-hat = scale diag(e^gamma) dO, zero past the chunk end
     float x[64];
-    const float e = r < len ? d.scale * eg : 0.f;
+    const float e = r < len ? d.scale * s_eg[r] : 0.f;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      ld_row_bf16(sm + GradASmem::DO + half * kSlab, r, x);
+      ld_row_bf16(sm + S::DO + half * kSlab, r, x);
 #pragma unroll
       for (int b = 0; b < 64; ++b) x[b] *= e;
-      st_row_bf16(sm + GradASmem::OH + half * kSlab, r, x);
+      st_row_bf16(sm + S::OH + half * kSlab, r, x);
     }
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
-  // Ph2: [KK;QK] (cols 0-63), W h (64-191), O-hat h^T (192-319), dVn h^T (320-447)
+  GDR_TRACE_MARK(2, 1);
+  // P2: [K;Q] K^T (0-63), W h (64-191), O-hat h^T -> dq (256-383), dVn h^T = -dW (384-511)
   if (ok && tid == 0) {
     tc::tc_fence_after();
-    tc::gemm(tb, kmaj(sm + GradASmem::KQ, 2 * kSlab), kmaj(sm + GradASmem::KQ, 2 * kSlab), 64, 8, false);
-    tc::gemm(tb + 64, kmaj(sm + GradASmem::W, kSlab), mnmaj(sm + GradASmem::H, 16384), 128, 8, false);
-    tc::gemm(tb + 192, kmaj(sm + GradASmem::OH, kSlab), kmaj(sm + GradASmem::H, 16384), 128, 8, false);
-    tc::gemm(tb + 320, kmaj(sm + GradASmem::DVN, kSlab), kmaj(sm + GradASmem::H, 16384), 128, 8, false);
+    tc::gemm(C_KK, kmaj(sm + S::KQ, 2 * kSlab), kmaj(sm + S::KQ, 2 * kSlab), 64, 8, false);
+    tc::gemm(tb + 64, kmaj(sm + S::W, kSlab), mnmaj(sm + S::H, 16384), 128, 8, false);
+    tc::gemm(C_DQ, kmaj(sm + S::OH, kSlab), kmaj(sm + S::H, 16384), 128, 8, false);
+    tc::gemm(C_DK, kmaj(sm + S::DVN, kSlab), kmaj(sm + S::H, 16384), 128, 8, false);
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
-  GDR_TRACE_MARK(2, 2);
   tc::tc_fence_after();
-  float* scr = reinterpret_cast<float*>(sm + GradASmem::SCR);
+  GDR_TRACE_MARK(2, 2);
+  if (ok && tid == 0) {  // O-hat and h are consumed: fetch V and T for the WY backward
+    tc::mbar_arrive_expect_tx(&bar_tma2, 3 * kSlab);
+    tc::tma_load_3d(sm + S::V, &tm_v, &bar_tma2, 0, j, t0);
+    tc::tma_load_3d(sm + S::V + kSlab, &tm_v, &bar_tma2, 64, j, t0);
+    tc::tma_load_2d(sm + S::T, &tm_t, &bar_tma2, 0, (int)(ch * 64));
+  }
+  float* scr = reinterpret_cast<float*>(sm + S::SCR);
+  float qh = 0.f;
   if (ok) {
     if (tid < 64) {
       float x[64], u[64];
-      float qh = 0.f;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         tmem_ld64(tb, warp, 64 + half * 64, x);  // (W h)[r]
-        ld_row_bf16(sm + GradASmem::UT + half * kSlab, r, u);
+        ld_row_bf16(sm + S::UT + half * kSlab, r, u);
 #pragma unroll
         for (int b = 0; b < 64; ++b) u[b] = r < len ? u[b] - x[b] : 0.f;
-        st_row_bf16(sm + GradASmem::VN + half * kSlab, r, u);
+        st_row_bf16(sm + S::VN + half * kSlab, r, u);
 #pragma unroll
         for (int b = 0; b < 64; ++b) u[b] *= dec;
-        st_row_bf16(sm + GradASmem::W + half * kSlab, r, u);  // Vn~ (W no longer needed)
-        tmem_ld64(tb, warp, 192 + half * 64, x);            // (O-hat h^T)[r]
-        ld_row_bf16(sm + GradASmem::KQ + kSlab + half * 2 * kSlab, r, u);  // q_r
+        st_row_bf16(sm + S::W + half * kSlab, r, u);  // Vn~ (W no longer needed)
+        tmem_ld64(tb, warp, 256 + half * 64, x);  // (O-hat h^T)[r]
+        ld_row_bf16(sm + S::KQ + kSlab + half * 2 * kSlab, r, u);  // q_r
 #pragma unroll
         for (int b = 0; b < 64; ++b) qh += x[b] * u[b];
-        tmem_ld64(tb, warp, 320 + half * 64, x);  // (dVn h^T)[r] = -dW[r]
+        tmem_ld64(tb, warp, 384 + half * 64, x);  // -dW[r]
 #pragma unroll
         for (int b = 0; b < 64; ++b) x[b] = -x[b];
-        st_row_bf16(sm + GradASmem::DVN + half * kSlab, r, x);  // dVn tile is free after Ph2
+        st_row_bf16(sm + S::DW + half * kSlab, r, x);  // own U row half already consumed
       }
-      s_qh[r] = qh;
     } else {  // Q K^T rows -> scratch (fp32)
       float x[64];
       tmem_ld64(tb, warp, 0, x);
@@ -383,83 +408,80 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
   tc::tc_fence_before();
   __syncthreads();
   GDR_TRACE_MARK(2, 3);
-  // Ph4: dO Vn^T (cols 0-63), K dh' (64-191), Vn~ dh'^T (320-447); dq stays in 192-319
+  // P4: dO Vn^T (64-127), K dh' (128-255), dk = Vn~ dh'^T (384-511)
   if (ok && tid == 0) {
-    tc::tma_store_2d(&tm_dwb, sm + GradASmem::DVN, 0, (int)(ch * 64));
-    tc::tma_store_2d(&tm_dwb, sm + GradASmem::DVN + kSlab, 64, (int)(ch * 64));
-    tc::bulk_commit();
     tc::tc_fence_after();
-    tc::gemm(tb, kmaj(sm + GradASmem::DO, kSlab), kmaj(sm + GradASmem::VN, kSlab), 64, 8, false);
-    tc::gemm(tb + 64, kmaj(sm + GradASmem::KQ, 2 * kSlab), mnmaj(sm + GradASmem::DH, 16384), 128, 8, false);
-    tc::gemm(tb + 320, kmaj(sm + GradASmem::W, kSlab), kmaj(sm + GradASmem::DH, 16384), 128, 8, false);
+    tc::gemm(tb + 64, kmaj(sm + S::DO, kSlab), kmaj(sm + S::VN, kSlab), 64, 8, false);
+    tc::gemm(tb + 128, kmaj(sm + S::KQ, 2 * kSlab), mnmaj(sm + S::DH, 16384), 128, 8, false);
+    tc::gemm(C_DK, kmaj(sm + S::W, kSlab), kmaj(sm + S::DH, 16384), 128, 8, false);
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
-  GDR_TRACE_MARK(2, 4);
   tc::tc_fence_after();
+  GDR_TRACE_MARK(2, 4);
+  float rowpp = 0.f, kdv = 0.f;
   if (ok && tid < 64) {
-    float x[64], v[64];
-    GDR_TRACE_MARK(2, 10);
-    tmem_ld64(tb, warp, 0, x);  // (dO Vn^T)[r]
-    GDR_TRACE_MARK(2, 11);
-    float rowpp = 0.f;
-    float gs[64], qk[64];  // all smem loads first: the compiler cannot prove the tiles do not alias
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {  // 32 columns at a time (register pressure)
+      float x[32], gs[32], qk[32];
+      tmem_ld32w(tb, warp, 64 + 32 * hf, x);  // (dO Vn^T)[r]
 #pragma unroll
-    for (int s = 0; s < 64; ++s) {
-      gs[s] = sgam[s];
-      qk[s] = scr[r * 65 + s];
+      for (int s = 0; s < 32; ++s) {
+        gs[s] = sgam[32 * hf + s];
+        qk[s] = scr[r * 65 + 32 * hf + s];
+      }
+#pragma unroll
+      for (int s = 0; s < 32; ++s) {
+        const int sc = 32 * hf + s;
+        const float dp = (sc <= r && r < len) ? d.scale * x[s] * fexp(gr - gs[s]) : 0.f;
+        x[s] = dp;
+        qk[s] *= dp;
+        rowpp += qk[s];
+      }
+#pragma unroll
+      for (int s = 0; s < 32; ++s) scr[r * 65 + 32 * hf + s] = qk[s];
+      st_halfrow_bf16(sm + S::DP, r, hf, x);  // dP (h no longer needed)
     }
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {  // (K dh')[r] . Vn[r], 32 columns at a time
+      float x[32], v[32];
+      tmem_ld32w(tb, warp, 128 + 32 * q, x);
+      ld_halfrow_bf16(sm + S::VN + (q >> 1) * kSlab, r, q & 1, v);
 #pragma unroll
-    for (int s = 0; s < 64; ++s) {
-      const float dp = (s <= r && r < len) ? d.scale * x[s] * fexp(gr - gs[s]) : 0.f;
-      x[s] = dp;
-      qk[s] *= dp;
-      rowpp += qk[s];
+      for (int b = 0; b < 32; ++b) kdv += x[b] * v[b];
     }
-    GDR_TRACE_MARK(2, 12);
-#pragma unroll
-    for (int s = 0; s < 64; ++s) scr[r * 65 + s] = qk[s];
-    s_rowpp[r] = rowpp;
-    GDR_TRACE_MARK(2, 13);
-    st_row_bf16(sm + GradASmem::H, r, x);  // dP (h no longer needed)
-    float kdv = 0.f;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tmem_ld64(tb, warp, 64 + half * 64, x);  // (K dh')[r]
-      ld_row_bf16(sm + GradASmem::VN + half * kSlab, r, v);
-#pragma unroll
-      for (int b = 0; b < 64; ++b) kdv += x[b] * v[b];
-    }
-    s_kdv[r] = r < len ? kdv : 0.f;
-    const float part = warp_sum(r < len ? dec * kdv : 0.f);  // e^{gC - g_r} k_r^T dh' vn_r
+    kdv = r < len ? kdv : 0.f;
+    const float part = warp_sum(dec * kdv);  // sum_s e^{gC - g_s} k_s^T dh' vn_s
     if ((tid & 31) == 0) s_red[tid >> 5] = part;
-    GDR_TRACE_MARK(2, 14);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
-  GDR_TRACE_MARK(2, 15);
   if (ok && tid < 64) {
     float cs = 0.f;
     for (int rr = 0; rr < 64; ++rr) cs += scr[rr * 65 + tid];
     s_colpp[tid] = cs;
   }
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_tma2, item_par, ws.status, kDevErrTimeoutBwd));
   GDR_TRACE_MARK(2, 5);
-  // Ph6: dq += dP K (cols 192-319), dk_A += dP^T Q (cols 320-447)
+  // P6: dq += dP K, dk += dP^T Q, dW K^T (64-127), dVn V^T (128-191)
   if (ok && tid == 0) {
     tc::tc_fence_after();
-    tc::gemm(tb + 192, kmaj(sm + GradASmem::H, kSlab), mnmaj(sm + GradASmem::KQ, 2 * kSlab), 128, 4, true);
-    tc::gemm(tb + 320, mnmaj(sm + GradASmem::H, kSlab), mnmaj(sm + GradASmem::KQ + kSlab, 2 * kSlab), 128, 4, true);
+    tc::gemm(C_DQ, kmaj(sm + S::DP, kSlab), mnmaj(sm + S::KQ, 2 * kSlab), 128, 4, true);
+    tc::gemm(C_DK, mnmaj(sm + S::DP, kSlab), mnmaj(sm + S::KQ + kSlab, 2 * kSlab), 128, 4, true);
+    tc::gemm(tb + 64, kmaj(sm + S::DW, kSlab), kmaj(sm + S::KQ, 2 * kSlab), 64, 8, false);
+    tc::gemm(tb + 128, kmaj(sm + S::DVN, kSlab), kmaj(sm + S::V, kSlab), 64, 8, false);
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
-  GDR_TRACE_MARK(2, 6);
   tc::tc_fence_after();
+  GDR_TRACE_MARK(2, 6);
   if (ok && tid < 64) {
-    float x[64];
+    float x[64], y[64];
+    // dq (final for one v-head per q/k head)
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      tmem_ld64(tb, warp, 192 + half * 64, x);
+      tmem_ld64(tb, warp, 256 + half * 64, x);
       if (kGroup) {
         if (r < len) {
           float* dst = ws.dq_part + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64;
@@ -467,227 +489,121 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradA_kernel(
           for (int b = 0; b < 64; b += 4) *reinterpret_cast<float4*>(dst + b) = make_float4(x[b], x[b + 1], x[b + 2], x[b + 3]);
         }
       } else if (len == 64) {
-        st_row_bf16(sm + GradASmem::OH + half * kSlab, r, x);  // full chunk: TMA store below
+        st_row_bf16(sm + S::DQS + half * kSlab, r, x);
       } else if (r < len) {
         st_global_bf16x64(dq + ((size_t)(t0 + r) * d.Hk + i) * 128 + half * 64, x);
       }
-      tmem_ld64(tb, warp, 320 + half * 64, x);
-      st_row_bf16(sm + GradASmem::VN + half * kSlab, r, x);
     }
-    float dga = 0.f;
-    if (r < len) {
-      dga = s_rowpp[r] - s_colpp[r] + s_qh[r] - dec * s_kdv[r];
-      if (r == len - 1) dga += fexp(gC) * hdh + (s_red[0] + s_red[1]);
-    }
-    ws.dgamA[ch * 64 + r] = dga;
   }
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before();
-  __syncthreads();
-  if (ok && tid == 0) {
-    tc::tma_store_2d(&tm_dka, sm + GradASmem::VN, 0, (int)(ch * 64));
-    tc::tma_store_2d(&tm_dka, sm + GradASmem::VN + kSlab, 64, (int)(ch * 64));
-    if (!kGroup && len == 64) {
-      tc::tma_store_3d(&tm_dq, sm + GradASmem::OH, 0, i, t0);
-      tc::tma_store_3d(&tm_dq, sm + GradASmem::OH + kSlab, 64, i, t0);
-    }
-    tc::bulk_commit();
-  }
-  if (tid == 0) tc::bulk_wait_read<0>();  // smem sources read before exit
-  GDR_TRACE_MARK(2, 7);
-  if (warp == 0) tc::tmem_dealloc(tb, 512);
-}
-
-// ---------------------------------------------------------------------------------
-// gradB
-// ---------------------------------------------------------------------------------
-struct GradBSmem {
-  static constexpr uint32_t K = 0;         // K, 2 slabs (16 KB)
-  static constexpr uint32_t V = 16384;     // V, 2 slabs (16 KB)
-  static constexpr uint32_t T = 32768;     // T bf16 [64][64] (8 KB)
-  static constexpr uint32_t TP = 40960;    // T' = T diag(beta e^gamma) (8 KB)
-  static constexpr uint32_t DW = 49152;    // dW, 2 slabs (16 KB)
-  static constexpr uint32_t DVN = 65536;   // dVn, 2 slabs (16 KB)
-  static constexpr uint32_t DT = 81920;    // dT (8 KB)
-  static constexpr uint32_t X = 90112;     // T^T dT (8 KB)
-  static constexpr uint32_t DAG = 98304;   // diag(beta) (dA * Gam) (8 KB)
-  static constexpr uint32_t KA = 106496;   // dk_A from gradA (16 KB)
-  static constexpr uint32_t SCR = 122880;  // fp32 [64][65]
-  static constexpr uint32_t GAM = SCR + 16640;
-  static constexpr uint32_t BYTES = GAM + 256;
-  // dv rows are staged in the V tile and dk rows in the K tile once those are consumed
-};
-
-template <bool kGroup>
-__global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
-    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-    const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_dw,
-    const __grid_constant__ CUtensorMap tm_dvn, const __grid_constant__ CUtensorMap tm_dka,
-    const __grid_constant__ CUtensorMap tm_dv, const __grid_constant__ CUtensorMap tm_dk, Dims d,
-    const bf16* __restrict__ beta, bf16* __restrict__ dk,
-    bf16* __restrict__ dv, float* __restrict__ dg, bf16* __restrict__ dbeta, Workspace ws) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = align1024(smem_raw);
-  __shared__ uint64_t bar_tma, bar_mma;
-  __shared__ uint32_t tmem_slot;
-  __shared__ float s_beta[64], s_dgam[64], s_colaa[64], s_eg[64];
-  const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
-  const int tid = threadIdx.x, warp = tid >> 5, r = tid & 63;
-  const int4 ci = ws.chunks[c];
-  const int len = ci.z, t0 = ci.y;
-  if (len <= 0) return;
-  const int Hv = d.Hv;
-  const size_t ch = (size_t)c * Hv + j;
-
-  if (tid == 0) {
-    tc::mbar_init(&bar_tma, 1);
-    tc::mbar_init(&bar_mma, 1);
-    tc::fence_barrier_init();
-  }
-  if (warp == 0) tc::tmem_alloc(&tmem_slot, 512);
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tb = tmem_slot;
-  GDR_TRACE_INIT();
-  if (tid == 0) {
-    uint64_t* bar = &bar_tma;
-    tc::mbar_arrive_expect_tx(bar, 11 * kSlab + 256);
-    tc::bulk_load(sm + GradBSmem::GAM, ws.gam + ch * 64, 256, bar);
-    tc::tma_load_2d(sm + GradBSmem::KA, &tm_dka, bar, 0, (int)(ch * 64));
-    tc::tma_load_2d(sm + GradBSmem::KA + kSlab, &tm_dka, bar, 64, (int)(ch * 64));
-    tc::tma_load_3d(sm + GradBSmem::K, &tm_k, bar, 0, i, t0);
-    tc::tma_load_3d(sm + GradBSmem::K + kSlab, &tm_k, bar, 64, i, t0);
-    tc::tma_load_3d(sm + GradBSmem::V, &tm_v, bar, 0, j, t0);
-    tc::tma_load_3d(sm + GradBSmem::V + kSlab, &tm_v, bar, 64, j, t0);
-    tc::tma_load_2d(sm + GradBSmem::T, &tm_t, bar, 0, (int)(ch * 64));
-    tc::tma_load_2d(sm + GradBSmem::DW, &tm_dw, bar, 0, (int)(ch * 64));
-    tc::tma_load_2d(sm + GradBSmem::DW + kSlab, &tm_dw, bar, 64, (int)(ch * 64));
-    tc::tma_load_2d(sm + GradBSmem::DVN, &tm_dvn, bar, 0, (int)(ch * 64));
-    tc::tma_load_2d(sm + GradBSmem::DVN + kSlab, &tm_dvn, bar, 64, (int)(ch * 64));
-  }
-  if (tid < 64) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * Hv + j]) : 0.f;
-  bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma, 0, ws.status, kDevErrTimeoutBwd));
-  GDR_TRACE_MARK(3, 0);
-  const float* sgam = reinterpret_cast<const float*>(sm + GradBSmem::GAM);
-  if (tid < 64) s_eg[tid] = fexp(sgam[tid]);
-  __syncthreads();
-  const float gr = sgam[r], eg = s_eg[r], br = s_beta[r];
-  if (ok && tid < 64) {  // T' row r = T[r][:] * beta e^gamma (per column)
-    float x[64];
-    ld_row_bf16(sm + GradBSmem::T, r, x);
+  if (ok && tid < 64) {
+    // dT = dW B_k^T + dVn B_v^T = (dW K^T) diag(beta e^gamma) + (dVn V^T) diag(beta);
+    // T * (dW K^T) (row r) for <dB_k[s], k_s> = sum_m T[m][s] (dW K^T)[m][s]
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+      float x[32], y[32], tr[32];
+      tmem_ld32w(tb, warp, 64 + 32 * hf, x);
+      tmem_ld32w(tb, warp, 128 + 32 * hf, y);
+      ld_halfrow_bf16(sm + S::T, r, hf, tr);
 #pragma unroll
-    for (int s = 0; s < 64; ++s) x[s] *= s_beta[s] * s_eg[s];
-    st_row_bf16(sm + GradBSmem::TP, r, x);
+      for (int s = 0; s < 32; ++s) {
+        const int sc = 32 * hf + s;
+        const float be = s_beta[sc] * s_eg[sc];
+        scr[r * 65 + sc] = tr[s] * x[s];
+        y[s] = (r < len && sc < len) ? be * x[s] + s_beta[sc] * y[s] : 0.f;
+        tr[s] *= be;  // T' = T diag(beta e^gamma)
+      }
+      st_halfrow_bf16(sm + S::DT, r, hf, y);
+      st_halfrow_bf16(sm + S::TP, r, hf, tr);
+    }
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
-  GDR_TRACE_MARK(3, 1);
-  // R1: K K^T (0-63), dW K^T (64-127), dVn V^T (128-191), T^T dW (192-319), T^T dVn (320-447)
+  if (ok && tid < 64) {
+    float cs = 0.f;
+    for (int rr = 0; rr < 64; ++rr) cs += scr[rr * 65 + tid];
+    s_colbk[tid] = cs;
+  }
+  GDR_TRACE_MARK(2, 7);
+  // R2: T^T dVn = dB_v (128-255), X = T^T dT (64-127)
   if (ok && tid == 0) {
+    if (!kGroup && len == 64) {
+      tc::tma_store_3d(&tm_dq, sm + S::DQS, 0, i, t0);
+      tc::tma_store_3d(&tm_dq, sm + S::DQS + kSlab, 64, i, t0);
+      tc::bulk_commit();
+    }
     tc::tc_fence_after();
-    tc::gemm(tb, kmaj(sm + GradBSmem::K, kSlab), kmaj(sm + GradBSmem::K, kSlab), 64, 8, false);
-    tc::gemm(tb + 64, kmaj(sm + GradBSmem::DW, kSlab), kmaj(sm + GradBSmem::K, kSlab), 64, 8, false);
-    tc::gemm(tb + 128, kmaj(sm + GradBSmem::DVN, kSlab), kmaj(sm + GradBSmem::V, kSlab), 64, 8, false);
-    tc::gemm(tb + 192, mnmaj(sm + GradBSmem::T, kSlab), mnmaj(sm + GradBSmem::DW, kSlab), 128, 4, false);
-    tc::gemm(tb + 320, mnmaj(sm + GradBSmem::T, kSlab), mnmaj(sm + GradBSmem::DVN, kSlab), 128, 4, false);
+    tc::gemm(tb + 128, mnmaj(sm + S::T, kSlab), mnmaj(sm + S::DVN, kSlab), 128, 4, false);
+    tc::gemm(tb + 64, mnmaj(sm + S::T, kSlab), mnmaj(sm + S::DT, kSlab), 64, 4, false);
     tc::mma_commit(&bar_mma);
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
-  GDR_TRACE_MARK(3, 2);
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
-  float* scr = reinterpret_cast<float*>(sm + GradBSmem::SCR);
-  float dbk = 0.f, dbv = 0.f;
+  GDR_TRACE_MARK(2, 8);
+  float dbv = 0.f;
   if (ok && tid < 64) {
     float x[64], y[64];
-    tmem_ld64(tb, warp, 0, x);  // K K^T row r
-#pragma unroll
-    for (int s = 0; s < 64; ++s) scr[r * 65 + s] = x[s];
-    tmem_ld64(tb, warp, 64, x);   // (dW K^T)[r]
-    tmem_ld64(tb, warp, 128, y);  // (dVn V^T)[r]
-#pragma unroll
-    for (int s = 0; s < 64; ++s)
-      x[s] = (r < len && s < len) ? s_beta[s] * (s_eg[s] * x[s] + y[s]) : 0.f;
-    st_row_bf16(sm + GradBSmem::DT, r, x);
+    const float br = s_beta[r];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      tmem_ld64(tb, warp, 192 + half * 64, x);  // dB_k[r]
-      ld_row_bf16(sm + GradBSmem::K + half * kSlab, r, y);
-#pragma unroll
-      for (int b = 0; b < 64; ++b) dbk += x[b] * y[b];
-      tmem_ld64(tb, warp, 320 + half * 64, x);  // dB_v[r]
-      ld_row_bf16(sm + GradBSmem::V + half * kSlab, r, y);
+      tmem_ld64(tb, warp, 128 + half * 64, x);  // dB_v[r]
+      ld_row_bf16(sm + S::V + half * kSlab, r, y);
 #pragma unroll
       for (int b = 0; b < 64; ++b) {
         dbv += x[b] * y[b];
         x[b] *= br;
       }
       if (len == 64)
-        st_row_bf16(sm + GradBSmem::V + half * kSlab, r, x);  // own row of V already consumed
+        st_row_bf16(sm + S::DVS + half * kSlab, r, x);
       else if (r < len)
         st_global_bf16x64(dv + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64, x);
     }
+    tmem_ld64(tb, warp, 64, x);  // X = T^T dT
+    st_row_bf16(sm + S::XT, r, x);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
-  GDR_TRACE_MARK(3, 3);
-  // R2: X = T^T dT (cols 448-511)
+  GDR_TRACE_MARK(2, 9);
+  // R3: X T^T (64-127)
   if (ok && tid == 0) {
     if (len == 64) {
-      tc::tma_store_3d(&tm_dv, sm + GradBSmem::V, 0, j, t0);
-      tc::tma_store_3d(&tm_dv, sm + GradBSmem::V + kSlab, 64, j, t0);
+      tc::tma_store_3d(&tm_dv, sm + S::DVS, 0, j, t0);
+      tc::tma_store_3d(&tm_dv, sm + S::DVS + kSlab, 64, j, t0);
       tc::bulk_commit();
     }
     tc::tc_fence_after();
-    tc::gemm(tb + 448, mnmaj(sm + GradBSmem::T, kSlab), mnmaj(sm + GradBSmem::DT, kSlab), 64, 4, false);
-    tc::mma_commit(&bar_mma);
-  }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
-  GDR_TRACE_MARK(3, 4);
-  tc::tc_fence_after();
-  if (ok && tid < 64) {
-    float x[64];
-    tmem_ld64(tb, warp, 448, x);
-    st_row_bf16(sm + GradBSmem::X, r, x);
-  }
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before();
-  __syncthreads();
-  GDR_TRACE_MARK(3, 5);
-  // R3: X T^T (cols 0-63)
-  if (ok && tid == 0) {
-    tc::tc_fence_after();
-    tc::gemm(tb, kmaj(sm + GradBSmem::X, kSlab), kmaj(sm + GradBSmem::T, kSlab), 64, 4, false);
+    tc::gemm(tb + 64, kmaj(sm + S::XT, kSlab), kmaj(sm + S::T, kSlab), 64, 4, false);
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
-  GDR_TRACE_MARK(3, 6);
   tc::tc_fence_after();
+  GDR_TRACE_MARK(2, 10);
   float akk = 0.f, rowaa = 0.f;
   if (ok && tid < 64) {
-    float x[64];
-    tmem_ld64(tb, warp, 0, x);
-    float gs[64], kk[64];  // all smem loads first: the compiler cannot prove the tiles do not alias
+    const float br = s_beta[r];
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+      float x[32], gs[32], kk[32];
+      tmem_ld32w(tb, warp, 64 + 32 * hf, x);   // (T^T dT T^T)[r]
+      tmem_ld32w(tb, warp, 32 * hf, kk);       // K K^T row r
 #pragma unroll
-    for (int s = 0; s < 64; ++s) {
-      gs[s] = sgam[s];
-      kk[s] = scr[r * 65 + s];
+      for (int s = 0; s < 32; ++s) gs[s] = sgam[32 * hf + s];
+#pragma unroll
+      for (int s = 0; s < 32; ++s) {
+        const int sc = 32 * hf + s;
+        // exp(gamma_r - gamma_s) only below the diagonal: above it the exponent is
+        // positive and can overflow, and 0 * inf would give NaN
+        const float dag = (sc < r && r < len) ? -x[s] * fexp(gr - gs[s]) : 0.f;
+        akk += dag * kk[s];
+        x[s] = br * dag;
+        kk[s] *= x[s];  // dA * A with A = beta_r Gam K K^T
+        rowaa += kk[s];
+      }
+#pragma unroll
+      for (int s = 0; s < 32; ++s) scr[r * 65 + 32 * hf + s] = kk[s];
+      st_halfrow_bf16(sm + S::DAG, r, hf, x);
     }
-#pragma unroll
-    for (int s = 0; s < 64; ++s) {
-      // exp(gamma_r - gamma_s) only below the diagonal: above it the exponent is
-      // positive and can overflow, and 0 * inf would give NaN
-      const float dag = (s < r && r < len) ? -x[s] * fexp(gr - gs[s]) : 0.f;
-      akk += dag * kk[s];
-      x[s] = br * dag;
-      kk[s] *= x[s];  // dA * A with A = beta_r Gam K K^T
-      rowaa += kk[s];
-    }
-#pragma unroll
-    for (int s = 0; s < 64; ++s) scr[r * 65 + s] = kk[s];
-    st_row_bf16(sm + GradBSmem::DAG, r, x);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
@@ -697,26 +613,23 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
     for (int rr = 0; rr < 64; ++rr) cs += scr[rr * 65 + tid];
     s_colaa[tid] = cs;
   }
-  GDR_TRACE_MARK(3, 7);
-  // R4: dk_B = T'^T dW + dAGb K + dAGb^T K (cols 64-191)
+  GDR_TRACE_MARK(2, 11);
+  // R4: dk += T'^T dW + dAGb K + dAGb^T K
   if (ok && tid == 0) {
     tc::tc_fence_after();
-    tc::gemm(tb + 64, mnmaj(sm + GradBSmem::TP, kSlab), mnmaj(sm + GradBSmem::DW, kSlab), 128, 4, false);
-    tc::gemm(tb + 64, kmaj(sm + GradBSmem::DAG, kSlab), mnmaj(sm + GradBSmem::K, kSlab), 128, 4, true);
-    tc::gemm(tb + 64, mnmaj(sm + GradBSmem::DAG, kSlab), mnmaj(sm + GradBSmem::K, kSlab), 128, 4, true);
+    tc::gemm(C_DK, mnmaj(sm + S::TP, kSlab), mnmaj(sm + S::DW, kSlab), 128, 4, true);
+    tc::gemm(C_DK, kmaj(sm + S::DAG, kSlab), mnmaj(sm + S::KQ, 2 * kSlab), 128, 4, true);
+    tc::gemm(C_DK, mnmaj(sm + S::DAG, kSlab), mnmaj(sm + S::KQ, 2 * kSlab), 128, 4, true);
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
-  GDR_TRACE_MARK(3, 8);
   tc::tc_fence_after();
+  GDR_TRACE_MARK(2, 12);
   if (ok && tid < 64) {
-    float x[64], y[64];
+    float x[64];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
-      tmem_ld64(tb, warp, 64 + half * 64, x);
-      ld_row_bf16(sm + GradBSmem::KA + half * kSlab, r, y);
-#pragma unroll
-      for (int b = 0; b < 64; ++b) x[b] += y[b];
+      tmem_ld64(tb, warp, 384 + half * 64, x);
       if (kGroup) {
         if (r < len) {
           float* dst = ws.dk_part + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64;
@@ -724,22 +637,26 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
           for (int b = 0; b < 64; b += 4) *reinterpret_cast<float4*>(dst + b) = make_float4(x[b], x[b + 1], x[b + 2], x[b + 3]);
         }
       } else if (len == 64) {
-        st_row_bf16(sm + GradBSmem::K + half * kSlab, r, x);  // K tile is free after R4
+        st_row_bf16(sm + S::DKS + half * kSlab, r, x);
       } else if (r < len) {
         st_global_bf16x64(dk + ((size_t)(t0 + r) * d.Hk + i) * 128 + half * 64, x);
       }
     }
-    if (r < len) dbeta[(size_t)(t0 + r) * Hv + j] = __float2bfloat16_rn(eg * dbk + dbv + akk);
-    s_dgam[r] = r < len ? ws.dgamA[ch * 64 + r] + br * eg * dbk + rowaa - s_colaa[r] : 0.f;
+    const float br = s_beta[r], eg = s_eg[r];
+    if (r < len) dbeta[(size_t)(t0 + r) * Hv + j] = __float2bfloat16_rn(eg * s_colbk[r] + dbv + akk);
+    float dgm = 0.f;
+    if (r < len) {
+      dgm = rowpp - s_colpp[r] + qh - dec * kdv + br * eg * s_colbk[r] + rowaa - s_colaa[r];
+      if (r == len - 1) dgm += fexp(gC) * hdh + (s_red[0] + s_red[1]);
+    }
+    s_dgam[r] = dgm;
   }
   tc::fence_proxy_async_smem();
   __syncthreads();
-  if (ok && tid == 0) {
-    if (!kGroup && len == 64) {
-      tc::tma_store_3d(&tm_dk, sm + GradBSmem::K, 0, i, t0);
-      tc::tma_store_3d(&tm_dk, sm + GradBSmem::K + kSlab, 64, i, t0);
-      tc::bulk_commit();
-    }
+  if (ok && tid == 0 && !kGroup && len == 64) {
+    tc::tma_store_3d(&tm_dk, sm + S::DKS, 0, i, t0);
+    tc::tma_store_3d(&tm_dk, sm + S::DKS + kSlab, 64, i, t0);
+    tc::bulk_commit();
   }
   if (ok && tid < 64) {  // dg = in-chunk reverse cumsum of d gamma (rows >= len hold 0)
     const int lane = tid & 31;
@@ -757,8 +674,13 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_gradB_kernel(
     const float v = s_colaa[tid] + (tid >= 32 ? s_colaa[31] : 0.f);
     if (rr < len) dg[(size_t)(t0 + rr) * Hv + j] = v;
   }
-  if (tid == 0) tc::bulk_wait_read<0>();  // smem sources read before exit
-  GDR_TRACE_MARK(3, 9);
+  if (tid == 0) tc::bulk_wait_read<0>();  // staging tiles read before the next item's loads
+  GDR_TRACE_MARK(2, 13);
+  item_par ^= 1;
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  }  // items
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, 512);
@@ -781,16 +703,14 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
   if (Tt == 0 && d.num_seqs == 0) return cudaSuccess;
   cudaError_t e = tc_launch_prep(d, a.q, a.k, a.v, a.g, a.beta, ws, 1, s, "bwd_prep");
   if (e != cudaSuccess) return e;
-  CUtensorMap tq{}, tk{}, tv{}, tdo{}, tw{}, tp{}, tdvn{}, tdh{}, tt{}, tdw{}, tdhs{}, tu{}, tka{}, tdq{}, tdk{}, tdv{},
-      thf{};
+  CUtensorMap tq{}, tk{}, tv{}, tdo{}, tw{}, tp{}, tdvn{}, tdh{}, tt{}, tdhs{}, tu{}, tdq{}, tdk{}, tdv{}, thf{};
   if (Tt > 0) {  // with no tokens no kernel reads the maps (see tc_forward)
     if (!map_3d(&tq, a.q, 128, d.Hk, Tt) || !map_3d(&tk, a.k, 128, d.Hk, Tt) || !map_3d(&tv, a.v, 128, d.Hv, Tt) ||
         !map_3d(&tdo, a.dO, 128, d.Hv, Tt) || !map_2d(&tw, ws.W, 128, rows) || !map_2d(&tp, ws.P, 64, rows) ||
         !map_2d(&tdvn, ws.dVn, 128, rows) || !map_2d(&tdh, ws.dhp, 128, rows * 2) || !map_2d(&tt, ws.Tb, 64, rows) ||
-        !map_2d(&tdw, ws.dWb, 128, rows) ||
         !map_2d_box(&tdhs, ws.dhp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, rows * 2, 64, 128) ||
-        !map_2d(&tu, ws.U, 128, rows) || !map_2d(&tka, ws.dKA, 128, rows) || !map_3d(&tdq, a.dq, 128, d.Hk, Tt) ||
-        !map_3d(&tdk, a.dk, 128, d.Hk, Tt) || !map_3d(&tdv, a.dv, 128, d.Hv, Tt) ||
+        !map_2d(&tu, ws.U, 128, rows) || !map_3d(&tdq, a.dq, 128, d.Hk, Tt) || !map_3d(&tdk, a.dk, 128, d.Hk, Tt) ||
+        !map_3d(&tdv, a.dv, 128, d.Hv, Tt) ||
         !map_2d_box(&thf, a.h_saved, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, rows * 2, 32, 128))
       return cudaErrorInvalidValue;
   }
@@ -802,30 +722,24 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     stage_mark(s, "bwd_walk");
   }
   if (d.max_chunks > 0 && Tt > 0) {
-    const dim3 grid(d.max_chunks, d.Hv);
-    const size_t sma = GradASmem::BYTES + 1024, smb = GradBSmem::BYTES + 1024;
+    int dev = 0, n_sm = 1;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    const long long n_items = (long long)d.max_chunks * d.Hv;
+    const dim3 grid((unsigned)(n_items < n_sm ? n_items : n_sm));  // persistent: one CTA per SM
+    const size_t smg = GradSmem::BYTES + 1024;
     if (d.G > 1) {
-      cudaFuncSetAttribute(tc_bwd_gradA_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sma);
-      tc_bwd_gradA_kernel<true><<<grid, kTcThreads, sma, s>>>(tq, tk, tdo, tw, tdvn, tdh, tu, tdw, tka, tdq, thf, d,
-                                                               (bf16*)a.dq, ws);
+      cudaFuncSetAttribute(tc_bwd_grad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
+      tc_bwd_grad_kernel<true><<<grid, kTcThreads, smg, s>>>(tq, tk, tv, tdo, tw, tu, tdvn, tdh, thf, tt, tdq, tdk,
+                                                              tdv, d, (const bf16*)a.beta, (bf16*)a.dq,
+                                                              (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
     } else {
-      cudaFuncSetAttribute(tc_bwd_gradA_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sma);
-      tc_bwd_gradA_kernel<false><<<grid, kTcThreads, sma, s>>>(tq, tk, tdo, tw, tdvn, tdh, tu, tdw, tka, tdq, thf,
-                                                                d, (bf16*)a.dq, ws);
-    }
-    stage_mark(s, "bwd_gradA");
-    if (d.G > 1) {
-      cudaFuncSetAttribute(tc_bwd_gradB_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smb);
-      tc_bwd_gradB_kernel<true><<<grid, kTcThreads, smb, s>>>(tk, tv, tt, tdw, tdvn, tka, tdv, tdk, d,
-                                                               (const bf16*)a.beta,
+      cudaFuncSetAttribute(tc_bwd_grad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
+      tc_bwd_grad_kernel<false><<<grid, kTcThreads, smg, s>>>(tq, tk, tv, tdo, tw, tu, tdvn, tdh, thf, tt, tdq, tdk,
+                                                               tdv, d, (const bf16*)a.beta, (bf16*)a.dq,
                                                                (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
-    } else {
-      cudaFuncSetAttribute(tc_bwd_gradB_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smb);
-      tc_bwd_gradB_kernel<false><<<grid, kTcThreads, smb, s>>>(tk, tv, tt, tdw, tdvn, tka, tdv, tdk, d,
-                                                                (const bf16*)a.beta,
-                                                                (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
     }
-    stage_mark(s, "bwd_gradB");
+    stage_mark(s, "bwd_grad");
     if (d.G > 1) {
       e = launch_group_reduce(d, a.dq, a.dk, ws, s);
       if (e != cudaSuccess) return e;

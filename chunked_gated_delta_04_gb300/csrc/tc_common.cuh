@@ -85,6 +85,45 @@ __device__ __forceinline__ void st_global_bf16x64(bf16* dst, const float* v) {
   }
 }
 
+// Store 32 fp32 values as bf16 into columns [32 * half, 32 * half + 32) of row `row`
+// of a 64-column swizzled slab.
+__device__ __forceinline__ void st_halfrow_bf16(unsigned char* slab, int row, int half, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int ch = 4 * half + c;
+    uint4 w;
+    uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[c * 8 + 2 * e], v[c * 8 + 2 * e + 1]);
+      wp[e] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(slab + row * 128 + (((ch ^ (row & 7)) & 7) << 4)) = w;
+  }
+}
+
+// Load columns [32 * half, 32 * half + 32) of row `row` (bf16) of a 64-column swizzled slab.
+__device__ __forceinline__ void ld_halfrow_bf16(const unsigned char* slab, int row, int half, float* v) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int ch = 4 * half + c;
+    const uint4 w = *reinterpret_cast<const uint4*>(slab + row * 128 + (((ch ^ (row & 7)) & 7) << 4));
+    const uint32_t* wp = reinterpret_cast<const uint32_t*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wp[e]));
+      v[c * 8 + 2 * e] = f.x;
+      v[c * 8 + 2 * e + 1] = f.y;
+    }
+  }
+}
+
+// Loads 32 TMEM columns [col, col + 32) of this thread's lane.
+__device__ __forceinline__ void tmem_ld32w(uint32_t tbase, int warp, int col, float* v) {
+  tc::tmem_ld32(tc::tmem_lane_addr(tbase, warp, col), v);
+  tc::tmem_wait_ld();
+}
+
 // Loads 64 TMEM columns [col, col + 64) of this thread's lane.
 __device__ __forceinline__ void tmem_ld64(uint32_t tbase, int warp, int col, float* v) {
   tc::tmem_ld32(tc::tmem_lane_addr(tbase, warp, col), v);
