@@ -243,13 +243,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
   __shared__ uint64_t bar_tma, bar_mma;
   __shared__ uint32_t tmem_slot;
   __shared__ float s_gam[64], s_beta[64], s_bexp[64], s_carry;
-  const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int4 ci = ws.chunks[c];
-  const int len = ci.z, t0 = ci.y;
-  if (len <= 0) return;
   const int Hv = d.Hv;
-  const size_t ch = (size_t)c * Hv + j;
 
   if (tid == 0) {
     tc::mbar_init(&bar_tma, 1);
@@ -262,6 +257,16 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
   tc::tc_fence_after();
   const uint32_t tbase = tmem_slot;
   GDR_TRACE_INIT();
+  // Persistent: each CTA walks the (chunk, v-head) items w = blockIdx.x + k * gridDim.x.
+  bool ok = true;
+  uint32_t item_par = 0;  // phase parity of bar_tma for the current item (bar_mma: 2 per item)
+  const int n_items = d.max_chunks * Hv;
+  for (int witem = blockIdx.x; witem < n_items && ok; witem += gridDim.x) {
+  const int c = witem / Hv, j = witem % Hv, i = j / d.G;
+  const int4 ci = ws.chunks[c];
+  const int len = ci.z, t0 = ci.y;
+  if (len <= 0) continue;  // empty chunk slot (uniform across the CTA)
+  const size_t ch = (size_t)c * Hv + j;
   if (tid == 0) {
     tc::mbar_arrive_expect_tx(&bar_tma, 6 * kSlab);
     tc::tma_load_3d(sm + PrepSmem::KQ, &tm_k, &bar_tma, 0, i, t0);
@@ -285,7 +290,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
       s_bexp[tid] = b * fexp(x);  // beta_s e^{gamma_s}
     }
   }
-  bool ok = __syncthreads_and(tc::mbar_wait(&bar_tma, 0, ws.status, kDevErrTimeoutPrep));
+  ok = __syncthreads_and(tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutPrep));
   GDR_TRACE_MARK(0, 0);
   const uint32_t s_kq = tc::smem_u32(sm + PrepSmem::KQ), s_v = tc::smem_u32(sm + PrepSmem::V);
   const uint32_t s_tt = tc::smem_u32(sm + PrepSmem::TT);
@@ -394,8 +399,15 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
     tc::tma_store_2d(&tm_u, sm + PrepSmem::KQ + 3 * kSlab, 64, (int)(ch * 64));
     tc::bulk_commit();
   }
-  if (tid == 0) tc::bulk_wait_read<0>();  // smem sources read before exit
+  if (tid == 0) tc::bulk_wait_read<0>();  // staging tiles read before the next item's loads
   GDR_TRACE_MARK(0, 5);
+  item_par ^= 1;
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  }  // items
+  tc::tc_fence_before();
+  __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tbase, 256);
 }
 
@@ -602,6 +614,15 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
 
 bool tc_available() { return get_encoder(); }
 
+// Persistent grid of the chunk-prep kernel: two CTAs per SM (shared memory allows two).
+static dim3 prep_grid(const Dims& d) {
+  int dev = 0, n_sm = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const long long n_items = (long long)d.max_chunks * d.Hv, cap = 2ll * n_sm;
+  return dim3((unsigned)(n_items < cap ? n_items : cap));
+}
+
 #ifdef GDR_TRACE
 extern "C" int gdr_debug_trace_fwd(unsigned long long* out) {
   return cudaMemcpyFromSymbol(out, tcx::g_gdr_trace, sizeof(tcx::g_gdr_trace)) == cudaSuccess ? 0 : 1;
@@ -626,7 +647,7 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
   if (d.max_chunks > 0 && Tt > 0) {
     const size_t smp = PrepSmem::BYTES + 1024;
     cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
-    tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, tp, d, a.g,
+    tc_prep_kernel<<<prep_grid(d), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, tp, d, a.g,
                                                                       (const bf16*)a.beta, ws, 0);
     stage_mark(s, "fwd_prep");
   }
@@ -652,7 +673,7 @@ cudaError_t tc_launch_prep(const Dims& d, const void* q, const void* k, const vo
   if (write_T && !map_2d(&tt, ws.Tb, 64, rows)) return cudaErrorInvalidValue;
   const size_t smp = PrepSmem::BYTES + 1024;
   cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
-  tc_prep_kernel<<<dim3(d.max_chunks, d.Hv), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, tt, d, g,
+  tc_prep_kernel<<<prep_grid(d), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, tt, d, g,
                                                                     (const bf16*)beta, ws, write_T);
   stage_mark(s, stage);
   return cudaGetLastError();
