@@ -52,7 +52,7 @@ _STAGE_ARR = None
 EXPORTS = ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes", "gdr_bwd_workspace_bytes",
            "gdr_fwd", "gdr_bwd", "gdr_workspace_status", "gdr_status_string", "gdr_path",
            "gdr_debug_set_stage_events", "gdr_debug_stage_count", "gdr_debug_stage_name",
-           "gdr_debug_launch_count", "gdr_fwd_noalloc", "gdr_debug_tc_gemm"]
+           "gdr_debug_launch_count", "gdr_fwd_noalloc", "gdr_debug_tc_gemm", "gdr_debug_timeout_selftest"]
 
 
 def _lib_handle():
@@ -90,6 +90,8 @@ def _lib_handle():
         lib.gdr_debug_launch_count.restype = ctypes.c_ulonglong
         lib.gdr_debug_tc_gemm.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
         lib.gdr_debug_tc_gemm.restype = i
+        lib.gdr_debug_timeout_selftest.argtypes = [vp, ctypes.c_ulonglong, vp, vp]
+        lib.gdr_debug_timeout_selftest.restype = i
         _LIB = lib
     return _LIB
 
@@ -211,6 +213,11 @@ def gdr_debug_stage_names() -> list:
 def gdr_debug_tc_gemm(A, B, D, N, K, a_mn, b_mn, status, stream=None) -> int:
     return _lib_handle().gdr_debug_tc_gemm(_ptr(A), _ptr(B), _ptr(D), N, K, a_mn, b_mn, _ptr(status),
                                            _stream_ptr(stream))
+
+
+def gdr_debug_timeout_selftest(status, limit_ns, waited_ns, stream=None) -> int:
+    return _lib_handle().gdr_debug_timeout_selftest(_ptr(status), int(limit_ns), _ptr(waited_ns),
+                                                    _stream_ptr(stream))
 
 
 def gdr_debug_launch_count() -> int:

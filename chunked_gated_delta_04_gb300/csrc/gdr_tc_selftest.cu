@@ -90,3 +90,37 @@ extern "C" int gdr_debug_tc_gemm(const void* A, const void* B, float* D, int N, 
                                                                   (uint32_t*)status);
   return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }
+
+namespace gdr {
+namespace {
+
+// A wait that can never complete (the mbarrier expects one arrival that nobody makes),
+// bounded by limit_ns: the kernel must give up, record the timeout bit and return.
+__global__ void tc_timeout_selftest_kernel(uint32_t* status, unsigned long long limit_ns,
+                                           unsigned long long* waited_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  const uint64_t t0 = tc::globaltimer_ns();
+  bool done = false;
+  while (!(done = tc::mbar_try_wait(&bar, 0))) {
+    if (tc::globaltimer_ns() - t0 > limit_ns) break;
+  }
+  if (!done && threadIdx.x == 0) {
+    atomicOr(status, kDevErrTimeoutFwd);
+    *waited_ns = tc::globaltimer_ns() - t0;
+  }
+}
+
+}  // namespace
+}  // namespace gdr
+
+extern "C" int gdr_debug_timeout_selftest(unsigned int* status, unsigned long long limit_ns,
+                                          unsigned long long* waited_ns, void* stream) {
+  if (limit_ns > 1000000000ull) return 1;  // at most 1 s
+  gdr::tc_timeout_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((uint32_t*)status, limit_ns, waited_ns);
+  return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}

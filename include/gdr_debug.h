@@ -37,6 +37,13 @@ unsigned long long gdr_debug_launch_count(void);
 int gdr_debug_tc_gemm(const void* A, const void* B, float* D, int N, int K, int a_mn, int b_mn,
                       unsigned int* status, void* stream);
 
+/* Failure-detection self-test: one kernel waits on an mbarrier that nothing ever
+ * completes, bounded by limit_ns (at most 1 s).  The wait must expire, set the timeout
+ * bit (GDR_ERR_TIMEOUT's bit, 1u << 1) in *status and return; *waited_ns receives how long
+ * it waited.  status and waited_ns are device pointers.  Returns 0 when launched. */
+int gdr_debug_timeout_selftest(unsigned int* status, unsigned long long limit_ns,
+                               unsigned long long* waited_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
