@@ -239,8 +239,10 @@ struct GradSmem {
   static constexpr uint32_t TP = VN, DQS = DH, DVS = W, DKS = DO, DW = UT;
 };
 
+constexpr int kGradThreads = 256;  // two warps per TMEM lane quarter, each on half the columns
+
 template <bool kGroup>
-__global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
+__global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
@@ -254,8 +256,13 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint64_t bar_tma, bar_tma2, bar_mma;
   __shared__ uint32_t tmem_slot;
-  __shared__ float s_beta[64], s_eg[64], s_dgam[64], s_colpp[64], s_colbk[64], s_colaa[64], s_red[4];
-  const int tid = threadIdx.x, warp = tid >> 5, r = tid & 63;
+  __shared__ float s_beta[64], s_eg[64], s_dgam[64], s_colpp[64], s_colbk[64], s_colaa[64], s_red[8];
+  // per-row partial sums of the two column halves: [half][row]
+  __shared__ float s_qh[2][64], s_rowpp[2][64], s_kdv[2][64], s_dbv[2][64], s_akk[2][64], s_rowaa[2][64];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, hf = warp >> 2;  // TMEM lane quarter, column half
+  const bool lo = quarter < 2;                    // lanes 0-63 (rows of the 64-row products)
+  const int r = (quarter & 1) * 32 + lane;        // row within the lane half
   const int Hv = d.Hv;
   using S = GradSmem;
 
@@ -315,45 +322,45 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
   const float dec = fexp(gC - gr);
   GDR_TRACE_MARK(2, 0);
 
-  // h row `tid`: fp32 slabs (32 columns) -> bf16 operand slabs (64 columns) in place;
-  // <dh', h> accumulated on the way.
+  // h: fp32 slabs (32 columns) -> bf16 operand slabs (64 columns) in place; thread = (row
+  // tid & 127, column half tid >> 7).  bf16 slab s overwrites fp32 slab s, which only the
+  // half-0 threads read before the barrier.  <dh', h> is accumulated on the way.
   float hdh = 0.f;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
+  {
+    const int hrow = tid & 127, hh = tid >> 7;
     float hv[64], dv_[64];
     if (ok) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const unsigned char* src = sm + S::H + (2 * half + q) * 16384 + tid * 128;
+        const unsigned char* src = sm + S::H + (2 * hh + q) * 16384 + hrow * 128;
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 f = *reinterpret_cast<const float4*>(src + (((c4 ^ (tid & 7)) & 7) << 4));
+          const float4 f = *reinterpret_cast<const float4*>(src + (((c4 ^ (hrow & 7)) & 7) << 4));
           hv[q * 32 + 4 * c4] = f.x; hv[q * 32 + 4 * c4 + 1] = f.y;
           hv[q * 32 + 4 * c4 + 2] = f.z; hv[q * 32 + 4 * c4 + 3] = f.w;
         }
       }
-      ld_row_bf16(sm + S::DH + half * 16384, tid, dv_);
+      ld_row_bf16(sm + S::DH + hh * 16384, hrow, dv_);
 #pragma unroll
       for (int b = 0; b < 64; ++b) hdh += hv[b] * dv_[b];
     }
     __syncthreads();
-    if (ok) st_row_bf16(sm + S::H + half * 16384, tid, hv);
+    if (ok) st_row_bf16(sm + S::H + hh * 16384, hrow, hv);
   }
-  hdh = block_sum128(hdh, s_red);
-  if (ok && tid < 64) {  // O-hat = scale diag(e^gamma) dO, zero past the chunk end
+  hdh = warp_sum(hdh);
+  if (lane == 0) s_red[warp] = hdh;
+  if (ok && lo) {  // O-hat = scale diag(e^gamma) dO, zero past the chunk end (half hf of row r)
     float x[64];
     const float e = r < len ? d.scale * s_eg[r] : 0.f;
+    ld_row_bf16(sm + S::DO + hf * kSlab, r, x);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      ld_row_bf16(sm + S::DO + half * kSlab, r, x);
-#pragma unroll
-      for (int b = 0; b < 64; ++b) x[b] *= e;
-      st_row_bf16(sm + S::OH + half * kSlab, r, x);
-    }
+    for (int b = 0; b < 64; ++b) x[b] *= e;
+    st_row_bf16(sm + S::OH + hf * kSlab, r, x);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
+  hdh = ((s_red[0] + s_red[1]) + (s_red[2] + s_red[3])) + ((s_red[4] + s_red[5]) + (s_red[6] + s_red[7]));
   GDR_TRACE_MARK(2, 1);
   // P2: [K;Q] K^T (0-63), W h (64-191), O-hat h^T -> dq (256-383), dVn h^T = -dW (384-511)
   if (ok && tid == 0) {
@@ -374,34 +381,32 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
     tc::tma_load_2d(sm + S::T, &tm_t, &bar_tma2, 0, (int)(ch * 64));
   }
   float* scr = reinterpret_cast<float*>(sm + S::SCR);
-  float qh = 0.f;
   if (ok) {
-    if (tid < 64) {
+    if (lo) {  // row r, columns [64 hf, 64 hf + 64)
       float x[64], u[64];
+      tmem_ld64(tb, warp, 64 + hf * 64, x);  // (W h)[r]
+      ld_row_bf16(sm + S::UT + hf * kSlab, r, u);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        tmem_ld64(tb, warp, 64 + half * 64, x);  // (W h)[r]
-        ld_row_bf16(sm + S::UT + half * kSlab, r, u);
+      for (int b = 0; b < 64; ++b) u[b] = r < len ? u[b] - x[b] : 0.f;
+      st_row_bf16(sm + S::VN + hf * kSlab, r, u);
 #pragma unroll
-        for (int b = 0; b < 64; ++b) u[b] = r < len ? u[b] - x[b] : 0.f;
-        st_row_bf16(sm + S::VN + half * kSlab, r, u);
+      for (int b = 0; b < 64; ++b) u[b] *= dec;
+      st_row_bf16(sm + S::W + hf * kSlab, r, u);  // Vn~ (W no longer needed)
+      tmem_ld64(tb, warp, 256 + hf * 64, x);     // (O-hat h^T)[r]
+      ld_row_bf16(sm + S::KQ + kSlab + hf * 2 * kSlab, r, u);  // q_r
+      float qh = 0.f;
 #pragma unroll
-        for (int b = 0; b < 64; ++b) u[b] *= dec;
-        st_row_bf16(sm + S::W + half * kSlab, r, u);  // Vn~ (W no longer needed)
-        tmem_ld64(tb, warp, 256 + half * 64, x);  // (O-hat h^T)[r]
-        ld_row_bf16(sm + S::KQ + kSlab + half * 2 * kSlab, r, u);  // q_r
+      for (int b = 0; b < 64; ++b) qh += x[b] * u[b];
+      s_qh[hf][r] = qh;
+      tmem_ld64(tb, warp, 384 + hf * 64, x);  // -dW[r]
 #pragma unroll
-        for (int b = 0; b < 64; ++b) qh += x[b] * u[b];
-        tmem_ld64(tb, warp, 384 + half * 64, x);  // -dW[r]
+      for (int b = 0; b < 64; ++b) x[b] = -x[b];
+      st_row_bf16(sm + S::DW + hf * kSlab, r, x);  // own U row half already consumed
+    } else {  // Q K^T row r, columns [32 hf, 32 hf + 32) -> scratch (fp32)
+      float x[32];
+      tmem_ld32w(tb, warp, 32 * hf, x);
 #pragma unroll
-        for (int b = 0; b < 64; ++b) x[b] = -x[b];
-        st_row_bf16(sm + S::DW + half * kSlab, r, x);  // own U row half already consumed
-      }
-    } else {  // Q K^T rows -> scratch (fp32)
-      float x[64];
-      tmem_ld64(tb, warp, 0, x);
-#pragma unroll
-      for (int s = 0; s < 64; ++s) scr[r * 65 + s] = x[s];
+      for (int s = 0; s < 32; ++s) scr[r * 65 + 32 * hf + s] = x[s];
     }
   }
   tc::fence_proxy_async_smem();
@@ -419,10 +424,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 4);
-  float rowpp = 0.f, kdv = 0.f;
-  if (ok && tid < 64) {
-#pragma unroll 1
-    for (int hf = 0; hf < 2; ++hf) {  // 32 columns at a time (register pressure)
+  if (ok && lo) {
+    {  // dP and dP * QK for columns [32 hf, 32 hf + 32)
       float x[32], gs[32], qk[32];
       tmem_ld32w(tb, warp, 64 + 32 * hf, x);  // (dO Vn^T)[r]
 #pragma unroll
@@ -430,6 +433,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
         gs[s] = sgam[32 * hf + s];
         qk[s] = scr[r * 65 + 32 * hf + s];
       }
+      float rowpp = 0.f;
 #pragma unroll
       for (int s = 0; s < 32; ++s) {
         const int sc = 32 * hf + s;
@@ -441,26 +445,30 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
 #pragma unroll
       for (int s = 0; s < 32; ++s) scr[r * 65 + 32 * hf + s] = qk[s];
       st_halfrow_bf16(sm + S::DP, r, hf, x);  // dP (h no longer needed)
+      s_rowpp[hf][r] = rowpp;
     }
+    float kdv = 0.f;
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {  // (K dh')[r] . Vn[r], 32 columns at a time
+    for (int q = 0; q < 2; ++q) {  // (K dh')[r] . Vn[r] over columns [64 hf + 32 q, +32)
       float x[32], v[32];
-      tmem_ld32w(tb, warp, 128 + 32 * q, x);
-      ld_halfrow_bf16(sm + S::VN + (q >> 1) * kSlab, r, q & 1, v);
+      tmem_ld32w(tb, warp, 128 + 64 * hf + 32 * q, x);
+      ld_halfrow_bf16(sm + S::VN + hf * kSlab, r, q, v);
 #pragma unroll
       for (int b = 0; b < 32; ++b) kdv += x[b] * v[b];
     }
-    kdv = r < len ? kdv : 0.f;
-    const float part = warp_sum(dec * kdv);  // sum_s e^{gC - g_s} k_s^T dh' vn_s
-    if ((tid & 31) == 0) s_red[tid >> 5] = part;
+    s_kdv[hf][r] = kdv;
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
-  if (ok && tid < 64) {
+  if (ok && tid < 64) {  // column sums of dP * QK; full k^T dh' vn per row
     float cs = 0.f;
     for (int rr = 0; rr < 64; ++rr) cs += scr[rr * 65 + tid];
     s_colpp[tid] = cs;
+    const float kdv = tid < len ? s_kdv[0][tid] + s_kdv[1][tid] : 0.f;
+    s_kdv[0][tid] = kdv;
+    const float part = warp_sum(tid < len ? fexp(gC - sgam[tid]) * kdv : 0.f);  // sum_s e^{gC - g_s} k_s^T dh' vn_s
+    if (lane == 0) s_red[warp] = part;
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_tma2, item_par, ws.status, kDevErrTimeoutBwd));
   GDR_TRACE_MARK(2, 5);
@@ -476,45 +484,38 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 6);
-  if (ok && tid < 64) {
-    float x[64], y[64];
-    // dq (final for one v-head per q/k head)
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tmem_ld64(tb, warp, 256 + half * 64, x);
+  if (ok && lo) {
+    {  // dq columns [64 hf, +64) (final for one v-head per q/k head)
+      float x[64];
+      tmem_ld64(tb, warp, 256 + hf * 64, x);
       if (kGroup) {
         if (r < len) {
-          float* dst = ws.dq_part + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64;
+          float* dst = ws.dq_part + ((size_t)(t0 + r) * Hv + j) * 128 + hf * 64;
 #pragma unroll
           for (int b = 0; b < 64; b += 4) *reinterpret_cast<float4*>(dst + b) = make_float4(x[b], x[b + 1], x[b + 2], x[b + 3]);
         }
       } else if (len == 64) {
-        st_row_bf16(sm + S::DQS + half * kSlab, r, x);
+        st_row_bf16(sm + S::DQS + hf * kSlab, r, x);
       } else if (r < len) {
-        st_global_bf16x64(dq + ((size_t)(t0 + r) * d.Hk + i) * 128 + half * 64, x);
+        st_global_bf16x64(dq + ((size_t)(t0 + r) * d.Hk + i) * 128 + hf * 64, x);
       }
     }
-  }
-  if (ok && tid < 64) {
     // dT = dW B_k^T + dVn B_v^T = (dW K^T) diag(beta e^gamma) + (dVn V^T) diag(beta);
-    // T * (dW K^T) (row r) for <dB_k[s], k_s> = sum_m T[m][s] (dW K^T)[m][s]
-#pragma unroll 1
-    for (int hf = 0; hf < 2; ++hf) {
-      float x[32], y[32], tr[32];
-      tmem_ld32w(tb, warp, 64 + 32 * hf, x);
-      tmem_ld32w(tb, warp, 128 + 32 * hf, y);
-      ld_halfrow_bf16(sm + S::T, r, hf, tr);
+    // T * (dW K^T) (row r) for <dB_k[s], k_s> = sum_m T[m][s] (dW K^T)[m][s]; columns [32 hf, +32)
+    float x[32], y[32], tr[32];
+    tmem_ld32w(tb, warp, 64 + 32 * hf, x);
+    tmem_ld32w(tb, warp, 128 + 32 * hf, y);
+    ld_halfrow_bf16(sm + S::T, r, hf, tr);
 #pragma unroll
-      for (int s = 0; s < 32; ++s) {
-        const int sc = 32 * hf + s;
-        const float be = s_beta[sc] * s_eg[sc];
-        scr[r * 65 + sc] = tr[s] * x[s];
-        y[s] = (r < len && sc < len) ? be * x[s] + s_beta[sc] * y[s] : 0.f;
-        tr[s] *= be;  // T' = T diag(beta e^gamma)
-      }
-      st_halfrow_bf16(sm + S::DT, r, hf, y);
-      st_halfrow_bf16(sm + S::TP, r, hf, tr);
+    for (int s = 0; s < 32; ++s) {
+      const int sc = 32 * hf + s;
+      const float be = s_beta[sc] * s_eg[sc];
+      scr[r * 65 + sc] = tr[s] * x[s];
+      y[s] = (r < len && sc < len) ? be * x[s] + s_beta[sc] * y[s] : 0.f;
+      tr[s] *= be;  // T' = T diag(beta e^gamma)
     }
+    st_halfrow_bf16(sm + S::DT, r, hf, y);
+    st_halfrow_bf16(sm + S::TP, r, hf, tr);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
@@ -540,26 +541,27 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 8);
-  float dbv = 0.f;
-  if (ok && tid < 64) {
-    float x[64], y[64];
-    const float br = s_beta[r];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tmem_ld64(tb, warp, 128 + half * 64, x);  // dB_v[r]
-      ld_row_bf16(sm + S::V + half * kSlab, r, y);
+  if (ok && lo) {
+    {  // dv = diag(beta) dB_v, columns [64 hf, +64)
+      float x[64], y[64];
+      const float br = s_beta[r];
+      float dbv = 0.f;
+      tmem_ld64(tb, warp, 128 + hf * 64, x);  // dB_v[r]
+      ld_row_bf16(sm + S::V + hf * kSlab, r, y);
 #pragma unroll
       for (int b = 0; b < 64; ++b) {
         dbv += x[b] * y[b];
         x[b] *= br;
       }
+      s_dbv[hf][r] = dbv;
       if (len == 64)
-        st_row_bf16(sm + S::DVS + half * kSlab, r, x);
+        st_row_bf16(sm + S::DVS + hf * kSlab, r, x);
       else if (r < len)
-        st_global_bf16x64(dv + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64, x);
+        st_global_bf16x64(dv + ((size_t)(t0 + r) * Hv + j) * 128 + hf * 64, x);
     }
-    tmem_ld64(tb, warp, 64, x);  // X = T^T dT
-    st_row_bf16(sm + S::XT, r, x);
+    float x[32];
+    tmem_ld32w(tb, warp, 64 + 32 * hf, x);  // X = T^T dT, columns [32 hf, +32)
+    st_halfrow_bf16(sm + S::XT, r, hf, x);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
@@ -579,31 +581,29 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 10);
-  float akk = 0.f, rowaa = 0.f;
-  if (ok && tid < 64) {
+  if (ok && lo) {  // columns [32 hf, +32)
     const float br = s_beta[r];
-#pragma unroll 1
-    for (int hf = 0; hf < 2; ++hf) {
-      float x[32], gs[32], kk[32];
-      tmem_ld32w(tb, warp, 64 + 32 * hf, x);   // (T^T dT T^T)[r]
-      tmem_ld32w(tb, warp, 32 * hf, kk);       // K K^T row r
+    float x[32], gs[32], kk[32], akk = 0.f, rowaa = 0.f;
+    tmem_ld32w(tb, warp, 64 + 32 * hf, x);   // (T^T dT T^T)[r]
+    tmem_ld32w(tb, warp, 32 * hf, kk);       // K K^T row r
 #pragma unroll
-      for (int s = 0; s < 32; ++s) gs[s] = sgam[32 * hf + s];
+    for (int s = 0; s < 32; ++s) gs[s] = sgam[32 * hf + s];
 #pragma unroll
-      for (int s = 0; s < 32; ++s) {
-        const int sc = 32 * hf + s;
-        // exp(gamma_r - gamma_s) only below the diagonal: above it the exponent is
-        // positive and can overflow, and 0 * inf would give NaN
-        const float dag = (sc < r && r < len) ? -x[s] * fexp(gr - gs[s]) : 0.f;
-        akk += dag * kk[s];
-        x[s] = br * dag;
-        kk[s] *= x[s];  // dA * A with A = beta_r Gam K K^T
-        rowaa += kk[s];
-      }
-#pragma unroll
-      for (int s = 0; s < 32; ++s) scr[r * 65 + 32 * hf + s] = kk[s];
-      st_halfrow_bf16(sm + S::DAG, r, hf, x);
+    for (int s = 0; s < 32; ++s) {
+      const int sc = 32 * hf + s;
+      // exp(gamma_r - gamma_s) only below the diagonal: above it the exponent is
+      // positive and can overflow, and 0 * inf would give NaN
+      const float dag = (sc < r && r < len) ? -x[s] * fexp(gr - gs[s]) : 0.f;
+      akk += dag * kk[s];
+      x[s] = br * dag;
+      kk[s] *= x[s];  // dA * A with A = beta_r Gam K K^T
+      rowaa += kk[s];
     }
+#pragma unroll
+    for (int s = 0; s < 32; ++s) scr[r * 65 + 32 * hf + s] = kk[s];
+    st_halfrow_bf16(sm + S::DAG, r, hf, x);
+    s_akk[hf][r] = akk;
+    s_rowaa[hf][r] = rowaa;
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
@@ -625,31 +625,32 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 12);
-  if (ok && tid < 64) {
+  if (ok && lo) {
     float x[64];
+    tmem_ld64(tb, warp, 384 + hf * 64, x);  // dk columns [64 hf, +64)
+    if (kGroup) {
+      if (r < len) {
+        float* dst = ws.dk_part + ((size_t)(t0 + r) * Hv + j) * 128 + hf * 64;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      tmem_ld64(tb, warp, 384 + half * 64, x);
-      if (kGroup) {
-        if (r < len) {
-          float* dst = ws.dk_part + ((size_t)(t0 + r) * Hv + j) * 128 + half * 64;
-#pragma unroll
-          for (int b = 0; b < 64; b += 4) *reinterpret_cast<float4*>(dst + b) = make_float4(x[b], x[b + 1], x[b + 2], x[b + 3]);
-        }
-      } else if (len == 64) {
-        st_row_bf16(sm + S::DKS + half * kSlab, r, x);
-      } else if (r < len) {
-        st_global_bf16x64(dk + ((size_t)(t0 + r) * d.Hk + i) * 128 + half * 64, x);
+        for (int b = 0; b < 64; b += 4) *reinterpret_cast<float4*>(dst + b) = make_float4(x[b], x[b + 1], x[b + 2], x[b + 3]);
       }
+    } else if (len == 64) {
+      st_row_bf16(sm + S::DKS + hf * kSlab, r, x);
+    } else if (r < len) {
+      st_global_bf16x64(dk + ((size_t)(t0 + r) * d.Hk + i) * 128 + hf * 64, x);
     }
-    const float br = s_beta[r], eg = s_eg[r];
-    if (r < len) dbeta[(size_t)(t0 + r) * Hv + j] = __float2bfloat16_rn(eg * s_colbk[r] + dbv + akk);
-    float dgm = 0.f;
-    if (r < len) {
-      dgm = rowpp - s_colpp[r] + qh - dec * kdv + br * eg * s_colbk[r] + rowaa - s_colaa[r];
-      if (r == len - 1) dgm += fexp(gC) * hdh + (s_red[0] + s_red[1]);
+    if (hf == 0) {  // per-row scalars: dbeta and d gamma
+      const float br = s_beta[r], eg = s_eg[r];
+      const float akk = s_akk[0][r] + s_akk[1][r], dbv = s_dbv[0][r] + s_dbv[1][r];
+      if (r < len) dbeta[(size_t)(t0 + r) * Hv + j] = __float2bfloat16_rn(eg * s_colbk[r] + dbv + akk);
+      float dgm = 0.f;
+      if (r < len) {
+        dgm = (s_rowpp[0][r] + s_rowpp[1][r]) - s_colpp[r] + (s_qh[0][r] + s_qh[1][r]) - dec * s_kdv[0][r] +
+              br * eg * s_colbk[r] + (s_rowaa[0][r] + s_rowaa[1][r]) - s_colaa[r];
+        if (r == len - 1) dgm += fexp(gC) * hdh + (s_red[0] + s_red[1]);
+      }
+      s_dgam[r] = dgm;
     }
-    s_dgam[r] = dgm;
   }
   tc::fence_proxy_async_smem();
   __syncthreads();
@@ -659,7 +660,6 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_grad_kernel(
     tc::bulk_commit();
   }
   if (ok && tid < 64) {  // dg = in-chunk reverse cumsum of d gamma (rows >= len hold 0)
-    const int lane = tid & 31;
     float x = s_dgam[63 - tid];  // reversed order: prefix sums become suffix sums
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -730,12 +730,12 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     const size_t smg = GradSmem::BYTES + 1024;
     if (d.G > 1) {
       cudaFuncSetAttribute(tc_bwd_grad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
-      tc_bwd_grad_kernel<true><<<grid, kTcThreads, smg, s>>>(tq, tk, tv, tdo, tw, tu, tdvn, tdh, thf, tt, tdq, tdk,
+      tc_bwd_grad_kernel<true><<<grid, kGradThreads, smg, s>>>(tq, tk, tv, tdo, tw, tu, tdvn, tdh, thf, tt, tdq, tdk,
                                                               tdv, d, (const bf16*)a.beta, (bf16*)a.dq,
                                                               (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
     } else {
       cudaFuncSetAttribute(tc_bwd_grad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
-      tc_bwd_grad_kernel<false><<<grid, kTcThreads, smg, s>>>(tq, tk, tv, tdo, tw, tu, tdvn, tdh, thf, tt, tdq, tdk,
+      tc_bwd_grad_kernel<false><<<grid, kGradThreads, smg, s>>>(tq, tk, tv, tdo, tw, tu, tdvn, tdh, thf, tt, tdq, tdk,
                                                                tdv, d, (const bf16*)a.beta, (bf16*)a.dq,
                                                                (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
     }
