@@ -65,8 +65,9 @@ def chunk_lengths(seqlens):
     return out
 
 
-def tensor_bytes(inp, w):
-    """Bytes of every operator-level tensor of one fwd+bwd call."""
+def tensor_bytes(inp, w, h_el=4):
+    """Bytes of every operator-level tensor of one fwd+bwd call (h_el: bytes per saved-state
+    element, 4 for fp32 h_saved and 2 for the bf16 option)."""
     el = 2 if w.dtype.itemsize == 2 else 4
     tok = sum(inp["seqlens"])
     N = inp["num_seqs"]
@@ -78,11 +79,11 @@ def tensor_bytes(inp, w):
         "q": qk, "k": qk, "dq": qk, "dk": qk, "v": vv, "o": vv, "dO": vv, "dv": vv,
         "g": tok * w.Hv * 4, "dg": tok * w.Hv * 4, "beta": tok * w.Hv * el, "dbeta": tok * w.Hv * el,
         "S0": st if inp["S0"] is not None else 0, "S_T": st, "dS_T": st if inp["dS_T"] is not None else 0,
-        "dS0": st, "h_saved": nch * w.Hv * w.DK * w.DV * 4,
+        "dS0": st, "h_saved": nch * w.Hv * w.DK * w.DV * h_el,
     }
 
 
-def work_model(inp, w):
+def work_model(inp, w, h_el=4):
     """Algorithmic FLOPs (the chunked method's GEMMs, C x C products dense, the T inverse
     as C^3/3) and compulsory HBM bytes of the forward and the backward."""
     G = w.Hv // w.Hk
@@ -93,7 +94,7 @@ def work_model(inp, w):
         fb += 14 * c * DK * DV + 2 * c * c * DK * (7 + 2 / G) + 10 * c * c * DV + 4 * c ** 3 + c ** 3 / 3
     ff *= w.Hv
     fb *= w.Hv
-    tb = tensor_bytes(inp, w)
+    tb = tensor_bytes(inp, w, h_el)
     bf = sum(tb[k] for k in ["q", "k", "v", "g", "beta", "o", "h_saved", "S0", "S_T"])
     bb = sum(tb[k] for k in ["q", "k", "v", "dO", "g", "beta", "h_saved", "dq", "dk", "dv", "dg", "dbeta",
                              "dS_T", "dS0"])
@@ -239,7 +240,7 @@ def reference_arm(args, w, inp):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w, inp),
+        "config": config_dict(w, inp, args.h_dtype),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(nthreads, units), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -248,13 +249,13 @@ def reference_arm(args, w, inp):
     return 0
 
 
-def config_dict(w, inp):
+def config_dict(w, inp, h_dtype="f32"):
     return {"workload": w.name, "B": w.B if inp["cu_seqlens"] is None else 1, "T": int(sum(inp["seqlens"])) if
             inp["cu_seqlens"] is not None else w.T, "Hk": w.Hk, "Hv": w.Hv, "DK": w.DK, "DV": w.DV,
             "layout": w.layout, "num_seqs": inp["num_seqs"], "chunk": CHUNK,
             "varlen": inp["cu_seqlens"] is not None, "S0": inp["S0"] is not None,
-            "dS_T": inp["dS_T"] is not None, "l2": "flushed (512 MB write) between timed steps",
-            "parallelism": "replicas"}
+            "dS_T": inp["dS_T"] is not None, "h_saved": h_dtype,
+            "l2": "flushed (512 MB write) between timed steps", "parallelism": "replicas"}
 
 
 def aggregate_throughput(local_ms, local_tokens, dist=None, device="cpu"):
@@ -281,6 +282,8 @@ def main():
     ap.add_argument("--workload", default="b2_t4096")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--h-dtype", default="f32", choices=["f32", "bf16"],
+                    help="dtype of the saved chunk-start states (bf16 halves the largest tensor)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -311,13 +314,14 @@ def main():
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     B, T, Hk, DK = d["q"].shape
     Hv, DV = d["v"].shape[2], d["v"].shape[3]
-    p = gdr.make_problem(B, T, Hk, Hv, DK, DV, d["q"].dtype, w.layout, d["cu_seqlens"])
+    h_dtype = torch.bfloat16 if args.h_dtype == "bf16" else torch.float32
+    p = gdr.make_problem(B, T, Hk, Hv, DK, DV, d["q"].dtype, w.layout, d["cu_seqlens"], h_dtype=h_dtype)
     stream = torch.cuda.current_stream()
     N = p.num_seqs
     sshape = (N, Hv, DK, DV) if w.layout == "KV" else (N, Hv, DV, DK)
     o = torch.empty_like(d["v"])
     S_T = torch.empty(sshape, dtype=torch.float32, device=dev)
-    h_saved = torch.empty((gdr.gdr_max_chunks(p), Hv, DK, DV), dtype=torch.float32, device=dev)
+    h_saved = torch.empty((gdr.gdr_max_chunks(p), Hv, DK, DV), dtype=h_dtype, device=dev)
     dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
     dg, dbeta = torch.empty_like(d["g"]), torch.empty_like(d["beta"])
     dS0 = torch.empty(sshape, dtype=torch.float32, device=dev)
@@ -397,7 +401,7 @@ def main():
     gdr.gdr_debug_set_stage_events(None)
     stage_ms = {k: statistics.mean(v) for k, v in stage_tot.items()}
 
-    wm = work_model(inp, w)
+    wm = work_model(inp, w, 2 if args.h_dtype == "bf16" else 4)
     hbm, bf16_burst, bf16_sus, peak_src = load_peaks()
     dom = max(stage_ms, key=stage_ms.get)
     alg = stage_alg_bytes(dom, wm["tensor_bytes"])
@@ -466,7 +470,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
             "data": "synthetic (seeded; see chunked_gated_delta_04_gb300/inputs.py)",
-            "config": config_dict(w, inp),
+            "config": config_dict(w, inp, args.h_dtype),
             "roofline": roofline,
             "step_roofline": {"ms": step_roof, "frac": step_roof / ms_per_step, "bound": "hbm" if
                               t_hbm_step >= t_flop_step else "tensor", "bytes": wm["bytes_fwd"] + wm["bytes_bwd"],

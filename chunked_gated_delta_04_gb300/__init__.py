@@ -36,7 +36,7 @@ class gdr_problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("Hk", ctypes.c_int), ("Hv", ctypes.c_int),
                 ("DK", ctypes.c_int), ("DV", ctypes.c_int), ("num_seqs", ctypes.c_int),
                 ("cu_seqlens", ctypes.c_void_p), ("dtype", ctypes.c_int), ("layout", ctypes.c_int),
-                ("scale", ctypes.c_float)]
+                ("scale", ctypes.c_float), ("h_dtype", ctypes.c_int)]
 
 
 class GDRError(RuntimeError):
@@ -117,8 +117,13 @@ def _stream_ptr(stream) -> Optional[int]:
     return stream.cuda_stream
 
 
-def make_problem(B, T, Hk, Hv, DK, DV, dtype, layout="KV", cu_seqlens=None, num_seqs=None, scale=None):
-    """Build a gdr_problem.  dtype: torch.float32/bfloat16; layout "KV"/"VK"."""
+def _dtype_code(dtype):
+    return GDR_DTYPE_BF16 if dtype == torch.bfloat16 else (GDR_DTYPE_F32 if dtype == torch.float32 else 99)
+
+
+def make_problem(B, T, Hk, Hv, DK, DV, dtype, layout="KV", cu_seqlens=None, num_seqs=None, scale=None,
+                 h_dtype=torch.float32):
+    """Build a gdr_problem.  dtype, h_dtype (of h_saved): torch.float32/bfloat16; layout "KV"/"VK"."""
     p = gdr_problem()
     p.B, p.T, p.Hk, p.Hv, p.DK, p.DV = B, T, Hk, Hv, DK, DV
     if cu_seqlens is not None:
@@ -127,7 +132,8 @@ def make_problem(B, T, Hk, Hv, DK, DV, dtype, layout="KV", cu_seqlens=None, num_
     else:
         p.cu_seqlens = None
         p.num_seqs = B if num_seqs is None else num_seqs
-    p.dtype = GDR_DTYPE_BF16 if dtype == torch.bfloat16 else (GDR_DTYPE_F32 if dtype == torch.float32 else 99)
+    p.dtype = _dtype_code(dtype)
+    p.h_dtype = _dtype_code(h_dtype)
     p.layout = {"KV": GDR_STATE_KV, "VK": GDR_STATE_VK}.get(layout, 99) if isinstance(layout, str) else layout
     p.scale = 0.0 if scale is None else float(scale)
     return p
@@ -229,10 +235,10 @@ def _check(st, where):
         raise GDRError(st, where)
 
 
-def _problem_for(q, v, cu_seqlens, layout, scale):
+def _problem_for(q, v, cu_seqlens, layout, scale, h_dtype=torch.float32):
     B, T, Hk, DK = q.shape
     Hv, DV = v.shape[2], v.shape[3]
-    return make_problem(B, T, Hk, Hv, DK, DV, q.dtype, layout, cu_seqlens, scale=scale)
+    return make_problem(B, T, Hk, Hv, DK, DV, q.dtype, layout, cu_seqlens, scale=scale, h_dtype=h_dtype)
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:
@@ -242,15 +248,15 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 # ------------------------------------------------------------------ allocating helpers
 def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, layout="KV", scale=None, output_final_state=True,
-            workspace=None, stream=None):
-    """Run gdr_fwd; returns (o, S_T or None, h_saved)."""
-    p = _problem_for(q, v, cu_seqlens, layout, scale)
+            workspace=None, stream=None, h_dtype=torch.float32):
+    """Run gdr_fwd; returns (o, S_T or None, h_saved).  h_dtype: dtype of h_saved."""
+    p = _problem_for(q, v, cu_seqlens, layout, scale, h_dtype)
     dev = q.device
     N = p.num_seqs
     o = torch.empty_like(v)
     sshape = (N, p.Hv, p.DK, p.DV) if layout == "KV" else (N, p.Hv, p.DV, p.DK)
     S_T = torch.empty(sshape, dtype=torch.float32, device=dev) if output_final_state else None
-    h_saved = torch.empty((gdr_max_chunks(p), p.Hv, p.DK, p.DV), dtype=torch.float32, device=dev)
+    h_saved = torch.empty((gdr_max_chunks(p), p.Hv, p.DK, p.DV), dtype=h_dtype, device=dev)
     if workspace is None:
         workspace = alloc_workspace(gdr_fwd_workspace_bytes(p), dev)
     _check(gdr_fwd(p, q, k, v, g, beta, S0, o, S_T, h_saved, workspace, stream=stream), "gdr_fwd")
@@ -259,8 +265,8 @@ def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, layout="KV", scale=None,
 
 def backward(q, k, v, g, beta, h_saved, dO, dS_T=None, cu_seqlens=None, layout="KV", scale=None,
              want_dS0=True, workspace=None, stream=None):
-    """Run gdr_bwd; returns (dq, dk, dv, dg, dbeta, dS0 or None)."""
-    p = _problem_for(q, v, cu_seqlens, layout, scale)
+    """Run gdr_bwd; returns (dq, dk, dv, dg, dbeta, dS0 or None).  h_saved's dtype selects h_dtype."""
+    p = _problem_for(q, v, cu_seqlens, layout, scale, h_saved.dtype)
     dev = q.device
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dg = torch.empty_like(g)
@@ -277,8 +283,8 @@ def backward(q, k, v, g, beta, h_saved, dO, dS_T=None, cu_seqlens=None, layout="
 
 class _GDRFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, S0, cu_seqlens, layout, scale):
-        o, S_T, h_saved = forward(q, k, v, g, beta, S0, cu_seqlens, layout, scale)
+    def forward(ctx, q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype):
+        o, S_T, h_saved = forward(q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype=h_dtype)
         ctx.save_for_backward(q, k, v, g, beta, h_saved, cu_seqlens)
         ctx.layout, ctx.scale, ctx.has_S0 = layout, scale, S0 is not None
         return o, S_T
@@ -289,9 +295,11 @@ class _GDRFunction(torch.autograd.Function):
         dq, dk, dv, dg, dbeta, dS0 = backward(q, k, v, g, beta, h_saved, do.contiguous(),
                                               None if dS_T is None else dS_T.contiguous(), cu_seqlens,
                                               ctx.layout, ctx.scale, want_dS0=ctx.has_S0)
-        return dq, dk, dv, dg, dbeta, dS0, None, None, None
+        return dq, dk, dv, dg, dbeta, dS0, None, None, None, None
 
 
-def chunk_gated_delta_rule(q, k, v, g, beta, initial_state=None, cu_seqlens=None, layout="KV", scale=None):
-    """Autograd entry point: returns (o, final_state).  Tensors as in include/gdr.h."""
-    return _GDRFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, layout, scale)
+def chunk_gated_delta_rule(q, k, v, g, beta, initial_state=None, cu_seqlens=None, layout="KV", scale=None,
+                           h_dtype=torch.float32):
+    """Autograd entry point: returns (o, final_state).  Tensors as in include/gdr.h; h_dtype is the
+    dtype of the chunk-start states kept for the backward (bfloat16 halves their memory)."""
+    return _GDRFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, layout, scale, h_dtype)

@@ -49,6 +49,7 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
   if (p->Hv % p->Hk != 0) return GDR_ERR_INVALID_ARG;
   if (p->dtype != GDR_DTYPE_F32 && p->dtype != GDR_DTYPE_BF16) return GDR_ERR_INVALID_ARG;
   if (p->layout != GDR_STATE_KV && p->layout != GDR_STATE_VK) return GDR_ERR_INVALID_ARG;
+  if (p->h_dtype != GDR_DTYPE_F32 && p->h_dtype != GDR_DTYPE_BF16) return GDR_ERR_INVALID_ARG;
   if (p->cu_seqlens != nullptr) {
     if (p->B != 1) return GDR_ERR_INVALID_ARG;
   } else if (p->num_seqs != p->B) {
@@ -74,6 +75,7 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
   d->dtype = p->dtype;
   d->layout = p->layout;
   d->cu = p->cu_seqlens;
+  d->h_bf16 = p->h_dtype == GDR_DTYPE_BF16 ? 1 : 0;
   d->path = (p->dtype == GDR_DTYPE_BF16 && p->DK == 128 && p->DV == 128 && maxc * p->Hv * kChunk < (1ll << 31) &&
              tc_available())
                 ? 1
@@ -135,7 +137,7 @@ size_t gdr_max_chunks(const gdr_problem* p) {
 size_t gdr_saved_states_bytes(const gdr_problem* p) {
   Dims d;
   if (resolve(p, &d) != GDR_OK) return 0;
-  return (size_t)d.max_chunks * d.Hv * d.DK * d.DV * sizeof(float);
+  return (size_t)d.max_chunks * d.Hv * d.DK * d.DV * (d.h_bf16 ? 2 : 4);
 }
 
 size_t gdr_fwd_workspace_bytes(const gdr_problem* p) {
@@ -157,7 +159,7 @@ int gdr_path(const gdr_problem* p) {
 }
 
 gdr_status gdr_fwd(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
-                   const void* beta, const float* S0, void* o, float* S_T, float* h_saved, void* workspace,
+                   const void* beta, const float* S0, void* o, float* S_T, void* h_saved, void* workspace,
                    size_t workspace_bytes, gdr_stream_t stream) {
   Dims d;
   gdr_status st = resolve(p, &d);
@@ -181,7 +183,7 @@ gdr_status gdr_fwd(const gdr_problem* p, const void* q, const void* k, const voi
 }
 
 gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
-                   const void* beta, const float* h_saved, const void* dO, const float* dS_T, void* dq,
+                   const void* beta, const void* h_saved, const void* dO, const float* dS_T, void* dq,
                    void* dk, void* dv, float* dg, void* dbeta, float* dS0, void* workspace,
                    size_t workspace_bytes, gdr_stream_t stream) {
   Dims d;

@@ -31,6 +31,7 @@ struct Dims {
   int layout;  // gdr_state_layout
   const int32_t* cu;  // device cu_seqlens or nullptr
   int path;    // 1 = tcgen05, 0 = SIMT
+  int h_bf16;  // h_saved holds bf16 (else fp32)
 };
 
 // Pointers into the caller's workspace.  Every region starts 256-byte aligned.
@@ -67,14 +68,14 @@ struct FwdArgs {
   const float* S0;
   void* o;
   float* S_T;
-  float* h_saved;
+  void* h_saved;  // fp32 or bf16 (Dims::h_bf16)
 };
 
 struct BwdArgs {
   const void *q, *k, *v;
   const float* g;
   const void* beta;
-  const float* h_saved;
+  const void* h_saved;  // fp32 or bf16 (Dims::h_bf16)
   const void* dO;
   const float* dS_T;
   void *dq, *dk, *dv;

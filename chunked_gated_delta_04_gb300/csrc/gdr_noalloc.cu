@@ -64,7 +64,7 @@ using namespace gdr;
 
 extern "C" gdr_status gdr_fwd_noalloc(const gdr_problem* p, const void* q, const void* k, const void* v,
                                       const float* g, const void* beta, const float* S0, void* o, float* S_T,
-                                      float* h_saved, gdr_stream_t stream) {
+                                      void* h_saved, gdr_stream_t stream) {
   Dims d;
   gdr_status st = resolve_problem(p, &d);
   if (st != GDR_OK) return st;

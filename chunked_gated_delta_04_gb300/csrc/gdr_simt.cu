@@ -117,6 +117,22 @@ __global__ void __launch_bounds__(kThreads) simt_prep_kernel(Dims d, const IT* _
   }
 }
 
+// Saved chunk-start states: fp32 or bf16 (Dims::h_bf16), read back as fp32.
+struct HView {
+  const void* base;  // first element of one chunk's [DK][DV] state
+  int hb;
+  __device__ __forceinline__ float operator[](size_t e) const {
+    return hb ? __bfloat162float(static_cast<const __nv_bfloat16*>(base)[e]) : static_cast<const float*>(base)[e];
+  }
+};
+
+__device__ __forceinline__ HView h_view(const void* h_saved, size_t ch, const Dims& d) {
+  const size_t off = ch * d.DK * d.DV;
+  return HView{d.h_bf16 ? (const void*)(static_cast<const __nv_bfloat16*>(h_saved) + off)
+                        : (const void*)(static_cast<const float*>(h_saved) + off),
+               d.h_bf16};
+}
+
 // ---------------------------------------------------------------------------------
 // forward state walk: one CTA per (sequence, v-head, DV slice)
 // ---------------------------------------------------------------------------------
@@ -124,7 +140,7 @@ template <typename IT>
 __global__ void __launch_bounds__(kThreads) simt_state_kernel(Dims d, const IT* __restrict__ k,
                                                               const float* __restrict__ S0,
                                                               float* __restrict__ S_T,
-                                                              float* __restrict__ h_saved, Workspace ws,
+                                                              void* __restrict__ h_saved, Workspace ws,
                                                               int dvs) {
   extern __shared__ float sm[];
   const int n = ws.seq_order[blockIdx.x], j = blockIdx.y, i = j / d.G;
@@ -146,7 +162,11 @@ __global__ void __launch_bounds__(kThreads) simt_state_kernel(Dims d, const IT* 
     const size_t ch = (size_t)c * Hv + j;
     for (int e = tid; e < DK * dvs; e += kThreads) {
       const int a = e / dvs, b = e % dvs;
-      h_saved[ch * DK * DV + (size_t)a * DV + dv0 + b] = sh[e];
+      const size_t hi = ch * DK * DV + (size_t)a * DV + dv0 + b;
+      if (d.h_bf16)
+        static_cast<__nv_bfloat16*>(h_saved)[hi] = __float2bfloat16_rn(sh[e]);
+      else
+        static_cast<float*>(h_saved)[hi] = sh[e];
     }
     for (int r = tid; r < kChunk; r += kThreads) sg[r] = ws.gam[ch * kChunk + r];
     const float* W = (const float*)ws.W + ch * kChunk * DK;
@@ -188,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) simt_state_kernel(Dims d, const IT* 
 template <typename IT>
 __global__ void __launch_bounds__(kThreads) simt_out_kernel(Dims d, const IT* __restrict__ q,
                                                             const IT* __restrict__ k,
-                                                            const float* __restrict__ h_saved,
+                                                            const void* __restrict__ h_saved,
                                                             IT* __restrict__ o, Workspace ws) {
   extern __shared__ float sm[];
   const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
@@ -221,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) simt_out_kernel(Dims d, const IT* __
     sP[r * kLd + s] = p;
   }
   __syncthreads();
-  const float* h = h_saved + ch * DK * DV;
+  const HView h = h_view(h_saved, ch, d);
   const float* Vn = (const float*)ws.Vn + ch * kChunk * DV;
   for (int e = tid; e < len * DV; e += kThreads) {
     const int r = e / DV, b = e % DV;
@@ -235,7 +255,7 @@ __global__ void __launch_bounds__(kThreads) simt_out_kernel(Dims d, const IT* __
 // ---------------------------------------------------------------------------------
 // backward: Vn = U - W h from the saved chunk-start states (chunk-parallel)
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) simt_vn_kernel(Dims d, const float* __restrict__ h_saved,
+__global__ void __launch_bounds__(kThreads) simt_vn_kernel(Dims d, const void* __restrict__ h_saved,
                                                            Workspace ws) {
   const int c = blockIdx.x, j = blockIdx.y;
   const int4 ci = ws.chunks[c];
@@ -243,7 +263,7 @@ __global__ void __launch_bounds__(kThreads) simt_vn_kernel(Dims d, const float* 
   if (len <= 0) return;
   const int DK = d.DK, DV = d.DV;
   const size_t ch = (size_t)c * d.Hv + j;
-  const float* h = h_saved + ch * DK * DV;
+  const HView h = h_view(h_saved, ch, d);
   const float* W = (const float*)ws.W + ch * kChunk * DK;
   const float* U = (const float*)ws.U + ch * kChunk * DV;
   float* Vn = (float*)ws.Vn + ch * kChunk * DV;
@@ -353,7 +373,7 @@ __global__ void __launch_bounds__(kThreads) simt_grad_kernel(Dims d, const IT* _
                                                              const IT* __restrict__ k,
                                                              const IT* __restrict__ v,
                                                              const IT* __restrict__ beta,
-                                                             const float* __restrict__ h_saved,
+                                                             const void* __restrict__ h_saved,
                                                              const IT* __restrict__ dO,
                                                              IT* __restrict__ dq, IT* __restrict__ dk,
                                                              IT* __restrict__ dv, float* __restrict__ dg,
@@ -380,7 +400,7 @@ __global__ void __launch_bounds__(kThreads) simt_grad_kernel(Dims d, const IT* _
   float* skdv = sdgam + kChunk;     // k_r^T dh' vn_r
   float* sred = skdv + kChunk;      // [32] block reduction scratch
   const size_t ch = (size_t)c * Hv + j;
-  const float* h = h_saved + ch * DK * DV;
+  const HView h = h_view(h_saved, ch, d);
   const float* dhp = (const float*)ws.dhp + ch * DK * DV;
   const float* Vn = (const float*)ws.Vn + ch * kChunk * DV;
   const float* Tg = ws.Tm + ch * kChunk * kChunk;

@@ -91,6 +91,20 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D map over a [rows][cols] bf16 matrix with a 32-column (64-byte) x box_rows box and
+// 64-byte swizzle: in the shared-memory tile, row r's 16-byte piece c sits at piece
+// position c ^ ((r >> 1) & 3).  (Unswizzled 64-byte rows make the TMA engine's
+// shared-memory reads much slower.)
+static bool map_2d_sw64(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {32, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 // ---------------------------------------------------------------------------------
@@ -412,34 +426,87 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
 }
 
 // ---------------------------------------------------------------------------------
-// tc_fwd_state: sequential chunk walk of one (sequence, v-head, 64-wide DV slice)
+// tc_fwd_state: sequential chunk walk of one (sequence, v-head, 32-wide DV slice).
+// The recurrence over chunks is serial, so the DV columns of the state are split
+// four ways (they evolve independently) to put 4 x sequences x v-heads CTAs on the
+// SMs, and each chunk's output rows are finished while the next chunk's first
+// product runs.
 // ---------------------------------------------------------------------------------
+constexpr int kStateSlices = 4;  // DV = 128 as four 32-column slices
+
 struct StateSmem {
   // per stage: [W|Q] x 2 slabs (32 KB), K 2 slabs (16 KB), [U | P] (16 KB)
   static constexpr uint32_t STAGE = 65536;
   static constexpr uint32_t WQ = 0, K = 32768, U = 49152, P = 57344;
-  static constexpr uint32_t H = 2 * STAGE;        // h as bf16 B operand: 128 rows x 128 B = 16 KB
-  static constexpr uint32_t VN = H + 16384;       // Vn (8 KB)
-  static constexpr uint32_t VT = VN + 8192;       // Vn scaled by e^{gamma_C - gamma} (8 KB)
-  static constexpr uint32_t HS = VT + 8192;       // h (fp32) staged for the TMA store: 2 x 16 KB
-  static constexpr uint32_t OS = HS + 32768;      // o rows (bf16) staged for the TMA store (8 KB)
-  static constexpr uint32_t GAM = OS + 8192;      // gamma of each stage: 2 x 256 B
+  static constexpr uint32_t HT = 2 * STAGE;       // h^T slice (bf16, K-major B operand): 2 slabs of 32 rows
+  static constexpr uint32_t VNT = HT + 8192;      // Vn^T slice: 32 rows x 64 tokens (4 KB)
+  static constexpr uint32_t VTT = VNT + 4096;     // (e^{gamma_C - gamma} Vn)^T slice (4 KB)
+  static constexpr uint32_t HS = VTT + 4096;      // h slice staged for the h_saved store: fp32 (16 KB) or bf16 (8 KB)
+  static constexpr uint32_t GAM = HS + 16384;     // gamma of each stage: 2 x 256 B
   static constexpr uint32_t BYTES = GAM + 512;
 };
+
+// 32 fp32 -> 32 bf16 in global memory (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void st_global_bf16x32(bf16* dst, const float* v) {
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    uint4 w;
+    uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[ch * 8 + 2 * e], v[ch * 8 + 2 * e + 1]);
+      wp[e] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    reinterpret_cast<uint4*>(dst)[ch] = w;
+  }
+}
+
+// Column `col` of a K-major operand tile of 32 rows (one row per DV column of the
+// slice): v[b] goes to row b.  Within a warp the 32 threads hold 32 consecutive
+// columns, so each store instruction touches one 64-byte run of a row.
+__device__ __forceinline__ void st_col32_bf16(unsigned char* tile, int col, const float* v) {
+#pragma unroll
+  for (int b = 0; b < 32; ++b)
+    *reinterpret_cast<bf16*>(tile + tc::sw128_off(b, col, 32)) = __float2bfloat16_rn(v[b]);
+}
+
+// Row `row` (32 fp32 -> bf16, 64 bytes) of a 64-byte-swizzled [rows][32] bf16 tile: piece
+// c at piece position c ^ ((row >> 1) & 3), which also spreads the 32 rows of a warp's
+// store instruction over all 32 banks.
+__device__ __forceinline__ void st_row_bf16x32_sw64(unsigned char* tile, int row, const float* v) {
+  uint4 w[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t* wp = reinterpret_cast<uint32_t*>(&w[c]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[c * 8 + 2 * e], v[c * 8 + 2 * e + 1]);
+      wp[e] = *reinterpret_cast<uint32_t*>(&b);
+    }
+  }
+  const int sw = (row >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(tile + row * 64 + ((c ^ sw) << 4)) = w[c];
+}
 
 __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
-    const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_hs,
-    const __grid_constant__ CUtensorMap tm_o, Dims d, const float* __restrict__ S0, float* __restrict__ S_T,
-    bf16* __restrict__ o, Workspace ws) {
+    const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_hs, Dims d,
+    const float* __restrict__ S0, float* __restrict__ S_T, bf16* __restrict__ o, Workspace ws) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
-  __shared__ uint64_t bar_load[2], bar_mma;
+  __shared__ uint64_t bar_load[2], bar_mma, bar_pv;
   __shared__ uint32_t tmem_slot;
-  const int n = ws.seq_order[blockIdx.x], j = blockIdx.y, i = j / d.G;
-  const int dv0 = blockIdx.z * 64;
+  // block -> (sequence in longest-first order, v-head, DV slice); the slices of one
+  // (sequence, head) are adjacent so they share its W/Q/K tiles in L2
+  const int slice = blockIdx.x % kStateSlices, rest = blockIdx.x / kStateSlices;
+  const int j = rest % d.Hv, n = ws.seq_order[rest / d.Hv], i = j / d.G;
+  const int dv0 = slice * 32;
   const int tid = threadIdx.x, warp = tid >> 5;
+  // thread 0 issues the MMAs; thread 32 (the "copy thread") issues every TMA load and
+  // store and waits on their bulk groups, so neither kind of issue delays the other
+  constexpr int kCopyTid = 32;
   const int Hv = d.Hv;
   const int c_begin = ws.seq_chunk_off[n], c_end = ws.seq_chunk_off[n + 1];
   const int t_seq = d.cu ? d.cu[n] : n * d.T;        // first token of the sequence
@@ -449,21 +516,23 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     tc::mbar_init(&bar_load[0], 1);
     tc::mbar_init(&bar_load[1], 1);
     tc::mbar_init(&bar_mma, 1);
+    tc::mbar_init(&bar_pv, 1);
     tc::fence_barrier_init();
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, 128);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tbase = tmem_slot;
-  const uint32_t D1 = tbase, D2 = tbase + 64, D3 = tbase + 128;
+  // TMEM: [W;Q] h^T (0-31), [U;P] Vn (32-63; lanes 64-127 = P Vn), K^T Vn~ (64-95)
+  const uint32_t D1 = tbase, D2 = tbase + 32, D3 = tbase + 64;
 
-  // h row `tid` (dk = tid), columns dv0 .. dv0 + 63
-  float h[64];
+  // h row `tid` (dk = tid), columns dv0 .. dv0 + 31
+  float h[32];
   {
     const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
 #pragma unroll
-    for (int b = 0; b < 64; ++b)
+    for (int b = 0; b < 32; ++b)
       h[b] = S0 ? S0[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] : 0.f;
   }
   auto issue_loads = [&](int c, int st) {
@@ -478,25 +547,41 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     tc::tma_load_3d(base + StateSmem::WQ + 3 * kSlab, &tm_q, &bar_load[st], 64, i, tc0);
     tc::tma_load_3d(base + StateSmem::K, &tm_k, &bar_load[st], 0, i, tc0);
     tc::tma_load_3d(base + StateSmem::K + kSlab, &tm_k, &bar_load[st], 64, i, tc0);
-    tc::tma_load_2d(base + StateSmem::U, &tm_u, &bar_load[st], dv0, (int)(chh * 64));
+    tc::tma_load_2d(base + StateSmem::U, &tm_u, &bar_load[st], dv0 & 64, (int)(chh * 64));  // 64-col tile
     tc::tma_load_2d(base + StateSmem::P, &tm_p, &bar_load[st], 0, (int)(chh * 64));
   };
-  if (tid == 0 && c_begin < c_end) issue_loads(c_begin, 0);
-  st_row_bf16(sm + StateSmem::H, tid, h);
+  if (tid == kCopyTid && c_begin < c_end) issue_loads(c_begin, 0);
+  st_col32_bf16(sm + StateSmem::HT, tid, h);
 
   bool ok = true;
   uint32_t mma_phase = 0;
   GDR_TRACE_INIT();
-  const uint32_t s_h = tc::smem_u32(sm + StateSmem::H), s_vn = tc::smem_u32(sm + StateSmem::VN);
-  const uint32_t s_vt = tc::smem_u32(sm + StateSmem::VT);
+  const uint32_t s_ht = tc::smem_u32(sm + StateSmem::HT), s_vnt = tc::smem_u32(sm + StateSmem::VNT);
+  const uint32_t s_vtt = tc::smem_u32(sm + StateSmem::VTT);
+  const int r = tid & 63;
+  // output rows of the previous chunk, finished during this chunk's first product
+  // (warps 2-3: row r = tid - 64): (Q h)[r] slice, e^{gamma_r}, chunk start and length
+  float xq[32];
+  float p_eg = 0.f;
+  int p_t0 = 0, p_len = 0;
+  auto finish_o = [&](uint32_t pv_phase) {  // o[r] = scale (e^{gamma_r} (Q h)[r] + (P Vn)[r]) of the previous chunk
+    float y[32];
+    if (!tc::mbar_wait(&bar_pv, pv_phase, ws.status, kDevErrTimeoutFwd)) return;
+    tc::tc_fence_after();
+    tmem_ld32w(tbase, warp, 32, y);
+    if (r < p_len) {
+#pragma unroll
+      for (int b = 0; b < 32; ++b) y[b] = d.scale * (p_eg * xq[b] + y[b]);
+      st_global_bf16x32(o + ((size_t)(p_t0 + r) * Hv + j) * 128 + dv0, y);
+    }
+  };
   for (int c = c_begin; c < c_end && ok; ++c) {
     const int it = c - c_begin, st = it & 1;
     const uint32_t ld_phase = (it >> 1) & 1;
     const int t0 = t_seq + it * 64;
     const int len = min(64, L - it * 64);
     const size_t chh = (size_t)c * Hv + j;
-    // h (bf16 B operand) was written at the end of the previous chunk / before the loop
-    const int r = tid & 63;
+    // h^T (bf16 B operand) was written at the end of the previous chunk / before the loop
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
@@ -511,39 +596,49 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     const uint32_t s_up = tc::smem_u32(stg + StateSmem::U);
     if (ok && tid == 0) {
       tc::tc_fence_after();
-      const uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
+      const uint32_t id = tc::idesc_bf16(128, 32, 0, 0);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)  // [W;Q] h
-        tc::mma_bf16(D1, tc::kmajor_step_desc(s_wq, 2 * kSlab, kk), tc::mnmajor_step_desc(s_h, 16384, kk), id, kk > 0);
+        tc::mma_bf16(D1, tc::kmajor_step_desc(s_wq, 2 * kSlab, kk), tc::kmajor_step_desc(s_ht, 4096, kk), id, kk > 0);
       tc::mma_commit(&bar_mma);
     }
-    if (tid == 0 && c + 1 < c_end) issue_loads(c + 1, st ^ 1);  // overlaps the MMA
-    // while [W;Q] h runs: stage the chunk-start state (fp32) for its h_saved store
-    st_row_f32x32(sm + StateSmem::HS, tid, h);
-    st_row_f32x32(sm + StateSmem::HS + 16384, tid, h + 32);
+    GDR_TRACE_MARK(1, 7);
+    if (tid == kCopyTid && c + 1 < c_end) issue_loads(c + 1, st ^ 1);  // overlaps the MMA
+    GDR_TRACE_MARK(1, 8);
+    // while [W;Q] h runs: stage the chunk-start state (fp32) for its h_saved store, and
+    // finish the previous chunk's output rows (P Vn is still in TMEM)
+    if (d.h_bf16)  // bf16 saved states: a 64-byte-swizzled [128][32] bf16 tile
+      st_row_bf16x32_sw64(sm + StateSmem::HS, tid, h);
+    else
+      st_row_f32x32(sm + StateSmem::HS, tid, h);
+    if (ok && warp >= 2 && it > 0) finish_o((it - 1) & 1);
     tc::fence_proxy_async_smem();
+    GDR_TRACE_MARK(1, 6);
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutFwd));
     mma_phase ^= 1;
     tc::tc_fence_after();
-    if (tid == 0) {  // h_saved[chunk] rows 0..127, columns dv0..dv0+63
+    if (ok && tid == kCopyTid) {  // h_saved[chunk] rows 0..127, columns dv0..dv0+31
       tc::tma_store_2d(&tm_hs, sm + StateSmem::HS, dv0, (int)(chh * 128));
-      tc::tma_store_2d(&tm_hs, sm + StateSmem::HS + 16384, dv0 + 32, (int)(chh * 128));
       tc::bulk_commit();
     }
     GDR_TRACE_MARK(1, 2);
-    float x[64];
     if (ok) {
-      tmem_ld64(tbase, warp, 0, x);
-      if (tid < 64) {  // Vn = U - W h
-        float u[64];
-        ld_row_bf16(stg + StateSmem::U, r, u);
+      if (warp < 2) {  // Vn = U - W h (rows >= len are zero: W and U are zero there)
+        float x[32], u[32];
+        tmem_ld32w(tbase, warp, 0, x);
+        ld_halfrow_bf16(stg + StateSmem::U, r, (dv0 >> 5) & 1, u);
 #pragma unroll
-        for (int b = 0; b < 64; ++b) u[b] -= x[b];
-        st_row_bf16(sm + StateSmem::VN, r, u);
+        for (int b = 0; b < 32; ++b) u[b] -= x[b];
+        st_col32_bf16(sm + StateSmem::VNT, r, u);
         const float dec = fexp(gC - gr);
 #pragma unroll
-        for (int b = 0; b < 64; ++b) u[b] *= dec;
-        st_row_bf16(sm + StateSmem::VT, r, u);
+        for (int b = 0; b < 32; ++b) u[b] *= dec;
+        st_col32_bf16(sm + StateSmem::VTT, r, u);
+      } else {  // keep (Q h)[r] for the output rows
+        tmem_ld32w(tbase, warp, 0, xq);
+        p_eg = fexp(gr);
+        p_t0 = t0;
+        p_len = len;
       }
     }
     tc::fence_proxy_async_smem();
@@ -552,62 +647,50 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     GDR_TRACE_MARK(1, 3);
     if (ok && tid == 0) {
       tc::tc_fence_after();
-      const uint32_t id = tc::idesc_bf16(128, 64, 0, 1);
-      const uint32_t idt = tc::idesc_bf16(128, 64, 1, 1);
+      const uint32_t id = tc::idesc_bf16(128, 32, 0, 0);
+      const uint32_t idt = tc::idesc_bf16(128, 32, 1, 0);
+      // K^T Vn~ (A = K^T, the MN-major view of the K tile) feeds the recurrence: first,
+      // with its own commit
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        // rows 64-127 of this A operand are P (rows 0-63 are the U tile: unused lanes)
-        tc::mma_bf16(D2, tc::kmajor_step_desc(s_up, kSlab, kk), tc::mnmajor_step_desc(s_vn, kSlab, kk), id, kk > 0);
-        // K^T Vn~: A = K^T (MN-major view of the K tile)
-        tc::mma_bf16(D3, tc::mnmajor_step_desc(s_k, kSlab, kk), tc::mnmajor_step_desc(s_vt, kSlab, kk), idt, kk > 0);
-      }
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma_bf16(D3, tc::mnmajor_step_desc(s_k, kSlab, kk), tc::kmajor_step_desc(s_vtt, 4096, kk), idt, kk > 0);
       tc::mma_commit(&bar_mma);
+      // P Vn for the output rows: rows 64-127 of this A operand are P (rows 0-63 are the
+      // U tile: unused lanes)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        tc::mma_bf16(D2, tc::kmajor_step_desc(s_up, kSlab, kk), tc::kmajor_step_desc(s_vnt, 4096, kk), id, kk > 0);
+      tc::mma_commit(&bar_pv);
     }
-    if (tid == 0) tc::bulk_wait_read<1>();  // the previous chunk's o store has left the staging tile
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutFwd));
     mma_phase ^= 1;
     tc::tc_fence_after();
     GDR_TRACE_MARK(1, 4);
     if (ok) {
-      float y[64];
-      tmem_ld64(tbase, warp, 128, y);  // h <- e^{gamma_C} h + K^T Vn~, then stage it for the next chunk
+      float y[32];
+      tmem_ld32w(tbase, warp, 64, y);  // h <- e^{gamma_C} h + K^T Vn~, then stage it for the next chunk
       const float eC = fexp(gC);
 #pragma unroll
-      for (int b = 0; b < 64; ++b) h[b] = eC * h[b] + y[b];
-      st_row_bf16(sm + StateSmem::H, tid, h);
-      if (tid >= 64) {  // O rows: x holds (Q h)[r], D2 lanes 64-127 hold (P Vn)[r]
-        tmem_ld64(tbase, warp, 64, y);
-        if (r < len) {
-          const float eg = fexp(gr);
-#pragma unroll
-          for (int b = 0; b < 64; ++b) y[b] = d.scale * (eg * x[b] + y[b]);
-          if (len == 64)
-            st_row_bf16(sm + StateSmem::OS, r, y);  // full chunk: one TMA store below
-          else
-            st_global_bf16x64(o + ((size_t)(t0 + r) * Hv + j) * 128 + dv0, y);
-        }
-      }
+      for (int b = 0; b < 32; ++b) h[b] = eC * h[b] + y[b];
+      st_col32_bf16(sm + StateSmem::HT, tid, h);
     }
-    if (tid == 0) tc::bulk_wait_read<0>();  // h staging free for the next chunk
-    tc::fence_proxy_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    if (ok && tid == 0 && len == 64) {
-      tc::tma_store_3d(&tm_o, sm + StateSmem::OS, dv0, j, t0);
-      tc::bulk_commit();
-    }
+    if (tid == kCopyTid) tc::bulk_wait_read<0>();  // h staging free for the next chunk
     GDR_TRACE_MARK(1, 5);
   }
-  if (tid == 0) tc::bulk_wait_read<0>();  // smem sources read before exit
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (ok && warp >= 2 && c_begin < c_end) finish_o((c_end - c_begin - 1) & 1);  // the last chunk's output rows
+  if (tid == kCopyTid) tc::bulk_wait_read<0>();  // smem sources read before exit
   if (ok && S_T) {
     const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
 #pragma unroll
-    for (int b = 0; b < 64; ++b)
+    for (int b = 0; b < 32; ++b)
       S_T[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] = h[b];
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tbase, 256);
+  if (warp == 0) tc::tmem_dealloc(tbase, 128);
 }
 
 }  // namespace
@@ -633,15 +716,16 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
   if (!get_encoder()) return cudaErrorNotSupported;
   // Maps are built only when there are tokens; with none, no kernel reads them (every
   // chunk slot is empty and the state kernel only copies S0 to S_T).
-  CUtensorMap tq{}, tk{}, tv{}, tw{}, tu{}, tp{}, ths{}, tov{};
+  CUtensorMap tq{}, tk{}, tv{}, tw{}, tu{}, tp{}, ths{};
   const uint64_t Tt = (uint64_t)d.T_total;
   const uint64_t rows = (uint64_t)d.max_chunks * d.Hv * 64;
   if (Tt == 0 && d.num_seqs == 0) return cudaSuccess;
   if (Tt > 0) {
     if (!map_3d(&tq, a.q, 128, d.Hk, Tt) || !map_3d(&tk, a.k, 128, d.Hk, Tt) || !map_3d(&tv, a.v, 128, d.Hv, Tt) ||
-        !map_3d(&tov, a.o, 128, d.Hv, Tt) || !map_2d(&tw, ws.W, 128, rows) || !map_2d(&tu, ws.U, 128, rows) ||
+        !map_2d(&tw, ws.W, 128, rows) || !map_2d(&tu, ws.U, 128, rows) ||
         !map_2d(&tp, ws.P, 64, rows) ||
-        !map_2d_box(&ths, a.h_saved, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, rows * 2, 32, 128))
+        !(d.h_bf16 ? map_2d_sw64(&ths, a.h_saved, 128, rows * 2, 128)
+                   : map_2d_box(&ths, a.h_saved, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, rows * 2, 32, 128)))
       return cudaErrorInvalidValue;
   }
   if (d.max_chunks > 0 && Tt > 0) {
@@ -654,8 +738,8 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
   if (d.num_seqs > 0) {
     const size_t sms = StateSmem::BYTES + 1024;
     cudaFuncSetAttribute(tc_fwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
-    tc_fwd_state_kernel<<<dim3(d.num_seqs, d.Hv, 2), kTcThreads, sms, s>>>(tq, tk, tw, tu, tp, ths, tov, d, a.S0,
-                                                                         a.S_T, (bf16*)a.o, ws);
+    tc_fwd_state_kernel<<<d.num_seqs * d.Hv * kStateSlices, kTcThreads, sms, s>>>(tq, tk, tw, tu, tp, ths, d, a.S0,
+                                                                                 a.S_T, (bf16*)a.o, ws);
     stage_mark(s, "fwd_state");
   }
   return cudaGetLastError();

@@ -33,29 +33,6 @@ using namespace tcx;
 using tc::kmaj;
 using tc::mnmaj;
 
-__device__ __forceinline__ void ld_row_bf16_g(const bf16* src, float* v) {  // 64 bf16 from global
-#pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    const uint4 w = reinterpret_cast<const uint4*>(src)[ch];
-    const uint32_t* wp = reinterpret_cast<const uint32_t*>(&w);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wp[e]));
-      v[ch * 8 + 2 * e] = f.x;
-      v[ch * 8 + 2 * e + 1] = f.y;
-    }
-  }
-}
-
-__device__ __forceinline__ float block_sum128(float x, float* red) {  // fixed-order sum over 128 threads
-  x = warp_sum(x);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
-  __syncthreads();
-  const float s = (red[0] + red[1]) + (red[2] + red[3]);
-  __syncthreads();
-  return s;
-}
-
 // ---------------------------------------------------------------------------------
 // walk
 // ---------------------------------------------------------------------------------
@@ -68,7 +45,9 @@ struct WalkSmem {
   static constexpr uint32_t BYTES = DOS + 8192;
 };
 
-__global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
+constexpr int kWalkThreads = 256;  // two warps per TMEM lane quarter, each on 32 of the 64 columns
+
+__global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
     const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dhs,
@@ -80,7 +59,14 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
   __shared__ uint32_t tmem_slot;
   const int n = ws.seq_order[blockIdx.x], j = blockIdx.y, i = j / d.G;
   const int dv0 = blockIdx.z * 64;
-  const int tid = threadIdx.x, warp = tid >> 5, r = tid & 63;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int hf = warp >> 2;            // column half [32 hf, 32 hf + 32) of the slice
+  const int dk = tid & 127;            // TMEM lane = row of the dh' slice
+  const int r = tid & 63;              // token row for the 64-row products (lanes 0-63)
+  const bool lo = (warp & 3) < 2;      // warps on TMEM lanes 0-63
+  // thread 0 issues the MMAs; thread 64 (the "copy thread", in a warp that has no part in
+  // the dVn rows) issues every TMA load and store and waits on their bulk groups
+  constexpr int kCopyTid = 64;
   const int Hv = d.Hv;
   const int c_begin = ws.seq_chunk_off[n], c_end = ws.seq_chunk_off[n + 1];
   const int t_seq = d.cu ? d.cu[n] : n * d.T;
@@ -97,14 +83,16 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tb = tmem_slot;
+  // TMEM: K dh' (0-63), P^T dO (64-127), W^T dVn (128-191), Q^T diag(e^gamma) dO (192-255)
   const uint32_t Da = tb, Db = tb + 64, Dc = tb + 128, Dd = tb + 192;
 
-  float dh[64];  // dL/dh at the end of the current chunk, row dk = tid, columns dv0..dv0+63
+  float dh[32];  // dL/dh at the end of the current chunk: row dk, columns dv0 + 32 hf + (0..31)
   {
     const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
+    const int c0 = dv0 + 32 * hf;
 #pragma unroll
-    for (int b = 0; b < 64; ++b)
-      dh[b] = dS_T ? dS_T[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] : 0.f;
+    for (int b = 0; b < 32; ++b)
+      dh[b] = dS_T ? dS_T[sb + (d.layout == 0 ? (size_t)dk * 128 + c0 + b : (size_t)(c0 + b) * 128 + dk)] : 0.f;
   }
   auto issue_loads = [&](int c, int st) {
     const int tc0 = t_seq + (c - c_begin) * 64;
@@ -122,93 +110,112 @@ __global__ void __launch_bounds__(kTcThreads) tc_bwd_walk_kernel(
     tc::tma_load_2d(base + WalkSmem::P, &tm_p, bar, 0, (int)(chh * 64));
     tc::tma_load_3d(base + WalkSmem::DO, &tm_do, bar, dv0, j, tc0);
   };
-  if (tid == 0 && c_begin < c_end) issue_loads(c_end - 1, 0);
+  if (tid == kCopyTid && c_begin < c_end) issue_loads(c_end - 1, 0);
 
   bool ok = true;
   uint32_t mma_phase = 0;
+  GDR_TRACE_INIT();
   for (int it = 0; c_end - 1 - it >= c_begin && ok; ++it) {
     const int c = c_end - 1 - it, st = it & 1;
     const uint32_t ld_phase = (it >> 1) & 1;
-    const int t0 = t_seq + (c - c_begin) * 64;
     const int len = min(64, L - (c - c_begin) * 64);
-    (void)t0;
     const size_t chh = (size_t)c * Hv + j;
-    st_row_bf16(sm + WalkSmem::DH, tid, dh);
+    st_halfrow_bf16(sm + WalkSmem::DH, dk, hf, dh);
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // dh' of this chunk -> workspace, straight from the operand tile
+    if (tid == kCopyTid) {  // dh' of this chunk -> workspace, straight from the operand tile
       tc::tma_store_2d(&tm_dhs, sm + WalkSmem::DH, dv0, (int)(chh * 128));
       tc::bulk_commit();
     }
+    GDR_TRACE_MARK(3, 0);
     ok = __syncthreads_and(tc::mbar_wait(&bar_load[st], ld_phase, ws.status, kDevErrTimeoutBwd));
+    GDR_TRACE_MARK(3, 1);
     unsigned char* stg = sm + st * WalkSmem::STAGE;
     const float* sgam = reinterpret_cast<const float*>(stg + WalkSmem::GAM);
     const float gC = sgam[len - 1], gr = sgam[r];
-    if (ok && tid >= 64) {  // diag(e^gamma) dO, zero past the chunk end
-      float x[64];
-      ld_row_bf16(stg + WalkSmem::DO, r, x);
-      const float e = r < len ? fexp(gr) : 0.f;
-#pragma unroll
-      for (int b = 0; b < 64; ++b) x[b] *= e;
-      st_row_bf16(sm + WalkSmem::DOS, r, x);
-    }
-    tc::fence_proxy_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
+    // the dh'-dependent products first; Q^T diag(e^gamma) dO waits for its scaled operand
     if (ok && tid == 0) {
       tc::tc_fence_after();
       tc::gemm(Da, kmaj(stg + WalkSmem::KQ, 2 * kSlab), mnmaj(sm + WalkSmem::DH, 16384), 64, 8, false);  // K dh'
       tc::gemm(Db, mnmaj(stg + WalkSmem::P, kSlab), mnmaj(stg + WalkSmem::DO, kSlab), 64, 4, false);     // P^T dO
-      tc::gemm(Dd, mnmaj(stg + WalkSmem::KQ + kSlab, 2 * kSlab), mnmaj(sm + WalkSmem::DOS, kSlab), 64, 4,
-               false);  // Q^T diag(e^gamma) dO
       tc::mma_commit(&bar_mma);
     }
-    if (tid == 0 && c - 1 >= c_begin) issue_loads(c - 1, st ^ 1);  // overlaps the MMAs
-    if (tid == 0) tc::bulk_wait_read<1>();  // the previous chunk's dVn store has left its tile
+    GDR_TRACE_MARK(3, 7);
+    if (tid == kCopyTid && c - 1 >= c_begin) issue_loads(c - 1, st ^ 1);  // overlaps the MMAs
+    GDR_TRACE_MARK(3, 8);
+    if (tid == kCopyTid) tc::bulk_wait_read<1>();  // the previous chunk's dVn store has left its tile
+    GDR_TRACE_MARK(3, 9);
+    if (ok && warp >= 4) {  // diag(e^gamma) dO, zero past the chunk end: row r, half (tid >> 6) & 1
+      float x[32];
+      const int h2 = (tid >> 6) & 1;
+      ld_halfrow_bf16(stg + WalkSmem::DO, r, h2, x);
+      const float e = r < len ? fexp(gr) : 0.f;
+#pragma unroll
+      for (int b = 0; b < 32; ++b) x[b] *= e;
+      st_halfrow_bf16(sm + WalkSmem::DOS, r, h2, x);
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (ok && tid == 0) {  // committed together with W^T dVn below
+      tc::tc_fence_after();
+      tc::gemm(Dd, mnmaj(stg + WalkSmem::KQ + kSlab, 2 * kSlab), mnmaj(sm + WalkSmem::DOS, kSlab), 64, 4,
+               false);  // Q^T diag(e^gamma) dO
+    }
+    GDR_TRACE_MARK(3, 2);
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutBwd));
     mma_phase ^= 1;
     tc::tc_fence_after();
-    if (ok && tid < 64) {
-      float x[64], y[64];
-      tmem_ld64(tb, warp, 0, x);
-      tmem_ld64(tb, warp, 64, y);
+    GDR_TRACE_MARK(3, 3);
+    if (ok && lo) {  // dVn = scale P^T dO + diag(e^{gamma_C - gamma}) K dh', row r, half hf
+      float x[32], y[32];
+      tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 32 * hf), x);
+      tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 64 + 32 * hf), y);
+      tc::tmem_wait_ld();
       const float dec = fexp(gC - gr);
 #pragma unroll
-      for (int b = 0; b < 64; ++b) y[b] = r < len ? d.scale * y[b] + dec * x[b] : 0.f;
-      st_row_bf16(sm + WalkSmem::DVN, r, y);
+      for (int b = 0; b < 32; ++b) y[b] = r < len ? d.scale * y[b] + dec * x[b] : 0.f;
+      st_halfrow_bf16(sm + WalkSmem::DVN, r, hf, y);
     }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     if (ok && tid == 0) {
-      tc::tma_store_2d(&tm_dvs, sm + WalkSmem::DVN, dv0, (int)(chh * 64));
-      tc::bulk_commit();
       tc::tc_fence_after();
       tc::gemm(Dc, mnmaj(stg + WalkSmem::W, kSlab), mnmaj(sm + WalkSmem::DVN, kSlab), 64, 4, false);  // W^T dVn
       tc::mma_commit(&bar_mma);
     }
+    if (ok && tid == kCopyTid) {
+      tc::tma_store_2d(&tm_dvs, sm + WalkSmem::DVN, dv0, (int)(chh * 64));
+      tc::bulk_commit();
+    }
+    GDR_TRACE_MARK(3, 4);
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutBwd));
     mma_phase ^= 1;
     tc::tc_fence_after();
+    GDR_TRACE_MARK(3, 5);
     if (ok) {
-      float x[64], y[64];
-      tmem_ld64(tb, warp, 128, x);
-      tmem_ld64(tb, warp, 192, y);
+      float x[32], y[32];
+      tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 128 + 32 * hf), x);
+      tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 192 + 32 * hf), y);
+      tc::tmem_wait_ld();
       const float eC = fexp(gC);
 #pragma unroll
-      for (int b = 0; b < 64; ++b) dh[b] = eC * dh[b] + d.scale * y[b] - x[b];
+      for (int b = 0; b < 32; ++b) dh[b] = eC * dh[b] + d.scale * y[b] - x[b];
     }
-    if (tid == 0) tc::bulk_wait_read<1>();  // this chunk's dh' store has left the operand tile
+    if (tid == kCopyTid) tc::bulk_wait_read<1>();  // this chunk's dh' store has left the operand tile
     tc::tc_fence_before();
     __syncthreads();
+    GDR_TRACE_MARK(3, 6);
   }
-  if (tid == 0) tc::bulk_wait_read<0>();  // smem sources read before exit
+  if (tid == kCopyTid) tc::bulk_wait_read<0>();  // smem sources read before exit
   if (ok && dS0) {
     const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
+    const int c0 = dv0 + 32 * hf;
 #pragma unroll
-    for (int b = 0; b < 64; ++b)
-      dS0[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] = dh[b];
+    for (int b = 0; b < 32; ++b)
+      dS0[sb + (d.layout == 0 ? (size_t)dk * 128 + c0 + b : (size_t)(c0 + b) * 128 + dk)] = dh[b];
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -263,6 +270,9 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   const int quarter = warp & 3, hf = warp >> 2;  // TMEM lane quarter, column half
   const bool lo = quarter < 2;                    // lanes 0-63 (rows of the 64-row products)
   const int r = (quarter & 1) * 32 + lane;        // row within the lane half
+  // thread 0 issues the MMAs; thread 64 (the "copy thread", in warp 2, which has no part
+  // in the 64-row epilogues) issues every TMA load and store and waits on the bulk groups
+  constexpr int kCopyTid = 64;
   const int Hv = d.Hv;
   using S = GradSmem;
 
@@ -281,39 +291,67 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   const uint32_t C_KK = tb, C_DQ = tb + 256, C_DK = tb + 384;
   GDR_TRACE_INIT();
   // Persistent: each CTA walks the (chunk, v-head) items w = blockIdx.x + k * gridDim.x,
-  // keeping its barriers, TMEM and (warm) instruction cache across items.
+  // keeping its barriers, TMEM and (warm) instruction cache across items.  The next
+  // item's tiles are fetched as soon as the current item is done with their buffers
+  // (dh' and dVn after R2, W after R3, K/Q, U, h and gamma after R4, dO after the dk
+  // store), all on the next phase of bar_tma, so the loads overlap the current item.
   bool ok = true;
   uint32_t item_par = 0;  // phase parity of bar_tma / bar_tma2 for the current item
   const int n_items = d.max_chunks * Hv;
-  for (int witem = blockIdx.x; witem < n_items && ok; witem += gridDim.x) {
+  auto next_item = [&](int w) {  // next non-empty item of this CTA after w (or n_items)
+    for (w += gridDim.x; w < n_items && ws.chunks[w / Hv].z <= 0; w += gridDim.x) {
+    }
+    return w < n_items ? w : n_items;
+  };
+  enum : int { kLdDhDvn = 1, kLdW = 2, kLdRest = 4, kLdDo = 8, kLdAll = 15 };
+  auto issue_loads = [&](int w, int groups) {  // copy thread only
+    const int c2 = w / Hv, j2 = w % Hv, i2 = j2 / d.G, tt = ws.chunks[c2].y;
+    const size_t ch2 = (size_t)c2 * Hv + j2;
+    uint64_t* bar = &bar_tma;
+    if (groups & kLdDhDvn) {  // the first group of an item sets the whole item's byte count
+      tc::mbar_arrive_expect_tx(bar, (d.h_bf16 ? 20 : 24) * kSlab + 256);
+      for (int q4 = 0; q4 < 4; ++q4)  // dh' rows (q4 & 1) * 64.., columns (q4 >> 1) * 64..
+        tc::tma_load_2d(sm + S::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
+                        (int)(ch2 * 128 + (q4 & 1) * 64));
+      tc::tma_load_2d(sm + S::DVN, &tm_dvn, bar, 0, (int)(ch2 * 64));
+      tc::tma_load_2d(sm + S::DVN + kSlab, &tm_dvn, bar, 64, (int)(ch2 * 64));
+    }
+    if (groups & kLdW) {
+      tc::tma_load_2d(sm + S::W, &tm_w, bar, 0, (int)(ch2 * 64));
+      tc::tma_load_2d(sm + S::W + kSlab, &tm_w, bar, 64, (int)(ch2 * 64));
+    }
+    if (groups & kLdRest) {
+      tc::bulk_load(sm + S::GAM, ws.gam + ch2 * 64, 256, bar);
+      tc::tma_load_3d(sm + S::KQ, &tm_k, bar, 0, i2, tt);
+      tc::tma_load_3d(sm + S::KQ + 2 * kSlab, &tm_k, bar, 64, i2, tt);
+      tc::tma_load_3d(sm + S::KQ + kSlab, &tm_q, bar, 0, i2, tt);
+      tc::tma_load_3d(sm + S::KQ + 3 * kSlab, &tm_q, bar, 64, i2, tt);
+      tc::tma_load_2d(sm + S::UT, &tm_u, bar, 0, (int)(ch2 * 64));
+      tc::tma_load_2d(sm + S::UT + kSlab, &tm_u, bar, 64, (int)(ch2 * 64));
+      if (d.h_bf16) {  // h (bf16) straight into its operand tile, laid out like dh'
+        for (int q4 = 0; q4 < 4; ++q4)
+          tc::tma_load_2d(sm + S::H + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_h, bar, (q4 >> 1) * 64,
+                          (int)(ch2 * 128 + (q4 & 1) * 64));
+      } else {  // h (fp32) as four 32-column slabs of 128 rows over H|VN|OH, converted in place
+        for (int q4 = 0; q4 < 4; ++q4)
+          tc::tma_load_2d(sm + S::H + q4 * 16384, &tm_h, bar, q4 * 32, (int)(ch2 * 128));
+      }
+    }
+    if (groups & kLdDo) {
+      tc::tma_load_3d(sm + S::DO, &tm_do, bar, 0, j2, tt);
+      tc::tma_load_3d(sm + S::DO + kSlab, &tm_do, bar, 64, j2, tt);
+    }
+  };
+  int witem = blockIdx.x < n_items && ws.chunks[blockIdx.x / Hv].z <= 0 ? next_item(blockIdx.x) : blockIdx.x;
+  if (tid == kCopyTid && witem < n_items) issue_loads(witem, kLdAll);
+  int pending = witem < n_items ? 0 : -1;  // groups of the next item issued so far (-1: none expected)
+  for (int wnext; witem < n_items && ok; witem = wnext) {
+  wnext = next_item(witem);
   const int c = witem / Hv, j = witem % Hv, i = j / d.G;
   const int4 ci = ws.chunks[c];
   const int len = ci.z, t0 = ci.y;
-  if (len <= 0) continue;  // empty chunk slot (uniform across the CTA)
   const size_t ch = (size_t)c * Hv + j;
-  if (tid == 0) {
-    uint64_t* bar = &bar_tma;
-    tc::mbar_arrive_expect_tx(bar, 24 * kSlab + 256);
-    tc::bulk_load(sm + S::GAM, ws.gam + ch * 64, 256, bar);
-    tc::tma_load_3d(sm + S::KQ, &tm_k, bar, 0, i, t0);
-    tc::tma_load_3d(sm + S::KQ + 2 * kSlab, &tm_k, bar, 64, i, t0);
-    tc::tma_load_3d(sm + S::KQ + kSlab, &tm_q, bar, 0, i, t0);
-    tc::tma_load_3d(sm + S::KQ + 3 * kSlab, &tm_q, bar, 64, i, t0);
-    tc::tma_load_3d(sm + S::DO, &tm_do, bar, 0, j, t0);
-    tc::tma_load_3d(sm + S::DO + kSlab, &tm_do, bar, 64, j, t0);
-    tc::tma_load_2d(sm + S::W, &tm_w, bar, 0, (int)(ch * 64));
-    tc::tma_load_2d(sm + S::W + kSlab, &tm_w, bar, 64, (int)(ch * 64));
-    tc::tma_load_2d(sm + S::DVN, &tm_dvn, bar, 0, (int)(ch * 64));
-    tc::tma_load_2d(sm + S::DVN + kSlab, &tm_dvn, bar, 64, (int)(ch * 64));
-    tc::tma_load_2d(sm + S::UT, &tm_u, bar, 0, (int)(ch * 64));
-    tc::tma_load_2d(sm + S::UT + kSlab, &tm_u, bar, 64, (int)(ch * 64));
-    for (int q4 = 0; q4 < 4; ++q4) {  // dh' rows (q4 & 1) * 64.., columns (q4 >> 1) * 64..
-      tc::tma_load_2d(sm + S::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
-                      (int)(ch * 128 + (q4 & 1) * 64));
-      // h (fp32) as four 32-column slabs of 128 rows over H|VN|OH, converted in place below
-      tc::tma_load_2d(sm + S::H + q4 * 16384, &tm_h, bar, q4 * 32, (int)(ch * 128));
-    }
-  }
+  pending = wnext < n_items ? 0 : -1;
   if (tid < 64) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * Hv + j]) : 0.f;
   ok = __syncthreads_and(tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutBwd));
   const float* sgam = reinterpret_cast<const float*>(sm + S::GAM);
@@ -326,7 +364,16 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   // tid & 127, column half tid >> 7).  bf16 slab s overwrites fp32 slab s, which only the
   // half-0 threads read before the barrier.  <dh', h> is accumulated on the way.
   float hdh = 0.f;
-  {
+  if (d.h_bf16) {  // h arrived as bf16 operand slabs: only <dh', h>
+    const int hrow = tid & 127, hh = tid >> 7;
+    float hv[64], dv_[64];
+    if (ok) {
+      ld_row_bf16(sm + S::H + hh * 16384, hrow, hv);
+      ld_row_bf16(sm + S::DH + hh * 16384, hrow, dv_);
+#pragma unroll
+      for (int b = 0; b < 64; ++b) hdh += hv[b] * dv_[b];
+    }
+  } else {
     const int hrow = tid & 127, hh = tid >> 7;
     float hv[64], dv_[64];
     if (ok) {
@@ -374,7 +421,7 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 2);
-  if (ok && tid == 0) {  // O-hat and h are consumed: fetch V and T for the WY backward
+  if (ok && tid == kCopyTid) {  // O-hat and h are consumed: fetch V and T for the WY backward
     tc::mbar_arrive_expect_tx(&bar_tma2, 3 * kSlab);
     tc::tma_load_3d(sm + S::V, &tm_v, &bar_tma2, 0, j, t0);
     tc::tma_load_3d(sm + S::V + kSlab, &tm_v, &bar_tma2, 64, j, t0);
@@ -527,12 +574,12 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   }
   GDR_TRACE_MARK(2, 7);
   // R2: T^T dVn = dB_v (128-255), X = T^T dT (64-127)
+  if (ok && tid == kCopyTid && !kGroup && len == 64) {
+    tc::tma_store_3d(&tm_dq, sm + S::DQS, 0, i, t0);
+    tc::tma_store_3d(&tm_dq, sm + S::DQS + kSlab, 64, i, t0);
+    tc::bulk_commit();
+  }
   if (ok && tid == 0) {
-    if (!kGroup && len == 64) {
-      tc::tma_store_3d(&tm_dq, sm + S::DQS, 0, i, t0);
-      tc::tma_store_3d(&tm_dq, sm + S::DQS + kSlab, 64, i, t0);
-      tc::bulk_commit();
-    }
     tc::tc_fence_after();
     tc::gemm(tb + 128, mnmaj(sm + S::T, kSlab), mnmaj(sm + S::DVN, kSlab), 128, 4, false);
     tc::gemm(tb + 64, mnmaj(sm + S::T, kSlab), mnmaj(sm + S::DT, kSlab), 64, 4, false);
@@ -540,6 +587,11 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
+  if (ok && tid == kCopyTid && pending >= 0) {  // dVn is consumed, dq has left its staging tile
+    tc::bulk_wait_read<0>();
+    issue_loads(wnext, kLdDhDvn);
+    pending |= kLdDhDvn;
+  }
   GDR_TRACE_MARK(2, 8);
   if (ok && lo) {
     {  // dv = diag(beta) dB_v, columns [64 hf, +64)
@@ -568,18 +620,23 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   __syncthreads();
   GDR_TRACE_MARK(2, 9);
   // R3: X T^T (64-127)
+  if (ok && tid == kCopyTid && len == 64) {
+    tc::tma_store_3d(&tm_dv, sm + S::DVS, 0, j, t0);
+    tc::tma_store_3d(&tm_dv, sm + S::DVS + kSlab, 64, j, t0);
+    tc::bulk_commit();
+  }
   if (ok && tid == 0) {
-    if (len == 64) {
-      tc::tma_store_3d(&tm_dv, sm + S::DVS, 0, j, t0);
-      tc::tma_store_3d(&tm_dv, sm + S::DVS + kSlab, 64, j, t0);
-      tc::bulk_commit();
-    }
     tc::tc_fence_after();
     tc::gemm(tb + 64, kmaj(sm + S::XT, kSlab), kmaj(sm + S::T, kSlab), 64, 4, false);
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
+  if (ok && tid == kCopyTid && pending >= 0) {  // dv has left its staging tile (W)
+    tc::bulk_wait_read<0>();
+    issue_loads(wnext, kLdW);
+    pending |= kLdW;
+  }
   GDR_TRACE_MARK(2, 10);
   if (ok && lo) {  // columns [32 hf, +32)
     const float br = s_beta[r];
@@ -624,6 +681,10 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
+  if (ok && tid == kCopyTid && pending >= 0) {  // every operand tile but dO (dk staging) is free
+    issue_loads(wnext, kLdRest);
+    pending |= kLdRest;
+  }
   GDR_TRACE_MARK(2, 12);
   if (ok && lo) {
     float x[64];
@@ -654,7 +715,7 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   }
   tc::fence_proxy_async_smem();
   __syncthreads();
-  if (ok && tid == 0 && !kGroup && len == 64) {
+  if (ok && tid == kCopyTid && !kGroup && len == 64) {
     tc::tma_store_3d(&tm_dk, sm + S::DKS, 0, i, t0);
     tc::tma_store_3d(&tm_dk, sm + S::DKS + kSlab, 64, i, t0);
     tc::bulk_commit();
@@ -674,13 +735,22 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
     const float v = s_colaa[tid] + (tid >= 32 ? s_colaa[31] : 0.f);
     if (rr < len) dg[(size_t)(t0 + rr) * Hv + j] = v;
   }
-  if (tid == 0) tc::bulk_wait_read<0>();  // staging tiles read before the next item's loads
+  if (tid == kCopyTid) {
+    tc::bulk_wait_read<0>();  // staging tiles read before the next item's loads
+    if (ok && pending >= 0) {
+      issue_loads(wnext, kLdDo);
+      pending |= kLdDo;
+    }
+  }
   GDR_TRACE_MARK(2, 13);
   item_par ^= 1;
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   }  // items
+  // A failed wait ends the walk early: let the next item's loads that are already in
+  // flight land (bounded) before the CTA gives up its shared memory.
+  if (tid == kCopyTid && !ok && pending > 0) (void)tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutBwd);
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, 512);
@@ -711,13 +781,14 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
         !map_2d_box(&tdhs, ws.dhp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, 128, rows * 2, 64, 128) ||
         !map_2d(&tu, ws.U, 128, rows) || !map_3d(&tdq, a.dq, 128, d.Hk, Tt) || !map_3d(&tdk, a.dk, 128, d.Hk, Tt) ||
         !map_3d(&tdv, a.dv, 128, d.Hv, Tt) ||
-        !map_2d_box(&thf, a.h_saved, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, rows * 2, 32, 128))
+        !(d.h_bf16 ? map_2d(&thf, a.h_saved, 128, rows * 2)
+                   : map_2d_box(&thf, a.h_saved, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, rows * 2, 32, 128)))
       return cudaErrorInvalidValue;
   }
   if (d.num_seqs > 0) {
     const size_t sm = WalkSmem::BYTES + 1024;
     cudaFuncSetAttribute(tc_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    tc_bwd_walk_kernel<<<dim3(d.num_seqs, d.Hv, 2), kTcThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, d, a.dS_T,
+    tc_bwd_walk_kernel<<<dim3(d.num_seqs, d.Hv, 2), kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, d, a.dS_T,
                                                                         a.dS0, ws);
     stage_mark(s, "bwd_walk");
   }

@@ -30,11 +30,12 @@
  *      beta, dbeta        [B, T, Hv]         dtype
  *      S0, S_T, dS_T, dS0 [num_seqs, Hv, DK, DV] float32 for GDR_STATE_KV (stores S^T),
  *                         [num_seqs, Hv, DV, DK] float32 for GDR_STATE_VK (stores S)
- *      h_saved            [max_chunks, Hv, DK, DV] float32: S^T at the START of every
- *                         64-token chunk, whatever the state layout; chunk c of sequence
- *                         n sits at index chunk_offset[n] + c with
- *                         chunk_offset[n] = sum_{n' < n} ceil(L_n' / 64).  Slots past
- *                         the last real chunk (varlen upper bound) are left untouched.
+ *      h_saved            [max_chunks, Hv, DK, DV] of h_dtype (float32 by default, or
+ *                         bf16): S^T at the START of every 64-token chunk, whatever the
+ *                         state layout; chunk c of sequence n sits at index
+ *                         chunk_offset[n] + c with chunk_offset[n] = sum_{n' < n}
+ *                         ceil(L_n' / 64).  Slots past the last real chunk (varlen upper
+ *                         bound) are left untouched.
  *    Variable length: B = 1, T = total tokens, cu_seqlens (device, int32,
  *    num_seqs + 1 entries, cu_seqlens[0] = 0, non-decreasing, last = T) delimits the
  *    sequences; empty sequences are allowed (S_T = S0, dS0 = dS_T).
@@ -80,13 +81,17 @@ typedef struct {
   gdr_dtype dtype;           /* dtype of q, k, v, beta, o, dO, dq, dk, dv, dbeta */
   gdr_state_layout layout;   /* orientation of S0, S_T, dS_T, dS0 */
   float scale;               /* output scale; <= 0 selects 1/sqrt(DK) */
+  gdr_dtype h_dtype;         /* dtype of h_saved: GDR_DTYPE_F32 (default: the states as the
+                                forward carries them) or GDR_DTYPE_BF16 (half the bytes of the
+                                largest tensor, rounded to bf16; the backward then reads the
+                                rounded states, so its gradients carry that rounding) */
 } gdr_problem;
 
 /* Upper bound on the number of 64-token chunks: B * ceil(T/64) for fixed length,
  * floor(T/64) + num_seqs for varlen.  Returns 0 for an invalid problem. */
 size_t gdr_max_chunks(const gdr_problem* p);
 
-/* Bytes of h_saved: gdr_max_chunks(p) * Hv * DK * DV * 4. */
+/* Bytes of h_saved: gdr_max_chunks(p) * Hv * DK * DV * (4 for F32, 2 for BF16 h_dtype). */
 size_t gdr_saved_states_bytes(const gdr_problem* p);
 
 /* Bytes of the scratch workspace that gdr_fwd / gdr_bwd need (device memory,
@@ -102,7 +107,7 @@ size_t gdr_bwd_workspace_bytes(const gdr_problem* p);
  * workspace/workspace_bytes: see gdr_fwd_workspace_bytes. */
 gdr_status gdr_fwd(const gdr_problem* p, const void* q, const void* k, const void* v,
                    const float* g, const void* beta, const float* S0, void* o, float* S_T,
-                   float* h_saved, void* workspace, size_t workspace_bytes, gdr_stream_t stream);
+                   void* h_saved, void* workspace, size_t workspace_bytes, gdr_stream_t stream);
 
 /* Backward (the fused backward "fused_gdr_bwd" of FlashQLA PR #34: walks the chunks
  * in reverse carrying the state gradient dh).
@@ -112,7 +117,7 @@ gdr_status gdr_fwd(const gdr_problem* p, const void* q, const void* k, const voi
  *        dS0 (nullable: not written).  All outputs are overwritten.
  * The result is bitwise deterministic: no floating-point atomics. */
 gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const void* v,
-                   const float* g, const void* beta, const float* h_saved, const void* dO,
+                   const float* g, const void* beta, const void* h_saved, const void* dO,
                    const float* dS_T, void* dq, void* dk, void* dv, float* dg, void* dbeta,
                    float* dS0, void* workspace, size_t workspace_bytes, gdr_stream_t stream);
 
@@ -139,7 +144,7 @@ gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const voi
 #define GDR_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)64 << 20)
 gdr_status gdr_fwd_noalloc(const gdr_problem* p, const void* q, const void* k, const void* v,
                            const float* g, const void* beta, const float* S0, void* o, float* S_T,
-                           float* h_saved, gdr_stream_t stream);
+                           void* h_saved, gdr_stream_t stream);
 
 /* Synchronises `stream`, then reads the status word that the kernels of the last
  * gdr_fwd / gdr_bwd using `workspace` left there: GDR_OK, or GDR_ERR_TIMEOUT if a

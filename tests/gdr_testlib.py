@@ -23,12 +23,12 @@ def to_device(inp: dict, dev="cuda") -> dict:
     return out
 
 
-def run_gpu(inp: dict, backward: bool = True, stream=None) -> dict:
+def run_gpu(inp: dict, backward: bool = True, stream=None, h_dtype=torch.float32) -> dict:
     """Run gdr_fwd (+ gdr_bwd) on device copies of ``inp``; returns device tensors."""
     d = to_device(inp)
     layout = inp["layout"]
     o, S_T, h_saved = gdr.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["cu_seqlens"], layout,
-                                  stream=stream)
+                                  stream=stream, h_dtype=h_dtype)
     res = {"o": o, "S_T": S_T, "h_saved": h_saved}
     if backward:
         dq, dk, dv, dg, dbeta, dS0 = gdr.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], h_saved, d["dO"],

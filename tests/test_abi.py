@@ -52,6 +52,9 @@ def test_size_queries(lib):
     assert gdr.gdr_max_chunks(pv) == 300 // 64 + 3
     assert gdr.gdr_path(prob(DK=128, DV=128)) in (0, 1)
     assert gdr.gdr_path(prob(dtype=torch.float32)) == 0
+    # bf16 saved states: half the bytes, same workspaces
+    assert gdr.gdr_saved_states_bytes(prob(h_dtype=torch.bfloat16)) == 6 * 4 * 64 * 32 * 2
+    assert gdr.gdr_fwd_workspace_bytes(prob(h_dtype=torch.bfloat16)) == gdr.gdr_fwd_workspace_bytes(p)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -61,6 +64,7 @@ def test_size_queries(lib):
     (dict(layout=7), gdr.GDR_ERR_INVALID_ARG),
     (dict(dtype=torch.float16), gdr.GDR_ERR_INVALID_ARG),
     (dict(T=-1), gdr.GDR_ERR_INVALID_ARG),
+    (dict(h_dtype=torch.float16), gdr.GDR_ERR_INVALID_ARG),  # h_saved is fp32 or bf16
 ])
 def test_bad_problems_are_rejected(lib, kw, code):
     p = prob(**kw)

@@ -159,3 +159,42 @@ def test_tensor_core_path_is_selected_for_bf16_d128():
     assert gdr.gdr_path(p) == 1
     p32 = gdr.make_problem(1, 128, 1, 1, 64, 64, torch.float32, "KV")
     assert gdr.gdr_path(p32) == 0
+
+
+# ---------------------------------------------------------------- bf16 saved chunk states
+# h_saved rounded to bf16 (half the bytes of the largest tensor).  The backward reads
+# the rounded states, and the SIMT forward computes o from them, so every output is
+# held to the bf16 bar (2e-2) whatever the input dtype.
+H_BF16_CASES = [
+    # name, dtype, B, T, Hk, Hv, D, layout, seqlens
+    ("tc_b2_t300", torch.bfloat16, 2, 300, 2, 2, 128, "VK", None),
+    ("tc_gva_varlen", torch.bfloat16, 1, None, 1, 2, 128, "KV", [0, 1, 64, 77, 200]),
+    ("simt_bf16_d64", torch.bfloat16, 1, 150, 1, 1, 64, "KV", None),
+    ("simt_f32_d32", torch.float32, 2, 130, 2, 4, 32, "VK", None),
+]
+
+
+@pytest.mark.parametrize("case", H_BF16_CASES, ids=[c[0] for c in H_BF16_CASES])
+def test_bf16_saved_states_match_oracle(case):
+    name, dt, B, T, Hk, Hv, D, layout, lens = case
+    if lens is None:
+        w = small_workload(name, dt, B, T, Hk, Hv, D, D, layout)
+    else:
+        w = small_workload(name, dt, Hk=Hk, Hv=Hv, DK=D, DV=D, seqlens=lens, layout=layout)
+    inp = make_inputs(w)
+    res = run_gpu(inp, h_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert res["h_saved"].dtype == torch.bfloat16
+    compare(res, reference(inp), 2e-2)
+
+
+def test_bf16_saved_states_leave_tensor_core_forward_unchanged():
+    """On the tensor-core path h_dtype only changes what is stored: o and S_T are bitwise
+    the same, and the bf16 states are the fp32 states rounded to nearest even."""
+    w = small_workload("hcmp", torch.bfloat16, B=2, T=257, Hk=1, Hv=2, DK=128, DV=128)
+    inp = make_inputs(w)
+    r32 = run_gpu(inp, backward=False)
+    r16 = run_gpu(inp, backward=False, h_dtype=torch.bfloat16)
+    assert torch.equal(r32["o"], r16["o"])
+    assert torch.equal(r32["S_T"], r16["S_T"])
+    assert torch.equal(r32["h_saved"].to(torch.bfloat16), r16["h_saved"])
