@@ -298,3 +298,88 @@ def test_reference_layouts_are_transposes():
     assert np.array_equal(ref_kv["S_T"], np.swapaxes(ref_vk["S_T"], -1, -2))
     assert np.array_equal(ref_kv["dS0"], np.swapaxes(ref_vk["dS0"], -1, -2))
     assert ref_kv["h_saved"].shape == (2, 2, 8, 4)
+
+
+# ---------------------------------------------------------------- fused input prologue
+def _raw_inputs(rng, T=70, Hk=1, Hv=2, D=8):
+    return {
+        "q": 2.0 * rng.standard_normal((1, T, Hk, D)), "k": 0.5 * rng.standard_normal((1, T, Hk, D)),
+        "v": rng.standard_normal((1, T, Hv, D)), "dO": rng.standard_normal((1, T, Hv, D)),
+        "g": rng.standard_normal((1, T, Hv)), "beta": rng.standard_normal((1, T, Hv)),
+        "S0": 0.1 * rng.standard_normal((1, Hv, D, D)), "dS_T": 0.1 * rng.standard_normal((1, Hv, D, D)),
+        "cu_seqlens": None,
+    }
+
+
+def test_prologue_maps_closed_values():
+    from oracle import prologue as pl
+
+    np.testing.assert_allclose(pl.logsigmoid(np.array([0.0])), [-np.log(2.0)], rtol=1e-15)
+    np.testing.assert_allclose(pl.sigmoid(np.array([0.0, np.log(3.0)])), [0.5, 0.75], rtol=1e-15)
+    # extreme logits stay finite and take their limits
+    big = np.array([-1000.0, 1000.0])
+    np.testing.assert_allclose(pl.logsigmoid(big), [-1000.0, 0.0], atol=1e-300)
+    np.testing.assert_allclose(pl.sigmoid(big), [0.0, 1.0], atol=1e-300)
+    x_hat, s = pl.l2norm(np.array([[3.0, 4.0]]))
+    np.testing.assert_allclose(x_hat, [[3.0 / np.sqrt(25 + 1e-6), 4.0 / np.sqrt(25 + 1e-6)]], rtol=1e-15)
+    np.testing.assert_allclose(s, [[1.0 / np.sqrt(25 + 1e-6)]], rtol=1e-15)
+
+
+def test_prologue_without_flags_is_the_operator(rng):
+    from oracle import prologue as pl
+
+    inp = _raw_inputs(rng)
+    inp["g"] = pl.logsigmoid(inp["g"])
+    inp["beta"] = pl.sigmoid(inp["beta"])
+    a = pl.reference_with_prologue(inp, "KV", 0)
+    b = oracle.reference(inp, "KV")
+    for key in b:
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_prologue_forward_is_the_operator_on_mapped_inputs(rng):
+    from oracle import prologue as pl
+
+    raw = _raw_inputs(rng)
+    mapped = dict(raw)
+    mapped["q"] = raw["q"] / np.linalg.norm(raw["q"], axis=-1, keepdims=True)
+    mapped["k"] = raw["k"] / np.linalg.norm(raw["k"], axis=-1, keepdims=True)
+    mapped["g"] = np.log(1.0 / (1.0 + np.exp(-raw["g"])))
+    mapped["beta"] = 1.0 / (1.0 + np.exp(-raw["beta"]))
+    a = pl.reference_with_prologue(raw, "KV", 7, backward=False)
+    b = oracle.reference(mapped, "KV", backward=False)
+    for key in ["o", "S_T", "h_saved"]:
+        assert relmax(a[key], b[key]) < 1e-6, key  # eps = 1e-6 in the norm only
+
+
+@pytest.mark.parametrize("flags", [7, 1, 2, 4])
+def test_prologue_gradients_match_central_differences(rng, flags):
+    from oracle import prologue as pl
+
+    inp = _raw_inputs(rng)
+    if not flags & 2:
+        inp["g"] = pl.logsigmoid(inp["g"])
+    if not flags & 4:
+        inp["beta"] = pl.sigmoid(inp["beta"])
+    ref = pl.reference_with_prologue(inp, "KV", flags)
+    grads = {"q": ref["dq"], "k": ref["dk"], "g": ref["dg"], "beta": ref["dbeta"]}
+
+    def loss():
+        r = pl.reference_with_prologue(inp, "KV", flags, backward=False, nthreads=1)
+        return float((r["o"] * inp["dO"]).sum() + (r["S_T"] * inp["dS_T"]).sum())
+
+    for name in ["q", "k", "g", "beta"]:
+        x = inp[name]
+        grad = grads[name]
+        gmax = max(np.abs(grad).max(), 1e-12)
+        for f in rng.choice(np.arange(x.size), size=10, replace=False):
+            idx = np.unravel_index(f, x.shape)
+            x0 = x[idx]
+            h = 1e-6 * max(1.0, abs(x0))
+            x[idx] = x0 + h
+            lp = loss()
+            x[idx] = x0 - h
+            lm = loss()
+            x[idx] = x0
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - grad[idx]) / gmax < 1e-6, (flags, name, idx, fd, grad[idx])
