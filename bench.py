@@ -47,6 +47,8 @@ STAGE_IO = {
     "bwd_grad": ("q k v dO beta h_saved", "dq dk dv dg dbeta"),
 
     "bwd_group_reduce": ("", "dq dk"),
+    "prologue": ("q k g beta", ""),
+    "prologue_bwd": ("", "dq dk dg dbeta"),
 }
 
 
@@ -205,14 +207,19 @@ def _head_slice(inp, qk_heads):
     return out
 
 
-def time_oracle(inp, w, n_qk_heads, nthreads):
-    """Times the fp64 oracle (fwd + bwd) on the first n_qk_heads q/k heads of every
-    sequence; returns (seconds, tokens-equivalent of the full workload processed)."""
+def time_oracle(inp, w, n_qk_heads, nthreads, prologue=0):
+    """Times the fp64 oracle (fwd + bwd, with the fused input prologue when asked) on the
+    first n_qk_heads q/k heads of every sequence; returns (seconds, tokens-equivalent of the
+    full workload processed)."""
     import oracle
+    from oracle import prologue as oracle_prologue
 
     sub = _head_slice(inp, list(range(n_qk_heads)))
     t0 = time.perf_counter()
-    oracle.reference(sub, inp["layout"], backward=True, nthreads=nthreads)
+    if prologue:
+        oracle_prologue.reference_with_prologue(sub, inp["layout"], prologue, backward=True, nthreads=nthreads)
+    else:
+        oracle.reference(sub, inp["layout"], backward=True, nthreads=nthreads)
     dt = time.perf_counter() - t0
     tokens = sum(inp["seqlens"]) * n_qk_heads / w.Hk
     return dt, tokens
@@ -226,10 +233,10 @@ def reference_arm(args, w, inp):
     # per step: as many q/k heads (with their v-heads) of every sequence as there are host cores
     n_heads = max(1, min(w.Hk, nthreads // max(1, inp["num_seqs"])))
     for _ in range(args.warmup):
-        time_oracle(inp, w, n_heads, nthreads)
+        time_oracle(inp, w, n_heads, nthreads, 7 if args.prologue else 0)
     total_t, total_tok = 0.0, 0.0
     for _ in range(args.steps):
-        dt, tok = time_oracle(inp, w, n_heads, nthreads)
+        dt, tok = time_oracle(inp, w, n_heads, nthreads, 7 if args.prologue else 0)
         total_t += dt
         total_tok += tok
     value = total_tok / total_t
@@ -240,7 +247,7 @@ def reference_arm(args, w, inp):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w, inp, args.h_dtype),
+        "config": config_dict(w, inp, args.h_dtype, args.prologue),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(nthreads, units), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -249,12 +256,13 @@ def reference_arm(args, w, inp):
     return 0
 
 
-def config_dict(w, inp, h_dtype="f32"):
+def config_dict(w, inp, h_dtype="f32", prologue=False):
     return {"workload": w.name, "B": w.B if inp["cu_seqlens"] is None else 1, "T": int(sum(inp["seqlens"])) if
             inp["cu_seqlens"] is not None else w.T, "Hk": w.Hk, "Hv": w.Hv, "DK": w.DK, "DV": w.DV,
             "layout": w.layout, "num_seqs": inp["num_seqs"], "chunk": CHUNK,
             "varlen": inp["cu_seqlens"] is not None, "S0": inp["S0"] is not None,
             "dS_T": inp["dS_T"] is not None, "h_saved": h_dtype,
+            "prologue": "qk_l2norm+g_logsigmoid+beta_sigmoid (raw inputs)" if prologue else "none",
             "l2": "flushed (512 MB write) between timed steps", "parallelism": "replicas"}
 
 
@@ -284,6 +292,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--h-dtype", default="f32", choices=["f32", "bf16"],
                     help="dtype of the saved chunk-start states (bf16 halves the largest tensor)")
+    ap.add_argument("--prologue", action="store_true",
+                    help="raw q, k, gate and beta logits; the operator applies the L2 norm, logsigmoid, sigmoid")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -292,7 +302,8 @@ def main():
     from chunked_gated_delta_04_gb300.inputs import WORKLOADS, make_inputs
 
     w = WORKLOADS[args.workload]
-    inp = make_inputs(w)
+    inp = make_inputs(w, raw=args.prologue)
+    prologue_bits = 7 if args.prologue else 0
     if args.impl == "reference":
         return reference_arm(args, w, inp)
 
@@ -315,7 +326,8 @@ def main():
     B, T, Hk, DK = d["q"].shape
     Hv, DV = d["v"].shape[2], d["v"].shape[3]
     h_dtype = torch.bfloat16 if args.h_dtype == "bf16" else torch.float32
-    p = gdr.make_problem(B, T, Hk, Hv, DK, DV, d["q"].dtype, w.layout, d["cu_seqlens"], h_dtype=h_dtype)
+    p = gdr.make_problem(B, T, Hk, Hv, DK, DV, d["q"].dtype, w.layout, d["cu_seqlens"], h_dtype=h_dtype,
+                         prologue=prologue_bits)
     stream = torch.cuda.current_stream()
     N = p.num_seqs
     sshape = (N, Hv, DK, DV) if w.layout == "KV" else (N, Hv, DV, DK)
@@ -396,8 +408,11 @@ def main():
             fn()
             torch.cuda.synchronize()
             names = gdr.gdr_debug_stage_names()
-            for i, nm in enumerate(names):
-                stage_tot.setdefault(nm, []).append(events[i].elapsed_time(events[i + 1]))
+            per_call = {}
+            for i, nm in enumerate(names):  # a stage may launch several kernels: sum them per call
+                per_call[nm] = per_call.get(nm, 0.0) + events[i].elapsed_time(events[i + 1])
+            for nm, t in per_call.items():
+                stage_tot.setdefault(nm, []).append(t)
     gdr.gdr_debug_set_stage_events(None)
     stage_ms = {k: statistics.mean(v) for k, v in stage_tot.items()}
 
@@ -454,7 +469,7 @@ def main():
         tot_t = tot_tok = 0.0
         reps = 0
         while tot_t < 10.0 and reps < 50:
-            dt, tok = time_oracle(inp, w, n_heads, nthreads)
+            dt, tok = time_oracle(inp, w, n_heads, nthreads, 7 if args.prologue else 0)
             tot_t += dt
             tot_tok += tok
             reps += 1
@@ -470,7 +485,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
             "data": "synthetic (seeded; see chunked_gated_delta_04_gb300/inputs.py)",
-            "config": config_dict(w, inp, args.h_dtype),
+            "config": config_dict(w, inp, args.h_dtype, args.prologue),
             "roofline": roofline,
             "step_roofline": {"ms": step_roof, "frac": step_roof / ms_per_step, "bound": "hbm" if
                               t_hbm_step >= t_flop_step else "tensor", "bytes": wm["bytes_fwd"] + wm["bytes_bwd"],

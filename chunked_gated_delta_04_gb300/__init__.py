@@ -29,6 +29,8 @@ GDR_OK, GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED, GDR_ERR_ALIGNMENT, GDR_ERR_CUD
     GDR_ERR_WORKSPACE = range(7)
 GDR_DTYPE_F32, GDR_DTYPE_BF16 = 0, 1
 GDR_STATE_KV, GDR_STATE_VK = 0, 1
+GDR_PROLOGUE_QK_L2NORM, GDR_PROLOGUE_G_LOGSIGMOID, GDR_PROLOGUE_BETA_SIGMOID = 1, 2, 4
+GDR_PROLOGUE_ALL = 7
 CHUNK = 64
 
 
@@ -36,7 +38,7 @@ class gdr_problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("Hk", ctypes.c_int), ("Hv", ctypes.c_int),
                 ("DK", ctypes.c_int), ("DV", ctypes.c_int), ("num_seqs", ctypes.c_int),
                 ("cu_seqlens", ctypes.c_void_p), ("dtype", ctypes.c_int), ("layout", ctypes.c_int),
-                ("scale", ctypes.c_float), ("h_dtype", ctypes.c_int)]
+                ("scale", ctypes.c_float), ("h_dtype", ctypes.c_int), ("prologue", ctypes.c_uint)]
 
 
 class GDRError(RuntimeError):
@@ -122,8 +124,9 @@ def _dtype_code(dtype):
 
 
 def make_problem(B, T, Hk, Hv, DK, DV, dtype, layout="KV", cu_seqlens=None, num_seqs=None, scale=None,
-                 h_dtype=torch.float32):
-    """Build a gdr_problem.  dtype, h_dtype (of h_saved): torch.float32/bfloat16; layout "KV"/"VK"."""
+                 h_dtype=torch.float32, prologue=0):
+    """Build a gdr_problem.  dtype, h_dtype (of h_saved): torch.float32/bfloat16; layout "KV"/"VK";
+    prologue: bit set of GDR_PROLOGUE_* (the matching inputs are raw)."""
     p = gdr_problem()
     p.B, p.T, p.Hk, p.Hv, p.DK, p.DV = B, T, Hk, Hv, DK, DV
     if cu_seqlens is not None:
@@ -134,6 +137,7 @@ def make_problem(B, T, Hk, Hv, DK, DV, dtype, layout="KV", cu_seqlens=None, num_
         p.num_seqs = B if num_seqs is None else num_seqs
     p.dtype = _dtype_code(dtype)
     p.h_dtype = _dtype_code(h_dtype)
+    p.prologue = int(prologue)
     p.layout = {"KV": GDR_STATE_KV, "VK": GDR_STATE_VK}.get(layout, 99) if isinstance(layout, str) else layout
     p.scale = 0.0 if scale is None else float(scale)
     return p
@@ -235,10 +239,11 @@ def _check(st, where):
         raise GDRError(st, where)
 
 
-def _problem_for(q, v, cu_seqlens, layout, scale, h_dtype=torch.float32):
+def _problem_for(q, v, cu_seqlens, layout, scale, h_dtype=torch.float32, prologue=0):
     B, T, Hk, DK = q.shape
     Hv, DV = v.shape[2], v.shape[3]
-    return make_problem(B, T, Hk, Hv, DK, DV, q.dtype, layout, cu_seqlens, scale=scale, h_dtype=h_dtype)
+    return make_problem(B, T, Hk, Hv, DK, DV, q.dtype, layout, cu_seqlens, scale=scale, h_dtype=h_dtype,
+                        prologue=prologue)
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:
@@ -248,9 +253,10 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 # ------------------------------------------------------------------ allocating helpers
 def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, layout="KV", scale=None, output_final_state=True,
-            workspace=None, stream=None, h_dtype=torch.float32):
-    """Run gdr_fwd; returns (o, S_T or None, h_saved).  h_dtype: dtype of h_saved."""
-    p = _problem_for(q, v, cu_seqlens, layout, scale, h_dtype)
+            workspace=None, stream=None, h_dtype=torch.float32, prologue=0):
+    """Run gdr_fwd; returns (o, S_T or None, h_saved).  h_dtype: dtype of h_saved; prologue:
+    GDR_PROLOGUE_* bits (q, k, g, beta raw where set)."""
+    p = _problem_for(q, v, cu_seqlens, layout, scale, h_dtype, prologue)
     dev = q.device
     N = p.num_seqs
     o = torch.empty_like(v)
@@ -264,9 +270,10 @@ def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, layout="KV", scale=None,
 
 
 def backward(q, k, v, g, beta, h_saved, dO, dS_T=None, cu_seqlens=None, layout="KV", scale=None,
-             want_dS0=True, workspace=None, stream=None):
-    """Run gdr_bwd; returns (dq, dk, dv, dg, dbeta, dS0 or None).  h_saved's dtype selects h_dtype."""
-    p = _problem_for(q, v, cu_seqlens, layout, scale, h_saved.dtype)
+             want_dS0=True, workspace=None, stream=None, prologue=0):
+    """Run gdr_bwd; returns (dq, dk, dv, dg, dbeta, dS0 or None).  h_saved's dtype selects h_dtype;
+    with prologue bits the gradients are w.r.t. the raw inputs."""
+    p = _problem_for(q, v, cu_seqlens, layout, scale, h_saved.dtype, prologue)
     dev = q.device
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dg = torch.empty_like(g)
@@ -283,10 +290,11 @@ def backward(q, k, v, g, beta, h_saved, dO, dS_T=None, cu_seqlens=None, layout="
 
 class _GDRFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype):
-        o, S_T, h_saved = forward(q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype=h_dtype)
+    def forward(ctx, q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype, prologue):
+        o, S_T, h_saved = forward(q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype=h_dtype,
+                                  prologue=prologue)
         ctx.save_for_backward(q, k, v, g, beta, h_saved, cu_seqlens)
-        ctx.layout, ctx.scale, ctx.has_S0 = layout, scale, S0 is not None
+        ctx.layout, ctx.scale, ctx.has_S0, ctx.prologue = layout, scale, S0 is not None, prologue
         return o, S_T
 
     @staticmethod
@@ -294,12 +302,13 @@ class _GDRFunction(torch.autograd.Function):
         q, k, v, g, beta, h_saved, cu_seqlens = ctx.saved_tensors
         dq, dk, dv, dg, dbeta, dS0 = backward(q, k, v, g, beta, h_saved, do.contiguous(),
                                               None if dS_T is None else dS_T.contiguous(), cu_seqlens,
-                                              ctx.layout, ctx.scale, want_dS0=ctx.has_S0)
-        return dq, dk, dv, dg, dbeta, dS0, None, None, None, None
+                                              ctx.layout, ctx.scale, want_dS0=ctx.has_S0, prologue=ctx.prologue)
+        return dq, dk, dv, dg, dbeta, dS0, None, None, None, None, None
 
 
 def chunk_gated_delta_rule(q, k, v, g, beta, initial_state=None, cu_seqlens=None, layout="KV", scale=None,
-                           h_dtype=torch.float32):
+                           h_dtype=torch.float32, prologue=0):
     """Autograd entry point: returns (o, final_state).  Tensors as in include/gdr.h; h_dtype is the
-    dtype of the chunk-start states kept for the backward (bfloat16 halves their memory)."""
-    return _GDRFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, layout, scale, h_dtype)
+    dtype of the chunk-start states kept for the backward (bfloat16 halves their memory); prologue
+    (GDR_PROLOGUE_* bits) makes the operator normalise q, k and map raw gate / beta logits itself."""
+    return _GDRFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, layout, scale, h_dtype, prologue)

@@ -50,6 +50,7 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
   if (p->dtype != GDR_DTYPE_F32 && p->dtype != GDR_DTYPE_BF16) return GDR_ERR_INVALID_ARG;
   if (p->layout != GDR_STATE_KV && p->layout != GDR_STATE_VK) return GDR_ERR_INVALID_ARG;
   if (p->h_dtype != GDR_DTYPE_F32 && p->h_dtype != GDR_DTYPE_BF16) return GDR_ERR_INVALID_ARG;
+  if (p->prologue & ~7u) return GDR_ERR_INVALID_ARG;
   if (p->cu_seqlens != nullptr) {
     if (p->B != 1) return GDR_ERR_INVALID_ARG;
   } else if (p->num_seqs != p->B) {
@@ -76,6 +77,7 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
   d->layout = p->layout;
   d->cu = p->cu_seqlens;
   d->h_bf16 = p->h_dtype == GDR_DTYPE_BF16 ? 1 : 0;
+  d->prologue = (int)p->prologue;
   d->path = (p->dtype == GDR_DTYPE_BF16 && p->DK == 128 && p->DV == 128 && maxc * p->Hv * kChunk < (1ll << 31) &&
              tc_available())
                 ? 1
@@ -119,9 +121,34 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
       w.dk_part = (float*)take(sizeof(float) * (size_t)d.T_total * d.Hv * d.DK);
     }
   }
+  if (d.prologue) {
+    const size_t in_el = d.dtype == GDR_DTYPE_BF16 ? 2 : 4;
+    if (d.prologue & GDR_PROLOGUE_QK_L2NORM) {
+      w.qn = take(in_el * (size_t)d.T_total * d.Hk * d.DK);
+      w.kn = take(in_el * (size_t)d.T_total * d.Hk * d.DK);
+    }
+    if (d.prologue & GDR_PROLOGUE_G_LOGSIGMOID) w.gn = (float*)take(sizeof(float) * (size_t)d.T_total * d.Hv);
+    if (d.prologue & GDR_PROLOGUE_BETA_SIGMOID) w.bn = take(in_el * (size_t)d.T_total * d.Hv);
+  }
   if (ws) *ws = w;
   return off;
 }
+
+// With prologue bits set: runs the forward prologue and points the operator's q, k, g,
+// beta at its outputs (the raw pointers stay with the caller for the backward map).
+template <typename Args>
+cudaError_t apply_prologue(const Dims& d, Args& a, const Workspace& ws, cudaStream_t s) {
+  if (!d.prologue) return cudaSuccess;
+  const cudaError_t e = launch_prologue_fwd(d, a.q, a.k, a.g, a.beta, ws, s);
+  if (d.prologue & GDR_PROLOGUE_QK_L2NORM) {
+    a.q = ws.qn;
+    a.k = ws.kn;
+  }
+  if (d.prologue & GDR_PROLOGUE_G_LOGSIGMOID) a.g = ws.gn;
+  if (d.prologue & GDR_PROLOGUE_BETA_SIGMOID) a.beta = ws.bn;
+  return e;
+}
+template cudaError_t apply_prologue<FwdArgs>(const Dims&, FwdArgs&, const Workspace&, cudaStream_t);
 
 }  // namespace gdr
 
@@ -178,6 +205,7 @@ gdr_status gdr_fwd(const gdr_problem* p, const void* q, const void* k, const voi
   FwdArgs a{q, k, v, g, beta, S0, o, S_T, h_saved};
   stage_begin(s);
   cudaError_t e = launch_index(d, ws, s);
+  if (e == cudaSuccess) e = apply_prologue(d, a, ws, s);
   if (e == cudaSuccess) e = d.path == 1 ? tc_forward(d, a, ws, s) : simt_forward(d, a, ws, s);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
@@ -205,7 +233,10 @@ gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const voi
   BwdArgs a{q, k, v, g, beta, h_saved, dO, dS_T, dq, dk, dv, dg, dbeta, dS0};
   stage_begin(s);
   cudaError_t e = launch_index(d, ws, s);
+  if (e == cudaSuccess) e = apply_prologue(d, a, ws, s);
   if (e == cudaSuccess) e = d.path == 1 ? tc_backward(d, a, ws, s) : simt_backward(d, a, ws, s);
+  // gradients w.r.t. the raw inputs (in place; after the v-head group sum when Hv > Hk)
+  if (e == cudaSuccess) e = launch_prologue_bwd(d, q, k, g, beta, dq, dk, dg, dbeta, s);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 

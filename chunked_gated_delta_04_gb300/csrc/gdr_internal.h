@@ -32,6 +32,7 @@ struct Dims {
   const int32_t* cu;  // device cu_seqlens or nullptr
   int path;    // 1 = tcgen05, 0 = SIMT
   int h_bf16;  // h_saved holds bf16 (else fp32)
+  int prologue;  // gdr_prologue_flags bits
 };
 
 // Pointers into the caller's workspace.  Every region starts 256-byte aligned.
@@ -53,6 +54,12 @@ struct Workspace {
   void* dVn;     // tensor-core backward: dL/dVn, bf16 [max_chunks][Hv][64][DV]
   float* dq_part;  // backward, Hv > Hk: [T_total][Hv][DK]
   float* dk_part;  // backward, Hv > Hk: [T_total][Hv][DK]
+  // fused prologue outputs (input dtype unless noted): normalised q, k [T_total][Hk][DK],
+  // g = logsigmoid(a) fp32 [T_total][Hv], beta = sigmoid(b) [T_total][Hv]
+  void* qn;
+  void* kn;
+  float* gn;
+  void* bn;
 };
 
 // Validates *p and fills *d (the checks of gdr_fwd / gdr_bwd on the problem itself).
@@ -89,6 +96,17 @@ struct BwdArgs {
 void stage_mark(cudaStream_t s, const char* stage);
 // Called at the start of every gdr_fwd / gdr_bwd (records event 0 when enabled).
 void stage_begin(cudaStream_t s);
+
+// Fused input prologue (gdr_prologue.cu): the forward maps q, k, g, beta into ws.qn/kn/gn/bn
+// (only the parts whose bit is set); the backward maps dq, dk, dg, dbeta in place.
+cudaError_t launch_prologue_fwd(const Dims& d, const void* q, const void* k, const float* g, const void* beta,
+                                const Workspace& ws, cudaStream_t s);
+cudaError_t launch_prologue_bwd(const Dims& d, const void* q, const void* k, const float* g, const void* beta,
+                                void* dq, void* dk, float* dg, void* dbeta, cudaStream_t s);
+// Runs the forward prologue (if any bit is set) and points a.q, a.k, a.g, a.beta at its
+// outputs; Args is FwdArgs or BwdArgs.
+template <typename Args>
+cudaError_t apply_prologue(const Dims& d, Args& a, const Workspace& ws, cudaStream_t s);
 
 // K0: chunk index (chunks, seq offsets, longest-first order) and status reset.
 cudaError_t launch_index(const Dims& d, const Workspace& ws, cudaStream_t s);

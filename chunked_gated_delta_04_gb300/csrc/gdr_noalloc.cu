@@ -81,6 +81,7 @@ extern "C" gdr_status gdr_fwd_noalloc(const gdr_problem* p, const void* q, const
   FwdArgs a{q, k, v, g, beta, S0, o, S_T, h_saved};
   stage_begin(s);
   cudaError_t e = launch_index(d, ws, s);
+  if (e == cudaSuccess) e = apply_prologue(d, a, ws, s);
   if (e == cudaSuccess) e = d.path == 1 ? tc_forward(d, a, ws, s) : simt_forward(d, a, ws, s);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }

@@ -6,7 +6,9 @@ in this order): sequence lengths (varlen only), q, k, v, dO, g-logits, beta-logi
 S0, dS_T.  Then q and k are L2-normalised per token, g = logsigmoid(x + g_shift),
 beta = sigmoid(x), and q, k, v, dO, beta are cast to the compute dtype.  g, S0 and
 dS_T stay fp32; S0 and dS_T are 0.1 * N(0, 1) drawn directly in the storage layout
-([N, Hv, DK, DV] for "KV", [N, Hv, DV, DK] for "VK").
+([N, Hv, DK, DV] for "KV", [N, Hv, DV, DK] for "VK").  With ``raw=True`` (inputs of the
+operator's fused prologue) the same draws are returned without the maps: q and k not
+normalised, g = the gate logit x + g_shift, beta = the beta logit (cast to the dtype).
 
 The five named workloads are the chunked gated delta rule shapes of the benchmark
 (chunk 64):
@@ -55,8 +57,8 @@ WORKLOADS = {
 }
 
 
-def make_inputs(w: Workload) -> dict:
-    """Generate the C-ABI input tensors (CPU) for workload ``w``.
+def make_inputs(w: Workload, raw: bool = False) -> dict:
+    """Generate the C-ABI input tensors (CPU) for workload ``w`` (``raw``: see the module doc).
 
     Returns q, k [B,T,Hk,DK]; v, dO [B,T,Hv,DV] (compute dtype); g [B,T,Hv] fp32;
     beta [B,T,Hv] (compute dtype); S0, dS_T fp32 or None; cu_seqlens int32 [N+1] or None;
@@ -88,10 +90,13 @@ def make_inputs(w: Workload) -> dict:
     sshape = (N, w.Hv, w.DK, w.DV) if w.layout == "KV" else (N, w.Hv, w.DV, w.DK)
     S0 = 0.1 * torch.randn(*sshape, generator=gen, dtype=f32) if w.with_S0 else None
     dST = 0.1 * torch.randn(*sshape, generator=gen, dtype=f32) if w.with_dST else None
-    q = torch.nn.functional.normalize(q, dim=-1)
-    k = torch.nn.functional.normalize(k, dim=-1)
-    g = torch.nn.functional.logsigmoid(g_logit + w.g_shift)
-    beta = torch.sigmoid(b_logit)
+    if raw:
+        g, beta = g_logit + w.g_shift, b_logit
+    else:
+        q = torch.nn.functional.normalize(q, dim=-1)
+        k = torch.nn.functional.normalize(k, dim=-1)
+        g = torch.nn.functional.logsigmoid(g_logit + w.g_shift)
+        beta = torch.sigmoid(b_logit)
     dt = w.dtype
     return {
         "q": q.to(dt).contiguous(), "k": k.to(dt).contiguous(), "v": v.to(dt).contiguous(),

@@ -73,6 +73,20 @@ typedef enum { GDR_DTYPE_F32 = 0, GDR_DTYPE_BF16 = 1 } gdr_dtype;
 
 typedef enum { GDR_STATE_KV = 0, GDR_STATE_VK = 1 } gdr_state_layout;
 
+/* Input prologue applied inside the operator (bits of gdr_problem.prologue).  With a bit
+ * set the corresponding arguments are RAW and the matching gradients are with respect to
+ * them (eps = 1e-6; the maps are the usual preparation of the operator's inputs):
+ *   QK_L2NORM      q, k are raw; the operator uses q * (sum q^2 + eps)^(-1/2) per token
+ *                  and head (same for k); dq, dk are gradients w.r.t. the raw q, k.
+ *   G_LOGSIGMOID   g holds the raw gate logit a; the log decay is logsigmoid(a); dg = dL/da.
+ *   BETA_SIGMOID   beta holds the raw logit b; the operator uses sigmoid(b) (rounded to the
+ *                  input dtype); dbeta = dL/db. */
+typedef enum {
+  GDR_PROLOGUE_QK_L2NORM = 1,
+  GDR_PROLOGUE_G_LOGSIGMOID = 2,
+  GDR_PROLOGUE_BETA_SIGMOID = 4
+} gdr_prologue_flags;
+
 typedef struct {
   int B, T;                  /* fixed length: B sequences of T tokens; varlen: B = 1, T = total */
   int Hk, Hv, DK, DV;        /* q/k heads, v heads (Hv % Hk == 0), key and value widths */
@@ -85,6 +99,7 @@ typedef struct {
                                 forward carries them) or GDR_DTYPE_BF16 (half the bytes of the
                                 largest tensor, rounded to bf16; the backward then reads the
                                 rounded states, so its gradients carry that rounding) */
+  unsigned int prologue;     /* bit set of gdr_prologue_flags; 0 = inputs used as given */
 } gdr_problem;
 
 /* Upper bound on the number of 64-token chunks: B * ceil(T/64) for fixed length,

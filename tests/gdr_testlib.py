@@ -23,16 +23,17 @@ def to_device(inp: dict, dev="cuda") -> dict:
     return out
 
 
-def run_gpu(inp: dict, backward: bool = True, stream=None, h_dtype=torch.float32) -> dict:
+def run_gpu(inp: dict, backward: bool = True, stream=None, h_dtype=torch.float32, prologue=0) -> dict:
     """Run gdr_fwd (+ gdr_bwd) on device copies of ``inp``; returns device tensors."""
     d = to_device(inp)
     layout = inp["layout"]
     o, S_T, h_saved = gdr.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["cu_seqlens"], layout,
-                                  stream=stream, h_dtype=h_dtype)
+                                  stream=stream, h_dtype=h_dtype, prologue=prologue)
     res = {"o": o, "S_T": S_T, "h_saved": h_saved}
     if backward:
         dq, dk, dv, dg, dbeta, dS0 = gdr.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], h_saved, d["dO"],
-                                                  d["dS_T"], d["cu_seqlens"], layout, stream=stream)
+                                                  d["dS_T"], d["cu_seqlens"], layout, stream=stream,
+                                                  prologue=prologue)
         res.update(dq=dq, dk=dk, dv=dv, dg=dg, dbeta=dbeta, dS0=dS0)
     return res
 
@@ -100,5 +101,9 @@ def slice_result(res: dict, qk_heads, vh) -> dict:
     return out
 
 
-def reference(inp: dict, backward=True) -> dict:
+def reference(inp: dict, backward=True, prologue=0) -> dict:
+    if prologue:
+        from oracle import prologue as pl
+
+        return pl.reference_with_prologue(inp, inp["layout"], prologue, backward=backward)
     return oracle.reference(inp, inp["layout"], backward=backward)

@@ -55,6 +55,9 @@ def test_size_queries(lib):
     # bf16 saved states: half the bytes, same workspaces
     assert gdr.gdr_saved_states_bytes(prob(h_dtype=torch.bfloat16)) == 6 * 4 * 64 * 32 * 2
     assert gdr.gdr_fwd_workspace_bytes(prob(h_dtype=torch.bfloat16)) == gdr.gdr_fwd_workspace_bytes(p)
+    # the fused prologue keeps its mapped inputs in the workspace
+    assert gdr.gdr_fwd_workspace_bytes(prob(prologue=7)) > gdr.gdr_fwd_workspace_bytes(p)
+    assert gdr.gdr_bwd_workspace_bytes(prob(prologue=1)) > gdr.gdr_bwd_workspace_bytes(p)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -65,6 +68,7 @@ def test_size_queries(lib):
     (dict(dtype=torch.float16), gdr.GDR_ERR_INVALID_ARG),
     (dict(T=-1), gdr.GDR_ERR_INVALID_ARG),
     (dict(h_dtype=torch.float16), gdr.GDR_ERR_INVALID_ARG),  # h_saved is fp32 or bf16
+    (dict(prologue=8), gdr.GDR_ERR_INVALID_ARG),              # unknown prologue bit
 ])
 def test_bad_problems_are_rejected(lib, kw, code):
     p = prob(**kw)

@@ -198,3 +198,56 @@ def test_bf16_saved_states_leave_tensor_core_forward_unchanged():
     assert torch.equal(r32["o"], r16["o"])
     assert torch.equal(r32["S_T"], r16["S_T"])
     assert torch.equal(r32["h_saved"].to(torch.bfloat16), r16["h_saved"])
+
+
+# ---------------------------------------------------------------- fused input prologue
+# Raw q, k (not normalised), raw gate and beta logits; the operator applies the q/k L2
+# norm, logsigmoid and sigmoid itself and returns gradients w.r.t. the raw tensors.
+PROLOGUE_CASES = [
+    # name, dtype, B, T, Hk, Hv, D, layout, seqlens, flags
+    ("tc_all", torch.bfloat16, 2, 300, 2, 2, 128, "KV", None, 7),
+    ("tc_gva_varlen_all", torch.bfloat16, 1, None, 1, 2, 128, "VK", [0, 1, 64, 77, 200], 7),
+    ("tc_qk_only", torch.bfloat16, 1, 150, 1, 1, 128, "KV", None, 1),
+    ("tc_g_only", torch.bfloat16, 1, 150, 1, 1, 128, "KV", None, 2),
+    ("tc_beta_only", torch.bfloat16, 1, 150, 1, 1, 128, "KV", None, 4),
+    ("simt_f32_all", torch.float32, 2, 130, 2, 4, 32, "VK", None, 7),
+    ("simt_bf16_d64_all", torch.bfloat16, 1, 150, 1, 1, 64, "KV", None, 7),
+]
+
+
+@pytest.mark.parametrize("case", PROLOGUE_CASES, ids=[c[0] for c in PROLOGUE_CASES])
+def test_fused_prologue_matches_oracle(case):
+    name, dt, B, T, Hk, Hv, D, layout, lens, flags = case
+    if lens is None:
+        w = small_workload(name, dt, B, T, Hk, Hv, D, D, layout)
+    else:
+        w = small_workload(name, dt, Hk=Hv // 2 if Hv > 1 else 1, Hv=Hv, DK=D, DV=D, seqlens=lens, layout=layout)
+    inp = make_inputs(w, raw=True)
+    # inputs whose prologue bit is off are passed already mapped
+    if not flags & 1:
+        for key in ["q", "k"]:
+            inp[key] = torch.nn.functional.normalize(inp[key].float(), dim=-1).to(dt)
+    if not flags & 2:
+        inp["g"] = torch.nn.functional.logsigmoid(inp["g"])
+    if not flags & 4:
+        inp["beta"] = torch.sigmoid(inp["beta"].float()).to(dt)
+    res = run_gpu(inp, prologue=flags)
+    torch.cuda.synchronize()
+    compare(res, reference(inp, prologue=flags), tol_for(dt))
+
+
+def test_fused_prologue_autograd():
+    import chunked_gated_delta_04_gb300 as gdr
+
+    w = small_workload("agp", torch.bfloat16, T=100, DK=128, DV=128)
+    inp = make_inputs(w, raw=True)
+    dev = {k_: (v_.cuda() if isinstance(v_, torch.Tensor) else v_) for k_, v_ in inp.items()}
+    leaves = {k_: dev[k_].clone().requires_grad_(True) for k_ in ["q", "k", "v", "g", "beta", "S0"]}
+    o, ST = gdr.chunk_gated_delta_rule(leaves["q"], leaves["k"], leaves["v"], leaves["g"], leaves["beta"],
+                                       leaves["S0"], None, "KV", prologue=gdr.GDR_PROLOGUE_ALL)
+    loss = (o.float() * dev["dO"].float()).sum() + (ST * dev["dS_T"]).sum()
+    loss.backward()
+    ref = reference(inp, prologue=7)
+    got = {"o": o, "S_T": ST, "dq": leaves["q"].grad, "dk": leaves["k"].grad, "dv": leaves["v"].grad,
+           "dg": leaves["g"].grad, "dbeta": leaves["beta"].grad, "dS0": leaves["S0"].grad}
+    compare(got, ref, tol_for(torch.bfloat16))
