@@ -116,7 +116,7 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
       w.Tb = take(el * chH * kChunk * kChunk);
       w.dVn = take(el * chH * kChunk * d.DV);
     }
-    if (d.G > 1) {
+    if (d.G > 1 && !grad_pair_mode(d)) {
       w.dq_part = (float*)take(sizeof(float) * (size_t)d.T_total * d.Hv * d.DK);
       w.dk_part = (float*)take(sizeof(float) * (size_t)d.T_total * d.Hv * d.DK);
     }

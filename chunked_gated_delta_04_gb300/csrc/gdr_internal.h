@@ -129,6 +129,7 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows);
 bool map_2d_box(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32_t esz, uint64_t cols,
                 uint64_t rows, uint32_t box_cols, uint32_t box_rows);
 bool tc_bwd_available();  // the tensor-core backward is built
+bool grad_pair_mode(const Dims& d);  // Hv = 2 Hk tensor-core backward: dq/dk summed on chip
 // The chunk-prep kernel (W, U, P, gamma; with write_T also T) on the tensor cores.
 cudaError_t tc_launch_prep(const Dims& d, const void* q, const void* k, const void* v, const float* g,
                            const void* beta, const Workspace& ws, int write_T, cudaStream_t s, const char* stage);

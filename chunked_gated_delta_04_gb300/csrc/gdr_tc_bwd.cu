@@ -21,6 +21,7 @@
 // No floating-point atomics anywhere: every reduction has a fixed order, so the
 // backward is bitwise deterministic.
 #include <cudaTypedefs.h>
+#include <cstdio>
 
 #include "gdr_internal.h"
 #include "tc_common.cuh"
@@ -32,6 +33,21 @@ namespace {
 using namespace tcx;
 using tc::kmaj;
 using tc::mnmaj;
+
+// 32 fp32 -> 32 bf16 in global memory (64 bytes, 16-byte aligned).
+__device__ __forceinline__ void st_global_bf16x32(bf16* dst, const float* v) {
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    uint4 w;
+    uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      __nv_bfloat162 b = __floats2bfloat162_rn(v[ch * 8 + 2 * e], v[ch * 8 + 2 * e + 1]);
+      wp[e] = *reinterpret_cast<uint32_t*>(&b);
+    }
+    reinterpret_cast<uint4*>(dst)[ch] = w;
+  }
+}
 
 // ---------------------------------------------------------------------------------
 // walk
@@ -248,7 +264,13 @@ struct GradSmem {
 
 constexpr int kGradThreads = 256;  // two warps per TMEM lane quarter, each on half the columns
 
-template <bool kGroup>
+// kGroup: Hv > Hk; dq, dk are summed over the v-heads of a q/k head.  kPair (Hv = 2 Hk,
+// launched as clusters of two CTAs): the two CTAs of a cluster take the two v-heads of one
+// q/k head on the same chunk, and each finalises half of the dq and dk columns, adding the
+// partner's partial sent through distributed shared memory (no fp32 partials in HBM and
+// no separate reduction).  Otherwise (kGroup alone) fp32 partials go to the workspace and
+// launch_group_reduce sums them.
+template <bool kGroup, bool kPair = false>
 __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -262,6 +284,7 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint64_t bar_tma, bar_tma2, bar_mma;
+  __shared__ uint64_t bar_qfree, bar_qdata, bar_kfree, bar_kdata;  // pair exchange (kPair)
   __shared__ uint32_t tmem_slot;
   __shared__ float s_beta[64], s_eg[64], s_dgam[64], s_colpp[64], s_colbk[64], s_colaa[64], s_red[8];
   // per-row partial sums of the two column halves: [half][row]
@@ -276,16 +299,24 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   const int Hv = d.Hv;
   using S = GradSmem;
 
+  const uint32_t rank = kPair ? tc::cluster_ctarank() : 0u, peer = rank ^ 1u;
   if (tid == 0) {
     tc::mbar_init(&bar_tma, 1);
     tc::mbar_init(&bar_tma2, 1);
     tc::mbar_init(&bar_mma, 1);
+    if (kPair) {
+      tc::mbar_init(&bar_qfree, 1);
+      tc::mbar_init(&bar_qdata, 1);
+      tc::mbar_init(&bar_kfree, 1);
+      tc::mbar_init(&bar_kdata, 1);
+    }
     tc::fence_barrier_init();
   }
   if (warp == 0) tc::tmem_alloc(&tmem_slot, 512);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  if (kPair) tc::cluster_sync();  // the partner's barriers exist before anyone arrives on them
   const uint32_t tb = tmem_slot;
   // TMEM columns: [K K^T ; Q K^T] 0-63 (K K^T kept to the end); dq 256-383; dk 384-511.
   const uint32_t C_KK = tb, C_DQ = tb + 256, C_DK = tb + 384;
@@ -297,15 +328,22 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   // store), all on the next phase of bar_tma, so the loads overlap the current item.
   bool ok = true;
   uint32_t item_par = 0;  // phase parity of bar_tma / bar_tma2 for the current item
-  const int n_items = d.max_chunks * Hv;
+  // items: (chunk, v-head), or with kPair (chunk, q/k head) shared by the cluster, whose
+  // CTA `rank` takes v-head 2 i + rank
+  const int n_items = kPair ? d.max_chunks * d.Hk : d.max_chunks * Hv;
+  const int item0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int istep = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  auto chunk_of = [&](int w) { return kPair ? w / d.Hk : w / Hv; };
+  auto vhead_of = [&](int w) { return kPair ? (w % d.Hk) * 2 + (int)rank : w % Hv; };
   auto next_item = [&](int w) {  // next non-empty item of this CTA after w (or n_items)
-    for (w += gridDim.x; w < n_items && ws.chunks[w / Hv].z <= 0; w += gridDim.x) {
+    for (w += istep; w < n_items && ws.chunks[chunk_of(w)].z <= 0; w += istep) {
     }
     return w < n_items ? w : n_items;
   };
+  int cur_len = 0, cur_t0 = 0, cur_i = 0;  // the current item (for pair_reduce)
   enum : int { kLdDhDvn = 1, kLdW = 2, kLdRest = 4, kLdDo = 8, kLdAll = 15 };
   auto issue_loads = [&](int w, int groups) {  // copy thread only
-    const int c2 = w / Hv, j2 = w % Hv, i2 = j2 / d.G, tt = ws.chunks[c2].y;
+    const int c2 = chunk_of(w), j2 = vhead_of(w), i2 = j2 / d.G, tt = ws.chunks[c2].y;
     const size_t ch2 = (size_t)c2 * Hv + j2;
     uint64_t* bar = &bar_tma;
     if (groups & kLdDhDvn) {  // the first group of an item sets the whole item's byte count
@@ -342,14 +380,63 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
       tc::tma_load_3d(sm + S::DO + kSlab, &tm_do, bar, 64, j2, tt);
     }
   };
-  int witem = blockIdx.x < n_items && ws.chunks[blockIdx.x / Hv].z <= 0 ? next_item(blockIdx.x) : blockIdx.x;
+  // kPair: combine one 64 x 128 fp32 result (dq or dk, TMEM columns col..col+127) of the two
+  // CTAs.  This CTA finalises columns [64 rank, +64): the lo threads of the other half (hf !=
+  // rank) stream their 64 columns of row r into the partner's receive tile `buf` with st.async
+  // (each 16-byte piece completes 16 bytes on the partner's bar_data), once the partner has
+  // said the tile is free; the lo threads of this half wait for the partner's 16 KB, add and
+  // write bf16.  buf is [64][64] fp32 with the 16-byte pieces of row r rotated by (r & 15).
+  // Every thread calls it; all waits are bounded (and made warp-uniform: the loops hold
+  // warp-collective TMEM loads).
+  auto pair_reduce = [&](uint32_t col, uint32_t buf_off, uint64_t* bar_free, uint64_t* bar_data, bf16* out,
+                         bool okin) {
+    bool okw = true;
+    if (tid == 0) tc::mbar_arrive_expect_tx(bar_data, 64 * 256);  // the partner's half for this item
+    if (okin && lo && hf != (int)rank) {
+      okw = __all_sync(0xffffffffu, tc::mbar_wait_cluster(bar_free, item_par, ws.status, kDevErrTimeoutBwd));
+      const uint32_t dst = tc::mapa(tc::smem_u32(sm + buf_off), peer) + (uint32_t)r * 256u;
+      const uint32_t cbar = tc::mapa(tc::smem_u32(bar_data), peer);
+#pragma unroll 1
+      for (int q2 = 0; q2 < 2 && okw; ++q2) {
+        float x[32];
+        tmem_ld32w(tb, warp, col + hf * 64 + 32 * q2, x);
+#pragma unroll
+        for (int p4 = 0; p4 < 8; ++p4)
+          tc::st_async_cluster_f32x4(dst + (uint32_t)(((8 * q2 + p4) ^ (r & 15)) << 4), x[4 * p4], x[4 * p4 + 1],
+                                     x[4 * p4 + 2], x[4 * p4 + 3], cbar);
+      }
+    }
+    if (okin && lo && hf == (int)rank) {
+      okw = __all_sync(0xffffffffu, tc::mbar_wait_cluster(bar_data, item_par, ws.status, kDevErrTimeoutBwd));
+      const unsigned char* src = sm + buf_off + r * 256;
+#pragma unroll 1
+      for (int q2 = 0; q2 < 2 && okw; ++q2) {
+        float x[32];
+        tmem_ld32w(tb, warp, col + hf * 64 + 32 * q2, x);
+#pragma unroll
+        for (int p4 = 0; p4 < 8; ++p4) {
+          const float4 t = *reinterpret_cast<const float4*>(src + (((8 * q2 + p4) ^ (r & 15)) << 4));
+          x[4 * p4] += t.x;
+          x[4 * p4 + 1] += t.y;
+          x[4 * p4 + 2] += t.z;
+          x[4 * p4 + 3] += t.w;
+        }
+        if (r < cur_len) st_global_bf16x32(out + ((size_t)(cur_t0 + r) * d.Hk + cur_i) * 128 + rank * 64 + 32 * q2, x);
+      }
+    }
+    return (bool)__syncthreads_and(okin && okw);
+  };
+  int witem = item0 < n_items && ws.chunks[chunk_of(item0)].z <= 0 ? next_item(item0) : item0;
   if (tid == kCopyTid && witem < n_items) issue_loads(witem, kLdAll);
   int pending = witem < n_items ? 0 : -1;  // groups of the next item issued so far (-1: none expected)
   for (int wnext; witem < n_items && ok; witem = wnext) {
   wnext = next_item(witem);
-  const int c = witem / Hv, j = witem % Hv, i = j / d.G;
+  const int c = chunk_of(witem), j = vhead_of(witem), i = j / d.G;
   const int4 ci = ws.chunks[c];
   const int len = ci.z, t0 = ci.y;
+  cur_len = len;
+  cur_t0 = t0;
+  cur_i = i;
   const size_t ch = (size_t)c * Hv + j;
   pending = wnext < n_items ? 0 : -1;
   if (tid < 64) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * Hv + j]) : 0.f;
@@ -470,6 +557,10 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
+  if (kPair && tid == 0) {  // P4 was the last reader of DH and DO: the partner may fill them
+    tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&bar_qfree), peer));
+    tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&bar_kfree), peer));
+  }
   GDR_TRACE_MARK(2, 4);
   if (ok && lo) {
     {  // dP and dP * QK for columns [32 hf, 32 hf + 32)
@@ -531,8 +622,9 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 6);
+  if (kPair) ok = pair_reduce(256, S::DH, &bar_qfree, &bar_qdata, dq, ok);  // dq; DH receives
   if (ok && lo) {
-    {  // dq columns [64 hf, +64) (final for one v-head per q/k head)
+    if (!kPair) {  // dq columns [64 hf, +64) (final for one v-head per q/k head)
       float x[64];
       tmem_ld64(tb, warp, 256 + hf * 64, x);
       if (kGroup) {
@@ -686,10 +778,12 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
     pending |= kLdRest;
   }
   GDR_TRACE_MARK(2, 12);
+  if (kPair) ok = pair_reduce(384, S::DO, &bar_kfree, &bar_kdata, dk, ok);  // dk; DO receives
   if (ok && lo) {
     float x[64];
-    tmem_ld64(tb, warp, 384 + hf * 64, x);  // dk columns [64 hf, +64)
-    if (kGroup) {
+    if (!kPair) tmem_ld64(tb, warp, 384 + hf * 64, x);  // dk columns [64 hf, +64)
+    if (kPair) {
+    } else if (kGroup) {
       if (r < len) {
         float* dst = ws.dk_part + ((size_t)(t0 + r) * Hv + j) * 128 + hf * 64;
 #pragma unroll
@@ -754,9 +848,15 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tb, 512);
+  // no CTA of a pair leaves while its partner may still write into its shared memory
+  if (kPair) tc::cluster_sync();
 }
 
 }  // namespace
+
+// Hv = 2 Hk on the tensor-core path: the gradient kernel runs as clusters of two CTAs that
+// sum dq and dk on chip (no fp32 partials in the workspace).
+bool grad_pair_mode(const Dims& d) { return d.path == 1 && d.G == 2; }
 
 bool tc_bwd_available() { return get_encoder(); }
 
@@ -799,7 +899,32 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     const long long n_items = (long long)d.max_chunks * d.Hv;
     const dim3 grid((unsigned)(n_items < n_sm ? n_items : n_sm));  // persistent: one CTA per SM
     const size_t smg = GradSmem::BYTES + 1024;
-    if (d.G > 1) {
+    if (grad_pair_mode(d)) {  // clusters of two CTAs, one per v-head of a q/k head
+      auto kern = tc_bwd_grad_kernel<true, true>;
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.blockDim = dim3(kGradThreads);
+      cfg.dynamicSmemBytes = smg;
+      cfg.stream = s;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      cfg.gridDim = dim3(2);
+      int n_clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&n_clusters, kern, &cfg) != cudaSuccess || n_clusters < 1) n_clusters = 1;
+      const long long pairs = (long long)d.max_chunks * d.Hk;
+      cfg.gridDim = dim3(2u * (unsigned)(pairs < n_clusters ? pairs : n_clusters));  // persistent
+#ifdef GDR_TRACE
+      fprintf(stderr, "grad pair mode: %d co-resident clusters, grid %u\n", n_clusters, cfg.gridDim.x);
+#endif
+      e = cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, tdo, tw, tu, tdvn, tdh, thf, tt, tdq, tdk, tdv, d,
+                             (const bf16*)a.beta, (bf16*)a.dq, (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
+      if (e != cudaSuccess) return e;
+    } else if (d.G > 1) {
       cudaFuncSetAttribute(tc_bwd_grad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
       tc_bwd_grad_kernel<true><<<grid, kGradThreads, smg, s>>>(tq, tk, tv, tdo, tw, tu, tdvn, tdh, thf, tt, tdq, tdk,
                                                               tdv, d, (const bf16*)a.beta, (bf16*)a.dq,
@@ -811,7 +936,7 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
                                                                (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
     }
     stage_mark(s, "bwd_grad");
-    if (d.G > 1) {
+    if (d.G > 1 && !grad_pair_mode(d)) {
       e = launch_group_reduce(d, a.dq, a.dk, ws, s);
       if (e != cudaSuccess) return e;
     }
