@@ -47,6 +47,7 @@ STAGE_IO = {
     "bwd_grad": ("q k v dO beta h_saved", "dq dk dv dg dbeta"),
 
     "bwd_group_reduce": ("", "dq dk"),
+    "bwd_walkgrad": ("q k v dO beta h_saved dS_T", "dq dk dv dg dbeta dS0"),
     "prologue": ("q k g beta", ""),
     "prologue_bwd": ("", "dq dk dg dbeta"),
 }

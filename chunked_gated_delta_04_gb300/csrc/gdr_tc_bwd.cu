@@ -63,18 +63,44 @@ struct WalkSmem {
 
 constexpr int kWalkThreads = 256;  // two warps per TMEM lane quarter, each on 32 of the 64 columns
 
-__global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
-    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
-    const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dhs,
-    const __grid_constant__ CUtensorMap tm_dvs, Dims d, const float* __restrict__ dS_T, float* __restrict__ dS0,
-    Workspace ws) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = align1024(smem_raw);
+// Counts one finished slice of a chunk: its TMA stores (async proxy) are complete; make them
+// visible at GPU scope before the count.
+__device__ __forceinline__ void publish_chunk(uint32_t* flag) {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+  atomicAdd(flag, 1u);
+}
+
+// Bounded wait until *flag >= target (acquire at GPU scope), then orders the caller's later
+// TMA loads after it.  On expiry sets `bit` in *status and returns false.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t target, uint32_t* status, uint32_t bit) {
+  uint32_t v;
+  const uint64_t t0 = tc::globaltimer_ns();
+  while (true) {
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v >= target) break;
+    if (tc::globaltimer_ns() - t0 > tc::kWaitLimitNs) {
+      atomicOr(status, bit);
+      return false;
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
+// One walk unit = (sequence, v-head, 64-wide DV slice); `unit` = (seq rank * Hv + v-head) * 2 +
+// slice, sequences longest first.  tb: 256 TMEM columns owned by the caller.  With kPublish
+// the copy thread counts each chunk into ws.walk_flags[chunk * Hv + v-head] once its dh' and
+// dVn tiles have fully reached memory (the fused walk + gradient kernel waits on it).
+template <bool kPublish>
+__device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_w,
+                                          const CUtensorMap& tm_p, const CUtensorMap& tm_do,
+                                          const CUtensorMap& tm_dhs, const CUtensorMap& tm_dvs, const Dims& d,
+                                          const float* __restrict__ dS_T, float* __restrict__ dS0,
+                                          const Workspace& ws, int unit, uint32_t tb, unsigned char* sm) {
   __shared__ uint64_t bar_load[2], bar_mma;
-  __shared__ uint32_t tmem_slot;
-  const int n = ws.seq_order[blockIdx.x], j = blockIdx.y, i = j / d.G;
-  const int dv0 = blockIdx.z * 64;
+  const int n = ws.seq_order[unit / (2 * d.Hv)], j = (unit >> 1) % d.Hv, i = j / d.G;
+  const int dv0 = (unit & 1) * 64;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int hf = warp >> 2;            // column half [32 hf, 32 hf + 32) of the slice
   const int dk = tid & 127;            // TMEM lane = row of the dh' slice
@@ -94,11 +120,9 @@ __global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
     tc::mbar_init(&bar_mma, 1);
     tc::fence_barrier_init();
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  const uint32_t tb = tmem_slot;
   // TMEM: K dh' (0-63), P^T dO (64-127), W^T dVn (128-191), Q^T diag(e^gamma) dO (192-255)
   const uint32_t Da = tb, Db = tb + 64, Dc = tb + 128, Dd = tb + 192;
 
@@ -130,6 +154,7 @@ __global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
 
   bool ok = true;
   uint32_t mma_phase = 0;
+  int prev_c = -1;  // kPublish: chunk whose stores are in flight
   GDR_TRACE_INIT();
   for (int it = 0; c_end - 1 - it >= c_begin && ok; ++it) {
     const int c = c_end - 1 - it, st = it & 1;
@@ -220,12 +245,27 @@ __global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
 #pragma unroll
       for (int b = 0; b < 32; ++b) dh[b] = eC * dh[b] + d.scale * y[b] - x[b];
     }
-    if (tid == kCopyTid) tc::bulk_wait_read<1>();  // this chunk's dh' store has left the operand tile
+    if (tid == kCopyTid) {
+      tc::bulk_wait_read<1>();  // this chunk's dh' store has left the operand tile
+      if (kPublish) {  // the previous chunk's two stores have had a whole chunk to land
+        if (prev_c >= 0) {
+          tc::bulk_wait<2>();
+          publish_chunk(ws.walk_flags + (size_t)prev_c * Hv + j);
+        }
+        prev_c = c;
+      }
+    }
     tc::tc_fence_before();
     __syncthreads();
     GDR_TRACE_MARK(3, 6);
   }
-  if (tid == kCopyTid) tc::bulk_wait_read<0>();  // smem sources read before exit
+  if (tid == kCopyTid) {
+    tc::bulk_wait_read<0>();  // smem sources read before exit
+    if (kPublish && prev_c >= 0) {
+      tc::bulk_wait<0>();
+      publish_chunk(ws.walk_flags + (size_t)prev_c * Hv + j);
+    }
+  }
   if (ok && dS0) {
     const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
     const int c0 = dv0 + 32 * hf;
@@ -235,7 +275,28 @@ __global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tb, 256);
+  if (tid == 0) {  // the next unit of this CTA initialises them again
+    tc::mbar_inval(&bar_load[0]);
+    tc::mbar_inval(&bar_load[1]);
+    tc::mbar_inval(&bar_mma);
+  }
+}
+
+__global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
+    const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dhs,
+    const __grid_constant__ CUtensorMap tm_dvs, Dims d, const float* __restrict__ dS_T, float* __restrict__ dS0,
+    Workspace ws) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = align1024(smem_raw);
+  __shared__ uint32_t tmem_slot;
+  if (threadIdx.x < 32) tc::tmem_alloc(&tmem_slot, 256);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  walk_body<false>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvs, d, dS_T, dS0, ws, (int)blockIdx.x, tmem_slot, sm);
+  if (threadIdx.x < 32) tc::tmem_dealloc(tmem_slot, 256);
 }
 
 // ---------------------------------------------------------------------------------
@@ -270,22 +331,21 @@ constexpr int kGradThreads = 256;  // two warps per TMEM lane quarter, each on h
 // partner's partial sent through distributed shared memory (no fp32 partials in HBM and
 // no separate reduction).  Otherwise (kGroup alone) fp32 partials go to the workspace and
 // launch_group_reduce sums them.
-template <bool kGroup, bool kPair = false>
-__global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
-    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
-    const __grid_constant__ CUtensorMap tm_dvn, const __grid_constant__ CUtensorMap tm_dh,
-    const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_t,
-    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
-    const __grid_constant__ CUtensorMap tm_dv, Dims d, const bf16* __restrict__ beta, bf16* __restrict__ dq,
+// kDyn (fused walk + gradient kernel, fixed length): items are claimed from ws.grad_queue in the
+// order the walk finishes them (last chunk of every sequence first), and a chunk's dh' and dVn
+// tiles are loaded only once both walk slices have counted it in ws.walk_flags.
+// tb: 512 TMEM columns owned by the caller.
+template <bool kGroup, bool kPair, bool kDyn>
+__device__ __forceinline__ void grad_body(
+    const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_do,
+    const CUtensorMap& tm_w, const CUtensorMap& tm_u, const CUtensorMap& tm_dvn, const CUtensorMap& tm_dh,
+    const CUtensorMap& tm_h, const CUtensorMap& tm_t, const CUtensorMap& tm_dq, const CUtensorMap& tm_dk,
+    const CUtensorMap& tm_dv, const Dims& d, const bf16* __restrict__ beta, bf16* __restrict__ dq,
     bf16* __restrict__ dk, bf16* __restrict__ dv, float* __restrict__ dg, bf16* __restrict__ dbeta,
-    Workspace ws) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = align1024(smem_raw);
+    const Workspace& ws, uint32_t tb, unsigned char* sm) {
   __shared__ uint64_t bar_tma, bar_tma2, bar_mma;
   __shared__ uint64_t bar_qfree, bar_qdata, bar_kfree, bar_kdata;  // pair exchange (kPair)
-  __shared__ uint32_t tmem_slot;
+  __shared__ int s_claim;                                          // kDyn: the next item
   __shared__ float s_beta[64], s_eg[64], s_dgam[64], s_colpp[64], s_colbk[64], s_colaa[64], s_red[8];
   // per-row partial sums of the two column halves: [half][row]
   __shared__ float s_qh[2][64], s_rowpp[2][64], s_kdv[2][64], s_dbv[2][64], s_akk[2][64], s_rowaa[2][64];
@@ -312,12 +372,10 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
     }
     tc::fence_barrier_init();
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_slot, 512);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   if (kPair) tc::cluster_sync();  // the partner's barriers exist before anyone arrives on them
-  const uint32_t tb = tmem_slot;
   // TMEM columns: [K K^T ; Q K^T] 0-63 (K K^T kept to the end); dq 256-383; dk 384-511.
   const uint32_t C_KK = tb, C_DQ = tb + 256, C_DK = tb + 384;
   GDR_TRACE_INIT();
@@ -333,7 +391,16 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   const int n_items = kPair ? d.max_chunks * d.Hk : d.max_chunks * Hv;
   const int item0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int istep = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  auto chunk_of = [&](int w) { return kPair ? w / d.Hk : w / Hv; };
+  // kDyn (fixed length, nc chunks per sequence): item w = (walk step s, sequence n, v-head j)
+  // -> chunk n * nc + nc - 1 - s
+  const int nc_seq = kDyn ? d.max_chunks / (d.num_seqs > 0 ? d.num_seqs : 1) : 1;
+  auto chunk_of = [&](int w) {
+    if (kDyn) {
+      const int per_step = d.num_seqs * Hv;
+      return ((w % per_step) / Hv) * nc_seq + nc_seq - 1 - w / per_step;
+    }
+    return kPair ? w / d.Hk : w / Hv;
+  };
   auto vhead_of = [&](int w) { return kPair ? (w % d.Hk) * 2 + (int)rank : w % Hv; };
   auto next_item = [&](int w) {  // next non-empty item of this CTA after w (or n_items)
     for (w += istep; w < n_items && ws.chunks[chunk_of(w)].z <= 0; w += istep) {
@@ -347,6 +414,9 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
     const size_t ch2 = (size_t)c2 * Hv + j2;
     uint64_t* bar = &bar_tma;
     if (groups & kLdDhDvn) {  // the first group of an item sets the whole item's byte count
+      // kDyn: dh' and dVn of this chunk come from the walk running in the same kernel; on a
+      // timeout the loads are left out and the item's own bounded wait ends the walk
+      if (kDyn && !wait_flag(ws.walk_flags + ch2, 2u, ws.status, kDevErrTimeoutBwd)) return;
       tc::mbar_arrive_expect_tx(bar, (d.h_bf16 ? 20 : 24) * kSlab + 256);
       for (int q4 = 0; q4 < 4; ++q4)  // dh' rows (q4 & 1) * 64.., columns (q4 >> 1) * 64..
         tc::tma_load_2d(sm + S::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
@@ -426,11 +496,24 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
     }
     return (bool)__syncthreads_and(okin && okw);
   };
-  int witem = item0 < n_items && ws.chunks[chunk_of(item0)].z <= 0 ? next_item(item0) : item0;
+  int witem;
+  if (kDyn) {
+    if (tid == kCopyTid) s_claim = (int)atomicAdd(ws.grad_queue, 1u);
+    __syncthreads();
+    witem = s_claim;
+    __syncthreads();
+  } else {
+    witem = item0 < n_items && ws.chunks[chunk_of(item0)].z <= 0 ? next_item(item0) : item0;
+  }
   if (tid == kCopyTid && witem < n_items) issue_loads(witem, kLdAll);
   int pending = witem < n_items ? 0 : -1;  // groups of the next item issued so far (-1: none expected)
   for (int wnext; witem < n_items && ok; witem = wnext) {
-  wnext = next_item(witem);
+  if (kDyn) {
+    if (tid == kCopyTid) s_claim = (int)atomicAdd(ws.grad_queue, 1u);  // read by all after the first barrier
+    wnext = n_items;
+  } else {
+    wnext = next_item(witem);
+  }
   const int c = chunk_of(witem), j = vhead_of(witem), i = j / d.G;
   const int4 ci = ws.chunks[c];
   const int len = ci.z, t0 = ci.y;
@@ -438,9 +521,10 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   cur_t0 = t0;
   cur_i = i;
   const size_t ch = (size_t)c * Hv + j;
-  pending = wnext < n_items ? 0 : -1;
   if (tid < 64) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * Hv + j]) : 0.f;
   ok = __syncthreads_and(tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutBwd));
+  if (kDyn) wnext = s_claim < n_items ? s_claim : n_items;
+  pending = wnext < n_items ? 0 : -1;
   const float* sgam = reinterpret_cast<const float*>(sm + S::GAM);
   if (tid < 64) s_eg[tid] = fexp(sgam[tid]);
   const float gC = sgam[len - 1], gr = sgam[r];
@@ -847,9 +931,62 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   if (tid == kCopyTid && !ok && pending > 0) (void)tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutBwd);
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tb, 512);
+}
+
+template <bool kGroup, bool kPair = false>
+__global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
+    const __grid_constant__ CUtensorMap tm_dvn, const __grid_constant__ CUtensorMap tm_dh,
+    const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_t,
+    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+    const __grid_constant__ CUtensorMap tm_dv, Dims d, const bf16* __restrict__ beta, bf16* __restrict__ dq,
+    bf16* __restrict__ dk, bf16* __restrict__ dv, float* __restrict__ dg, bf16* __restrict__ dbeta,
+    Workspace ws) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = align1024(smem_raw);
+  __shared__ uint32_t tmem_slot;
+  if (threadIdx.x < 32) tc::tmem_alloc(&tmem_slot, 512);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  grad_body<kGroup, kPair, false>(tm_q, tm_k, tm_v, tm_do, tm_w, tm_u, tm_dvn, tm_dh, tm_h, tm_t, tm_dq, tm_dk,
+                                  tm_dv, d, beta, dq, dk, dv, dg, dbeta, ws, tmem_slot, sm);
+  if (threadIdx.x < 32) tc::tmem_dealloc(tmem_slot, 512);
   // no CTA of a pair leaves while its partner may still write into its shared memory
   if (kPair) tc::cluster_sync();
+}
+
+// The backward's reverse walk and its gradient kernel in one cooperative launch (every CTA
+// resident, one per SM): CTAs first run walk units (64 at B=2, H=16, leaving the other SMs
+// free), then every CTA claims gradient items in the order the walk completes chunks, so the
+// gradients of late chunks overlap the walk of early ones.
+template <bool kGroup>
+__global__ void __launch_bounds__(kGradThreads) tc_bwd_walkgrad_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
+    const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_dvn,
+    const __grid_constant__ CUtensorMap tm_dh, const __grid_constant__ CUtensorMap tm_dhs,
+    const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_t,
+    const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
+    const __grid_constant__ CUtensorMap tm_dv, Dims d, const float* __restrict__ dS_T, float* __restrict__ dS0,
+    const bf16* __restrict__ beta, bf16* __restrict__ dq, bf16* __restrict__ dk, bf16* __restrict__ dv,
+    float* __restrict__ dg, bf16* __restrict__ dbeta, Workspace ws) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = align1024(smem_raw);
+  __shared__ uint32_t tmem_slot;
+  if (threadIdx.x < 32) tc::tmem_alloc(&tmem_slot, 512);  // both roles' columns
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const int n_units = d.num_seqs * d.Hv * 2;
+  for (int u = (int)blockIdx.x; u < n_units; u += (int)gridDim.x)
+    walk_body<true>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvn, d, dS_T, dS0, ws, u, tmem_slot, sm);
+  grad_body<kGroup, false, true>(tm_q, tm_k, tm_v, tm_do, tm_w, tm_u, tm_dvn, tm_dh, tm_h, tm_t, tm_dq, tm_dk,
+                                 tm_dv, d, beta, dq, dk, dv, dg, dbeta, ws, tmem_slot, sm);
+  if (threadIdx.x < 32) tc::tmem_dealloc(tmem_slot, 512);
 }
 
 }  // namespace
@@ -857,6 +994,12 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
 // Hv = 2 Hk on the tensor-core path: the gradient kernel runs as clusters of two CTAs that
 // sum dq and dk on chip (no fp32 partials in the workspace).
 bool grad_pair_mode(const Dims& d) { return d.path == 1 && d.G == 2; }
+
+// Fixed-length batches on the tensor-core path (not the pair mode): walk and gradients run as
+// one cooperative kernel, see tc_bwd_walkgrad_kernel.
+bool fused_walk_grad(const Dims& d) {
+  return d.path == 1 && d.cu == nullptr && !grad_pair_mode(d) && d.num_seqs > 0 && d.T_total > 0;
+}
 
 bool tc_bwd_available() { return get_encoder(); }
 
@@ -885,11 +1028,40 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
                    : map_2d_box(&thf, a.h_saved, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, rows * 2, 32, 128)))
       return cudaErrorInvalidValue;
   }
+  if (fused_walk_grad(d)) {  // walk and gradients in one cooperative kernel
+    int dev = 0, n_sm = 1, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    const size_t smg = GradSmem::BYTES + 1024;
+    auto kern = d.G > 1 ? tc_bwd_walkgrad_kernel<true> : tc_bwd_walkgrad_kernel<false>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGradThreads, smg) != cudaSuccess || per_sm < 1)
+      return cudaErrorInvalidConfiguration;
+    e = cudaMemsetAsync(ws.walk_flags, 0, sizeof(uint32_t) * ((size_t)d.max_chunks * d.Hv + 64), s);
+    if (e != cudaSuccess) return e;
+    const bf16* beta = (const bf16*)a.beta;
+    bf16 *dq = (bf16*)a.dq, *dk = (bf16*)a.dk, *dv = (bf16*)a.dv, *dbeta = (bf16*)a.dbeta;
+    const float* dS_T = a.dS_T;
+    float *dS0 = a.dS0, *dg = a.dg;
+    Dims dd = d;
+    Workspace w = ws;
+    void* args[] = {&tq, &tk, &tv, &tdo, &tw, &tu, &tp, &tdvn, &tdh, &tdhs, &thf, &tt, &tdq, &tdk, &tdv, &dd,
+                    (void*)&dS_T, (void*)&dS0, (void*)&beta, (void*)&dq, (void*)&dk, (void*)&dv, (void*)&dg,
+                    (void*)&dbeta, &w};
+    e = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)(per_sm * n_sm)), dim3(kGradThreads), args, smg, s);
+    if (e != cudaSuccess) return e;
+    stage_mark(s, "bwd_walkgrad");
+    if (d.G > 1) {
+      e = launch_group_reduce(d, a.dq, a.dk, ws, s);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+  }
   if (d.num_seqs > 0) {
     const size_t sm = WalkSmem::BYTES + 1024;
     cudaFuncSetAttribute(tc_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    tc_bwd_walk_kernel<<<dim3(d.num_seqs, d.Hv, 2), kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, d, a.dS_T,
-                                                                        a.dS0, ws);
+    tc_bwd_walk_kernel<<<d.num_seqs * d.Hv * 2, kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, d, a.dS_T,
+                                                                      a.dS0, ws);
     stage_mark(s, "bwd_walk");
   }
   if (d.max_chunks > 0 && Tt > 0) {
