@@ -114,20 +114,37 @@ struct PrepSmem {
   static constexpr uint32_t KQ = 0;              // [K | Q] x 2 slabs: 32 KB
   static constexpr uint32_t V = 32768;           // 2 slabs: 16 KB
   static constexpr uint32_t TT = V + 16384;      // [T' | T''] bf16: 16 KB
-  static constexpr uint32_t A = TT + 16384;      // fp32 A [64][65]
-  static constexpr uint32_t TF = A + 17408;      // fp32 T [64][65]
+  static constexpr uint32_t A = TT + 16384;      // fp32 A [64][68] (row stride kLdA)
+  static constexpr uint32_t TF = A + 17408;      // fp32 T [64][68]
   static constexpr uint32_t Y = TF + 17408;      // fp32 3 x [16][16] block products
   static constexpr uint32_t PS = Y + 4096;       // P (then T) staged for TMA stores: 8 KB
   static constexpr uint32_t BYTES = PS + 8192;   // 110 KB (two CTAs per SM)
 };
 
-// T = (I + A)^{-1} for strictly lower-triangular A (fp32, row stride 65) by recursive
+// Row stride (floats) of the fp32 A and T tiles: rows start 16-byte aligned for vector
+// loads, and 68 = 4 (mod 32) keeps 8 rows read at one column on distinct banks.
+constexpr int kLdA = 68;
+
+// 4 * N consecutive floats from shared memory (16-byte aligned) into v.
+template <int N>
+__device__ __forceinline__ void ld_f4(const float* __restrict__ src, float* v) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float4 t = reinterpret_cast<const float4*>(src)[i];
+    v[4 * i] = t.x;
+    v[4 * i + 1] = t.y;
+    v[4 * i + 2] = t.z;
+    v[4 * i + 3] = t.w;
+  }
+}
+
+// T = (I + A)^{-1} for strictly lower-triangular A (fp32, row stride kLdA) by recursive
 // 2 x 2 block inversion: with L = [[L11, 0], [L21, L22]], L^{-1} = [[L11^{-1}, 0],
 // [-L22^{-1} L21 L11^{-1}, L22^{-1}]].  Steps: the four 16 x 16 diagonal inverses by
 // forward substitution (one thread per column); the two 16 x 16 off-diagonal blocks
 // of the 32 x 32 diagonal halves; the 32 x 32 lower-left block.  Every product is
-// register-tiled (all loads of a thread before its stores).  Writes the full T
-// (zeros above the diagonal) into sT (row stride 65).  All 128 threads take part.
+// register-tiled with vector loads (all loads of a thread before its stores).  Writes the
+// full T (zeros above the diagonal) into sT (row stride kLdA).  All 128 threads take part.
 __device__ __forceinline__ void solve_unit_lower64(const float* __restrict__ sA, float* __restrict__ sT,
                                                    float* __restrict__ sY, int tid) {
 #ifdef GDR_TRACE
@@ -141,22 +158,22 @@ __device__ __forceinline__ void solve_unit_lower64(const float* __restrict__ sA,
 #else
 #define SOLVE_MARK(k)
 #endif
-  for (int e = tid; e < 64 * 65; e += kTcThreads) sT[e] = 0.f;
+  for (int e = tid; e < 64 * kLdA / 4; e += kTcThreads) reinterpret_cast<float4*>(sT)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
   SOLVE_MARK(0);
   if (tid < 64) {  // diagonal 16 x 16 blocks
     const int b = tid >> 4, c = tid & 15;
-    const float* Ab = sA + (16 * b) * 65 + 16 * b;
+    const float* Ab = sA + (16 * b) * kLdA + 16 * b;
     float col[16];
 #pragma unroll
     for (int rr = 0; rr < 16; ++rr) {
       float acc = (rr == c) ? 1.f : 0.f;
 #pragma unroll
-      for (int m = 0; m < rr; ++m) acc -= Ab[rr * 65 + m] * col[m];
+      for (int m = 0; m < rr; ++m) acc -= Ab[rr * kLdA + m] * col[m];
       col[rr] = acc;
     }
 #pragma unroll
-    for (int rr = 0; rr < 16; ++rr) sT[(16 * b + rr) * 65 + 16 * b + c] = col[rr];
+    for (int rr = 0; rr < 16; ++rr) sT[(16 * b + rr) * kLdA + 16 * b + c] = col[rr];
   }
   __syncthreads();
   SOLVE_MARK(1);
@@ -164,35 +181,27 @@ __device__ __forceinline__ void solve_unit_lower64(const float* __restrict__ sA,
     const int b = tid >> 6, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
     const int r0 = 16 * (2 * b + 1), c0 = 16 * (2 * b);
     float x[16], z[16][4], o[4];
+    ld_f4<4>(sA + (r0 + rr) * kLdA + c0, x);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      x[k] = sA[(r0 + rr) * 65 + c0 + k];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) z[k][q] = sT[(c0 + k) * 65 + c0 + c4 + q];
-    }
+    for (int k = 0; k < 16; ++k) ld_f4<1>(sT + (c0 + k) * kLdA + c0 + c4, z[k]);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       o[q] = 0.f;
 #pragma unroll
       for (int k = 0; k < 16; ++k) o[q] += x[k] * z[k][q];
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) sY[b * 256 + rr * 16 + c4 + q] = o[q];
+    *reinterpret_cast<float4*>(sY + b * 256 + rr * 16 + c4) = make_float4(o[0], o[1], o[2], o[3]);
     __syncthreads();
+    ld_f4<4>(sT + (r0 + rr) * kLdA + r0, x);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      x[k] = sT[(r0 + rr) * 65 + r0 + k];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) z[k][q] = sY[b * 256 + k * 16 + c4 + q];
-    }
+    for (int k = 0; k < 16; ++k) ld_f4<1>(sY + b * 256 + k * 16 + c4, z[k]);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       o[q] = 0.f;
 #pragma unroll
       for (int k = 0; k < 16; ++k) o[q] += x[k] * z[k][q];
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) sT[(r0 + rr) * 65 + c0 + c4 + q] = -o[q];
+    *reinterpret_cast<float4*>(sT + (r0 + rr) * kLdA + c0 + c4) = make_float4(-o[0], -o[1], -o[2], -o[3]);
   }
   __syncthreads();
   SOLVE_MARK(2);
@@ -204,38 +213,33 @@ __device__ __forceinline__ void solve_unit_lower64(const float* __restrict__ sA,
 #pragma unroll
     for (int kh = 0; kh < 32; kh += 16) {
       float x[16], z[16][8];
+      ld_f4<4>(sA + (32 + rr) * kLdA + kh, x);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        x[k] = sA[(32 + rr) * 65 + kh + k];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) z[k][q] = sT[(kh + k) * 65 + c8 + q];
-      }
+      for (int k = 0; k < 16; ++k) ld_f4<2>(sT + (kh + k) * kLdA + c8, z[k]);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
 #pragma unroll
         for (int k = 0; k < 16; ++k) o[q] += x[k] * z[k][q];
     }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) sY[rr * 32 + c8 + q] = o[q];
+    *reinterpret_cast<float4*>(sY + rr * 32 + c8) = make_float4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<float4*>(sY + rr * 32 + c8 + 4) = make_float4(o[4], o[5], o[6], o[7]);
     __syncthreads();
 #pragma unroll
     for (int q = 0; q < 8; ++q) o[q] = 0.f;
 #pragma unroll
     for (int kh = 0; kh < 32; kh += 16) {
       float x[16], z[16][8];
+      ld_f4<4>(sT + (32 + rr) * kLdA + 32 + kh, x);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        x[k] = sT[(32 + rr) * 65 + 32 + kh + k];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) z[k][q] = sY[(kh + k) * 32 + c8 + q];
-      }
+      for (int k = 0; k < 16; ++k) ld_f4<2>(sY + (kh + k) * 32 + c8, z[k]);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
 #pragma unroll
         for (int k = 0; k < 16; ++k) o[q] += x[k] * z[k][q];
     }
-#pragma unroll
-    for (int q = 0; q < 8; ++q) sT[(32 + rr) * 65 + c8 + q] = -o[q];
+    float* dst = sT + (32 + rr) * kLdA + c8;
+    *reinterpret_cast<float4*>(dst) = make_float4(-o[0], -o[1], -o[2], -o[3]);
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(-o[4], -o[5], -o[6], -o[7]);
   }
   __syncthreads();
   SOLVE_MARK(3);
@@ -271,6 +275,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
   tc::tc_fence_after();
   const uint32_t tbase = tmem_slot;
   GDR_TRACE_INIT();
+  GDR_TRACE_CTA_BEGIN();
   // Persistent: each CTA walks the (chunk, v-head) items w = blockIdx.x + k * gridDim.x.
   bool ok = true;
   uint32_t item_par = 0;  // phase parity of bar_tma for the current item (bar_mma: 2 per item)
@@ -334,7 +339,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
 #pragma unroll
       for (int s = 0; s < 64; ++s) row[s] = (s < r && r < len) ? br * fexp(gr - gs[s]) * row[s] : 0.f;
 #pragma unroll
-      for (int s = 0; s < 64; ++s) sA[r * 65 + s] = row[s];
+      for (int s = 0; s < 64; s += 4)
+        *reinterpret_cast<float4*>(sA + r * kLdA + s) = make_float4(row[s], row[s + 1], row[s + 2], row[s + 3]);
     } else {  // P row r
 #pragma unroll
       for (int s = 0; s < 64; ++s) row[s] = (s <= r && r < len) ? row[s] * fexp(gr - s_gam[s]) : 0.f;
@@ -357,15 +363,12 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
   if (ok) {  // rows of T' = T diag(beta e^gamma) (threads 0-63), T'' = T diag(beta) (64-127)
     const int r = tid & 63;
     float x[64];
+    ld_f4<16>(sT + r * kLdA, x);
 #pragma unroll
-    for (int s2 = 0; s2 < 64; ++s2) {
-      const float t = sT[r * 65 + s2];
-      x[s2] = t * (tid < 64 ? s_bexp[s2] : s_beta[s2]);
-    }
+    for (int s2 = 0; s2 < 64; ++s2) x[s2] *= (tid < 64 ? s_bexp[s2] : s_beta[s2]);
     st_row_bf16(sm + PrepSmem::TT + (tid < 64 ? 0 : kSlab), r, x);
     if (write_T && tid < 64) {  // T itself for the backward
-#pragma unroll
-      for (int s2 = 0; s2 < 64; ++s2) x[s2] = sT[r * 65 + s2];
+      ld_f4<16>(sT + r * kLdA, x);
       st_row_bf16(sm + PrepSmem::PS, r, x);
     }
   }
@@ -420,6 +423,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
   __syncthreads();
   tc::tc_fence_after();
   }  // items
+  GDR_TRACE_CTA_END();
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tbase, 256);
@@ -709,6 +713,9 @@ static dim3 prep_grid(const Dims& d) {
 #ifdef GDR_TRACE
 extern "C" int gdr_debug_trace_fwd(unsigned long long* out) {
   return cudaMemcpyFromSymbol(out, tcx::g_gdr_trace, sizeof(tcx::g_gdr_trace)) == cudaSuccess ? 0 : 1;
+}
+extern "C" int gdr_debug_cta_span_fwd(unsigned long long* out) {
+  return cudaMemcpyFromSymbol(out, tcx::g_gdr_cta_span, sizeof(tcx::g_gdr_cta_span)) == cudaSuccess ? 0 : 1;
 }
 #endif
 

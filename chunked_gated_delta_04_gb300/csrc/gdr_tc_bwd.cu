@@ -58,7 +58,9 @@ struct WalkSmem {
   static constexpr uint32_t DH = 2 * STAGE;       // dh' as bf16 B operand: 128 rows x 128 B
   static constexpr uint32_t DVN = DH + 16384;     // dVn bf16 [64][64]
   static constexpr uint32_t DOS = DVN + 8192;     // diag(e^gamma) dO bf16 [64][64]
-  static constexpr uint32_t BYTES = DOS + 8192;
+  static constexpr uint32_t DVN2 = DOS + 8192;    // second dVn tile: chunks alternate, so a store
+                                                  // has a whole chunk to read its tile
+  static constexpr uint32_t BYTES = DVN2 + 8192;
 };
 
 constexpr int kWalkThreads = 256;  // two warps per TMEM lane quarter, each on 32 of the 64 columns
@@ -154,7 +156,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
 
   bool ok = true;
   uint32_t mma_phase = 0;
-  int prev_c = -1;  // kPublish: chunk whose stores are in flight
+  int prev1 = -1, prev2 = -1;  // kPublish: the last two chunks, whose stores may be in flight
   GDR_TRACE_INIT();
   for (int it = 0; c_end - 1 - it >= c_begin && ok; ++it) {
     const int c = c_end - 1 - it, st = it & 1;
@@ -185,7 +187,9 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
     GDR_TRACE_MARK(3, 7);
     if (tid == kCopyTid && c - 1 >= c_begin) issue_loads(c - 1, st ^ 1);  // overlaps the MMAs
     GDR_TRACE_MARK(3, 8);
-    if (tid == kCopyTid) tc::bulk_wait_read<1>();  // the previous chunk's dVn store has left its tile
+    // this chunk's dVn tile was last stored two chunks ago (groups since: dh', dVn, dh')
+    unsigned char* dvn_t = sm + ((it & 1) ? WalkSmem::DVN2 : WalkSmem::DVN);
+    if (tid == kCopyTid) tc::bulk_wait_read<3>();
     GDR_TRACE_MARK(3, 9);
     if (ok && warp >= 4) {  // diag(e^gamma) dO, zero past the chunk end: row r, half (tid >> 6) & 1
       float x[32];
@@ -217,18 +221,18 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       const float dec = fexp(gC - gr);
 #pragma unroll
       for (int b = 0; b < 32; ++b) y[b] = r < len ? d.scale * y[b] + dec * x[b] : 0.f;
-      st_halfrow_bf16(sm + WalkSmem::DVN, r, hf, y);
+      st_halfrow_bf16(dvn_t, r, hf, y);
     }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     if (ok && tid == 0) {
       tc::tc_fence_after();
-      tc::gemm(Dc, mnmaj(stg + WalkSmem::W, kSlab), mnmaj(sm + WalkSmem::DVN, kSlab), 64, 4, false);  // W^T dVn
+      tc::gemm(Dc, mnmaj(stg + WalkSmem::W, kSlab), mnmaj(dvn_t, kSlab), 64, 4, false);  // W^T dVn
       tc::mma_commit(&bar_mma);
     }
     if (ok && tid == kCopyTid) {
-      tc::tma_store_2d(&tm_dvs, sm + WalkSmem::DVN, dv0, (int)(chh * 64));
+      tc::tma_store_2d(&tm_dvs, dvn_t, dv0, (int)(chh * 64));
       tc::bulk_commit();
     }
     GDR_TRACE_MARK(3, 4);
@@ -247,12 +251,13 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
     }
     if (tid == kCopyTid) {
       tc::bulk_wait_read<1>();  // this chunk's dh' store has left the operand tile
-      if (kPublish) {  // the previous chunk's two stores have had a whole chunk to land
-        if (prev_c >= 0) {
-          tc::bulk_wait<2>();
-          publish_chunk(ws.walk_flags + (size_t)prev_c * Hv + j);
+      if (kPublish) {  // the stores of two chunks ago have had two chunks to land
+        if (prev2 >= 0) {
+          tc::bulk_wait<4>();
+          publish_chunk(ws.walk_flags + (size_t)prev2 * Hv + j);
         }
-        prev_c = c;
+        prev2 = prev1;
+        prev1 = c;
       }
     }
     tc::tc_fence_before();
@@ -261,9 +266,10 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
   }
   if (tid == kCopyTid) {
     tc::bulk_wait_read<0>();  // smem sources read before exit
-    if (kPublish && prev_c >= 0) {
+    if (kPublish && prev1 >= 0) {
       tc::bulk_wait<0>();
-      publish_chunk(ws.walk_flags + (size_t)prev_c * Hv + j);
+      if (prev2 >= 0) publish_chunk(ws.walk_flags + (size_t)prev2 * Hv + j);
+      publish_chunk(ws.walk_flags + (size_t)prev1 * Hv + j);
     }
   }
   if (ok && dS0) {

@@ -13,6 +13,26 @@ namespace tcx {
 // spent between consecutive marks into a per-translation-unit table [kernel][mark].
 #ifdef GDR_TRACE
 static __device__ unsigned long long g_gdr_trace[8][32];
+static __device__ unsigned long long g_gdr_cta_span[1024][3];  // per CTA: start, end (ns), SM id
+#define GDR_TRACE_CTA_BEGIN()                                                                      \
+  do {                                                                                             \
+    if (threadIdx.x == 0 && blockIdx.x < 1024) {                                                   \
+      unsigned long long t_;                                                                       \
+      unsigned int sm_;                                                                            \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                      \
+      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));                                             \
+      g_gdr_cta_span[blockIdx.x][0] = t_;                                                          \
+      g_gdr_cta_span[blockIdx.x][2] = sm_;                                                         \
+    }                                                                                              \
+  } while (0)
+#define GDR_TRACE_CTA_END()                                                                        \
+  do {                                                                                             \
+    if (threadIdx.x == 0 && blockIdx.x < 1024) {                                                   \
+      unsigned long long t_;                                                                       \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                      \
+      g_gdr_cta_span[blockIdx.x][1] = t_;                                                          \
+    }                                                                                              \
+  } while (0)
 #define GDR_TRACE_INIT() unsigned long long gdr_tprev_ = clock64()
 #define GDR_TRACE_MARK(kid, slot)                                                                  \
   do {                                                                                             \
@@ -23,6 +43,12 @@ static __device__ unsigned long long g_gdr_trace[8][32];
     }                                                                                              \
   } while (0)
 #else
+#define GDR_TRACE_CTA_BEGIN() \
+  do {                        \
+  } while (0)
+#define GDR_TRACE_CTA_END() \
+  do {                      \
+  } while (0)
 #define GDR_TRACE_INIT() \
   do {                   \
   } while (0)
