@@ -251,3 +251,17 @@ def test_fused_prologue_autograd():
     got = {"o": o, "S_T": ST, "dq": leaves["q"].grad, "dk": leaves["k"].grad, "dv": leaves["v"].grad,
            "dg": leaves["g"].grad, "dbeta": leaves["beta"].grad, "dS0": leaves["S0"].grad}
     compare(got, ref, tol_for(torch.bfloat16))
+
+
+# ---------------------------------------------------------------- fused backward coverage
+# Fixed-length tensor-core batches run the reverse walk and the gradients as one cooperative
+# kernel.  These cases cover a CTA running several walk units (more (sequence, head, DV half)
+# units than SMs), and Hv = 4 Hk (fp32 partials and the group reduce after the fused kernel).
+@pytest.mark.parametrize("name,B,T,Hk,Hv", [("many_walk_units", 10, 130, 8, 8), ("gva4", 2, 150, 1, 4)])
+def test_fused_backward_shapes(name, B, T, Hk, Hv):
+    import chunked_gated_delta_04_gb300 as gdr
+
+    w = small_workload(name, torch.bfloat16, B=B, T=T, Hk=Hk, Hv=Hv, DK=128, DV=128)
+    p = gdr.make_problem(B, T, Hk, Hv, 128, 128, torch.bfloat16, "KV")
+    assert gdr.gdr_path(p) == 1
+    _check(w)
