@@ -13,14 +13,15 @@
 namespace gdr {
 
 constexpr int kIndexThreads = 1024;
-constexpr int kMaxOrderedSeqs = 8192;  // above this the order is the identity
+constexpr int kMaxOrderedSeqs = kMaxFusedSeqs;  // above this the order is the identity
 
 __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t* __restrict__ cu,
                                                                   int num_seqs, int T, int max_chunks,
                                                                   int4* __restrict__ chunks,
                                                                   int* __restrict__ off,
                                                                   int* __restrict__ order,
-                                                                  uint32_t* __restrict__ status) {
+                                                                  uint32_t* __restrict__ status,
+                                                                  int* __restrict__ step_off) {
   __shared__ int warp_tot[32];
   __shared__ int s_bad;
   __shared__ int s_carry;
@@ -116,12 +117,68 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
   } else {
     for (int n = tid; n < num_seqs; n += kIndexThreads) order[n] = n;
   }
+
+  // Walk-step table of the fused backward (step_off != nullptr; requires the sorted order):
+  // at reverse step s the walk finishes local chunk nc(n) - 1 - s of every sequence with
+  // nc(n) > s, i.e. of the first cnt(s) sequences in longest-first order.  step_off[s] =
+  // sum_{s' < s} cnt(s') for s = 0..S (S = the longest sequence's chunk count), and
+  // step_off[max_chunks + 1] = S.  Gradient item q * Hv + j with step_off[s] <= q <
+  // step_off[s + 1] is v-head j of sequence order[q - step_off[s]] at step s.
+  if (step_off != nullptr && bad) {  // nothing is computed: no walk steps, no gradient items
+    if (tid == 0) step_off[0] = step_off[max_chunks + 1] = 0;
+  } else if (step_off != nullptr) {
+    __syncthreads();
+    auto nc_of_rank = [&](int r) { return off[order[r] + 1] - off[order[r]]; };
+    const int S = num_seqs > 0 ? nc_of_rank(0) : 0;
+    for (int st = tid; st < S; st += kIndexThreads) {  // cnt(st): first rank with nc <= st
+      int lo = 0, hi = num_seqs;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (nc_of_rank(mid) > st) lo = mid + 1; else hi = mid;
+      }
+      step_off[st + 1] = lo;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      step_off[0] = 0;
+      step_off[max_chunks + 1] = S;
+      s_carry = 0;
+    }
+    __syncthreads();
+    for (int base = 1; base <= S; base += kIndexThreads) {  // inclusive scan of step_off[1..S]
+      const int st = base + tid;
+      int x = st <= S ? step_off[st] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) warp_tot[warp] = x;
+      __syncthreads();
+      if (warp == 0) {
+        int t = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, t, o);
+          if (lane >= o) t += y;
+        }
+        warp_tot[lane] = t;
+      }
+      __syncthreads();
+      const int carry = s_carry;
+      const int incl = x + (warp > 0 ? warp_tot[warp - 1] : 0);
+      if (st <= S) step_off[st] = carry + incl;
+      __syncthreads();
+      if (tid == kIndexThreads - 1) s_carry = carry + incl;
+      __syncthreads();
+    }
+  }
 }
 
 cudaError_t launch_index(const Dims& d, const Workspace& ws, cudaStream_t s) {
   gdr_index_kernel<<<1, kIndexThreads, 0, s>>>(d.cu, d.num_seqs, d.cu ? (int)d.T_total : d.T,
                                                d.max_chunks, ws.chunks, ws.seq_chunk_off, ws.seq_order,
-                                               ws.status);
+                                               ws.status, ws.step_off);
   stage_mark(s, "index");
   return cudaGetLastError();
 }

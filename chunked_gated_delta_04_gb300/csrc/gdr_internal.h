@@ -58,6 +58,7 @@ struct Workspace {
   // of finished walk slices [max_chunks][Hv], and the gradient items' claim counter
   uint32_t* walk_flags;
   uint32_t* grad_queue;
+  int* step_off;  // [max_chunks + 2]: the walk-step prefix table built by the index kernel
   // fused prologue outputs (input dtype unless noted): normalised q, k [T_total][Hk][DK],
   // g = logsigmoid(a) fp32 [T_total][Hv], beta = sigmoid(b) [T_total][Hv]
   void* qn;
@@ -134,7 +135,8 @@ bool map_2d_box(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32
                 uint64_t rows, uint32_t box_cols, uint32_t box_rows);
 bool tc_bwd_available();  // the tensor-core backward is built
 bool grad_pair_mode(const Dims& d);  // Hv = 2 Hk tensor-core backward: dq/dk summed on chip
-bool fused_walk_grad(const Dims& d);  // fixed-length tensor-core backward: walk and gradients in one kernel
+bool fused_walk_grad(const Dims& d);  // tensor-core backward: walk and gradients in one kernel
+constexpr int kMaxFusedSeqs = 8192;   // the fused backward needs the longest-first order (index kernel)
 // The chunk-prep kernel (W, U, P, gamma; with write_T also T) on the tensor cores.
 cudaError_t tc_launch_prep(const Dims& d, const void* q, const void* k, const void* v, const float* g,
                            const void* beta, const Workspace& ws, int write_T, cudaStream_t s, const char* stage);

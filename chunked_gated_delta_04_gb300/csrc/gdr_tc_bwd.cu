@@ -337,8 +337,8 @@ constexpr int kGradThreads = 256;  // two warps per TMEM lane quarter, each on h
 // partner's partial sent through distributed shared memory (no fp32 partials in HBM and
 // no separate reduction).  Otherwise (kGroup alone) fp32 partials go to the workspace and
 // launch_group_reduce sums them.
-// kDyn (fused walk + gradient kernel, fixed length): items are claimed from ws.grad_queue in the
-// order the walk finishes them (last chunk of every sequence first), and a chunk's dh' and dVn
+// kDyn (fused walk + gradient kernel): items are claimed from ws.grad_queue in the order the
+// walk finishes them (last chunk of every sequence first), and a chunk's dh' and dVn
 // tiles are loaded only once both walk slices have counted it in ws.walk_flags.
 // tb: 512 TMEM columns owned by the caller.
 template <bool kGroup, bool kPair, bool kDyn>
@@ -351,7 +351,7 @@ __device__ __forceinline__ void grad_body(
     const Workspace& ws, uint32_t tb, unsigned char* sm) {
   __shared__ uint64_t bar_tma, bar_tma2, bar_mma;
   __shared__ uint64_t bar_qfree, bar_qdata, bar_kfree, bar_kdata;  // pair exchange (kPair)
-  __shared__ int s_claim;                                          // kDyn: the next item
+  __shared__ int s_claim, s_claim_c;                               // kDyn: the next item, its chunk
   __shared__ float s_beta[64], s_eg[64], s_dgam[64], s_colpp[64], s_colbk[64], s_colaa[64], s_red[8];
   // per-row partial sums of the two column halves: [half][row]
   __shared__ float s_qh[2][64], s_rowpp[2][64], s_kdv[2][64], s_dbv[2][64], s_akk[2][64], s_rowaa[2][64];
@@ -393,17 +393,23 @@ __device__ __forceinline__ void grad_body(
   bool ok = true;
   uint32_t item_par = 0;  // phase parity of bar_tma / bar_tma2 for the current item
   // items: (chunk, v-head), or with kPair (chunk, q/k head) shared by the cluster, whose
-  // CTA `rank` takes v-head 2 i + rank
-  const int n_items = kPair ? d.max_chunks * d.Hk : d.max_chunks * Hv;
+  // CTA `rank` takes v-head 2 i + rank; with kDyn every real chunk's v-heads, in walk order
+  const int n_steps = kDyn ? ws.step_off[d.max_chunks + 1] : 0;
+  const int n_items = kDyn ? ws.step_off[n_steps] * Hv : (kPair ? d.max_chunks * d.Hk : d.max_chunks * Hv);
   const int item0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int istep = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  // kDyn (fixed length, nc chunks per sequence): item w = (walk step s, sequence n, v-head j)
-  // -> chunk n * nc + nc - 1 - s
-  const int nc_seq = kDyn ? d.max_chunks / (d.num_seqs > 0 ? d.num_seqs : 1) : 1;
+  // kDyn: item w = q * Hv + v-head with step_off[s] <= q < step_off[s + 1]: sequence
+  // order[q - step_off[s]], its chunk finished at reverse step s
   auto chunk_of = [&](int w) {
     if (kDyn) {
-      const int per_step = d.num_seqs * Hv;
-      return ((w % per_step) / Hv) * nc_seq + nc_seq - 1 - w / per_step;
+      const int q = w / Hv;
+      int lo = 0, hi = n_steps - 1;  // last s with step_off[s] <= q
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ws.step_off[mid] <= q) lo = mid; else hi = mid - 1;
+      }
+      const int n = ws.seq_order[q - ws.step_off[lo]];
+      return ws.seq_chunk_off[n + 1] - 1 - lo;
     }
     return kPair ? w / d.Hk : w / Hv;
   };
@@ -415,8 +421,8 @@ __device__ __forceinline__ void grad_body(
   };
   int cur_len = 0, cur_t0 = 0, cur_i = 0;  // the current item (for pair_reduce)
   enum : int { kLdDhDvn = 1, kLdW = 2, kLdRest = 4, kLdDo = 8, kLdAll = 15 };
-  auto issue_loads = [&](int w, int groups) {  // copy thread only
-    const int c2 = chunk_of(w), j2 = vhead_of(w), i2 = j2 / d.G, tt = ws.chunks[c2].y;
+  auto issue_loads = [&](int w, int c2, int groups) {  // copy thread only; c2 = chunk_of(w)
+    const int j2 = vhead_of(w), i2 = j2 / d.G, tt = ws.chunks[c2].y;
     const size_t ch2 = (size_t)c2 * Hv + j2;
     uint64_t* bar = &bar_tma;
     if (groups & kLdDhDvn) {  // the first group of an item sets the whole item's byte count
@@ -502,25 +508,31 @@ __device__ __forceinline__ void grad_body(
     }
     return (bool)__syncthreads_and(okin && okw);
   };
-  int witem;
+  // kDyn: the copy thread claims an item and decodes its chunk (a search of the step table)
+  // once; the other threads read both from shared memory after a barrier
+  auto claim = [&]() {
+    const int w = (int)atomicAdd(ws.grad_queue, 1u);
+    s_claim = w;
+    s_claim_c = w < n_items ? chunk_of(w) : 0;
+  };
+  int witem, cur_c = 0;
   if (kDyn) {
-    if (tid == kCopyTid) s_claim = (int)atomicAdd(ws.grad_queue, 1u);
+    if (tid == kCopyTid) claim();
     __syncthreads();
     witem = s_claim;
+    cur_c = s_claim_c;
     __syncthreads();
   } else {
     witem = item0 < n_items && ws.chunks[chunk_of(item0)].z <= 0 ? next_item(item0) : item0;
   }
-  if (tid == kCopyTid && witem < n_items) issue_loads(witem, kLdAll);
+  if (tid == kCopyTid && witem < n_items) issue_loads(witem, kDyn ? cur_c : chunk_of(witem), kLdAll);
   int pending = witem < n_items ? 0 : -1;  // groups of the next item issued so far (-1: none expected)
-  for (int wnext; witem < n_items && ok; witem = wnext) {
-  if (kDyn) {
-    if (tid == kCopyTid) s_claim = (int)atomicAdd(ws.grad_queue, 1u);  // read by all after the first barrier
-    wnext = n_items;
-  } else {
-    wnext = next_item(witem);
-  }
-  const int c = chunk_of(witem), j = vhead_of(witem), i = j / d.G;
+  int cl_w = n_items, cl_c = 0;            // kDyn, copy thread: the claimed next item and its chunk
+  while (witem < n_items && ok) {
+  // the next item (kDyn: claimed at the first prefetch point, known to all after the item)
+  const int wnext = kDyn ? n_items : next_item(witem);
+  const int cnext = kDyn ? 0 : (wnext < n_items ? chunk_of(wnext) : 0);
+  const int c = kDyn ? cur_c : chunk_of(witem), j = vhead_of(witem), i = j / d.G;
   const int4 ci = ws.chunks[c];
   const int len = ci.z, t0 = ci.y;
   cur_len = len;
@@ -529,8 +541,7 @@ __device__ __forceinline__ void grad_body(
   const size_t ch = (size_t)c * Hv + j;
   if (tid < 64) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * Hv + j]) : 0.f;
   ok = __syncthreads_and(tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutBwd));
-  if (kDyn) wnext = s_claim < n_items ? s_claim : n_items;
-  pending = wnext < n_items ? 0 : -1;
+  pending = (kDyn || wnext < n_items) ? 0 : -1;  // kDyn: decided when the next item is claimed
   const float* sgam = reinterpret_cast<const float*>(sm + S::GAM);
   if (tid < 64) s_eg[tid] = fexp(sgam[tid]);
   const float gC = sgam[len - 1], gr = sgam[r];
@@ -771,8 +782,16 @@ __device__ __forceinline__ void grad_body(
   tc::tc_fence_after();
   if (ok && tid == kCopyTid && pending >= 0) {  // dVn is consumed, dq has left its staging tile
     tc::bulk_wait_read<0>();
-    issue_loads(wnext, kLdDhDvn);
-    pending |= kLdDhDvn;
+    if (kDyn) {  // claim the next item now, off the other threads' path
+      claim();
+      cl_w = s_claim;
+      cl_c = s_claim_c;
+      if (cl_w >= n_items) pending = -1;
+    }
+    if (pending >= 0) {
+      issue_loads(kDyn ? cl_w : wnext, kDyn ? cl_c : cnext, kLdDhDvn);
+      pending |= kLdDhDvn;
+    }
   }
   GDR_TRACE_MARK(2, 8);
   if (ok && lo) {
@@ -816,7 +835,7 @@ __device__ __forceinline__ void grad_body(
   tc::tc_fence_after();
   if (ok && tid == kCopyTid && pending >= 0) {  // dv has left its staging tile (W)
     tc::bulk_wait_read<0>();
-    issue_loads(wnext, kLdW);
+    issue_loads(kDyn ? cl_w : wnext, kDyn ? cl_c : cnext, kLdW);
     pending |= kLdW;
   }
   GDR_TRACE_MARK(2, 10);
@@ -864,7 +883,7 @@ __device__ __forceinline__ void grad_body(
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   if (ok && tid == kCopyTid && pending >= 0) {  // every operand tile but dO (dk staging) is free
-    issue_loads(wnext, kLdRest);
+    issue_loads(kDyn ? cl_w : wnext, kDyn ? cl_c : cnext, kLdRest);
     pending |= kLdRest;
   }
   GDR_TRACE_MARK(2, 12);
@@ -922,7 +941,7 @@ __device__ __forceinline__ void grad_body(
   if (tid == kCopyTid) {
     tc::bulk_wait_read<0>();  // staging tiles read before the next item's loads
     if (ok && pending >= 0) {
-      issue_loads(wnext, kLdDo);
+      issue_loads(kDyn ? cl_w : wnext, kDyn ? cl_c : cnext, kLdDo);
       pending |= kLdDo;
     }
   }
@@ -931,6 +950,12 @@ __device__ __forceinline__ void grad_body(
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  if (kDyn) {  // claimed at this item's first prefetch point (if that ran: else ok is false)
+    witem = ok ? s_claim : n_items;
+    cur_c = s_claim_c;
+  } else {
+    witem = wnext;
+  }
   }  // items
   // A failed wait ends the walk early: let the next item's loads that are already in
   // flight land (bounded) before the CTA gives up its shared memory.
@@ -1001,10 +1026,11 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_walkgrad_kernel(
 // sum dq and dk on chip (no fp32 partials in the workspace).
 bool grad_pair_mode(const Dims& d) { return d.path == 1 && d.G == 2; }
 
-// Fixed-length batches on the tensor-core path (not the pair mode): walk and gradients run as
-// one cooperative kernel, see tc_bwd_walkgrad_kernel.
+// Tensor-core backward (not the pair mode; at most kMaxFusedSeqs sequences, whose longest-first
+// order the item queue needs): walk and gradients run as one cooperative kernel, see
+// tc_bwd_walkgrad_kernel.
 bool fused_walk_grad(const Dims& d) {
-  return d.path == 1 && d.cu == nullptr && !grad_pair_mode(d) && d.num_seqs > 0 && d.T_total > 0;
+  return d.path == 1 && !grad_pair_mode(d) && d.num_seqs > 0 && d.num_seqs <= kMaxFusedSeqs && d.T_total > 0;
 }
 
 bool tc_bwd_available() { return get_encoder(); }
