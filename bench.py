@@ -248,7 +248,7 @@ def reference_arm(args, w, inp):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w, inp, args.h_dtype, args.prologue),
+        "config": config_dict(w, inp, args.h_dtype, args.prologue, args.recompute_wy),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(nthreads, units), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -257,13 +257,14 @@ def reference_arm(args, w, inp):
     return 0
 
 
-def config_dict(w, inp, h_dtype="f32", prologue=False):
+def config_dict(w, inp, h_dtype="f32", prologue=False, recompute_wy=False):
     return {"workload": w.name, "B": w.B if inp["cu_seqlens"] is None else 1, "T": int(sum(inp["seqlens"])) if
             inp["cu_seqlens"] is not None else w.T, "Hk": w.Hk, "Hv": w.Hv, "DK": w.DK, "DV": w.DV,
             "layout": w.layout, "num_seqs": inp["num_seqs"], "chunk": CHUNK,
             "varlen": inp["cu_seqlens"] is not None, "S0": inp["S0"] is not None,
             "dS_T": inp["dS_T"] is not None, "h_saved": h_dtype,
             "prologue": "qk_l2norm+g_logsigmoid+beta_sigmoid (raw inputs)" if prologue else "none",
+            "wy_factors": "recomputed by the backward" if recompute_wy else "saved by the forward (save_wy)",
             "l2": "flushed (512 MB write) between timed steps", "parallelism": "replicas"}
 
 
@@ -295,6 +296,9 @@ def main():
                     help="dtype of the saved chunk-start states (bf16 halves the largest tensor)")
     ap.add_argument("--prologue", action="store_true",
                     help="raw q, k, gate and beta logits; the operator applies the L2 norm, logsigmoid, sigmoid")
+    ap.add_argument("--recompute-wy", action="store_true",
+                    help="the backward recomputes the chunk factors (gamma, W, U, P, T) instead of reading the "
+                         "ones the forward saved")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -328,13 +332,13 @@ def main():
     Hv, DV = d["v"].shape[2], d["v"].shape[3]
     h_dtype = torch.bfloat16 if args.h_dtype == "bf16" else torch.float32
     p = gdr.make_problem(B, T, Hk, Hv, DK, DV, d["q"].dtype, w.layout, d["cu_seqlens"], h_dtype=h_dtype,
-                         prologue=prologue_bits)
+                         prologue=prologue_bits, save_wy=not args.recompute_wy)
     stream = torch.cuda.current_stream()
     N = p.num_seqs
     sshape = (N, Hv, DK, DV) if w.layout == "KV" else (N, Hv, DV, DK)
     o = torch.empty_like(d["v"])
     S_T = torch.empty(sshape, dtype=torch.float32, device=dev)
-    h_saved = torch.empty((gdr.gdr_max_chunks(p), Hv, DK, DV), dtype=h_dtype, device=dev)
+    h_saved = gdr.alloc_saved(p, h_dtype, dev)
     dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
     dg, dbeta = torch.empty_like(d["g"]), torch.empty_like(d["beta"])
     dS0 = torch.empty(sshape, dtype=torch.float32, device=dev)
@@ -519,7 +523,7 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
             "data": "synthetic (seeded; see chunked_gated_delta_04_gb300/inputs.py)",
-            "config": config_dict(w, inp, args.h_dtype, args.prologue),
+            "config": config_dict(w, inp, args.h_dtype, args.prologue, args.recompute_wy),
             "roofline": roofline,
             "step_roofline": {"ms": step_roof, "frac": step_roof / ms_per_step, "bound": "hbm" if
                               t_hbm_step >= t_flop_step else "tensor", "bytes": wm["bytes_fwd"] + wm["bytes_bwd"],

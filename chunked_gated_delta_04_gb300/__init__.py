@@ -17,6 +17,7 @@ torch; ``chunk_gated_delta_rule`` is the autograd entry point.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 from typing import Optional
 
@@ -38,7 +39,8 @@ class gdr_problem(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("T", ctypes.c_int), ("Hk", ctypes.c_int), ("Hv", ctypes.c_int),
                 ("DK", ctypes.c_int), ("DV", ctypes.c_int), ("num_seqs", ctypes.c_int),
                 ("cu_seqlens", ctypes.c_void_p), ("dtype", ctypes.c_int), ("layout", ctypes.c_int),
-                ("scale", ctypes.c_float), ("h_dtype", ctypes.c_int), ("prologue", ctypes.c_uint)]
+                ("scale", ctypes.c_float), ("h_dtype", ctypes.c_int), ("prologue", ctypes.c_uint),
+                ("save_wy", ctypes.c_int)]
 
 
 class GDRError(RuntimeError):
@@ -124,9 +126,10 @@ def _dtype_code(dtype):
 
 
 def make_problem(B, T, Hk, Hv, DK, DV, dtype, layout="KV", cu_seqlens=None, num_seqs=None, scale=None,
-                 h_dtype=torch.float32, prologue=0):
+                 h_dtype=torch.float32, prologue=0, save_wy=False):
     """Build a gdr_problem.  dtype, h_dtype (of h_saved): torch.float32/bfloat16; layout "KV"/"VK";
-    prologue: bit set of GDR_PROLOGUE_* (the matching inputs are raw)."""
+    prologue: bit set of GDR_PROLOGUE_* (the matching inputs are raw); save_wy: the forward keeps
+    its chunk factors in the saved buffer for the backward."""
     p = gdr_problem()
     p.B, p.T, p.Hk, p.Hv, p.DK, p.DV = B, T, Hk, Hv, DK, DV
     if cu_seqlens is not None:
@@ -138,6 +141,7 @@ def make_problem(B, T, Hk, Hv, DK, DV, dtype, layout="KV", cu_seqlens=None, num_
     p.dtype = _dtype_code(dtype)
     p.h_dtype = _dtype_code(h_dtype)
     p.prologue = int(prologue)
+    p.save_wy = int(save_wy) if isinstance(save_wy, (bool, int)) else 99
     p.layout = {"KV": GDR_STATE_KV, "VK": GDR_STATE_VK}.get(layout, 99) if isinstance(layout, str) else layout
     p.scale = 0.0 if scale is None else float(scale)
     return p
@@ -239,11 +243,30 @@ def _check(st, where):
         raise GDRError(st, where)
 
 
-def _problem_for(q, v, cu_seqlens, layout, scale, h_dtype=torch.float32, prologue=0):
+def _problem_for(q, v, cu_seqlens, layout, scale, h_dtype=torch.float32, prologue=0, save_wy=False):
     B, T, Hk, DK = q.shape
     Hv, DV = v.shape[2], v.shape[3]
     return make_problem(B, T, Hk, Hv, DK, DV, q.dtype, layout, cu_seqlens, scale=scale, h_dtype=h_dtype,
-                        prologue=prologue)
+                        prologue=prologue, save_wy=save_wy)
+
+
+def alloc_saved(p, h_dtype, device) -> torch.Tensor:
+    """The saved buffer of problem p: a [max_chunks, Hv, DK, DV] h_dtype view of the chunk-start
+    states whose storage also holds the saved factors when p.save_wy is set (the view starts at
+    the buffer's first byte, so its data pointer is the buffer's)."""
+    nbytes = gdr_saved_states_bytes(p)
+    shape = (gdr_max_chunks(p), p.Hv, p.DK, p.DV)
+    states = math.prod(shape) * torch.empty((), dtype=h_dtype).element_size()
+    buf = torch.empty(max(nbytes, states), dtype=torch.uint8, device=device)
+    return buf[:states].view(h_dtype).view(shape)
+
+
+def _check_saved(p, h_saved):
+    need = gdr_saved_states_bytes(p)
+    have = h_saved.untyped_storage().nbytes() - h_saved.storage_offset() * h_saved.element_size()
+    if have < need:
+        raise ValueError(f"saved buffer holds {have} bytes, the problem needs {need} (save_wy={p.save_wy}): "
+                         "allocate it with alloc_saved")
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:
@@ -253,16 +276,17 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 # ------------------------------------------------------------------ allocating helpers
 def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, layout="KV", scale=None, output_final_state=True,
-            workspace=None, stream=None, h_dtype=torch.float32, prologue=0):
+            workspace=None, stream=None, h_dtype=torch.float32, prologue=0, save_wy=False):
     """Run gdr_fwd; returns (o, S_T or None, h_saved).  h_dtype: dtype of h_saved; prologue:
-    GDR_PROLOGUE_* bits (q, k, g, beta raw where set)."""
-    p = _problem_for(q, v, cu_seqlens, layout, scale, h_dtype, prologue)
+    GDR_PROLOGUE_* bits (q, k, g, beta raw where set); save_wy: h_saved's storage also keeps the
+    chunk factors, and backward() must be given save_wy=True too."""
+    p = _problem_for(q, v, cu_seqlens, layout, scale, h_dtype, prologue, save_wy)
     dev = q.device
     N = p.num_seqs
     o = torch.empty_like(v)
     sshape = (N, p.Hv, p.DK, p.DV) if layout == "KV" else (N, p.Hv, p.DV, p.DK)
     S_T = torch.empty(sshape, dtype=torch.float32, device=dev) if output_final_state else None
-    h_saved = torch.empty((gdr_max_chunks(p), p.Hv, p.DK, p.DV), dtype=h_dtype, device=dev)
+    h_saved = alloc_saved(p, h_dtype, dev)
     if workspace is None:
         workspace = alloc_workspace(gdr_fwd_workspace_bytes(p), dev)
     _check(gdr_fwd(p, q, k, v, g, beta, S0, o, S_T, h_saved, workspace, stream=stream), "gdr_fwd")
@@ -270,10 +294,11 @@ def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, layout="KV", scale=None,
 
 
 def backward(q, k, v, g, beta, h_saved, dO, dS_T=None, cu_seqlens=None, layout="KV", scale=None,
-             want_dS0=True, workspace=None, stream=None, prologue=0):
+             want_dS0=True, workspace=None, stream=None, prologue=0, save_wy=False):
     """Run gdr_bwd; returns (dq, dk, dv, dg, dbeta, dS0 or None).  h_saved's dtype selects h_dtype;
-    with prologue bits the gradients are w.r.t. the raw inputs."""
-    p = _problem_for(q, v, cu_seqlens, layout, scale, h_saved.dtype, prologue)
+    with prologue bits the gradients are w.r.t. the raw inputs; save_wy as given to forward()."""
+    p = _problem_for(q, v, cu_seqlens, layout, scale, h_saved.dtype, prologue, save_wy)
+    _check_saved(p, h_saved)
     dev = q.device
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dg = torch.empty_like(g)
@@ -290,11 +315,12 @@ def backward(q, k, v, g, beta, h_saved, dO, dS_T=None, cu_seqlens=None, layout="
 
 class _GDRFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype, prologue):
+    def forward(ctx, q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype, prologue, save_wy):
         o, S_T, h_saved = forward(q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype=h_dtype,
-                                  prologue=prologue)
+                                  prologue=prologue, save_wy=save_wy)
         ctx.save_for_backward(q, k, v, g, beta, h_saved, cu_seqlens)
         ctx.layout, ctx.scale, ctx.has_S0, ctx.prologue = layout, scale, S0 is not None, prologue
+        ctx.save_wy = save_wy
         return o, S_T
 
     @staticmethod
@@ -302,13 +328,17 @@ class _GDRFunction(torch.autograd.Function):
         q, k, v, g, beta, h_saved, cu_seqlens = ctx.saved_tensors
         dq, dk, dv, dg, dbeta, dS0 = backward(q, k, v, g, beta, h_saved, do.contiguous(),
                                               None if dS_T is None else dS_T.contiguous(), cu_seqlens,
-                                              ctx.layout, ctx.scale, want_dS0=ctx.has_S0, prologue=ctx.prologue)
-        return dq, dk, dv, dg, dbeta, dS0, None, None, None, None, None
+                                              ctx.layout, ctx.scale, want_dS0=ctx.has_S0, prologue=ctx.prologue,
+                                              save_wy=ctx.save_wy)
+        return dq, dk, dv, dg, dbeta, dS0, None, None, None, None, None, None
 
 
 def chunk_gated_delta_rule(q, k, v, g, beta, initial_state=None, cu_seqlens=None, layout="KV", scale=None,
-                           h_dtype=torch.float32, prologue=0):
+                           h_dtype=torch.float32, prologue=0, save_wy=True):
     """Autograd entry point: returns (o, final_state).  Tensors as in include/gdr.h; h_dtype is the
     dtype of the chunk-start states kept for the backward (bfloat16 halves their memory); prologue
-    (GDR_PROLOGUE_* bits) makes the operator normalise q, k and map raw gate / beta logits itself."""
-    return _GDRFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, layout, scale, h_dtype, prologue)
+    (GDR_PROLOGUE_* bits) makes the operator normalise q, k and map raw gate / beta logits itself;
+    save_wy (default) keeps the forward's chunk factors for the backward (49408 bytes per chunk and
+    v-head more saved memory, no recomputation in the backward; same results bit for bit)."""
+    return _GDRFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, layout, scale, h_dtype, prologue,
+                              save_wy)

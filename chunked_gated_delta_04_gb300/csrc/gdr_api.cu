@@ -51,6 +51,7 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
   if (p->layout != GDR_STATE_KV && p->layout != GDR_STATE_VK) return GDR_ERR_INVALID_ARG;
   if (p->h_dtype != GDR_DTYPE_F32 && p->h_dtype != GDR_DTYPE_BF16) return GDR_ERR_INVALID_ARG;
   if (p->prologue & ~7u) return GDR_ERR_INVALID_ARG;
+  if (p->save_wy != 0 && p->save_wy != 1) return GDR_ERR_INVALID_ARG;
   if (p->cu_seqlens != nullptr) {
     if (p->B != 1) return GDR_ERR_INVALID_ARG;
   } else if (p->num_seqs != p->B) {
@@ -82,6 +83,7 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
              tc_available())
                 ? 1
                 : 0;
+  d->save_wy = d->path == 1 ? p->save_wy : 0;
   return GDR_OK;
 }
 
@@ -104,16 +106,18 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
   w.chunks = (int4*)take(sizeof(int4) * (size_t)d.max_chunks);
   w.seq_chunk_off = (int*)take(sizeof(int) * ((size_t)d.num_seqs + 1));
   w.seq_order = (int*)take(sizeof(int) * ((size_t)d.num_seqs + 1));
-  w.gam = (float*)take(sizeof(float) * chH * kChunk);
-  w.W = take(el * chH * kChunk * d.DK);
-  w.U = take(el * chH * kChunk * d.DV);
+  if (!d.save_wy) {  // else in the saved buffer (attach_saved_factors)
+    w.gam = (float*)take(sizeof(float) * chH * kChunk);
+    w.W = take(el * chH * kChunk * d.DK);
+    w.U = take(el * chH * kChunk * d.DV);
+    if (d.path == 1) w.P = take(el * chH * kChunk * kChunk);
+  }
   if (d.path == 0) w.Vn = take(el * chH * kChunk * d.DV);
-  if (d.path == 1) w.P = take(el * chH * kChunk * kChunk);
   if (backward) {
     if (d.path == 0) w.Tm = (float*)take(sizeof(float) * chH * kChunk * kChunk);
     w.dhp = take(el * chH * d.DK * d.DV);
     if (d.path == 1) {
-      w.Tb = take(el * chH * kChunk * kChunk);
+      if (!d.save_wy) w.Tb = take(el * chH * kChunk * kChunk);
       w.dVn = take(el * chH * kChunk * d.DV);
     }
     if (fused_walk_grad(d)) {  // one region: flags then the claim counter (zeroed per call)
@@ -137,6 +141,39 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
   }
   if (ws) *ws = w;
   return off;
+}
+
+// Saved buffer: the chunk-start states, then (save_wy, tensor-core path only) per region,
+// 256-byte aligned: gamma fp32 [chunks][Hv][64], W bf16 [..][64][DK], U bf16 [..][64][DV],
+// P bf16 [..][64][64], T bf16 [..][64][64].
+static size_t saved_layout(const Dims& d, const char* base, Workspace* ws) {
+  const size_t chH = (size_t)d.max_chunks * d.Hv;
+  size_t off = align256(chH * d.DK * d.DV * (d.h_bf16 ? 2 : 4));
+  if (!d.save_wy) return off;
+  auto take = [&](size_t bytes) -> char* {
+    char* p = base ? const_cast<char*>(base) + off : nullptr;
+    off += align256(bytes);
+    return p;
+  };
+  float* gam = (float*)take(sizeof(float) * chH * kChunk);
+  void* W = take(2 * chH * kChunk * d.DK);
+  void* U = take(2 * chH * kChunk * d.DV);
+  void* P = take(2 * chH * kChunk * kChunk);
+  void* T = take(2 * chH * kChunk * kChunk);
+  if (ws) {
+    ws->gam = gam;
+    ws->W = W;
+    ws->U = U;
+    ws->P = P;
+    ws->Tb = T;
+  }
+  return off;
+}
+
+size_t saved_bytes(const Dims& d) { return saved_layout(d, nullptr, nullptr); }
+
+void attach_saved_factors(const Dims& d, const void* saved, Workspace* ws) {
+  if (d.save_wy) saved_layout(d, (const char*)saved, ws);
 }
 
 // With prologue bits set: runs the forward prologue and points the operator's q, k, g,
@@ -169,7 +206,8 @@ size_t gdr_max_chunks(const gdr_problem* p) {
 size_t gdr_saved_states_bytes(const gdr_problem* p) {
   Dims d;
   if (resolve(p, &d) != GDR_OK) return 0;
-  return (size_t)d.max_chunks * d.Hv * d.DK * d.DV * (d.h_bf16 ? 2 : 4);
+  if (!d.save_wy) return (size_t)d.max_chunks * d.Hv * d.DK * d.DV * (d.h_bf16 ? 2 : 4);
+  return saved_bytes(d);
 }
 
 size_t gdr_fwd_workspace_bytes(const gdr_problem* p) {
@@ -181,7 +219,7 @@ size_t gdr_fwd_workspace_bytes(const gdr_problem* p) {
 size_t gdr_bwd_workspace_bytes(const gdr_problem* p) {
   Dims d;
   if (resolve(p, &d) != GDR_OK) return 0;
-  if (d.path == 1 && !tc_bwd_available()) d.path = 0;
+  if (d.path == 1 && !tc_bwd_available()) d.path = d.save_wy = 0;
   return layout_workspace(d, true, nullptr, nullptr);
 }
 
@@ -206,6 +244,7 @@ gdr_status gdr_fwd(const gdr_problem* p, const void* q, const void* k, const voi
   Workspace ws;
   const size_t need = layout_workspace(d, false, (char*)workspace, &ws);
   if (workspace_bytes < need) return GDR_ERR_WORKSPACE;
+  attach_saved_factors(d, h_saved, &ws);
   cudaStream_t s = (cudaStream_t)stream;
   FwdArgs a{q, k, v, g, beta, S0, o, S_T, h_saved};
   stage_begin(s);
@@ -222,7 +261,7 @@ gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const voi
   Dims d;
   gdr_status st = resolve(p, &d);
   if (st != GDR_OK) return st;
-  if (d.path == 1 && !tc_bwd_available()) d.path = 0;
+  if (d.path == 1 && !tc_bwd_available()) d.path = d.save_wy = 0;
   const bool any_tokens = d.T_total > 0;
   if (any_tokens && (!q || !k || !v || !g || !beta || !h_saved || !dO || !dq || !dk || !dv || !dg || !dbeta))
     return GDR_ERR_INVALID_ARG;
@@ -234,6 +273,7 @@ gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const voi
   Workspace ws;
   const size_t need = layout_workspace(d, true, (char*)workspace, &ws);
   if (workspace_bytes < need) return GDR_ERR_WORKSPACE;
+  attach_saved_factors(d, h_saved, &ws);
   cudaStream_t s = (cudaStream_t)stream;
   BwdArgs a{q, k, v, g, beta, h_saved, dO, dS_T, dq, dk, dv, dg, dbeta, dS0};
   stage_begin(s);

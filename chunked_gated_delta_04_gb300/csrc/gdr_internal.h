@@ -33,6 +33,7 @@ struct Dims {
   int path;    // 1 = tcgen05, 0 = SIMT
   int h_bf16;  // h_saved holds bf16 (else fp32)
   int prologue;  // gdr_prologue_flags bits
+  int save_wy;   // tensor-core path: gamma, W, U, P, T live in the saved buffer (see attach_saved_factors)
 };
 
 // Pointers into the caller's workspace.  Every region starts 256-byte aligned.
@@ -72,6 +73,11 @@ gdr_status resolve_problem(const gdr_problem* p, Dims* d);
 
 // Computes the workspace layout; with base == nullptr only the size is returned.
 size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws);
+
+// Bytes of the saved buffer (states, then the saved factors when d.save_wy).
+size_t saved_bytes(const Dims& d);
+// With d.save_wy: points ws->gam, W, U, P, Tb at the factor regions of the saved buffer.
+void attach_saved_factors(const Dims& d, const void* saved, Workspace* ws);
 
 struct FwdArgs {
   const void *q, *k, *v;

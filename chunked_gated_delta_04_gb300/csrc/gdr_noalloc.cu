@@ -77,6 +77,7 @@ extern "C" gdr_status gdr_fwd_noalloc(const gdr_problem* p, const void* q, const
   if (scratch_address(&scratch) != cudaSuccess) return GDR_ERR_CUDA;
   Workspace ws;
   layout_workspace(d, false, (char*)scratch, &ws);
+  attach_saved_factors(d, h_saved, &ws);
   cudaStream_t s = (cudaStream_t)stream;
   FwdArgs a{q, k, v, g, beta, S0, o, S_T, h_saved};
   stage_begin(s);

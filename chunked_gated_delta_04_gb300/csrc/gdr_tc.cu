@@ -723,7 +723,7 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
   if (!get_encoder()) return cudaErrorNotSupported;
   // Maps are built only when there are tokens; with none, no kernel reads them (every
   // chunk slot is empty and the state kernel only copies S0 to S_T).
-  CUtensorMap tq{}, tk{}, tv{}, tw{}, tu{}, tp{}, ths{};
+  CUtensorMap tq{}, tk{}, tv{}, tw{}, tu{}, tp{}, ths{}, tt{};
   const uint64_t Tt = (uint64_t)d.T_total;
   const uint64_t rows = (uint64_t)d.max_chunks * d.Hv * 64;
   if (Tt == 0 && d.num_seqs == 0) return cudaSuccess;
@@ -734,12 +734,14 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
         !(d.h_bf16 ? map_2d_sw64(&ths, a.h_saved, 128, rows * 2, 128)
                    : map_2d_box(&ths, a.h_saved, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, rows * 2, 32, 128)))
       return cudaErrorInvalidValue;
+    // saved factors: T is kept for the backward too
+    if (d.save_wy && !map_2d(&tt, ws.Tb, 64, rows)) return cudaErrorInvalidValue;
   }
   if (d.max_chunks > 0 && Tt > 0) {
     const size_t smp = PrepSmem::BYTES + 1024;
     cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
-    tc_prep_kernel<<<prep_grid(d), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, tp, d, a.g,
-                                                                      (const bf16*)a.beta, ws, 0);
+    tc_prep_kernel<<<prep_grid(d), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, d.save_wy ? tt : tp, d, a.g,
+                                                                      (const bf16*)a.beta, ws, d.save_wy);
     stage_mark(s, "fwd_prep");
   }
   if (d.num_seqs > 0) {

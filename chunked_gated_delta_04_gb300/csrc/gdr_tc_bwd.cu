@@ -1046,7 +1046,8 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
   const uint64_t Tt = (uint64_t)d.T_total;
   const uint64_t rows = (uint64_t)d.max_chunks * d.Hv * 64;
   if (Tt == 0 && d.num_seqs == 0) return cudaSuccess;
-  cudaError_t e = tc_launch_prep(d, a.q, a.k, a.v, a.g, a.beta, ws, 1, s, "bwd_prep");
+  // the chunk factors: recomputed, or (save_wy) kept by the forward in the saved buffer
+  cudaError_t e = d.save_wy ? cudaSuccess : tc_launch_prep(d, a.q, a.k, a.v, a.g, a.beta, ws, 1, s, "bwd_prep");
   if (e != cudaSuccess) return e;
   CUtensorMap tq{}, tk{}, tv{}, tdo{}, tw{}, tp{}, tdvn{}, tdh{}, tt{}, tdhs{}, tu{}, tdq{}, tdk{}, tdv{}, thf{};
   if (Tt > 0) {  // with no tokens no kernel reads the maps (see tc_forward)

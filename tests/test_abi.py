@@ -58,6 +58,18 @@ def test_size_queries(lib):
     # the fused prologue keeps its mapped inputs in the workspace
     assert gdr.gdr_fwd_workspace_bytes(prob(prologue=7)) > gdr.gdr_fwd_workspace_bytes(p)
     assert gdr.gdr_bwd_workspace_bytes(prob(prologue=1)) > gdr.gdr_bwd_workspace_bytes(p)
+    # saved factors: on the tensor-core path 49408 bytes per (chunk, v-head) move from the
+    # workspaces into the saved buffer; elsewhere the option changes nothing
+    assert gdr.gdr_saved_states_bytes(prob(save_wy=True)) == gdr.gdr_saved_states_bytes(p)  # SIMT shape
+    pt, pts = prob(DK=128, DV=128), prob(DK=128, DV=128, save_wy=True)
+    chH = 6 * 4
+    if gdr.gdr_path(pt) == 1:
+        assert gdr.gdr_saved_states_bytes(pts) == gdr.gdr_saved_states_bytes(pt) + chH * 49408
+        assert gdr.gdr_fwd_workspace_bytes(pts) < gdr.gdr_fwd_workspace_bytes(pt)
+        assert gdr.gdr_bwd_workspace_bytes(pts) < gdr.gdr_bwd_workspace_bytes(pt)
+    else:
+        assert gdr.gdr_saved_states_bytes(pts) == gdr.gdr_saved_states_bytes(pt)
+        assert gdr.gdr_fwd_workspace_bytes(pts) == gdr.gdr_fwd_workspace_bytes(pt)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -69,6 +81,7 @@ def test_size_queries(lib):
     (dict(T=-1), gdr.GDR_ERR_INVALID_ARG),
     (dict(h_dtype=torch.float16), gdr.GDR_ERR_INVALID_ARG),  # h_saved is fp32 or bf16
     (dict(prologue=8), gdr.GDR_ERR_INVALID_ARG),              # unknown prologue bit
+    (dict(save_wy=2), gdr.GDR_ERR_INVALID_ARG),               # save_wy is 0 or 1
 ])
 def test_bad_problems_are_rejected(lib, kw, code):
     p = prob(**kw)

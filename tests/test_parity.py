@@ -11,8 +11,10 @@ import numpy as np
 import pytest
 import torch
 
+import chunked_gated_delta_04_gb300 as gdr
 from chunked_gated_delta_04_gb300.inputs import WORKLOADS, make_inputs, small_workload
-from gdr_testlib import compare, head_slice, reference, run_gpu, slice_result, tol_for
+from gdr_testlib import (OUT_KEYS_BWD, OUT_KEYS_FWD, compare, head_slice, reference, run_gpu, slice_result,
+                         to_device, tol_for)
 
 pytestmark = pytest.mark.gpu
 
@@ -186,6 +188,47 @@ def test_bf16_saved_states_match_oracle(case):
     torch.cuda.synchronize()
     assert res["h_saved"].dtype == torch.bfloat16
     compare(res, reference(inp), 2e-2)
+
+
+SAVE_WY_CASES = [
+    # name, B, T, Hk, Hv, layout, seqlens, h_dtype, prologue
+    ("fused_b2_t300_vk", 2, 300, 2, 2, "VK", None, torch.float32, 0),        # fused walk + grad
+    ("pair_varlen", 1, None, 1, 2, "KV", [0, 1, 64, 77, 200], torch.float32, 0),  # Hv = 2 Hk clusters
+    ("group4_t130", 1, 130, 1, 4, "KV", None, torch.bfloat16, 0),            # group partials
+    ("fused_prologue", 2, 193, 2, 2, "KV", None, torch.float32, 7),          # raw inputs
+]
+
+
+@pytest.mark.parametrize("case", SAVE_WY_CASES, ids=[c[0] for c in SAVE_WY_CASES])
+def test_saved_factors_give_identical_results(case):
+    """save_wy only moves where the chunk factors come from (kept by the forward instead of
+    recomputed by the backward, by the same kernel on the same inputs): every output is bitwise
+    the same as without it, and the oracle agrees."""
+    name, B, T, Hk, Hv, layout, lens, h_dtype, pro = case
+    if lens is None:
+        w = small_workload(name, torch.bfloat16, B, T, Hk, Hv, 128, 128, layout)
+    else:
+        w = small_workload(name, torch.bfloat16, Hk=Hk, Hv=Hv, DK=128, DV=128, seqlens=lens, layout=layout)
+    inp = make_inputs(w, raw=bool(pro))
+    base = run_gpu(inp, h_dtype=h_dtype, prologue=pro)
+    res = run_gpu(inp, h_dtype=h_dtype, prologue=pro, save_wy=True)
+    torch.cuda.synchronize()
+    n_chunks = sum(-(-L // 64) for L in inp["seqlens"])  # slots past the real chunks stay unwritten
+    for key in OUT_KEYS_FWD + OUT_KEYS_BWD:
+        if base.get(key) is not None:
+            a, b = (base[key], res[key]) if key != "h_saved" else (base[key][:n_chunks], res[key][:n_chunks])
+            assert torch.equal(a, b), key
+    compare(res, reference(inp, prologue=pro), 2e-2)
+
+
+def test_saved_factors_need_the_larger_buffer():
+    w = small_workload("wyb", torch.bfloat16, 1, 130, 1, 1, 128, 128)
+    inp = make_inputs(w)
+    d = to_device(inp)
+    _, _, hs = gdr.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], None, "KV")
+    with pytest.raises(ValueError):  # a states-only buffer cannot hold the factors
+        gdr.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], hs, d["dO"], d["dS_T"], None, "KV",
+                     save_wy=True)
 
 
 def test_bf16_saved_states_leave_tensor_core_forward_unchanged():
