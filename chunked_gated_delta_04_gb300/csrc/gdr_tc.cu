@@ -438,16 +438,23 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
 // ---------------------------------------------------------------------------------
 constexpr int kStateSlices = 4;  // DV = 128 as four 32-column slices
 
+// kSingle = false: two stages of the chunk tiles, so all of chunk c + 1's tiles load while
+// chunk c runs (~161 KB, one CTA per SM).  kSingle = true: one buffer per tile, each refilled
+// for the next chunk as soon as its last reader is done ([W|Q] and gamma after the first
+// product, U after the Vn epilogue, K and P once the previous chunk's P Vn has run): ~97 KB,
+// two CTAs per SM, for grids larger than the SM count.  A chain is ~20 % slower single-buffered.
+template <bool kSingle>
 struct StateSmem {
+  static constexpr uint32_t NST = kSingle ? 1 : 2;
   // per stage: [W|Q] x 2 slabs (32 KB), K 2 slabs (16 KB), [U | P] (16 KB)
   static constexpr uint32_t STAGE = 65536;
   static constexpr uint32_t WQ = 0, K = 32768, U = 49152, P = 57344;
-  static constexpr uint32_t HT = 2 * STAGE;       // h^T slice (bf16, K-major B operand): 2 slabs of 32 rows
+  static constexpr uint32_t HT = NST * STAGE;     // h^T slice (bf16, K-major B operand): 2 slabs of 32 rows
   static constexpr uint32_t VNT = HT + 8192;      // Vn^T slice: 32 rows x 64 tokens (4 KB)
   static constexpr uint32_t VTT = VNT + 4096;     // (e^{gamma_C - gamma} Vn)^T slice (4 KB)
   static constexpr uint32_t HS = VTT + 4096;      // h slice staged for the h_saved store: fp32 (16 KB) or bf16 (8 KB)
-  static constexpr uint32_t GAM = HS + 16384;     // gamma of each stage: 2 x 256 B
-  static constexpr uint32_t BYTES = GAM + 512;
+  static constexpr uint32_t GAM = HS + 16384;     // gamma of each stage: 256 B each
+  static constexpr uint32_t BYTES = GAM + NST * 256;
 };
 
 // 32 fp32 -> 32 bf16 in global memory (64 bytes, 16-byte aligned).
@@ -493,6 +500,7 @@ __device__ __forceinline__ void st_row_bf16x32_sw64(unsigned char* tile, int row
   for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(tile + row * 64 + ((c ^ sw) << 4)) = w[c];
 }
 
+template <bool kSingle>
 __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
@@ -500,7 +508,10 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     const float* __restrict__ S0, float* __restrict__ S_T, bf16* __restrict__ o, Workspace ws) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
-  __shared__ uint64_t bar_load[2], bar_mma, bar_pv;
+  using SS = StateSmem<kSingle>;
+  // two stages: bar_load[st] per stage; single buffers: bar_load[0] = [W|Q] and gamma,
+  // bar_load[1] = U, bar_kp = K and P (one phase per chunk each)
+  __shared__ uint64_t bar_load[2], bar_kp, bar_mma, bar_pv;
   __shared__ uint32_t tmem_slot;
   // block -> (sequence in longest-first order, v-head, DV slice); the slices of one
   // (sequence, head) are adjacent so they share its W/Q/K tiles in L2
@@ -519,6 +530,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
   if (tid == 0) {
     tc::mbar_init(&bar_load[0], 1);
     tc::mbar_init(&bar_load[1], 1);
+    tc::mbar_init(&bar_kp, 1);
     tc::mbar_init(&bar_mma, 1);
     tc::mbar_init(&bar_pv, 1);
     tc::fence_barrier_init();
@@ -539,29 +551,60 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     for (int b = 0; b < 32; ++b)
       h[b] = S0 ? S0[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] : 0.f;
   }
-  auto issue_loads = [&](int c, int st) {
+  auto issue_loads = [&](int c, int st) {  // two stages: every tile of chunk c
     const int tc0 = t_seq + (c - c_begin) * 64;
     const size_t chh = (size_t)c * Hv + j;
-    unsigned char* base = sm + st * StateSmem::STAGE;
+    unsigned char* base = sm + st * SS::STAGE;
     tc::mbar_arrive_expect_tx(&bar_load[st], 8 * kSlab + 256);
-    tc::bulk_load(sm + StateSmem::GAM + st * 256, ws.gam + chh * 64, 256, &bar_load[st]);
-    tc::tma_load_2d(base + StateSmem::WQ, &tm_w, &bar_load[st], 0, (int)(chh * 64));
-    tc::tma_load_2d(base + StateSmem::WQ + 2 * kSlab, &tm_w, &bar_load[st], 64, (int)(chh * 64));
-    tc::tma_load_3d(base + StateSmem::WQ + kSlab, &tm_q, &bar_load[st], 0, i, tc0);
-    tc::tma_load_3d(base + StateSmem::WQ + 3 * kSlab, &tm_q, &bar_load[st], 64, i, tc0);
-    tc::tma_load_3d(base + StateSmem::K, &tm_k, &bar_load[st], 0, i, tc0);
-    tc::tma_load_3d(base + StateSmem::K + kSlab, &tm_k, &bar_load[st], 64, i, tc0);
-    tc::tma_load_2d(base + StateSmem::U, &tm_u, &bar_load[st], dv0 & 64, (int)(chh * 64));  // 64-col tile
-    tc::tma_load_2d(base + StateSmem::P, &tm_p, &bar_load[st], 0, (int)(chh * 64));
+    tc::bulk_load(sm + SS::GAM + st * 256, ws.gam + chh * 64, 256, &bar_load[st]);
+    tc::tma_load_2d(base + SS::WQ, &tm_w, &bar_load[st], 0, (int)(chh * 64));
+    tc::tma_load_2d(base + SS::WQ + 2 * kSlab, &tm_w, &bar_load[st], 64, (int)(chh * 64));
+    tc::tma_load_3d(base + SS::WQ + kSlab, &tm_q, &bar_load[st], 0, i, tc0);
+    tc::tma_load_3d(base + SS::WQ + 3 * kSlab, &tm_q, &bar_load[st], 64, i, tc0);
+    tc::tma_load_3d(base + SS::K, &tm_k, &bar_load[st], 0, i, tc0);
+    tc::tma_load_3d(base + SS::K + kSlab, &tm_k, &bar_load[st], 64, i, tc0);
+    tc::tma_load_2d(base + SS::U, &tm_u, &bar_load[st], dv0 & 64, (int)(chh * 64));  // 64-col tile
+    tc::tma_load_2d(base + SS::P, &tm_p, &bar_load[st], 0, (int)(chh * 64));
   };
-  if (tid == kCopyTid && c_begin < c_end) issue_loads(c_begin, 0);
-  st_col32_bf16(sm + StateSmem::HT, tid, h);
+  auto load_wq = [&](int c) {  // single buffers: [W|Q] and gamma of chunk c
+    const int tc0 = t_seq + (c - c_begin) * 64;
+    const size_t chh = (size_t)c * Hv + j;
+    tc::mbar_arrive_expect_tx(&bar_load[0], 4 * kSlab + 256);
+    tc::bulk_load(sm + SS::GAM, ws.gam + chh * 64, 256, &bar_load[0]);
+    tc::tma_load_2d(sm + SS::WQ, &tm_w, &bar_load[0], 0, (int)(chh * 64));
+    tc::tma_load_2d(sm + SS::WQ + 2 * kSlab, &tm_w, &bar_load[0], 64, (int)(chh * 64));
+    tc::tma_load_3d(sm + SS::WQ + kSlab, &tm_q, &bar_load[0], 0, i, tc0);
+    tc::tma_load_3d(sm + SS::WQ + 3 * kSlab, &tm_q, &bar_load[0], 64, i, tc0);
+  };
+  auto load_u = [&](int c) {  // single buffers: U of chunk c
+    const size_t chh = (size_t)c * Hv + j;
+    tc::mbar_arrive_expect_tx(&bar_load[1], kSlab);
+    tc::tma_load_2d(sm + SS::U, &tm_u, &bar_load[1], dv0 & 64, (int)(chh * 64));
+  };
+  auto load_kp = [&](int c) {  // single buffers: K and P of chunk c
+    const int tc0 = t_seq + (c - c_begin) * 64;
+    const size_t chh = (size_t)c * Hv + j;
+    tc::mbar_arrive_expect_tx(&bar_kp, 3 * kSlab);
+    tc::tma_load_3d(sm + SS::K, &tm_k, &bar_kp, 0, i, tc0);
+    tc::tma_load_3d(sm + SS::K + kSlab, &tm_k, &bar_kp, 64, i, tc0);
+    tc::tma_load_2d(sm + SS::P, &tm_p, &bar_kp, 0, (int)(chh * 64));
+  };
+  if (tid == kCopyTid && c_begin < c_end) {
+    if (kSingle) {
+      load_wq(c_begin);
+      load_u(c_begin);
+      load_kp(c_begin);
+    } else {
+      issue_loads(c_begin, 0);
+    }
+  }
+  st_col32_bf16(sm + SS::HT, tid, h);
 
   bool ok = true;
   uint32_t mma_phase = 0;
   GDR_TRACE_INIT();
-  const uint32_t s_ht = tc::smem_u32(sm + StateSmem::HT), s_vnt = tc::smem_u32(sm + StateSmem::VNT);
-  const uint32_t s_vtt = tc::smem_u32(sm + StateSmem::VTT);
+  const uint32_t s_ht = tc::smem_u32(sm + SS::HT), s_vnt = tc::smem_u32(sm + SS::VNT);
+  const uint32_t s_vtt = tc::smem_u32(sm + SS::VTT);
   const int r = tid & 63;
   // output rows of the previous chunk, finished during this chunk's first product
   // (warps 2-3: row r = tid - 64): (Q h)[r] slice, e^{gamma_r}, chunk start and length
@@ -580,8 +623,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     }
   };
   for (int c = c_begin; c < c_end && ok; ++c) {
-    const int it = c - c_begin, st = it & 1;
-    const uint32_t ld_phase = (it >> 1) & 1;
+    const int it = c - c_begin, st = kSingle ? 0 : it & 1;
+    const uint32_t ld_phase = kSingle ? it & 1 : (it >> 1) & 1;  // phase of this chunk's tile barriers
     const int t0 = t_seq + it * 64;
     const int len = min(64, L - it * 64);
     const size_t chh = (size_t)c * Hv + j;
@@ -592,12 +635,12 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     GDR_TRACE_MARK(1, 0);
     ok = __syncthreads_and(tc::mbar_wait(&bar_load[st], ld_phase, ws.status, kDevErrTimeoutFwd));
     GDR_TRACE_MARK(1, 1);
-    const float* sgam = reinterpret_cast<const float*>(sm + StateSmem::GAM + st * 256);
+    const float* sgam = reinterpret_cast<const float*>(sm + SS::GAM + st * 256);
     const float gC = sgam[len - 1];
     const float gr = sgam[r];
-    unsigned char* stg = sm + st * StateSmem::STAGE;
-    const uint32_t s_wq = tc::smem_u32(stg + StateSmem::WQ), s_k = tc::smem_u32(stg + StateSmem::K);
-    const uint32_t s_up = tc::smem_u32(stg + StateSmem::U);
+    unsigned char* stg = sm + st * SS::STAGE;
+    const uint32_t s_wq = tc::smem_u32(stg + SS::WQ), s_k = tc::smem_u32(stg + SS::K);
+    const uint32_t s_up = tc::smem_u32(stg + SS::U);
     if (ok && tid == 0) {
       tc::tc_fence_after();
       const uint32_t id = tc::idesc_bf16(128, 32, 0, 0);
@@ -607,14 +650,19 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
       tc::mma_commit(&bar_mma);
     }
     GDR_TRACE_MARK(1, 7);
-    if (tid == kCopyTid && c + 1 < c_end) issue_loads(c + 1, st ^ 1);  // overlaps the MMA
+    if (!kSingle && tid == kCopyTid && c + 1 < c_end) issue_loads(c + 1, st ^ 1);  // overlaps the MMA
+    // single buffers: this chunk's K and P, once the previous chunk's P Vn (their last
+    // reader) has run
+    if (kSingle && ok && tid == kCopyTid && it > 0 &&
+        tc::mbar_wait(&bar_pv, (it - 1) & 1, ws.status, kDevErrTimeoutFwd))
+      load_kp(c);
     GDR_TRACE_MARK(1, 8);
     // while [W;Q] h runs: stage the chunk-start state (fp32) for its h_saved store, and
     // finish the previous chunk's output rows (P Vn is still in TMEM)
     if (d.h_bf16)  // bf16 saved states: a 64-byte-swizzled [128][32] bf16 tile
-      st_row_bf16x32_sw64(sm + StateSmem::HS, tid, h);
+      st_row_bf16x32_sw64(sm + SS::HS, tid, h);
     else
-      st_row_f32x32(sm + StateSmem::HS, tid, h);
+      st_row_f32x32(sm + SS::HS, tid, h);
     if (ok && warp >= 2 && it > 0) finish_o((it - 1) & 1);
     tc::fence_proxy_async_smem();
     GDR_TRACE_MARK(1, 6);
@@ -622,22 +670,25 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     mma_phase ^= 1;
     tc::tc_fence_after();
     if (ok && tid == kCopyTid) {  // h_saved[chunk] rows 0..127, columns dv0..dv0+31
-      tc::tma_store_2d(&tm_hs, sm + StateSmem::HS, dv0, (int)(chh * 128));
+      tc::tma_store_2d(&tm_hs, sm + SS::HS, dv0, (int)(chh * 128));
       tc::bulk_commit();
+      if (kSingle && c + 1 < c_end) load_wq(c + 1);  // [W|Q] and gamma were last read by [W;Q] h
     }
     GDR_TRACE_MARK(1, 2);
     if (ok) {
       if (warp < 2) {  // Vn = U - W h (rows >= len are zero: W and U are zero there)
         float x[32], u[32];
+        const bool uok = !kSingle || __all_sync(0xffffffffu, tc::mbar_wait(&bar_load[1], ld_phase, ws.status,
+                                                                            kDevErrTimeoutFwd));
         tmem_ld32w(tbase, warp, 0, x);
-        ld_halfrow_bf16(stg + StateSmem::U, r, (dv0 >> 5) & 1, u);
+        if (uok) ld_halfrow_bf16(stg + SS::U, r, (dv0 >> 5) & 1, u);
 #pragma unroll
-        for (int b = 0; b < 32; ++b) u[b] -= x[b];
-        st_col32_bf16(sm + StateSmem::VNT, r, u);
+        for (int b = 0; b < 32; ++b) u[b] = uok ? u[b] - x[b] : 0.f;
+        st_col32_bf16(sm + SS::VNT, r, u);
         const float dec = fexp(gC - gr);
 #pragma unroll
         for (int b = 0; b < 32; ++b) u[b] *= dec;
-        st_col32_bf16(sm + StateSmem::VTT, r, u);
+        st_col32_bf16(sm + SS::VTT, r, u);
       } else {  // keep (Q h)[r] for the output rows
         tmem_ld32w(tbase, warp, 0, xq);
         p_eg = fexp(gr);
@@ -649,7 +700,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     tc::tc_fence_before();
     __syncthreads();
     GDR_TRACE_MARK(1, 3);
-    if (ok && tid == 0) {
+    if (kSingle && ok && tid == kCopyTid && c + 1 < c_end) load_u(c + 1);  // U was last read just above
+    if (ok && tid == 0 && (!kSingle || tc::mbar_wait(&bar_kp, ld_phase, ws.status, kDevErrTimeoutFwd))) {
       tc::tc_fence_after();
       const uint32_t id = tc::idesc_bf16(128, 32, 0, 0);
       const uint32_t idt = tc::idesc_bf16(128, 32, 1, 0);
@@ -676,7 +728,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
       const float eC = fexp(gC);
 #pragma unroll
       for (int b = 0; b < 32; ++b) h[b] = eC * h[b] + y[b];
-      st_col32_bf16(sm + StateSmem::HT, tid, h);
+      st_col32_bf16(sm + SS::HT, tid, h);
     }
     if (tid == kCopyTid) tc::bulk_wait_read<0>();  // h staging free for the next chunk
     GDR_TRACE_MARK(1, 5);
@@ -745,10 +797,16 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
     stage_mark(s, "fwd_prep");
   }
   if (d.num_seqs > 0) {
-    const size_t sms = StateSmem::BYTES + 1024;
-    cudaFuncSetAttribute(tc_fwd_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
-    tc_fwd_state_kernel<<<d.num_seqs * d.Hv * kStateSlices, kTcThreads, sms, s>>>(tq, tk, tw, tu, tp, ths, d, a.S0,
-                                                                                 a.S_T, (bf16*)a.o, ws);
+    // more CTAs than SMs: the single-buffered variant, two CTAs per SM, so they all run at once
+    int dev = 0, n_sm = 1;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    const long long n_cta = (long long)d.num_seqs * d.Hv * kStateSlices;
+    const bool single = n_cta > n_sm;
+    const size_t sms = (single ? StateSmem<true>::BYTES : StateSmem<false>::BYTES) + 1024;
+    auto kern = single ? tc_fwd_state_kernel<true> : tc_fwd_state_kernel<false>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
+    kern<<<(unsigned)n_cta, kTcThreads, sms, s>>>(tq, tk, tw, tu, tp, ths, d, a.S0, a.S_T, (bf16*)a.o, ws);
     stage_mark(s, "fwd_state");
   }
   return cudaGetLastError();

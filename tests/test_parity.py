@@ -44,6 +44,9 @@ SMALL = [
     ("bf16_t300_b2", torch.bfloat16, 2, 300, 2, 2, 128, "VK", True, True),
     ("bf16_gva", torch.bfloat16, 1, 192, 1, 2, 128, "KV", False, False),
     ("bf16_d64", torch.bfloat16, 1, 100, 1, 1, 64, "KV", True, True),
+    # more state CTAs (sequences x v-heads x 4) than SMs: the single-buffered state kernel
+    ("bf16_many_ctas", torch.bfloat16, 3, 200, 13, 13, 128, "KV", True, True),
+    ("bf16_many_ctas_gva", torch.bfloat16, 1, 200, 10, 40, 128, "VK", True, False),
 ]
 
 
