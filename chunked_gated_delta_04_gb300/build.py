@@ -38,25 +38,36 @@ def _deps():
         os.path.join(INCLUDE, "gdr.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+FLAGS_STAMP = LIB + ".flags"  # the flags the library was built with (a rebuild when they change)
+
+
+def _flags(debug: bool = False) -> list:
+    flags = GENCODE + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+                       "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
+    if debug:
+        flags += ["-DGDR_DEBUG_DELAY=1"]
+    return flags + os.environ.get("GDR_NVCC_EXTRA", "").split()
+
+
+def up_to_date(debug: bool = False) -> bool:
+    if not os.path.exists(LIB) or not os.path.exists(FLAGS_STAMP):
         return False
+    with open(FLAGS_STAMP) as f:
+        if f.read() != " ".join(_flags(debug)):
+            return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
 def build(force: bool = False, debug: bool = False, verbose: bool = False) -> str:
-    if not force and not debug and up_to_date():
+    if not force and up_to_date(debug):
         return LIB
     nvcc = nvcc_path()
     os.makedirs(BUILD_DIR, exist_ok=True)
-    flags = GENCODE + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
-                       "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
-    if debug:
-        flags += ["-DGDR_DEBUG_DELAY=1"]
-    flags += os.environ.get("GDR_NVCC_EXTRA", "").split()
+    flags = _flags(debug)
+    stamp = " ".join(flags)
     if verbose:
-        flags += ["-Xptxas", "-v"]
+        flags = flags + ["-Xptxas", "-v"]
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
@@ -79,6 +90,8 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(FLAGS_STAMP, "w") as f:
+        f.write(stamp)
     return LIB
 
 

@@ -124,6 +124,7 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
       w.walk_flags = (uint32_t*)take(sizeof(uint32_t) * ((size_t)d.max_chunks * d.Hv + 64));
       w.grad_queue = w.walk_flags ? w.walk_flags + (size_t)d.max_chunks * d.Hv : nullptr;
       w.step_off = (int*)take(sizeof(int) * ((size_t)d.max_chunks + 2));
+      w.grad_chunk = (int*)take(sizeof(int) * ((size_t)d.max_chunks + 1));
     }
     if (d.G > 1 && !grad_pair_mode(d)) {
       w.dq_part = (float*)take(sizeof(float) * (size_t)d.T_total * d.Hv * d.DK);

@@ -21,7 +21,8 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
                                                                   int* __restrict__ off,
                                                                   int* __restrict__ order,
                                                                   uint32_t* __restrict__ status,
-                                                                  int* __restrict__ step_off) {
+                                                                  int* __restrict__ step_off,
+                                                                  int* __restrict__ grad_chunk) {
   __shared__ int warp_tot[32];
   __shared__ int s_bad;
   __shared__ int s_carry;
@@ -123,7 +124,8 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
   // nc(n) > s, i.e. of the first cnt(s) sequences in longest-first order.  step_off[s] =
   // sum_{s' < s} cnt(s') for s = 0..S (S = the longest sequence's chunk count), and
   // step_off[max_chunks + 1] = S.  Gradient item q * Hv + j with step_off[s] <= q <
-  // step_off[s + 1] is v-head j of sequence order[q - step_off[s]] at step s.
+  // step_off[s + 1] is v-head j of sequence order[q - step_off[s]] at step s, whose chunk
+  // grad_chunk[q] lists.
   if (step_off != nullptr && bad) {  // nothing is computed: no walk steps, no gradient items
     if (tid == 0) step_off[0] = step_off[max_chunks + 1] = 0;
   } else if (step_off != nullptr) {
@@ -172,13 +174,23 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
       if (tid == kIndexThreads - 1) s_carry = carry + incl;
       __syncthreads();
     }
+    // the chunk of every queue position, so the gradient role decodes an item with one load
+    const int n_q = step_off[S];
+    for (int q = tid; q < n_q; q += kIndexThreads) {
+      int lo = 0, hi = S - 1;  // last step s with step_off[s] <= q
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (step_off[mid] <= q) lo = mid; else hi = mid - 1;
+      }
+      grad_chunk[q] = off[order[q - step_off[lo]] + 1] - 1 - lo;
+    }
   }
 }
 
 cudaError_t launch_index(const Dims& d, const Workspace& ws, cudaStream_t s) {
   gdr_index_kernel<<<1, kIndexThreads, 0, s>>>(d.cu, d.num_seqs, d.cu ? (int)d.T_total : d.T,
                                                d.max_chunks, ws.chunks, ws.seq_chunk_off, ws.seq_order,
-                                               ws.status, ws.step_off);
+                                               ws.status, ws.step_off, ws.grad_chunk);
   stage_mark(s, "index");
   return cudaGetLastError();
 }

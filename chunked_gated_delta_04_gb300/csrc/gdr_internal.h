@@ -60,6 +60,7 @@ struct Workspace {
   uint32_t* walk_flags;
   uint32_t* grad_queue;
   int* step_off;  // [max_chunks + 2]: the walk-step prefix table built by the index kernel
+  int* grad_chunk;  // [max_chunks]: chunk of queue position q (gradient items q * Hv + v-head)
   // fused prologue outputs (input dtype unless noted): normalised q, k [T_total][Hk][DK],
   // g = logsigmoid(a) fp32 [T_total][Hv], beta = sigmoid(b) [T_total][Hv]
   void* qn;

@@ -352,7 +352,10 @@ __device__ __forceinline__ void grad_body(
   __shared__ uint64_t bar_tma, bar_tma2, bar_mma;
   __shared__ uint64_t bar_qfree, bar_qdata, bar_kfree, bar_kdata;  // pair exchange (kPair)
   __shared__ int s_claim, s_claim_c;                               // kDyn: the next item, its chunk
-  __shared__ float s_beta[64], s_eg[64], s_dgam[64], s_colpp[64], s_colbk[64], s_colaa[64], s_red[8];
+  __shared__ float s_beta[64], s_eg[64], s_dgam[64], s_red[8];
+  // column sums of 64 x 64 fp32 products in scratch, as four partial sums over 16 rows each
+  // (all 256 threads: column tid & 63, rows 16 (tid >> 6) ..), added where they are used
+  __shared__ float s_colpp[4][64], s_colbk[4][64], s_colaa[4][64];
   // per-row partial sums of the two column halves: [half][row]
   __shared__ float s_qh[2][64], s_rowpp[2][64], s_kdv[2][64], s_dbv[2][64], s_akk[2][64], s_rowaa[2][64];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -398,19 +401,10 @@ __device__ __forceinline__ void grad_body(
   const int n_items = kDyn ? ws.step_off[n_steps] * Hv : (kPair ? d.max_chunks * d.Hk : d.max_chunks * Hv);
   const int item0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int istep = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  // kDyn: item w = q * Hv + v-head with step_off[s] <= q < step_off[s + 1]: sequence
-  // order[q - step_off[s]], its chunk finished at reverse step s
+  // kDyn: item w = q * Hv + v-head, queue position q in walk order (the index kernel lists
+  // each position's chunk)
   auto chunk_of = [&](int w) {
-    if (kDyn) {
-      const int q = w / Hv;
-      int lo = 0, hi = n_steps - 1;  // last s with step_off[s] <= q
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (ws.step_off[mid] <= q) lo = mid; else hi = mid - 1;
-      }
-      const int n = ws.seq_order[q - ws.step_off[lo]];
-      return ws.seq_chunk_off[n + 1] - 1 - lo;
-    }
+    if (kDyn) return ws.grad_chunk[w / Hv];
     return kPair ? w / d.Hk : w / Hv;
   };
   auto vhead_of = [&](int w) { return kPair ? (w % d.Hk) * 2 + (int)rank : w % Hv; };
@@ -428,7 +422,9 @@ __device__ __forceinline__ void grad_body(
     if (groups & kLdDhDvn) {  // the first group of an item sets the whole item's byte count
       // kDyn: dh' and dVn of this chunk come from the walk running in the same kernel; on a
       // timeout the loads are left out and the item's own bounded wait ends the walk
+      GDR_TRACE_CLK(tw0);
       if (kDyn && !wait_flag(ws.walk_flags + ch2, 2u, ws.status, kDevErrTimeoutBwd)) return;
+      GDR_TRACE_SINCE(2, 20, tw0);
       tc::mbar_arrive_expect_tx(bar, (d.h_bf16 ? 20 : 24) * kSlab + 256);
       for (int q4 = 0; q4 < 4; ++q4)  // dh' rows (q4 & 1) * 64.., columns (q4 >> 1) * 64..
         tc::tma_load_2d(sm + S::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
@@ -508,13 +504,16 @@ __device__ __forceinline__ void grad_body(
     }
     return (bool)__syncthreads_and(okin && okw);
   };
-  // kDyn: the copy thread claims an item and decodes its chunk (a search of the step table)
-  // once; the other threads read both from shared memory after a barrier
+  // kDyn: the copy thread claims an item and decodes its chunk once; the other threads read
+  // both from shared memory after a barrier.  Inside the item loop the claim is split so its
+  // two dependent global round trips stay off the critical path: the counter is bumped at the
+  // start of an item, the chunk fetched after P4, and the item published after R2.
   auto claim = [&]() {
     const int w = (int)atomicAdd(ws.grad_queue, 1u);
     s_claim = w;
     s_claim_c = w < n_items ? chunk_of(w) : 0;
   };
+  int pre_w = n_items, pre_c = 0;  // kDyn, copy thread: the next item, claimed ahead
   int witem, cur_c = 0;
   if (kDyn) {
     if (tid == kCopyTid) claim();
@@ -539,6 +538,7 @@ __device__ __forceinline__ void grad_body(
   cur_t0 = t0;
   cur_i = i;
   const size_t ch = (size_t)c * Hv + j;
+  if (kDyn && tid == kCopyTid) pre_w = (int)atomicAdd(ws.grad_queue, 1u);  // used after R2
   if (tid < 64) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * Hv + j]) : 0.f;
   ok = __syncthreads_and(tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutBwd));
   pending = (kDyn || wnext < n_items) ? 0 : -1;  // kDyn: decided when the next item is claimed
@@ -616,6 +616,19 @@ __device__ __forceinline__ void grad_body(
     tc::tma_load_2d(sm + S::T, &tm_t, &bar_tma2, 0, (int)(ch * 64));
   }
   float* scr = reinterpret_cast<float*>(sm + S::SCR);
+  auto col_partial = [&](float (*dst)[64]) {
+    const int cc = tid & 63, g = tid >> 6;
+    const float* src = scr + g * 16 * 65 + cc;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int rr = 0; rr < 16; rr += 4) {
+      a0 += src[rr * 65];
+      a1 += src[(rr + 1) * 65];
+      a2 += src[(rr + 2) * 65];
+      a3 += src[(rr + 3) * 65];
+    }
+    dst[g][cc] = (a0 + a1) + (a2 + a3);
+  };
   if (ok) {
     if (lo) {  // row r, columns [64 hf, 64 hf + 64)
       float x[64], u[64];
@@ -658,6 +671,7 @@ __device__ __forceinline__ void grad_body(
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
+  if (kDyn && tid == kCopyTid) pre_c = pre_w < n_items ? chunk_of(pre_w) : 0;  // used after R2
   if (kPair && tid == 0) {  // P4 was the last reader of DH and DO: the partner may fill them
     tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&bar_qfree), peer));
     tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&bar_kfree), peer));
@@ -700,10 +714,8 @@ __device__ __forceinline__ void grad_body(
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
-  if (ok && tid < 64) {  // column sums of dP * QK; full k^T dh' vn per row
-    float cs = 0.f;
-    for (int rr = 0; rr < 64; ++rr) cs += scr[rr * 65 + tid];
-    s_colpp[tid] = cs;
+  if (ok) col_partial(s_colpp);  // column sums of dP * QK
+  if (ok && tid < 64) {  // full k^T dh' vn per row
     const float kdv = tid < len ? s_kdv[0][tid] + s_kdv[1][tid] : 0.f;
     s_kdv[0][tid] = kdv;
     const float part = warp_sum(tid < len ? fexp(gC - sgam[tid]) * kdv : 0.f);  // sum_s e^{gC - g_s} k_s^T dh' vn_s
@@ -760,11 +772,7 @@ __device__ __forceinline__ void grad_body(
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
-  if (ok && tid < 64) {
-    float cs = 0.f;
-    for (int rr = 0; rr < 64; ++rr) cs += scr[rr * 65 + tid];
-    s_colbk[tid] = cs;
-  }
+  if (ok) col_partial(s_colbk);
   GDR_TRACE_MARK(2, 7);
   // R2: T^T dVn = dB_v (128-255), X = T^T dT (64-127)
   if (ok && tid == kCopyTid && !kGroup && len == 64) {
@@ -781,11 +789,14 @@ __device__ __forceinline__ void grad_body(
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   if (ok && tid == kCopyTid && pending >= 0) {  // dVn is consumed, dq has left its staging tile
+    GDR_TRACE_CLK(tb21);
     tc::bulk_wait_read<0>();
-    if (kDyn) {  // claim the next item now, off the other threads' path
-      claim();
-      cl_w = s_claim;
-      cl_c = s_claim_c;
+    GDR_TRACE_SINCE(2, 21, tb21);
+    if (kDyn) {  // publish the item claimed ahead
+      GDR_TRACE_CLK(tc24);
+      s_claim = cl_w = pre_w;
+      s_claim_c = cl_c = pre_c;
+      GDR_TRACE_SINCE(2, 24, tc24);
       if (cl_w >= n_items) pending = -1;
     }
     if (pending >= 0) {
@@ -834,7 +845,9 @@ __device__ __forceinline__ void grad_body(
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   if (ok && tid == kCopyTid && pending >= 0) {  // dv has left its staging tile (W)
+    GDR_TRACE_CLK(tb22);
     tc::bulk_wait_read<0>();
+    GDR_TRACE_SINCE(2, 22, tb22);
     issue_loads(kDyn ? cl_w : wnext, kDyn ? cl_c : cnext, kLdW);
     pending |= kLdW;
   }
@@ -866,11 +879,7 @@ __device__ __forceinline__ void grad_body(
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
-  if (ok && tid < 64) {
-    float cs = 0.f;
-    for (int rr = 0; rr < 64; ++rr) cs += scr[rr * 65 + tid];
-    s_colaa[tid] = cs;
-  }
+  if (ok) col_partial(s_colaa);
   GDR_TRACE_MARK(2, 11);
   // R4: dk += T'^T dW + dAGb K + dAGb^T K
   if (ok && tid == 0) {
@@ -906,11 +915,14 @@ __device__ __forceinline__ void grad_body(
     if (hf == 0) {  // per-row scalars: dbeta and d gamma
       const float br = s_beta[r], eg = s_eg[r];
       const float akk = s_akk[0][r] + s_akk[1][r], dbv = s_dbv[0][r] + s_dbv[1][r];
-      if (r < len) dbeta[(size_t)(t0 + r) * Hv + j] = __float2bfloat16_rn(eg * s_colbk[r] + dbv + akk);
+      const float colbk = (s_colbk[0][r] + s_colbk[1][r]) + (s_colbk[2][r] + s_colbk[3][r]);
+      const float colpp = (s_colpp[0][r] + s_colpp[1][r]) + (s_colpp[2][r] + s_colpp[3][r]);
+      const float colaa = (s_colaa[0][r] + s_colaa[1][r]) + (s_colaa[2][r] + s_colaa[3][r]);
+      if (r < len) dbeta[(size_t)(t0 + r) * Hv + j] = __float2bfloat16_rn(eg * colbk + dbv + akk);
       float dgm = 0.f;
       if (r < len) {
-        dgm = (s_rowpp[0][r] + s_rowpp[1][r]) - s_colpp[r] + (s_qh[0][r] + s_qh[1][r]) - dec * s_kdv[0][r] +
-              br * eg * s_colbk[r] + (s_rowaa[0][r] + s_rowaa[1][r]) - s_colaa[r];
+        dgm = (s_rowpp[0][r] + s_rowpp[1][r]) - colpp + (s_qh[0][r] + s_qh[1][r]) - dec * s_kdv[0][r] +
+              br * eg * colbk + (s_rowaa[0][r] + s_rowaa[1][r]) - colaa;
         if (r == len - 1) dgm += fexp(gC) * hdh + (s_red[0] + s_red[1]);
       }
       s_dgam[r] = dgm;
@@ -930,22 +942,25 @@ __device__ __forceinline__ void grad_body(
       const float y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
-    s_colaa[tid] = x;  // s_colaa is free again: reuse it for the warp totals
+    s_colaa[0][tid] = x;  // s_colaa is free again: reuse it for the warp totals
   }
   __syncthreads();
   if (ok && tid < 64) {
     const int rr = 63 - tid;
-    const float v = s_colaa[tid] + (tid >= 32 ? s_colaa[31] : 0.f);
+    const float v = s_colaa[0][tid] + (tid >= 32 ? s_colaa[0][31] : 0.f);
     if (rr < len) dg[(size_t)(t0 + rr) * Hv + j] = v;
   }
   if (tid == kCopyTid) {
+    GDR_TRACE_CLK(tb23);
     tc::bulk_wait_read<0>();  // staging tiles read before the next item's loads
+    GDR_TRACE_SINCE(2, 23, tb23);
     if (ok && pending >= 0) {
       issue_loads(kDyn ? cl_w : wnext, kDyn ? cl_c : cnext, kLdDo);
       pending |= kLdDo;
     }
   }
   GDR_TRACE_MARK(2, 13);
+  GDR_TRACE_COUNT(2, 31);
   item_par ^= 1;
   tc::tc_fence_before();
   __syncthreads();

@@ -9,9 +9,13 @@
 namespace gdr {
 namespace tcx {
 
-// Opt-in phase trace (-DGDR_TRACE): thread 0 of CTA (0,0,0) adds the clock64() cycles
-// spent between consecutive marks into a per-translation-unit table [kernel][mark].
+// Opt-in phase trace (-DGDR_TRACE): thread 0 of CTA GDR_TRACE_BLOCK (default 0) adds the
+// clock64() cycles spent between consecutive marks into a per-translation-unit table
+// [kernel][mark]; GDR_TRACE_COUNT adds 1 to a slot (e.g. items processed).
 #ifdef GDR_TRACE
+#ifndef GDR_TRACE_BLOCK
+#define GDR_TRACE_BLOCK 0
+#endif
 static __device__ unsigned long long g_gdr_trace[8][32];
 static __device__ unsigned long long g_gdr_cta_span[1024][3];  // per CTA: start, end (ns), SM id
 #define GDR_TRACE_CTA_BEGIN()                                                                      \
@@ -36,11 +40,22 @@ static __device__ unsigned long long g_gdr_cta_span[1024][3];  // per CTA: start
 #define GDR_TRACE_INIT() unsigned long long gdr_tprev_ = clock64()
 #define GDR_TRACE_MARK(kid, slot)                                                                  \
   do {                                                                                             \
-    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {               \
+    if (threadIdx.x == 0 && blockIdx.x == GDR_TRACE_BLOCK && blockIdx.y == 0 && blockIdx.z == 0) { \
       const unsigned long long now_ = clock64();                                                   \
       g_gdr_trace[kid][slot] += now_ - gdr_tprev_;                                                 \
       gdr_tprev_ = now_;                                                                           \
     }                                                                                              \
+  } while (0)
+#define GDR_TRACE_COUNT(kid, slot)                                                                 \
+  do {                                                                                             \
+    if (threadIdx.x == 0 && blockIdx.x == GDR_TRACE_BLOCK && blockIdx.y == 0 && blockIdx.z == 0)   \
+      g_gdr_trace[kid][slot] += 1;                                                                 \
+  } while (0)
+// cycles one thread spends in a region (any thread of the traced CTA)
+#define GDR_TRACE_CLK(var) const unsigned long long var = clock64()
+#define GDR_TRACE_SINCE(kid, slot, var)                                                            \
+  do {                                                                                             \
+    if (blockIdx.x == GDR_TRACE_BLOCK) atomicAdd(&g_gdr_trace[kid][slot], clock64() - (var));     \
   } while (0)
 #else
 #define GDR_TRACE_CTA_BEGIN() \
@@ -54,6 +69,15 @@ static __device__ unsigned long long g_gdr_cta_span[1024][3];  // per CTA: start
   } while (0)
 #define GDR_TRACE_MARK(kid, slot) \
   do {                            \
+  } while (0)
+#define GDR_TRACE_COUNT(kid, slot) \
+  do {                             \
+  } while (0)
+#define GDR_TRACE_CLK(var) \
+  do {                     \
+  } while (0)
+#define GDR_TRACE_SINCE(kid, slot, var) \
+  do {                                  \
   } while (0)
 #endif
 
