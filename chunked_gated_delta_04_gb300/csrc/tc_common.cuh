@@ -42,14 +42,14 @@ static __device__ unsigned long long g_gdr_cta_span[1024][3];  // per CTA: start
   do {                                                                                             \
     if (threadIdx.x == 0 && blockIdx.x == GDR_TRACE_BLOCK && blockIdx.y == 0 && blockIdx.z == 0) { \
       const unsigned long long now_ = clock64();                                                   \
-      g_gdr_trace[kid][slot] += now_ - gdr_tprev_;                                                 \
+      atomicAdd(&g_gdr_trace[kid][slot], now_ - gdr_tprev_); /* a reduction: nothing waits on it */ \
       gdr_tprev_ = now_;                                                                           \
     }                                                                                              \
   } while (0)
 #define GDR_TRACE_COUNT(kid, slot)                                                                 \
   do {                                                                                             \
     if (threadIdx.x == 0 && blockIdx.x == GDR_TRACE_BLOCK && blockIdx.y == 0 && blockIdx.z == 0)   \
-      g_gdr_trace[kid][slot] += 1;                                                                 \
+      atomicAdd(&g_gdr_trace[kid][slot], 1ull);                                                    \
   } while (0)
 // cycles one thread spends in a region (any thread of the traced CTA)
 #define GDR_TRACE_CLK(var) const unsigned long long var = clock64()
