@@ -21,6 +21,8 @@
 // No floating-point atomics anywhere: every reduction has a fixed order, so the
 // backward is bitwise deterministic.
 #include <cudaTypedefs.h>
+
+#include <algorithm>
 #include <cstdio>
 
 #include "gdr_internal.h"
@@ -52,18 +54,24 @@ __device__ __forceinline__ void st_global_bf16x32(bf16* dst, const float* v) {
 // ---------------------------------------------------------------------------------
 // walk
 // ---------------------------------------------------------------------------------
+// NC = 64: a walk unit is one half of DV (two units per sequence and v-head, shorter
+// epilogues: for chains that are the critical path).  NC = 128: one unit per sequence and
+// v-head (half the SM time per chain: for batches whose gradients dominate).
+template <int NC>
 struct WalkSmem {
-  static constexpr uint32_t STAGE = 66560;  // KQ 32 KB | W 16 KB | P 8 KB | dO 8 KB | gamma 256 B (+pad)
-  static constexpr uint32_t KQ = 0, W = 32768, P = 49152, DO = 57344, GAM = 65536;
-  static constexpr uint32_t DH = 2 * STAGE;       // dh' as bf16 B operand: 128 rows x 128 B
-  static constexpr uint32_t DVN = DH + 16384;     // dVn bf16 [64][64]
-  static constexpr uint32_t DOS = DVN + 8192;     // diag(e^gamma) dO bf16 [64][64]
-  static constexpr uint32_t DVN2 = DOS + 8192;    // second dVn tile: chunks alternate, so a store
-                                                  // has a whole chunk to read its tile
-  static constexpr uint32_t BYTES = DVN2 + 8192;
+  // per stage: KQ 32 KB | W 16 KB | P 8 KB | dO (NC/64 slabs of 8 KB) | gamma 256 B (+pad)
+  static constexpr uint32_t KQ = 0, W = 32768, P = 49152, DO = 57344;
+  static constexpr uint32_t GAM = DO + (NC / 64) * 8192;
+  static constexpr uint32_t STAGE = (GAM + 256 + 1023) / 1024 * 1024;
+  static constexpr uint32_t DH = 2 * STAGE;              // dh' as bf16 B operand: NC/64 slabs of 128 rows x 128 B
+  static constexpr uint32_t DVN = DH + (NC / 64) * 16384;  // dVn bf16 [64][NC]
+  static constexpr uint32_t DOS = DVN + (NC / 64) * 8192;  // diag(e^gamma) dO bf16 [64][NC]
+  // NC = 64: a second dVn tile (chunks alternate, so a store has a whole chunk to read its tile)
+  static constexpr uint32_t DVN2 = DOS + (NC / 64) * 8192;
+  static constexpr uint32_t BYTES = DVN2 + (NC == 64 ? 8192 : 0);
 };
 
-constexpr int kWalkThreads = 256;  // two warps per TMEM lane quarter, each on 32 of the 64 columns
+constexpr int kWalkThreads = 256;  // two warps per TMEM lane quarter, each on half of the slice's columns
 
 // Counts one finished slice of a chunk: its TMA stores (async proxy) are complete; make them
 // visible at GPU scope before the count.
@@ -90,21 +98,25 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t target,
   return true;
 }
 
-// One walk unit = (sequence, v-head, 64-wide DV slice); `unit` = (seq rank * Hv + v-head) * 2 +
-// slice, sequences longest first.  tb: 256 TMEM columns owned by the caller.  With kPublish
-// the copy thread counts each chunk into ws.walk_flags[chunk * Hv + v-head] once its dh' and
-// dVn tiles have fully reached memory (the fused walk + gradient kernel waits on it).
-template <bool kPublish>
+// One walk unit = (sequence, v-head, NC-wide DV slice); `unit` = (seq rank * Hv + v-head) *
+// (128 / NC) + slice, sequences longest first.  tb: 4 NC TMEM columns owned by the caller.
+// With kPublish the copy thread counts each chunk into ws.walk_flags[chunk * Hv + v-head] once
+// its dh' and dVn tiles have fully reached memory (the fused walk + gradient kernel waits on it).
+template <int NC, bool kPublish>
 __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_w,
                                           const CUtensorMap& tm_p, const CUtensorMap& tm_do,
                                           const CUtensorMap& tm_dhs, const CUtensorMap& tm_dvs, const Dims& d,
                                           const float* __restrict__ dS_T, float* __restrict__ dS0,
                                           const Workspace& ws, int unit, uint32_t tb, unsigned char* sm) {
+  using WS = WalkSmem<NC>;
+  constexpr int kSl = 128 / NC;     // walk units per (sequence, v-head)
+  constexpr int CPT = NC / 2;       // columns per thread: half hf of the slice
+  constexpr int NSL = NC / 64;      // 64-column slabs of the slice
   __shared__ uint64_t bar_load[2], bar_mma;
-  const int n = ws.seq_order[unit / (2 * d.Hv)], j = (unit >> 1) % d.Hv, i = j / d.G;
-  const int dv0 = (unit & 1) * 64;
+  const int n = ws.seq_order[unit / (kSl * d.Hv)], j = (unit / kSl) % d.Hv, i = j / d.G;
+  const int dv0 = (unit % kSl) * NC;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int hf = warp >> 2;            // column half [32 hf, 32 hf + 32) of the slice
+  const int hf = warp >> 2;            // column half [CPT hf, CPT hf + CPT) of the slice
   const int dk = tid & 127;            // TMEM lane = row of the dh' slice
   const int r = tid & 63;              // token row for the 64-row products (lanes 0-63)
   const bool lo = (warp & 3) < 2;      // warps on TMEM lanes 0-63
@@ -125,32 +137,33 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  // TMEM: K dh' (0-63), P^T dO (64-127), W^T dVn (128-191), Q^T diag(e^gamma) dO (192-255)
-  const uint32_t Da = tb, Db = tb + 64, Dc = tb + 128, Dd = tb + 192;
+  // TMEM: K dh' (0), P^T dO (NC), W^T dVn (2 NC), Q^T diag(e^gamma) dO (3 NC)
+  const uint32_t Da = tb, Db = tb + NC, Dc = tb + 2 * NC, Dd = tb + 3 * NC;
 
-  float dh[32];  // dL/dh at the end of the current chunk: row dk, columns dv0 + 32 hf + (0..31)
+  float dh[CPT];  // dL/dh at the end of the current chunk: row dk, columns dv0 + CPT hf + (0..CPT-1)
   {
     const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
-    const int c0 = dv0 + 32 * hf;
+    const int c0 = dv0 + CPT * hf;
 #pragma unroll
-    for (int b = 0; b < 32; ++b)
+    for (int b = 0; b < CPT; ++b)
       dh[b] = dS_T ? dS_T[sb + (d.layout == 0 ? (size_t)dk * 128 + c0 + b : (size_t)(c0 + b) * 128 + dk)] : 0.f;
   }
   auto issue_loads = [&](int c, int st) {
     const int tc0 = t_seq + (c - c_begin) * 64;
     const size_t chh = (size_t)c * Hv + j;
-    unsigned char* base = sm + st * WalkSmem::STAGE;
+    unsigned char* base = sm + st * WS::STAGE;
     uint64_t* bar = &bar_load[st];
-    tc::mbar_arrive_expect_tx(bar, 8 * kSlab + 256);
-    tc::bulk_load(base + WalkSmem::GAM, ws.gam + chh * 64, 256, bar);
-    tc::tma_load_3d(base + WalkSmem::KQ, &tm_k, bar, 0, i, tc0);
-    tc::tma_load_3d(base + WalkSmem::KQ + 2 * kSlab, &tm_k, bar, 64, i, tc0);
-    tc::tma_load_3d(base + WalkSmem::KQ + kSlab, &tm_q, bar, 0, i, tc0);
-    tc::tma_load_3d(base + WalkSmem::KQ + 3 * kSlab, &tm_q, bar, 64, i, tc0);
-    tc::tma_load_2d(base + WalkSmem::W, &tm_w, bar, 0, (int)(chh * 64));
-    tc::tma_load_2d(base + WalkSmem::W + kSlab, &tm_w, bar, 64, (int)(chh * 64));
-    tc::tma_load_2d(base + WalkSmem::P, &tm_p, bar, 0, (int)(chh * 64));
-    tc::tma_load_3d(base + WalkSmem::DO, &tm_do, bar, dv0, j, tc0);
+    tc::mbar_arrive_expect_tx(bar, (7 + NSL) * kSlab + 256);
+    tc::bulk_load(base + WS::GAM, ws.gam + chh * 64, 256, bar);
+    tc::tma_load_3d(base + WS::KQ, &tm_k, bar, 0, i, tc0);
+    tc::tma_load_3d(base + WS::KQ + 2 * kSlab, &tm_k, bar, 64, i, tc0);
+    tc::tma_load_3d(base + WS::KQ + kSlab, &tm_q, bar, 0, i, tc0);
+    tc::tma_load_3d(base + WS::KQ + 3 * kSlab, &tm_q, bar, 64, i, tc0);
+    tc::tma_load_2d(base + WS::W, &tm_w, bar, 0, (int)(chh * 64));
+    tc::tma_load_2d(base + WS::W + kSlab, &tm_w, bar, 64, (int)(chh * 64));
+    tc::tma_load_2d(base + WS::P, &tm_p, bar, 0, (int)(chh * 64));
+#pragma unroll
+    for (int sl = 0; sl < NSL; ++sl) tc::tma_load_3d(base + WS::DO + sl * kSlab, &tm_do, bar, dv0 + 64 * sl, j, tc0);
   };
   if (tid == kCopyTid && c_begin < c_end) issue_loads(c_end - 1, 0);
 
@@ -163,49 +176,68 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
     const uint32_t ld_phase = (it >> 1) & 1;
     const int len = min(64, L - (c - c_begin) * 64);
     const size_t chh = (size_t)c * Hv + j;
-    st_halfrow_bf16(sm + WalkSmem::DH, dk, hf, dh);
+    // dh' as the B operand: slab CPT hf / 64 holds columns [64 s, 64 s + 64) of the slice
+    if constexpr (NC == 64)
+      st_halfrow_bf16(sm + WS::DH, dk, hf, dh);
+    else
+      st_row_bf16(sm + WS::DH + hf * 16384, dk, dh);
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     if (tid == kCopyTid) {  // dh' of this chunk -> workspace, straight from the operand tile
-      tc::tma_store_2d(&tm_dhs, sm + WalkSmem::DH, dv0, (int)(chh * 128));
+#pragma unroll
+      for (int sl = 0; sl < NSL; ++sl) tc::tma_store_2d(&tm_dhs, sm + WS::DH + sl * 16384, dv0 + 64 * sl, (int)(chh * 128));
       tc::bulk_commit();
     }
     GDR_TRACE_MARK(3, 0);
     ok = __syncthreads_and(tc::mbar_wait(&bar_load[st], ld_phase, ws.status, kDevErrTimeoutBwd));
     GDR_TRACE_MARK(3, 1);
-    unsigned char* stg = sm + st * WalkSmem::STAGE;
-    const float* sgam = reinterpret_cast<const float*>(stg + WalkSmem::GAM);
+    unsigned char* stg = sm + st * WS::STAGE;
+    const float* sgam = reinterpret_cast<const float*>(stg + WS::GAM);
     const float gC = sgam[len - 1], gr = sgam[r];
     // the dh'-dependent products first; Q^T diag(e^gamma) dO waits for its scaled operand
     if (ok && tid == 0) {
       tc::tc_fence_after();
-      tc::gemm(Da, kmaj(stg + WalkSmem::KQ, 2 * kSlab), mnmaj(sm + WalkSmem::DH, 16384), 64, 8, false);  // K dh'
-      tc::gemm(Db, mnmaj(stg + WalkSmem::P, kSlab), mnmaj(stg + WalkSmem::DO, kSlab), 64, 4, false);     // P^T dO
+      tc::gemm(Da, kmaj(stg + WS::KQ, 2 * kSlab), mnmaj(sm + WS::DH, 16384), NC, 8, false);  // K dh'
+      tc::gemm(Db, mnmaj(stg + WS::P, kSlab), mnmaj(stg + WS::DO, kSlab), NC, 4, false);     // P^T dO
       tc::mma_commit(&bar_mma);
     }
     GDR_TRACE_MARK(3, 7);
     if (tid == kCopyTid && c - 1 >= c_begin) issue_loads(c - 1, st ^ 1);  // overlaps the MMAs
     GDR_TRACE_MARK(3, 8);
-    // this chunk's dVn tile was last stored two chunks ago (groups since: dh', dVn, dh')
-    unsigned char* dvn_t = sm + ((it & 1) ? WalkSmem::DVN2 : WalkSmem::DVN);
-    if (tid == kCopyTid) tc::bulk_wait_read<3>();
+    // NC = 64: this chunk's dVn tile was last stored two chunks ago (groups since: dh', dVn,
+    // dh'); NC = 128: one tile, stored one chunk ago (group since: this chunk's dh')
+    unsigned char* dvn_t = sm + ((NC == 64 && (it & 1)) ? WS::DVN2 : WS::DVN);
+    if (tid == kCopyTid) {
+      if constexpr (NC == 64)
+        tc::bulk_wait_read<3>();
+      else
+        tc::bulk_wait_read<1>();
+    }
     GDR_TRACE_MARK(3, 9);
     if (ok && warp >= 4) {  // diag(e^gamma) dO, zero past the chunk end: row r, half (tid >> 6) & 1
-      float x[32];
       const int h2 = (tid >> 6) & 1;
-      ld_halfrow_bf16(stg + WalkSmem::DO, r, h2, x);
       const float e = r < len ? fexp(gr) : 0.f;
+      if constexpr (NC == 64) {
+        float x[32];
+        ld_halfrow_bf16(stg + WS::DO, r, h2, x);
 #pragma unroll
-      for (int b = 0; b < 32; ++b) x[b] *= e;
-      st_halfrow_bf16(sm + WalkSmem::DOS, r, h2, x);
+        for (int b = 0; b < 32; ++b) x[b] *= e;
+        st_halfrow_bf16(sm + WS::DOS, r, h2, x);
+      } else {
+        float x[64];
+        ld_row_bf16(stg + WS::DO + h2 * kSlab, r, x);
+#pragma unroll
+        for (int b = 0; b < 64; ++b) x[b] *= e;
+        st_row_bf16(sm + WS::DOS + h2 * kSlab, r, x);
+      }
     }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     if (ok && tid == 0) {  // committed together with W^T dVn below
       tc::tc_fence_after();
-      tc::gemm(Dd, mnmaj(stg + WalkSmem::KQ + kSlab, 2 * kSlab), mnmaj(sm + WalkSmem::DOS, kSlab), 64, 4,
+      tc::gemm(Dd, mnmaj(stg + WS::KQ + kSlab, 2 * kSlab), mnmaj(sm + WS::DOS, kSlab), NC, 4,
                false);  // Q^T diag(e^gamma) dO
     }
     GDR_TRACE_MARK(3, 2);
@@ -214,25 +246,32 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
     tc::tc_fence_after();
     GDR_TRACE_MARK(3, 3);
     if (ok && lo) {  // dVn = scale P^T dO + diag(e^{gamma_C - gamma}) K dh', row r, half hf
-      float x[32], y[32];
-      tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 32 * hf), x);
-      tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 64 + 32 * hf), y);
-      tc::tmem_wait_ld();
       const float dec = fexp(gC - gr);
+#pragma unroll 1
+      for (int q = 0; q < CPT / 32; ++q) {  // 32 columns at a time: [CPT hf + 32 q, +32)
+        float x[32], y[32];
+        tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, CPT * hf + 32 * q), x);
+        tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, NC + CPT * hf + 32 * q), y);
+        tc::tmem_wait_ld();
 #pragma unroll
-      for (int b = 0; b < 32; ++b) y[b] = r < len ? d.scale * y[b] + dec * x[b] : 0.f;
-      st_halfrow_bf16(dvn_t, r, hf, y);
+        for (int b = 0; b < 32; ++b) y[b] = r < len ? d.scale * y[b] + dec * x[b] : 0.f;
+        if constexpr (NC == 64)
+          st_halfrow_bf16(dvn_t, r, hf, y);
+        else
+          st_halfrow_bf16(dvn_t + hf * kSlab, r, q, y);
+      }
     }
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
     __syncthreads();
     if (ok && tid == 0) {
       tc::tc_fence_after();
-      tc::gemm(Dc, mnmaj(stg + WalkSmem::W, kSlab), mnmaj(dvn_t, kSlab), 64, 4, false);  // W^T dVn
+      tc::gemm(Dc, mnmaj(stg + WS::W, kSlab), mnmaj(dvn_t, kSlab), NC, 4, false);  // W^T dVn
       tc::mma_commit(&bar_mma);
     }
     if (ok && tid == kCopyTid) {
-      tc::tma_store_2d(&tm_dvs, dvn_t, dv0, (int)(chh * 64));
+#pragma unroll
+      for (int sl = 0; sl < NSL; ++sl) tc::tma_store_2d(&tm_dvs, dvn_t + sl * kSlab, dv0 + 64 * sl, (int)(chh * 64));
       tc::bulk_commit();
     }
     GDR_TRACE_MARK(3, 4);
@@ -241,13 +280,16 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
     tc::tc_fence_after();
     GDR_TRACE_MARK(3, 5);
     if (ok) {
-      float x[32], y[32];
-      tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 128 + 32 * hf), x);
-      tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 192 + 32 * hf), y);
-      tc::tmem_wait_ld();
       const float eC = fexp(gC);
 #pragma unroll
-      for (int b = 0; b < 32; ++b) dh[b] = eC * dh[b] + d.scale * y[b] - x[b];
+      for (int q = 0; q < CPT / 32; ++q) {
+        float x[32], y[32];
+        tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 2 * NC + CPT * hf + 32 * q), x);
+        tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 3 * NC + CPT * hf + 32 * q), y);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int b = 0; b < 32; ++b) dh[32 * q + b] = eC * dh[32 * q + b] + d.scale * y[b] - x[b];
+      }
     }
     if (tid == kCopyTid) {
       tc::bulk_wait_read<1>();  // this chunk's dh' store has left the operand tile
@@ -274,9 +316,9 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
   }
   if (ok && dS0) {
     const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
-    const int c0 = dv0 + 32 * hf;
+    const int c0 = dv0 + CPT * hf;
 #pragma unroll
-    for (int b = 0; b < 32; ++b)
+    for (int b = 0; b < CPT; ++b)
       dS0[sb + (d.layout == 0 ? (size_t)dk * 128 + c0 + b : (size_t)(c0 + b) * 128 + dk)] = dh[b];
   }
   tc::tc_fence_before();
@@ -288,6 +330,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
   }
 }
 
+template <int NC>
 __global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
@@ -297,12 +340,13 @@ __global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint32_t tmem_slot;
-  if (threadIdx.x < 32) tc::tmem_alloc(&tmem_slot, 256);
+  if (threadIdx.x < 32) tc::tmem_alloc(&tmem_slot, 4 * NC);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  walk_body<false>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvs, d, dS_T, dS0, ws, (int)blockIdx.x, tmem_slot, sm);
-  if (threadIdx.x < 32) tc::tmem_dealloc(tmem_slot, 256);
+  walk_body<NC, false>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvs, d, dS_T, dS0, ws, (int)blockIdx.x, tmem_slot,
+                       sm);
+  if (threadIdx.x < 32) tc::tmem_dealloc(tmem_slot, 4 * NC);
 }
 
 // ---------------------------------------------------------------------------------
@@ -423,7 +467,7 @@ __device__ __forceinline__ void grad_body(
       // kDyn: dh' and dVn of this chunk come from the walk running in the same kernel; on a
       // timeout the loads are left out and the item's own bounded wait ends the walk
       GDR_TRACE_CLK(tw0);
-      if (kDyn && !wait_flag(ws.walk_flags + ch2, 2u, ws.status, kDevErrTimeoutBwd)) return;
+      if (kDyn && !wait_flag(ws.walk_flags + ch2, (uint32_t)d.walk_units, ws.status, kDevErrTimeoutBwd)) return;
       GDR_TRACE_SINCE(2, 20, tw0);
       tc::mbar_arrive_expect_tx(bar, (d.h_bf16 ? 20 : 24) * kSlab + 256);
       for (int q4 = 0; q4 < 4; ++q4)  // dh' rows (q4 & 1) * 64.., columns (q4 >> 1) * 64..
@@ -1008,7 +1052,7 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
 // resident, one per SM): CTAs first run walk units (64 at B=2, H=16, leaving the other SMs
 // free), then every CTA claims gradient items in the order the walk completes chunks, so the
 // gradients of late chunks overlap the walk of early ones.
-template <bool kGroup>
+template <bool kGroup, int NC>
 __global__ void __launch_bounds__(kGradThreads) tc_bwd_walkgrad_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -1027,9 +1071,9 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_walkgrad_kernel(
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  const int n_units = d.num_seqs * d.Hv * 2;
+  const int n_units = d.num_seqs * d.Hv * (128 / NC);
   for (int u = (int)blockIdx.x; u < n_units; u += (int)gridDim.x)
-    walk_body<true>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvn, d, dS_T, dS0, ws, u, tmem_slot, sm);
+    walk_body<NC, true>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvn, d, dS_T, dS0, ws, u, tmem_slot, sm);
   grad_body<kGroup, false, true>(tm_q, tm_k, tm_v, tm_do, tm_w, tm_u, tm_dvn, tm_dh, tm_h, tm_t, tm_dq, tm_dk,
                                  tm_dv, d, beta, dq, dk, dv, dg, dbeta, ws, tmem_slot, sm);
   if (threadIdx.x < 32) tc::tmem_dealloc(tmem_slot, 512);
@@ -1076,12 +1120,23 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
                    : map_2d_box(&thf, a.h_saved, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, 128, rows * 2, 32, 128)))
       return cudaErrorInvalidValue;
   }
+  int dev = 0, n_sm = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  // Walk units per (sequence, v-head): the two DV halves (shorter epilogues, so a shorter
+  // chain) while the walk units fill at most a quarter of the SMs, i.e. when there are so few
+  // chains that the walk is the critical path; else one unit over all of DV, which takes half
+  // the SM time per chain and leaves the SMs to the gradient items.
+  Dims dd = d;
+  dd.walk_units = (long long)d.num_seqs * d.Hv * 2 * 4 <= n_sm ? 2 : 1;
+  const bool halves = dd.walk_units == 2;
   if (fused_walk_grad(d)) {  // walk and gradients in one cooperative kernel
-    int dev = 0, n_sm = 1, per_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    const size_t smg = GradSmem::BYTES + 1024;
-    auto kern = d.G > 1 ? tc_bwd_walkgrad_kernel<true> : tc_bwd_walkgrad_kernel<false>;
+    int per_sm = 0;
+    const size_t smg =
+        (halves ? std::max(GradSmem::BYTES, WalkSmem<64>::BYTES) : std::max(GradSmem::BYTES, WalkSmem<128>::BYTES)) +
+        1024;
+    auto kern = d.G > 1 ? (halves ? tc_bwd_walkgrad_kernel<true, 64> : tc_bwd_walkgrad_kernel<true, 128>)
+                        : (halves ? tc_bwd_walkgrad_kernel<false, 64> : tc_bwd_walkgrad_kernel<false, 128>);
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGradThreads, smg) != cudaSuccess || per_sm < 1)
       return cudaErrorInvalidConfiguration;
@@ -1091,7 +1146,6 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     bf16 *dq = (bf16*)a.dq, *dk = (bf16*)a.dk, *dv = (bf16*)a.dv, *dbeta = (bf16*)a.dbeta;
     const float* dS_T = a.dS_T;
     float *dS0 = a.dS0, *dg = a.dg;
-    Dims dd = d;
     Workspace w = ws;
     void* args[] = {&tq, &tk, &tv, &tdo, &tw, &tu, &tp, &tdvn, &tdh, &tdhs, &thf, &tt, &tdq, &tdk, &tdv, &dd,
                     (void*)&dS_T, (void*)&dS0, (void*)&beta, (void*)&dq, (void*)&dk, (void*)&dv, (void*)&dg,
@@ -1106,16 +1160,14 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     return cudaGetLastError();
   }
   if (d.num_seqs > 0) {
-    const size_t sm = WalkSmem::BYTES + 1024;
-    cudaFuncSetAttribute(tc_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    tc_bwd_walk_kernel<<<d.num_seqs * d.Hv * 2, kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, d, a.dS_T,
-                                                                      a.dS0, ws);
+    const size_t sm = (halves ? WalkSmem<64>::BYTES : WalkSmem<128>::BYTES) + 1024;
+    auto kern = halves ? tc_bwd_walk_kernel<64> : tc_bwd_walk_kernel<128>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    kern<<<d.num_seqs * d.Hv * dd.walk_units, kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, dd, a.dS_T,
+                                                                    a.dS0, ws);
     stage_mark(s, "bwd_walk");
   }
   if (d.max_chunks > 0 && Tt > 0) {
-    int dev = 0, n_sm = 1;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     const long long n_items = (long long)d.max_chunks * d.Hv;
     const dim3 grid((unsigned)(n_items < n_sm ? n_items : n_sm));  // persistent: one CTA per SM
     const size_t smg = GradSmem::BYTES + 1024;

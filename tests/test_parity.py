@@ -303,11 +303,28 @@ def test_fused_prologue_autograd():
 # Fixed-length tensor-core batches run the reverse walk and the gradients as one cooperative
 # kernel.  These cases cover a CTA running several walk units (more (sequence, head, DV half)
 # units than SMs), and Hv = 4 Hk (fp32 partials and the group reduce after the fused kernel).
-@pytest.mark.parametrize("name,B,T,Hk,Hv", [("many_walk_units", 10, 130, 8, 8), ("gva4", 2, 150, 1, 4)])
+@pytest.mark.parametrize("name,B,T,Hk,Hv", [("many_walk_units", 10, 130, 8, 8), ("gva4", 2, 150, 1, 4),
+                                             ("few_chains_dv_halves", 1, 300, 2, 2)])
 def test_fused_backward_shapes(name, B, T, Hk, Hv):
     import chunked_gated_delta_04_gb300 as gdr
 
     w = small_workload(name, torch.bfloat16, B=B, T=T, Hk=Hk, Hv=Hv, DK=128, DV=128)
     p = gdr.make_problem(B, T, Hk, Hv, 128, 128, torch.bfloat16, "KV")
     assert gdr.gdr_path(p) == 1
+    _check(w)
+
+
+# The walk runs as two DV halves per (sequence, v-head) while its units fill at most a quarter
+# of the SMs (few chains: the walk is the critical path) and as one full-width unit otherwise.
+# Full width through the stand-alone walk (cluster-pair gradients, Hv = 2 Hk, variable length)
+# and through the fused kernel (fixed length), against the oracle.
+@pytest.mark.parametrize("name,B,T,Hk,Hv,lens", [
+    ("full_width_pair_varlen", 1, None, 4, 8, [0, 70, 130, 1, 200, 64]),
+    ("full_width_fused", 3, 200, 8, 8, None),
+])
+def test_walk_full_width(name, B, T, Hk, Hv, lens):
+    if lens is None:
+        w = small_workload(name, torch.bfloat16, B=B, T=T, Hk=Hk, Hv=Hv, DK=128, DV=128)
+    else:
+        w = small_workload(name, torch.bfloat16, Hk=Hk, Hv=Hv, DK=128, DV=128, seqlens=lens)
     _check(w)
