@@ -40,6 +40,7 @@ STAGE_IO = {
     "index": ("", ""),
     "fwd_prep": ("q k v g beta", ""),
     "fwd_state": ("q k S0", "o h_saved S_T"),
+    "fwd_fused": ("q k v g beta S0", "o h_saved S_T"),
     "fwd_out": ("q", "o"),
     "bwd_prep": ("q k v g beta", ""),
     "bwd_vn": ("h_saved", ""),

@@ -132,6 +132,12 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
       w.dk_part = (float*)take(sizeof(float) * (size_t)d.T_total * d.Hv * d.DK);
     }
   }
+  if (!backward && fused_fwd_possible(d)) {  // one region: flags, then the claim counters (zeroed per call)
+    w.fwd_flags = (uint32_t*)take(sizeof(uint32_t) * ((size_t)d.max_chunks * d.Hv + 64));
+    w.fwd_queue = w.fwd_flags ? w.fwd_flags + (size_t)d.max_chunks * d.Hv : nullptr;
+    w.step_off = (int*)take(sizeof(int) * ((size_t)d.max_chunks + 2));
+    w.fwd_chunk = (int*)take(sizeof(int) * ((size_t)d.max_chunks + 1));
+  }
   if (d.prologue) {
     const size_t in_el = d.dtype == GDR_DTYPE_BF16 ? 2 : 4;
     if (d.prologue & GDR_PROLOGUE_QK_L2NORM) {

@@ -22,7 +22,8 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
                                                                   int* __restrict__ order,
                                                                   uint32_t* __restrict__ status,
                                                                   int* __restrict__ step_off,
-                                                                  int* __restrict__ grad_chunk) {
+                                                                  int* __restrict__ grad_chunk,
+                                                                  int* __restrict__ fwd_chunk) {
   __shared__ int warp_tot[32];
   __shared__ int s_bad;
   __shared__ int s_carry;
@@ -119,7 +120,8 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
     for (int n = tid; n < num_seqs; n += kIndexThreads) order[n] = n;
   }
 
-  // Walk-step table of the fused backward (step_off != nullptr; requires the sorted order):
+  // Step table of the fused kernels (step_off != nullptr; requires the sorted order), in the
+  // backward's terms (the forward's step s is local chunk s of the same sequences):
   // at reverse step s the walk finishes local chunk nc(n) - 1 - s of every sequence with
   // nc(n) > s, i.e. of the first cnt(s) sequences in longest-first order.  step_off[s] =
   // sum_{s' < s} cnt(s') for s = 0..S (S = the longest sequence's chunk count), and
@@ -174,7 +176,8 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
       if (tid == kIndexThreads - 1) s_carry = carry + incl;
       __syncthreads();
     }
-    // the chunk of every queue position, so the gradient role decodes an item with one load
+    // the chunk of every queue position, so a claimed item decodes with one load: reverse
+    // step s of the backward walk is local chunk nc - 1 - s, forward step s local chunk s
     const int n_q = step_off[S];
     for (int q = tid; q < n_q; q += kIndexThreads) {
       int lo = 0, hi = S - 1;  // last step s with step_off[s] <= q
@@ -182,7 +185,9 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
         const int mid = (lo + hi + 1) >> 1;
         if (step_off[mid] <= q) lo = mid; else hi = mid - 1;
       }
-      grad_chunk[q] = off[order[q - step_off[lo]] + 1] - 1 - lo;
+      const int n = order[q - step_off[lo]];
+      if (grad_chunk) grad_chunk[q] = off[n + 1] - 1 - lo;
+      if (fwd_chunk) fwd_chunk[q] = off[n] + lo;
     }
   }
 }
@@ -190,7 +195,7 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
 cudaError_t launch_index(const Dims& d, const Workspace& ws, cudaStream_t s) {
   gdr_index_kernel<<<1, kIndexThreads, 0, s>>>(d.cu, d.num_seqs, d.cu ? (int)d.T_total : d.T,
                                                d.max_chunks, ws.chunks, ws.seq_chunk_off, ws.seq_order,
-                                               ws.status, ws.step_off, ws.grad_chunk);
+                                               ws.status, ws.step_off, ws.grad_chunk, ws.fwd_chunk);
   stage_mark(s, "index");
   return cudaGetLastError();
 }

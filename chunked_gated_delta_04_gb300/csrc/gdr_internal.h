@@ -62,6 +62,12 @@ struct Workspace {
   uint32_t* grad_queue;
   int* step_off;  // [max_chunks + 2]: the walk-step prefix table built by the index kernel
   int* grad_chunk;  // [max_chunks]: chunk of queue position q (gradient items q * Hv + v-head)
+  // fused forward (prep + state in one kernel): per (chunk, v-head) flag set when its prep is
+  // stored [max_chunks][Hv]; claim counters {prep items, state units}; the chunk of every
+  // queue position in forward step order (local chunk s of every sequence)
+  uint32_t* fwd_flags;
+  uint32_t* fwd_queue;
+  int* fwd_chunk;
   // fused prologue outputs (input dtype unless noted): normalised q, k [T_total][Hk][DK],
   // g = logsigmoid(a) fp32 [T_total][Hv], beta = sigmoid(b) [T_total][Hv]
   void* qn;
@@ -144,6 +150,7 @@ bool map_2d_box(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint32
 bool tc_bwd_available();  // the tensor-core backward is built
 bool grad_pair_mode(const Dims& d);  // Hv = 2 Hk tensor-core backward: dq/dk summed on chip
 bool fused_walk_grad(const Dims& d);  // tensor-core backward: walk and gradients in one kernel
+bool fused_fwd_possible(const Dims& d);  // tensor-core forward: prep and state may run as one kernel
 constexpr int kMaxFusedSeqs = 8192;   // the fused backward needs the longest-first order (index kernel)
 // The chunk-prep kernel (W, U, P, gamma; with write_T also T) on the tensor cores.
 cudaError_t tc_launch_prep(const Dims& d, const void* q, const void* k, const void* v, const float* g,

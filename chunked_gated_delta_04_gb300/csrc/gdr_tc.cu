@@ -23,6 +23,9 @@
 //             chunk's tiles into the other stage while the current chunk computes.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cstdio>
+
 #include <mutex>
 
 #include "../../include/gdr_debug.h"
@@ -246,54 +249,125 @@ __device__ __forceinline__ void solve_unit_lower64(const float* __restrict__ sA,
 #undef SOLVE_MARK
 }
 
-__global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
-                                                             const __grid_constant__ CUtensorMap tm_k,
-                                                             const __grid_constant__ CUtensorMap tm_v,
-                                                             const __grid_constant__ CUtensorMap tm_w,
-                                                             const __grid_constant__ CUtensorMap tm_u,
-                                                             const __grid_constant__ CUtensorMap tm_p,
-                                                             const __grid_constant__ CUtensorMap tm_t, Dims d,
-                                                             const float* __restrict__ g,
-                                                             const bf16* __restrict__ beta, Workspace ws,
-                                                             int write_T) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = align1024(smem_raw);
-  __shared__ uint64_t bar_tma, bar_mma;
+// Publishes one finished chunk-head of the fused forward: its TMA stores (async proxy) and
+// gamma (plain stores before the caller's barrier) are complete; make them visible at GPU scope
+// before the flag.
+__device__ __forceinline__ void publish_prep(uint32_t* flag) {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __threadfence();
+  atomicAdd(flag, 1u);
+}
+
+// Bounded wait until *flag != 0 (acquire at GPU scope), then orders the caller's later TMA
+// loads after it.  On expiry sets `bit` in *status and returns false.
+__device__ __forceinline__ bool wait_prep(const uint32_t* flag, uint32_t* status, uint32_t bit) {
+  uint32_t v;
+  const uint64_t t0 = tc::globaltimer_ns();
+  while (true) {
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v != 0u) break;
+    if (tc::globaltimer_ns() - t0 > tc::kWaitLimitNs) {
+      atomicOr(status, bit);
+      return false;
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
+// The chunk prep of a CTA's items (chunk c, v-head j).  kFused = false: the persistent grid's
+// items w = blockIdx.x + k * gridDim.x in chunk-major order.  kFused = true (fused forward
+// kernel): items claimed from ws.fwd_queue in the forward's step order (queue position q =
+// w / Hv holds chunk ws.fwd_chunk[q]); each item's stores are waited for and counted into
+// ws.fwd_flags[c * Hv + j], one item late so the wait overlaps the next item's loads.
+template <bool kFused>
+__device__ __forceinline__ void prep_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                          const CUtensorMap& tm_w, const CUtensorMap& tm_u, const CUtensorMap& tm_p,
+                                          const CUtensorMap& tm_t, const Dims& d, const float* __restrict__ g,
+                                          const bf16* __restrict__ beta, const Workspace& ws, int write_T,
+                                          unsigned char* sm) {
+  // kFused: one CTA per SM with the state's shared memory, so the q/k/v tiles have two stages
+  // (the second after PrepSmem::BYTES, checked at the fused kernel) and the next item's tiles
+  // load during this item
+  __shared__ uint64_t bar_tma[2], bar_mma;
   __shared__ uint32_t tmem_slot;
   __shared__ float s_gam[64], s_beta[64], s_bexp[64], s_carry;
+  __shared__ int s_item[4];  // the current item and its chunk; kFused: the next (claimed ahead)
   const int tid = threadIdx.x, warp = tid >> 5;
   const int Hv = d.Hv;
 
   if (tid == 0) {
-    tc::mbar_init(&bar_tma, 1);
+    tc::mbar_init(&bar_tma[0], 1);
+    tc::mbar_init(&bar_tma[1], 1);
     tc::mbar_init(&bar_mma, 1);
     tc::fence_barrier_init();
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_slot, 256);
+  if (warp == 0) tc::tmem_alloc<256>(&tmem_slot);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tbase = tmem_slot;
   GDR_TRACE_INIT();
   GDR_TRACE_CTA_BEGIN();
-  // Persistent: each CTA walks the (chunk, v-head) items w = blockIdx.x + k * gridDim.x.
   bool ok = true;
   uint32_t item_par = 0;  // phase parity of bar_tma for the current item (bar_mma: 2 per item)
-  const int n_items = d.max_chunks * Hv;
-  for (int witem = blockIdx.x; witem < n_items && ok; witem += gridDim.x) {
-  const int c = witem / Hv, j = witem % Hv, i = j / d.G;
+  const int n_items = kFused ? ws.step_off[ws.step_off[d.max_chunks + 1]] * Hv : d.max_chunks * Hv;
+  // the next item and its chunk into s_item[slot], s_item[slot + 1] (thread 0 decides; everyone
+  // reads them after a barrier)
+  auto next_item = [&](int w, int slot) {
+    if (kFused) {
+      const int q = (int)atomicAdd(ws.fwd_queue, 1u);
+      s_item[slot] = q < n_items ? q : n_items;
+      s_item[slot + 1] = q < n_items ? ws.fwd_chunk[q / Hv] : 0;
+    } else {
+      w = w < 0 ? (int)blockIdx.x : w + (int)gridDim.x;
+      s_item[slot] = w;
+      s_item[slot + 1] = w < n_items ? w / Hv : 0;
+    }
+  };
+  // q/k/v tiles of item w (chunk cc) into stage st
+  auto issue_loads = [&](int w, int cc, int st) {
+    const int j2 = w % Hv, i2 = j2 / d.G, tt = ws.chunks[cc].y;
+    unsigned char* kq = sm + (st ? PrepSmem::BYTES : PrepSmem::KQ);
+    unsigned char* vv = sm + (st ? PrepSmem::BYTES + 2 * 16384 : PrepSmem::V);
+    tc::mbar_arrive_expect_tx(&bar_tma[st], 6 * kSlab);
+    tc::tma_load_3d(kq, &tm_k, &bar_tma[st], 0, i2, tt);
+    tc::tma_load_3d(kq + 2 * kSlab, &tm_k, &bar_tma[st], 64, i2, tt);
+    tc::tma_load_3d(kq + kSlab, &tm_q, &bar_tma[st], 0, i2, tt);
+    tc::tma_load_3d(kq + 3 * kSlab, &tm_q, &bar_tma[st], 64, i2, tt);
+    tc::tma_load_3d(vv, &tm_v, &bar_tma[st], 0, j2, tt);
+    tc::tma_load_3d(vv + kSlab, &tm_v, &bar_tma[st], 64, j2, tt);
+  };
+  if (tid == 0) {
+    next_item(-1, 0);
+    if (kFused && s_item[0] < n_items) issue_loads(s_item[0], s_item[1], 0);
+  }
+  __syncthreads();
+  int witem = s_item[0], c = s_item[1];
+  int pub = -1;  // kFused: the flag index of the previous item, not yet published
+  int it = 0;    // kFused: items done (stage it & 1, phase (it >> 1) & 1)
+  while (witem < n_items && ok) {
+  const int j = witem % Hv, i = j / d.G;
   const int4 ci = ws.chunks[c];
   const int len = ci.z, t0 = ci.y;
-  if (len <= 0) continue;  // empty chunk slot (uniform across the CTA)
   const size_t ch = (size_t)c * Hv + j;
+  const int st = kFused ? (it & 1) : 0;
+  unsigned char* const kq_t = sm + (st ? PrepSmem::BYTES : PrepSmem::KQ);
+  unsigned char* const v_t = sm + (st ? PrepSmem::BYTES + 2 * 16384 : PrepSmem::V);
+  if (len > 0) {  // (an empty chunk slot: uniform across the CTA)
   if (tid == 0) {
-    tc::mbar_arrive_expect_tx(&bar_tma, 6 * kSlab);
-    tc::tma_load_3d(sm + PrepSmem::KQ, &tm_k, &bar_tma, 0, i, t0);
-    tc::tma_load_3d(sm + PrepSmem::KQ + 2 * kSlab, &tm_k, &bar_tma, 64, i, t0);
-    tc::tma_load_3d(sm + PrepSmem::KQ + kSlab, &tm_q, &bar_tma, 0, i, t0);
-    tc::tma_load_3d(sm + PrepSmem::KQ + 3 * kSlab, &tm_q, &bar_tma, 64, i, t0);
-    tc::tma_load_3d(sm + PrepSmem::V, &tm_v, &bar_tma, 0, j, t0);
-    tc::tma_load_3d(sm + PrepSmem::V + kSlab, &tm_v, &bar_tma, 64, j, t0);
+    if (kFused) {  // claim the next item and load its tiles into the other stage, whose last
+                   // reader (two items ago) is done; then publish the previous item
+      next_item(witem, 2);
+      if (s_item[2] < n_items) issue_loads(s_item[2], s_item[3], st ^ 1);
+      if (pub >= 0) {
+        tc::bulk_wait<0>();
+        publish_prep(ws.fwd_flags + pub);
+        pub = -1;
+      }
+    } else {
+      issue_loads(witem, c, 0);
+    }
   }
   // gamma (in-chunk cumsum of g) and beta, zero past the chunk end
   {
@@ -309,9 +383,10 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
       s_bexp[tid] = b * fexp(x);  // beta_s e^{gamma_s}
     }
   }
-  ok = __syncthreads_and(tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutPrep));
+  ok = __syncthreads_and(tc::mbar_wait(&bar_tma[st], kFused ? (uint32_t)(it >> 1) & 1u : item_par, ws.status,
+                                       kDevErrTimeoutPrep));
   GDR_TRACE_MARK(0, 0);
-  const uint32_t s_kq = tc::smem_u32(sm + PrepSmem::KQ), s_v = tc::smem_u32(sm + PrepSmem::V);
+  const uint32_t s_kq = tc::smem_u32(kq_t), s_v = tc::smem_u32(v_t);
   const uint32_t s_tt = tc::smem_u32(sm + PrepSmem::TT);
   if (ok && tid == 0) {
     tc::tc_fence_after();
@@ -398,7 +473,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
   if (ok) {  // W rows (threads 0-63) and U rows (threads 64-127) staged in the free K/Q tiles
     const int r = tid & 63;
     const int col = tid < 64 ? 0 : 128;
-    unsigned char* stg = sm + PrepSmem::KQ + (tid < 64 ? 0 : 2 * kSlab);
+    unsigned char* stg = kq_t + (tid < 64 ? 0 : 2 * kSlab);
     float v[64];
     tmem_ld64(tbase, warp, col, v);
     st_row_bf16(stg, r, v);
@@ -410,23 +485,53 @@ __global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_consta
   tc::tc_fence_before();
   __syncthreads();
   if (ok && tid == 0) {
-    tc::tma_store_2d(&tm_w, sm + PrepSmem::KQ, 0, (int)(ch * 64));
-    tc::tma_store_2d(&tm_w, sm + PrepSmem::KQ + kSlab, 64, (int)(ch * 64));
-    tc::tma_store_2d(&tm_u, sm + PrepSmem::KQ + 2 * kSlab, 0, (int)(ch * 64));
-    tc::tma_store_2d(&tm_u, sm + PrepSmem::KQ + 3 * kSlab, 64, (int)(ch * 64));
+    tc::tma_store_2d(&tm_w, kq_t, 0, (int)(ch * 64));
+    tc::tma_store_2d(&tm_w, kq_t + kSlab, 64, (int)(ch * 64));
+    tc::tma_store_2d(&tm_u, kq_t + 2 * kSlab, 0, (int)(ch * 64));
+    tc::tma_store_2d(&tm_u, kq_t + 3 * kSlab, 64, (int)(ch * 64));
     tc::bulk_commit();
   }
   if (tid == 0) tc::bulk_wait_read<0>();  // staging tiles read before the next item's loads
   GDR_TRACE_MARK(0, 5);
   item_par ^= 1;
+  ++it;
+  if (kFused && tid == 0) pub = (int)ch;
+  }  // len > 0
+  if (!kFused && tid == 0) next_item(witem, 0);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  witem = s_item[kFused ? 2 : 0];
+  c = s_item[kFused ? 3 : 1];
+  __syncthreads();  // s_item is rewritten by the next claim
   }  // items
+  if (kFused && tid == 0 && pub >= 0) {  // the last item (its gamma stores are behind the barriers above)
+    tc::bulk_wait<0>();
+    publish_prep(ws.fwd_flags + pub);
+  }
   GDR_TRACE_CTA_END();
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tbase, 256);
+  if (tid == 0) {  // a later role of this CTA (none today) would initialise them again
+    tc::mbar_inval(&bar_tma[0]);
+    tc::mbar_inval(&bar_tma[1]);
+    tc::mbar_inval(&bar_mma);
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads) tc_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                             const __grid_constant__ CUtensorMap tm_k,
+                                                             const __grid_constant__ CUtensorMap tm_v,
+                                                             const __grid_constant__ CUtensorMap tm_w,
+                                                             const __grid_constant__ CUtensorMap tm_u,
+                                                             const __grid_constant__ CUtensorMap tm_p,
+                                                             const __grid_constant__ CUtensorMap tm_t, Dims d,
+                                                             const float* __restrict__ g,
+                                                             const bf16* __restrict__ beta, Workspace ws,
+                                                             int write_T) {
+  extern __shared__ unsigned char smem_raw[];
+  prep_body<false>(tm_q, tm_k, tm_v, tm_w, tm_u, tm_p, tm_t, d, g, beta, ws, write_T, align1024(smem_raw));
 }
 
 // ---------------------------------------------------------------------------------
@@ -500,14 +605,16 @@ __device__ __forceinline__ void st_row_bf16x32_sw64(unsigned char* tile, int row
   for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(tile + row * 64 + ((c ^ sw) << 4)) = w[c];
 }
 
-template <bool kSingle>
-__global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
-    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
-    const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_hs, Dims d,
-    const float* __restrict__ S0, float* __restrict__ S_T, bf16* __restrict__ o, Workspace ws) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* sm = align1024(smem_raw);
+// One state unit `cta` = (sequence rank, v-head, DV slice), slice fastest.  kFused (fused
+// forward kernel, double-buffered): chunk c's W, U, P and gamma are loaded only after the prep
+// role has counted (c, v-head) in ws.fwd_flags; the copy thread waits for chunk c + 1 while
+// chunk c's first product runs, off the chain.
+template <bool kSingle, bool kFused>
+__device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_w,
+                                           const CUtensorMap& tm_u, const CUtensorMap& tm_p,
+                                           const CUtensorMap& tm_hs, const Dims& d, const float* __restrict__ S0,
+                                           float* __restrict__ S_T, bf16* __restrict__ o, const Workspace& ws,
+                                           int cta, unsigned char* sm) {
   using SS = StateSmem<kSingle>;
   // two stages: bar_load[st] per stage; single buffers: bar_load[0] = [W|Q] and gamma,
   // bar_load[1] = U, bar_kp = K and P (one phase per chunk each)
@@ -515,7 +622,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
   __shared__ uint32_t tmem_slot;
   // block -> (sequence in longest-first order, v-head, DV slice); the slices of one
   // (sequence, head) are adjacent so they share its W/Q/K tiles in L2
-  const int slice = blockIdx.x % kStateSlices, rest = blockIdx.x / kStateSlices;
+  const int slice = cta % kStateSlices, rest = cta / kStateSlices;
   const int j = rest % d.Hv, n = ws.seq_order[rest / d.Hv], i = j / d.G;
   const int dv0 = slice * 32;
   const int tid = threadIdx.x, warp = tid >> 5;
@@ -535,7 +642,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     tc::mbar_init(&bar_pv, 1);
     tc::fence_barrier_init();
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_slot, 128);
+  if (warp == 0) tc::tmem_alloc<128>(&tmem_slot);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -589,7 +696,14 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     tc::tma_load_3d(sm + SS::K + kSlab, &tm_k, &bar_kp, 64, i, tc0);
     tc::tma_load_2d(sm + SS::P, &tm_p, &bar_kp, 0, (int)(chh * 64));
   };
-  if (tid == kCopyTid && c_begin < c_end) {
+  // kFused: the prep role's flag of chunk c (bounded wait; on expiry the loads are left out
+  // and the consumer's own bounded wait ends the chain).  (Reading the next chunk's flag a
+  // chunk early with a relaxed load and an acquire fence when it was set measured slower: the
+  // fence costs more than the poll it replaces.)
+  auto prep_ready = [&](int c) {
+    return !kFused || wait_prep(ws.fwd_flags + (size_t)c * Hv + j, ws.status, kDevErrTimeoutFwd);
+  };
+  if (tid == kCopyTid && c_begin < c_end && prep_ready(c_begin)) {
     if (kSingle) {
       load_wq(c_begin);
       load_u(c_begin);
@@ -598,6 +712,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
       issue_loads(c_begin, 0);
     }
   }
+  static_assert(!(kSingle && kFused), "the fused forward runs the double-buffered state");
   st_col32_bf16(sm + SS::HT, tid, h);
 
   bool ok = true;
@@ -650,7 +765,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
       tc::mma_commit(&bar_mma);
     }
     GDR_TRACE_MARK(1, 7);
-    if (!kSingle && tid == kCopyTid && c + 1 < c_end) issue_loads(c + 1, st ^ 1);  // overlaps the MMA
+    if (!kSingle && tid == kCopyTid && c + 1 < c_end && prep_ready(c + 1)) issue_loads(c + 1, st ^ 1);  // overlaps the MMA
     // single buffers: this chunk's K and P, once the previous chunk's P Vn (their last
     // reader) has run
     if (kSingle && ok && tid == kCopyTid && it > 0 &&
@@ -749,9 +864,54 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
   if (warp == 0) tc::tmem_dealloc(tbase, 128);
 }
 
+template <bool kSingle>
+__global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
+    const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_hs, Dims d,
+    const float* __restrict__ S0, float* __restrict__ S_T, bf16* __restrict__ o, Workspace ws) {
+  extern __shared__ unsigned char smem_raw[];
+  state_body<kSingle, false>(tm_q, tm_k, tm_w, tm_u, tm_p, tm_hs, d, S0, S_T, o, ws, (int)blockIdx.x,
+                             align1024(smem_raw));
+}
+
+// The forward's prep and state recurrence in one cooperative launch (every CTA resident, one
+// per SM): the first n_state CTAs to start (a counter) run the state units, double-buffered;
+// every other CTA runs the prep role, whose items are claimed in the forward's step order, so
+// chunk c of every chain is prepared before chunk c + 1 of any.  State units wait only for prep
+// items, which never wait: every wait ends.
+static_assert(PrepSmem::BYTES + 3 * 16384 <= StateSmem<false>::BYTES, "the fused prep role's second tile stage");
+__global__ void __launch_bounds__(kTcThreads) tc_fwd_fused_kernel(
+    const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_w,
+    const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_p,
+    const __grid_constant__ CUtensorMap tm_t, const __grid_constant__ CUtensorMap tm_hs, Dims d,
+    const float* __restrict__ g, const bf16* __restrict__ beta, const float* __restrict__ S0,
+    float* __restrict__ S_T, bf16* __restrict__ o, Workspace ws, int write_T, int n_state) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ int s_role;
+  if (threadIdx.x == 0) {
+    const int u = (int)atomicAdd(ws.fwd_queue + 1, 1u);
+    s_role = u < n_state ? u : -1;  // -1: prep
+  }
+  __syncthreads();
+  const int role = s_role;
+  if (role >= 0)
+    state_body<false, true>(tm_q, tm_k, tm_w, tm_u, tm_p, tm_hs, d, S0, S_T, o, ws, role, align1024(smem_raw));
+  else
+    prep_body<true>(tm_q, tm_k, tm_v, tm_w, tm_u, tm_p, tm_t, d, g, beta, ws, write_T, align1024(smem_raw));
+}
+
 }  // namespace
 
 bool tc_available() { return get_encoder(); }
+
+// The forward's prep and state can share one cooperative kernel when the step table exists
+// (sorted order: at most kMaxFusedSeqs sequences); tc_forward decides per launch whether the
+// state units fit (see tc_fwd_fused_kernel).
+bool fused_fwd_possible(const Dims& d) {
+  return d.path == 1 && d.num_seqs > 0 && d.num_seqs <= kMaxFusedSeqs && d.T_total > 0 && d.max_chunks > 0;
+}
 
 // Persistent grid of the chunk-prep kernel: two CTAs per SM (shared memory allows two).
 static dim3 prep_grid(const Dims& d) {
@@ -789,6 +949,44 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
     // saved factors: T is kept for the backward too
     if (d.save_wy && !map_2d(&tt, ws.Tb, 64, rows)) return cudaErrorInvalidValue;
   }
+  int dev = 0, n_sm = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const long long n_cta = (long long)d.num_seqs * d.Hv * kStateSlices;
+  // Prep and state in one cooperative kernel when there are at most half as many state units as
+  // SMs (few long chains): one CTA per SM, the state units double-buffered, the other SMs
+  // preparing chunks in step order.  (Two CTAs per SM, a state unit beside a prep CTA, would
+  // serve more chains, but the occupancy calculation of a cooperative launch admits one CTA per
+  // SM for kernels that allocate tensor memory.)  Otherwise the two launches below.
+  if (fused_fwd_possible(d) && n_cta * 2 <= n_sm) {
+    const size_t smf = std::max<size_t>(PrepSmem::BYTES, StateSmem<false>::BYTES) + 1024;
+    auto kern = tc_fwd_fused_kernel;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf);
+    int per_sm = 0;
+    const cudaError_t qe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTcThreads, smf);
+    if (qe != cudaSuccess) (void)cudaGetLastError();  // our own query's error: fall back below
+    if (qe == cudaSuccess && per_sm == 1) {
+      cudaError_t e = cudaMemsetAsync(ws.fwd_flags, 0,
+                                      sizeof(uint32_t) * ((size_t)d.max_chunks * d.Hv + 64), s);
+      if (e != cudaSuccess) return e;
+      Dims dd = d;
+      Workspace w = ws;
+      const float* g = a.g;
+      const bf16* beta = (const bf16*)a.beta;
+      const float* S0 = a.S0;
+      float* S_T = a.S_T;
+      bf16* o = (bf16*)a.o;
+      int write_T = d.save_wy;
+      int n_state = (int)n_cta;
+      CUtensorMap& tt_arg = d.save_wy ? tt : tp;
+      void* args[] = {&tq, &tk, &tv, &tw, &tu, &tp, &tt_arg, &ths, &dd, (void*)&g, (void*)&beta, (void*)&S0,
+                      (void*)&S_T, (void*)&o, &w, &write_T, &n_state};
+      e = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)n_sm), dim3(kTcThreads), args, smf, s);
+      if (e != cudaSuccess) return e;
+      stage_mark(s, "fwd_fused");
+      return cudaGetLastError();
+    }
+  }
   if (d.max_chunks > 0 && Tt > 0) {
     const size_t smp = PrepSmem::BYTES + 1024;
     cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
@@ -798,10 +996,6 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
   }
   if (d.num_seqs > 0) {
     // more CTAs than SMs: the single-buffered variant, two CTAs per SM, so they all run at once
-    int dev = 0, n_sm = 1;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    const long long n_cta = (long long)d.num_seqs * d.Hv * kStateSlices;
     const bool single = n_cta > n_sm;
     const size_t sms = (single ? StateSmem<true>::BYTES : StateSmem<false>::BYTES) + 1024;
     auto kern = single ? tc_fwd_state_kernel<true> : tc_fwd_state_kernel<false>;

@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint32_t tmem_slot;
-  if (threadIdx.x < 32) tc::tmem_alloc(&tmem_slot, 4 * NC);
+  if (threadIdx.x < 32) tc::tmem_alloc<4 * NC>(&tmem_slot);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -1037,7 +1037,7 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint32_t tmem_slot;
-  if (threadIdx.x < 32) tc::tmem_alloc(&tmem_slot, 512);
+  if (threadIdx.x < 32) tc::tmem_alloc<512>(&tmem_slot);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -1067,7 +1067,7 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_walkgrad_kernel(
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint32_t tmem_slot;
-  if (threadIdx.x < 32) tc::tmem_alloc(&tmem_slot, 512);  // both roles' columns
+  if (threadIdx.x < 32) tc::tmem_alloc<512>(&tmem_slot);  // both roles' columns
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();

@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(128) tc_selftest_kernel(const __nv_bfloat16* _
     tc::mbar_init(&bar, 1);
     tc::fence_barrier_init();
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_slot, 128);
+  if (warp == 0) tc::tmem_alloc<128>(&tmem_slot);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();

@@ -218,9 +218,13 @@ __device__ __forceinline__ void bulk_wait() {
 
 // ------------------------------------------------------------------ TMEM
 // Allocation is warp-wide (one warp calls it); writes the TMEM base address to *slot.
-__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+// Allocates kCols TMEM columns (a power of two, 32..512) for this CTA, written to *slot; the
+// column count is an immediate operand.
+template <uint32_t kCols>
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot) {
+  static_assert(kCols >= 32 && kCols <= 512 && (kCols & (kCols - 1)) == 0, "TMEM columns: power of two, 32..512");
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
-               "r"(ncols)
+               "n"(kCols)
                : "memory");
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
