@@ -18,6 +18,10 @@ The five named workloads are the chunked gated delta rule shapes of the benchmar
   varlen8       bf16, 8 sequences of U{256..8192} tokens packed by cu_seqlens, H=16, D=128
   long_t65536   bf16, B=1, T=65536, H=16, D=128, "VK" layout, g = logsigmoid(N(2, 1))
   gva_b4_t8192  bf16, B=4, T=8192, Hk=16, Hv=32, D=128, no initial/final state
+
+and two smaller cases with the same kernel choices, sized for profiler captures:
+long_t16384 (B=1, T=16384, otherwise long_t65536) and gva_b2_t4096 (B=2, T=4096, otherwise
+gva_b4_t8192).
 """
 from __future__ import annotations
 
@@ -54,6 +58,11 @@ WORKLOADS = {
     "long_t65536": Workload("long_t65536", torch.bfloat16, 1, 65536, 16, 16, 128, 128, "VK", True, True,
                             g_shift=2.0),
     "gva_b4_t8192": Workload("gva_b4_t8192", torch.bfloat16, 4, 8192, 16, 32, 128, 128, "KV", False, False),
+    # smaller cases of the same kernels' launch configurations, for profiler captures that must
+    # stay within a few GB of device memory
+    "long_t16384": Workload("long_t16384", torch.bfloat16, 1, 16384, 16, 16, 128, 128, "VK", True, True,
+                            g_shift=2.0),
+    "gva_b2_t4096": Workload("gva_b2_t4096", torch.bfloat16, 2, 4096, 16, 32, 128, 128, "KV", False, False),
 }
 
 
