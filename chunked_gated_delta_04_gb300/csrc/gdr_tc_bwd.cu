@@ -595,7 +595,8 @@ __device__ __forceinline__ void grad_body(
   // h: fp32 slabs (32 columns) -> bf16 operand slabs (64 columns) in place; thread = (row
   // tid & 127, column half tid >> 7).  bf16 slab s overwrites fp32 slab s, which only the
   // half-0 threads read before the barrier.  <dh', h> is accumulated on the way.
-  float hdh = 0.f;
+  // dot products below keep four partial sums (a quarter of one running sum's dependent adds)
+  float hdh4[4] = {0.f, 0.f, 0.f, 0.f};
   if (d.h_bf16) {  // h arrived as bf16 operand slabs: only <dh', h>
     const int hrow = tid & 127, hh = tid >> 7;
     float hv[64], dv_[64];
@@ -603,7 +604,7 @@ __device__ __forceinline__ void grad_body(
       ld_row_bf16(sm + S::H + hh * 16384, hrow, hv);
       ld_row_bf16(sm + S::DH + hh * 16384, hrow, dv_);
 #pragma unroll
-      for (int b = 0; b < 64; ++b) hdh += hv[b] * dv_[b];
+      for (int b = 0; b < 64; ++b) hdh4[b & 3] += hv[b] * dv_[b];
     }
   } else {
     const int hrow = tid & 127, hh = tid >> 7;
@@ -621,12 +622,12 @@ __device__ __forceinline__ void grad_body(
       }
       ld_row_bf16(sm + S::DH + hh * 16384, hrow, dv_);
 #pragma unroll
-      for (int b = 0; b < 64; ++b) hdh += hv[b] * dv_[b];
+      for (int b = 0; b < 64; ++b) hdh4[b & 3] += hv[b] * dv_[b];
     }
     __syncthreads();
     if (ok) st_row_bf16(sm + S::H + hh * 16384, hrow, hv);
   }
-  hdh = warp_sum(hdh);
+  float hdh = warp_sum((hdh4[0] + hdh4[1]) + (hdh4[2] + hdh4[3]));
   if (lane == 0) s_red[warp] = hdh;
   if (ok && lo) {  // O-hat = scale diag(e^gamma) dO, zero past the chunk end (half hf of row r)
     float x[64];
@@ -686,10 +687,10 @@ __device__ __forceinline__ void grad_body(
       st_row_bf16(sm + S::W + hf * kSlab, r, u);  // Vn~ (W no longer needed)
       tmem_ld64(tb, warp, 256 + hf * 64, x);     // (O-hat h^T)[r]
       ld_row_bf16(sm + S::KQ + kSlab + hf * 2 * kSlab, r, u);  // q_r
-      float qh = 0.f;
+      float qh4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int b = 0; b < 64; ++b) qh += x[b] * u[b];
-      s_qh[hf][r] = qh;
+      for (int b = 0; b < 64; ++b) qh4[b & 3] += x[b] * u[b];
+      s_qh[hf][r] = (qh4[0] + qh4[1]) + (qh4[2] + qh4[3]);
       tmem_ld64(tb, warp, 384 + hf * 64, x);  // -dW[r]
 #pragma unroll
       for (int b = 0; b < 64; ++b) x[b] = -x[b];
@@ -730,30 +731,31 @@ __device__ __forceinline__ void grad_body(
         gs[s] = sgam[32 * hf + s];
         qk[s] = scr[r * 65 + 32 * hf + s];
       }
-      float rowpp = 0.f;
+      float rowpp4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int s = 0; s < 32; ++s) {
         const int sc = 32 * hf + s;
         const float dp = (sc <= r && r < len) ? d.scale * x[s] * fexp(gr - gs[s]) : 0.f;
         x[s] = dp;
         qk[s] *= dp;
-        rowpp += qk[s];
+        rowpp4[s & 3] += qk[s];
       }
+      const float rowpp = (rowpp4[0] + rowpp4[1]) + (rowpp4[2] + rowpp4[3]);
 #pragma unroll
       for (int s = 0; s < 32; ++s) scr[r * 65 + 32 * hf + s] = qk[s];
       st_halfrow_bf16(sm + S::DP, r, hf, x);  // dP (h no longer needed)
       s_rowpp[hf][r] = rowpp;
     }
-    float kdv = 0.f;
+    float kdv4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
     for (int q = 0; q < 2; ++q) {  // (K dh')[r] . Vn[r] over columns [64 hf + 32 q, +32)
       float x[32], v[32];
       tmem_ld32w(tb, warp, 128 + 64 * hf + 32 * q, x);
       ld_halfrow_bf16(sm + S::VN + hf * kSlab, r, q, v);
 #pragma unroll
-      for (int b = 0; b < 32; ++b) kdv += x[b] * v[b];
+      for (int b = 0; b < 32; ++b) kdv4[b & 3] += x[b] * v[b];
     }
-    s_kdv[hf][r] = kdv;
+    s_kdv[hf][r] = (kdv4[0] + kdv4[1]) + (kdv4[2] + kdv4[3]);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
@@ -853,15 +855,15 @@ __device__ __forceinline__ void grad_body(
     {  // dv = diag(beta) dB_v, columns [64 hf, +64)
       float x[64], y[64];
       const float br = s_beta[r];
-      float dbv = 0.f;
+      float dbv4[4] = {0.f, 0.f, 0.f, 0.f};
       tmem_ld64(tb, warp, 128 + hf * 64, x);  // dB_v[r]
       ld_row_bf16(sm + S::V + hf * kSlab, r, y);
 #pragma unroll
       for (int b = 0; b < 64; ++b) {
-        dbv += x[b] * y[b];
+        dbv4[b & 3] += x[b] * y[b];
         x[b] *= br;
       }
-      s_dbv[hf][r] = dbv;
+      s_dbv[hf][r] = (dbv4[0] + dbv4[1]) + (dbv4[2] + dbv4[3]);
       if (len == 64)
         st_row_bf16(sm + S::DVS + hf * kSlab, r, x);
       else if (r < len)
@@ -898,7 +900,7 @@ __device__ __forceinline__ void grad_body(
   GDR_TRACE_MARK(2, 10);
   if (ok && lo) {  // columns [32 hf, +32)
     const float br = s_beta[r];
-    float x[32], gs[32], kk[32], akk = 0.f, rowaa = 0.f;
+    float x[32], gs[32], kk[32], akk4[4] = {0.f, 0.f, 0.f, 0.f}, rowaa4[4] = {0.f, 0.f, 0.f, 0.f};
     tmem_ld32w(tb, warp, 64 + 32 * hf, x);   // (T^T dT T^T)[r]
     tmem_ld32w(tb, warp, 32 * hf, kk);       // K K^T row r
 #pragma unroll
@@ -909,16 +911,16 @@ __device__ __forceinline__ void grad_body(
       // exp(gamma_r - gamma_s) only below the diagonal: above it the exponent is
       // positive and can overflow, and 0 * inf would give NaN
       const float dag = (sc < r && r < len) ? -x[s] * fexp(gr - gs[s]) : 0.f;
-      akk += dag * kk[s];
+      akk4[s & 3] += dag * kk[s];
       x[s] = br * dag;
       kk[s] *= x[s];  // dA * A with A = beta_r Gam K K^T
-      rowaa += kk[s];
+      rowaa4[s & 3] += kk[s];
     }
 #pragma unroll
     for (int s = 0; s < 32; ++s) scr[r * 65 + 32 * hf + s] = kk[s];
     st_halfrow_bf16(sm + S::DAG, r, hf, x);
-    s_akk[hf][r] = akk;
-    s_rowaa[hf][r] = rowaa;
+    s_akk[hf][r] = (akk4[0] + akk4[1]) + (akk4[2] + akk4[3]);
+    s_rowaa[hf][r] = (rowaa4[0] + rowaa4[1]) + (rowaa4[2] + rowaa4[3]);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
