@@ -356,20 +356,26 @@ __global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
 struct GradSmem {
   static constexpr uint32_t KQ = 0;             // [K | Q] x 2 slabs (32 KB), to the end
   static constexpr uint32_t DO = 32768;         // dO (16 KB) -> dk staging
-  static constexpr uint32_t W = 49152;          // W (16 KB) -> Vn~ -> dv staging
-  static constexpr uint32_t DVN = 65536;        // dVn (16 KB), to the WY backward
+  // O-hat = scale diag(e^gamma) dO and dVn interleaved by 64-column slab (slab s of O-hat at
+  // OD + 16 KB s, of dVn 8 KB after it), so [O-hat; dVn] is one 128-row K-major operand
+  // (32 KB); O-hat -> V after the first product, dVn to the WY backward
+  static constexpr uint32_t OD = 49152;
   static constexpr uint32_t DH = 81920;         // dh' (32 KB) -> dq staging
-  static constexpr uint32_t H = 114688;         // h fp32 lands in H|VN|OH (64 KB); h bf16 (32 KB)
-                                                //   -> dP | dT | X | dAGb (8 KB each)
+  static constexpr uint32_t H = 114688;         // h bf16 (32 KB) -> dP | dT | X | dAGb (8 KB each);
+                                                //   h fp32 lands in H, H + 16 KB, VN and SCR
   static constexpr uint32_t VN = 147456;        // Vn (16 KB) -> T'
-  static constexpr uint32_t OH = 163840;        // scale diag(e^gamma) dO (16 KB) -> V
+  static constexpr uint32_t W = 163840;         // W (16 KB) -> Vn~ -> dv staging
   static constexpr uint32_t UT = 180224;        // U (16 KB) -> dW
   static constexpr uint32_t SCR = 196608;       // fp32 [64][65] scratch for row/column sums
   static constexpr uint32_t GAM = SCR + 16640;  // gamma (256 B)
   static constexpr uint32_t BYTES = GAM + 256;
-  // V and T are fetched right after P2 into the O-hat tile and the last 8 KB of H (T is
+  static constexpr uint32_t OD_SLAB = 16384;    // slab stride of O-hat, dVn and V
+  // V and T are fetched right after P2 into the O-hat slabs and the last 8 KB of H (T is
   // last read by the X T^T product, before dAGb is written there)
-  static constexpr uint32_t V = OH, T = H + 24576, DP = H, DT = H + 8192, XT = H + 16384, DAG = H + 24576;
+  static constexpr uint32_t OH = OD, DVN = OD + 8192, V = OD;
+  static constexpr uint32_t T = H + 24576, DP = H, DT = H + 8192, XT = H + 16384, DAG = H + 24576;
+  // fp32 h slab k (32 columns of 128 rows, 16 KB)
+  static constexpr uint32_t hf32(int k) { return k < 3 ? H + (uint32_t)k * 16384 : SCR; }
   static constexpr uint32_t TP = VN, DQS = DH, DVS = W, DKS = DO, DW = UT;
 };
 
@@ -474,7 +480,7 @@ __device__ __forceinline__ void grad_body(
         tc::tma_load_2d(sm + S::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
                         (int)(ch2 * 128 + (q4 & 1) * 64));
       tc::tma_load_2d(sm + S::DVN, &tm_dvn, bar, 0, (int)(ch2 * 64));
-      tc::tma_load_2d(sm + S::DVN + kSlab, &tm_dvn, bar, 64, (int)(ch2 * 64));
+      tc::tma_load_2d(sm + S::DVN + S::OD_SLAB, &tm_dvn, bar, 64, (int)(ch2 * 64));
     }
     if (groups & kLdW) {
       tc::tma_load_2d(sm + S::W, &tm_w, bar, 0, (int)(ch2 * 64));
@@ -492,9 +498,9 @@ __device__ __forceinline__ void grad_body(
         for (int q4 = 0; q4 < 4; ++q4)
           tc::tma_load_2d(sm + S::H + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_h, bar, (q4 >> 1) * 64,
                           (int)(ch2 * 128 + (q4 & 1) * 64));
-      } else {  // h (fp32) as four 32-column slabs of 128 rows over H|VN|OH, converted in place
+      } else {  // h (fp32) as four 32-column slabs of 128 rows, converted into H
         for (int q4 = 0; q4 < 4; ++q4)
-          tc::tma_load_2d(sm + S::H + q4 * 16384, &tm_h, bar, q4 * 32, (int)(ch2 * 128));
+          tc::tma_load_2d(sm + S::hf32(q4), &tm_h, bar, q4 * 32, (int)(ch2 * 128));
       }
     }
     if (groups & kLdDo) {
@@ -612,7 +618,7 @@ __device__ __forceinline__ void grad_body(
     if (ok) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const unsigned char* src = sm + S::H + (2 * hh + q) * 16384 + hrow * 128;
+        const unsigned char* src = sm + S::hf32(2 * hh + q) + hrow * 128;
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
           const float4 f = *reinterpret_cast<const float4*>(src + (((c4 ^ (hrow & 7)) & 7) << 4));
@@ -635,20 +641,20 @@ __device__ __forceinline__ void grad_body(
     ld_row_bf16(sm + S::DO + hf * kSlab, r, x);
 #pragma unroll
     for (int b = 0; b < 64; ++b) x[b] *= e;
-    st_row_bf16(sm + S::OH + hf * kSlab, r, x);
+    st_row_bf16(sm + S::OH + hf * S::OD_SLAB, r, x);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   hdh = ((s_red[0] + s_red[1]) + (s_red[2] + s_red[3])) + ((s_red[4] + s_red[5]) + (s_red[6] + s_red[7]));
   GDR_TRACE_MARK(2, 1);
-  // P2: [K;Q] K^T (0-63), W h (64-191), O-hat h^T -> dq (256-383), dVn h^T = -dW (384-511)
+  // P2: [K;Q] K^T (0-63), W h (64-191), [O-hat; dVn] h^T (256-383): lanes 0-63 start dq,
+  // lanes 64-127 are dVn h^T = -dW
   if (ok && tid == 0) {
     tc::tc_fence_after();
     tc::gemm(C_KK, kmaj(sm + S::KQ, 2 * kSlab), kmaj(sm + S::KQ, 2 * kSlab), 64, 8, false);
     tc::gemm(tb + 64, kmaj(sm + S::W, kSlab), mnmaj(sm + S::H, 16384), 128, 8, false);
-    tc::gemm(C_DQ, kmaj(sm + S::OH, kSlab), kmaj(sm + S::H, 16384), 128, 8, false);
-    tc::gemm(C_DK, kmaj(sm + S::DVN, kSlab), kmaj(sm + S::H, 16384), 128, 8, false);
+    tc::gemm(C_DQ, kmaj(sm + S::OD, S::OD_SLAB), kmaj(sm + S::H, 16384), 128, 8, false);
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
@@ -657,7 +663,7 @@ __device__ __forceinline__ void grad_body(
   if (ok && tid == kCopyTid) {  // O-hat and h are consumed: fetch V and T for the WY backward
     tc::mbar_arrive_expect_tx(&bar_tma2, 3 * kSlab);
     tc::tma_load_3d(sm + S::V, &tm_v, &bar_tma2, 0, j, t0);
-    tc::tma_load_3d(sm + S::V + kSlab, &tm_v, &bar_tma2, 64, j, t0);
+    tc::tma_load_3d(sm + S::V + S::OD_SLAB, &tm_v, &bar_tma2, 64, j, t0);
     tc::tma_load_2d(sm + S::T, &tm_t, &bar_tma2, 0, (int)(ch * 64));
   }
   float* scr = reinterpret_cast<float*>(sm + S::SCR);
@@ -691,10 +697,6 @@ __device__ __forceinline__ void grad_body(
 #pragma unroll
       for (int b = 0; b < 64; ++b) qh4[b & 3] += x[b] * u[b];
       s_qh[hf][r] = (qh4[0] + qh4[1]) + (qh4[2] + qh4[3]);
-      tmem_ld64(tb, warp, 384 + hf * 64, x);  // -dW[r]
-#pragma unroll
-      for (int b = 0; b < 64; ++b) x[b] = -x[b];
-      st_row_bf16(sm + S::DW + hf * kSlab, r, x);  // own U row half already consumed
     } else {  // Q K^T row r, columns [32 hf, 32 hf + 32) -> scratch (fp32)
       float x[32];
       tmem_ld32w(tb, warp, 32 * hf, x);
@@ -714,6 +716,16 @@ __device__ __forceinline__ void grad_body(
     tc::gemm(C_DK, kmaj(sm + S::W, kSlab), kmaj(sm + S::DH, 16384), 128, 8, false);
     tc::mma_commit(&bar_mma);
   }
+  if (ok && !lo) {  // while P4 runs: -dW from lanes 64-127 of the stacked product into U's tile,
+                    // whose readers finished before the barrier above (row r, half hf)
+    tc::tc_fence_after();
+    float x[64];
+    tmem_ld64(tb, warp, 256 + hf * 64, x);
+#pragma unroll
+    for (int b = 0; b < 64; ++b) x[b] = -x[b];
+    st_row_bf16(sm + S::DW + hf * kSlab, r, x);
+  }
+  tc::fence_proxy_async_smem();
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   if (kDyn && tid == kCopyTid) pre_c = pre_w < n_items ? chunk_of(pre_w) : 0;  // used after R2
@@ -775,7 +787,7 @@ __device__ __forceinline__ void grad_body(
     tc::gemm(C_DQ, kmaj(sm + S::DP, kSlab), mnmaj(sm + S::KQ, 2 * kSlab), 128, 4, true);
     tc::gemm(C_DK, mnmaj(sm + S::DP, kSlab), mnmaj(sm + S::KQ + kSlab, 2 * kSlab), 128, 4, true);
     tc::gemm(tb + 64, kmaj(sm + S::DW, kSlab), kmaj(sm + S::KQ, 2 * kSlab), 64, 8, false);
-    tc::gemm(tb + 128, kmaj(sm + S::DVN, kSlab), kmaj(sm + S::V, kSlab), 64, 8, false);
+    tc::gemm(tb + 128, kmaj(sm + S::DVN, S::OD_SLAB), kmaj(sm + S::V, S::OD_SLAB), 64, 8, false);
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
@@ -828,7 +840,7 @@ __device__ __forceinline__ void grad_body(
   }
   if (ok && tid == 0) {
     tc::tc_fence_after();
-    tc::gemm(tb + 128, mnmaj(sm + S::T, kSlab), mnmaj(sm + S::DVN, kSlab), 128, 4, false);
+    tc::gemm(tb + 128, mnmaj(sm + S::T, kSlab), mnmaj(sm + S::DVN, S::OD_SLAB), 128, 4, false);
     tc::gemm(tb + 64, mnmaj(sm + S::T, kSlab), mnmaj(sm + S::DT, kSlab), 64, 4, false);
     tc::mma_commit(&bar_mma);
   }
@@ -857,7 +869,7 @@ __device__ __forceinline__ void grad_body(
       const float br = s_beta[r];
       float dbv4[4] = {0.f, 0.f, 0.f, 0.f};
       tmem_ld64(tb, warp, 128 + hf * 64, x);  // dB_v[r]
-      ld_row_bf16(sm + S::V + hf * kSlab, r, y);
+      ld_row_bf16(sm + S::V + hf * S::OD_SLAB, r, y);
 #pragma unroll
       for (int b = 0; b < 64; ++b) {
         dbv4[b & 3] += x[b] * y[b];
