@@ -708,10 +708,11 @@ __device__ __forceinline__ void grad_body(
   tc::tc_fence_before();
   __syncthreads();
   GDR_TRACE_MARK(2, 3);
-  // P4: dO Vn^T (64-127), K dh' (128-255), dk = Vn~ dh'^T (384-511)
+  // P4: dO Vn^T (64-127, lanes 64-127: the operand's rows start one slab early, so dP is the
+  // other lane half's epilogue), K dh' (128-255), dk = Vn~ dh'^T (384-511)
   if (ok && tid == 0) {
     tc::tc_fence_after();
-    tc::gemm(tb + 64, kmaj(sm + S::DO, kSlab), kmaj(sm + S::VN, kSlab), 64, 8, false);
+    tc::gemm(tb + 64, kmaj(sm + S::DO - kSlab, kSlab), kmaj(sm + S::VN, kSlab), 64, 8, false);
     tc::gemm(tb + 128, kmaj(sm + S::KQ, 2 * kSlab), mnmaj(sm + S::DH, 16384), 128, 8, false);
     tc::gemm(C_DK, kmaj(sm + S::W, kSlab), kmaj(sm + S::DH, 16384), 128, 8, false);
     tc::mma_commit(&bar_mma);
@@ -734,8 +735,8 @@ __device__ __forceinline__ void grad_body(
     tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&bar_kfree), peer));
   }
   GDR_TRACE_MARK(2, 4);
-  if (ok && lo) {
-    {  // dP and dP * QK for columns [32 hf, 32 hf + 32)
+  if (ok && !lo) {  // lanes 64-127: dP and dP * QK for row r, columns [32 hf, 32 hf + 32)
+    {
       float x[32], gs[32], qk[32];
       tmem_ld32w(tb, warp, 64 + 32 * hf, x);  // (dO Vn^T)[r]
 #pragma unroll
@@ -758,6 +759,8 @@ __device__ __forceinline__ void grad_body(
       st_halfrow_bf16(sm + S::DP, r, hf, x);  // dP (h no longer needed)
       s_rowpp[hf][r] = rowpp;
     }
+  }
+  if (ok && lo) {  // lanes 0-63 meanwhile
     float kdv4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
     for (int q = 0; q < 2; ++q) {  // (K dh')[r] . Vn[r] over columns [64 hf + 32 q, +32)
@@ -781,18 +784,37 @@ __device__ __forceinline__ void grad_body(
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_tma2, item_par, ws.status, kDevErrTimeoutBwd));
   GDR_TRACE_MARK(2, 5);
-  // P6: dq += dP K, dk += dP^T Q, dW K^T (64-127), dVn V^T (128-191)
+  // P6: dq += dP K, dk += dP^T Q; on lanes 64-127 (operand rows shifted by one slab: [.; dW]
+  // and [V; dVn]) dW K^T (64-127) and dVn V^T (128-191)
   if (ok && tid == 0) {
     tc::tc_fence_after();
     tc::gemm(C_DQ, kmaj(sm + S::DP, kSlab), mnmaj(sm + S::KQ, 2 * kSlab), 128, 4, true);
     tc::gemm(C_DK, mnmaj(sm + S::DP, kSlab), mnmaj(sm + S::KQ + kSlab, 2 * kSlab), 128, 4, true);
-    tc::gemm(tb + 64, kmaj(sm + S::DW, kSlab), kmaj(sm + S::KQ, 2 * kSlab), 64, 8, false);
-    tc::gemm(tb + 128, kmaj(sm + S::DVN, S::OD_SLAB), kmaj(sm + S::V, S::OD_SLAB), 64, 8, false);
+    tc::gemm(tb + 64, kmaj(sm + S::DW - kSlab, kSlab), kmaj(sm + S::KQ, 2 * kSlab), 64, 8, false);
+    tc::gemm(tb + 128, kmaj(sm + S::OD, S::OD_SLAB), kmaj(sm + S::V, S::OD_SLAB), 64, 8, false);
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 6);
+  if (ok && !lo) {
+    // lanes 64-127, row r: dT = dW B_k^T + dVn B_v^T = (dW K^T) diag(beta e^gamma) + (dVn V^T)
+    // diag(beta); T * (dW K^T) for <dB_k[s], k_s> = sum_m T[m][s] (dW K^T)[m][s]; columns [32 hf, +32)
+    float x[32], y[32], tr[32];
+    tmem_ld32w(tb, warp, 64 + 32 * hf, x);
+    tmem_ld32w(tb, warp, 128 + 32 * hf, y);
+    ld_halfrow_bf16(sm + S::T, r, hf, tr);
+#pragma unroll
+    for (int s = 0; s < 32; ++s) {
+      const int sc = 32 * hf + s;
+      const float be = s_beta[sc] * s_eg[sc];
+      scr[r * 65 + sc] = tr[s] * x[s];
+      y[s] = (r < len && sc < len) ? be * x[s] + s_beta[sc] * y[s] : 0.f;
+      tr[s] *= be;  // T' = T diag(beta e^gamma)
+    }
+    st_halfrow_bf16(sm + S::DT, r, hf, y);
+    st_halfrow_bf16(sm + S::TP, r, hf, tr);
+  }
   if (kPair) ok = pair_reduce(256, S::DH, &bar_qfree, &bar_qdata, dq, ok);  // dq; DH receives
   if (ok && lo) {
     if (!kPair) {  // dq columns [64 hf, +64) (final for one v-head per q/k head)
@@ -810,29 +832,14 @@ __device__ __forceinline__ void grad_body(
         st_global_bf16x64(dq + ((size_t)(t0 + r) * d.Hk + i) * 128 + hf * 64, x);
       }
     }
-    // dT = dW B_k^T + dVn B_v^T = (dW K^T) diag(beta e^gamma) + (dVn V^T) diag(beta);
-    // T * (dW K^T) (row r) for <dB_k[s], k_s> = sum_m T[m][s] (dW K^T)[m][s]; columns [32 hf, +32)
-    float x[32], y[32], tr[32];
-    tmem_ld32w(tb, warp, 64 + 32 * hf, x);
-    tmem_ld32w(tb, warp, 128 + 32 * hf, y);
-    ld_halfrow_bf16(sm + S::T, r, hf, tr);
-#pragma unroll
-    for (int s = 0; s < 32; ++s) {
-      const int sc = 32 * hf + s;
-      const float be = s_beta[sc] * s_eg[sc];
-      scr[r * 65 + sc] = tr[s] * x[s];
-      y[s] = (r < len && sc < len) ? be * x[s] + s_beta[sc] * y[s] : 0.f;
-      tr[s] *= be;  // T' = T diag(beta e^gamma)
-    }
-    st_halfrow_bf16(sm + S::DT, r, hf, y);
-    st_halfrow_bf16(sm + S::TP, r, hf, tr);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   if (ok) col_partial(s_colbk);
   GDR_TRACE_MARK(2, 7);
-  // R2: T^T dVn = dB_v (128-255), X = T^T dT (64-127)
+  // R2: T^T dVn = dB_v (128-255), X = T^T dT (64-127, lanes 64-127: T^T's M atoms start one
+  // slab early)
   if (ok && tid == kCopyTid && !kGroup && len == 64) {
     tc::tma_store_3d(&tm_dq, sm + S::DQS, 0, i, t0);
     tc::tma_store_3d(&tm_dq, sm + S::DQS + kSlab, 64, i, t0);
@@ -841,7 +848,7 @@ __device__ __forceinline__ void grad_body(
   if (ok && tid == 0) {
     tc::tc_fence_after();
     tc::gemm(tb + 128, mnmaj(sm + S::T, kSlab), mnmaj(sm + S::DVN, S::OD_SLAB), 128, 4, false);
-    tc::gemm(tb + 64, mnmaj(sm + S::T, kSlab), mnmaj(sm + S::DT, kSlab), 64, 4, false);
+    tc::gemm(tb + 64, mnmaj(sm + S::T - kSlab, kSlab), mnmaj(sm + S::DT, kSlab), 64, 4, false);
     tc::mma_commit(&bar_mma);
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
@@ -881,8 +888,10 @@ __device__ __forceinline__ void grad_body(
       else if (r < len)
         st_global_bf16x64(dv + ((size_t)(t0 + r) * Hv + j) * 128 + hf * 64, x);
     }
+  }
+  if (ok && !lo) {  // lanes 64-127 meanwhile: X = T^T dT, row r, columns [32 hf, +32)
     float x[32];
-    tmem_ld32w(tb, warp, 64 + 32 * hf, x);  // X = T^T dT, columns [32 hf, +32)
+    tmem_ld32w(tb, warp, 64 + 32 * hf, x);
     st_halfrow_bf16(sm + S::XT, r, hf, x);
   }
   tc::fence_proxy_async_smem();
