@@ -250,12 +250,12 @@ __device__ __forceinline__ void solve_unit_lower64(const float* __restrict__ sA,
 }
 
 // Publishes one finished chunk-head of the fused forward: its TMA stores (async proxy) and
-// gamma (plain stores before the caller's barrier) are complete; make them visible at GPU scope
-// before the flag.
+// gamma (plain stores before the caller's barrier) are complete; order them before the flag
+// (proxy fence) and set it with a GPU-scope release reduction (pairs with the waiter's acquire
+// load; cheaper than a full fence).
 __device__ __forceinline__ void publish_prep(uint32_t* flag) {
   asm volatile("fence.proxy.async.global;" ::: "memory");
-  __threadfence();
-  atomicAdd(flag, 1u);
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(flag) : "memory");
 }
 
 // Bounded wait until *flag != 0 (acquire at GPU scope), then orders the caller's later TMA

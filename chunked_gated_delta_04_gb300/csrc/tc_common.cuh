@@ -18,6 +18,22 @@ namespace tcx {
 #endif
 static __device__ unsigned long long g_gdr_trace[8][32];
 static __device__ unsigned long long g_gdr_cta_span[1024][3];  // per CTA: start, end (ns), SM id
+// per CTA, free-form timeline slots (globaltimer ns or counts), written by GDR_TRACE_INFO
+static __device__ unsigned long long g_gdr_cta_info[1024][8];
+#define GDR_TRACE_NOW()                                              \
+  ([]() {                                                            \
+    unsigned long long t_;                                           \
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));          \
+    return t_;                                                       \
+  }())
+#define GDR_TRACE_INFO_SET(slot, v)                                  \
+  do {                                                               \
+    if (blockIdx.x < 1024) g_gdr_cta_info[blockIdx.x][slot] = (v);   \
+  } while (0)
+#define GDR_TRACE_INFO_ADD(slot, v)                                  \
+  do {                                                               \
+    if (blockIdx.x < 1024) atomicAdd(&g_gdr_cta_info[blockIdx.x][slot], (unsigned long long)(v)); \
+  } while (0)
 #define GDR_TRACE_CTA_BEGIN()                                                                      \
   do {                                                                                             \
     if (threadIdx.x == 0 && blockIdx.x < 1024) {                                                   \
@@ -58,6 +74,13 @@ static __device__ unsigned long long g_gdr_cta_span[1024][3];  // per CTA: start
     if (blockIdx.x == GDR_TRACE_BLOCK) atomicAdd(&g_gdr_trace[kid][slot], clock64() - (var));     \
   } while (0)
 #else
+#define GDR_TRACE_NOW() 0ull
+#define GDR_TRACE_INFO_SET(slot, v) \
+  do {                              \
+  } while (0)
+#define GDR_TRACE_INFO_ADD(slot, v) \
+  do {                              \
+  } while (0)
 #define GDR_TRACE_CTA_BEGIN() \
   do {                        \
   } while (0)
