@@ -172,19 +172,23 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
   uint32_t mma_phase = 0;
   int prev1 = -1, prev2 = -1;  // kPublish: the last two chunks, whose stores may be in flight
   GDR_TRACE_INIT();
-  for (int it = 0; c_end - 1 - it >= c_begin && ok; ++it) {
-    const int c = c_end - 1 - it, st = it & 1;
-    const uint32_t ld_phase = (it >> 1) & 1;
-    const int len = min(64, L - (c - c_begin) * 64);
-    const size_t chh = (size_t)c * Hv + j;
-    // dh' as the B operand: slab CPT hf / 64 holds columns [64 s, 64 s + 64) of the slice
+  // dh' as the B operand: slab CPT hf / 64 holds columns [64 s, 64 s + 64) of the slice; written
+  // here for the first chunk and at the end of each chunk for the next
+  auto stage_dh = [&]() {
     if constexpr (NC == 64)
       st_halfrow_bf16(sm + WS::DH, dk, hf, dh);
     else
       st_row_bf16(sm + WS::DH + hf * 16384, dk, dh);
     tc::fence_proxy_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
+  };
+  stage_dh();
+  tc::tc_fence_before();
+  __syncthreads();
+  for (int it = 0; c_end - 1 - it >= c_begin && ok; ++it) {
+    const int c = c_end - 1 - it, st = it & 1;
+    const uint32_t ld_phase = (it >> 1) & 1;
+    const int len = min(64, L - (c - c_begin) * 64);
+    const size_t chh = (size_t)c * Hv + j;
     if (tid == kCopyTid) {  // dh' of this chunk -> workspace, straight from the operand tile
 #pragma unroll
       for (int sl = 0; sl < NSL; ++sl) tc::tma_store_2d(&tm_dhs, sm + WS::DH + sl * 16384, dv0 + 64 * sl, (int)(chh * 128));
@@ -276,6 +280,9 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       tc::bulk_commit();
     }
     GDR_TRACE_MARK(3, 4);
+    // this chunk's dh' store has left the operand tile (only the dVn group may still read):
+    // the tile takes the next chunk's dh' right after the update below
+    if (tid == kCopyTid) tc::bulk_wait_read<1>();
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutBwd));
     mma_phase ^= 1;
     tc::tc_fence_after();
@@ -291,9 +298,9 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
 #pragma unroll
         for (int b = 0; b < 32; ++b) dh[32 * q + b] = eC * dh[32 * q + b] + d.scale * y[b] - x[b];
       }
+      stage_dh();  // the next chunk's dh' operand (one barrier for both)
     }
     if (tid == kCopyTid) {
-      tc::bulk_wait_read<1>();  // this chunk's dh' store has left the operand tile
       if (kPublish) {  // the stores of two chunks ago have had two chunks to land
         if (prev2 >= 0) {
           tc::bulk_wait<4>();
