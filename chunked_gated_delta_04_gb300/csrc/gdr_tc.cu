@@ -743,10 +743,10 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     const int t0 = t_seq + it * 64;
     const int len = min(64, L - it * 64);
     const size_t chh = (size_t)c * Hv + j;
-    // h^T (bf16 B operand) was written at the end of the previous chunk / before the loop
+    // h^T (bf16 B operand) was written at the end of the previous chunk / before the loop; one
+    // barrier publishes it and this chunk's tiles
     tc::fence_proxy_async_smem();
     tc::tc_fence_before();
-    __syncthreads();
     GDR_TRACE_MARK(1, 0);
     ok = __syncthreads_and(tc::mbar_wait(&bar_load[st], ld_phase, ws.status, kDevErrTimeoutFwd));
     GDR_TRACE_MARK(1, 1);
