@@ -14,6 +14,9 @@ namespace gdr {
 
 constexpr int kIndexThreads = 1024;
 constexpr int kMaxOrderedSeqs = kMaxFusedSeqs;  // above this the order is the identity
+// Offsets, order and step table up to this size are also kept in shared memory, so the binary
+// searches below read them there instead of making dependent global round trips.
+constexpr int kSmemCap = 2048;
 
 __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t* __restrict__ cu,
                                                                   int num_seqs, int T, int max_chunks,
@@ -27,7 +30,11 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
   __shared__ int warp_tot[32];
   __shared__ int s_bad;
   __shared__ int s_carry;
+  __shared__ int s_off[kSmemCap + 1], s_order[kSmemCap], s_step[kSmemCap + 1];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool small_n = num_seqs + 1 <= kSmemCap;  // off and order mirrored in shared memory
+  auto OFF = [&](int n) { return small_n ? s_off[n] : off[n]; };
+  auto ORD = [&](int r) { return small_n ? s_order[r] : order[r]; };
   if (tid == 0) {
     for (int w = 0; w < 64; ++w) status[w] = 0u;  // fresh status for this call
     s_bad = 0;
@@ -74,7 +81,10 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
     __syncthreads();
     const int carry = s_carry;
     const int incl = x + (warp > 0 ? warp_tot[warp - 1] : 0);
-    if (n < num_seqs) off[n] = carry + incl - nc;
+    if (n < num_seqs) {
+      off[n] = carry + incl - nc;
+      if (small_n) s_off[n] = carry + incl - nc;
+    }
     __syncthreads();
     if (tid == kIndexThreads - 1) s_carry = carry + incl;
     __syncthreads();
@@ -84,7 +94,10 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
     if (tid == 0) status[0] |= kDevErrBadCuSeqlens;
     total = 0;
   }
-  if (tid == 0) off[num_seqs] = total;
+  if (tid == 0) {
+    off[num_seqs] = total;
+    if (small_n) s_off[num_seqs] = total;
+  }
   __syncthreads();
 
   for (int c = tid; c < max_chunks; c += kIndexThreads) {
@@ -93,12 +106,12 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
       int lo = 0, hi = num_seqs - 1;  // last n with off[n] <= c
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (off[mid] <= c) lo = mid; else hi = mid - 1;
+        if (OFF(mid) <= c) lo = mid; else hi = mid - 1;
       }
       const int n = lo;
       const int start = cu ? cu[n] : n * T;
       const int L = cu ? cu[n + 1] - cu[n] : T;
-      const int local = c - off[n];
+      const int local = c - OFF(n);
       const int len = min(kChunk, L - local * kChunk);
       ci = make_int4(n, start + local * kChunk, len, local);
     }
@@ -115,9 +128,13 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
         rank += (Lm > Ln) || (Lm == Ln && m < n);
       }
       order[rank] = n;
+      if (small_n) s_order[rank] = n;
     }
   } else {
-    for (int n = tid; n < num_seqs; n += kIndexThreads) order[n] = n;
+    for (int n = tid; n < num_seqs; n += kIndexThreads) {
+      order[n] = n;
+      if (small_n) s_order[n] = n;
+    }
   }
 
   // Step table of the fused kernels (step_off != nullptr; requires the sorted order), in the
@@ -132,8 +149,10 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
     if (tid == 0) step_off[0] = step_off[max_chunks + 1] = 0;
   } else if (step_off != nullptr) {
     __syncthreads();
-    auto nc_of_rank = [&](int r) { return off[order[r] + 1] - off[order[r]]; };
+    auto nc_of_rank = [&](int r) { return OFF(ORD(r) + 1) - OFF(ORD(r)); };
     const int S = num_seqs > 0 ? nc_of_rank(0) : 0;
+    const bool small_s = S + 1 <= kSmemCap;  // step table mirrored in shared memory
+    auto STEP = [&](int st) { return small_s ? s_step[st] : step_off[st]; };
     for (int st = tid; st < S; st += kIndexThreads) {  // cnt(st): first rank with nc <= st
       int lo = 0, hi = num_seqs;
       while (lo < hi) {
@@ -141,17 +160,19 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
         if (nc_of_rank(mid) > st) lo = mid + 1; else hi = mid;
       }
       step_off[st + 1] = lo;
+      if (small_s) s_step[st + 1] = lo;
     }
     __syncthreads();
     if (tid == 0) {
       step_off[0] = 0;
+      if (small_s) s_step[0] = 0;
       step_off[max_chunks + 1] = S;
       s_carry = 0;
     }
     __syncthreads();
     for (int base = 1; base <= S; base += kIndexThreads) {  // inclusive scan of step_off[1..S]
       const int st = base + tid;
-      int x = st <= S ? step_off[st] : 0;
+      int x = st <= S ? STEP(st) : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -171,23 +192,26 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
       __syncthreads();
       const int carry = s_carry;
       const int incl = x + (warp > 0 ? warp_tot[warp - 1] : 0);
-      if (st <= S) step_off[st] = carry + incl;
+      if (st <= S) {
+        step_off[st] = carry + incl;
+        if (small_s) s_step[st] = carry + incl;
+      }
       __syncthreads();
       if (tid == kIndexThreads - 1) s_carry = carry + incl;
       __syncthreads();
     }
     // the chunk of every queue position, so a claimed item decodes with one load: reverse
     // step s of the backward walk is local chunk nc - 1 - s, forward step s local chunk s
-    const int n_q = step_off[S];
+    const int n_q = STEP(S);
     for (int q = tid; q < n_q; q += kIndexThreads) {
       int lo = 0, hi = S - 1;  // last step s with step_off[s] <= q
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (step_off[mid] <= q) lo = mid; else hi = mid - 1;
+        if (STEP(mid) <= q) lo = mid; else hi = mid - 1;
       }
-      const int n = order[q - step_off[lo]];
-      if (grad_chunk) grad_chunk[q] = off[n + 1] - 1 - lo;
-      if (fwd_chunk) fwd_chunk[q] = off[n] + lo;
+      const int n = ORD(q - STEP(lo));
+      if (grad_chunk) grad_chunk[q] = OFF(n + 1) - 1 - lo;
+      if (fwd_chunk) fwd_chunk[q] = OFF(n) + lo;
     }
   }
 }
