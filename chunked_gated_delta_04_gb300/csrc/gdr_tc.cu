@@ -658,7 +658,9 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     for (int b = 0; b < 32; ++b)
       h[b] = S0 ? S0[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] : 0.f;
   }
-  auto issue_loads = [&](int c, int st) {  // two stages: every tile of chunk c
+  // two stages: every tile of chunk c into stage st; U and P last, once the P Vn of chunk
+  // it_prev (the stage's previous user, -1: none), their last reader, is done (bar_pv)
+  auto issue_loads = [&](int c, int st, int it_prev) {
     const int tc0 = t_seq + (c - c_begin) * 64;
     const size_t chh = (size_t)c * Hv + j;
     unsigned char* base = sm + st * SS::STAGE;
@@ -670,6 +672,8 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     tc::tma_load_3d(base + SS::WQ + 3 * kSlab, &tm_q, &bar_load[st], 64, i, tc0);
     tc::tma_load_3d(base + SS::K, &tm_k, &bar_load[st], 0, i, tc0);
     tc::tma_load_3d(base + SS::K + kSlab, &tm_k, &bar_load[st], 64, i, tc0);
+    // (on a timeout the tiles stay out and the consumers' own bounded wait ends the chain)
+    if (it_prev >= 0 && !tc::mbar_wait(&bar_pv, (uint32_t)it_prev & 1u, ws.status, kDevErrTimeoutFwd)) return;
     tc::tma_load_2d(base + SS::U, &tm_u, &bar_load[st], dv0 & 64, (int)(chh * 64));  // 64-col tile
     tc::tma_load_2d(base + SS::P, &tm_p, &bar_load[st], 0, (int)(chh * 64));
   };
@@ -709,7 +713,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
       load_u(c_begin);
       load_kp(c_begin);
     } else {
-      issue_loads(c_begin, 0);
+      issue_loads(c_begin, 0, -1);
     }
   }
   static_assert(!(kSingle && kFused), "the fused forward runs the double-buffered state");
@@ -765,7 +769,8 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
       tc::mma_commit(&bar_mma);
     }
     GDR_TRACE_MARK(1, 7);
-    if (!kSingle && tid == kCopyTid && c + 1 < c_end && prep_ready(c + 1)) issue_loads(c + 1, st ^ 1);  // overlaps the MMA
+    // two stages: chunk c + 1's tiles go where chunk c - 1's were
+    if (!kSingle && tid == kCopyTid && c + 1 < c_end && prep_ready(c + 1)) issue_loads(c + 1, st ^ 1, it - 1);
     // single buffers: this chunk's K and P, once the previous chunk's P Vn (their last
     // reader) has run
     if (kSingle && ok && tid == kCopyTid && it > 0 &&
