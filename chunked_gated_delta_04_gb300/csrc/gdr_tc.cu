@@ -658,8 +658,9 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     for (int b = 0; b < 32; ++b)
       h[b] = S0 ? S0[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] : 0.f;
   }
-  // two stages: every tile of chunk c into stage st; U and P last, once the P Vn of chunk
-  // it_prev (the stage's previous user, -1: none), their last reader, is done (bar_pv)
+  // two stages: every tile of chunk c into stage st; P last, once the P Vn of chunk it_prev
+  // (the stage's previous user, -1: none), its last reader, is done (bar_pv).  (P Vn also
+  // reads the U tile as the unused rows 0-63 of its operand: those lanes are never read.)
   auto issue_loads = [&](int c, int st, int it_prev) {
     const int tc0 = t_seq + (c - c_begin) * 64;
     const size_t chh = (size_t)c * Hv + j;
@@ -672,9 +673,9 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     tc::tma_load_3d(base + SS::WQ + 3 * kSlab, &tm_q, &bar_load[st], 64, i, tc0);
     tc::tma_load_3d(base + SS::K, &tm_k, &bar_load[st], 0, i, tc0);
     tc::tma_load_3d(base + SS::K + kSlab, &tm_k, &bar_load[st], 64, i, tc0);
-    // (on a timeout the tiles stay out and the consumers' own bounded wait ends the chain)
-    if (it_prev >= 0 && !tc::mbar_wait(&bar_pv, (uint32_t)it_prev & 1u, ws.status, kDevErrTimeoutFwd)) return;
     tc::tma_load_2d(base + SS::U, &tm_u, &bar_load[st], dv0 & 64, (int)(chh * 64));  // 64-col tile
+    // (on a timeout the tile stays out and the consumers' own bounded wait ends the chain)
+    if (it_prev >= 0 && !tc::mbar_wait(&bar_pv, (uint32_t)it_prev & 1u, ws.status, kDevErrTimeoutFwd)) return;
     tc::tma_load_2d(base + SS::P, &tm_p, &bar_load[st], 0, (int)(chh * 64));
   };
   auto load_wq = [&](int c) {  // single buffers: [W|Q] and gamma of chunk c
