@@ -559,7 +559,14 @@ struct StateSmem {
   static constexpr uint32_t VTT = VNT + 4096;     // (e^{gamma_C - gamma} Vn)^T slice (4 KB)
   static constexpr uint32_t HS = VTT + 4096;      // h slice staged for the h_saved store: fp32 (16 KB) or bf16 (8 KB)
   static constexpr uint32_t GAM = HS + 16384;     // gamma of each stage: 256 B each
-  static constexpr uint32_t BYTES = GAM + NST * 256;
+  // two stages: chunk c's P tile rotates over three buffers (the stages' P slots and PX), so a
+  // chunk's P is loaded where P Vn of chunk c - 3 read, which the previous chunk's first
+  // product has waited for; single buffer: the stage's slot
+  static constexpr uint32_t PX = (GAM + NST * 256 + 1023) / 1024 * 1024;
+  static constexpr uint32_t BYTES = kSingle ? GAM + NST * 256 : PX + 8192;
+  __host__ __device__ static constexpr uint32_t pbuf(int c) {
+    return c % 3 == 2 ? PX : (uint32_t)(c % 3) * STAGE + P;
+  }
 };
 
 // 32 fp32 -> 32 bf16 in global memory (64 bytes, 16-byte aligned).
@@ -658,10 +665,9 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     for (int b = 0; b < 32; ++b)
       h[b] = S0 ? S0[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] : 0.f;
   }
-  // two stages: every tile of chunk c into stage st; P last, once the P Vn of chunk it_prev
-  // (the stage's previous user, -1: none), its last reader, is done (bar_pv).  (P Vn also
-  // reads the U tile as the unused rows 0-63 of its operand: those lanes are never read.)
-  auto issue_loads = [&](int c, int st, int it_prev) {
+  // two stages: every tile of chunk c into stage st, P into its rotating buffer (whose last
+  // reader, P Vn of chunk c - 3, completed before chunk c - 2's first product did)
+  auto issue_loads = [&](int c, int st) {
     const int tc0 = t_seq + (c - c_begin) * 64;
     const size_t chh = (size_t)c * Hv + j;
     unsigned char* base = sm + st * SS::STAGE;
@@ -674,9 +680,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     tc::tma_load_3d(base + SS::K, &tm_k, &bar_load[st], 0, i, tc0);
     tc::tma_load_3d(base + SS::K + kSlab, &tm_k, &bar_load[st], 64, i, tc0);
     tc::tma_load_2d(base + SS::U, &tm_u, &bar_load[st], dv0 & 64, (int)(chh * 64));  // 64-col tile
-    // (on a timeout the tile stays out and the consumers' own bounded wait ends the chain)
-    if (it_prev >= 0 && !tc::mbar_wait(&bar_pv, (uint32_t)it_prev & 1u, ws.status, kDevErrTimeoutFwd)) return;
-    tc::tma_load_2d(base + SS::P, &tm_p, &bar_load[st], 0, (int)(chh * 64));
+    tc::tma_load_2d(sm + SS::pbuf(c - c_begin), &tm_p, &bar_load[st], 0, (int)(chh * 64));
   };
   auto load_wq = [&](int c) {  // single buffers: [W|Q] and gamma of chunk c
     const int tc0 = t_seq + (c - c_begin) * 64;
@@ -714,7 +718,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
       load_u(c_begin);
       load_kp(c_begin);
     } else {
-      issue_loads(c_begin, 0, -1);
+      issue_loads(c_begin, 0);
     }
   }
   static_assert(!(kSingle && kFused), "the fused forward runs the double-buffered state");
@@ -760,7 +764,8 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     const float gr = sgam[r];
     unsigned char* stg = sm + st * SS::STAGE;
     const uint32_t s_wq = tc::smem_u32(stg + SS::WQ), s_k = tc::smem_u32(stg + SS::K);
-    const uint32_t s_up = tc::smem_u32(stg + SS::U);
+    // A operand of P Vn: P as rows 64-127; rows 0-63 (the 8 KB before it) give unused lanes
+    const uint32_t s_up = kSingle ? tc::smem_u32(stg + SS::U) : tc::smem_u32(sm + SS::pbuf(it)) - 8192u;
     if (ok && tid == 0) {
       tc::tc_fence_after();
       const uint32_t id = tc::idesc_bf16(128, 32, 0, 0);
@@ -771,7 +776,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     }
     GDR_TRACE_MARK(1, 7);
     // two stages: chunk c + 1's tiles go where chunk c - 1's were
-    if (!kSingle && tid == kCopyTid && c + 1 < c_end && prep_ready(c + 1)) issue_loads(c + 1, st ^ 1, it - 1);
+    if (!kSingle && tid == kCopyTid && c + 1 < c_end && prep_ready(c + 1)) issue_loads(c + 1, st ^ 1);
     // single buffers: this chunk's K and P, once the previous chunk's P Vn (their last
     // reader) has run
     if (kSingle && ok && tid == kCopyTid && it > 0 &&
@@ -832,8 +837,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
       for (int kk = 0; kk < 4; ++kk)
         tc::mma_bf16(D3, tc::mnmajor_step_desc(s_k, kSlab, kk), tc::kmajor_step_desc(s_vtt, 4096, kk), idt, kk > 0);
       tc::mma_commit(&bar_mma);
-      // P Vn for the output rows: rows 64-127 of this A operand are P (rows 0-63 are the
-      // U tile: unused lanes)
+      // P Vn for the output rows: rows 64-127 of this A operand are P (rows 0-63: unused lanes)
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         tc::mma_bf16(D2, tc::kmajor_step_desc(s_up, kSlab, kk), tc::kmajor_step_desc(s_vnt, 4096, kk), id, kk > 0);
