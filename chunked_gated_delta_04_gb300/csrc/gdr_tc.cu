@@ -709,8 +709,19 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
   // and the consumer's own bounded wait ends the chain).  (Reading the next chunk's flag a
   // chunk early with a relaxed load and an acquire fence when it was set measured slower: the
   // fence costs more than the poll it replaces.)
+  // A thread of warp 3 (kPollTid) reads chunk c + 2's flag (acquire) while chunk c's
+  // recurrence product runs and leaves what it saw in s_seen; the copy thread then skips its own
+  // poll of that chunk when the flag was already set (ordered through the CTA barriers between).
+  constexpr int kPollTid = 96;
+  __shared__ uint32_t s_seen[2];
+  if (tid == 0) s_seen[0] = s_seen[1] = 0u;
   auto prep_ready = [&](int c) {
-    return !kFused || wait_prep(ws.fwd_flags + (size_t)c * Hv + j, ws.status, kDevErrTimeoutFwd);
+    if (!kFused) return true;
+    if (c - c_begin >= 2 && s_seen[c & 1] != 0u) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    return wait_prep(ws.fwd_flags + (size_t)c * Hv + j, ws.status, kDevErrTimeoutFwd);
   };
   if (tid == kCopyTid && c_begin < c_end && prep_ready(c_begin)) {
     if (kSingle) {
@@ -826,6 +837,12 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     tc::tc_fence_before();
     __syncthreads();
     GDR_TRACE_MARK(1, 3);
+    if (kFused && tid == kPollTid && c + 2 < c_end) {
+      uint32_t v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ws.fwd_flags + (size_t)(c + 2) * Hv + j)
+                   : "memory");
+      s_seen[(c + 2) & 1] = v;
+    }
     if (kSingle && ok && tid == kCopyTid && c + 1 < c_end) load_u(c + 1);  // U was last read just above
     if (ok && tid == 0 && (!kSingle || tc::mbar_wait(&bar_kp, ld_phase, ws.status, kDevErrTimeoutFwd))) {
       tc::tc_fence_after();
