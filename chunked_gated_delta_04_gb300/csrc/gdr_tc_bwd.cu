@@ -214,10 +214,12 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
     // dh'); NC = 128: one tile, stored one chunk ago (group since: this chunk's dh')
     unsigned char* dvn_t = sm + ((NC == 64 && (it & 1)) ? WS::DVN2 : WS::DVN);
     if (tid == kCopyTid) {
+      GDR_TRACE_CLK(tdv);
       if constexpr (NC == 64)
         tc::bulk_wait_read<3>();
       else
         tc::bulk_wait_read<1>();
+      GDR_TRACE_SINCE(3, 20, tdv);
     }
     GDR_TRACE_MARK(3, 9);
     if (ok && warp >= 4) {  // diag(e^gamma) dO, zero past the chunk end: row r, half (tid >> 6) & 1
@@ -250,6 +252,19 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
     mma_phase ^= 1;
     tc::tc_fence_after();
     GDR_TRACE_MARK(3, 3);
+    // kPublish: the copy thread's warp has no part in the dVn rows, so it counts chunk c + 2 (the
+    // stores of two chunks ago; bulk groups since: dh', dVn, dh') here, where most of the
+    // ~1k-cycle GPU-scope release overlaps the epilogue instead of delaying the chunk's last
+    // barrier.  (A standalone acq_rel fence in the earlier MMA-issue window, with only a relaxed
+    // count here, measured ~1.9k cycles: slower.)
+    if (kPublish && tid == kCopyTid && prev2 >= 0) {
+      GDR_TRACE_CLK(tpw);
+      tc::bulk_wait<3>();
+      GDR_TRACE_SINCE(3, 22, tpw);
+      GDR_TRACE_CLK(tpp);
+      publish_chunk(ws.walk_flags + (size_t)prev2 * Hv + j);
+      GDR_TRACE_SINCE(3, 23, tpp);
+    }
     if (ok && lo) {  // dVn = scale P^T dO + diag(e^{gamma_C - gamma}) K dh', row r, half hf
       const float dec = fexp(gC - gr);
 #pragma unroll 1
@@ -282,7 +297,11 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
     GDR_TRACE_MARK(3, 4);
     // this chunk's dh' store has left the operand tile (only the dVn group may still read):
     // the tile takes the next chunk's dh' right after the update below
-    if (tid == kCopyTid) tc::bulk_wait_read<1>();
+    if (tid == kCopyTid) {
+      GDR_TRACE_CLK(tdr);
+      tc::bulk_wait_read<1>();
+      GDR_TRACE_SINCE(3, 21, tdr);
+    }
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutBwd));
     mma_phase ^= 1;
     tc::tc_fence_after();
@@ -300,15 +319,9 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       }
       stage_dh();  // the next chunk's dh' operand (one barrier for both)
     }
-    if (tid == kCopyTid) {
-      if (kPublish) {  // the stores of two chunks ago have had two chunks to land
-        if (prev2 >= 0) {
-          tc::bulk_wait<4>();
-          publish_chunk(ws.walk_flags + (size_t)prev2 * Hv + j);
-        }
-        prev2 = prev1;
-        prev1 = c;
-      }
+    if (tid == kCopyTid && kPublish) {
+      prev2 = prev1;
+      prev1 = c;
     }
     tc::tc_fence_before();
     __syncthreads();
