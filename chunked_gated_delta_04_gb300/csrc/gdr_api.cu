@@ -62,7 +62,8 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
   if (T_total >= (1ll << 31) / (p->Hv > p->Hk ? p->Hv : p->Hk)) return GDR_ERR_UNSUPPORTED;
   long long maxc = p->cu_seqlens ? (long long)p->T / kChunk + p->num_seqs
                                  : (long long)p->B * ((p->T + kChunk - 1) / kChunk);
-  if (maxc >= (1ll << 31) / p->Hv) return GDR_ERR_UNSUPPORTED;
+  // the saved states' rows (chunk-head x 128) are addressed with 32-bit tile coordinates
+  if (maxc * p->Hv * 128 >= (1ll << 31)) return GDR_ERR_UNSUPPORTED;
   d->B = p->B;
   d->T = p->T;
   d->Hk = p->Hk;

@@ -82,6 +82,8 @@ def test_size_queries(lib):
     (dict(h_dtype=torch.float16), gdr.GDR_ERR_INVALID_ARG),  # h_saved is fp32 or bf16
     (dict(prologue=8), gdr.GDR_ERR_INVALID_ARG),              # unknown prologue bit
     (dict(save_wy=2), gdr.GDR_ERR_INVALID_ARG),               # save_wy is 0 or 1
+    # 2^30 token-heads but 2^24 chunk-heads: the saved states' 128-row blocks would pass 2^31
+    (dict(T=1 << 27), gdr.GDR_ERR_UNSUPPORTED),
 ])
 def test_bad_problems_are_rejected(lib, kw, code):
     p = prob(**kw)
@@ -90,6 +92,12 @@ def test_bad_problems_are_rejected(lib, kw, code):
                      stream=0)
     assert st == code
     assert gdr.gdr_max_chunks(p) == 0
+
+
+def test_largest_accepted_chunk_count(lib):
+    # one chunk fewer per sequence than the rejected case above: 2^24 - 8 chunk-heads
+    p = prob(T=(1 << 27) - 64)
+    assert gdr.gdr_max_chunks(p) == 2 * ((1 << 21) - 1)
 
 
 def test_pointer_and_workspace_checks(lib):
