@@ -246,7 +246,7 @@ def reference_arm(args, w, inp):
         total_tok += tok
     value = total_tok / total_t
     units = inp["num_seqs"] * n_heads
-    sample = (f"per step: fp64 oracle fwd+bwd on {n_heads} of {w.Hk} q/k heads (with its {w.Hv // w.Hk} v-heads) "
+    sample = (f"per step: fp64 oracle fwd+bwd on {n_heads} of {w.Hk} q/k heads (each with its {w.Hv // w.Hk} v-head{'s' if w.Hv // w.Hk > 1 else ''}) "
               f"of all {inp['num_seqs']} sequences ({sum(inp['seqlens'])} tokens); tokens scaled by {n_heads}/{w.Hk}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
