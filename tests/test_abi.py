@@ -126,3 +126,21 @@ def test_pointer_and_workspace_checks(lib):
 def test_status_strings(lib):
     for s in range(7):
         assert gdr.gdr_status_string(s).startswith("GDR_")
+
+
+def test_saved_buffer_helpers(lib):
+    # the binding's saved buffer: a states view whose storage also holds the saved factors;
+    # a buffer too small for the problem is refused on the host before any call
+    for save_wy in (False, True):
+        p = prob(DK=128, DV=128, save_wy=save_wy)
+        h = gdr.alloc_saved(p, torch.float32, "cpu")
+        assert tuple(h.shape) == (gdr.gdr_max_chunks(p), p.Hv, 128, 128) and h.dtype == torch.float32
+        assert h.untyped_storage().nbytes() >= gdr.gdr_saved_states_bytes(p)
+        gdr._check_saved(p, h)
+    p = prob(DK=128, DV=128, save_wy=True)
+    small = torch.empty((gdr.gdr_max_chunks(p), p.Hv, 128, 128), dtype=torch.float32)
+    if gdr.gdr_saved_states_bytes(p) > small.untyped_storage().nbytes():  # tensor-core path
+        with pytest.raises(ValueError):
+            gdr._check_saved(p, small)
+    hb = gdr.alloc_saved(prob(h_dtype=torch.bfloat16), torch.bfloat16, "cpu")
+    assert hb.dtype == torch.bfloat16
