@@ -137,8 +137,8 @@ cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, 
 // Sums dq_part / dk_part over the v-heads of each q/k head into dq / dk (dtype).
 cudaError_t launch_group_reduce(const Dims& d, void* dq, void* dk, const Workspace& ws, cudaStream_t s);
 
-// tcgen05 kernels (bf16, DK = DV = 128).  tc_available() is false when this build
-// leaves them out.
+// tcgen05 kernels (bf16, DK = DV = 128).  tc_available() is false when the library was
+// compiled without them.
 bool tc_available();
 // Tensor maps (host): 3D over [rows][heads][cols] with a 64 x 1 x 64 box, 2D over
 // [rows][cols] with a 64 x 64 box; bf16, 128-byte swizzle.

@@ -62,7 +62,7 @@ typedef struct CUstream_st* gdr_stream_t; /* = cudaStream_t; NULL = legacy defau
 typedef enum {
   GDR_OK = 0,
   GDR_ERR_INVALID_ARG = 1, /* null required pointer, bad shape, bad enum value */
-  GDR_ERR_UNSUPPORTED = 2, /* a shape/dtype combination this build does not implement, or a size
+  GDR_ERR_UNSUPPORTED = 2, /* a shape/dtype combination the library does not implement, or a size
                               beyond B*T*max(Hk,Hv) < 2^31 and max_chunks*Hv*128 < 2^31 */
   GDR_ERR_ALIGNMENT = 3,   /* a base pointer is not 16-byte aligned */
   GDR_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed (launch, tensor map, ...) */
