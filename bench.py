@@ -88,15 +88,19 @@ def tensor_bytes(inp, w, h_el=4):
     }
 
 
-def work_model(inp, w, h_el=4):
+def work_model(inp, w, h_el=4, save_wy=False):
     """Algorithmic FLOPs (the chunked method's GEMMs, C x C products dense, the T inverse
-    as C^3/3) and compulsory HBM bytes of the forward and the backward."""
+    as C^3/3) and compulsory HBM bytes of the forward and the backward.  With save_wy the
+    backward reads the chunk factors the forward kept instead of recomputing them, so its
+    flops leave out W = T' K (2 c^2 DK), U = T'' V (2 c^2 DV) and the inverse (c^3 / 3)."""
     G = w.Hv // w.Hk
     DK, DV = w.DK, w.DV
     ff = fb = 0.0
     for c in chunk_lengths(inp["seqlens"]):
         ff += 4 * c * c * DK / G + 2 * c * c * DK + 4 * c * c * DV + 6 * c * DK * DV + c ** 3 / 3
         fb += 14 * c * DK * DV + 2 * c * c * DK * (7 + 2 / G) + 10 * c * c * DV + 4 * c ** 3 + c ** 3 / 3
+        if save_wy:
+            fb -= 2 * c * c * DK + 2 * c * c * DV + c ** 3 / 3
     ff *= w.Hv
     fb *= w.Hv
     tb = tensor_bytes(inp, w, h_el)
@@ -429,7 +433,7 @@ def main():
     gdr.gdr_debug_set_stage_events(None)
     stage_ms = {k: statistics.mean(v) for k, v in stage_tot.items()}
 
-    wm = work_model(inp, w, 2 if args.h_dtype == "bf16" else 4)
+    wm = work_model(inp, w, 2 if args.h_dtype == "bf16" else 4, save_wy=not args.recompute_wy)
     hbm, bf16_burst, bf16_sus, peak_src = load_peaks()
     dom = max(stage_ms, key=stage_ms.get)
     alg = stage_alg_bytes(dom, wm["tensor_bytes"])
@@ -533,7 +537,9 @@ def main():
                               t_hbm_step >= t_flop_step else "tensor", "bytes": wm["bytes_fwd"] + wm["bytes_bwd"],
                               "flops": wm["flops_fwd"] + wm["flops_bwd"]},
             "fwd": dir_obj(fwd_ms, wm["flops_fwd"], wm["bytes_fwd"]),
-            "bwd": dir_obj(bwd_ms, wm["flops_bwd"], wm["bytes_bwd"]),
+            "bwd": {**dir_obj(bwd_ms, wm["flops_bwd"], wm["bytes_bwd"]),
+                    "flops_counted": "with the chunk-factor recompute" if args.recompute_wy else
+                    "without the chunk-factor recompute (W, U, T read from the forward's saved buffer)"},
             "stages_ms": stage_ms,
             "path": "tcgen05" if gdr.gdr_path(p) == 1 else "simt",
             "cpu_baseline": cpu,

@@ -56,7 +56,45 @@ _STAGE_ARR = None
 EXPORTS = ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes", "gdr_bwd_workspace_bytes",
            "gdr_fwd", "gdr_bwd", "gdr_workspace_status", "gdr_status_string", "gdr_path",
            "gdr_debug_set_stage_events", "gdr_debug_stage_count", "gdr_debug_stage_name",
-           "gdr_debug_launch_count", "gdr_fwd_noalloc", "gdr_debug_tc_gemm", "gdr_debug_timeout_selftest"]
+           "gdr_debug_launch_count", "gdr_fwd_noalloc", "gdr_noalloc_status", "gdr_debug_tc_gemm", "gdr_debug_timeout_selftest"]
+
+
+def _open(path: str):
+    """dlopen one build of the library and declare its entry points' C signatures."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER(gdr_problem)
+    vp, sz, i, u32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)
+    for name in ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes",
+                 "gdr_bwd_workspace_bytes"]:
+        getattr(lib, name).argtypes = [P]
+        getattr(lib, name).restype = sz
+    lib.gdr_path.argtypes = [P]
+    lib.gdr_path.restype = i
+    lib.gdr_fwd.argtypes = [P] + [vp] * 9 + [vp, sz, vp]
+    lib.gdr_fwd.restype = i
+    lib.gdr_bwd.argtypes = [P] + [vp] * 14 + [vp, sz, vp]
+    lib.gdr_bwd.restype = i
+    lib.gdr_fwd_noalloc.argtypes = [P] + [vp] * 9 + [vp]
+    lib.gdr_fwd_noalloc.restype = i
+    lib.gdr_noalloc_status.argtypes = [vp, u32p]
+    lib.gdr_noalloc_status.restype = i
+    lib.gdr_workspace_status.argtypes = [vp, vp, u32p]
+    lib.gdr_workspace_status.restype = i
+    lib.gdr_status_string.argtypes = [i]
+    lib.gdr_status_string.restype = ctypes.c_char_p
+    lib.gdr_debug_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i]
+    lib.gdr_debug_set_stage_events.restype = None
+    lib.gdr_debug_stage_count.argtypes = []
+    lib.gdr_debug_stage_count.restype = i
+    lib.gdr_debug_stage_name.argtypes = [i]
+    lib.gdr_debug_stage_name.restype = ctypes.c_char_p
+    lib.gdr_debug_launch_count.argtypes = []
+    lib.gdr_debug_launch_count.restype = ctypes.c_ulonglong
+    lib.gdr_debug_tc_gemm.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
+    lib.gdr_debug_tc_gemm.restype = i
+    lib.gdr_debug_timeout_selftest.argtypes = [vp, ctypes.c_ulonglong, vp, vp]
+    lib.gdr_debug_timeout_selftest.restype = i
+    return lib
 
 
 def _lib_handle():
@@ -65,39 +103,27 @@ def _lib_handle():
     if _LIB is None:
         if not os.path.exists(LIB_PATH):
             raise ImportError(f"libgdr.so not built ({LIB_PATH}); run `python -m chunked_gated_delta_04_gb300.build`")
-        lib = ctypes.CDLL(LIB_PATH)
-        P = ctypes.POINTER(gdr_problem)
-        vp, sz, i, u32p = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)
-        for name in ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes",
-                     "gdr_bwd_workspace_bytes"]:
-            getattr(lib, name).argtypes = [P]
-            getattr(lib, name).restype = sz
-        lib.gdr_path.argtypes = [P]
-        lib.gdr_path.restype = i
-        lib.gdr_fwd.argtypes = [P] + [vp] * 9 + [vp, sz, vp]
-        lib.gdr_fwd.restype = i
-        lib.gdr_bwd.argtypes = [P] + [vp] * 14 + [vp, sz, vp]
-        lib.gdr_bwd.restype = i
-        lib.gdr_fwd_noalloc.argtypes = [P] + [vp] * 9 + [vp]
-        lib.gdr_fwd_noalloc.restype = i
-        lib.gdr_workspace_status.argtypes = [vp, vp, u32p]
-        lib.gdr_workspace_status.restype = i
-        lib.gdr_status_string.argtypes = [i]
-        lib.gdr_status_string.restype = ctypes.c_char_p
-        lib.gdr_debug_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i]
-        lib.gdr_debug_set_stage_events.restype = None
-        lib.gdr_debug_stage_count.argtypes = []
-        lib.gdr_debug_stage_count.restype = i
-        lib.gdr_debug_stage_name.argtypes = [i]
-        lib.gdr_debug_stage_name.restype = ctypes.c_char_p
-        lib.gdr_debug_launch_count.argtypes = []
-        lib.gdr_debug_launch_count.restype = ctypes.c_ulonglong
-        lib.gdr_debug_tc_gemm.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
-        lib.gdr_debug_tc_gemm.restype = i
-        lib.gdr_debug_timeout_selftest.argtypes = [vp, ctypes.c_ulonglong, vp, vp]
-        lib.gdr_debug_timeout_selftest.restype = i
-        _LIB = lib
+        _LIB = _open(LIB_PATH)
     return _LIB
+
+
+class library:
+    """Context manager: route every call of this module through another build of the library
+    (e.g. the delay-injection build libgdr_delay.so) and restore the default one after."""
+
+    def __init__(self, path: str):
+        self.path = path
+
+    def __enter__(self):
+        global _LIB
+        self.saved = _lib_handle()
+        _LIB = _open(self.path)
+        return _LIB
+
+    def __exit__(self, *exc):
+        global _LIB
+        _LIB = self.saved
+        return False
 
 
 def load():
@@ -191,6 +217,13 @@ def gdr_fwd_noalloc(p, q, k, v, g, beta, S0, o, S_T, h_saved, stream=None) -> in
 
 
 NOALLOC_MAX_WORKSPACE_BYTES = 64 << 20
+
+
+def gdr_noalloc_status(stream=None):
+    """Synchronises the stream; returns (status, raw flag bits) of gdr_fwd_noalloc's status word."""
+    flags = ctypes.c_uint32(0)
+    st = _lib_handle().gdr_noalloc_status(_stream_ptr(stream), ctypes.byref(flags))
+    return st, flags.value
 
 
 def gdr_workspace_status(workspace, stream=None):

@@ -15,13 +15,18 @@
 //    this entry point has run).  Problems whose forward workspace would be larger
 //    are refused with GDR_ERR_WORKSPACE.
 //  - In host code the array's name is only a host-side stand-in; its device address
-//    is looked up with cudaGetSymbolAddress once per device (on the first call made
-//    with that device current) and cached.
+//    is looked up with cudaGetSymbolAddress on the first call made in each CUDA context
+//    of a device (the device current) and cached with that context's id, so a context
+//    created anew (after cudaDeviceReset, say) looks it up again instead of using an
+//    address of the old one.  With CUDA_MODULE_LOADING=EAGER the array is reserved on
+//    every device whose context loads the library, whether or not this entry point runs.
 //  - All calls share the one array and leave their contents behind.  The forward
 //    writes every scratch word it reads before reading it, and its first kernel
 //    clears the status word, so nothing has to be zeroed between calls.  Two calls
 //    whose work overlaps on the GPU (different streams, no ordering) race on the
 //    array and give wrong results: serialise them.
+//  - Device-side errors (a malformed cu_seqlens, a bounded wait that ran out) land in
+//    the array's status word; gdr_noalloc_status reads it, allocating nothing.
 #include <mutex>
 
 #include "gdr_internal.h"
@@ -35,25 +40,58 @@ constexpr int kMaxDevices = 128;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch per device, or nullptr
+struct ScratchEntry {
+  unsigned long long ctx_id;  // CUDA context the address belongs to
+  void* ptr;                  // device address of g_noalloc_scratch in it, or nullptr
+};
+ScratchEntry g_noalloc[kMaxDevices];
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Device address of the scratch array on the current device (set up on first use).
+// Id of the current CUDA context (driver entry points looked up once through the runtime).
+cudaError_t current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  if (!get_current || !get_id) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess)
+      return cudaErrorNotSupported;
+    get_current = (GetCurrent)f1;
+    get_id = (GetId)f2;
+  }
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of the scratch array in the current device's context (set up on first
+// use in that context).
 cudaError_t scratch_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  e = cudaSetDevice(dev);  // makes the device's primary context current (CUDA 12+ initialises it here)
+  if (e != cudaSuccess) return e;
+  unsigned long long ctx = 0;
+  e = current_context_id(&ctx);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  if (g_noalloc[dev].ptr == nullptr || g_noalloc[dev].ctx_id != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
     if (p == nullptr || ((uintptr_t)p & 255u) != 0) return cudaErrorInvalidDevicePointer;
-    g_noalloc_ptr[dev] = p;
+    g_noalloc[dev] = ScratchEntry{ctx, p};
   }
-  *out = g_noalloc_ptr[dev];
+  *out = g_noalloc[dev].ptr;
   return cudaSuccess;
 }
 
@@ -85,4 +123,10 @@ extern "C" gdr_status gdr_fwd_noalloc(const gdr_problem* p, const void* q, const
   if (e == cudaSuccess) e = apply_prologue(d, a, ws, s);
   if (e == cudaSuccess) e = d.path == 1 ? tc_forward(d, a, ws, s) : simt_forward(d, a, ws, s);
   return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+extern "C" gdr_status gdr_noalloc_status(gdr_stream_t stream, uint32_t* flags) {
+  void* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return GDR_ERR_CUDA;
+  return gdr_workspace_status(scratch, stream, flags);  // the status word heads the array
 }

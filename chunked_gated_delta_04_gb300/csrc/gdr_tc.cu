@@ -150,20 +150,10 @@ __device__ __forceinline__ void ld_f4(const float* __restrict__ src, float* v) {
 // full T (zeros above the diagonal) into sT (row stride kLdA).  All 128 threads take part.
 __device__ __forceinline__ void solve_unit_lower64(const float* __restrict__ sA, float* __restrict__ sT,
                                                    float* __restrict__ sY, int tid) {
-#ifdef GDR_TRACE
-  unsigned long long ts_ = clock64();
-#define SOLVE_MARK(k)                                                   \
-  if (tid == 0 && blockIdx.x == 0 && blockIdx.y == 0) {                 \
-    const unsigned long long n_ = clock64();                            \
-    g_gdr_trace[0][16 + (k)] += n_ - ts_;                               \
-    ts_ = n_;                                                           \
-  }
-#else
-#define SOLVE_MARK(k)
-#endif
+  GDR_TRACE_INIT();
   for (int e = tid; e < 64 * kLdA / 4; e += kTcThreads) reinterpret_cast<float4*>(sT)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
-  SOLVE_MARK(0);
+  GDR_TRACE_MARK(0, 16 + 0);
   if (tid < 64) {  // diagonal 16 x 16 blocks
     const int b = tid >> 4, c = tid & 15;
     const float* Ab = sA + (16 * b) * kLdA + 16 * b;
@@ -179,7 +169,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float* __restrict__ sA,
     for (int rr = 0; rr < 16; ++rr) sT[(16 * b + rr) * kLdA + 16 * b + c] = col[rr];
   }
   __syncthreads();
-  SOLVE_MARK(1);
+  GDR_TRACE_MARK(0, 16 + 1);
   {  // T_{2b+1,2b} = -T_{2b+1,2b+1} A_{2b+1,2b} T_{2b,2b}, b = 0, 1; thread: 1 row x 4 columns
     const int b = tid >> 6, rr = (tid >> 2) & 15, c4 = (tid & 3) * 4;
     const int r0 = 16 * (2 * b + 1), c0 = 16 * (2 * b);
@@ -207,7 +197,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float* __restrict__ sA,
     *reinterpret_cast<float4*>(sT + (r0 + rr) * kLdA + c0 + c4) = make_float4(-o[0], -o[1], -o[2], -o[3]);
   }
   __syncthreads();
-  SOLVE_MARK(2);
+  GDR_TRACE_MARK(0, 16 + 2);
   {  // T_[23][01] = -T_[23][23] A_[23][01] T_[01][01] (32 x 32); thread: 1 row x 8 columns
     const int rr = tid >> 2, c8 = (tid & 3) * 8;
     float o[8];
@@ -245,8 +235,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float* __restrict__ sA,
     *reinterpret_cast<float4*>(dst + 4) = make_float4(-o[4], -o[5], -o[6], -o[7]);
   }
   __syncthreads();
-  SOLVE_MARK(3);
-#undef SOLVE_MARK
+  GDR_TRACE_MARK(0, 16 + 3);
 }
 
 // Publishes one finished chunk-head of the fused forward: its TMA stores (async proxy) and
@@ -356,12 +345,14 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tm_q, const CUtenso
   unsigned char* const v_t = sm + (st ? PrepSmem::BYTES + 2 * 16384 : PrepSmem::V);
   if (len > 0) {  // (an empty chunk slot: uniform across the CTA)
   if (tid == 0) {
+    GDR_DELAY(1);
     if (kFused) {  // claim the next item and load its tiles into the other stage, whose last
                    // reader (two items ago) is done; then publish the previous item
       next_item(witem, 2);
       if (s_item[2] < n_items) issue_loads(s_item[2], s_item[3], st ^ 1);
       if (pub >= 0) {
         tc::bulk_wait<0>();
+        GDR_DELAY(2);
         publish_prep(ws.fwd_flags + pub);
         pub = -1;
       }
@@ -787,6 +778,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     }
     GDR_TRACE_MARK(1, 7);
     // two stages: chunk c + 1's tiles go where chunk c - 1's were
+    if (tid == kCopyTid) GDR_DELAY(3);
     if (!kSingle && tid == kCopyTid && c + 1 < c_end && prep_ready(c + 1)) issue_loads(c + 1, st ^ 1);
     // single buffers: this chunk's K and P, once the previous chunk's P Vn (their last
     // reader) has run
@@ -814,6 +806,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     GDR_TRACE_MARK(1, 2);
     if (ok) {
       if (warp < 2) {  // Vn = U - W h (rows >= len are zero: W and U are zero there)
+        if (warp == 1) GDR_DELAY(4);
         float x[32], u[32];
         const bool uok = !kSingle || __all_sync(0xffffffffu, tc::mbar_wait(&bar_load[1], ld_phase, ws.status,
                                                                             kDevErrTimeoutFwd));
@@ -838,6 +831,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     __syncthreads();
     GDR_TRACE_MARK(1, 3);
     if (kFused && tid == kPollTid && c + 2 < c_end) {
+      GDR_DELAY(6);
       uint32_t v;
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ws.fwd_flags + (size_t)(c + 2) * Hv + j)
                    : "memory");
@@ -845,6 +839,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     }
     if (kSingle && ok && tid == kCopyTid && c + 1 < c_end) load_u(c + 1);  // U was last read just above
     if (ok && tid == 0 && (!kSingle || tc::mbar_wait(&bar_kp, ld_phase, ws.status, kDevErrTimeoutFwd))) {
+      GDR_DELAY(5);
       tc::tc_fence_after();
       const uint32_t id = tc::idesc_bf16(128, 32, 0, 0);
       const uint32_t idt = tc::idesc_bf16(128, 32, 1, 0);

@@ -208,7 +208,10 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       tc::mma_commit(&bar_mma);
     }
     GDR_TRACE_MARK(3, 7);
-    if (tid == kCopyTid && c - 1 >= c_begin) issue_loads(c - 1, st ^ 1);  // overlaps the MMAs
+    if (tid == kCopyTid && c - 1 >= c_begin) {  // overlaps the MMAs
+      GDR_DELAY(10);
+      issue_loads(c - 1, st ^ 1);
+    }
     GDR_TRACE_MARK(3, 8);
     // NC = 64: this chunk's dVn tile was last stored two chunks ago (groups since: dh', dVn,
     // dh'); NC = 128: one tile, stored one chunk ago (group since: this chunk's dh')
@@ -262,10 +265,12 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       tc::bulk_wait<3>();
       GDR_TRACE_SINCE(3, 22, tpw);
       GDR_TRACE_CLK(tpp);
+      GDR_DELAY(11);
       publish_chunk(ws.walk_flags + (size_t)prev2 * Hv + j);
       GDR_TRACE_SINCE(3, 23, tpp);
     }
     if (ok && lo) {  // dVn = scale P^T dO + diag(e^{gamma_C - gamma}) K dh', row r, half hf
+      if (warp == 1) GDR_DELAY(12);
       const float dec = fexp(gC - gr);
 #pragma unroll 1
       for (int q = 0; q < CPT / 32; ++q) {  // 32 columns at a time: [CPT hf + 32 q, +32)
@@ -285,6 +290,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
     tc::tc_fence_before();
     __syncthreads();
     if (ok && tid == 0) {
+      GDR_DELAY(13);
       tc::tc_fence_after();
       tc::gemm(Dc, mnmaj(stg + WS::W, kSlab), mnmaj(dvn_t, kSlab), NC, 4, false);  // W^T dVn
       tc::mma_commit(&bar_mma);
@@ -487,6 +493,7 @@ __device__ __forceinline__ void grad_body(
   int cur_len = 0, cur_t0 = 0, cur_i = 0;  // the current item (for pair_reduce)
   enum : int { kLdDhDvn = 1, kLdW = 2, kLdRest = 4, kLdDo = 8, kLdAll = 15 };
   auto issue_loads = [&](int w, int c2, int groups) {  // copy thread only; c2 = chunk_of(w)
+    GDR_DELAY(20);
     const int j2 = vhead_of(w), i2 = j2 / d.G, tt = ws.chunks[c2].y;
     const size_t ch2 = (size_t)c2 * Hv + j2;
     uint64_t* bar = &bar_tma;
@@ -544,6 +551,7 @@ __device__ __forceinline__ void grad_body(
     bool okw = true;
     if (tid == 0) tc::mbar_arrive_expect_tx(bar_data, 64 * 256);  // the partner's half for this item
     if (okin && lo && hf != (int)rank) {
+      if (rank == 1u) GDR_DELAY(23);
       okw = __all_sync(0xffffffffu, tc::mbar_wait_cluster(bar_free, item_par, ws.status, kDevErrTimeoutBwd));
       const uint32_t dst = tc::mapa(tc::smem_u32(sm + buf_off), peer) + (uint32_t)r * 256u;
       const uint32_t cbar = tc::mapa(tc::smem_u32(bar_data), peer);
@@ -734,6 +742,7 @@ __device__ __forceinline__ void grad_body(
   // P4: dO Vn^T (64-127, lanes 64-127: the operand's rows start one slab early, so dP is the
   // other lane half's epilogue), K dh' (128-255), dk = Vn~ dh'^T (384-511)
   if (ok && tid == 0) {
+    GDR_DELAY(22);
     tc::tc_fence_after();
     tc::gemm(tb + 64, kmaj(sm + S::DO - kSlab, kSlab), kmaj(sm + S::VN, kSlab), 64, 8, false);
     tc::gemm(tb + 128, kmaj(sm + S::KQ, 2 * kSlab), mnmaj(sm + S::DH, 16384), 128, 8, false);
@@ -759,6 +768,7 @@ __device__ __forceinline__ void grad_body(
   }
   GDR_TRACE_MARK(2, 4);
   if (ok && !lo) {  // lanes 64-127: dP and dP * QK for row r, columns [32 hf, 32 hf + 32)
+    if (warp == 7) GDR_DELAY(21);
     {
       float x[32], gs[32], qk[32];
       tmem_ld32w(tb, warp, 64 + 32 * hf, x);  // (dO Vn^T)[r]

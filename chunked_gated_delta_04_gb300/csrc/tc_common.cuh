@@ -4,105 +4,11 @@
 
 #include <cuda_bf16.h>
 
+#include "gdr_instrument.cuh"
 #include "tc_primitives.cuh"
 
 namespace gdr {
 namespace tcx {
-
-// Opt-in phase trace (-DGDR_TRACE): thread 0 of CTA GDR_TRACE_BLOCK (default 0) adds the
-// clock64() cycles spent between consecutive marks into a per-translation-unit table
-// [kernel][mark]; GDR_TRACE_COUNT adds 1 to a slot (e.g. items processed).
-#ifdef GDR_TRACE
-#ifndef GDR_TRACE_BLOCK
-#define GDR_TRACE_BLOCK 0
-#endif
-static __device__ unsigned long long g_gdr_trace[8][32];
-static __device__ unsigned long long g_gdr_cta_span[1024][3];  // per CTA: start, end (ns), SM id
-// per CTA, free-form timeline slots (globaltimer ns or counts), written by GDR_TRACE_INFO
-static __device__ unsigned long long g_gdr_cta_info[1024][8];
-#define GDR_TRACE_NOW()                                              \
-  ([]() {                                                            \
-    unsigned long long t_;                                           \
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));          \
-    return t_;                                                       \
-  }())
-#define GDR_TRACE_INFO_SET(slot, v)                                  \
-  do {                                                               \
-    if (blockIdx.x < 1024) g_gdr_cta_info[blockIdx.x][slot] = (v);   \
-  } while (0)
-#define GDR_TRACE_INFO_ADD(slot, v)                                  \
-  do {                                                               \
-    if (blockIdx.x < 1024) atomicAdd(&g_gdr_cta_info[blockIdx.x][slot], (unsigned long long)(v)); \
-  } while (0)
-#define GDR_TRACE_CTA_BEGIN()                                                                      \
-  do {                                                                                             \
-    if (threadIdx.x == 0 && blockIdx.x < 1024) {                                                   \
-      unsigned long long t_;                                                                       \
-      unsigned int sm_;                                                                            \
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                      \
-      asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));                                             \
-      g_gdr_cta_span[blockIdx.x][0] = t_;                                                          \
-      g_gdr_cta_span[blockIdx.x][2] = sm_;                                                         \
-    }                                                                                              \
-  } while (0)
-#define GDR_TRACE_CTA_END()                                                                        \
-  do {                                                                                             \
-    if (threadIdx.x == 0 && blockIdx.x < 1024) {                                                   \
-      unsigned long long t_;                                                                       \
-      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                                      \
-      g_gdr_cta_span[blockIdx.x][1] = t_;                                                          \
-    }                                                                                              \
-  } while (0)
-#define GDR_TRACE_INIT() unsigned long long gdr_tprev_ = clock64()
-#define GDR_TRACE_MARK(kid, slot)                                                                  \
-  do {                                                                                             \
-    if (threadIdx.x == 0 && blockIdx.x == GDR_TRACE_BLOCK && blockIdx.y == 0 && blockIdx.z == 0) { \
-      const unsigned long long now_ = clock64();                                                   \
-      atomicAdd(&g_gdr_trace[kid][slot], now_ - gdr_tprev_); /* a reduction: nothing waits on it */ \
-      gdr_tprev_ = now_;                                                                           \
-    }                                                                                              \
-  } while (0)
-#define GDR_TRACE_COUNT(kid, slot)                                                                 \
-  do {                                                                                             \
-    if (threadIdx.x == 0 && blockIdx.x == GDR_TRACE_BLOCK && blockIdx.y == 0 && blockIdx.z == 0)   \
-      atomicAdd(&g_gdr_trace[kid][slot], 1ull);                                                    \
-  } while (0)
-// cycles one thread spends in a region (any thread of the traced CTA)
-#define GDR_TRACE_CLK(var) const unsigned long long var = clock64()
-#define GDR_TRACE_SINCE(kid, slot, var)                                                            \
-  do {                                                                                             \
-    if (blockIdx.x == GDR_TRACE_BLOCK) atomicAdd(&g_gdr_trace[kid][slot], clock64() - (var));     \
-  } while (0)
-#else
-#define GDR_TRACE_NOW() 0ull
-#define GDR_TRACE_INFO_SET(slot, v) \
-  do {                              \
-  } while (0)
-#define GDR_TRACE_INFO_ADD(slot, v) \
-  do {                              \
-  } while (0)
-#define GDR_TRACE_CTA_BEGIN() \
-  do {                        \
-  } while (0)
-#define GDR_TRACE_CTA_END() \
-  do {                      \
-  } while (0)
-#define GDR_TRACE_INIT() \
-  do {                   \
-  } while (0)
-#define GDR_TRACE_MARK(kid, slot) \
-  do {                            \
-  } while (0)
-#define GDR_TRACE_COUNT(kid, slot) \
-  do {                             \
-  } while (0)
-#define GDR_TRACE_CLK(var) \
-  do {                     \
-  } while (0)
-#define GDR_TRACE_SINCE(kid, slot, var) \
-  do {                                  \
-  } while (0)
-#endif
 
 using bf16 = __nv_bfloat16;
 constexpr int kTcThreads = 128;

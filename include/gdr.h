@@ -156,25 +156,35 @@ gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const voi
  * memory and cannot allocate any themselves: e.g. a plugin whose host framework
  * owns all device memory and forbids side allocations, or a latency-critical loop
  * where a cudaMalloc, which may synchronise the whole device, is not acceptable.
- * Same arguments, results and errors as gdr_fwd, minus the workspace.
+ * Same arguments and results as gdr_fwd, minus the workspace; host-side errors are
+ * returned as by gdr_fwd, device-side ones are read with gdr_noalloc_status.
  *  - Its scratch is one array of GDR_NOALLOC_MAX_WORKSPACE_BYTES in device memory,
  *    owned by the library: every GPU that loads this part of the library keeps that
- *    much memory until the process exits (with CUDA's default lazy module loading,
- *    only GPUs on which this entry point has run).  It allocates nothing, ever.
+ *    much memory until the process exits.  With CUDA's default lazy module loading that
+ *    is only GPUs on which this entry point has run; with CUDA_MODULE_LOADING=EAGER it
+ *    is every GPU whose context loads libgdr.so, whether or not the entry point runs.
+ *    It allocates nothing, ever.
  *  - A problem whose gdr_fwd_workspace_bytes exceeds the limit is refused with
  *    GDR_ERR_WORKSPACE before anything is launched.
- *  - It runs on the current device.  The first call on each device looks up the
- *    array's device address (cudaGetSymbolAddress) and caches it, so make that first
- *    call before any stream capture begins.
+ *  - It runs on the current device.  The first call in each CUDA context of a device
+ *    (the first call on the device, and again after a reset created a new context)
+ *    looks up the array's device address (cudaGetSymbolAddress) and caches it, so make
+ *    that first call before any stream capture begins.
  *  - Every call uses the same array and leaves its contents behind; nothing needs
  *    clearing between calls.  Calls whose GPU work can overlap (e.g. on two
  *    unordered streams) race on the array and corrupt each other's results:
- *    serialise them.  The array's status word is not readable through
- *    gdr_workspace_status. */
+ *    serialise them. */
 #define GDR_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)64 << 20)
 gdr_status gdr_fwd_noalloc(const gdr_problem* p, const void* q, const void* k, const void* v,
                            const float* g, const void* beta, const float* S0, void* o, float* S_T,
                            void* h_saved, gdr_stream_t stream);
+
+/* The status word of gdr_fwd_noalloc's array, as gdr_workspace_status reads a workspace's
+ * (no counterpart on the pages; allocates nothing): synchronises `stream`, then returns
+ * GDR_OK, GDR_ERR_INVALID_ARG (the kernels found cu_seqlens malformed and computed
+ * nothing) or GDR_ERR_TIMEOUT (a bounded wait ran out; the outputs are invalid) for the
+ * last gdr_fwd_noalloc on the current device.  *flags (nullable) receives the raw bits. */
+gdr_status gdr_noalloc_status(gdr_stream_t stream, uint32_t* flags);
 
 /* Synchronises `stream`, then reads the status word that the kernels of the last
  * gdr_fwd / gdr_bwd using `workspace` left there: GDR_OK, or GDR_ERR_TIMEOUT if a

@@ -18,3 +18,19 @@ def rng():
     import numpy as np
 
     return np.random.default_rng(1234)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Write the parity margins the full-size GPU tests recorded (nothing when none ran)."""
+    import gdr_testlib
+
+    if not gdr_testlib._MARGINS:
+        return
+    try:
+        import torch
+
+        name = torch.cuda.get_device_name(0)
+    except Exception:  # noqa: BLE001 - the name is only a label
+        name = "unknown GPU"
+    path = os.environ.get("GDR_PARITY_MARGINS", os.path.join(ROOT, "profiles", "parity_margins.md"))
+    gdr_testlib.write_margins(path, name)

@@ -92,3 +92,19 @@ def test_ncu_traffic_is_reported_only_for_unchanged_sources():
             assert got == float(nbytes)
         else:
             assert got is None
+
+
+def test_saved_factors_leave_the_recompute_out_of_the_backward_flops():
+    # with the forward's chunk factors saved the backward does not form W = T' K (2 c^2 DK),
+    # U = T'' V (2 c^2 DV) or the inverse (c^3 / 3): at c = 64, D = 128 that is 2.18 MFLOP less
+    # per chunk-head, 34.1 kFLOP less per token-head (476.5 -> 442.4 kFLOP)
+    import bench
+
+    m, w = _model("b2_t4096")
+    inp = {"seqlens": [w.T] * w.B, "num_seqs": w.B, "S0": object(), "dS_T": object()}
+    ms = bench.work_model(inp, w, save_wy=True)
+    th = w.B * w.T * w.Hv
+    per_chunk = 2 * 64 * 64 * 128 * 2 + 64 ** 3 / 3
+    assert (m["flops_bwd"] - ms["flops_bwd"]) / th == pytest.approx(per_chunk / 64, rel=1e-12)
+    assert ms["flops_bwd"] / th == pytest.approx(442.4e3, rel=2e-4)
+    assert ms["flops_fwd"] == m["flops_fwd"] and ms["bytes_bwd"] == m["bytes_bwd"]

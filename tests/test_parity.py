@@ -13,22 +13,22 @@ import torch
 
 import chunked_gated_delta_04_gb300 as gdr
 from chunked_gated_delta_04_gb300.inputs import WORKLOADS, make_inputs, small_workload
-from gdr_testlib import (OUT_KEYS_BWD, OUT_KEYS_FWD, compare, head_slice, reference, run_gpu, slice_result,
-                         to_device, tol_for)
+from gdr_testlib import (OUT_KEYS_BWD, OUT_KEYS_FWD, compare, head_slice, record_margins, reference, run_gpu,
+                         slice_result, to_device, tol_for)
 
 pytestmark = pytest.mark.gpu
 
 
-def _check(w, heads=None):
+def _check(w, heads=None, ref=None, **run_kw):
     inp = make_inputs(w)
-    res = run_gpu(inp)
+    res = run_gpu(inp, **run_kw)
     torch.cuda.synchronize()
     if heads is not None:
         sub, vh = head_slice(inp, heads)
-        ref = reference(sub)
+        ref = reference(sub) if ref is None else ref
         res = slice_result(res, heads, vh)
     else:
-        ref = reference(inp)
+        ref = reference(inp) if ref is None else ref
     return compare(res, ref, tol_for(w.dtype))
 
 
@@ -74,12 +74,35 @@ def test_tiny_fp32_workload():
     _check(WORKLOADS["tiny_fp32"])
 
 
+# The named workloads at full size, on sampled heads (every token and chunk of those heads), in
+# each mode the benchmark can run: the backward recomputing the chunk factors, the forward
+# saving them (the benchmark's default), and (b2_t4096) bf16 chunk-start states.  Each case's
+# per-tensor rel_max is recorded in the parity-margins table (see gdr_testlib.record_margins).
+NAMED = [("tiny_fp32", None, "simt", {}),
+         ("b2_t4096", [0, 15], "recompute", {}),
+         ("b2_t4096", [0, 15], "saved", {"save_wy": True}),
+         ("b2_t4096", [0, 15], "saved, h bf16", {"save_wy": True, "h_dtype": torch.bfloat16}),
+         ("varlen8", [3], "recompute", {}),
+         ("varlen8", [3], "saved", {"save_wy": True}),
+         ("long_t65536", [7], "recompute", {}),
+         ("long_t65536", [7], "saved", {"save_wy": True}),
+         ("gva_b4_t8192", [0], "recompute", {}),
+         ("gva_b4_t8192", [0], "saved", {"save_wy": True})]
+_REF_CACHE = {}
+
+
 @pytest.mark.slow
-@pytest.mark.parametrize("name,heads", [("b2_t4096", [0, 15]), ("varlen8", [3]), ("long_t65536", [7]),
-                                        ("gva_b4_t8192", [0])])
-def test_named_workloads_sampled_heads(name, heads):
-    errs = _check(WORKLOADS[name], heads)
-    print(name, errs)
+@pytest.mark.parametrize("name,heads,mode,kw", NAMED, ids=[f"{c[0]}-{c[2].replace(', ', '-').replace(' ', '_')}"
+                                                            for c in NAMED])
+def test_named_workloads_sampled_heads(name, heads, mode, kw):
+    w = WORKLOADS[name]
+    key = (name, tuple(heads) if heads else None)
+    if key not in _REF_CACHE:  # the oracle's answer does not depend on the mode: compute it once
+        _REF_CACHE.clear()
+        inp = make_inputs(w)
+        _REF_CACHE[key] = reference(head_slice(inp, heads)[0] if heads else inp)
+    errs = _check(w, heads, ref=_REF_CACHE[key], **kw)
+    record_margins(name, mode, "all" if heads is None else ",".join(map(str, heads)), errs, tol_for(w.dtype))
 
 
 def test_varlen_matches_separate_fixed_length_runs():
