@@ -47,6 +47,9 @@ class GDRError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         msg = _lib_handle().gdr_status_string(status).decode() if _LIB is not None else str(status)
+        if status == GDR_ERR_CUDA and _LIB is not None:
+            ce = _LIB.gdr_debug_last_cuda_error()
+            msg += f" ({_LIB.gdr_debug_cuda_error_string(ce).decode()}, cudaError {ce})"
         super().__init__(f"{where}: {msg}")
 
 
@@ -56,7 +59,7 @@ _STAGE_ARR = None
 EXPORTS = ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes", "gdr_bwd_workspace_bytes",
            "gdr_fwd", "gdr_bwd", "gdr_workspace_status", "gdr_status_string", "gdr_path",
            "gdr_debug_set_stage_events", "gdr_debug_stage_count", "gdr_debug_stage_name",
-           "gdr_debug_launch_count", "gdr_fwd_noalloc", "gdr_noalloc_status", "gdr_debug_tc_gemm", "gdr_debug_timeout_selftest"]
+           "gdr_debug_launch_count", "gdr_debug_last_cuda_error", "gdr_debug_cuda_error_string", "gdr_fwd_noalloc", "gdr_noalloc_status", "gdr_debug_tc_gemm", "gdr_debug_timeout_selftest"]
 
 
 def _open(path: str):
@@ -90,6 +93,10 @@ def _open(path: str):
     lib.gdr_debug_stage_name.restype = ctypes.c_char_p
     lib.gdr_debug_launch_count.argtypes = []
     lib.gdr_debug_launch_count.restype = ctypes.c_ulonglong
+    lib.gdr_debug_last_cuda_error.argtypes = []
+    lib.gdr_debug_last_cuda_error.restype = i
+    lib.gdr_debug_cuda_error_string.argtypes = [i]
+    lib.gdr_debug_cuda_error_string.restype = ctypes.c_char_p
     lib.gdr_debug_tc_gemm.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
     lib.gdr_debug_tc_gemm.restype = i
     lib.gdr_debug_timeout_selftest.argtypes = [vp, ctypes.c_ulonglong, vp, vp]

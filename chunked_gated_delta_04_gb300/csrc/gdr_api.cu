@@ -19,7 +19,16 @@ int g_stage_n = 0;
 int g_stage_i = 0;
 const char* g_stage_names[kMaxStages];
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<int> g_last_cuda_error{0};  // the last CUDA error an entry point turned into GDR_ERR_CUDA
+
+gdr_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return GDR_OK;
+  g_last_cuda_error.store((int)e, std::memory_order_relaxed);
+  return GDR_ERR_CUDA;
+}
 }  // namespace
+
+gdr_status status_of(cudaError_t e) { return cuda_status(e); }
 
 void stage_begin(cudaStream_t s) {
   g_stage_i = 0;
@@ -260,7 +269,7 @@ gdr_status gdr_fwd(const gdr_problem* p, const void* q, const void* k, const voi
   cudaError_t e = launch_index(d, ws, s);
   if (e == cudaSuccess) e = apply_prologue(d, a, ws, s);
   if (e == cudaSuccess) e = d.path == 1 ? tc_forward(d, a, ws, s) : simt_forward(d, a, ws, s);
-  return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+  return cuda_status(e);
 }
 
 gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
@@ -291,7 +300,7 @@ gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const voi
   if (e == cudaSuccess) e = d.path == 1 ? tc_backward(d, a, ws, s) : simt_backward(d, a, ws, s);
   // gradients w.r.t. the raw inputs (in place; after the v-head group sum when Hv > Hk)
   if (e == cudaSuccess) e = launch_prologue_bwd(d, q, k, g, beta, dq, dk, dg, dbeta, s);
-  return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+  return cuda_status(e);
 }
 
 gdr_status gdr_workspace_status(const void* workspace, gdr_stream_t stream, uint32_t* flags) {
@@ -306,6 +315,10 @@ gdr_status gdr_workspace_status(const void* workspace, gdr_stream_t stream, uint
   if (word & (kDevErrTimeoutFwd | kDevErrTimeoutBwd | kDevErrTimeoutPrep)) return GDR_ERR_TIMEOUT;
   return GDR_OK;
 }
+
+int gdr_debug_last_cuda_error(void) { return g_last_cuda_error.load(std::memory_order_relaxed); }
+
+const char* gdr_debug_cuda_error_string(int e) { return cudaGetErrorString((cudaError_t)e); }
 
 void gdr_debug_set_stage_events(void** events, int n) {
   g_stage_events = (cudaEvent_t*)events;

@@ -76,6 +76,10 @@ struct Workspace {
   void* bn;
 };
 
+// GDR_OK for cudaSuccess; otherwise records e for gdr_debug_last_cuda_error and returns
+// GDR_ERR_CUDA.
+gdr_status status_of(cudaError_t e);
+
 // Validates *p and fills *d (the checks of gdr_fwd / gdr_bwd on the problem itself).
 gdr_status resolve_problem(const gdr_problem* p, Dims* d);
 

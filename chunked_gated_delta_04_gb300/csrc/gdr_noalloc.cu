@@ -122,7 +122,7 @@ extern "C" gdr_status gdr_fwd_noalloc(const gdr_problem* p, const void* q, const
   cudaError_t e = launch_index(d, ws, s);
   if (e == cudaSuccess) e = apply_prologue(d, a, ws, s);
   if (e == cudaSuccess) e = d.path == 1 ? tc_forward(d, a, ws, s) : simt_forward(d, a, ws, s);
-  return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+  return status_of(e);
 }
 
 extern "C" gdr_status gdr_noalloc_status(gdr_stream_t stream, uint32_t* flags) {

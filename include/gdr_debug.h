@@ -15,6 +15,10 @@
  *
  * Launch counter: gdr_debug_launch_count() returns how many kernels this process
  * has launched through the library so far.
+ *
+ * CUDA errors: when an entry point returns GDR_ERR_CUDA, gdr_debug_last_cuda_error()
+ * gives the cudaError_t behind it (0 if none has occurred in this process) and
+ * gdr_debug_cuda_error_string() its text.
  */
 #ifndef GDR_DEBUG_H_
 #define GDR_DEBUG_H_
@@ -27,6 +31,8 @@ void gdr_debug_set_stage_events(void** events, int n);
 int gdr_debug_stage_count(void);
 const char* gdr_debug_stage_name(int i);
 unsigned long long gdr_debug_launch_count(void);
+int gdr_debug_last_cuda_error(void);
+const char* gdr_debug_cuda_error_string(int e);
 
 /* Device self-test of the tensor-core operand layouts: one tcgen05 GEMM on one CTA,
  * D[m][n] = sum_k Amat[m][k] Bmat[k][n] (M = 128, N in {64, 128}, K in {64, 128}),
