@@ -162,8 +162,9 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
 }
 
 // Saved buffer: the chunk-start states, then (save_wy, tensor-core path only) per region,
-// 256-byte aligned: gamma fp32 [chunks][Hv][64], W bf16 [..][64][DK], U bf16 [..][64][DV],
-// P bf16 [..][64][64], T bf16 [..][64][64].
+// 256-byte aligned: gamma fp32 [chunks][Hv][64], W bf16 [..][64][DK], U bf16 [..][64][DV]
+// (replaced by Vn = U - W h by the forward's state kernel), P bf16 [..][64][64], T bf16
+// [..][64][64].
 static size_t saved_layout(const Dims& d, const char* base, Workspace* ws) {
   const size_t chH = (size_t)d.max_chunks * d.Hv;
   size_t off = align256(chH * d.DK * d.DV * (d.h_bf16 ? 2 : 4));

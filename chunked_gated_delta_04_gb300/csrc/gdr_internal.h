@@ -45,7 +45,7 @@ struct Workspace {
   int* seq_order;      // [num_seqs] sequences, longest first
   // intermediates (fp32 on the SIMT path, bf16 on the tensor-core path)
   void* W;       // [max_chunks][Hv][64][DK]
-  void* U;       // [max_chunks][Hv][64][DV]
+  void* U;       // [max_chunks][Hv][64][DV]; tensor-core backward: Vn = U - W h in its place
   void* P;       // tensor-core path: [max_chunks][Hv][64][64]
   float* gam;    // [max_chunks][Hv][64] in-chunk cumsum of g
   void* Vn;      // [max_chunks][Hv][64][DV]

@@ -804,6 +804,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
       if (kSingle && c + 1 < c_end) load_wq(c + 1);  // [W|Q] and gamma were last read by [W;Q] h
     }
     GDR_TRACE_MARK(1, 2);
+    float vn_keep[32];  // saved factors: this thread's Vn row slice, stored once the chain has moved on
     if (ok) {
       if (warp < 2) {  // Vn = U - W h (rows >= len are zero: W and U are zero there)
         if (warp == 1) GDR_DELAY(4);
@@ -815,6 +816,8 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
 #pragma unroll
         for (int b = 0; b < 32; ++b) u[b] = uok ? u[b] - x[b] : 0.f;
         st_col32_bf16(sm + SS::VNT, r, u);
+#pragma unroll
+        for (int b = 0; b < 32; ++b) vn_keep[b] = u[b];
         const float dec = fexp(gC - gr);
 #pragma unroll
         for (int b = 0; b < 32; ++b) u[b] *= dec;
@@ -855,6 +858,10 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
         tc::mma_bf16(D2, tc::kmajor_step_desc(s_up, kSlab, kk), tc::kmajor_step_desc(s_vnt, 4096, kk), id, kk > 0);
       tc::mma_commit(&bar_pv);
     }
+    // saved factors: Vn replaces U in the saved buffer (the backward reads Vn; each slice writes
+    // only its own columns, which no other CTA reads), off the chain: after the MMA issue
+    if (ok && d.save_wy && warp < 2)
+      st_global_bf16x32(reinterpret_cast<bf16*>(ws.U) + (chh * 64 + r) * 128 + dv0, vn_keep);
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutFwd));
     mma_phase ^= 1;
     tc::tc_fence_after();

@@ -8,8 +8,9 @@
 //            dVn = scale P^T dO + diag(e^{gamma_C - gamma}) K dh'
 //            dh  = e^{gamma_C} dh' + scale Q^T diag(e^gamma) dO - W^T dVn
 //          writes dh' and dVn of every chunk (bf16) and dS0.
-//   grad   one CTA per (chunk, v-head), everything on chip:
-//            Vn = U - W h,  dP = scale (dO Vn^T) * Gam,
+//   grad   one CTA per (chunk, v-head), everything on chip, from Vn = U - W h (left in U's
+//          place by the forward with saved chunk factors, else by tc_vn_kernel):
+//            dP = scale (dO Vn^T) * Gam,
 //            dq = scale diag(e^gamma) dO h^T + dP K,
 //            dk = dP^T Q + diag(e^{gamma_C - gamma}) Vn dh'^T + ...,  dW = -dVn h^T,
 //          then the WY backward through W = T' K, U = T'' V, T = (I + A)^{-1}:
@@ -377,6 +378,116 @@ __global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
 }
 
 // ---------------------------------------------------------------------------------
+// vn: Vn = U - W h of every (chunk, v-head), written over U.  The gradient kernels read Vn
+// from U's place; with saved chunk factors the forward's state kernel leaves it there, with
+// recomputed factors this kernel does, after the chunk prep.  Persistent, one CTA per SM.
+// ---------------------------------------------------------------------------------
+struct VnSmem {
+  static constexpr uint32_t W = 0;       // W, two 64-column slabs; the M = 128 operand's unused
+                                          // rows read the next 16 KB (U)
+  static constexpr uint32_t U = 16384;   // U, two slabs
+  static constexpr uint32_t H = 32768;   // h bf16: two slabs of [128 dk][64 dv]
+  static constexpr uint32_t HF = 65536;  // h fp32 as landed: four slabs of [128][32]
+  static constexpr uint32_t BYTES = HF + 65536;
+};
+
+__global__ void __launch_bounds__(kTcThreads) tc_vn_kernel(const __grid_constant__ CUtensorMap tm_w,
+                                                          const __grid_constant__ CUtensorMap tm_u,
+                                                          const __grid_constant__ CUtensorMap tm_h, Dims d,
+                                                          Workspace ws) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = align1024(smem_raw);
+  using S = VnSmem;
+  __shared__ uint64_t bar_tma, bar_mma;
+  __shared__ uint32_t tmem_slot;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) {
+    tc::mbar_init(&bar_tma, 1);
+    tc::mbar_init(&bar_mma, 1);
+    tc::fence_barrier_init();
+  }
+  if (warp == 0) tc::tmem_alloc<128>(&tmem_slot);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tb = tmem_slot;
+  const int Hv = d.Hv, n_items = d.max_chunks * Hv;
+  bool ok = true;
+  uint32_t par = 0;
+  for (int w = (int)blockIdx.x; w < n_items && ok; w += (int)gridDim.x) {
+    const int c = w / Hv, j = w % Hv;
+    const int len = ws.chunks[c].z;
+    if (len <= 0) continue;  // an empty chunk slot (uniform across the CTA)
+    const size_t ch = (size_t)c * Hv + j;
+    if (tid == 0) {
+      tc::mbar_arrive_expect_tx(&bar_tma, (d.h_bf16 ? 8 : 12) * kSlab);
+      tc::tma_load_2d(sm + S::W, &tm_w, &bar_tma, 0, (int)(ch * 64));
+      tc::tma_load_2d(sm + S::W + kSlab, &tm_w, &bar_tma, 64, (int)(ch * 64));
+      tc::tma_load_2d(sm + S::U, &tm_u, &bar_tma, 0, (int)(ch * 64));
+      tc::tma_load_2d(sm + S::U + kSlab, &tm_u, &bar_tma, 64, (int)(ch * 64));
+      for (int q4 = 0; q4 < 4; ++q4) {
+        if (d.h_bf16)  // straight into the operand tile: rows (q4 & 1) * 64.., columns (q4 >> 1) * 64..
+          tc::tma_load_2d(sm + S::H + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_h, &bar_tma, (q4 >> 1) * 64,
+                          (int)(ch * 128 + (q4 & 1) * 64));
+        else  // 32 fp32 columns of all 128 rows
+          tc::tma_load_2d(sm + S::HF + q4 * 16384, &tm_h, &bar_tma, q4 * 32, (int)(ch * 128));
+      }
+    }
+    ok = __syncthreads_and(tc::mbar_wait(&bar_tma, par, ws.status, kDevErrTimeoutBwd));
+    if (ok && !d.h_bf16) {  // h fp32 -> bf16 operand, row tid (128-byte-swizzled 32-column slabs)
+      float hv[64];
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const unsigned char* src = sm + S::HF + (2 * hh + q) * 16384 + tid * 128;
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 f = *reinterpret_cast<const float4*>(src + (((c4 ^ (tid & 7)) & 7) << 4));
+            hv[q * 32 + 4 * c4] = f.x;
+            hv[q * 32 + 4 * c4 + 1] = f.y;
+            hv[q * 32 + 4 * c4 + 2] = f.z;
+            hv[q * 32 + 4 * c4 + 3] = f.w;
+          }
+        }
+        st_row_bf16(sm + S::H + hh * 16384, tid, hv);
+      }
+    }
+    tc::fence_proxy_async_smem();
+    tc::tc_fence_before();
+    __syncthreads();
+    if (ok && tid == 0) {  // W h: rows 0-63 (lanes 0-63)
+      tc::tc_fence_after();
+      tc::gemm(tb, kmaj(sm + S::W, kSlab), mnmaj(sm + S::H, 16384), 128, 8, false);
+      tc::mma_commit(&bar_mma);
+    }
+    ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, par, ws.status, kDevErrTimeoutBwd));
+    tc::tc_fence_after();
+    if (ok && warp < 2) {  // row r = tid: Vn = U - W h, zero past the chunk end, over U's row
+      const int r = tid;
+      bf16* dst = reinterpret_cast<bf16*>(ws.U) + (ch * 64 + r) * 128;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        float x[64], u[64];
+        tmem_ld64(tb, warp, 64 * hh, x);
+        ld_row_bf16(sm + S::U + hh * kSlab, r, u);
+#pragma unroll
+        for (int b = 0; b < 64; ++b) u[b] = r < len ? u[b] - x[b] : 0.f;
+        st_global_bf16x32(dst + 64 * hh, u);
+        st_global_bf16x32(dst + 64 * hh + 32, u + 32);
+      }
+    }
+    par ^= 1;
+    tc::tc_fence_before();
+    __syncthreads();  // the tiles and the accumulator are free for the next item
+    tc::tc_fence_after();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tb, 128);
+}
+
+// ---------------------------------------------------------------------------------
 // grad: all gradients of one (chunk, v-head)
 // ---------------------------------------------------------------------------------
 // Shared memory (1024-aligned tiles; later users of a tile noted after the arrow).
@@ -390,9 +501,9 @@ struct GradSmem {
   static constexpr uint32_t DH = 81920;         // dh' (32 KB) -> dq staging
   static constexpr uint32_t H = 114688;         // h bf16 (32 KB) -> dP | dT | X | dAGb (8 KB each);
                                                 //   h fp32 lands in H, H + 16 KB, VN and SCR
-  static constexpr uint32_t VN = 147456;        // Vn (16 KB) -> T'
-  static constexpr uint32_t W = 163840;         // W (16 KB) -> Vn~ -> dv staging
-  static constexpr uint32_t UT = 180224;        // U (16 KB) -> dW
+  static constexpr uint32_t VN = 147456;        // Vn~ (16 KB) -> T'
+  static constexpr uint32_t W = 163840;         // Vn as loaded (16 KB) -> dv staging
+  static constexpr uint32_t UT = 180224;        // dW (16 KB)
   static constexpr uint32_t SCR = 196608;       // fp32 [64][65] scratch for row/column sums
   static constexpr uint32_t GAM = SCR + 16640;  // gamma (256 B)
   static constexpr uint32_t BYTES = GAM + 256;
@@ -472,6 +583,7 @@ __device__ __forceinline__ void grad_body(
   // store), all on the next phase of bar_tma, so the loads overlap the current item.
   bool ok = true;
   uint32_t item_par = 0;  // phase parity of bar_tma / bar_tma2 for the current item
+  uint32_t mma_par = 0;   // phase parity of bar_mma (five commits per item: it alternates)
   // items: (chunk, v-head), or with kPair (chunk, q/k head) shared by the cluster, whose
   // CTA `rank` takes v-head 2 i + rank; with kDyn every real chunk's v-heads, in walk order
   const int n_steps = kDyn ? ws.step_off[d.max_chunks + 1] : 0;
@@ -505,16 +617,16 @@ __device__ __forceinline__ void grad_body(
       if (kDyn && !wait_flag(ws.walk_flags + ch2, (uint32_t)d.walk_units, ws.status, kDevErrTimeoutBwd)) return;
       GDR_TRACE_INFO_ADD(4, GDR_TRACE_NOW() - tf0_);
       GDR_TRACE_SINCE(2, 20, tw0);
-      tc::mbar_arrive_expect_tx(bar, (d.h_bf16 ? 20 : 24) * kSlab + 256);
+      tc::mbar_arrive_expect_tx(bar, (d.h_bf16 ? 18 : 22) * kSlab + 256);
       for (int q4 = 0; q4 < 4; ++q4)  // dh' rows (q4 & 1) * 64.., columns (q4 >> 1) * 64..
         tc::tma_load_2d(sm + S::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
                         (int)(ch2 * 128 + (q4 & 1) * 64));
       tc::tma_load_2d(sm + S::DVN, &tm_dvn, bar, 0, (int)(ch2 * 64));
       tc::tma_load_2d(sm + S::DVN + S::OD_SLAB, &tm_dvn, bar, 64, (int)(ch2 * 64));
     }
-    if (groups & kLdW) {
-      tc::tma_load_2d(sm + S::W, &tm_w, bar, 0, (int)(ch2 * 64));
-      tc::tma_load_2d(sm + S::W + kSlab, &tm_w, bar, 64, (int)(ch2 * 64));
+    if (groups & kLdW) {  // Vn (in U's place in memory) into W's tile, once the dv store has read it
+      tc::tma_load_2d(sm + S::W, &tm_u, bar, 0, (int)(ch2 * 64));
+      tc::tma_load_2d(sm + S::W + kSlab, &tm_u, bar, 64, (int)(ch2 * 64));
     }
     if (groups & kLdRest) {
       tc::bulk_load(sm + S::GAM, ws.gam + ch2 * 64, 256, bar);
@@ -522,8 +634,6 @@ __device__ __forceinline__ void grad_body(
       tc::tma_load_3d(sm + S::KQ + 2 * kSlab, &tm_k, bar, 64, i2, tt);
       tc::tma_load_3d(sm + S::KQ + kSlab, &tm_q, bar, 0, i2, tt);
       tc::tma_load_3d(sm + S::KQ + 3 * kSlab, &tm_q, bar, 64, i2, tt);
-      tc::tma_load_2d(sm + S::UT, &tm_u, bar, 0, (int)(ch2 * 64));
-      tc::tma_load_2d(sm + S::UT + kSlab, &tm_u, bar, 64, (int)(ch2 * 64));
       if (d.h_bf16) {  // h (bf16) straight into its operand tile, laid out like dh'
         for (int q4 = 0; q4 < 4; ++q4)
           tc::tma_load_2d(sm + S::H + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_h, bar, (q4 >> 1) * 64,
@@ -666,29 +776,40 @@ __device__ __forceinline__ void grad_body(
   }
   float hdh = warp_sum((hdh4[0] + hdh4[1]) + (hdh4[2] + hdh4[3]));
   if (lane == 0) s_red[warp] = hdh;
-  if (ok && lo) {  // O-hat = scale diag(e^gamma) dO, zero past the chunk end (half hf of row r)
+  if (ok && lo) {  // half hf of row r
     float x[64];
+    // O-hat = scale diag(e^gamma) dO, zero past the chunk end
     const float e = r < len ? d.scale * s_eg[r] : 0.f;
     ld_row_bf16(sm + S::DO + hf * kSlab, r, x);
 #pragma unroll
     for (int b = 0; b < 64; ++b) x[b] *= e;
     st_row_bf16(sm + S::OH + hf * S::OD_SLAB, r, x);
+    // Vn~ = diag(e^{gamma_C - gamma}) Vn (Vn arrives in W's tile) into VN's tile, which the fp32
+    // h no longer occupies past the conversion's barrier
+    ld_row_bf16(sm + S::W + hf * kSlab, r, x);
+#pragma unroll
+    for (int b = 0; b < 64; ++b) x[b] *= dec;
+    st_row_bf16(sm + S::VN + hf * kSlab, r, x);
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   hdh = ((s_red[0] + s_red[1]) + (s_red[2] + s_red[3])) + ((s_red[4] + s_red[5]) + (s_red[6] + s_red[7]));
   GDR_TRACE_MARK(2, 1);
-  // P2: [K;Q] K^T (0-63), W h (64-191), [O-hat; dVn] h^T (256-383): lanes 0-63 start dq,
-  // lanes 64-127 are dVn h^T = -dW
+  // P2: [K;Q] K^T (0-63: K K^T on lanes 0-63, Q K^T on lanes 64-127), [O-hat; dVn] h^T
+  // (256-383: lanes 0-63 start dq, lanes 64-127 are dVn h^T = -dW), dO Vn^T (64-127, lanes
+  // 64-127: the operand's rows start one slab early) and dk = Vn~ dh'^T (384-511)
   if (ok && tid == 0) {
     tc::tc_fence_after();
     tc::gemm(C_KK, kmaj(sm + S::KQ, 2 * kSlab), kmaj(sm + S::KQ, 2 * kSlab), 64, 8, false);
-    tc::gemm(tb + 64, kmaj(sm + S::W, kSlab), mnmaj(sm + S::H, 16384), 128, 8, false);
     tc::gemm(C_DQ, kmaj(sm + S::OD, S::OD_SLAB), kmaj(sm + S::H, 16384), 128, 8, false);
+    GDR_DELAY(22);
+    tc::gemm(tb + 64, kmaj(sm + S::DO - kSlab, kSlab), kmaj(sm + S::W, kSlab), 64, 8, false);
+    tc::gemm(C_DK, kmaj(sm + S::VN, kSlab), kmaj(sm + S::DH, 16384), 128, 8, false);
     tc::mma_commit(&bar_mma);
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
+  mma_par ^= 1;
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 2);
   if (ok && tid == kCopyTid) {  // O-hat and h are consumed: fetch V and T for the WY backward
@@ -696,6 +817,11 @@ __device__ __forceinline__ void grad_body(
     tc::tma_load_3d(sm + S::V, &tm_v, &bar_tma2, 0, j, t0);
     tc::tma_load_3d(sm + S::V + S::OD_SLAB, &tm_v, &bar_tma2, 64, j, t0);
     tc::tma_load_2d(sm + S::T, &tm_t, &bar_tma2, 0, (int)(ch * 64));
+  }
+  if (kDyn && tid == kCopyTid) pre_c = pre_w < n_items ? chunk_of(pre_w) : 0;  // used after R2
+  if (kPair && tid == 0) {  // P2 was the last reader of DH and DO: the partner may fill them
+    tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&bar_qfree), peer));
+    tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&bar_kfree), peer));
   }
   float* scr = reinterpret_cast<float*>(sm + S::SCR);
   auto col_partial = [&](float (*dst)[64]) {
@@ -712,107 +838,57 @@ __device__ __forceinline__ void grad_body(
     dst[g][cc] = (a0 + a1) + (a2 + a3);
   };
   if (ok) {
-    if (lo) {  // row r, columns [64 hf, 64 hf + 64)
+    if (lo) {  // row r, columns [64 hf, +64): q_r . (O-hat h^T)[r] and k_r . (Vn~ dh'^T)[r]
       float x[64], u[64];
-      tmem_ld64(tb, warp, 64 + hf * 64, x);  // (W h)[r]
-      ld_row_bf16(sm + S::UT + hf * kSlab, r, u);
-#pragma unroll
-      for (int b = 0; b < 64; ++b) u[b] = r < len ? u[b] - x[b] : 0.f;
-      st_row_bf16(sm + S::VN + hf * kSlab, r, u);
-#pragma unroll
-      for (int b = 0; b < 64; ++b) u[b] *= dec;
-      st_row_bf16(sm + S::W + hf * kSlab, r, u);  // Vn~ (W no longer needed)
-      tmem_ld64(tb, warp, 256 + hf * 64, x);     // (O-hat h^T)[r]
+      tmem_ld64(tb, warp, 256 + hf * 64, x);                    // (O-hat h^T)[r]
       ld_row_bf16(sm + S::KQ + kSlab + hf * 2 * kSlab, r, u);  // q_r
-      float qh4[4] = {0.f, 0.f, 0.f, 0.f};
+      float a4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int b = 0; b < 64; ++b) qh4[b & 3] += x[b] * u[b];
-      s_qh[hf][r] = (qh4[0] + qh4[1]) + (qh4[2] + qh4[3]);
-    } else {  // Q K^T row r, columns [32 hf, 32 hf + 32) -> scratch (fp32)
-      float x[32];
-      tmem_ld32w(tb, warp, 32 * hf, x);
+      for (int b = 0; b < 64; ++b) a4[b & 3] += x[b] * u[b];
+      s_qh[hf][r] = (a4[0] + a4[1]) + (a4[2] + a4[3]);
+      tmem_ld64(tb, warp, 384 + hf * 64, x);                    // (Vn~ dh'^T)[r]
+      ld_row_bf16(sm + S::KQ + hf * 2 * kSlab, r, u);           // k_r
+      float k4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int s = 0; s < 32; ++s) scr[r * 65 + 32 * hf + s] = x[s];
+      for (int b = 0; b < 64; ++b) k4[b & 3] += x[b] * u[b];
+      s_kdv[hf][r] = (k4[0] + k4[1]) + (k4[2] + k4[3]);        // e^{gamma_C - gamma_r} k_r^T dh' vn_r
+    } else {  // lanes 64-127, row r
+      {         // -dW, columns [64 hf, +64), into U's tile (not loaded: Vn comes ready)
+        float x[64];
+        tmem_ld64(tb, warp, 256 + hf * 64, x);
+#pragma unroll
+        for (int b = 0; b < 64; ++b) x[b] = -x[b];
+        st_row_bf16(sm + S::DW + hf * kSlab, r, x);
+      }
+      if (warp == 7) GDR_DELAY(21);
+      // dP and dP * QK, columns [32 hf, +32)
+      float x[32], qk[32];
+      tmem_ld32w(tb, warp, 64 + 32 * hf, x);  // (dO Vn^T)[r]
+      tmem_ld32w(tb, warp, 32 * hf, qk);      // (Q K^T)[r]
+      float rowpp4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int s = 0; s < 32; ++s) {
+        const int sc = 32 * hf + s;
+        const float dp = (sc <= r && r < len) ? d.scale * x[s] * fexp(gr - sgam[sc]) : 0.f;
+        x[s] = dp;
+        qk[s] *= dp;
+        rowpp4[s & 3] += qk[s];
+      }
+#pragma unroll
+      for (int s = 0; s < 32; ++s) scr[r * 65 + 32 * hf + s] = qk[s];
+      st_halfrow_bf16(sm + S::DP, r, hf, x);  // dP (h no longer needed)
+      s_rowpp[hf][r] = (rowpp4[0] + rowpp4[1]) + (rowpp4[2] + rowpp4[3]);
     }
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
   __syncthreads();
   GDR_TRACE_MARK(2, 3);
-  // P4: dO Vn^T (64-127, lanes 64-127: the operand's rows start one slab early, so dP is the
-  // other lane half's epilogue), K dh' (128-255), dk = Vn~ dh'^T (384-511)
-  if (ok && tid == 0) {
-    GDR_DELAY(22);
-    tc::tc_fence_after();
-    tc::gemm(tb + 64, kmaj(sm + S::DO - kSlab, kSlab), kmaj(sm + S::VN, kSlab), 64, 8, false);
-    tc::gemm(tb + 128, kmaj(sm + S::KQ, 2 * kSlab), mnmaj(sm + S::DH, 16384), 128, 8, false);
-    tc::gemm(C_DK, kmaj(sm + S::W, kSlab), kmaj(sm + S::DH, 16384), 128, 8, false);
-    tc::mma_commit(&bar_mma);
-  }
-  if (ok && !lo) {  // while P4 runs: -dW from lanes 64-127 of the stacked product into U's tile,
-                    // whose readers finished before the barrier above (row r, half hf)
-    tc::tc_fence_after();
-    float x[64];
-    tmem_ld64(tb, warp, 256 + hf * 64, x);
-#pragma unroll
-    for (int b = 0; b < 64; ++b) x[b] = -x[b];
-    st_row_bf16(sm + S::DW + hf * kSlab, r, x);
-  }
-  tc::fence_proxy_async_smem();
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
-  tc::tc_fence_after();
-  if (kDyn && tid == kCopyTid) pre_c = pre_w < n_items ? chunk_of(pre_w) : 0;  // used after R2
-  if (kPair && tid == 0) {  // P4 was the last reader of DH and DO: the partner may fill them
-    tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&bar_qfree), peer));
-    tc::mbar_arrive_cluster(tc::mapa(tc::smem_u32(&bar_kfree), peer));
-  }
-  GDR_TRACE_MARK(2, 4);
-  if (ok && !lo) {  // lanes 64-127: dP and dP * QK for row r, columns [32 hf, 32 hf + 32)
-    if (warp == 7) GDR_DELAY(21);
-    {
-      float x[32], gs[32], qk[32];
-      tmem_ld32w(tb, warp, 64 + 32 * hf, x);  // (dO Vn^T)[r]
-#pragma unroll
-      for (int s = 0; s < 32; ++s) {
-        gs[s] = sgam[32 * hf + s];
-        qk[s] = scr[r * 65 + 32 * hf + s];
-      }
-      float rowpp4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int s = 0; s < 32; ++s) {
-        const int sc = 32 * hf + s;
-        const float dp = (sc <= r && r < len) ? d.scale * x[s] * fexp(gr - gs[s]) : 0.f;
-        x[s] = dp;
-        qk[s] *= dp;
-        rowpp4[s & 3] += qk[s];
-      }
-      const float rowpp = (rowpp4[0] + rowpp4[1]) + (rowpp4[2] + rowpp4[3]);
-#pragma unroll
-      for (int s = 0; s < 32; ++s) scr[r * 65 + 32 * hf + s] = qk[s];
-      st_halfrow_bf16(sm + S::DP, r, hf, x);  // dP (h no longer needed)
-      s_rowpp[hf][r] = rowpp;
-    }
-  }
-  if (ok && lo) {  // lanes 0-63 meanwhile
-    float kdv4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-    for (int q = 0; q < 2; ++q) {  // (K dh')[r] . Vn[r] over columns [64 hf + 32 q, +32)
-      float x[32], v[32];
-      tmem_ld32w(tb, warp, 128 + 64 * hf + 32 * q, x);
-      ld_halfrow_bf16(sm + S::VN + hf * kSlab, r, q, v);
-#pragma unroll
-      for (int b = 0; b < 32; ++b) kdv4[b & 3] += x[b] * v[b];
-    }
-    s_kdv[hf][r] = (kdv4[0] + kdv4[1]) + (kdv4[2] + kdv4[3]);
-  }
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before();
-  __syncthreads();
   if (ok) col_partial(s_colpp);  // column sums of dP * QK
-  if (ok && tid < 64) {  // full k^T dh' vn per row
+  if (ok && tid < 64) {  // sum_s e^{gC - g_s} k_s^T dh' vn_s
     const float kdv = tid < len ? s_kdv[0][tid] + s_kdv[1][tid] : 0.f;
     s_kdv[0][tid] = kdv;
-    const float part = warp_sum(tid < len ? fexp(gC - sgam[tid]) * kdv : 0.f);  // sum_s e^{gC - g_s} k_s^T dh' vn_s
+    const float part = warp_sum(kdv);
     if (lane == 0) s_red[warp] = part;
   }
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_tma2, item_par, ws.status, kDevErrTimeoutBwd));
@@ -827,7 +903,8 @@ __device__ __forceinline__ void grad_body(
     tc::gemm(tb + 128, kmaj(sm + S::OD, S::OD_SLAB), kmaj(sm + S::V, S::OD_SLAB), 64, 8, false);
     tc::mma_commit(&bar_mma);
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
+  mma_par ^= 1;
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 6);
   if (ok && !lo) {
@@ -884,7 +961,8 @@ __device__ __forceinline__ void grad_body(
     tc::gemm(tb + 64, mnmaj(sm + S::T - kSlab, kSlab), mnmaj(sm + S::DT, kSlab), 64, 4, false);
     tc::mma_commit(&bar_mma);
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
+  mma_par ^= 1;
   tc::tc_fence_after();
   if (ok && tid == kCopyTid && pending >= 0) {  // dVn is consumed, dq has left its staging tile
     GDR_TRACE_CLK(tb21);
@@ -942,7 +1020,8 @@ __device__ __forceinline__ void grad_body(
     tc::gemm(tb + 64, kmaj(sm + S::XT, kSlab), kmaj(sm + S::T, kSlab), 64, 4, false);
     tc::mma_commit(&bar_mma);
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 0, ws.status, kDevErrTimeoutBwd));
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
+  mma_par ^= 1;
   tc::tc_fence_after();
   if (ok && tid == kCopyTid && pending >= 0) {  // dv has left its staging tile (W)
     GDR_TRACE_CLK(tb22);
@@ -989,7 +1068,8 @@ __device__ __forceinline__ void grad_body(
     tc::gemm(C_DK, mnmaj(sm + S::DAG, kSlab), mnmaj(sm + S::KQ, 2 * kSlab), 128, 4, true);
     tc::mma_commit(&bar_mma);
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutBwd));
+  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
+  mma_par ^= 1;
   tc::tc_fence_after();
   if (ok && tid == kCopyTid && pending >= 0) {  // every operand tile but dO (dk staging) is free
     issue_loads(kDyn ? cl_w : wnext, kDyn ? cl_c : cnext, kLdRest);
@@ -1021,7 +1101,7 @@ __device__ __forceinline__ void grad_body(
       if (r < len) dbeta[(size_t)(t0 + r) * Hv + j] = __float2bfloat16_rn(eg * colbk + dbv + akk);
       float dgm = 0.f;
       if (r < len) {
-        dgm = (s_rowpp[0][r] + s_rowpp[1][r]) - colpp + (s_qh[0][r] + s_qh[1][r]) - dec * s_kdv[0][r] +
+        dgm = (s_rowpp[0][r] + s_rowpp[1][r]) - colpp + (s_qh[0][r] + s_qh[1][r]) - s_kdv[0][r] +
               br * eg * colbk + (s_rowaa[0][r] + s_rowaa[1][r]) - colaa;
         if (r == len - 1) dgm += fexp(gC) * hdh + (s_red[0] + s_red[1]);
       }
@@ -1186,6 +1266,13 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
   int dev = 0, n_sm = 1;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (!d.save_wy && d.max_chunks > 0 && Tt > 0) {  // recomputed factors: Vn over U (see tc_vn_kernel)
+    const long long n_items = (long long)d.max_chunks * d.Hv;
+    const size_t smv = VnSmem::BYTES + 1024;
+    cudaFuncSetAttribute(tc_vn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smv);
+    tc_vn_kernel<<<(unsigned)(n_items < n_sm ? n_items : n_sm), kTcThreads, smv, s>>>(tw, tu, thf, d, ws);
+    stage_mark(s, "bwd_vn");
+  }
   // Walk units per (sequence, v-head): the two DV halves (shorter epilogues, so a shorter
   // chain) while the walk units fill at most a quarter of the SMs, i.e. when there are so few
   // chains that the walk is the critical path; else one unit over all of DV, which takes half

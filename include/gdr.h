@@ -102,7 +102,7 @@ typedef struct {
                                 rounded states, so its gradients carry that rounding) */
   unsigned int prologue;     /* bit set of gdr_prologue_flags; 0 = inputs used as given */
   int save_wy;               /* 0 or 1.  1: the forward also keeps its per-chunk factors
-                                (gamma, W, U, P and T of the WY form, see "Saved factors"
+                                (gamma, W, Vn, P and T of the WY form, see "Saved factors"
                                 below) in the saved buffer after the states, and the
                                 backward reads them instead of recomputing them.  Same
                                 results bit for bit; honoured on the tensor-core path,
@@ -118,10 +118,11 @@ size_t gdr_max_chunks(const gdr_problem* p);
  * factors.
  * Saved factors (save_wy): after the states, per (chunk, v-head) of the chunk index, in
  * this order, each region starting 256-byte aligned: gamma fp32 [64] (in-chunk cumulative
- * sum of g), W bf16 [64][DK], U bf16 [64][DV], P bf16 [64][64], T bf16 [64][64] (chunked
+ * sum of g), W bf16 [64][DK], Vn bf16 [64][DV], P bf16 [64][64], T bf16 [64][64] (chunked
  * WY form of the gated delta rule: T = (I + strictly lower diag(beta) Gamma K K^T)^{-1},
- * W = T diag(beta e^gamma) K, U = T diag(beta) V, P = masked decayed Q K^T).  gdr_bwd
- * requires them to come from gdr_fwd with the same problem and inputs. */
+ * W = T diag(beta e^gamma) K, U = T diag(beta) V, Vn = U - W h with h the chunk-start
+ * state, P = masked decayed Q K^T).  gdr_bwd requires them to come from gdr_fwd with the
+ * same problem and inputs. */
 size_t gdr_saved_states_bytes(const gdr_problem* p);
 
 /* Bytes of the scratch workspace that gdr_fwd / gdr_bwd need (device memory,
