@@ -94,7 +94,6 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
                 ? 1
                 : 0;
   d->save_wy = d->path == 1 ? p->save_wy : 0;
-  d->walk_units = 2;  // chosen per launch by the tensor-core backward
   return GDR_OK;
 }
 

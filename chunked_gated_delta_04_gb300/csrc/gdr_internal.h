@@ -34,7 +34,6 @@ struct Dims {
   int h_bf16;  // h_saved holds bf16 (else fp32)
   int prologue;  // gdr_prologue_flags bits
   int save_wy;   // tensor-core path: gamma, W, U, P, T live in the saved buffer (see attach_saved_factors)
-  int walk_units;  // tensor-core backward: walk units per (sequence, v-head): 2 (DV halves) or 1
 };
 
 // Pointers into the caller's workspace.  Every region starts 256-byte aligned.

@@ -55,29 +55,47 @@ __device__ __forceinline__ void st_global_bf16x32(bf16* dst, const float* v) {
 // ---------------------------------------------------------------------------------
 // walk
 // ---------------------------------------------------------------------------------
-// NC = 64: a walk unit is one half of DV (two units per sequence and v-head, shorter
-// epilogues: for chains that are the critical path).  NC = 128: one unit per sequence and
-// v-head (half the SM time per chain: for batches whose gradients dominate).
-template <int NC>
+// One walk unit = (sequence, v-head), all of DK and DV, chunks in reverse.  dh (dL/dh at the
+// end of the current chunk, "dh'") stays in registers, fp32.  Per chunk, with
+//   K^ = diag(e^{gamma_C - gamma} / scale) K,   Q^ = diag(scale e^gamma) Q
+// formed in place in the chunk's shared-memory tiles (rows past the chunk end zero):
+//   accV = P^T dO + K^ dh'             = dVn / scale  (64 tokens on TMEM lanes 0-63)
+//   dVn  = scale accV, zero past the chunk end
+//   accH = Q^^T dO - W^T dVn           (DK x DV; the minus is the MMA's negate-A bit)
+//   dh   = e^{gamma_C} dh' + accH
+// Roles (12 warps): warps 0-7 run the epilogues (dVn on the four warps of lanes 0-63, dh on
+// all eight) and the four warps of lanes 64-127 form the next chunk's K^ and Q^ while the dVn
+// epilogue runs; in the third warpgroup, warp 8 (lane 0) issues every MMA, warp 9 (lane 0)
+// stores dh' and dVn of every chunk to the workspace and, with kPublish, counts each chunk
+// into ws.walk_flags once its stores have landed, and warp 10 (lane 0) issues the TMA loads
+// and L2 prefetches.  The roles hand off through mbarriers only.
+// P^T dO and Q^^T dO do not need dh', so they run while the previous chunk's epilogues do: a
+// chunk's chain is the 8 MMAs of K^ dh', the dVn epilogue, the 4 MMAs of W^T dVn and the dh
+// epilogue.  Tiles are loaded one chunk ahead (two stages) after an L2 prefetch one chunk
+// before that.
 struct WalkSmem {
-  // per stage: KQ 32 KB | W 16 KB | P 8 KB | dO (NC/64 slabs of 8 KB) | gamma 256 B (+pad)
-  static constexpr uint32_t KQ = 0, W = 32768, P = 49152, DO = 57344;
-  static constexpr uint32_t GAM = DO + (NC / 64) * 8192;
-  static constexpr uint32_t STAGE = (GAM + 256 + 1023) / 1024 * 1024;
-  static constexpr uint32_t DH = 2 * STAGE;              // dh' as bf16 B operand: NC/64 slabs of 128 rows x 128 B
-  static constexpr uint32_t DVN = DH + (NC / 64) * 16384;  // dVn bf16 [64][NC]
-  static constexpr uint32_t DOS = DVN + (NC / 64) * 8192;  // diag(e^gamma) dO bf16 [64][NC]
-  // NC = 64: a second dVn tile (chunks alternate, so a store has a whole chunk to read its tile)
-  static constexpr uint32_t DVN2 = DOS + (NC / 64) * 8192;
-  static constexpr uint32_t BYTES = DVN2 + (NC == 64 ? 8192 : 0);
+  // per stage: [K | Q] interleaved by 64-column slab (K rows 0-63 and, as the unused rows 64-127
+  // of the M = 128 operand, Q) 32 KB | W 16 KB | dO 16 KB | P 8 KB | gamma 256 B
+  static constexpr uint32_t KQ = 0, W = 32768, DO = 49152, P = 65536, GAM = 73728;
+  static constexpr uint32_t STAGE = 74752;
+  static constexpr uint32_t DH = 2 * STAGE;    // dh' bf16: two slabs of [128 dk][64 dv]
+  static constexpr uint32_t DVN = DH + 32768;  // two dVn tiles (chunks alternate), [64 tokens][128 dv]
+  static constexpr uint32_t BYTES = DVN + 2 * 16384;
 };
+static_assert(WalkSmem::GAM + 256 <= WalkSmem::STAGE && WalkSmem::STAGE % 1024 == 0, "walk stage layout");
 
-constexpr int kWalkThreads = 256;  // two warps per TMEM lane quarter, each on half of the slice's columns
+// 8 epilogue warps, then one warpgroup of roles: MMA, store, load and a spare (setmaxnreg works
+// on whole warpgroups, see tc_bwd_walkgrad_kernel)
+constexpr int kWalkThreads = 384;
+constexpr int kWalkMmaTid = 256;      // lane 0 of warp 8
+constexpr int kWalkCopyTid = 288;     // lane 0 of warp 9
+constexpr int kWalkLoadTid = 320;     // lane 0 of warp 10
+constexpr uint32_t kWalkTmemCols = 512;  // accV x 2 at 0, accH x 2 at 256 (128 columns each)
 
-// Counts one finished slice of a chunk: its TMA stores (async proxy) are complete; order them
-// before the count (proxy fence) and publish it with a GPU-scope release reduction (pairs with
-// the waiter's acquire load).  A full fence (__threadfence) before a relaxed add measured
-// ~1.6k cycles per call on the walk's chain.
+// Counts one finished chunk: its TMA stores (async proxy) are complete; order them before the
+// count (proxy fence) and publish it with a GPU-scope release reduction (pairs with the
+// waiter's acquire load).  A full fence (__threadfence) before a relaxed add measured ~1.6k
+// cycles per call.
 __device__ __forceinline__ void publish_chunk(uint32_t* flag) {
   asm volatile("fence.proxy.async.global;" ::: "memory");
   asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(flag) : "memory");
@@ -100,266 +118,348 @@ __device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t target,
   return true;
 }
 
-// One walk unit = (sequence, v-head, NC-wide DV slice); `unit` = (seq rank * Hv + v-head) *
-// (128 / NC) + slice, sequences longest first.  tb: 4 NC TMEM columns owned by the caller.
-// With kPublish the copy thread counts each chunk into ws.walk_flags[chunk * Hv + v-head] once
-// its dh' and dVn tiles have fully reached memory (the fused walk + gradient kernel waits on it).
-template <int NC, bool kPublish>
+// Bounded wait made uniform across the calling warp (every lane waits on the same barrier).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32_t* status, uint32_t bit) {
+  return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity, status, bit));
+}
+
+// One walk unit; `unit` = sequence rank (longest first) * Hv + v-head.  tb: the caller's 512
+// TMEM columns.  Every thread of the CTA (kWalkThreads) calls it.
+template <bool kPublish>
 __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_w,
                                           const CUtensorMap& tm_p, const CUtensorMap& tm_do,
                                           const CUtensorMap& tm_dhs, const CUtensorMap& tm_dvs, const Dims& d,
                                           const float* __restrict__ dS_T, float* __restrict__ dS0,
                                           const Workspace& ws, int unit, uint32_t tb, unsigned char* sm) {
-  using WS = WalkSmem<NC>;
-  constexpr int kSl = 128 / NC;     // walk units per (sequence, v-head)
-  constexpr int CPT = NC / 2;       // columns per thread: half hf of the slice
-  constexpr int NSL = NC / 64;      // 64-column slabs of the slice
-  __shared__ uint64_t bar_load[2], bar_mma;
-  const int n = ws.seq_order[unit / (kSl * d.Hv)], j = (unit / kSl) % d.Hv, i = j / d.G;
-  const int dv0 = (unit % kSl) * NC;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int hf = warp >> 2;            // column half [CPT hf, CPT hf + CPT) of the slice
-  const int dk = tid & 127;            // TMEM lane = row of the dh' slice
-  const int r = tid & 63;              // token row for the 64-row products (lanes 0-63)
-  const bool lo = (warp & 3) < 2;      // warps on TMEM lanes 0-63
-  // thread 0 issues the MMAs; thread 64 (the "copy thread", in a warp that has no part in
-  // the dVn rows) issues every TMA load and store and waits on their bulk groups
-  constexpr int kCopyTid = 64;
+  using WS = WalkSmem;
+  __shared__ uint64_t bar_load[2], bar_scaled[2], bar_vfull[2], bar_hfull[2], bar_dvn[2], bar_dvnfree[2];
+  __shared__ uint64_t bar_dh, bar_dhfree, bar_drain;
+  const int n = ws.seq_order[unit / d.Hv], j = unit % d.Hv, i = j / d.G;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hv = d.Hv;
   const int c_begin = ws.seq_chunk_off[n], c_end = ws.seq_chunk_off[n + 1];
+  const int nch = c_end - c_begin;
   const int t_seq = d.cu ? d.cu[n] : n * d.T;
   const int L = d.cu ? d.cu[n + 1] - t_seq : d.T;
+  uint32_t* const status = ws.status;
+  constexpr uint32_t kBit = kDevErrTimeoutBwd;
+  // walk step it = 0, 1, ... is chunk c_end - 1 - it (stage it & 1); its first token, length
+  auto chunk_of = [&](int it) { return c_end - 1 - it; };
+  auto tok0_of = [&](int it) { return t_seq + (nch - 1 - it) * 64; };
+  auto len_of = [&](int it) { return min(64, L - (nch - 1 - it) * 64); };
+  const uint32_t accV0 = tb, accH0 = tb + 256;
 
   if (tid == 0) {
-    tc::mbar_init(&bar_load[0], 1);
-    tc::mbar_init(&bar_load[1], 1);
-    tc::mbar_init(&bar_mma, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&bar_load[s], 1);
+      tc::mbar_init(&bar_scaled[s], 4);
+      tc::mbar_init(&bar_vfull[s], 1);
+      tc::mbar_init(&bar_hfull[s], 1);
+      tc::mbar_init(&bar_dvn[s], 8);
+      tc::mbar_init(&bar_dvnfree[s], 1);
+    }
+    tc::mbar_init(&bar_dh, 8);
+    tc::mbar_init(&bar_dhfree, 1);
+    tc::mbar_init(&bar_drain, 1);
     tc::fence_barrier_init();
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  // TMEM: K dh' (0), P^T dO (NC), W^T dVn (2 NC), Q^T diag(e^gamma) dO (3 NC)
-  const uint32_t Da = tb, Db = tb + NC, Dc = tb + 2 * NC, Dd = tb + 3 * NC;
 
-  float dh[CPT];  // dL/dh at the end of the current chunk: row dk, columns dv0 + CPT hf + (0..CPT-1)
-  {
-    const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
-    const int c0 = dv0 + CPT * hf;
-#pragma unroll
-    for (int b = 0; b < CPT; ++b)
-      dh[b] = dS_T ? dS_T[sb + (d.layout == 0 ? (size_t)dk * 128 + c0 + b : (size_t)(c0 + b) * 128 + dk)] : 0.f;
-  }
-  auto issue_loads = [&](int c, int st) {
-    const int tc0 = t_seq + (c - c_begin) * 64;
-    const size_t chh = (size_t)c * Hv + j;
-    unsigned char* base = sm + st * WS::STAGE;
-    uint64_t* bar = &bar_load[st];
-    tc::mbar_arrive_expect_tx(bar, (7 + NSL) * kSlab + 256);
-    tc::bulk_load(base + WS::GAM, ws.gam + chh * 64, 256, bar);
-    tc::tma_load_3d(base + WS::KQ, &tm_k, bar, 0, i, tc0);
-    tc::tma_load_3d(base + WS::KQ + 2 * kSlab, &tm_k, bar, 64, i, tc0);
-    tc::tma_load_3d(base + WS::KQ + kSlab, &tm_q, bar, 0, i, tc0);
-    tc::tma_load_3d(base + WS::KQ + 3 * kSlab, &tm_q, bar, 64, i, tc0);
-    tc::tma_load_2d(base + WS::W, &tm_w, bar, 0, (int)(chh * 64));
-    tc::tma_load_2d(base + WS::W + kSlab, &tm_w, bar, 64, (int)(chh * 64));
-    tc::tma_load_2d(base + WS::P, &tm_p, bar, 0, (int)(chh * 64));
-#pragma unroll
-    for (int sl = 0; sl < NSL; ++sl) tc::tma_load_3d(base + WS::DO + sl * kSlab, &tm_do, bar, dv0 + 64 * sl, j, tc0);
-  };
-  if (tid == kCopyTid && c_begin < c_end) issue_loads(c_end - 1, 0);
-
-  bool ok = true;
-  uint32_t mma_phase = 0;
-  int prev1 = -1, prev2 = -1;  // kPublish: the last two chunks, whose stores may be in flight
-  GDR_TRACE_INIT();
-  // dh' as the B operand: slab CPT hf / 64 holds columns [64 s, 64 s + 64) of the slice; written
-  // here for the first chunk and at the end of each chunk for the next
-  auto stage_dh = [&]() {
-    if constexpr (NC == 64)
-      st_halfrow_bf16(sm + WS::DH, dk, hf, dh);
-    else
-      st_row_bf16(sm + WS::DH + hf * 16384, dk, dh);
-    tc::fence_proxy_async_smem();
-  };
-  stage_dh();
-  tc::tc_fence_before();
-  __syncthreads();
-  for (int it = 0; c_end - 1 - it >= c_begin && ok; ++it) {
-    const int c = c_end - 1 - it, st = it & 1;
-    const uint32_t ld_phase = (it >> 1) & 1;
-    const int len = min(64, L - (c - c_begin) * 64);
-    const size_t chh = (size_t)c * Hv + j;
-    if (tid == kCopyTid) {  // dh' of this chunk -> workspace, straight from the operand tile
-#pragma unroll
-      for (int sl = 0; sl < NSL; ++sl) tc::tma_store_2d(&tm_dhs, sm + WS::DH + sl * 16384, dv0 + 64 * sl, (int)(chh * 128));
-      tc::bulk_commit();
+  if (tid == kWalkLoadTid) {
+    // ---------------------------------------------------------------- load role
+    auto issue_loads = [&](int it) {
+      const int st = it & 1, tc0 = tok0_of(it);
+      const size_t chh = (size_t)chunk_of(it) * Hv + j;
+      unsigned char* base = sm + st * WS::STAGE;
+      uint64_t* bar = &bar_load[st];
+      GDR_DELAY(14);
+      tc::mbar_arrive_expect_tx(bar, 9 * kSlab + 256);
+      tc::bulk_load(base + WS::GAM, ws.gam + chh * 64, 256, bar);
+      tc::tma_load_3d(base + WS::KQ, &tm_k, bar, 0, i, tc0);
+      tc::tma_load_3d(base + WS::KQ + 2 * kSlab, &tm_k, bar, 64, i, tc0);
+      tc::tma_load_3d(base + WS::KQ + kSlab, &tm_q, bar, 0, i, tc0);
+      tc::tma_load_3d(base + WS::KQ + 3 * kSlab, &tm_q, bar, 64, i, tc0);
+      tc::tma_load_3d(base + WS::DO, &tm_do, bar, 0, j, tc0);
+      tc::tma_load_3d(base + WS::DO + kSlab, &tm_do, bar, 64, j, tc0);
+      tc::tma_load_2d(base + WS::P, &tm_p, bar, 0, (int)(chh * 64));
+      tc::tma_load_2d(base + WS::W, &tm_w, bar, 0, (int)(chh * 64));
+      tc::tma_load_2d(base + WS::W + kSlab, &tm_w, bar, 64, (int)(chh * 64));
+    };
+    auto prefetch = [&](int it) {  // the same tiles into L2, a chunk before their load
+      const int tc0 = tok0_of(it);
+      const size_t chh = (size_t)chunk_of(it) * Hv + j;
+      tc::bulk_prefetch_l2(ws.gam + chh * 64, 256);
+      tc::tma_prefetch_l2_3d(&tm_k, 0, i, tc0);
+      tc::tma_prefetch_l2_3d(&tm_k, 64, i, tc0);
+      tc::tma_prefetch_l2_3d(&tm_q, 0, i, tc0);
+      tc::tma_prefetch_l2_3d(&tm_q, 64, i, tc0);
+      tc::tma_prefetch_l2_3d(&tm_do, 0, j, tc0);
+      tc::tma_prefetch_l2_3d(&tm_do, 64, j, tc0);
+      tc::tma_prefetch_l2_2d(&tm_p, 0, (int)(chh * 64));
+      tc::tma_prefetch_l2_2d(&tm_w, 0, (int)(chh * 64));
+      tc::tma_prefetch_l2_2d(&tm_w, 64, (int)(chh * 64));
+    };
+    int loaded = -1;  // last walk step whose tiles were requested
+    if (nch > 0) {
+      issue_loads(0);
+      loaded = 0;
     }
-    GDR_TRACE_MARK(3, 0);
-    ok = __syncthreads_and(tc::mbar_wait(&bar_load[st], ld_phase, ws.status, kDevErrTimeoutBwd));
-    GDR_TRACE_MARK(3, 1);
-    unsigned char* stg = sm + st * WS::STAGE;
-    const float* sgam = reinterpret_cast<const float*>(stg + WS::GAM);
-    const float gC = sgam[len - 1], gr = sgam[r];
-    // the dh'-dependent products first; Q^T diag(e^gamma) dO waits for its scaled operand
-    if (ok && tid == 0) {
+    if (nch > 1) {
+      issue_loads(1);
+      loaded = 1;
+    }
+    if (nch > 2) prefetch(2);
+    // step it + 2 goes into step it's stage once its last MMA (W^T dVn) has completed; the
+    // epilogue warps stop reading a stage before that
+    for (int it = 0; it + 2 < nch; ++it) {
+      if (!tc::mbar_wait(&bar_hfull[it & 1], (it >> 1) & 1, status, kBit)) break;
+      GDR_TRACE_CLK(tl0);
+      issue_loads(it + 2);
+      loaded = it + 2;
+      if (it + 3 < nch) prefetch(it + 3);
+      GDR_TRACE_SINCE(3, 16, tl0);
+    }
+    // every load requested has landed (bounded) before the CTA's shared memory serves the
+    // next role.  A stage's earlier loads completed before its next was requested (their MMAs
+    // had read them), so only the last load of each stage can be pending; waiting on an older
+    // phase of a barrier that has moved on two phases would not return.
+    for (int it = loaded > 0 ? loaded - 1 : 0; it <= loaded; ++it)
+      (void)tc::mbar_wait(&bar_load[it & 1], (it >> 1) & 1, status, kBit);
+  } else if (tid == kWalkMmaTid) {
+    // ---------------------------------------------------------------- MMA role
+    // the products that do not need dh': P^T dO into accV, Q^^T dO into accH
+    auto issue_free = [&](int it) -> bool {
+      const int st = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      unsigned char* stg = sm + st * WS::STAGE;
+      if (!tc::mbar_wait(&bar_load[st], ph, status, kBit)) return false;
       tc::tc_fence_after();
-      tc::gemm(Da, kmaj(stg + WS::KQ, 2 * kSlab), mnmaj(sm + WS::DH, 16384), NC, 8, false);  // K dh'
-      tc::gemm(Db, mnmaj(stg + WS::P, kSlab), mnmaj(stg + WS::DO, kSlab), NC, 4, false);     // P^T dO
-      tc::mma_commit(&bar_mma);
-    }
-    GDR_TRACE_MARK(3, 7);
-    if (tid == kCopyTid && c - 1 >= c_begin) {  // overlaps the MMAs
-      GDR_DELAY(10);
-      issue_loads(c - 1, st ^ 1);
-    }
-    GDR_TRACE_MARK(3, 8);
-    // NC = 64: this chunk's dVn tile was last stored two chunks ago (groups since: dh', dVn,
-    // dh'); NC = 128: one tile, stored one chunk ago (group since: this chunk's dh')
-    unsigned char* dvn_t = sm + ((NC == 64 && (it & 1)) ? WS::DVN2 : WS::DVN);
-    if (tid == kCopyTid) {
-      GDR_TRACE_CLK(tdv);
-      if constexpr (NC == 64)
-        tc::bulk_wait_read<3>();
-      else
-        tc::bulk_wait_read<1>();
-      GDR_TRACE_SINCE(3, 20, tdv);
-    }
-    GDR_TRACE_MARK(3, 9);
-    if (ok && warp >= 4) {  // diag(e^gamma) dO, zero past the chunk end: row r, half (tid >> 6) & 1
-      const int h2 = (tid >> 6) & 1;
-      const float e = r < len ? fexp(gr) : 0.f;
-      if constexpr (NC == 64) {
-        float x[32];
-        ld_halfrow_bf16(stg + WS::DO, r, h2, x);
-#pragma unroll
-        for (int b = 0; b < 32; ++b) x[b] *= e;
-        st_halfrow_bf16(sm + WS::DOS, r, h2, x);
-      } else {
-        float x[64];
-        ld_row_bf16(stg + WS::DO + h2 * kSlab, r, x);
-#pragma unroll
-        for (int b = 0; b < 64; ++b) x[b] *= e;
-        st_row_bf16(sm + WS::DOS + h2 * kSlab, r, x);
-      }
-    }
-    tc::fence_proxy_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    if (ok && tid == 0) {  // committed together with W^T dVn below
+      tc::gemm(accV0 + 128 * st, tc::mnmaj(stg + WS::P, kSlab), tc::mnmaj(stg + WS::DO, kSlab), 128, 4, false);
+      if (!tc::mbar_wait(&bar_scaled[st], ph, status, kBit)) return false;
       tc::tc_fence_after();
-      tc::gemm(Dd, mnmaj(stg + WS::KQ + kSlab, 2 * kSlab), mnmaj(sm + WS::DOS, kSlab), NC, 4,
-               false);  // Q^T diag(e^gamma) dO
-    }
-    GDR_TRACE_MARK(3, 2);
-    ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutBwd));
-    mma_phase ^= 1;
-    tc::tc_fence_after();
-    GDR_TRACE_MARK(3, 3);
-    // kPublish: the copy thread's warp has no part in the dVn rows, so it counts chunk c + 2 (the
-    // stores of two chunks ago; bulk groups since: dh', dVn, dh') here, where most of the
-    // ~1k-cycle GPU-scope release overlaps the epilogue instead of delaying the chunk's last
-    // barrier.  (A standalone acq_rel fence in the earlier MMA-issue window, with only a relaxed
-    // count here, measured ~1.9k cycles: slower.)
-    if (kPublish && tid == kCopyTid && prev2 >= 0) {
-      GDR_TRACE_CLK(tpw);
-      tc::bulk_wait<3>();
-      GDR_TRACE_SINCE(3, 22, tpw);
-      GDR_TRACE_CLK(tpp);
-      GDR_DELAY(11);
-      publish_chunk(ws.walk_flags + (size_t)prev2 * Hv + j);
-      GDR_TRACE_SINCE(3, 23, tpp);
-    }
-    if (ok && lo) {  // dVn = scale P^T dO + diag(e^{gamma_C - gamma}) K dh', row r, half hf
-      if (warp == 1) GDR_DELAY(12);
-      const float dec = fexp(gC - gr);
-#pragma unroll 1
-      for (int q = 0; q < CPT / 32; ++q) {  // 32 columns at a time: [CPT hf + 32 q, +32)
-        float x[32], y[32];
-        tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, CPT * hf + 32 * q), x);
-        tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, NC + CPT * hf + 32 * q), y);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int b = 0; b < 32; ++b) y[b] = r < len ? d.scale * y[b] + dec * x[b] : 0.f;
-        if constexpr (NC == 64)
-          st_halfrow_bf16(dvn_t, r, hf, y);
-        else
-          st_halfrow_bf16(dvn_t + hf * kSlab, r, q, y);
-      }
-    }
-    tc::fence_proxy_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    if (ok && tid == 0) {
+      tc::gemm(accH0 + 128 * st, tc::mnmaj(stg + WS::KQ + kSlab, 2 * kSlab), tc::mnmaj(stg + WS::DO, kSlab), 128, 4,
+               false);
+      return true;
+    };
+    bool ok = true;
+    if (nch > 0) ok = issue_free(0);
+    for (int it = 0; it < nch && ok; ++it) {
+      const int st = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      unsigned char* stg = sm + st * WS::STAGE;
+      // the chain: K^ dh' once dh' is staged, then W^T dVn once dVn is
+      GDR_TRACE_CLK(tw0);
+      ok = tc::mbar_wait(&bar_dh, it & 1, status, kBit);
+      GDR_TRACE_SINCE(3, 10, tw0);
+      if (!ok) break;
+      tc::tc_fence_after();
       GDR_DELAY(13);
+      GDR_TRACE_CLK(tw1);
+      tc::gemm(accV0 + 128 * st, tc::kmaj(stg + WS::KQ, 2 * kSlab), tc::mnmaj(sm + WS::DH, 16384), 128, 8, true);
+      tc::mma_commit(&bar_vfull[st]);
+      GDR_TRACE_SINCE(3, 11, tw1);
+      GDR_TRACE_CLK(tw2);
+      ok = tc::mbar_wait(&bar_dvn[st], ph, status, kBit);
+      GDR_TRACE_SINCE(3, 12, tw2);
+      if (!ok) break;
       tc::tc_fence_after();
-      tc::gemm(Dc, mnmaj(stg + WS::W, kSlab), mnmaj(dvn_t, kSlab), NC, 4, false);  // W^T dVn
-      tc::mma_commit(&bar_mma);
+      GDR_TRACE_CLK(tw3);
+      tc::gemm(accH0 + 128 * st, tc::mnmaj(stg + WS::W, kSlab), tc::mnmaj(sm + WS::DVN + st * 16384, kSlab), 128,
+               4, true, true);
+      tc::mma_commit(&bar_hfull[st]);
+      GDR_TRACE_SINCE(3, 13, tw3);
+      // the next chunk's dh'-free products
+      GDR_TRACE_CLK(tw4);
+      if (it + 1 < nch) ok = issue_free(it + 1);
+      GDR_TRACE_SINCE(3, 14, tw4);
     }
-    if (ok && tid == kCopyTid) {
-#pragma unroll
-      for (int sl = 0; sl < NSL; ++sl) tc::tma_store_2d(&tm_dvs, dvn_t + sl * kSlab, dv0 + 64 * sl, (int)(chh * 64));
+    // drain: every MMA issued has completed before the CTA's tensor memory serves the next role
+    tc::mma_commit(&bar_drain);
+    (void)tc::mbar_wait(&bar_drain, 0, status, kBit);
+  } else if (tid == kWalkCopyTid) {
+    // ---------------------------------------------------------------- store + publish role
+    int pub = -1;  // kPublish: the previous step's chunk, whose count is still due
+    for (int it = 0; it < nch; ++it) {
+      const int st = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      const size_t chh = (size_t)chunk_of(it) * Hv + j;
+      GDR_TRACE_CLK(tc0_);
+      if (!tc::mbar_wait(&bar_dh, it & 1, status, kBit)) break;
+      GDR_TRACE_SINCE(3, 20, tc0_);
+      GDR_DELAY(10);
+      tc::tma_store_2d(&tm_dhs, sm + WS::DH, 0, (int)(chh * 128));
+      tc::tma_store_2d(&tm_dhs, sm + WS::DH + 16384, 64, (int)(chh * 128));
       tc::bulk_commit();
-    }
-    GDR_TRACE_MARK(3, 4);
-    // this chunk's dh' store has left the operand tile (only the dVn group may still read):
-    // the tile takes the next chunk's dh' right after the update below
-    if (tid == kCopyTid) {
-      GDR_TRACE_CLK(tdr);
-      tc::bulk_wait_read<1>();
-      GDR_TRACE_SINCE(3, 21, tdr);
-    }
-    ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutBwd));
-    mma_phase ^= 1;
-    tc::tc_fence_after();
-    GDR_TRACE_MARK(3, 5);
-    if (ok) {
-      const float eC = fexp(gC);
-#pragma unroll
-      for (int q = 0; q < CPT / 32; ++q) {
-        float x[32], y[32];
-        tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 2 * NC + CPT * hf + 32 * q), x);
-        tc::tmem_ld32(tc::tmem_lane_addr(tb, warp, 3 * NC + CPT * hf + 32 * q), y);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int b = 0; b < 32; ++b) dh[32 * q + b] = eC * dh[32 * q + b] + d.scale * y[b] - x[b];
+      tc::bulk_wait_read<0>();  // the dh' tile has been read: the next dh' may replace it
+      tc::mbar_arrive(&bar_dhfree);
+      if (!tc::mbar_wait(&bar_dvn[st], ph, status, kBit)) break;
+      unsigned char* dvn = sm + WS::DVN + st * 16384;
+      tc::tma_store_2d(&tm_dvs, dvn, 0, (int)(chh * 64));
+      tc::tma_store_2d(&tm_dvs, dvn + kSlab, 64, (int)(chh * 64));
+      tc::bulk_commit();
+      tc::bulk_wait_read<0>();
+      tc::mbar_arrive(&bar_dvnfree[st]);
+      GDR_TRACE_CLK(tc1_);
+      if (kPublish && pub >= 0) {  // the previous step's two groups have landed
+        tc::bulk_wait<2>();
+        GDR_DELAY(11);
+        publish_chunk(ws.walk_flags + (size_t)pub * Hv + j);
       }
-      stage_dh();  // the next chunk's dh' operand (one barrier for both)
+      GDR_TRACE_SINCE(3, 21, tc1_);
+      pub = chunk_of(it);
     }
-    if (tid == kCopyTid && kPublish) {
-      prev2 = prev1;
-      prev1 = c;
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-    GDR_TRACE_MARK(3, 6);
-  }
-  if (tid == kCopyTid) {
-    tc::bulk_wait_read<0>();  // smem sources read before exit
-    if (kPublish && prev1 >= 0) {
-      tc::bulk_wait<0>();
-      if (prev2 >= 0) publish_chunk(ws.walk_flags + (size_t)prev2 * Hv + j);
-      publish_chunk(ws.walk_flags + (size_t)prev1 * Hv + j);
-    }
-  }
-  if (ok && dS0) {
-    const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
-    const int c0 = dv0 + CPT * hf;
+    tc::bulk_wait<0>();
+    if (kPublish && pub >= 0) publish_chunk(ws.walk_flags + (size_t)pub * Hv + j);
+  } else if (tid < 256) {
+    // ---------------------------------------------------------------- epilogue warps
+    const int ln = (warp & 3) * 32 + lane;  // TMEM lane: token of accV (lanes 0-63), dk of accH
+    const int hf = warp >> 2;               // accV: dv [64 hf, +64); accH: dv [64 hf, +64)
+    const bool lo = (warp & 3) < 2;         // the dVn rows (lanes 0-63)
+    const float scale = d.scale, inv_scale = 1.f / d.scale;
+    // lanes 64-127 warps: K^ and Q^ of step it in place, one row of both slabs of K (threads
+    // 0-63) or of Q (64-127) per thread
+    auto scale_tiles = [&](int it) -> bool {
+      const int st = it & 1;
+      GDR_TRACE_CLK(ts0);
+      if (!warp_wait(&bar_load[st], (it >> 1) & 1, status, kBit)) return false;
+      if (tid == 64) GDR_TRACE_SINCE(3, 17, ts0);
+      unsigned char* stg = sm + st * WS::STAGE;
+      const float* g = reinterpret_cast<const float*>(stg + WS::GAM);
+      const int len = len_of(it);
+      const int h = ((warp & 3) - 2) * 32 + lane + 64 * hf;  // 0..127
+      const int r = h & 63, isq = h >> 6;
+      const float f = r < len ? (isq ? scale * fexp(g[r]) : fexp(g[len - 1] - g[r]) * inv_scale) : 0.f;
+#pragma unroll 1
+      for (int k = 0; k < 2; ++k) {  // slabs: K at 0 and 2 kSlab, Q at kSlab and 3 kSlab
+        unsigned char* slab = stg + WS::KQ + (2 * k + isq) * kSlab;
+        float x[64];
+        ld_row_bf16(slab, r, x);
 #pragma unroll
-    for (int b = 0; b < CPT; ++b)
-      dS0[sb + (d.layout == 0 ? (size_t)dk * 128 + c0 + b : (size_t)(c0 + b) * 128 + dk)] = dh[b];
+        for (int b = 0; b < 64; ++b) x[b] *= f;
+        st_row_bf16(slab, r, x);
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar_scaled[st]);
+      return true;
+    };
+    float dh[64];
+    {
+      const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
+#pragma unroll
+      for (int b = 0; b < 64; ++b)
+        dh[b] = dS_T ? dS_T[sb + (d.layout == 0 ? (size_t)ln * 128 + 64 * hf + b : (size_t)(64 * hf + b) * 128 + ln)]
+                     : 0.f;
+    }
+    auto stage_dh = [&]() {  // dh' of the next step as the MMA's bf16 operand
+      st_row_bf16(sm + WS::DH + hf * 16384, ln, dh);
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar_dh);
+    };
+    bool ok = true;
+    if (nch > 0) {
+      stage_dh();
+      if (!lo) ok = scale_tiles(0);
+    }
+    GDR_TRACE_INIT();
+    for (int it = 0; it < nch && ok; ++it) {
+      const int st = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      const int len = len_of(it);
+      ok = warp_wait(&bar_vfull[st], ph, status, kBit);
+      GDR_TRACE_MARK(3, 0);
+      if (!ok) break;
+      tc::tc_fence_after();
+      // gamma_C while the stage still holds this step (it is reloaded after W^T dVn)
+      const float gC = reinterpret_cast<const float*>(sm + st * WS::STAGE + WS::GAM)[len - 1];
+      if (lo) {  // dVn = scale accV, token row ln, columns [64 hf, +64), zero past the chunk end
+        float x[64];
+        tmem_ld64(accV0 + 128 * st, warp, 64 * hf, x);
+        tc::tc_fence_before();
+        GDR_TRACE_MARK(3, 7);
+        if (it >= 2) {
+          ok = warp_wait(&bar_dvnfree[st], ((it - 2) >> 1) & 1, status, kBit);
+          if (!ok) break;
+        }
+        GDR_TRACE_MARK(3, 8);
+        if (warp == 1) GDR_DELAY(12);
+        const float f = ln < len ? scale : 0.f;
+#pragma unroll
+        for (int b = 0; b < 64; ++b) x[b] *= f;
+        st_row_bf16(sm + WS::DVN + st * 16384 + hf * kSlab, ln, x);
+        GDR_TRACE_MARK(3, 9);
+        tc::fence_proxy_async_smem();
+      }
+      // every epilogue warp counts in (the others have read gamma_C, so the stage may be
+      // reloaded once W^T dVn, which waits for this, has run)
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&bar_dvn[st]);
+      // meanwhile the lanes 64-127 warps prepare the next step's K^, Q^
+      if (!lo && it + 1 < nch) {
+        ok = scale_tiles(it + 1);
+        if (!ok) break;
+      }
+      GDR_TRACE_MARK(3, 2);
+      GDR_TRACE_MARK(3, 1);
+      // dh = e^{gamma_C} dh' + accH, staged as the next step's dh'
+      ok = warp_wait(&bar_hfull[st], ph, status, kBit);
+      GDR_TRACE_MARK(3, 3);
+      if (!ok) break;
+      tc::tc_fence_after();
+      {
+        float y0[32], y1[32];
+        tc::tmem_ld32(tc::tmem_lane_addr(accH0 + 128 * st, warp, 64 * hf), y0);
+        tc::tmem_ld32(tc::tmem_lane_addr(accH0 + 128 * st, warp, 64 * hf + 32), y1);
+        tc::tmem_wait_ld();
+        tc::tc_fence_before();
+        const float eC = fexp(gC);
+#pragma unroll
+        for (int b = 0; b < 32; ++b) {
+          dh[b] = eC * dh[b] + y0[b];
+          dh[32 + b] = eC * dh[32 + b] + y1[b];
+        }
+      }
+      GDR_TRACE_MARK(3, 4);
+      if (it + 1 < nch) {
+        ok = warp_wait(&bar_dhfree, it & 1, status, kBit);
+        GDR_TRACE_MARK(3, 5);
+        if (!ok) break;
+        stage_dh();
+      }
+      GDR_TRACE_MARK(3, 6);
+    }
+    if (ok && dS0) {
+      const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
+#pragma unroll
+      for (int b = 0; b < 64; ++b)
+        dS0[sb + (d.layout == 0 ? (size_t)ln * 128 + 64 * hf + b : (size_t)(64 * hf + b) * 128 + ln)] = dh[b];
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (tid == 0) {  // the next unit of this CTA initialises them again
-    tc::mbar_inval(&bar_load[0]);
-    tc::mbar_inval(&bar_load[1]);
-    tc::mbar_inval(&bar_mma);
+  if (tid == 0) {  // the next unit of this CTA (or the next role) initialises them again
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_inval(&bar_load[s]);
+      tc::mbar_inval(&bar_scaled[s]);
+      tc::mbar_inval(&bar_vfull[s]);
+      tc::mbar_inval(&bar_hfull[s]);
+      tc::mbar_inval(&bar_dvn[s]);
+      tc::mbar_inval(&bar_dvnfree[s]);
+    }
+    tc::mbar_inval(&bar_dh);
+    tc::mbar_inval(&bar_dhfree);
+    tc::mbar_inval(&bar_drain);
   }
+  __syncthreads();
+  tc::tc_fence_after();
 }
 
-template <int NC>
-__global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
+// The reverse walk alone (cluster-pair gradients, or more sequences than the fused kernel's
+// order table holds): one CTA per (sequence, v-head).
+__global__ void __launch_bounds__(kWalkThreads, 1) tc_bwd_walk_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
     const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dhs,
@@ -368,13 +468,12 @@ __global__ void __launch_bounds__(kWalkThreads) tc_bwd_walk_kernel(
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint32_t tmem_slot;
-  if (threadIdx.x < 32) tc::tmem_alloc<4 * NC>(&tmem_slot);
+  if (threadIdx.x < 32) tc::tmem_alloc<kWalkTmemCols>(&tmem_slot);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  walk_body<NC, false>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvs, d, dS_T, dS0, ws, (int)blockIdx.x, tmem_slot,
-                       sm);
-  if (threadIdx.x < 32) tc::tmem_dealloc(tmem_slot, 4 * NC);
+  walk_body<false>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvs, d, dS_T, dS0, ws, (int)blockIdx.x, tmem_slot, sm);
+  if (threadIdx.x < 32) tc::tmem_dealloc(tmem_slot, kWalkTmemCols);
 }
 
 // ---------------------------------------------------------------------------------
@@ -519,6 +618,12 @@ struct GradSmem {
 
 constexpr int kGradThreads = 256;  // two warps per TMEM lane quarter, each on half the columns
 
+// The gradient role's barriers: named barrier 1 over its kGradThreads threads (warps 0-7), so
+// that a kernel may run the role on part of a larger CTA (the fused walk + gradient kernel,
+// whose walk role also has an MMA warp and a copy warp).
+__device__ __forceinline__ void gsync() { tc::named_sync(1, kGradThreads); }
+__device__ __forceinline__ bool gsync_and(bool p) { return tc::named_sync_and(1, kGradThreads, p); }
+
 // kGroup: Hv > Hk; dq, dk are summed over the v-heads of a q/k head.  kPair (Hv = 2 Hk,
 // launched as clusters of two CTAs): the two CTAs of a cluster take the two v-heads of one
 // q/k head on the same chunk, and each finalises half of the dq and dk columns, adding the
@@ -570,7 +675,7 @@ __device__ __forceinline__ void grad_body(
     tc::fence_barrier_init();
   }
   tc::tc_fence_before();
-  __syncthreads();
+  gsync();
   tc::tc_fence_after();
   if (kPair) tc::cluster_sync();  // the partner's barriers exist before anyone arrives on them
   // TMEM columns: [K K^T ; Q K^T] 0-63 (K K^T kept to the end); dq 256-383; dk 384-511.
@@ -614,7 +719,7 @@ __device__ __forceinline__ void grad_body(
       // timeout the loads are left out and the item's own bounded wait ends the walk
       GDR_TRACE_CLK(tw0);
       const unsigned long long tf0_ = GDR_TRACE_NOW();
-      if (kDyn && !wait_flag(ws.walk_flags + ch2, (uint32_t)d.walk_units, ws.status, kDevErrTimeoutBwd)) return;
+      if (kDyn && !wait_flag(ws.walk_flags + ch2, 1u, ws.status, kDevErrTimeoutBwd)) return;
       GDR_TRACE_INFO_ADD(4, GDR_TRACE_NOW() - tf0_);
       GDR_TRACE_SINCE(2, 20, tw0);
       tc::mbar_arrive_expect_tx(bar, (d.h_bf16 ? 18 : 22) * kSlab + 256);
@@ -693,7 +798,7 @@ __device__ __forceinline__ void grad_body(
         if (r < cur_len) st_global_bf16x32(out + ((size_t)(cur_t0 + r) * d.Hk + cur_i) * 128 + rank * 64 + 32 * q2, x);
       }
     }
-    return (bool)__syncthreads_and(okin && okw);
+    return (bool)gsync_and(okin && okw);
   };
   // kDyn: the copy thread claims an item and decodes its chunk once; the other threads read
   // both from shared memory after a barrier.  Inside the item loop the claim is split so its
@@ -708,10 +813,10 @@ __device__ __forceinline__ void grad_body(
   int witem, cur_c = 0;
   if (kDyn) {
     if (tid == kCopyTid) claim();
-    __syncthreads();
+    gsync();
     witem = s_claim;
     cur_c = s_claim_c;
-    __syncthreads();
+    gsync();
   } else {
     witem = item0 < n_items && ws.chunks[chunk_of(item0)].z <= 0 ? next_item(item0) : item0;
   }
@@ -731,7 +836,7 @@ __device__ __forceinline__ void grad_body(
   const size_t ch = (size_t)c * Hv + j;
   if (kDyn && tid == kCopyTid) pre_w = (int)atomicAdd(ws.grad_queue, 1u);  // used after R2
   if (tid < 64) s_beta[tid] = tid < len ? __bfloat162float(beta[(size_t)(t0 + tid) * Hv + j]) : 0.f;
-  ok = __syncthreads_and(tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutBwd));
+  ok = gsync_and(tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutBwd));
   pending = (kDyn || wnext < n_items) ? 0 : -1;  // kDyn: decided when the next item is claimed
   const float* sgam = reinterpret_cast<const float*>(sm + S::GAM);
   if (tid < 64) s_eg[tid] = fexp(sgam[tid]);
@@ -771,7 +876,7 @@ __device__ __forceinline__ void grad_body(
 #pragma unroll
       for (int b = 0; b < 64; ++b) hdh4[b & 3] += hv[b] * dv_[b];
     }
-    __syncthreads();
+    gsync();
     if (ok) st_row_bf16(sm + S::H + hh * 16384, hrow, hv);
   }
   float hdh = warp_sum((hdh4[0] + hdh4[1]) + (hdh4[2] + hdh4[3]));
@@ -793,7 +898,7 @@ __device__ __forceinline__ void grad_body(
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
-  __syncthreads();
+  gsync();
   hdh = ((s_red[0] + s_red[1]) + (s_red[2] + s_red[3])) + ((s_red[4] + s_red[5]) + (s_red[6] + s_red[7]));
   GDR_TRACE_MARK(2, 1);
   // P2: [K;Q] K^T (0-63: K K^T on lanes 0-63, Q K^T on lanes 64-127), [O-hat; dVn] h^T
@@ -808,7 +913,7 @@ __device__ __forceinline__ void grad_body(
     tc::gemm(C_DK, kmaj(sm + S::VN, kSlab), kmaj(sm + S::DH, 16384), 128, 8, false);
     tc::mma_commit(&bar_mma);
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
+  ok = gsync_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
   mma_par ^= 1;
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 2);
@@ -882,7 +987,7 @@ __device__ __forceinline__ void grad_body(
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
-  __syncthreads();
+  gsync();
   GDR_TRACE_MARK(2, 3);
   if (ok) col_partial(s_colpp);  // column sums of dP * QK
   if (ok && tid < 64) {  // sum_s e^{gC - g_s} k_s^T dh' vn_s
@@ -891,7 +996,7 @@ __device__ __forceinline__ void grad_body(
     const float part = warp_sum(kdv);
     if (lane == 0) s_red[warp] = part;
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_tma2, item_par, ws.status, kDevErrTimeoutBwd));
+  ok = gsync_and(ok && tc::mbar_wait(&bar_tma2, item_par, ws.status, kDevErrTimeoutBwd));
   GDR_TRACE_MARK(2, 5);
   // P6: dq += dP K, dk += dP^T Q; on lanes 64-127 (operand rows shifted by one slab: [.; dW]
   // and [V; dVn]) dW K^T (64-127) and dVn V^T (128-191)
@@ -903,7 +1008,7 @@ __device__ __forceinline__ void grad_body(
     tc::gemm(tb + 128, kmaj(sm + S::OD, S::OD_SLAB), kmaj(sm + S::V, S::OD_SLAB), 64, 8, false);
     tc::mma_commit(&bar_mma);
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
+  ok = gsync_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
   mma_par ^= 1;
   tc::tc_fence_after();
   GDR_TRACE_MARK(2, 6);
@@ -945,7 +1050,7 @@ __device__ __forceinline__ void grad_body(
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
-  __syncthreads();
+  gsync();
   if (ok) col_partial(s_colbk);
   GDR_TRACE_MARK(2, 7);
   // R2: T^T dVn = dB_v (128-255), X = T^T dT (64-127, lanes 64-127: T^T's M atoms start one
@@ -961,7 +1066,7 @@ __device__ __forceinline__ void grad_body(
     tc::gemm(tb + 64, mnmaj(sm + S::T - kSlab, kSlab), mnmaj(sm + S::DT, kSlab), 64, 4, false);
     tc::mma_commit(&bar_mma);
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
+  ok = gsync_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
   mma_par ^= 1;
   tc::tc_fence_after();
   if (ok && tid == kCopyTid && pending >= 0) {  // dVn is consumed, dq has left its staging tile
@@ -1007,7 +1112,7 @@ __device__ __forceinline__ void grad_body(
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
-  __syncthreads();
+  gsync();
   GDR_TRACE_MARK(2, 9);
   // R3: X T^T (64-127)
   if (ok && tid == kCopyTid && len == 64) {
@@ -1020,7 +1125,7 @@ __device__ __forceinline__ void grad_body(
     tc::gemm(tb + 64, kmaj(sm + S::XT, kSlab), kmaj(sm + S::T, kSlab), 64, 4, false);
     tc::mma_commit(&bar_mma);
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
+  ok = gsync_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
   mma_par ^= 1;
   tc::tc_fence_after();
   if (ok && tid == kCopyTid && pending >= 0) {  // dv has left its staging tile (W)
@@ -1057,7 +1162,7 @@ __device__ __forceinline__ void grad_body(
   }
   tc::fence_proxy_async_smem();
   tc::tc_fence_before();
-  __syncthreads();
+  gsync();
   if (ok) col_partial(s_colaa);
   GDR_TRACE_MARK(2, 11);
   // R4: dk += T'^T dW + dAGb K + dAGb^T K
@@ -1068,7 +1173,7 @@ __device__ __forceinline__ void grad_body(
     tc::gemm(C_DK, mnmaj(sm + S::DAG, kSlab), mnmaj(sm + S::KQ, 2 * kSlab), 128, 4, true);
     tc::mma_commit(&bar_mma);
   }
-  ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
+  ok = gsync_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
   mma_par ^= 1;
   tc::tc_fence_after();
   if (ok && tid == kCopyTid && pending >= 0) {  // every operand tile but dO (dk staging) is free
@@ -1109,7 +1214,7 @@ __device__ __forceinline__ void grad_body(
     }
   }
   tc::fence_proxy_async_smem();
-  __syncthreads();
+  gsync();
   if (ok && tid == kCopyTid && !kGroup && len == 64) {
     tc::tma_store_3d(&tm_dk, sm + S::DKS, 0, i, t0);
     tc::tma_store_3d(&tm_dk, sm + S::DKS + kSlab, 64, i, t0);
@@ -1124,7 +1229,7 @@ __device__ __forceinline__ void grad_body(
     }
     s_colaa[0][tid] = x;  // s_colaa is free again: reuse it for the warp totals
   }
-  __syncthreads();
+  gsync();
   if (ok && tid < 64) {
     const int rr = 63 - tid;
     const float v = s_colaa[0][tid] + (tid >= 32 ? s_colaa[0][31] : 0.f);
@@ -1144,7 +1249,7 @@ __device__ __forceinline__ void grad_body(
   if (tid == 0) GDR_TRACE_INFO_ADD(3, 1);
   item_par ^= 1;
   tc::tc_fence_before();
-  __syncthreads();
+  gsync();
   tc::tc_fence_after();
   if (kDyn) {  // claimed at this item's first prefetch point (if that ran: else ok is false)
     witem = ok ? s_claim : n_items;
@@ -1157,7 +1262,7 @@ __device__ __forceinline__ void grad_body(
   // flight land (bounded) before the CTA gives up its shared memory.
   if (tid == kCopyTid && !ok && pending > 0) (void)tc::mbar_wait(&bar_tma, item_par, ws.status, kDevErrTimeoutBwd);
   tc::tc_fence_before();
-  __syncthreads();
+  gsync();
 }
 
 template <bool kGroup, bool kPair = false>
@@ -1186,11 +1291,19 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
 }
 
 // The backward's reverse walk and its gradient kernel in one cooperative launch (every CTA
-// resident, one per SM): CTAs first run walk units (64 at B=2, H=16, leaving the other SMs
+// resident, one per SM): CTAs first run walk units (32 at B=2, H=16, leaving the other SMs
 // free), then every CTA claims gradient items in the order the walk completes chunks, so the
-// gradients of late chunks overlap the walk of early ones.
-template <bool kGroup, int NC>
-__global__ void __launch_bounds__(kGradThreads) tc_bwd_walkgrad_kernel(
+// gradients of late chunks overlap the walk of early ones.  Launched with kWalkThreads (384)
+// threads: three warps of a register-file quarter (warps q, q + 4, q + 8) cap a thread at 168
+// registers, enough for the walk.  For the gradient role the third warpgroup (the walk's MMA,
+// store and load warps) hands its registers to warps 0-7: setmaxnreg.dec to 40 there and
+// setmaxnreg.inc to 232 here, 4 x 32 x 40 + 8 x 32 x 232 = 384 x 168 registers, which is
+// exactly the block's allocation (the launcher checks the kernel was built with 168 per
+// thread), so the increase never waits for registers that are not there.
+constexpr uint32_t kWalkRegs = 168, kGradRegs = 232, kIdleRegs = 40;
+static_assert(4 * 32 * kIdleRegs + 8 * 32 * kGradRegs == (uint32_t)kWalkThreads * kWalkRegs, "register split");
+template <bool kGroup>
+__global__ void __launch_bounds__(kWalkThreads, 1) tc_bwd_walkgrad_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
@@ -1208,11 +1321,16 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_walkgrad_kernel(
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  const int n_units = d.num_seqs * d.Hv * (128 / NC);
+  const int n_units = d.num_seqs * d.Hv;
   if (threadIdx.x == 0) GDR_TRACE_INFO_SET(0, GDR_TRACE_NOW());
   for (int u = (int)blockIdx.x; u < n_units; u += (int)gridDim.x)
-    walk_body<NC, true>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvn, d, dS_T, dS0, ws, u, tmem_slot, sm);
+    walk_body<true>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvn, d, dS_T, dS0, ws, u, tmem_slot, sm);
   if (threadIdx.x == 0) GDR_TRACE_INFO_SET(1, GDR_TRACE_NOW());
+  if (threadIdx.x >= kGradThreads) {  // the walk's single-thread roles: registers to the gradients
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kIdleRegs) : "memory");
+    return;
+  }
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kGradRegs) : "memory");
   grad_body<kGroup, false, true>(tm_q, tm_k, tm_v, tm_do, tm_w, tm_u, tm_dvn, tm_dh, tm_h, tm_t, tm_dq, tm_dk,
                                  tm_dv, d, beta, dq, dk, dv, dg, dbeta, ws, tmem_slot, sm);
   if (threadIdx.x == 0) GDR_TRACE_INFO_SET(2, GDR_TRACE_NOW());
@@ -1273,22 +1391,18 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     tc_vn_kernel<<<(unsigned)(n_items < n_sm ? n_items : n_sm), kTcThreads, smv, s>>>(tw, tu, thf, d, ws);
     stage_mark(s, "bwd_vn");
   }
-  // Walk units per (sequence, v-head): the two DV halves (shorter epilogues, so a shorter
-  // chain) while the walk units fill at most a quarter of the SMs, i.e. when there are so few
-  // chains that the walk is the critical path; else one unit over all of DV, which takes half
-  // the SM time per chain and leaves the SMs to the gradient items.
+  // One walk unit per (sequence, v-head), over all of DV.
   Dims dd = d;
-  dd.walk_units = (long long)d.num_seqs * d.Hv * 2 * 4 <= n_sm ? 2 : 1;
-  const bool halves = dd.walk_units == 2;
-  if (fused_walk_grad(d)) {  // walk and gradients in one cooperative kernel
+  auto kern = d.G > 1 ? tc_bwd_walkgrad_kernel<true> : tc_bwd_walkgrad_kernel<false>;
+  // the fused kernel's register split assumes the block holds exactly kWalkRegs per thread; a
+  // build that allocated another count runs the walk and the gradients as two launches
+  cudaFuncAttributes fa{};
+  const bool regs_ok = cudaFuncGetAttributes(&fa, (const void*)kern) == cudaSuccess && fa.numRegs == (int)kWalkRegs;
+  if (fused_walk_grad(d) && regs_ok) {  // walk and gradients in one cooperative kernel
     int per_sm = 0;
-    const size_t smg =
-        (halves ? std::max(GradSmem::BYTES, WalkSmem<64>::BYTES) : std::max(GradSmem::BYTES, WalkSmem<128>::BYTES)) +
-        1024;
-    auto kern = d.G > 1 ? (halves ? tc_bwd_walkgrad_kernel<true, 64> : tc_bwd_walkgrad_kernel<true, 128>)
-                        : (halves ? tc_bwd_walkgrad_kernel<false, 64> : tc_bwd_walkgrad_kernel<false, 128>);
+    const size_t smg = std::max(GradSmem::BYTES, WalkSmem::BYTES) + 1024;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGradThreads, smg) != cudaSuccess || per_sm < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWalkThreads, smg) != cudaSuccess || per_sm < 1)
       return cudaErrorInvalidConfiguration;
     e = cudaMemsetAsync(ws.walk_flags, 0, sizeof(uint32_t) * ((size_t)d.max_chunks * d.Hv + 64), s);
     if (e != cudaSuccess) return e;
@@ -1300,7 +1414,8 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     void* args[] = {&tq, &tk, &tv, &tdo, &tw, &tu, &tp, &tdvn, &tdh, &tdhs, &thf, &tt, &tdq, &tdk, &tdv, &dd,
                     (void*)&dS_T, (void*)&dS0, (void*)&beta, (void*)&dq, (void*)&dk, (void*)&dv, (void*)&dg,
                     (void*)&dbeta, &w};
-    e = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)(per_sm * n_sm)), dim3(kGradThreads), args, smg, s);
+    e = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)(per_sm * n_sm)), dim3(kWalkThreads), args, smg,
+                                    s);
     if (e != cudaSuccess) return e;
     stage_mark(s, "bwd_walkgrad");
     if (d.G > 1) {
@@ -1310,11 +1425,10 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     return cudaGetLastError();
   }
   if (d.num_seqs > 0) {
-    const size_t sm = (halves ? WalkSmem<64>::BYTES : WalkSmem<128>::BYTES) + 1024;
-    auto kern = halves ? tc_bwd_walk_kernel<64> : tc_bwd_walk_kernel<128>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    kern<<<d.num_seqs * d.Hv * dd.walk_units, kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, dd, a.dS_T,
-                                                                    a.dS0, ws);
+    const size_t sm = WalkSmem::BYTES + 1024;
+    cudaFuncSetAttribute(tc_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    tc_bwd_walk_kernel<<<d.num_seqs * d.Hv, kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, dd, a.dS_T,
+                                                                  a.dS0, ws);
     stage_mark(s, "bwd_walk");
   }
   if (d.max_chunks > 0 && Tt > 0) {

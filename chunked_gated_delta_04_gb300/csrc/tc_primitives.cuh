@@ -160,6 +160,26 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// L2 prefetch of one box of a tensor map (no shared memory, no completion to track).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// L2 prefetch of `bytes` (multiple of 16) at a 16-byte aligned global address.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -214,6 +234,27 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 template <int N>
 __device__ __forceinline__ void bulk_wait() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ------------------------------------------------------------------ named barriers
+// Barrier `id` (1..15) over the first `n` threads that reach it (n a multiple of 32): lets a
+// subset of the CTA's warps synchronise while the others run another role.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// named_sync that also returns the AND of `pred` over the participating threads.
+__device__ __forceinline__ bool named_sync_and(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
 }
 
 // ------------------------------------------------------------------ TMEM
@@ -332,10 +373,11 @@ __device__ __forceinline__ uint64_t step_desc(const Opnd& o, int kk) {
   return o.mn ? mnmajor_step_desc(o.base, o.stride, kk) : kmajor_step_desc(o.base, o.stride, kk);
 }
 
-// D (+)= A * B with M = 128, K = 16 * ksteps.  Issued by one thread.
+// D (+)= A * B with M = 128, K = 16 * ksteps.  Issued by one thread.  neg_a: D (+)= -A * B
+// (the instruction descriptor's negate-A bit).
 __device__ __forceinline__ void gemm(uint32_t d_tmem, const Opnd& a, const Opnd& b, int N, int ksteps,
-                                     bool accumulate) {
-  const uint32_t id = idesc_bf16(128, N, a.mn, b.mn);
+                                     bool accumulate, bool neg_a = false) {
+  const uint32_t id = idesc_bf16(128, N, a.mn, b.mn) | (neg_a ? (1u << 13) : 0u);
   for (int kk = 0; kk < ksteps; ++kk) mma_bf16(d_tmem, step_desc(a, kk), step_desc(b, kk), id, (accumulate || kk > 0) ? 1u : 0u);
 }
 
