@@ -98,10 +98,12 @@ __global__ void __launch_bounds__(kThreads) simt_prep_kernel(Dims d, const IT* _
   const size_t ch = (size_t)c * Hv + j;
   float* W = (float*)ws.W + ch * kChunk * DK;
   float* U = (float*)ws.U + ch * kChunk * DV;
+  for (int r = tid; r < kChunk; r += kThreads) sA[r * kLd + r] = sb[r] * __expf(sg[r]);  // beta e^gamma on A's (unused) diagonal
+  __syncthreads();
   for (int e = tid; e < kChunk * DK; e += kThreads) {
     const int r = e / DK, x = e % DK;
     float acc = 0.f;
-    for (int s = 0; s <= r && s < len; ++s) acc += sT[r * kLd + s] * sb[s] * __expf(sg[s]) * sK[s * DK + x];
+    for (int s = 0; s <= r && s < len; ++s) acc += sT[r * kLd + s] * sA[s * kLd + s] * sK[s * DK + x];
     W[e] = r < len ? acc : 0.f;
   }
   for (int e = tid; e < kChunk * DV; e += kThreads) {
@@ -149,6 +151,7 @@ __global__ void __launch_bounds__(kThreads) simt_state_kernel(Dims d, const IT* 
   float* sh = sm;               // [DK][dvs]
   float* sVn = sh + DK * dvs;   // [64][dvs]
   float* sg = sVn + kChunk * dvs;
+  float* sdec = sg + kChunk;    // e^{gamma_C - gamma_r} of the current chunk
   const int tid = threadIdx.x;
   for (int e = tid; e < DK * dvs; e += kThreads) {
     const int a = e / dvs, b = e % dvs;
@@ -185,11 +188,12 @@ __global__ void __launch_bounds__(kThreads) simt_state_kernel(Dims d, const IT* 
     __syncthreads();
     const float gC = sg[len - 1];
     const float eC = __expf(gC);
+    for (int r = tid; r < kChunk; r += kThreads) sdec[r] = r < len ? __expf(gC - sg[r]) : 0.f;
+    __syncthreads();
     for (int e = tid; e < DK * dvs; e += kThreads) {
       const int a = e / dvs, b = e % dvs;
       float acc = 0.f;
-      for (int r = 0; r < len; ++r)
-        acc += __expf(gC - sg[r]) * ldf(k + ((size_t)(t0 + r) * Hk + i) * DK + a) * sVn[r * dvs + b];
+      for (int r = 0; r < len; ++r) acc += sdec[r] * ldf(k + ((size_t)(t0 + r) * Hk + i) * DK + a) * sVn[r * dvs + b];
       sh[e] = eC * sh[e] + acc;
     }
     __syncthreads();
@@ -299,6 +303,11 @@ __global__ void __launch_bounds__(kThreads) simt_walk_kernel(Dims d, const IT* _
   float* sdVn = sdh + DK * dvs;      // [64][dvs]
   float* sP = sdVn + kChunk * dvs;   // [64][65]
   float* sg = sP + kChunk * kLd;     // [64]
+  // the chunk's q, k (rows of DK + 1 floats) and dO slice (dvs + 1), staged as fp32
+  const int LK = DK + 1, LD = dvs + 1;
+  float* sq = sg + kChunk;
+  float* sk = sq + kChunk * LK;
+  float* sdo = sk + kChunk * LK;
   const int tid = threadIdx.x;
   for (int e = tid; e < DK * dvs; e += kThreads) {
     const int a = e / dvs, b = e % dvs;
@@ -315,15 +324,23 @@ __global__ void __launch_bounds__(kThreads) simt_walk_kernel(Dims d, const IT* _
       ((float*)ws.dhp)[ch * DK * DV + (size_t)a * DV + dv0 + b] = sdh[e];
     }
     for (int r = tid; r < kChunk; r += kThreads) sg[r] = ws.gam[ch * kChunk + r];
+    for (int e = tid; e < kChunk * DK; e += kThreads) {
+      const int r = e / DK, x = e % DK;
+      const bool in = r < len;
+      sq[r * LK + x] = in ? ldf(q + ((size_t)(t0 + r) * Hk + i) * DK + x) : 0.f;
+      sk[r * LK + x] = in ? ldf(k + ((size_t)(t0 + r) * Hk + i) * DK + x) : 0.f;
+    }
+    for (int e = tid; e < kChunk * dvs; e += kThreads) {
+      const int r = e / dvs, b = e % dvs;
+      sdo[r * LD + b] = r < len ? ldf(dO + ((size_t)(t0 + r) * Hv + j) * DV + dv0 + b) : 0.f;
+    }
     __syncthreads();
     for (int e = tid; e < kChunk * kChunk; e += kThreads) {
       const int r = e / kChunk, s = e % kChunk;
       float p = 0.f;
       if (s <= r && r < len) {
         float dot = 0.f;
-        const IT* qr = q + ((size_t)(t0 + r) * Hk + i) * DK;
-        const IT* ks = k + ((size_t)(t0 + s) * Hk + i) * DK;
-        for (int x = 0; x < DK; ++x) dot += ldf(qr + x) * ldf(ks + x);
+        for (int x = 0; x < DK; ++x) dot += sq[r * LK + x] * sk[s * LK + x];
         p = dot * __expf(sg[r] - sg[s]);
       }
       sP[r * kLd + s] = p;
@@ -335,9 +352,8 @@ __global__ void __launch_bounds__(kThreads) simt_walk_kernel(Dims d, const IT* _
       float acc = 0.f;
       if (s < len) {
         float a1 = 0.f, a2 = 0.f;
-        for (int r = s; r < len; ++r) a1 += sP[r * kLd + s] * ldf(dO + ((size_t)(t0 + r) * Hv + j) * DV + dv0 + b);
-        const IT* ks = k + ((size_t)(t0 + s) * Hk + i) * DK;
-        for (int a = 0; a < DK; ++a) a2 += ldf(ks + a) * sdh[a * dvs + b];
+        for (int r = s; r < len; ++r) a1 += sP[r * kLd + s] * sdo[r * LD + b];
+        for (int a = 0; a < DK; ++a) a2 += sk[s * LK + a] * sdh[a * dvs + b];
         acc = d.scale * a1 + __expf(gC - sg[s]) * a2;
       }
       sdVn[e] = acc;
@@ -349,8 +365,7 @@ __global__ void __launch_bounds__(kThreads) simt_walk_kernel(Dims d, const IT* _
       const int a = e / dvs, b = e % dvs;
       float a1 = 0.f, a2 = 0.f;
       for (int r = 0; r < len; ++r) {
-        a1 += __expf(sg[r]) * ldf(q + ((size_t)(t0 + r) * Hk + i) * DK + a) *
-              ldf(dO + ((size_t)(t0 + r) * Hv + j) * DV + dv0 + b);
+        a1 += __expf(sg[r]) * sq[r * LK + a] * sdo[r * LD + b];
         a2 += W[r * DK + a] * sdVn[r * dvs + b];
       }
       sdh[e] = eC * sdh[e] + d.scale * a1 - a2;
@@ -368,7 +383,10 @@ __global__ void __launch_bounds__(kThreads) simt_walk_kernel(Dims d, const IT* _
 // ---------------------------------------------------------------------------------
 // backward gradients of one chunk (chunk-parallel)
 // ---------------------------------------------------------------------------------
-template <typename IT>
+// kS (DK, DV <= 64): the chunk's q, k, v, dO and Vn are staged in shared memory as fp32 rows
+// padded by one float (conflict-free column walks), so the dot-product loops below read shared
+// memory instead of making dependent global round trips.
+template <typename IT, bool kS>
 __global__ void __launch_bounds__(kThreads) simt_grad_kernel(Dims d, const IT* __restrict__ q,
                                                              const IT* __restrict__ k,
                                                              const IT* __restrict__ v,
@@ -404,10 +422,33 @@ __global__ void __launch_bounds__(kThreads) simt_grad_kernel(Dims d, const IT* _
   const float* dhp = (const float*)ws.dhp + ch * DK * DV;
   const float* Vn = (const float*)ws.Vn + ch * kChunk * DV;
   const float* Tg = ws.Tm + ch * kChunk * kChunk;
-  auto Q = [&](int r, int x) { return ldf(q + ((size_t)(t0 + r) * Hk + i) * DK + x); };
-  auto K = [&](int r, int x) { return ldf(k + ((size_t)(t0 + r) * Hk + i) * DK + x); };
-  auto V = [&](int r, int x) { return ldf(v + ((size_t)(t0 + r) * Hv + j) * DV + x); };
-  auto DO = [&](int r, int x) { return ldf(dO + ((size_t)(t0 + r) * Hv + j) * DV + x); };
+  const int LK = DK + 1, LV = DV + 1;  // kS: staged row strides
+  float* sQs = sred + 32;
+  float* sKs = sQs + kChunk * LK;
+  float* sVs = sKs + kChunk * LK;
+  float* sDOs = sVs + kChunk * LV;
+  float* sVns = sDOs + kChunk * LV;
+  if (kS) {  // rows past the chunk end: zero (every use below is masked to r, s < len anyway)
+    for (int e = tid; e < kChunk * DK; e += kThreads) {
+      const int r = e / DK, x = e % DK;
+      const bool in = r < len;
+      sQs[r * LK + x] = in ? ldf(q + ((size_t)(t0 + r) * Hk + i) * DK + x) : 0.f;
+      sKs[r * LK + x] = in ? ldf(k + ((size_t)(t0 + r) * Hk + i) * DK + x) : 0.f;
+    }
+    for (int e = tid; e < kChunk * DV; e += kThreads) {
+      const int r = e / DV, x = e % DV;
+      const bool in = r < len;
+      sVs[r * LV + x] = in ? ldf(v + ((size_t)(t0 + r) * Hv + j) * DV + x) : 0.f;
+      sDOs[r * LV + x] = in ? ldf(dO + ((size_t)(t0 + r) * Hv + j) * DV + x) : 0.f;
+      sVns[r * LV + x] = Vn[e];
+    }
+    __syncthreads();
+  }
+  auto Q = [&](int r, int x) { return kS ? sQs[r * LK + x] : ldf(q + ((size_t)(t0 + r) * Hk + i) * DK + x); };
+  auto K = [&](int r, int x) { return kS ? sKs[r * LK + x] : ldf(k + ((size_t)(t0 + r) * Hk + i) * DK + x); };
+  auto V = [&](int r, int x) { return kS ? sVs[r * LV + x] : ldf(v + ((size_t)(t0 + r) * Hv + j) * DV + x); };
+  auto DO = [&](int r, int x) { return kS ? sDOs[r * LV + x] : ldf(dO + ((size_t)(t0 + r) * Hv + j) * DV + x); };
+  auto VN = [&](int r, int x) { return kS ? sVns[r * LV + x] : Vn[r * DV + x]; };
 
   for (int r = tid; r < kChunk; r += kThreads) {
     sg[r] = ws.gam[ch * kChunk + r];
@@ -447,7 +488,7 @@ __global__ void __launch_bounds__(kThreads) simt_grad_kernel(Dims d, const IT* _
     float p = 0.f;
     if (s <= r && r < len) {
       float dot = 0.f;
-      for (int b = 0; b < DV; ++b) dot += DO(r, b) * Vn[s * DV + b];
+      for (int b = 0; b < DV; ++b) dot += DO(r, b) * VN(s, b);
       p = d.scale * dot * Gam(r, s);
     }
     sdP[r * kLd + s] = p;
@@ -510,7 +551,7 @@ __global__ void __launch_bounds__(kThreads) simt_grad_kernel(Dims d, const IT* _
       dot_qh += DO(r, b) * qh;
       float kd = 0.f;
       for (int a = 0; a < DK; ++a) kd += K(r, a) * dhp[(size_t)a * DV + b];
-      kdv += kd * Vn[r * DV + b];
+      kdv += kd * VN(r, b);
     }
     for (int a = lane; a < DK; a += 32) {
       float dBk = 0.f;
@@ -522,7 +563,7 @@ __global__ void __launch_bounds__(kThreads) simt_grad_kernel(Dims d, const IT* _
       float dka = 0.f;
       for (int s = r; s < len; ++s) dka += sdP[s * kLd + r] * Q(s, a);
       float vd = 0.f;
-      for (int b = 0; b < DV; ++b) vd += Vn[r * DV + b] * dhp[(size_t)a * DV + b];
+      for (int b = 0; b < DV; ++b) vd += VN(r, b) * dhp[(size_t)a * DV + b];
       dka += decr * vd + br * egr * dBk;
       float a1 = 0.f, a2 = 0.f;
       for (int s = 0; s < r; ++s) a1 += sdT[r * kLd + s] * Gam(r, s) * K(s, a);
@@ -624,7 +665,7 @@ cudaError_t simt_forward_t(const Dims& d, const FwdArgs& a, const Workspace& ws,
   if (d.num_seqs > 0) {
     const int dvs = dv_slice(d);
     const dim3 gs(d.num_seqs, d.Hv, d.DV / dvs);
-    size_t sms = sizeof(float) * (d.DK * dvs + kChunk * dvs + kChunk);
+    size_t sms = sizeof(float) * (d.DK * dvs + kChunk * dvs + 2 * kChunk);
     cudaFuncSetAttribute(simt_state_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
     simt_state_kernel<IT><<<gs, kThreads, sms, s>>>(d, (const IT*)a.k, a.S0, a.S_T, a.h_saved, ws, dvs);
     stage_mark(s, "fwd_state");
@@ -654,7 +695,7 @@ cudaError_t simt_backward_t(const Dims& d, const BwdArgs& a, const Workspace& ws
   if (d.num_seqs > 0) {
     const int dvs = dv_slice(d);
     const dim3 gs(d.num_seqs, d.Hv, d.DV / dvs);
-    size_t smw = sizeof(float) * (d.DK * dvs + kChunk * dvs + kChunk * kLd + kChunk);
+    size_t smw = sizeof(float) * (d.DK * dvs + kChunk * dvs + kChunk * kLd + kChunk + kChunk * (2 * (d.DK + 1) + dvs + 1));
     cudaFuncSetAttribute(simt_walk_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smw);
     simt_walk_kernel<IT><<<gs, kThreads, smw, s>>>(d, (const IT*)a.q, (const IT*)a.k, (const IT*)a.dO,
                                                    a.dS_T, a.dS0, ws, dvs);
@@ -662,9 +703,12 @@ cudaError_t simt_backward_t(const Dims& d, const BwdArgs& a, const Workspace& ws
   }
   if (d.max_chunks > 0) {
     const dim3 gc(d.max_chunks, d.Hv);
+    const bool stage = d.DK <= 64 && d.DV <= 64;
     size_t smg = sizeof(float) * (6 * kChunk * kLd + kChunk * d.DV + kChunk * d.DK + 4 * kChunk + 32);
-    cudaFuncSetAttribute(simt_grad_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
-    simt_grad_kernel<IT><<<gc, kThreads, smg, s>>>(d, (const IT*)a.q, (const IT*)a.k, (const IT*)a.v,
+    if (stage) smg += sizeof(float) * kChunk * (2 * (d.DK + 1) + 3 * (d.DV + 1));
+    auto grad = stage ? simt_grad_kernel<IT, true> : simt_grad_kernel<IT, false>;
+    cudaFuncSetAttribute(grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
+    grad<<<gc, kThreads, smg, s>>>(d, (const IT*)a.q, (const IT*)a.k, (const IT*)a.v,
                                                    (const IT*)a.beta, a.h_saved, (const IT*)a.dO,
                                                    (IT*)a.dq, (IT*)a.dk, (IT*)a.dv, a.dg, (IT*)a.dbeta, ws);
     stage_mark(s, "bwd_grad");
