@@ -3,7 +3,7 @@
 // The backward (the fused backward of FlashQLA PR #34, which walks the chunks in
 // reverse carrying the state gradient dh) runs as three stages here:
 //   prep   (gdr_tc.cu) W, U, P, gamma and T of every chunk, chunk-parallel.
-//   walk   one CTA per (sequence, v-head, 64-wide DV slice), chunks in reverse; dh
+//   walk   one CTA per (sequence, v-head), all of DK and DV, chunks in reverse; dh
 //          (dL/dh at the chunk end, "dh'") stays in registers:
 //            dVn = scale P^T dO + diag(e^{gamma_C - gamma}) K dh'
 //            dh  = e^{gamma_C} dh' + scale Q^T diag(e^gamma) dO - W^T dVn
@@ -632,7 +632,7 @@ __device__ __forceinline__ bool gsync_and(bool p) { return tc::named_sync_and(1,
 // launch_group_reduce sums them.
 // kDyn (fused walk + gradient kernel): items are claimed from ws.grad_queue in the order the
 // walk finishes them (last chunk of every sequence first), and a chunk's dh' and dVn
-// tiles are loaded only once both walk slices have counted it in ws.walk_flags.
+// tiles are loaded only once the walk unit has counted it in ws.walk_flags.
 // tb: 512 TMEM columns owned by the caller.
 template <bool kGroup, bool kPair, bool kDyn>
 __device__ __forceinline__ void grad_body(
