@@ -304,6 +304,8 @@ def main():
                     help="dtype of the saved chunk-start states (bf16 halves the largest tensor)")
     ap.add_argument("--prologue", action="store_true",
                     help="raw q, k, gate and beta logits; the operator applies the L2 norm, logsigmoid, sigmoid")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time direct C-ABI calls instead of a CUDA-graph replay of the same calls")
     ap.add_argument("--recompute-wy", action="store_true",
                     help="the backward recomputes the chunk factors (gamma, W, U, P, T) instead of reading the "
                          "ones the forward saved")
@@ -370,9 +372,25 @@ def main():
         if st != 0:
             raise RuntimeError(f"gdr_bwd: {gdr.gdr_status_string(st)}")
 
-    def step():
-        fwd()
-        bwd()
+    def step(strm=None):
+        fwd(strm=strm)
+        bwd(strm=strm)
+
+    def capture(fn):
+        """A CUDA graph of fn's launches (the same C-ABI calls, recorded once on a capture
+        stream); None when capture is not possible."""
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(device=dev)
+        cs.wait_stream(stream)
+        try:
+            with torch.cuda.graph(g, stream=cs, capture_error_mode="relaxed"):
+                fn(strm=torch.cuda.current_stream())
+        except Exception as exc:  # e.g. a launch kind the driver cannot capture
+            print(f"graph capture failed, timing direct calls: {exc}", file=sys.stderr)
+            torch.cuda.synchronize()
+            return None
+        torch.cuda.synchronize()
+        return g
 
     def flush():
         flush_buf.fill_(1)
@@ -396,41 +414,70 @@ def main():
     if st != 0:
         raise RuntimeError(f"device status after warm-up: {gdr.gdr_status_string(st)} (flags {flags:#x})")
 
-    # ---- main timed region: exactly K steps
+    # Kernel launches of one step (counted by the library on a direct call).
     launches0 = gdr.gdr_debug_launch_count()
+    flush()
+    step()
+    torch.cuda.synchronize()
+    launches_per_step = gdr.gdr_debug_launch_count() - launches0
+    # The timed steps replay a CUDA graph of the step's C-ABI calls: the same kernels with the
+    # same arguments, without the host's per-launch gaps (small workloads are launch-bound).
+    graphs = {}
+    if not args.no_graph:
+        for name, fn in (("step", step), ("fwd", fwd), ("bwd", bwd)):
+            graphs[name] = capture(fn)
+            if graphs[name] is None:
+                graphs = {}
+                break
+    run = {name: (g.replay if g is not None else None) for name, g in graphs.items()}
+    run_step = run.get("step") or step
+    launch_mode = "cuda_graph" if graphs else "direct"
+
+    # ---- main timed region: exactly K steps
     with ClockSampler(local_rank) as clk:
         barrier()
         torch.cuda.synchronize()
-        step_ms = timed(step, args.steps)
+        step_ms = timed(run_step, args.steps)
         torch.cuda.synchronize()
         barrier()
-    launches = gdr.gdr_debug_launch_count() - launches0
+    launches = launches_per_step * args.steps
     tokens = float(sum(inp["seqlens"]))
     value, total_ms = aggregate_throughput(sum(step_ms), tokens * args.steps, dist, dev)
     ms_per_step = total_ms / args.steps
 
     # ---- fwd / bwd separately (informational)
-    fwd_ms = statistics.median(timed(fwd, max(5, args.steps // 2)))
-    bwd_ms = statistics.median(timed(bwd, max(5, args.steps // 2)))
+    fwd_ms = statistics.median(timed(run.get("fwd") or fwd, max(5, args.steps // 2)))
+    bwd_ms = statistics.median(timed(run.get("bwd") or bwd, max(5, args.steps // 2)))
 
     # ---- per-kernel times with stage events (separate pass; the main loop has no hooks)
     nev = 16
     events = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
-    gdr.gdr_debug_set_stage_events(events)
     stage_tot = {}
     reps = max(5, args.steps // 2)
+    stage_runs = []
+    for fn in (fwd, bwd):  # each direction with its stage events (recorded inside the graph)
+        gdr.gdr_debug_set_stage_events(events)
+        g = capture(fn) if graphs else None
+        if g is None:
+            stage_runs.append((fn, None))
+        else:
+            stage_runs.append((g.replay, gdr.gdr_debug_stage_names()))
+        gdr.gdr_debug_set_stage_events(None)
     for _ in range(reps):
-        for fn in (fwd, bwd):
+        for fn, names_at_capture in stage_runs:
+            if names_at_capture is None:
+                gdr.gdr_debug_set_stage_events(events)
             flush()
             fn()
             torch.cuda.synchronize()
-            names = gdr.gdr_debug_stage_names()
+            names = names_at_capture if names_at_capture is not None else gdr.gdr_debug_stage_names()
+            if names_at_capture is None:
+                gdr.gdr_debug_set_stage_events(None)
             per_call = {}
             for i, nm in enumerate(names):  # a stage may launch several kernels: sum them per call
                 per_call[nm] = per_call.get(nm, 0.0) + events[i].elapsed_time(events[i + 1])
             for nm, t in per_call.items():
                 stage_tot.setdefault(nm, []).append(t)
-    gdr.gdr_debug_set_stage_events(None)
     stage_ms = {k: statistics.mean(v) for k, v in stage_tot.items()}
 
     wm = work_model(inp, w, 2 if args.h_dtype == "bf16" else 4, save_wy=not args.recompute_wy)
@@ -546,6 +593,7 @@ def main():
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "pipelined": "2 buffer sets; upload, compute, download on 3 streams"},
             "gpu_launches": launches,
+            "launch": launch_mode,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -9,6 +9,8 @@
 #include "gdr_internal.h"
 #include "../../include/gdr_debug.h"
 #include <atomic>
+#include <mutex>
+#include <vector>
 
 namespace gdr {
 
@@ -30,16 +32,25 @@ gdr_status cuda_status(cudaError_t e) {
 
 gdr_status status_of(cudaError_t e) { return cuda_status(e); }
 
+// A stage event: a plain record, or an event-record node when the stream is being captured.
+void record_stage_event(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
+}
+
 void stage_begin(cudaStream_t s) {
   g_stage_i = 0;
-  if (g_stage_events && g_stage_n > 0) cudaEventRecord(g_stage_events[0], s);
+  if (g_stage_events && g_stage_n > 0) record_stage_event(g_stage_events[0], s);
 }
 
 void stage_mark(cudaStream_t s, const char* stage) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (g_stage_events && g_stage_i + 1 < g_stage_n && g_stage_i < kMaxStages) {
     g_stage_names[g_stage_i] = stage;
-    cudaEventRecord(g_stage_events[g_stage_i + 1], s);
+    record_stage_event(g_stage_events[g_stage_i + 1], s);
     ++g_stage_i;
   }
 }
@@ -101,6 +112,51 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
 
 gdr_status resolve_problem(const gdr_problem* p, Dims* d) { return resolve(p, d); }
 
+cudaError_t current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static std::atomic<GetCurrent> get_current{nullptr};
+  static std::atomic<GetId> get_id{nullptr};
+  if (!get_current.load() || !get_id.load()) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q2 != cudaDriverEntryPointSuccess)
+      return cudaErrorNotSupported;
+    get_current.store((GetCurrent)f1);
+    get_id.store((GetId)f2);
+  }
+  CUcontext ctx = nullptr;
+  if (get_current.load()(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  return get_id.load()(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+cudaError_t set_smem_once(const void* func, size_t bytes) {
+  struct Entry {
+    const void* func;
+    unsigned long long ctx;
+    size_t bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  unsigned long long ctx = 0;
+  const bool known_ctx = current_context_id(&ctx) == cudaSuccess;
+  if (known_ctx) {
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : done)
+      if (e.func == func && e.ctx == ctx && e.bytes >= bytes) return cudaSuccess;
+  }
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && known_ctx) {
+    std::lock_guard<std::mutex> lock(mu);
+    done.push_back(Entry{func, ctx, bytes});
+  }
+  return e;
+}
+
 size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws) {
   size_t off = 0;
   auto take = [&](size_t bytes) -> char* {
@@ -129,6 +185,10 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
     if (d.path == 1) {
       if (!d.save_wy) w.Tb = take(el * chH * kChunk * kChunk);
       w.dVn = take(el * chH * kChunk * d.DV);
+    } else if (simt_small(d)) {
+      w.dVn = take(el * chH * kChunk * d.DV);
+      w.Pf = (float*)take(sizeof(float) * chH * kChunk * kChunk);
+      w.Ak = (float*)take(sizeof(float) * chH * kChunk * kChunk);
     }
     if (fused_walk_grad(d)) {  // one region: flags then the claim counter (zeroed per call)
       w.walk_flags = (uint32_t*)take(sizeof(uint32_t) * ((size_t)d.max_chunks * d.Hv + 64));

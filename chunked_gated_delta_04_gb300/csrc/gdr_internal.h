@@ -52,7 +52,9 @@ struct Workspace {
   void* dhp;     // backward: [max_chunks][Hv][DK][DV] state gradient at each chunk's end
                  // (fp32 on the SIMT path, bf16 on the tensor-core path)
   void* Tb;      // tensor-core backward: T = (I + A)^{-1}, bf16 [max_chunks][Hv][64][64]
-  void* dVn;     // tensor-core backward: dL/dVn, bf16 [max_chunks][Hv][64][DV]
+  void* dVn;     // backward: dL/dVn [max_chunks][Hv][64][DV] (bf16 tensor-core path, fp32 small-head SIMT path)
+  float* Pf;     // small-head SIMT backward: Q K^T * Gam on and below the diagonal [max_chunks][Hv][64][64]
+  float* Ak;     // small-head SIMT backward: K K^T * Gam below the diagonal [max_chunks][Hv][64][64]
   float* dq_part;  // backward, Hv > Hk: [T_total][Hv][DK]
   float* dk_part;  // backward, Hv > Hk: [T_total][Hv][DK]
   // fused walk + gradient kernel (fixed-length tensor-core backward): per (chunk, v-head) count
@@ -78,6 +80,13 @@ struct Workspace {
 // GDR_OK for cudaSuccess; otherwise records e for gdr_debug_last_cuda_error and returns
 // GDR_ERR_CUDA.
 gdr_status status_of(cudaError_t e);
+
+// Id of the current CUDA context (unique per context, also across resets); driver entry points
+// looked up once through the runtime.
+cudaError_t current_context_id(unsigned long long* id);
+// Raises a kernel's dynamic shared-memory limit to `bytes`, once per kernel and CUDA context
+// (cudaFuncSetAttribute is a driver round trip on every call).
+cudaError_t set_smem_once(const void* func, size_t bytes);
 
 // Validates *p and fills *d (the checks of gdr_fwd / gdr_bwd on the problem itself).
 gdr_status resolve_problem(const gdr_problem* p, Dims* d);
@@ -130,12 +139,21 @@ cudaError_t launch_prologue_bwd(const Dims& d, const void* q, const void* k, con
 template <typename Args>
 cudaError_t apply_prologue(const Dims& d, Args& a, const Workspace& ws, cudaStream_t s);
 
-// K0: chunk index (chunks, seq offsets, longest-first order) and status reset.
+// K0: chunk index (chunks, seq offsets, longest-first order) and status reset; for a
+// fixed-length problem only the status reset (index_folded).
 cudaError_t launch_index(const Dims& d, const Workspace& ws, cudaStream_t s);
 
 // fp32 SIMT kernels (any supported shape and dtype).
 cudaError_t simt_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s);
 cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cudaStream_t s);
+// The SIMT path's tile kernels for DK, DV <= 64 (gdr_simt_small.cu), which simt_forward and
+// simt_backward use when simt_small(d).
+bool simt_small(const Dims& d);
+// Fixed-length problems need no index kernel: the kernels compute chunk records and step
+// tables (gdr_chunks.cuh), and launch_index only resets the status word.
+bool index_folded(const Dims& d);
+cudaError_t simt_small_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s);
+cudaError_t simt_small_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cudaStream_t s);
 
 // Sums dq_part / dk_part over the v-heads of each q/k head into dq / dk (dtype).
 cudaError_t launch_group_reduce(const Dims& d, void* dq, void* dk, const Workspace& ws, cudaStream_t s);

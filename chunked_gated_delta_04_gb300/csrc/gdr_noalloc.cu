@@ -48,29 +48,6 @@ ScratchEntry g_noalloc[kMaxDevices];
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Id of the current CUDA context (driver entry points looked up once through the runtime).
-cudaError_t current_context_id(unsigned long long* id) {
-  using GetCurrent = CUresult (*)(CUcontext*);
-  using GetId = CUresult (*)(CUcontext, unsigned long long*);
-  static GetCurrent get_current = nullptr;
-  static GetId get_id = nullptr;
-  if (!get_current || !get_id) {
-    void* f1 = nullptr;
-    void* f2 = nullptr;
-    cudaDriverEntryPointQueryResult q1, q2;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
-        q1 != cudaDriverEntryPointSuccess ||
-        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
-        q2 != cudaDriverEntryPointSuccess)
-      return cudaErrorNotSupported;
-    get_current = (GetCurrent)f1;
-    get_id = (GetId)f2;
-  }
-  CUcontext ctx = nullptr;
-  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
-  return get_id(ctx, id) == CUDA_SUCCESS ? cudaSuccess : cudaErrorDeviceUninitialized;
-}
-
 // Device address of the scratch array in the current device's context (set up on first
 // use in that context).
 cudaError_t scratch_address(void** out) {

@@ -17,6 +17,7 @@
 //
 // Work layout: chunk-parallel kernels run one CTA per (chunk slot, v-head);
 // sequential kernels one CTA per (sequence, v-head, 32-wide slice of DV).
+#include "gdr_chunks.cuh"
 #include "gdr_device.cuh"
 #include "gdr_internal.h"
 
@@ -25,8 +26,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kLd = kChunk + 1;  // padded row length of 64 x 64 smem matrices
-
-__device__ __forceinline__ int4 load_chunk(const int4* chunks, int c) { return chunks[c]; }
 
 // ---------------------------------------------------------------------------------
 // prep: gamma, A, T, W, U of one chunk (and T for the backward)
@@ -38,7 +37,7 @@ __global__ void __launch_bounds__(kThreads) simt_prep_kernel(Dims d, const IT* _
                                                              const IT* __restrict__ beta, Workspace ws) {
   extern __shared__ float sm[];
   const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
-  const int4 ci = load_chunk(ws.chunks, c);
+  const int4 ci = idx_chunk(d, ws, c);
   const int len = ci.z, t0 = ci.y;
   if (len <= 0) return;
   const int DK = d.DK, DV = d.DV, Hv = d.Hv, Hk = d.Hk;
@@ -145,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) simt_state_kernel(Dims d, const IT* 
                                                               void* __restrict__ h_saved, Workspace ws,
                                                               int dvs) {
   extern __shared__ float sm[];
-  const int n = ws.seq_order[blockIdx.x], j = blockIdx.y, i = j / d.G;
+  const int n = idx_seq(d, ws, blockIdx.x), j = blockIdx.y, i = j / d.G;
   const int dv0 = blockIdx.z * dvs;
   const int DK = d.DK, DV = d.DV, Hv = d.Hv, Hk = d.Hk;
   float* sh = sm;               // [DK][dvs]
@@ -158,9 +157,9 @@ __global__ void __launch_bounds__(kThreads) simt_state_kernel(Dims d, const IT* 
     sh[e] = S0 ? S0[((size_t)n * Hv + j) * DK * DV + state_idx(d.layout, a, dv0 + b, DK, DV)] : 0.f;
   }
   __syncthreads();
-  const int c_begin = ws.seq_chunk_off[n], c_end = ws.seq_chunk_off[n + 1];
+  const int c_begin = idx_seq_off(d, ws, n), c_end = idx_seq_off(d, ws, n + 1);
   for (int c = c_begin; c < c_end; ++c) {
-    const int4 ci = ws.chunks[c];
+    const int4 ci = idx_chunk(d, ws, c);
     const int len = ci.z, t0 = ci.y;
     const size_t ch = (size_t)c * Hv + j;
     for (int e = tid; e < DK * dvs; e += kThreads) {
@@ -216,7 +215,7 @@ __global__ void __launch_bounds__(kThreads) simt_out_kernel(Dims d, const IT* __
                                                             IT* __restrict__ o, Workspace ws) {
   extern __shared__ float sm[];
   const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
-  const int4 ci = ws.chunks[c];
+  const int4 ci = idx_chunk(d, ws, c);
   const int len = ci.z, t0 = ci.y;
   if (len <= 0) return;
   const int DK = d.DK, DV = d.DV, Hv = d.Hv, Hk = d.Hk;
@@ -262,7 +261,7 @@ __global__ void __launch_bounds__(kThreads) simt_out_kernel(Dims d, const IT* __
 __global__ void __launch_bounds__(kThreads) simt_vn_kernel(Dims d, const void* __restrict__ h_saved,
                                                            Workspace ws) {
   const int c = blockIdx.x, j = blockIdx.y;
-  const int4 ci = ws.chunks[c];
+  const int4 ci = idx_chunk(d, ws, c);
   const int len = ci.z;
   if (len <= 0) return;
   const int DK = d.DK, DV = d.DV;
@@ -296,7 +295,7 @@ __global__ void __launch_bounds__(kThreads) simt_walk_kernel(Dims d, const IT* _
                                                              float* __restrict__ dS0, Workspace ws,
                                                              int dvs) {
   extern __shared__ float sm[];
-  const int n = ws.seq_order[blockIdx.x], j = blockIdx.y, i = j / d.G;
+  const int n = idx_seq(d, ws, blockIdx.x), j = blockIdx.y, i = j / d.G;
   const int dv0 = blockIdx.z * dvs;
   const int DK = d.DK, DV = d.DV, Hv = d.Hv, Hk = d.Hk;
   float* sdh = sm;                   // [DK][dvs]
@@ -314,9 +313,9 @@ __global__ void __launch_bounds__(kThreads) simt_walk_kernel(Dims d, const IT* _
     sdh[e] = dS_T ? dS_T[((size_t)n * Hv + j) * DK * DV + state_idx(d.layout, a, dv0 + b, DK, DV)] : 0.f;
   }
   __syncthreads();
-  const int c_begin = ws.seq_chunk_off[n], c_end = ws.seq_chunk_off[n + 1];
+  const int c_begin = idx_seq_off(d, ws, n), c_end = idx_seq_off(d, ws, n + 1);
   for (int c = c_end - 1; c >= c_begin; --c) {
-    const int4 ci = ws.chunks[c];
+    const int4 ci = idx_chunk(d, ws, c);
     const int len = ci.z, t0 = ci.y;
     const size_t ch = (size_t)c * Hv + j;
     for (int e = tid; e < DK * dvs; e += kThreads) {
@@ -398,7 +397,7 @@ __global__ void __launch_bounds__(kThreads) simt_grad_kernel(Dims d, const IT* _
                                                              IT* __restrict__ dbeta, Workspace ws) {
   extern __shared__ float sm[];
   const int c = blockIdx.x, j = blockIdx.y, i = j / d.G;
-  const int4 ci = ws.chunks[c];
+  const int4 ci = idx_chunk(d, ws, c);
   const int len = ci.z, t0 = ci.y;
   if (len <= 0) return;
   const int DK = d.DK, DV = d.DV, Hv = d.Hv, Hk = d.Hk;
@@ -657,7 +656,7 @@ cudaError_t simt_forward_t(const Dims& d, const FwdArgs& a, const Workspace& ws,
   if (d.max_chunks > 0) {
     const dim3 gc(d.max_chunks, d.Hv);
     size_t smp = sizeof(float) * (kChunk * d.DK + kChunk * d.DV + 2 * kChunk * kLd + 2 * kChunk);
-    cudaFuncSetAttribute(simt_prep_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
+    set_smem_once((const void*)simt_prep_kernel<IT>, smp);
     simt_prep_kernel<IT><<<gc, kThreads, smp, s>>>(d, (const IT*)a.k, (const IT*)a.v, a.g,
                                                    (const IT*)a.beta, ws);
     stage_mark(s, "fwd_prep");
@@ -666,14 +665,14 @@ cudaError_t simt_forward_t(const Dims& d, const FwdArgs& a, const Workspace& ws,
     const int dvs = dv_slice(d);
     const dim3 gs(d.num_seqs, d.Hv, d.DV / dvs);
     size_t sms = sizeof(float) * (d.DK * dvs + kChunk * dvs + 2 * kChunk);
-    cudaFuncSetAttribute(simt_state_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
+    set_smem_once((const void*)simt_state_kernel<IT>, sms);
     simt_state_kernel<IT><<<gs, kThreads, sms, s>>>(d, (const IT*)a.k, a.S0, a.S_T, a.h_saved, ws, dvs);
     stage_mark(s, "fwd_state");
   }
   if (d.max_chunks > 0) {
     const dim3 gc(d.max_chunks, d.Hv);
     size_t smo = sizeof(float) * (2 * kChunk * d.DK + kChunk * kLd + kChunk);
-    cudaFuncSetAttribute(simt_out_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smo);
+    set_smem_once((const void*)simt_out_kernel<IT>, smo);
     simt_out_kernel<IT><<<gc, kThreads, smo, s>>>(d, (const IT*)a.q, (const IT*)a.k, a.h_saved, (IT*)a.o, ws);
     stage_mark(s, "fwd_out");
   }
@@ -685,7 +684,7 @@ cudaError_t simt_backward_t(const Dims& d, const BwdArgs& a, const Workspace& ws
   if (d.max_chunks > 0) {
     const dim3 gc(d.max_chunks, d.Hv);
     size_t smp = sizeof(float) * (kChunk * d.DK + kChunk * d.DV + 2 * kChunk * kLd + 2 * kChunk);
-    cudaFuncSetAttribute(simt_prep_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
+    set_smem_once((const void*)simt_prep_kernel<IT>, smp);
     simt_prep_kernel<IT><<<gc, kThreads, smp, s>>>(d, (const IT*)a.k, (const IT*)a.v, a.g,
                                                    (const IT*)a.beta, ws);
     stage_mark(s, "bwd_prep");
@@ -696,7 +695,7 @@ cudaError_t simt_backward_t(const Dims& d, const BwdArgs& a, const Workspace& ws
     const int dvs = dv_slice(d);
     const dim3 gs(d.num_seqs, d.Hv, d.DV / dvs);
     size_t smw = sizeof(float) * (d.DK * dvs + kChunk * dvs + kChunk * kLd + kChunk + kChunk * (2 * (d.DK + 1) + dvs + 1));
-    cudaFuncSetAttribute(simt_walk_kernel<IT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smw);
+    set_smem_once((const void*)simt_walk_kernel<IT>, smw);
     simt_walk_kernel<IT><<<gs, kThreads, smw, s>>>(d, (const IT*)a.q, (const IT*)a.k, (const IT*)a.dO,
                                                    a.dS_T, a.dS0, ws, dvs);
     stage_mark(s, "bwd_walk");
@@ -707,7 +706,7 @@ cudaError_t simt_backward_t(const Dims& d, const BwdArgs& a, const Workspace& ws
     size_t smg = sizeof(float) * (6 * kChunk * kLd + kChunk * d.DV + kChunk * d.DK + 4 * kChunk + 32);
     if (stage) smg += sizeof(float) * kChunk * (2 * (d.DK + 1) + 3 * (d.DV + 1));
     auto grad = stage ? simt_grad_kernel<IT, true> : simt_grad_kernel<IT, false>;
-    cudaFuncSetAttribute(grad, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
+    set_smem_once((const void*)grad, smg);
     grad<<<gc, kThreads, smg, s>>>(d, (const IT*)a.q, (const IT*)a.k, (const IT*)a.v,
                                                    (const IT*)a.beta, a.h_saved, (const IT*)a.dO,
                                                    (IT*)a.dq, (IT*)a.dk, (IT*)a.dv, a.dg, (IT*)a.dbeta, ws);
@@ -723,11 +722,13 @@ cudaError_t simt_backward_t(const Dims& d, const BwdArgs& a, const Workspace& ws
 }  // namespace
 
 cudaError_t simt_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s) {
+  if (simt_small(d)) return simt_small_forward(d, a, ws, s);
   return d.dtype == GDR_DTYPE_F32 ? simt_forward_t<float>(d, a, ws, s)
                                   : simt_forward_t<__nv_bfloat16>(d, a, ws, s);
 }
 
 cudaError_t simt_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cudaStream_t s) {
+  if (simt_small(d)) return simt_small_backward(d, a, ws, s);
   return d.dtype == GDR_DTYPE_F32 ? simt_backward_t<float>(d, a, ws, s)
                                   : simt_backward_t<__nv_bfloat16>(d, a, ws, s);
 }

@@ -30,6 +30,7 @@
 
 #include "../../include/gdr_debug.h"
 #include "gdr_internal.h"
+#include "gdr_chunks.cuh"
 #include "tc_common.cuh"
 #include "tc_primitives.cuh"
 
@@ -300,14 +301,14 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tm_q, const CUtenso
   GDR_TRACE_CTA_BEGIN();
   bool ok = true;
   uint32_t item_par = 0;  // phase parity of bar_tma for the current item (bar_mma: 2 per item)
-  const int n_items = kFused ? ws.step_off[ws.step_off[d.max_chunks + 1]] * Hv : d.max_chunks * Hv;
+  const int n_items = kFused ? idx_step_off(d, ws, idx_n_steps(d, ws)) * Hv : d.max_chunks * Hv;
   // the next item and its chunk into s_item[slot], s_item[slot + 1] (thread 0 decides; everyone
   // reads them after a barrier)
   auto next_item = [&](int w, int slot) {
     if (kFused) {
       const int q = (int)atomicAdd(ws.fwd_queue, 1u);
       s_item[slot] = q < n_items ? q : n_items;
-      s_item[slot + 1] = q < n_items ? ws.fwd_chunk[q / Hv] : 0;
+      s_item[slot + 1] = q < n_items ? idx_fwd_chunk(d, ws, q / Hv) : 0;
     } else {
       w = w < 0 ? (int)blockIdx.x : w + (int)gridDim.x;
       s_item[slot] = w;
@@ -316,7 +317,7 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tm_q, const CUtenso
   };
   // q/k/v tiles of item w (chunk cc) into stage st
   auto issue_loads = [&](int w, int cc, int st) {
-    const int j2 = w % Hv, i2 = j2 / d.G, tt = ws.chunks[cc].y;
+    const int j2 = w % Hv, i2 = j2 / d.G, tt = idx_chunk(d, ws, cc).y;
     unsigned char* kq = sm + (st ? PrepSmem::BYTES : PrepSmem::KQ);
     unsigned char* vv = sm + (st ? PrepSmem::BYTES + 2 * 16384 : PrepSmem::V);
     tc::mbar_arrive_expect_tx(&bar_tma[st], 6 * kSlab);
@@ -337,7 +338,7 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tm_q, const CUtenso
   int it = 0;    // kFused: items done (stage it & 1, phase (it >> 1) & 1)
   while (witem < n_items && ok) {
   const int j = witem % Hv, i = j / d.G;
-  const int4 ci = ws.chunks[c];
+  const int4 ci = idx_chunk(d, ws, c);
   const int len = ci.z, t0 = ci.y;
   const size_t ch = (size_t)c * Hv + j;
   const int st = kFused ? (it & 1) : 0;
@@ -621,14 +622,14 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
   // block -> (sequence in longest-first order, v-head, DV slice); the slices of one
   // (sequence, head) are adjacent so they share its W/Q/K tiles in L2
   const int slice = cta % kStateSlices, rest = cta / kStateSlices;
-  const int j = rest % d.Hv, n = ws.seq_order[rest / d.Hv], i = j / d.G;
+  const int j = rest % d.Hv, n = idx_seq(d, ws, rest / d.Hv), i = j / d.G;
   const int dv0 = slice * 32;
   const int tid = threadIdx.x, warp = tid >> 5;
   // thread 0 issues the MMAs; thread 32 (the "copy thread") issues every TMA load and
   // store and waits on their bulk groups, so neither kind of issue delays the other
   constexpr int kCopyTid = 32;
   const int Hv = d.Hv;
-  const int c_begin = ws.seq_chunk_off[n], c_end = ws.seq_chunk_off[n + 1];
+  const int c_begin = idx_seq_off(d, ws, n), c_end = idx_seq_off(d, ws, n + 1);
   const int t_seq = d.cu ? d.cu[n] : n * d.T;        // first token of the sequence
   const int L = d.cu ? d.cu[n + 1] - t_seq : d.T;     // its length
 
@@ -990,7 +991,7 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
   if (fused_fwd_possible(d) && n_cta * 2 <= n_sm) {
     const size_t smf = std::max<size_t>(PrepSmem::BYTES, StateSmem<false>::BYTES) + 1024;
     auto kern = tc_fwd_fused_kernel;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf);
+    set_smem_once((const void*)kern, smf);
     int per_sm = 0;
     const cudaError_t qe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTcThreads, smf);
     if (qe != cudaSuccess) (void)cudaGetLastError();  // our own query's error: fall back below
@@ -1018,7 +1019,7 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
   }
   if (d.max_chunks > 0 && Tt > 0) {
     const size_t smp = PrepSmem::BYTES + 1024;
-    cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
+    set_smem_once((const void*)tc_prep_kernel, smp);
     tc_prep_kernel<<<prep_grid(d), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, d.save_wy ? tt : tp, d, a.g,
                                                                       (const bf16*)a.beta, ws, d.save_wy);
     stage_mark(s, "fwd_prep");
@@ -1028,7 +1029,7 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
     const bool single = n_cta > n_sm;
     const size_t sms = (single ? StateSmem<true>::BYTES : StateSmem<false>::BYTES) + 1024;
     auto kern = single ? tc_fwd_state_kernel<true> : tc_fwd_state_kernel<false>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sms);
+    set_smem_once((const void*)kern, sms);
     kern<<<(unsigned)n_cta, kTcThreads, sms, s>>>(tq, tk, tw, tu, tp, ths, d, a.S0, a.S_T, (bf16*)a.o, ws);
     stage_mark(s, "fwd_state");
   }
@@ -1046,7 +1047,7 @@ cudaError_t tc_launch_prep(const Dims& d, const void* q, const void* k, const vo
     return cudaErrorInvalidValue;
   if (write_T && !map_2d(&tt, ws.Tb, 64, rows)) return cudaErrorInvalidValue;
   const size_t smp = PrepSmem::BYTES + 1024;
-  cudaFuncSetAttribute(tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smp);
+  set_smem_once((const void*)tc_prep_kernel, smp);
   tc_prep_kernel<<<prep_grid(d), kTcThreads, smp, s>>>(tq, tk, tv, tw, tu, tp, tt, d, g,
                                                                     (const bf16*)beta, ws, write_T);
   stage_mark(s, stage);

@@ -27,6 +27,7 @@
 #include <cstdio>
 
 #include "gdr_internal.h"
+#include "gdr_chunks.cuh"
 #include "tc_common.cuh"
 #include "tc_primitives.cuh"
 
@@ -134,10 +135,10 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
   using WS = WalkSmem;
   __shared__ uint64_t bar_load[2], bar_scaled[2], bar_vfull[2], bar_hfull[2], bar_dvn[2], bar_dvnfree[2];
   __shared__ uint64_t bar_dh, bar_dhfree, bar_drain;
-  const int n = ws.seq_order[unit / d.Hv], j = unit % d.Hv, i = j / d.G;
+  const int n = idx_seq(d, ws, unit / d.Hv), j = unit % d.Hv, i = j / d.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hv = d.Hv;
-  const int c_begin = ws.seq_chunk_off[n], c_end = ws.seq_chunk_off[n + 1];
+  const int c_begin = idx_seq_off(d, ws, n), c_end = idx_seq_off(d, ws, n + 1);
   const int nch = c_end - c_begin;
   const int t_seq = d.cu ? d.cu[n] : n * d.T;
   const int L = d.cu ? d.cu[n + 1] - t_seq : d.T;
@@ -515,7 +516,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_vn_kernel(const __grid_constant
   uint32_t par = 0;
   for (int w = (int)blockIdx.x; w < n_items && ok; w += (int)gridDim.x) {
     const int c = w / Hv, j = w % Hv;
-    const int len = ws.chunks[c].z;
+    const int len = idx_chunk(d, ws, c).z;
     if (len <= 0) continue;  // an empty chunk slot (uniform across the CTA)
     const size_t ch = (size_t)c * Hv + j;
     if (tid == 0) {
@@ -691,19 +692,19 @@ __device__ __forceinline__ void grad_body(
   uint32_t mma_par = 0;   // phase parity of bar_mma (five commits per item: it alternates)
   // items: (chunk, v-head), or with kPair (chunk, q/k head) shared by the cluster, whose
   // CTA `rank` takes v-head 2 i + rank; with kDyn every real chunk's v-heads, in walk order
-  const int n_steps = kDyn ? ws.step_off[d.max_chunks + 1] : 0;
-  const int n_items = kDyn ? ws.step_off[n_steps] * Hv : (kPair ? d.max_chunks * d.Hk : d.max_chunks * Hv);
+  const int n_steps = kDyn ? idx_n_steps(d, ws) : 0;
+  const int n_items = kDyn ? idx_step_off(d, ws, n_steps) * Hv : (kPair ? d.max_chunks * d.Hk : d.max_chunks * Hv);
   const int item0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int istep = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   // kDyn: item w = q * Hv + v-head, queue position q in walk order (the index kernel lists
   // each position's chunk)
   auto chunk_of = [&](int w) {
-    if (kDyn) return ws.grad_chunk[w / Hv];
+    if (kDyn) return idx_grad_chunk(d, ws, w / Hv);
     return kPair ? w / d.Hk : w / Hv;
   };
   auto vhead_of = [&](int w) { return kPair ? (w % d.Hk) * 2 + (int)rank : w % Hv; };
   auto next_item = [&](int w) {  // next non-empty item of this CTA after w (or n_items)
-    for (w += istep; w < n_items && ws.chunks[chunk_of(w)].z <= 0; w += istep) {
+    for (w += istep; w < n_items && idx_chunk(d, ws, chunk_of(w)).z <= 0; w += istep) {
     }
     return w < n_items ? w : n_items;
   };
@@ -711,7 +712,7 @@ __device__ __forceinline__ void grad_body(
   enum : int { kLdDhDvn = 1, kLdW = 2, kLdRest = 4, kLdDo = 8, kLdAll = 15 };
   auto issue_loads = [&](int w, int c2, int groups) {  // copy thread only; c2 = chunk_of(w)
     GDR_DELAY(20);
-    const int j2 = vhead_of(w), i2 = j2 / d.G, tt = ws.chunks[c2].y;
+    const int j2 = vhead_of(w), i2 = j2 / d.G, tt = idx_chunk(d, ws, c2).y;
     const size_t ch2 = (size_t)c2 * Hv + j2;
     uint64_t* bar = &bar_tma;
     if (groups & kLdDhDvn) {  // the first group of an item sets the whole item's byte count
@@ -818,7 +819,7 @@ __device__ __forceinline__ void grad_body(
     cur_c = s_claim_c;
     gsync();
   } else {
-    witem = item0 < n_items && ws.chunks[chunk_of(item0)].z <= 0 ? next_item(item0) : item0;
+    witem = item0 < n_items && idx_chunk(d, ws, chunk_of(item0)).z <= 0 ? next_item(item0) : item0;
   }
   if (tid == kCopyTid && witem < n_items) issue_loads(witem, kDyn ? cur_c : chunk_of(witem), kLdAll);
   int pending = witem < n_items ? 0 : -1;  // groups of the next item issued so far (-1: none expected)
@@ -828,7 +829,7 @@ __device__ __forceinline__ void grad_body(
   const int wnext = kDyn ? n_items : next_item(witem);
   const int cnext = kDyn ? 0 : (wnext < n_items ? chunk_of(wnext) : 0);
   const int c = kDyn ? cur_c : chunk_of(witem), j = vhead_of(witem), i = j / d.G;
-  const int4 ci = ws.chunks[c];
+  const int4 ci = idx_chunk(d, ws, c);
   const int len = ci.z, t0 = ci.y;
   cur_len = len;
   cur_t0 = t0;
@@ -1387,7 +1388,7 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
   if (!d.save_wy && d.max_chunks > 0 && Tt > 0) {  // recomputed factors: Vn over U (see tc_vn_kernel)
     const long long n_items = (long long)d.max_chunks * d.Hv;
     const size_t smv = VnSmem::BYTES + 1024;
-    cudaFuncSetAttribute(tc_vn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smv);
+    set_smem_once((const void*)tc_vn_kernel, smv);
     tc_vn_kernel<<<(unsigned)(n_items < n_sm ? n_items : n_sm), kTcThreads, smv, s>>>(tw, tu, thf, d, ws);
     stage_mark(s, "bwd_vn");
   }
@@ -1401,7 +1402,7 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
   if (fused_walk_grad(d) && regs_ok) {  // walk and gradients in one cooperative kernel
     int per_sm = 0;
     const size_t smg = std::max(GradSmem::BYTES, WalkSmem::BYTES) + 1024;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
+    set_smem_once((const void*)kern, smg);
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWalkThreads, smg) != cudaSuccess || per_sm < 1)
       return cudaErrorInvalidConfiguration;
     e = cudaMemsetAsync(ws.walk_flags, 0, sizeof(uint32_t) * ((size_t)d.max_chunks * d.Hv + 64), s);
@@ -1426,7 +1427,7 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
   }
   if (d.num_seqs > 0) {
     const size_t sm = WalkSmem::BYTES + 1024;
-    cudaFuncSetAttribute(tc_bwd_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    set_smem_once((const void*)tc_bwd_walk_kernel, sm);
     tc_bwd_walk_kernel<<<d.num_seqs * d.Hv, kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, dd, a.dS_T,
                                                                   a.dS0, ws);
     stage_mark(s, "bwd_walk");
@@ -1437,7 +1438,7 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     const size_t smg = GradSmem::BYTES + 1024;
     if (grad_pair_mode(d)) {  // clusters of two CTAs, one per v-head of a q/k head
       auto kern = tc_bwd_grad_kernel<true, true>;
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
+      set_smem_once((const void*)kern, smg);
       cudaLaunchConfig_t cfg = {};
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1461,12 +1462,12 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
                              (const bf16*)a.beta, (bf16*)a.dq, (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
       if (e != cudaSuccess) return e;
     } else if (d.G > 1) {
-      cudaFuncSetAttribute(tc_bwd_grad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
+      set_smem_once((const void*)tc_bwd_grad_kernel<true>, smg);
       tc_bwd_grad_kernel<true><<<grid, kGradThreads, smg, s>>>(tq, tk, tv, tdo, tw, tu, tdvn, tdh, thf, tt, tdq, tdk,
                                                               tdv, d, (const bf16*)a.beta, (bf16*)a.dq,
                                                               (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);
     } else {
-      cudaFuncSetAttribute(tc_bwd_grad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smg);
+      set_smem_once((const void*)tc_bwd_grad_kernel<false>, smg);
       tc_bwd_grad_kernel<false><<<grid, kGradThreads, smg, s>>>(tq, tk, tv, tdo, tw, tu, tdvn, tdh, thf, tt, tdq, tdk,
                                                                tdv, d, (const bf16*)a.beta, (bf16*)a.dq,
                                                                (bf16*)a.dk, (bf16*)a.dv, a.dg, (bf16*)a.dbeta, ws);

@@ -11,7 +11,9 @@
  * bracketed and gdr_debug_stage_name(i) a stable stage name ("fwd_prep",
  * "bwd_grad", ...).  Pass events = NULL to switch it off.  The setting is
  * process-global host state and not thread-safe; the events stay owned by the
- * caller.
+ * caller.  A call made while its stream is being captured records them with
+ * cudaEventRecordExternal, which puts event-record nodes into the graph: every
+ * replay of the graph then times its kernels the same way.
  *
  * Launch counter: gdr_debug_launch_count() returns how many kernels this process
  * has launched through the library so far.
