@@ -104,7 +104,8 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
              tc_available())
                 ? 1
                 : 0;
-  d->save_wy = d->path == 1 ? p->save_wy : 0;
+  // saved chunk factors: the tensor-core path and the small-head SIMT path (gdr_simt_small.cu)
+  d->save_wy = (d->path == 1 || (p->DK <= 64 && p->DV <= 64)) ? p->save_wy : 0;
   return GDR_OK;
 }
 
@@ -177,8 +178,11 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
     w.W = take(el * chH * kChunk * d.DK);
     w.U = take(el * chH * kChunk * d.DV);
     if (d.path == 1) w.P = take(el * chH * kChunk * kChunk);
+  } else if (d.path == 0) {  // the small-head SIMT forward hands U from its prep to its state kernel
+    w.U = take(el * chH * kChunk * d.DV);
   }
   if (d.path == 0) w.Vn = take(el * chH * kChunk * d.DV);
+  if (simt_small(d)) w.Pf = (float*)take(sizeof(float) * chH * kChunk * kChunk);
   if (backward) {
     if (d.path == 0) w.Tm = (float*)take(sizeof(float) * chH * kChunk * kChunk);
     w.dhp = take(el * chH * d.DK * d.DV);
@@ -187,8 +191,9 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
       w.dVn = take(el * chH * kChunk * d.DV);
     } else if (simt_small(d)) {
       w.dVn = take(el * chH * kChunk * d.DV);
-      w.Pf = (float*)take(sizeof(float) * chH * kChunk * kChunk);
       w.Ak = (float*)take(sizeof(float) * chH * kChunk * kChunk);
+      w.PdO = (float*)take(sizeof(float) * chH * kChunk * d.DV);
+      w.QdO = (float*)take(sizeof(float) * chH * d.DK * d.DV);
     }
     if (fused_walk_grad(d)) {  // one region: flags then the claim counter (zeroed per call)
       w.walk_flags = (uint32_t*)take(sizeof(uint32_t) * ((size_t)d.max_chunks * d.Hv + 64));
@@ -220,10 +225,12 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
   return off;
 }
 
-// Saved buffer: the chunk-start states, then (save_wy, tensor-core path only) per region,
+// Saved buffer: the chunk-start states, then (save_wy) on the tensor-core path per region,
 // 256-byte aligned: gamma fp32 [chunks][Hv][64], W bf16 [..][64][DK], U bf16 [..][64][DV]
 // (replaced by Vn = U - W h by the forward's state kernel), P bf16 [..][64][64], T bf16
 // [..][64][64].
+// The small-head SIMT path keeps fp32 factors instead: gamma [..][64], W^T [..][DK][64],
+// T [..][64][64], K K^T * Gam (strictly lower) [..][64][64], P^T [..][64][64], Vn [..][64][DV].
 static size_t saved_layout(const Dims& d, const char* base, Workspace* ws) {
   const size_t chH = (size_t)d.max_chunks * d.Hv;
   size_t off = align256(chH * d.DK * d.DV * (d.h_bf16 ? 2 : 4));
@@ -233,6 +240,23 @@ static size_t saved_layout(const Dims& d, const char* base, Workspace* ws) {
     off += align256(bytes);
     return p;
   };
+  if (d.path == 0) {
+    float* gam = (float*)take(sizeof(float) * chH * kChunk);
+    void* Wt = take(sizeof(float) * chH * d.DK * kChunk);
+    float* T = (float*)take(sizeof(float) * chH * kChunk * kChunk);
+    float* Ak = (float*)take(sizeof(float) * chH * kChunk * kChunk);
+    float* Pt = (float*)take(sizeof(float) * chH * kChunk * kChunk);
+    void* Vn = take(sizeof(float) * chH * kChunk * d.DV);
+    if (ws) {
+      ws->gam = gam;
+      ws->W = Wt;
+      ws->Tm = T;
+      ws->Ak = Ak;
+      ws->Pf = Pt;
+      ws->Vn = Vn;
+    }
+    return off;
+  }
   float* gam = (float*)take(sizeof(float) * chH * kChunk);
   void* W = take(2 * chH * kChunk * d.DK);
   void* U = take(2 * chH * kChunk * d.DV);

@@ -219,8 +219,9 @@ __global__ void __launch_bounds__(kIndexThreads) gdr_index_kernel(const int32_t*
 bool index_folded(const Dims& d) { return d.cu == nullptr && d.max_chunks > 0 && d.num_seqs > 0; }
 
 cudaError_t launch_index(const Dims& d, const Workspace& ws, cudaStream_t s) {
-  // fixed length: the kernels compute every record (gdr_chunks.cuh); only the status is reset
-  if (index_folded(d)) return cudaMemsetAsync(ws.status, 0, 64 * sizeof(uint32_t), s);
+  // fixed length: the kernels compute every record (gdr_chunks.cuh); only the status is reset,
+  // by the first kernel on the small-head SIMT path (gdr_simt_small.cu), else here
+  if (index_folded(d)) return simt_small(d) ? cudaSuccess : cudaMemsetAsync(ws.status, 0, 64 * sizeof(uint32_t), s);
   gdr_index_kernel<<<1, kIndexThreads, 0, s>>>(d.cu, d.num_seqs, d.cu ? (int)d.T_total : d.T,
                                                d.max_chunks, ws.chunks, ws.seq_chunk_off, ws.seq_order,
                                                ws.status, ws.step_off, ws.grad_chunk, ws.fwd_chunk);

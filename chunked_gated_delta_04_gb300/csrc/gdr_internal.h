@@ -53,8 +53,11 @@ struct Workspace {
                  // (fp32 on the SIMT path, bf16 on the tensor-core path)
   void* Tb;      // tensor-core backward: T = (I + A)^{-1}, bf16 [max_chunks][Hv][64][64]
   void* dVn;     // backward: dL/dVn [max_chunks][Hv][64][DV] (bf16 tensor-core path, fp32 small-head SIMT path)
-  float* Pf;     // small-head SIMT backward: Q K^T * Gam on and below the diagonal [max_chunks][Hv][64][64]
+  float* Pf;     // small-head SIMT path: P = Q K^T * Gam on and below the diagonal [max_chunks][Hv][64][64];
+                 // the forward keeps it transposed (P^T, the state kernel's operand), the backward not
   float* Ak;     // small-head SIMT backward: K K^T * Gam below the diagonal [max_chunks][Hv][64][64]
+  float* PdO;    // small-head SIMT backward: scale P^T dO [max_chunks][Hv][64][DV]
+  float* QdO;    // small-head SIMT backward: (scale diag(e^gamma) Q)^T dO [max_chunks][Hv][DK][DV]
   float* dq_part;  // backward, Hv > Hk: [T_total][Hv][DK]
   float* dk_part;  // backward, Hv > Hk: [T_total][Hv][DK]
   // fused walk + gradient kernel (fixed-length tensor-core backward): per (chunk, v-head) count

@@ -105,8 +105,9 @@ typedef struct {
                                 (gamma, W, Vn, P and T of the WY form, see "Saved factors"
                                 below) in the saved buffer after the states, and the
                                 backward reads them instead of recomputing them.  Same
-                                results bit for bit; honoured on the tensor-core path,
-                                ignored (nothing saved) on the SIMT path. */
+                                results (bit for bit on the tensor-core path); honoured on
+                                the tensor-core path and on the SIMT path for DK, DV <= 64,
+                                ignored (nothing saved) for larger SIMT heads. */
 } gdr_problem;
 
 /* Upper bound on the number of 64-token chunks: B * ceil(T/64) for fixed length,
@@ -114,15 +115,18 @@ typedef struct {
 size_t gdr_max_chunks(const gdr_problem* p);
 
 /* Bytes of h_saved: gdr_max_chunks(p) * Hv * DK * DV * (4 for F32, 2 for BF16 h_dtype),
- * plus, with save_wy on the tensor-core path, gdr_max_chunks(p) * Hv * 49408 bytes of saved
- * factors.
+ * plus, with save_wy, the saved factors: on the tensor-core path gdr_max_chunks(p) * Hv *
+ * 49408 bytes; on the SIMT path (DK, DV <= 64) gdr_max_chunks(p) * Hv * 4 * (64 + 64 DK +
+ * 3 * 4096 + 64 DV) bytes, each region rounded up to 256 bytes.
  * Saved factors (save_wy): after the states, per (chunk, v-head) of the chunk index, in
  * this order, each region starting 256-byte aligned: gamma fp32 [64] (in-chunk cumulative
  * sum of g), W bf16 [64][DK], Vn bf16 [64][DV], P bf16 [64][64], T bf16 [64][64] (chunked
  * WY form of the gated delta rule: T = (I + strictly lower diag(beta) Gamma K K^T)^{-1},
  * W = T diag(beta e^gamma) K, U = T diag(beta) V, Vn = U - W h with h the chunk-start
- * state, P = masked decayed Q K^T).  gdr_bwd requires them to come from gdr_fwd with the
- * same problem and inputs. */
+ * state, P = masked decayed Q K^T).  The SIMT path keeps, in this order and all fp32: gamma
+ * [64], W^T [DK][64], T [64][64], the strictly lower decayed K K^T [64][64], P^T [64][64],
+ * Vn [64][DV].  gdr_bwd requires them to come from gdr_fwd with the same problem and
+ * inputs. */
 size_t gdr_saved_states_bytes(const gdr_problem* p);
 
 /* Bytes of the scratch workspace that gdr_fwd / gdr_bwd need (device memory,

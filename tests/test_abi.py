@@ -59,8 +59,15 @@ def test_size_queries(lib):
     assert gdr.gdr_fwd_workspace_bytes(prob(prologue=7)) > gdr.gdr_fwd_workspace_bytes(p)
     assert gdr.gdr_bwd_workspace_bytes(prob(prologue=1)) > gdr.gdr_bwd_workspace_bytes(p)
     # saved factors: on the tensor-core path 49408 bytes per (chunk, v-head) move from the
-    # workspaces into the saved buffer; elsewhere the option changes nothing
-    assert gdr.gdr_saved_states_bytes(prob(save_wy=True)) == gdr.gdr_saved_states_bytes(p)  # SIMT shape
+    # workspaces into the saved buffer; on the SIMT path with DK, DV <= 64 fp32 gamma, W^T, T,
+    # K K^T * Gam, P^T and Vn (each region 256-byte aligned); larger SIMT heads save nothing
+    def a256(x):
+        return (x + 255) // 256 * 256
+    chH = 6 * 4
+    factors = (a256(chH * 64 * 4) + a256(chH * 64 * 64 * 4) + 3 * a256(chH * 64 * 64 * 4) +
+               a256(chH * 64 * 32 * 4))
+    assert gdr.gdr_saved_states_bytes(prob(save_wy=True)) == a256(gdr.gdr_saved_states_bytes(p)) + factors
+    assert gdr.gdr_saved_states_bytes(prob(DK=96, DV=96, save_wy=True)) == gdr.gdr_saved_states_bytes(prob(DK=96, DV=96))
     pt, pts = prob(DK=128, DV=128), prob(DK=128, DV=128, save_wy=True)
     chH = 6 * 4
     if gdr.gdr_path(pt) == 1:

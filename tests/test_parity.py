@@ -79,6 +79,7 @@ def test_tiny_fp32_workload():
 # saving them (the benchmark's default), and (b2_t4096) bf16 chunk-start states.  Each case's
 # per-tensor rel_max is recorded in the parity-margins table (see gdr_testlib.record_margins).
 NAMED = [("tiny_fp32", None, "simt", {}),
+         ("tiny_fp32", None, "simt, saved", {"save_wy": True}),
          ("b2_t4096", [0, 15], "recompute", {}),
          ("b2_t4096", [0, 15], "saved", {"save_wy": True}),
          ("b2_t4096", [0, 15], "saved, h bf16", {"save_wy": True, "h_dtype": torch.bfloat16}),
@@ -217,24 +218,28 @@ def test_bf16_saved_states_match_oracle(case):
 
 
 SAVE_WY_CASES = [
-    # name, B, T, Hk, Hv, layout, seqlens, h_dtype, prologue
-    ("fused_b2_t300_vk", 2, 300, 2, 2, "VK", None, torch.float32, 0),        # fused walk + grad
-    ("pair_varlen", 1, None, 1, 2, "KV", [0, 1, 64, 77, 200], torch.float32, 0),  # Hv = 2 Hk clusters
-    ("group4_t130", 1, 130, 1, 4, "KV", None, torch.bfloat16, 0),            # group partials
-    ("fused_prologue", 2, 193, 2, 2, "KV", None, torch.float32, 7),          # raw inputs
+    # name, B, T, Hk, Hv, layout, seqlens, h_dtype, prologue, input dtype, D
+    ("fused_b2_t300_vk", 2, 300, 2, 2, "VK", None, torch.float32, 0, torch.bfloat16, 128),  # fused walk + grad
+    ("pair_varlen", 1, None, 1, 2, "KV", [0, 1, 64, 77, 200], torch.float32, 0, torch.bfloat16, 128),  # clusters
+    ("group4_t130", 1, 130, 1, 4, "KV", None, torch.bfloat16, 0, torch.bfloat16, 128),  # group partials
+    ("fused_prologue", 2, 193, 2, 2, "KV", None, torch.float32, 7, torch.bfloat16, 128),  # raw inputs
+    # the SIMT path for heads of at most 64 features (fp32 factors in the saved buffer)
+    ("simt_f32_b2_t130", 2, 130, 2, 2, "KV", None, torch.float32, 0, torch.float32, 64),
+    ("simt_f32_varlen_gva", 1, None, 1, 2, "VK", [0, 1, 64, 77, 200], torch.float32, 0, torch.float32, 32),
+    ("simt_bf16_d48_prologue", 2, 193, 2, 2, "KV", None, torch.float32, 7, torch.bfloat16, 48),
 ]
 
 
 @pytest.mark.parametrize("case", SAVE_WY_CASES, ids=[c[0] for c in SAVE_WY_CASES])
 def test_saved_factors_give_identical_results(case):
     """save_wy only moves where the chunk factors come from (kept by the forward instead of
-    recomputed by the backward, by the same kernel on the same inputs): every output is bitwise
+    recomputed by the backward, by the same code on the same inputs): every output is bitwise
     the same as without it, and the oracle agrees."""
-    name, B, T, Hk, Hv, layout, lens, h_dtype, pro = case
+    name, B, T, Hk, Hv, layout, lens, h_dtype, pro, dt, D = case
     if lens is None:
-        w = small_workload(name, torch.bfloat16, B, T, Hk, Hv, 128, 128, layout)
+        w = small_workload(name, dt, B, T, Hk, Hv, D, D, layout)
     else:
-        w = small_workload(name, torch.bfloat16, Hk=Hk, Hv=Hv, DK=128, DV=128, seqlens=lens, layout=layout)
+        w = small_workload(name, dt, Hk=Hk, Hv=Hv, DK=D, DV=D, seqlens=lens, layout=layout)
     inp = make_inputs(w, raw=bool(pro))
     base = run_gpu(inp, h_dtype=h_dtype, prologue=pro)
     res = run_gpu(inp, h_dtype=h_dtype, prologue=pro, save_wy=True)
@@ -244,7 +249,7 @@ def test_saved_factors_give_identical_results(case):
         if base.get(key) is not None:
             a, b = (base[key], res[key]) if key != "h_saved" else (base[key][:n_chunks], res[key][:n_chunks])
             assert torch.equal(a, b), key
-    compare(res, reference(inp, prologue=pro), 2e-2)
+    compare(res, reference(inp, prologue=pro), 1e-4 if dt == torch.float32 else 2e-2)
 
 
 def test_saved_factors_need_the_larger_buffer():
