@@ -51,6 +51,13 @@ STAGE_IO = {
     "bwd_group_reduce": ("", "dq dk"),
     "bwd_walkgrad": ("q k v dO beta h_saved dS_T", "dq dk dv dg dbeta dS0"),
     "prologue": ("q k g beta", ""),
+    # context-parallel passes: the outputs are written by both passes; the second is counted
+    "fwd_cp_maps": ("q k S0", ""),
+    "fwd_cp_scan": ("", ""),
+    "fwd_cp_state": ("q k", "o h_saved S_T"),
+    "bwd_cp_maps": ("dO dS_T", ""),
+    "bwd_cp_scan": ("", ""),
+    "bwd_cp_walk": ("dO", "dS0"),
     "prologue_bwd": ("", "dq dk dg dbeta"),
 }
 
@@ -256,7 +263,8 @@ def reference_arm(args, w, inp):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w, inp, args.h_dtype, args.prologue, args.recompute_wy),
+        "config": config_dict(w, inp, args.h_dtype, args.prologue, args.recompute_wy,
+                              (args.cp_fwd, args.cp_bwd)),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": min(nthreads, units), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -265,8 +273,9 @@ def reference_arm(args, w, inp):
     return 0
 
 
-def config_dict(w, inp, h_dtype="f32", prologue=False, recompute_wy=False):
-    return {"workload": w.name, "B": w.B if inp["cu_seqlens"] is None else 1, "T": int(sum(inp["seqlens"])) if
+def config_dict(w, inp, h_dtype="f32", prologue=False, recompute_wy=False, cp=(1, 1)):
+    extra = {"context_parallel_segments": {"fwd": cp[0], "bwd": cp[1]}} if max(cp) > 1 else {}
+    return {**extra, "workload": w.name, "B": w.B if inp["cu_seqlens"] is None else 1, "T": int(sum(inp["seqlens"])) if
             inp["cu_seqlens"] is not None else w.T, "Hk": w.Hk, "Hv": w.Hv, "DK": w.DK, "DV": w.DV,
             "layout": w.layout, "num_seqs": inp["num_seqs"], "chunk": CHUNK,
             "varlen": inp["cu_seqlens"] is not None, "S0": inp["S0"] is not None,
@@ -306,6 +315,10 @@ def main():
                     help="raw q, k, gate and beta logits; the operator applies the L2 norm, logsigmoid, sigmoid")
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct C-ABI calls instead of a CUDA-graph replay of the same calls")
+    ap.add_argument("--cp-fwd", type=int, default=1,
+                    help="intra-card context parallelism: segments per sequence in the forward (1: off)")
+    ap.add_argument("--cp-bwd", type=int, default=1,
+                    help="intra-card context parallelism: segments per sequence in the backward (1: off)")
     ap.add_argument("--recompute-wy", action="store_true",
                     help="the backward recomputes the chunk factors (gamma, W, U, P, T) instead of reading the "
                          "ones the forward saved")
@@ -342,7 +355,8 @@ def main():
     Hv, DV = d["v"].shape[2], d["v"].shape[3]
     h_dtype = torch.bfloat16 if args.h_dtype == "bf16" else torch.float32
     p = gdr.make_problem(B, T, Hk, Hv, DK, DV, d["q"].dtype, w.layout, d["cu_seqlens"], h_dtype=h_dtype,
-                         prologue=prologue_bits, save_wy=not args.recompute_wy)
+                         prologue=prologue_bits, save_wy=not args.recompute_wy, cp_fwd=args.cp_fwd,
+                         cp_bwd=args.cp_bwd)
     stream = torch.cuda.current_stream()
     N = p.num_seqs
     sshape = (N, Hv, DK, DV) if w.layout == "KV" else (N, Hv, DV, DK)
@@ -578,7 +592,8 @@ def main():
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
             "data": "synthetic (seeded; see chunked_gated_delta_04_gb300/inputs.py)",
-            "config": config_dict(w, inp, args.h_dtype, args.prologue, args.recompute_wy),
+            "config": config_dict(w, inp, args.h_dtype, args.prologue, args.recompute_wy,
+                                  (args.cp_fwd, args.cp_bwd)),
             "roofline": roofline,
             "step_roofline": {"ms": step_roof, "frac": step_roof / ms_per_step, "bound": "hbm" if
                               t_hbm_step >= t_flop_step else "tensor", "bytes": wm["bytes_fwd"] + wm["bytes_bwd"],

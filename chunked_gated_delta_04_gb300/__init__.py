@@ -40,7 +40,7 @@ class gdr_problem(ctypes.Structure):
                 ("DK", ctypes.c_int), ("DV", ctypes.c_int), ("num_seqs", ctypes.c_int),
                 ("cu_seqlens", ctypes.c_void_p), ("dtype", ctypes.c_int), ("layout", ctypes.c_int),
                 ("scale", ctypes.c_float), ("h_dtype", ctypes.c_int), ("prologue", ctypes.c_uint),
-                ("save_wy", ctypes.c_int)]
+                ("save_wy", ctypes.c_int), ("cp_fwd", ctypes.c_int), ("cp_bwd", ctypes.c_int)]
 
 
 class GDRError(RuntimeError):
@@ -59,7 +59,7 @@ _STAGE_ARR = None
 EXPORTS = ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes", "gdr_bwd_workspace_bytes",
            "gdr_fwd", "gdr_bwd", "gdr_workspace_status", "gdr_status_string", "gdr_path",
            "gdr_debug_set_stage_events", "gdr_debug_stage_count", "gdr_debug_stage_name",
-           "gdr_debug_launch_count", "gdr_debug_last_cuda_error", "gdr_debug_cuda_error_string", "gdr_fwd_noalloc", "gdr_noalloc_status", "gdr_debug_tc_gemm", "gdr_debug_timeout_selftest"]
+           "gdr_debug_launch_count", "gdr_debug_last_cuda_error", "gdr_debug_cuda_error_string", "gdr_fwd_noalloc", "gdr_noalloc_status", "gdr_debug_tc_gemm", "gdr_debug_timeout_selftest", "gdr_debug_cp_segment"]
 
 
 def _open(path: str):
@@ -101,6 +101,8 @@ def _open(path: str):
     lib.gdr_debug_tc_gemm.restype = i
     lib.gdr_debug_timeout_selftest.argtypes = [vp, ctypes.c_ulonglong, vp, vp]
     lib.gdr_debug_timeout_selftest.restype = i
+    lib.gdr_debug_cp_segment.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_int)]
+    lib.gdr_debug_cp_segment.restype = i
     return lib
 
 
@@ -159,10 +161,11 @@ def _dtype_code(dtype):
 
 
 def make_problem(B, T, Hk, Hv, DK, DV, dtype, layout="KV", cu_seqlens=None, num_seqs=None, scale=None,
-                 h_dtype=torch.float32, prologue=0, save_wy=False):
+                 h_dtype=torch.float32, prologue=0, save_wy=False, cp_fwd=1, cp_bwd=1):
     """Build a gdr_problem.  dtype, h_dtype (of h_saved): torch.float32/bfloat16; layout "KV"/"VK";
     prologue: bit set of GDR_PROLOGUE_* (the matching inputs are raw); save_wy: the forward keeps
-    its chunk factors in the saved buffer for the backward."""
+    its chunk factors in the saved buffer for the backward; cp_fwd, cp_bwd: context-parallel
+    segments per sequence of each direction (1: off)."""
     p = gdr_problem()
     p.B, p.T, p.Hk, p.Hv, p.DK, p.DV = B, T, Hk, Hv, DK, DV
     if cu_seqlens is not None:
@@ -175,6 +178,7 @@ def make_problem(B, T, Hk, Hv, DK, DV, dtype, layout="KV", cu_seqlens=None, num_
     p.h_dtype = _dtype_code(h_dtype)
     p.prologue = int(prologue)
     p.save_wy = int(save_wy) if isinstance(save_wy, (bool, int)) else 99
+    p.cp_fwd, p.cp_bwd = int(cp_fwd), int(cp_bwd)
     p.layout = {"KV": GDR_STATE_KV, "VK": GDR_STATE_VK}.get(layout, 99) if isinstance(layout, str) else layout
     p.scale = 0.0 if scale is None else float(scale)
     return p
@@ -274,6 +278,15 @@ def gdr_debug_timeout_selftest(status, limit_ns, waited_ns, stream=None) -> int:
                                                     _stream_ptr(stream))
 
 
+def gdr_debug_cp_segment(c0: int, c1: int, P: int, s: int):
+    """(first chunk, end chunk, number of segments) of context-parallel segment s (host only)."""
+    out = (ctypes.c_int * 3)()
+    st = _lib_handle().gdr_debug_cp_segment(c0, c1, P, s, out)
+    if st != 0:
+        raise ValueError(f"gdr_debug_cp_segment({c0}, {c1}, {P}, {s}): invalid arguments")
+    return tuple(out)
+
+
 def gdr_debug_launch_count() -> int:
     return _lib_handle().gdr_debug_launch_count()
 
@@ -283,11 +296,12 @@ def _check(st, where):
         raise GDRError(st, where)
 
 
-def _problem_for(q, v, cu_seqlens, layout, scale, h_dtype=torch.float32, prologue=0, save_wy=False):
+def _problem_for(q, v, cu_seqlens, layout, scale, h_dtype=torch.float32, prologue=0, save_wy=False, cp_fwd=1,
+                 cp_bwd=1):
     B, T, Hk, DK = q.shape
     Hv, DV = v.shape[2], v.shape[3]
     return make_problem(B, T, Hk, Hv, DK, DV, q.dtype, layout, cu_seqlens, scale=scale, h_dtype=h_dtype,
-                        prologue=prologue, save_wy=save_wy)
+                        prologue=prologue, save_wy=save_wy, cp_fwd=cp_fwd, cp_bwd=cp_bwd)
 
 
 def alloc_saved(p, h_dtype, device) -> torch.Tensor:
@@ -316,11 +330,12 @@ def alloc_workspace(nbytes: int, device) -> torch.Tensor:
 
 # ------------------------------------------------------------------ allocating helpers
 def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, layout="KV", scale=None, output_final_state=True,
-            workspace=None, stream=None, h_dtype=torch.float32, prologue=0, save_wy=False):
+            workspace=None, stream=None, h_dtype=torch.float32, prologue=0, save_wy=False, cp=1):
     """Run gdr_fwd; returns (o, S_T or None, h_saved).  h_dtype: dtype of h_saved; prologue:
     GDR_PROLOGUE_* bits (q, k, g, beta raw where set); save_wy: h_saved's storage also keeps the
-    chunk factors, and backward() must be given save_wy=True too."""
-    p = _problem_for(q, v, cu_seqlens, layout, scale, h_dtype, prologue, save_wy)
+    chunk factors, and backward() must be given save_wy=True too; cp: context-parallel segments
+    per sequence (1: off)."""
+    p = _problem_for(q, v, cu_seqlens, layout, scale, h_dtype, prologue, save_wy, cp_fwd=cp)
     dev = q.device
     N = p.num_seqs
     o = torch.empty_like(v)
@@ -334,10 +349,11 @@ def forward(q, k, v, g, beta, S0=None, cu_seqlens=None, layout="KV", scale=None,
 
 
 def backward(q, k, v, g, beta, h_saved, dO, dS_T=None, cu_seqlens=None, layout="KV", scale=None,
-             want_dS0=True, workspace=None, stream=None, prologue=0, save_wy=False):
+             want_dS0=True, workspace=None, stream=None, prologue=0, save_wy=False, cp=1):
     """Run gdr_bwd; returns (dq, dk, dv, dg, dbeta, dS0 or None).  h_saved's dtype selects h_dtype;
-    with prologue bits the gradients are w.r.t. the raw inputs; save_wy as given to forward()."""
-    p = _problem_for(q, v, cu_seqlens, layout, scale, h_saved.dtype, prologue, save_wy)
+    with prologue bits the gradients are w.r.t. the raw inputs; save_wy as given to forward(); cp:
+    context-parallel segments per sequence (1: off; independent of the forward's)."""
+    p = _problem_for(q, v, cu_seqlens, layout, scale, h_saved.dtype, prologue, save_wy, cp_bwd=cp)
     _check_saved(p, h_saved)
     dev = q.device
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -355,12 +371,12 @@ def backward(q, k, v, g, beta, h_saved, dO, dS_T=None, cu_seqlens=None, layout="
 
 class _GDRFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype, prologue, save_wy):
+    def forward(ctx, q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype, prologue, save_wy, cp_fwd, cp_bwd):
         o, S_T, h_saved = forward(q, k, v, g, beta, S0, cu_seqlens, layout, scale, h_dtype=h_dtype,
-                                  prologue=prologue, save_wy=save_wy)
+                                  prologue=prologue, save_wy=save_wy, cp=cp_fwd)
         ctx.save_for_backward(q, k, v, g, beta, h_saved, cu_seqlens)
         ctx.layout, ctx.scale, ctx.has_S0, ctx.prologue = layout, scale, S0 is not None, prologue
-        ctx.save_wy = save_wy
+        ctx.save_wy, ctx.cp_bwd = save_wy, cp_bwd
         return o, S_T
 
     @staticmethod
@@ -369,16 +385,18 @@ class _GDRFunction(torch.autograd.Function):
         dq, dk, dv, dg, dbeta, dS0 = backward(q, k, v, g, beta, h_saved, do.contiguous(),
                                               None if dS_T is None else dS_T.contiguous(), cu_seqlens,
                                               ctx.layout, ctx.scale, want_dS0=ctx.has_S0, prologue=ctx.prologue,
-                                              save_wy=ctx.save_wy)
-        return dq, dk, dv, dg, dbeta, dS0, None, None, None, None, None, None
+                                              save_wy=ctx.save_wy, cp=ctx.cp_bwd)
+        return dq, dk, dv, dg, dbeta, dS0, None, None, None, None, None, None, None, None
 
 
 def chunk_gated_delta_rule(q, k, v, g, beta, initial_state=None, cu_seqlens=None, layout="KV", scale=None,
-                           h_dtype=torch.float32, prologue=0, save_wy=True):
+                           h_dtype=torch.float32, prologue=0, save_wy=True, cp_fwd=1, cp_bwd=1):
     """Autograd entry point: returns (o, final_state).  Tensors as in include/gdr.h; h_dtype is the
     dtype of the chunk-start states kept for the backward (bfloat16 halves their memory); prologue
     (GDR_PROLOGUE_* bits) makes the operator normalise q, k and map raw gate / beta logits itself;
     save_wy (default) keeps the forward's chunk factors for the backward (49408 bytes per chunk and
-    v-head more saved memory, no recomputation in the backward; same results bit for bit)."""
+    v-head more saved memory, no recomputation in the backward; same results bit for bit); cp_fwd,
+    cp_bwd: context-parallel segments per sequence of each direction (1: off), for few long
+    sequences whose (sequence, v-head) chains would leave most SMs idle."""
     return _GDRFunction.apply(q, k, v, g, beta, initial_state, cu_seqlens, layout, scale, h_dtype, prologue,
-                              save_wy)
+                              save_wy, cp_fwd, cp_bwd)

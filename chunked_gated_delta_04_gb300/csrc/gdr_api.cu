@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include "gdr_internal.h"
+#include "gdr_chunks.cuh"
 #include "../../include/gdr_debug.h"
 #include <atomic>
 #include <mutex>
@@ -72,6 +73,8 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
   if (p->h_dtype != GDR_DTYPE_F32 && p->h_dtype != GDR_DTYPE_BF16) return GDR_ERR_INVALID_ARG;
   if (p->prologue & ~7u) return GDR_ERR_INVALID_ARG;
   if (p->save_wy != 0 && p->save_wy != 1) return GDR_ERR_INVALID_ARG;
+  if (p->cp_fwd < 0 || p->cp_fwd > kMaxCpSegments || p->cp_bwd < 0 || p->cp_bwd > kMaxCpSegments)
+    return GDR_ERR_INVALID_ARG;
   if (p->cu_seqlens != nullptr) {
     if (p->B != 1) return GDR_ERR_INVALID_ARG;
   } else if (p->num_seqs != p->B) {
@@ -106,6 +109,9 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
                 : 0;
   // saved chunk factors: the tensor-core path and the small-head SIMT path (gdr_simt_small.cu)
   d->save_wy = (d->path == 1 || (p->DK <= 64 && p->DV <= 64)) ? p->save_wy : 0;
+  // context-parallel segments: the tensor-core path (the SIMT path runs the plain chain)
+  d->cp_fwd = d->path == 1 && p->cp_fwd > 1 ? p->cp_fwd : 1;
+  d->cp_bwd = d->path == 1 && p->cp_bwd > 1 ? p->cp_bwd : 1;
   return GDR_OK;
 }
 
@@ -211,6 +217,13 @@ size_t layout_workspace(const Dims& d, bool backward, char* base, Workspace* ws)
     w.fwd_queue = w.fwd_flags ? w.fwd_flags + (size_t)d.max_chunks * d.Hv : nullptr;
     w.step_off = (int*)take(sizeof(int) * ((size_t)d.max_chunks + 2));
     w.fwd_chunk = (int*)take(sizeof(int) * ((size_t)d.max_chunks + 1));
+  }
+  const int cp = backward ? d.cp_bwd : d.cp_fwd;
+  if (d.path == 1 && cp > 1) {  // boundary states, transitions, zero-boundary results (CpArgs)
+    const size_t mats = (size_t)d.num_seqs * d.Hv * cp * 128 * 128 * sizeof(float);
+    w.cp_X = (float*)take(mats);
+    w.cp_M = (float*)take(mats);
+    w.cp_R = (float*)take(mats);
   }
   if (d.prologue) {
     const size_t in_el = d.dtype == GDR_DTYPE_BF16 ? 2 : 4;
@@ -321,7 +334,7 @@ size_t gdr_fwd_workspace_bytes(const gdr_problem* p) {
 size_t gdr_bwd_workspace_bytes(const gdr_problem* p) {
   Dims d;
   if (resolve(p, &d) != GDR_OK) return 0;
-  if (d.path == 1 && !tc_bwd_available()) d.path = d.save_wy = 0;
+  if (d.path == 1 && !tc_bwd_available()) d.path = d.save_wy = 0, d.cp_fwd = d.cp_bwd = 1;
   return layout_workspace(d, true, nullptr, nullptr);
 }
 
@@ -363,7 +376,7 @@ gdr_status gdr_bwd(const gdr_problem* p, const void* q, const void* k, const voi
   Dims d;
   gdr_status st = resolve(p, &d);
   if (st != GDR_OK) return st;
-  if (d.path == 1 && !tc_bwd_available()) d.path = d.save_wy = 0;
+  if (d.path == 1 && !tc_bwd_available()) d.path = d.save_wy = 0, d.cp_fwd = d.cp_bwd = 1;
   const bool any_tokens = d.T_total > 0;
   if (any_tokens && (!q || !k || !v || !g || !beta || !h_saved || !dO || !dq || !dk || !dv || !dg || !dbeta))
     return GDR_ERR_INVALID_ARG;
@@ -401,6 +414,15 @@ gdr_status gdr_workspace_status(const void* workspace, gdr_stream_t stream, uint
 }
 
 int gdr_debug_last_cuda_error(void) { return g_last_cuda_error.load(std::memory_order_relaxed); }
+
+int gdr_debug_cp_segment(int c0, int c1, int P, int s, int* out3) {
+  if (P < 1 || s < 0 || c1 < c0 || out3 == nullptr) return 1;
+  const int3 r = cp_segment(c0, c1, P, s);
+  out3[0] = r.x;
+  out3[1] = r.y;
+  out3[2] = r.z;
+  return 0;
+}
 
 const char* gdr_debug_cuda_error_string(int e) { return cudaGetErrorString((cudaError_t)e); }
 

@@ -55,4 +55,17 @@ __device__ __forceinline__ int idx_fwd_chunk(const Dims& d, const Workspace& ws,
   return n * idx_nc(d) + s;
 }
 
+// Context-parallel segments: the chunks [c0, c1) of one sequence cut into
+// nseg = max(1, min(P, c1 - c0)) segments whose chunk counts differ by at most one (the first
+// (c1 - c0) mod nseg one longer).  Returns {first chunk, end chunk, nseg} of segment s; a segment
+// s >= nseg is empty.
+__host__ __device__ __forceinline__ int3 cp_segment(int c0, int c1, int P, int s) {
+  const int nc = c1 - c0;
+  const int nseg = max(1, min(P, nc));
+  if (s >= nseg) return make_int3(c1, c1, nseg);
+  const int base = nc / nseg, extra = nc - base * nseg;
+  const int lo = c0 + s * base + min(s, extra);
+  return make_int3(lo, lo + base + (s < extra ? 1 : 0), nseg);
+}
+
 }  // namespace gdr

@@ -34,6 +34,22 @@ struct Dims {
   int h_bf16;  // h_saved holds bf16 (else fp32)
   int prologue;  // gdr_prologue_flags bits
   int save_wy;   // tensor-core path: gamma, W, U, P, T live in the saved buffer (see attach_saved_factors)
+  int cp_fwd, cp_bwd;  // segments per sequence of the context-parallel passes (1: none; tensor-core path)
+};
+
+constexpr int kMaxCpSegments = 64;
+
+// Context-parallel (segment-scan) passes of one direction.  Per (sequence, v-head) and segment s,
+// three DK x 128 fp32 matrices: X[s] a boundary state (forward: the state at the start of segment
+// s; backward: the state gradient at the end of segment s) and R[s] the segment's result from a
+// zero boundary, both row-major [DK][DV]; M[s] the segment's transition (forward Phi_s, backward
+// Phi_s^T), stored transposed (element [r][k] at k * 128 + r).
+struct CpArgs {
+  int pass;  // 0: no segments; 1: the first pass (maps); 3: the second pass (true boundaries)
+  int P;     // segments per sequence
+  float* X;  // [num_seqs][Hv][P][128][128]
+  float* M;
+  float* R;
 };
 
 // Pointers into the caller's workspace.  Every region starts 256-byte aligned.
@@ -78,6 +94,10 @@ struct Workspace {
   void* kn;
   float* gn;
   void* bn;
+  // context-parallel passes (Dims::cp_fwd or cp_bwd > 1): see CpArgs
+  float* cp_X;
+  float* cp_M;
+  float* cp_R;
 };
 
 // GDR_OK for cudaSuccess; otherwise records e for gdr_debug_last_cuda_error and returns
@@ -157,6 +177,11 @@ bool simt_small(const Dims& d);
 bool index_folded(const Dims& d);
 cudaError_t simt_small_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cudaStream_t s);
 cudaError_t simt_small_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cudaStream_t s);
+
+// The context-parallel scan between the two passes (gdr_cp.cu): per (sequence, v-head) the
+// boundary states X of segments 2 .. nseg - 1 (forward, X[s + 1] = M[s] X[s] + R[s] from X[1])
+// or nseg - 3 .. 0 (backward, X[s - 1] = M[s] X[s] + R[s] from X[nseg - 2]), in fp32.
+cudaError_t launch_cp_scan(const Dims& d, const Workspace& ws, int P, bool backward, cudaStream_t s);
 
 // Sums dq_part / dk_part over the v-heads of each q/k head into dq / dk (dtype).
 cudaError_t launch_group_reduce(const Dims& d, void* dq, void* dk, const Workspace& ws, cudaStream_t s);

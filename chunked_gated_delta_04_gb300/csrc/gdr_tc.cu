@@ -604,34 +604,121 @@ __device__ __forceinline__ void st_row_bf16x32_sw64(unsigned char* tile, int row
   for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(tile + row * 64 + ((c ^ sw) << 4)) = w[c];
 }
 
-// One state unit `cta` = (sequence rank, v-head, DV slice), slice fastest.  kFused (fused
+// What one state unit computes: a (sequence, v-head, 32-column DV slice) over a range of its
+// chunks, from a start state to an end state.  Without segments the range is the whole
+// sequence, from S0 to S_T.  The context-parallel passes (CpArgs) cut it into segments:
+//   first pass, per (sequence, v-head): segment 0 from S0 with every output, its end state into
+//     X[1] (or S_T when it is the only segment); and for each segment s = 1 .. nseg - 2 its
+//     zero-start end state R[s] (no outputs) and its transition M[s] = Phi_s (the same
+//     recurrence with U = 0 started from the identity's columns: h' = (e^{gamma_C} I - K~^T W) h);
+//   second pass: segments s = 1 .. nseg - 1 from X[s] with every output, the last into S_T.
+struct StateUnit {
+  int n, j, slice;
+  int c_begin, c_end;  // chunk range
+  int t_seq, L;        // first token of the range, tokens from there to the sequence end
+  const float* h0;     // start state of (n, j) (nullptr: zero) ...
+  int h0_kv;           // ... stored [DK][DV] (else [DV][DK])
+  bool h0_eye;         // start from the identity's columns instead
+  float* h1;           // end state (nullptr: not written), orientation h1_kv
+  int h1_kv;
+  bool outputs;        // o, h_saved and the saved Vn
+  bool zero_u;         // U taken as zero (transition columns)
+  bool skip;           // nothing to compute
+};
+
+__device__ __forceinline__ int state_units_per_chain(const CpArgs& cp) {
+  return cp.pass == 1 ? 4 + 8 * (cp.P - 2) : (cp.pass == 3 ? 4 * (cp.P - 1) : 4);
+}
+
+// Unit `cta` of a state launch: (sequence rank, v-head, unit within the chain), the last fastest.
+__device__ __forceinline__ StateUnit state_unit(const Dims& d, const Workspace& ws, const CpArgs& cp, int cta,
+                                                const float* S0, float* S_T) {
+  StateUnit u{};
+  const int per = state_units_per_chain(cp);
+  const int k = cta % per, rest = cta / per;
+  u.j = rest % d.Hv;
+  u.n = idx_seq(d, ws, rest / d.Hv);
+  int seg = 0, mode = 0;  // mode 0: every output; 1: zero start; 2: transition
+  if (cp.pass == 1 && k >= 4) {
+    const int e = k - 4;
+    seg = 1 + e / 8;
+    u.slice = e & 3;
+    mode = (e & 7) < 4 ? 1 : 2;
+  } else if (cp.pass == 3) {
+    seg = 1 + k / 4;
+    u.slice = k & 3;
+  } else {
+    u.slice = k;
+  }
+  const int s0 = idx_seq_off(d, ws, u.n), s1 = idx_seq_off(d, ws, u.n + 1);
+  const int t_seq = d.cu ? d.cu[u.n] : u.n * d.T;
+  const int L = d.cu ? d.cu[u.n + 1] - t_seq : d.T;
+  const size_t sb = ((size_t)u.n * d.Hv + u.j) * 128 * 128;
+  u.c_begin = s0;
+  u.c_end = s1;
+  u.t_seq = t_seq;
+  u.L = L;
+  u.h0 = S0 ? S0 + sb : nullptr;
+  u.h0_kv = d.layout == 0;
+  u.h1 = S_T ? S_T + sb : nullptr;
+  u.h1_kv = d.layout == 0;
+  u.outputs = true;
+  if (cp.pass == 0) return u;
+  const int3 sg = cp_segment(s0, s1, cp.P, seg);
+  auto mat = [&](float* base, int s2) { return base + (sb * cp.P) + (size_t)s2 * 128 * 128; };
+  u.c_begin = sg.x;
+  u.c_end = sg.y;
+  u.t_seq = t_seq + (sg.x - s0) * kChunk;
+  u.L = L - (sg.x - s0) * kChunk;
+  if (cp.pass == 1) {
+    if (mode == 0) {
+      if (sg.z > 1) {
+        u.h1 = mat(cp.X, 1);
+        u.h1_kv = 1;
+      }
+    } else {
+      u.skip = seg >= sg.z - 1;
+      u.outputs = false;
+      u.h0 = nullptr;
+      u.h0_eye = mode == 2;
+      u.zero_u = mode == 2;
+      u.h1 = mat(mode == 2 ? cp.M : cp.R, seg);
+      u.h1_kv = mode == 2 ? 0 : 1;  // M transposed: the scan reads M^T[k][r] = M[r][k] as rows
+    }
+  } else {
+    u.skip = seg >= sg.z;
+    u.h0 = mat(cp.X, seg);
+    u.h0_kv = 1;
+    if (seg != sg.z - 1) u.h1 = nullptr;
+  }
+  return u;
+}
+
+// One state unit (see StateUnit).  kFused (fused
 // forward kernel, double-buffered): chunk c's W, U, P and gamma are loaded only after the prep
 // role has counted (c, v-head) in ws.fwd_flags; the copy thread waits for chunk c + 1 while
 // chunk c's first product runs, off the chain.
 template <bool kSingle, bool kFused>
 __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_w,
                                            const CUtensorMap& tm_u, const CUtensorMap& tm_p,
-                                           const CUtensorMap& tm_hs, const Dims& d, const float* __restrict__ S0,
-                                           float* __restrict__ S_T, bf16* __restrict__ o, const Workspace& ws,
-                                           int cta, unsigned char* sm) {
+                                           const CUtensorMap& tm_hs, const Dims& d, bf16* __restrict__ o,
+                                           const Workspace& ws, const StateUnit& un, unsigned char* sm) {
   using SS = StateSmem<kSingle>;
   // two stages: bar_load[st] per stage; single buffers: bar_load[0] = [W|Q] and gamma,
   // bar_load[1] = U, bar_kp = K and P (one phase per chunk each)
   __shared__ uint64_t bar_load[2], bar_kp, bar_mma, bar_pv;
   __shared__ uint32_t tmem_slot;
-  // block -> (sequence in longest-first order, v-head, DV slice); the slices of one
-  // (sequence, head) are adjacent so they share its W/Q/K tiles in L2
-  const int slice = cta % kStateSlices, rest = cta / kStateSlices;
-  const int j = rest % d.Hv, n = idx_seq(d, ws, rest / d.Hv), i = j / d.G;
-  const int dv0 = slice * 32;
+  // the slices of one (sequence, head) are adjacent units, so they share its W/Q/K tiles in L2
+  const int j = un.j, i = j / d.G;
+  const int dv0 = un.slice * 32;
   const int tid = threadIdx.x, warp = tid >> 5;
   // thread 0 issues the MMAs; thread 32 (the "copy thread") issues every TMA load and
   // store and waits on their bulk groups, so neither kind of issue delays the other
   constexpr int kCopyTid = 32;
   const int Hv = d.Hv;
-  const int c_begin = idx_seq_off(d, ws, n), c_end = idx_seq_off(d, ws, n + 1);
-  const int t_seq = d.cu ? d.cu[n] : n * d.T;        // first token of the sequence
-  const int L = d.cu ? d.cu[n + 1] - t_seq : d.T;     // its length
+  const int c_begin = un.c_begin, c_end = un.c_end;
+  const int t_seq = un.t_seq;  // first token of the range
+  const int L = un.L;          // tokens from there to the sequence end
 
   if (tid == 0) {
     tc::mbar_init(&bar_load[0], 1);
@@ -651,38 +738,43 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
 
   // h row `tid` (dk = tid), columns dv0 .. dv0 + 31
   float h[32];
-  {
-    const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
 #pragma unroll
-    for (int b = 0; b < 32; ++b)
-      h[b] = S0 ? S0[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] : 0.f;
-  }
+  for (int b = 0; b < 32; ++b)
+    h[b] = un.h0_eye ? (tid == dv0 + b ? 1.f : 0.f)
+           : un.h0   ? un.h0[un.h0_kv ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid]
+                     : 0.f;
   // two stages: every tile of chunk c into stage st, P into its rotating buffer (whose last
   // reader, P Vn of chunk c - 3, completed before chunk c - 2's first product did)
   auto issue_loads = [&](int c, int st) {
     const int tc0 = t_seq + (c - c_begin) * 64;
     const size_t chh = (size_t)c * Hv + j;
     unsigned char* base = sm + st * SS::STAGE;
-    tc::mbar_arrive_expect_tx(&bar_load[st], 8 * kSlab + 256);
+    // Q and P feed only the output rows: units without outputs leave them out (the products
+    // that read those tiles then fill TMEM lanes no one reads)
+    tc::mbar_arrive_expect_tx(&bar_load[st], (un.outputs ? 8 : 5) * kSlab + 256);
     tc::bulk_load(sm + SS::GAM + st * 256, ws.gam + chh * 64, 256, &bar_load[st]);
     tc::tma_load_2d(base + SS::WQ, &tm_w, &bar_load[st], 0, (int)(chh * 64));
     tc::tma_load_2d(base + SS::WQ + 2 * kSlab, &tm_w, &bar_load[st], 64, (int)(chh * 64));
-    tc::tma_load_3d(base + SS::WQ + kSlab, &tm_q, &bar_load[st], 0, i, tc0);
-    tc::tma_load_3d(base + SS::WQ + 3 * kSlab, &tm_q, &bar_load[st], 64, i, tc0);
+    if (un.outputs) {
+      tc::tma_load_3d(base + SS::WQ + kSlab, &tm_q, &bar_load[st], 0, i, tc0);
+      tc::tma_load_3d(base + SS::WQ + 3 * kSlab, &tm_q, &bar_load[st], 64, i, tc0);
+    }
     tc::tma_load_3d(base + SS::K, &tm_k, &bar_load[st], 0, i, tc0);
     tc::tma_load_3d(base + SS::K + kSlab, &tm_k, &bar_load[st], 64, i, tc0);
     tc::tma_load_2d(base + SS::U, &tm_u, &bar_load[st], dv0 & 64, (int)(chh * 64));  // 64-col tile
-    tc::tma_load_2d(sm + SS::pbuf(c - c_begin), &tm_p, &bar_load[st], 0, (int)(chh * 64));
+    if (un.outputs) tc::tma_load_2d(sm + SS::pbuf(c - c_begin), &tm_p, &bar_load[st], 0, (int)(chh * 64));
   };
   auto load_wq = [&](int c) {  // single buffers: [W|Q] and gamma of chunk c
     const int tc0 = t_seq + (c - c_begin) * 64;
     const size_t chh = (size_t)c * Hv + j;
-    tc::mbar_arrive_expect_tx(&bar_load[0], 4 * kSlab + 256);
+    tc::mbar_arrive_expect_tx(&bar_load[0], (un.outputs ? 4 : 2) * kSlab + 256);
     tc::bulk_load(sm + SS::GAM, ws.gam + chh * 64, 256, &bar_load[0]);
     tc::tma_load_2d(sm + SS::WQ, &tm_w, &bar_load[0], 0, (int)(chh * 64));
     tc::tma_load_2d(sm + SS::WQ + 2 * kSlab, &tm_w, &bar_load[0], 64, (int)(chh * 64));
-    tc::tma_load_3d(sm + SS::WQ + kSlab, &tm_q, &bar_load[0], 0, i, tc0);
-    tc::tma_load_3d(sm + SS::WQ + 3 * kSlab, &tm_q, &bar_load[0], 64, i, tc0);
+    if (un.outputs) {
+      tc::tma_load_3d(sm + SS::WQ + kSlab, &tm_q, &bar_load[0], 0, i, tc0);
+      tc::tma_load_3d(sm + SS::WQ + 3 * kSlab, &tm_q, &bar_load[0], 64, i, tc0);
+    }
   };
   auto load_u = [&](int c) {  // single buffers: U of chunk c
     const size_t chh = (size_t)c * Hv + j;
@@ -692,10 +784,10 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
   auto load_kp = [&](int c) {  // single buffers: K and P of chunk c
     const int tc0 = t_seq + (c - c_begin) * 64;
     const size_t chh = (size_t)c * Hv + j;
-    tc::mbar_arrive_expect_tx(&bar_kp, 3 * kSlab);
+    tc::mbar_arrive_expect_tx(&bar_kp, (un.outputs ? 3 : 2) * kSlab);
     tc::tma_load_3d(sm + SS::K, &tm_k, &bar_kp, 0, i, tc0);
     tc::tma_load_3d(sm + SS::K + kSlab, &tm_k, &bar_kp, 64, i, tc0);
-    tc::tma_load_2d(sm + SS::P, &tm_p, &bar_kp, 0, (int)(chh * 64));
+    if (un.outputs) tc::tma_load_2d(sm + SS::P, &tm_p, &bar_kp, 0, (int)(chh * 64));
   };
   // kFused: the prep role's flag of chunk c (bounded wait; on expiry the loads are left out
   // and the consumer's own bounded wait ends the chain).  (Reading the next chunk's flag a
@@ -743,7 +835,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     if (!tc::mbar_wait(&bar_pv, pv_phase, ws.status, kDevErrTimeoutFwd)) return;
     tc::tc_fence_after();
     tmem_ld32w(tbase, warp, 32, y);
-    if (r < p_len) {
+    if (r < p_len && un.outputs) {
 #pragma unroll
       for (int b = 0; b < 32; ++b) y[b] = d.scale * (p_eg * xq[b] + y[b]);
       st_global_bf16x32(o + ((size_t)(p_t0 + r) * Hv + j) * 128 + dv0, y);
@@ -800,8 +892,10 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     mma_phase ^= 1;
     tc::tc_fence_after();
     if (ok && tid == kCopyTid) {  // h_saved[chunk] rows 0..127, columns dv0..dv0+31
-      tc::tma_store_2d(&tm_hs, sm + SS::HS, dv0, (int)(chh * 128));
-      tc::bulk_commit();
+      if (un.outputs) {
+        tc::tma_store_2d(&tm_hs, sm + SS::HS, dv0, (int)(chh * 128));
+        tc::bulk_commit();
+      }
       if (kSingle && c + 1 < c_end) load_wq(c + 1);  // [W|Q] and gamma were last read by [W;Q] h
     }
     GDR_TRACE_MARK(1, 2);
@@ -815,7 +909,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
         tmem_ld32w(tbase, warp, 0, x);
         if (uok) ld_halfrow_bf16(stg + SS::U, r, (dv0 >> 5) & 1, u);
 #pragma unroll
-        for (int b = 0; b < 32; ++b) u[b] = uok ? u[b] - x[b] : 0.f;
+        for (int b = 0; b < 32; ++b) u[b] = uok ? (un.zero_u ? -x[b] : u[b] - x[b]) : 0.f;
         st_col32_bf16(sm + SS::VNT, r, u);
 #pragma unroll
         for (int b = 0; b < 32; ++b) vn_keep[b] = u[b];
@@ -861,7 +955,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     }
     // saved factors: Vn replaces U in the saved buffer (the backward reads Vn; each slice writes
     // only its own columns, which no other CTA reads), off the chain: after the MMA issue
-    if (ok && d.save_wy && warp < 2)
+    if (ok && d.save_wy && warp < 2 && un.outputs)
       st_global_bf16x32(reinterpret_cast<bf16*>(ws.U) + (chh * 64 + r) * 128 + dv0, vn_keep);
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutFwd));
     mma_phase ^= 1;
@@ -883,11 +977,10 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
   tc::tc_fence_after();
   if (ok && warp >= 2 && c_begin < c_end) finish_o((c_end - c_begin - 1) & 1);  // the last chunk's output rows
   if (tid == kCopyTid) tc::bulk_wait_read<0>();  // smem sources read before exit
-  if (ok && S_T) {
-    const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
+  if (ok && un.h1) {
 #pragma unroll
     for (int b = 0; b < 32; ++b)
-      S_T[sb + (d.layout == 0 ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid)] = h[b];
+      un.h1[un.h1_kv ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid] = h[b];
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -899,10 +992,11 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
     const __grid_constant__ CUtensorMap tm_p, const __grid_constant__ CUtensorMap tm_hs, Dims d,
-    const float* __restrict__ S0, float* __restrict__ S_T, bf16* __restrict__ o, Workspace ws) {
+    const float* __restrict__ S0, float* __restrict__ S_T, bf16* __restrict__ o, Workspace ws, CpArgs cp) {
   extern __shared__ unsigned char smem_raw[];
-  state_body<kSingle, false>(tm_q, tm_k, tm_w, tm_u, tm_p, tm_hs, d, S0, S_T, o, ws, (int)blockIdx.x,
-                             align1024(smem_raw));
+  const StateUnit un = state_unit(d, ws, cp, (int)blockIdx.x, S0, S_T);
+  if (un.skip) return;  // uniform over the block, before any barrier or tensor memory
+  state_body<kSingle, false>(tm_q, tm_k, tm_w, tm_u, tm_p, tm_hs, d, o, ws, un, align1024(smem_raw));
 }
 
 // The forward's prep and state recurrence in one cooperative launch (every CTA resident, one
@@ -927,7 +1021,8 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_fused_kernel(
   __syncthreads();
   const int role = s_role;
   if (role >= 0)
-    state_body<false, true>(tm_q, tm_k, tm_w, tm_u, tm_p, tm_hs, d, S0, S_T, o, ws, role, align1024(smem_raw));
+    state_body<false, true>(tm_q, tm_k, tm_w, tm_u, tm_p, tm_hs, d, o, ws,
+                            state_unit(d, ws, CpArgs{}, role, S0, S_T), align1024(smem_raw));
   else
     prep_body<true>(tm_q, tm_k, tm_v, tm_w, tm_u, tm_p, tm_t, d, g, beta, ws, write_T, align1024(smem_raw));
 }
@@ -988,7 +1083,7 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
   // preparing chunks in step order.  (Two CTAs per SM, a state unit beside a prep CTA, would
   // serve more chains, but the occupancy calculation of a cooperative launch admits one CTA per
   // SM for kernels that allocate tensor memory.)  Otherwise the two launches below.
-  if (fused_fwd_possible(d) && n_cta * 2 <= n_sm) {
+  if (fused_fwd_possible(d) && n_cta * 2 <= n_sm && d.cp_fwd <= 1) {
     const size_t smf = std::max<size_t>(PrepSmem::BYTES, StateSmem<false>::BYTES) + 1024;
     auto kern = tc_fwd_fused_kernel;
     set_smem_once((const void*)kern, smf);
@@ -1024,15 +1119,30 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
                                                                       (const bf16*)a.beta, ws, d.save_wy);
     stage_mark(s, "fwd_prep");
   }
-  if (d.num_seqs > 0) {
+  auto state_launch = [&](const CpArgs& cp, long long units, const char* stage) -> cudaError_t {
+    if (units <= 0) return cudaSuccess;
     // more CTAs than SMs: the single-buffered variant, two CTAs per SM, so they all run at once
-    const bool single = n_cta > n_sm;
+    const bool single = units > n_sm;
     const size_t sms = (single ? StateSmem<true>::BYTES : StateSmem<false>::BYTES) + 1024;
     auto kern = single ? tc_fwd_state_kernel<true> : tc_fwd_state_kernel<false>;
     set_smem_once((const void*)kern, sms);
-    kern<<<(unsigned)n_cta, kTcThreads, sms, s>>>(tq, tk, tw, tu, tp, ths, d, a.S0, a.S_T, (bf16*)a.o, ws);
-    stage_mark(s, "fwd_state");
+    kern<<<(unsigned)units, kTcThreads, sms, s>>>(tq, tk, tw, tu, tp, ths, d, a.S0, a.S_T, (bf16*)a.o, ws, cp);
+    stage_mark(s, stage);
+    return cudaGetLastError();
+  };
+  if (d.num_seqs > 0 && d.cp_fwd > 1 && Tt > 0) {
+    // context parallel: segment 0 and every middle segment's maps, the scan of the boundary
+    // states, then segments 1 .. nseg - 1 from their true start states (see StateUnit)
+    const int P = d.cp_fwd;
+    const long long chains = (long long)d.num_seqs * d.Hv;
+    CpArgs cp{1, P, ws.cp_X, ws.cp_M, ws.cp_R};
+    cudaError_t e = state_launch(cp, chains * (4 + 8 * (P - 2)), "fwd_cp_maps");
+    if (e == cudaSuccess && P > 2) e = launch_cp_scan(d, ws, P, false, s);
+    cp.pass = 3;
+    if (e == cudaSuccess) e = state_launch(cp, chains * 4 * (P - 1), "fwd_cp_state");
+    return e;
   }
+  if (d.num_seqs > 0) return state_launch(CpArgs{}, n_cta, "fwd_state");
   return cudaGetLastError();
 }
 

@@ -124,24 +124,111 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
   return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity, status, bit));
 }
 
-// One walk unit; `unit` = sequence rank (longest first) * Hv + v-head.  tb: the caller's 512
-// TMEM columns.  Every thread of the CTA (kWalkThreads) calls it.
+// What one walk unit computes: a (sequence, v-head) walked backward over a range of its
+// chunks, from the state gradient at the range's end to the one at its start.  Without
+// segments the range is the whole sequence, from dS_T to dS0, and every chunk's dh' and dVn go
+// to the workspace.  The context-parallel passes (CpArgs) cut it into segments:
+//   first pass, per (sequence, v-head): the last segment from dS_T with its stores, its start
+//     gradient into X[nseg - 2] (or dS0 when it is the only segment); and for each segment
+//     s = 1 .. nseg - 2 its walk from a zero end gradient R[s] = E_s and its transposed
+//     transition M[s] = Phi_s^T (the walk with dO = 0 from the identity: dh = A_c^T dh'), both
+//     without stores;
+//   second pass: segments s = 0 .. nseg - 2 from X[s] with their stores, segment 0 into dS0.
+struct WalkUnit {
+  int n, j;
+  int c_begin, c_end;  // chunk range
+  int t_seq, L;        // first token of the range, tokens from there to the sequence end
+  const float* g0;     // gradient at the range's end (nullptr: zero) ...
+  int g0_kv;           // ... stored [DK][DV] (else [DV][DK])
+  bool g0_eye;         // the identity instead
+  float* g1;           // gradient at the range's start (nullptr: not written), orientation g1_kv
+  int g1_kv;
+  bool stores;         // dh' and dVn of every chunk to the workspace
+  bool zero_do;        // dO taken as zero (transition columns)
+  bool skip;           // nothing to compute
+};
+
+__device__ __forceinline__ int walk_units_per_chain(const CpArgs& cp) {
+  return cp.pass == 1 ? 1 + 2 * (cp.P - 2) : (cp.pass == 3 ? cp.P - 1 : 1);
+}
+
+// Unit `unit` of a walk launch: (sequence rank, v-head, unit within the chain), the last fastest.
+__device__ __forceinline__ WalkUnit walk_unit(const Dims& d, const Workspace& ws, const CpArgs& cp, int unit,
+                                              const float* dS_T, float* dS0) {
+  WalkUnit u{};
+  const int per = walk_units_per_chain(cp);
+  const int k = unit % per, rest = unit / per;
+  u.j = rest % d.Hv;
+  u.n = idx_seq(d, ws, rest / d.Hv);
+  const int s0 = idx_seq_off(d, ws, u.n), s1 = idx_seq_off(d, ws, u.n + 1);
+  const int t_seq = d.cu ? d.cu[u.n] : u.n * d.T;
+  const int L = d.cu ? d.cu[u.n + 1] - t_seq : d.T;
+  const size_t sb = ((size_t)u.n * d.Hv + u.j) * 128 * 128;
+  u.c_begin = s0;
+  u.c_end = s1;
+  u.t_seq = t_seq;
+  u.L = L;
+  u.g0 = dS_T ? dS_T + sb : nullptr;
+  u.g0_kv = d.layout == 0;
+  u.g1 = dS0 ? dS0 + sb : nullptr;
+  u.g1_kv = d.layout == 0;
+  u.stores = true;
+  if (cp.pass == 0) return u;
+  const int nseg = cp_segment(s0, s1, cp.P, 0).z;
+  int seg, mode = 0;  // mode 0: true walk with stores; 1: zero end gradient; 2: transition
+  if (cp.pass == 1) {
+    seg = k == 0 ? nseg - 1 : 1 + (k - 1) / 2;
+    mode = k == 0 ? 0 : 1 + ((k - 1) & 1);
+  } else {
+    seg = k;
+  }
+  const int3 sg = cp_segment(s0, s1, cp.P, seg);
+  auto mat = [&](float* base, int s2) { return base + (sb * cp.P) + (size_t)s2 * 128 * 128; };
+  u.c_begin = sg.x;
+  u.c_end = sg.y;
+  u.t_seq = t_seq + (sg.x - s0) * kChunk;
+  u.L = L - (sg.x - s0) * kChunk;
+  if (cp.pass == 1) {
+    if (mode == 0) {
+      if (nseg > 1) {
+        u.g1 = mat(cp.X, nseg - 2);
+        u.g1_kv = 1;
+      }
+    } else {
+      u.skip = seg > nseg - 2;
+      u.stores = false;
+      u.g0 = nullptr;
+      u.g0_eye = mode == 2;
+      u.zero_do = mode == 2;
+      u.g1 = mat(mode == 2 ? cp.M : cp.R, seg);
+      u.g1_kv = mode == 2 ? 0 : 1;  // M transposed: the scan reads M^T[k][r] = M[r][k] as rows
+    }
+  } else {
+    u.skip = seg > nseg - 2;
+    u.g0 = mat(cp.X, seg);
+    u.g0_kv = 1;
+    if (seg != 0) u.g1 = nullptr;
+  }
+  return u;
+}
+
+// One walk unit (see WalkUnit).  tb: the caller's 512 TMEM columns.  Every thread of the CTA
+// (kWalkThreads) calls it.
 template <bool kPublish>
 __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_w,
                                           const CUtensorMap& tm_p, const CUtensorMap& tm_do,
                                           const CUtensorMap& tm_dhs, const CUtensorMap& tm_dvs, const Dims& d,
-                                          const float* __restrict__ dS_T, float* __restrict__ dS0,
-                                          const Workspace& ws, int unit, uint32_t tb, unsigned char* sm) {
+                                          const Workspace& ws, const WalkUnit& un, uint32_t tb, unsigned char* sm) {
   using WS = WalkSmem;
   __shared__ uint64_t bar_load[2], bar_scaled[2], bar_vfull[2], bar_hfull[2], bar_dvn[2], bar_dvnfree[2];
   __shared__ uint64_t bar_dh, bar_dhfree, bar_drain;
-  const int n = idx_seq(d, ws, unit / d.Hv), j = unit % d.Hv, i = j / d.G;
+  const int j = un.j, i = j / d.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Hv = d.Hv;
-  const int c_begin = idx_seq_off(d, ws, n), c_end = idx_seq_off(d, ws, n + 1);
+  const int c_begin = un.c_begin, c_end = un.c_end;
   const int nch = c_end - c_begin;
-  const int t_seq = d.cu ? d.cu[n] : n * d.T;
-  const int L = d.cu ? d.cu[n + 1] - t_seq : d.T;
+  const int t_seq = un.t_seq;
+  const int L = un.L;
   uint32_t* const status = ws.status;
   constexpr uint32_t kBit = kDevErrTimeoutBwd;
   // walk step it = 0, 1, ... is chunk c_end - 1 - it (stage it & 1); its first token, length
@@ -176,15 +263,20 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       unsigned char* base = sm + st * WS::STAGE;
       uint64_t* bar = &bar_load[st];
       GDR_DELAY(14);
-      tc::mbar_arrive_expect_tx(bar, 9 * kSlab + 256);
+      // Q, dO and P feed only the dO products: the transition walk (dO = 0) leaves them out
+      // (the scaling of Q's rows and the skipped products then touch stale tiles no one reads)
+      const bool dO_tiles = !un.zero_do;
+      tc::mbar_arrive_expect_tx(bar, (dO_tiles ? 9 : 4) * kSlab + 256);
       tc::bulk_load(base + WS::GAM, ws.gam + chh * 64, 256, bar);
       tc::tma_load_3d(base + WS::KQ, &tm_k, bar, 0, i, tc0);
       tc::tma_load_3d(base + WS::KQ + 2 * kSlab, &tm_k, bar, 64, i, tc0);
-      tc::tma_load_3d(base + WS::KQ + kSlab, &tm_q, bar, 0, i, tc0);
-      tc::tma_load_3d(base + WS::KQ + 3 * kSlab, &tm_q, bar, 64, i, tc0);
-      tc::tma_load_3d(base + WS::DO, &tm_do, bar, 0, j, tc0);
-      tc::tma_load_3d(base + WS::DO + kSlab, &tm_do, bar, 64, j, tc0);
-      tc::tma_load_2d(base + WS::P, &tm_p, bar, 0, (int)(chh * 64));
+      if (dO_tiles) {
+        tc::tma_load_3d(base + WS::KQ + kSlab, &tm_q, bar, 0, i, tc0);
+        tc::tma_load_3d(base + WS::KQ + 3 * kSlab, &tm_q, bar, 64, i, tc0);
+        tc::tma_load_3d(base + WS::DO, &tm_do, bar, 0, j, tc0);
+        tc::tma_load_3d(base + WS::DO + kSlab, &tm_do, bar, 64, j, tc0);
+        tc::tma_load_2d(base + WS::P, &tm_p, bar, 0, (int)(chh * 64));
+      }
       tc::tma_load_2d(base + WS::W, &tm_w, bar, 0, (int)(chh * 64));
       tc::tma_load_2d(base + WS::W + kSlab, &tm_w, bar, 64, (int)(chh * 64));
     };
@@ -194,11 +286,13 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       tc::bulk_prefetch_l2(ws.gam + chh * 64, 256);
       tc::tma_prefetch_l2_3d(&tm_k, 0, i, tc0);
       tc::tma_prefetch_l2_3d(&tm_k, 64, i, tc0);
-      tc::tma_prefetch_l2_3d(&tm_q, 0, i, tc0);
-      tc::tma_prefetch_l2_3d(&tm_q, 64, i, tc0);
-      tc::tma_prefetch_l2_3d(&tm_do, 0, j, tc0);
-      tc::tma_prefetch_l2_3d(&tm_do, 64, j, tc0);
-      tc::tma_prefetch_l2_2d(&tm_p, 0, (int)(chh * 64));
+      if (!un.zero_do) {
+        tc::tma_prefetch_l2_3d(&tm_q, 0, i, tc0);
+        tc::tma_prefetch_l2_3d(&tm_q, 64, i, tc0);
+        tc::tma_prefetch_l2_3d(&tm_do, 0, j, tc0);
+        tc::tma_prefetch_l2_3d(&tm_do, 64, j, tc0);
+        tc::tma_prefetch_l2_2d(&tm_p, 0, (int)(chh * 64));
+      }
       tc::tma_prefetch_l2_2d(&tm_w, 0, (int)(chh * 64));
       tc::tma_prefetch_l2_2d(&tm_w, 64, (int)(chh * 64));
     };
@@ -237,11 +331,13 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       unsigned char* stg = sm + st * WS::STAGE;
       if (!tc::mbar_wait(&bar_load[st], ph, status, kBit)) return false;
       tc::tc_fence_after();
-      tc::gemm(accV0 + 128 * st, tc::mnmaj(stg + WS::P, kSlab), tc::mnmaj(stg + WS::DO, kSlab), 128, 4, false);
+      if (!un.zero_do)
+        tc::gemm(accV0 + 128 * st, tc::mnmaj(stg + WS::P, kSlab), tc::mnmaj(stg + WS::DO, kSlab), 128, 4, false);
       if (!tc::mbar_wait(&bar_scaled[st], ph, status, kBit)) return false;
       tc::tc_fence_after();
-      tc::gemm(accH0 + 128 * st, tc::mnmaj(stg + WS::KQ + kSlab, 2 * kSlab), tc::mnmaj(stg + WS::DO, kSlab), 128, 4,
-               false);
+      if (!un.zero_do)
+        tc::gemm(accH0 + 128 * st, tc::mnmaj(stg + WS::KQ + kSlab, 2 * kSlab), tc::mnmaj(stg + WS::DO, kSlab), 128,
+                 4, false);
       return true;
     };
     bool ok = true;
@@ -258,7 +354,8 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       tc::tc_fence_after();
       GDR_DELAY(13);
       GDR_TRACE_CLK(tw1);
-      tc::gemm(accV0 + 128 * st, tc::kmaj(stg + WS::KQ, 2 * kSlab), tc::mnmaj(sm + WS::DH, 16384), 128, 8, true);
+      tc::gemm(accV0 + 128 * st, tc::kmaj(stg + WS::KQ, 2 * kSlab), tc::mnmaj(sm + WS::DH, 16384), 128, 8,
+               !un.zero_do);
       tc::mma_commit(&bar_vfull[st]);
       GDR_TRACE_SINCE(3, 11, tw1);
       GDR_TRACE_CLK(tw2);
@@ -268,7 +365,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       tc::tc_fence_after();
       GDR_TRACE_CLK(tw3);
       tc::gemm(accH0 + 128 * st, tc::mnmaj(stg + WS::W, kSlab), tc::mnmaj(sm + WS::DVN + st * 16384, kSlab), 128,
-               4, true, true);
+               4, !un.zero_do, true);
       tc::mma_commit(&bar_hfull[st]);
       GDR_TRACE_SINCE(3, 13, tw3);
       // the next chunk's dh'-free products
@@ -290,17 +387,21 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       if (!tc::mbar_wait(&bar_dh, it & 1, status, kBit)) break;
       GDR_TRACE_SINCE(3, 20, tc0_);
       GDR_DELAY(10);
-      tc::tma_store_2d(&tm_dhs, sm + WS::DH, 0, (int)(chh * 128));
-      tc::tma_store_2d(&tm_dhs, sm + WS::DH + 16384, 64, (int)(chh * 128));
-      tc::bulk_commit();
-      tc::bulk_wait_read<0>();  // the dh' tile has been read: the next dh' may replace it
+      if (un.stores) {
+        tc::tma_store_2d(&tm_dhs, sm + WS::DH, 0, (int)(chh * 128));
+        tc::tma_store_2d(&tm_dhs, sm + WS::DH + 16384, 64, (int)(chh * 128));
+        tc::bulk_commit();
+        tc::bulk_wait_read<0>();  // the dh' tile has been read: the next dh' may replace it
+      }
       tc::mbar_arrive(&bar_dhfree);
       if (!tc::mbar_wait(&bar_dvn[st], ph, status, kBit)) break;
-      unsigned char* dvn = sm + WS::DVN + st * 16384;
-      tc::tma_store_2d(&tm_dvs, dvn, 0, (int)(chh * 64));
-      tc::tma_store_2d(&tm_dvs, dvn + kSlab, 64, (int)(chh * 64));
-      tc::bulk_commit();
-      tc::bulk_wait_read<0>();
+      if (un.stores) {
+        unsigned char* dvn = sm + WS::DVN + st * 16384;
+        tc::tma_store_2d(&tm_dvs, dvn, 0, (int)(chh * 64));
+        tc::tma_store_2d(&tm_dvs, dvn + kSlab, 64, (int)(chh * 64));
+        tc::bulk_commit();
+        tc::bulk_wait_read<0>();
+      }
       tc::mbar_arrive(&bar_dvnfree[st]);
       GDR_TRACE_CLK(tc1_);
       if (kPublish && pub >= 0) {  // the previous step's two groups have landed
@@ -347,13 +448,11 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       return true;
     };
     float dh[64];
-    {
-      const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
 #pragma unroll
-      for (int b = 0; b < 64; ++b)
-        dh[b] = dS_T ? dS_T[sb + (d.layout == 0 ? (size_t)ln * 128 + 64 * hf + b : (size_t)(64 * hf + b) * 128 + ln)]
-                     : 0.f;
-    }
+    for (int b = 0; b < 64; ++b)
+      dh[b] = un.g0_eye ? (ln == 64 * hf + b ? 1.f : 0.f)
+              : un.g0   ? un.g0[un.g0_kv ? (size_t)ln * 128 + 64 * hf + b : (size_t)(64 * hf + b) * 128 + ln]
+                        : 0.f;
     auto stage_dh = [&]() {  // dh' of the next step as the MMA's bf16 operand
       st_row_bf16(sm + WS::DH + hf * 16384, ln, dh);
       tc::fence_proxy_async_smem();
@@ -432,11 +531,10 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       }
       GDR_TRACE_MARK(3, 6);
     }
-    if (ok && dS0) {
-      const size_t sb = ((size_t)n * Hv + j) * 128 * 128;
+    if (ok && un.g1) {
 #pragma unroll
       for (int b = 0; b < 64; ++b)
-        dS0[sb + (d.layout == 0 ? (size_t)ln * 128 + 64 * hf + b : (size_t)(64 * hf + b) * 128 + ln)] = dh[b];
+        un.g1[un.g1_kv ? (size_t)ln * 128 + 64 * hf + b : (size_t)(64 * hf + b) * 128 + ln] = dh[b];
     }
   }
   tc::tc_fence_before();
@@ -465,15 +563,17 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tc_bwd_walk_kernel(
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
     const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dhs,
     const __grid_constant__ CUtensorMap tm_dvs, Dims d, const float* __restrict__ dS_T, float* __restrict__ dS0,
-    Workspace ws) {
+    Workspace ws, CpArgs cp) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
+  const WalkUnit un = walk_unit(d, ws, cp, (int)blockIdx.x, dS_T, dS0);
+  if (un.skip) return;  // uniform over the block, before any barrier or tensor memory
   __shared__ uint32_t tmem_slot;
   if (threadIdx.x < 32) tc::tmem_alloc<kWalkTmemCols>(&tmem_slot);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  walk_body<false>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvs, d, dS_T, dS0, ws, (int)blockIdx.x, tmem_slot, sm);
+  walk_body<false>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvs, d, ws, un, tmem_slot, sm);
   if (threadIdx.x < 32) tc::tmem_dealloc(tmem_slot, kWalkTmemCols);
 }
 
@@ -1325,7 +1425,8 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tc_bwd_walkgrad_kernel(
   const int n_units = d.num_seqs * d.Hv;
   if (threadIdx.x == 0) GDR_TRACE_INFO_SET(0, GDR_TRACE_NOW());
   for (int u = (int)blockIdx.x; u < n_units; u += (int)gridDim.x)
-    walk_body<true>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvn, d, dS_T, dS0, ws, u, tmem_slot, sm);
+    walk_body<true>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvn, d, ws, walk_unit(d, ws, CpArgs{}, u, dS_T, dS0),
+                    tmem_slot, sm);
   if (threadIdx.x == 0) GDR_TRACE_INFO_SET(1, GDR_TRACE_NOW());
   if (threadIdx.x >= kGradThreads) {  // the walk's single-thread roles: registers to the gradients
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kIdleRegs) : "memory");
@@ -1399,7 +1500,7 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
   // build that allocated another count runs the walk and the gradients as two launches
   cudaFuncAttributes fa{};
   const bool regs_ok = cudaFuncGetAttributes(&fa, (const void*)kern) == cudaSuccess && fa.numRegs == (int)kWalkRegs;
-  if (fused_walk_grad(d) && regs_ok) {  // walk and gradients in one cooperative kernel
+  if (fused_walk_grad(d) && regs_ok && d.cp_bwd <= 1) {  // walk and gradients in one cooperative kernel
     int per_sm = 0;
     const size_t smg = std::max(GradSmem::BYTES, WalkSmem::BYTES) + 1024;
     set_smem_once((const void*)kern, smg);
@@ -1425,12 +1526,29 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     }
     return cudaGetLastError();
   }
-  if (d.num_seqs > 0) {
+  auto walk_launch = [&](const CpArgs& cp, long long units, const char* stage) -> cudaError_t {
+    if (units <= 0) return cudaSuccess;
     const size_t sm = WalkSmem::BYTES + 1024;
     set_smem_once((const void*)tc_bwd_walk_kernel, sm);
-    tc_bwd_walk_kernel<<<d.num_seqs * d.Hv, kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, dd, a.dS_T,
-                                                                  a.dS0, ws);
-    stage_mark(s, "bwd_walk");
+    tc_bwd_walk_kernel<<<(unsigned)units, kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, dd, a.dS_T, a.dS0,
+                                                                ws, cp);
+    stage_mark(s, stage);
+    return cudaGetLastError();
+  };
+  if (d.num_seqs > 0 && d.cp_bwd > 1 && Tt > 0) {
+    // context parallel: the last segment's walk and every middle segment's maps, the scan of the
+    // boundary gradients, then segments 0 .. nseg - 2 from their true end gradients (WalkUnit)
+    const int P = d.cp_bwd;
+    const long long chains = (long long)d.num_seqs * d.Hv;
+    CpArgs cp{1, P, ws.cp_X, ws.cp_M, ws.cp_R};
+    e = walk_launch(cp, chains * (1 + 2 * (P - 2)), "bwd_cp_maps");
+    if (e == cudaSuccess && P > 2) e = launch_cp_scan(d, ws, P, true, s);
+    cp.pass = 3;
+    if (e == cudaSuccess) e = walk_launch(cp, chains * (P - 1), "bwd_cp_walk");
+    if (e != cudaSuccess) return e;
+  } else if (d.num_seqs > 0) {
+    e = walk_launch(CpArgs{}, (long long)d.num_seqs * d.Hv, "bwd_walk");
+    if (e != cudaSuccess) return e;
   }
   if (d.max_chunks > 0 && Tt > 0) {
     const long long n_items = (long long)d.max_chunks * d.Hv;

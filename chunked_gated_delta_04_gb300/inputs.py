@@ -63,6 +63,10 @@ WORKLOADS = {
     "long_t16384": Workload("long_t16384", torch.bfloat16, 1, 16384, 16, 16, 128, 128, "VK", True, True,
                             g_shift=2.0),
     "gva_b2_t4096": Workload("gva_b2_t4096", torch.bfloat16, 2, 4096, 16, 32, 128, 128, "KV", False, False),
+    # the long-sequence workload with 2 heads (8 chunk chains at 4 DV slices): the case intra-card
+    # context parallelism is for, where the plain chains leave most SMs idle
+    "long_h2_t65536": Workload("long_h2_t65536", torch.bfloat16, 1, 65536, 2, 2, 128, 128, "VK", True, True,
+                               g_shift=2.0),
 }
 
 

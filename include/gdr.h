@@ -108,6 +108,21 @@ typedef struct {
                                 results (bit for bit on the tensor-core path); honoured on
                                 the tensor-core path and on the SIMT path for DK, DV <= 64,
                                 ignored (nothing saved) for larger SIMT heads. */
+  int cp_fwd, cp_bwd;        /* intra-card context parallelism (FlashQLA PR #34, "Current
+                                status"), per direction: 0 or 1 = off; P in 2..64 = every
+                                sequence is cut at chunk boundaries into min(P, its chunk
+                                count) segments of nearly equal chunk counts (the first ones
+                                one longer), which run side by side: a first pass finds
+                                each segment's end state from a zero start and its state
+                                transition (the same recurrence on the identity with the
+                                values set to zero), a short scan gives every segment its
+                                true start state, and a second pass evaluates the segments
+                                from those (the backward mirrors this with the state
+                                gradient).  Same results up to rounding (the transitions
+                                and the scan replace part of the chain's bf16 products).
+                                It pays when few (sequence, v-head) chains leave most SMs
+                                idle.  Honoured on the tensor-core path, ignored on the
+                                SIMT path.  Zero-initialised structs keep it off. */
 } gdr_problem;
 
 /* Upper bound on the number of 64-token chunks: B * ceil(T/64) for fixed length,

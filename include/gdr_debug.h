@@ -52,6 +52,13 @@ int gdr_debug_tc_gemm(const void* A, const void* B, float* D, int N, int K, int 
 int gdr_debug_timeout_selftest(unsigned int* status, unsigned long long limit_ns,
                                unsigned long long* waited_ns, void* stream);
 
+/* The context-parallel split of gdr_problem.cp_fwd / cp_bwd: the chunks [c0, c1) of one
+ * sequence cut into nseg = max(1, min(P, c1 - c0)) segments whose chunk counts differ by at
+ * most one, the longer ones first.  Writes {first chunk, end chunk, nseg} of segment s into
+ * out3 (a segment s >= nseg is empty: {c1, c1, nseg}).  Host only; returns 0, or non-zero for
+ * P < 1, s < 0, c1 < c0 or a null out3. */
+int gdr_debug_cp_segment(int c0, int c1, int P, int s, int* out3);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,17 +24,18 @@ def to_device(inp: dict, dev="cuda") -> dict:
 
 
 def run_gpu(inp: dict, backward: bool = True, stream=None, h_dtype=torch.float32, prologue=0,
-            save_wy=False) -> dict:
-    """Run gdr_fwd (+ gdr_bwd) on device copies of ``inp``; returns device tensors."""
+            save_wy=False, cp_fwd=1, cp_bwd=1) -> dict:
+    """Run gdr_fwd (+ gdr_bwd) on device copies of ``inp``; returns device tensors.  cp_fwd, cp_bwd:
+    context-parallel segments per sequence of each direction (1: off)."""
     d = to_device(inp)
     layout = inp["layout"]
     o, S_T, h_saved = gdr.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["S0"], d["cu_seqlens"], layout,
-                                  stream=stream, h_dtype=h_dtype, prologue=prologue, save_wy=save_wy)
+                                  stream=stream, h_dtype=h_dtype, prologue=prologue, save_wy=save_wy, cp=cp_fwd)
     res = {"o": o, "S_T": S_T, "h_saved": h_saved}
     if backward:
         dq, dk, dv, dg, dbeta, dS0 = gdr.backward(d["q"], d["k"], d["v"], d["g"], d["beta"], h_saved, d["dO"],
                                                   d["dS_T"], d["cu_seqlens"], layout, stream=stream,
-                                                  prologue=prologue, save_wy=save_wy)
+                                                  prologue=prologue, save_wy=save_wy, cp=cp_bwd)
         res.update(dq=dq, dk=dk, dv=dv, dg=dg, dbeta=dbeta, dS0=dS0)
     return res
 

@@ -89,6 +89,8 @@ def test_size_queries(lib):
     (dict(h_dtype=torch.float16), gdr.GDR_ERR_INVALID_ARG),  # h_saved is fp32 or bf16
     (dict(prologue=8), gdr.GDR_ERR_INVALID_ARG),              # unknown prologue bit
     (dict(save_wy=2), gdr.GDR_ERR_INVALID_ARG),               # save_wy is 0 or 1
+    (dict(cp_fwd=-1), gdr.GDR_ERR_INVALID_ARG),               # context-parallel segments: 0 .. 64
+    (dict(cp_bwd=65), gdr.GDR_ERR_INVALID_ARG),
     # 2^30 token-heads but 2^24 chunk-heads: the saved states' 128-row blocks would pass 2^31
     (dict(T=1 << 27), gdr.GDR_ERR_UNSUPPORTED),
 ])
@@ -99,6 +101,46 @@ def test_bad_problems_are_rejected(lib, kw, code):
                      stream=0)
     assert st == code
     assert gdr.gdr_max_chunks(p) == 0
+
+
+def test_context_parallel_workspace(lib):
+    # off (0 or 1) costs nothing; P segments add three [num_seqs][Hv][P][128][128] fp32 matrices
+    # per direction on the tensor-core path (the SIMT path ignores the setting)
+    p = prob(DK=128, DV=128)
+    for cp in (0, 1):
+        assert gdr.gdr_fwd_workspace_bytes(prob(DK=128, DV=128, cp_fwd=cp)) == gdr.gdr_fwd_workspace_bytes(p)
+    pf, pb = prob(DK=128, DV=128, cp_fwd=4), prob(DK=128, DV=128, cp_bwd=3)
+    mats = 2 * 4 * 128 * 128 * 4
+    if gdr.gdr_path(p) == 1:
+        assert gdr.gdr_fwd_workspace_bytes(pf) == gdr.gdr_fwd_workspace_bytes(p) + 3 * 4 * mats
+        assert gdr.gdr_bwd_workspace_bytes(pf) == gdr.gdr_bwd_workspace_bytes(p)
+        assert gdr.gdr_bwd_workspace_bytes(pb) == gdr.gdr_bwd_workspace_bytes(p) + 3 * 3 * mats
+    else:
+        assert gdr.gdr_fwd_workspace_bytes(pf) == gdr.gdr_fwd_workspace_bytes(p)
+        assert gdr.gdr_bwd_workspace_bytes(pb) == gdr.gdr_bwd_workspace_bytes(p)
+    assert gdr.gdr_fwd_workspace_bytes(prob(cp_fwd=8)) == gdr.gdr_fwd_workspace_bytes(prob())  # SIMT shape
+
+
+def test_context_parallel_split_matches_the_oracle(lib):
+    """The library's segment split is the oracle's (sizes within one, the longer ones first,
+    clamped to the chunk count, one empty segment for an empty sequence)."""
+    from oracle.context_parallel import split_chunks
+    for nc in [0, 1, 2, 7, 14, 64, 1024, 1031]:
+        for P in [1, 2, 3, 4, 5, 8, 14, 16, 64]:
+            want = split_chunks(nc, P)
+            c0 = 5  # a sequence whose first chunk is global chunk 5
+            got = []
+            nseg = gdr.gdr_debug_cp_segment(c0, c0 + nc, P, 0)[2]
+            assert nseg == max(1, min(P, nc))
+            for s in range(nseg):
+                lo, hi, n2 = gdr.gdr_debug_cp_segment(c0, c0 + nc, P, s)
+                assert n2 == nseg
+                if hi > lo:
+                    got.append((lo - c0, hi - c0))
+            assert got == want, (nc, P, got, want)
+            assert gdr.gdr_debug_cp_segment(c0, c0 + nc, P, nseg) == (c0 + nc, c0 + nc, nseg)
+    with pytest.raises(ValueError):
+        gdr.gdr_debug_cp_segment(0, 10, 0, 0)
 
 
 def test_largest_accepted_chunk_count(lib):

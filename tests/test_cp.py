@@ -1,0 +1,70 @@
+"""GPU parity of intra-card context parallelism (FlashQLA PR #34, "Current status": intra-card CP,
+with forward and backward segment counts set independently).
+
+Each sequence is cut into segments at chunk boundaries; the first pass computes segment maps, a
+scan chains the boundary states, and the second pass evaluates every segment from its true
+boundary.  The results are the operator's own, so every case is compared with the fp64 oracle
+(the plain recurrence) at the usual bars, over segment counts from 2 to more than a sequence's
+chunk count, ragged tails, empty and one-token sequences, grouped v-heads (pair and partial
+sums), both state layouts, bf16 saved states, saved chunk factors and slow decay.
+"""
+import pytest
+import torch
+
+from chunked_gated_delta_04_gb300.inputs import make_inputs, small_workload
+from gdr_testlib import compare, reference, run_gpu, tol_for
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # name, workload kwargs, run kwargs
+    ("t841_p2", dict(B=1, T=841, Hk=2, Hv=2), dict(cp_fwd=2, cp_bwd=2)),
+    ("t841_p3_p4", dict(B=1, T=841, Hk=2, Hv=2), dict(cp_fwd=3, cp_bwd=4)),
+    ("t841_p5_p3_saved", dict(B=1, T=841, Hk=2, Hv=2), dict(cp_fwd=5, cp_bwd=3, save_wy=True)),
+    # one segment per chunk, and more segments than chunks (clamped to the chunk count)
+    ("t841_p14", dict(B=1, T=841, Hk=1, Hv=1), dict(cp_fwd=14, cp_bwd=14)),
+    ("t841_p20", dict(B=1, T=841, Hk=1, Hv=1), dict(cp_fwd=20, cp_bwd=20)),
+    ("b2_vk_pair", dict(B=2, T=500, Hk=1, Hv=2, layout="VK"), dict(cp_fwd=4, cp_bwd=4)),
+    ("gva4_nostates", dict(B=1, T=700, Hk=1, Hv=4, with_S0=False, with_dST=False), dict(cp_fwd=3, cp_bwd=3)),
+    ("varlen", dict(Hk=1, Hv=2, seqlens=[0, 1, 64, 77, 200, 900]), dict(cp_fwd=4, cp_bwd=6)),
+    ("h_bf16_saved", dict(B=1, T=1000, Hk=1, Hv=2), dict(cp_fwd=4, cp_bwd=4, save_wy=True,
+                                                         h_dtype=torch.bfloat16)),
+    ("fwd_only_cp", dict(B=1, T=600, Hk=1, Hv=1), dict(cp_fwd=4, cp_bwd=1)),
+    ("bwd_only_cp", dict(B=1, T=600, Hk=1, Hv=1), dict(cp_fwd=1, cp_bwd=4)),
+    # slow decay (g = logsigmoid(N(2, 1)), the long-sequence workload's gates): the transitions
+    # barely contract, so errors in them are not damped along the scan
+    ("slow_decay_t4096_p8", dict(B=1, T=4096, Hk=1, Hv=1, layout="VK", g_shift=2.0), dict(cp_fwd=8, cp_bwd=8)),
+]
+
+
+@pytest.mark.parametrize("name,wkw,rkw", CASES, ids=[c[0] for c in CASES])
+def test_cp_matches_oracle(name, wkw, rkw):
+    w = small_workload("cp_" + name, torch.bfloat16, DK=128, DV=128, **wkw)
+    inp = make_inputs(w)
+    res = run_gpu(inp, **rkw)
+    torch.cuda.synchronize()
+    compare(res, reference(inp), tol_for(w.dtype))
+
+
+def test_cp_is_deterministic():
+    """No float atomics and fixed summation orders: two runs agree bit for bit."""
+    w = small_workload("cp_det", torch.bfloat16, B=1, T=1500, Hk=2, Hv=2, DK=128, DV=128)
+    inp = make_inputs(w)
+    r0 = run_gpu(inp, cp_fwd=5, cp_bwd=5)
+    r1 = run_gpu(inp, cp_fwd=5, cp_bwd=5)
+    for key, val in r0.items():
+        if val is not None:
+            assert torch.equal(val, r1[key]), key
+
+
+def test_cp_close_to_single_chain():
+    """Segmenting changes only rounding: the results stay within the bf16 bar of the plain chain's."""
+    w = small_workload("cp_vs_chain", torch.bfloat16, B=1, T=2000, Hk=1, Hv=2, DK=128, DV=128)
+    inp = make_inputs(w)
+    base = run_gpu(inp)
+    cp = run_gpu(inp, cp_fwd=6, cp_bwd=6)
+    for key, val in base.items():
+        if val is None:
+            continue
+        a, b = val.float(), cp[key].float()
+        assert (a - b).abs().max().item() <= 2e-2 * a.abs().max().item(), key

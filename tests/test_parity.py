@@ -85,10 +85,13 @@ NAMED = [("tiny_fp32", None, "simt", {}),
          ("b2_t4096", [0, 15], "saved, h bf16", {"save_wy": True, "h_dtype": torch.bfloat16}),
          ("varlen8", [3], "recompute", {}),
          ("varlen8", [3], "saved", {"save_wy": True}),
+         ("varlen8", [3], "recompute, cp 3/5", {"cp_fwd": 3, "cp_bwd": 5}),
          ("long_t65536", [7], "recompute", {}),
          ("long_t65536", [7], "saved", {"save_wy": True}),
+         ("long_t65536", [7], "saved, cp 8/8", {"save_wy": True, "cp_fwd": 8, "cp_bwd": 8}),
          ("gva_b4_t8192", [0], "recompute", {}),
-         ("gva_b4_t8192", [0], "saved", {"save_wy": True})]
+         ("gva_b4_t8192", [0], "saved", {"save_wy": True}),
+         ("gva_b4_t8192", [0], "saved, cp 4/4", {"save_wy": True, "cp_fwd": 4, "cp_bwd": 4})]
 _REF_CACHE = {}
 
 
