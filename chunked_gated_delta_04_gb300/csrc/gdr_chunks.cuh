@@ -68,4 +68,26 @@ __host__ __device__ __forceinline__ int3 cp_segment(int c0, int c1, int P, int s
   return make_int3(lo, lo + base + (s < extra ? 1 : 0), nseg);
 }
 
+// The fused backward with context-parallel segments (fixed length, cp_bwd > 1; a separate
+// instantiation of the kernel, so the plain one carries none of this): queue position q in the
+// order the chunks' state gradients become available.  First every chunk of each
+// sequence's last segment (walked by the first pass, before the fused kernel), walk order; then
+// step t of the second pass's walks: chunk end(s) - 1 - t of segments s = 0 .. nseg - 2 of every
+// sequence (sequence fastest), the longer segments (s < extra) taking one step more.
+__device__ __forceinline__ int idx_cp_grad_chunk(const Dims& d, int q) {
+  const int nc = idx_nc(d), B = d.num_seqs;
+  const int nseg = max(1, min(d.cp_bwd, nc)), base = nc / nseg, extra = nc - base * nseg;
+  const int last_len = nseg == 1 ? nc : base;  // the last segment is never one of the longer ones
+  if (q < B * last_len) {
+    const int t = q / B, n = q - t * B;
+    return (n + 1) * nc - 1 - t;
+  }
+  q -= B * last_len;
+  const int K = B * (nseg - 1);  // chunks per step while every earlier segment has one
+  const int t = q < base * K ? q / K : base;
+  const int r = q - t * K;
+  const int n = r % B, s = r / B;
+  return n * nc + (s + 1) * base + min(s + 1, extra) - 1 - t;
+}
+
 }  // namespace gdr

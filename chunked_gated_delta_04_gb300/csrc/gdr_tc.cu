@@ -698,7 +698,7 @@ __device__ __forceinline__ StateUnit state_unit(const Dims& d, const Workspace& 
 // forward kernel, double-buffered): chunk c's W, U, P and gamma are loaded only after the prep
 // role has counted (c, v-head) in ws.fwd_flags; the copy thread waits for chunk c + 1 while
 // chunk c's first product runs, off the chain.
-template <bool kSingle, bool kFused>
+template <bool kSingle, bool kFused, bool kModes>
 __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_w,
                                            const CUtensorMap& tm_u, const CUtensorMap& tm_p,
                                            const CUtensorMap& tm_hs, const Dims& d, bf16* __restrict__ o,
@@ -719,6 +719,9 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
   const int c_begin = un.c_begin, c_end = un.c_end;
   const int t_seq = un.t_seq;  // first token of the range
   const int L = un.L;          // tokens from there to the sequence end
+  // kModes: the unit may be a first-pass map (no outputs, or U = 0 from the identity); without
+  // it those cases are compiled out (as the plain chain and the second pass run)
+  const bool outputs = !kModes || un.outputs, zero_u = kModes && un.zero_u, h0_eye = kModes && un.h0_eye;
 
   if (tid == 0) {
     tc::mbar_init(&bar_load[0], 1);
@@ -740,7 +743,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
   float h[32];
 #pragma unroll
   for (int b = 0; b < 32; ++b)
-    h[b] = un.h0_eye ? (tid == dv0 + b ? 1.f : 0.f)
+    h[b] = h0_eye ? (tid == dv0 + b ? 1.f : 0.f)
            : un.h0   ? un.h0[un.h0_kv ? (size_t)tid * 128 + dv0 + b : (size_t)(dv0 + b) * 128 + tid]
                      : 0.f;
   // two stages: every tile of chunk c into stage st, P into its rotating buffer (whose last
@@ -751,27 +754,27 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     unsigned char* base = sm + st * SS::STAGE;
     // Q and P feed only the output rows: units without outputs leave them out (the products
     // that read those tiles then fill TMEM lanes no one reads)
-    tc::mbar_arrive_expect_tx(&bar_load[st], (un.outputs ? 8 : 5) * kSlab + 256);
+    tc::mbar_arrive_expect_tx(&bar_load[st], (outputs ? 8 : 5) * kSlab + 256);
     tc::bulk_load(sm + SS::GAM + st * 256, ws.gam + chh * 64, 256, &bar_load[st]);
     tc::tma_load_2d(base + SS::WQ, &tm_w, &bar_load[st], 0, (int)(chh * 64));
     tc::tma_load_2d(base + SS::WQ + 2 * kSlab, &tm_w, &bar_load[st], 64, (int)(chh * 64));
-    if (un.outputs) {
+    if (outputs) {
       tc::tma_load_3d(base + SS::WQ + kSlab, &tm_q, &bar_load[st], 0, i, tc0);
       tc::tma_load_3d(base + SS::WQ + 3 * kSlab, &tm_q, &bar_load[st], 64, i, tc0);
     }
     tc::tma_load_3d(base + SS::K, &tm_k, &bar_load[st], 0, i, tc0);
     tc::tma_load_3d(base + SS::K + kSlab, &tm_k, &bar_load[st], 64, i, tc0);
     tc::tma_load_2d(base + SS::U, &tm_u, &bar_load[st], dv0 & 64, (int)(chh * 64));  // 64-col tile
-    if (un.outputs) tc::tma_load_2d(sm + SS::pbuf(c - c_begin), &tm_p, &bar_load[st], 0, (int)(chh * 64));
+    if (outputs) tc::tma_load_2d(sm + SS::pbuf(c - c_begin), &tm_p, &bar_load[st], 0, (int)(chh * 64));
   };
   auto load_wq = [&](int c) {  // single buffers: [W|Q] and gamma of chunk c
     const int tc0 = t_seq + (c - c_begin) * 64;
     const size_t chh = (size_t)c * Hv + j;
-    tc::mbar_arrive_expect_tx(&bar_load[0], (un.outputs ? 4 : 2) * kSlab + 256);
+    tc::mbar_arrive_expect_tx(&bar_load[0], (outputs ? 4 : 2) * kSlab + 256);
     tc::bulk_load(sm + SS::GAM, ws.gam + chh * 64, 256, &bar_load[0]);
     tc::tma_load_2d(sm + SS::WQ, &tm_w, &bar_load[0], 0, (int)(chh * 64));
     tc::tma_load_2d(sm + SS::WQ + 2 * kSlab, &tm_w, &bar_load[0], 64, (int)(chh * 64));
-    if (un.outputs) {
+    if (outputs) {
       tc::tma_load_3d(sm + SS::WQ + kSlab, &tm_q, &bar_load[0], 0, i, tc0);
       tc::tma_load_3d(sm + SS::WQ + 3 * kSlab, &tm_q, &bar_load[0], 64, i, tc0);
     }
@@ -784,10 +787,10 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
   auto load_kp = [&](int c) {  // single buffers: K and P of chunk c
     const int tc0 = t_seq + (c - c_begin) * 64;
     const size_t chh = (size_t)c * Hv + j;
-    tc::mbar_arrive_expect_tx(&bar_kp, (un.outputs ? 3 : 2) * kSlab);
+    tc::mbar_arrive_expect_tx(&bar_kp, (outputs ? 3 : 2) * kSlab);
     tc::tma_load_3d(sm + SS::K, &tm_k, &bar_kp, 0, i, tc0);
     tc::tma_load_3d(sm + SS::K + kSlab, &tm_k, &bar_kp, 64, i, tc0);
-    if (un.outputs) tc::tma_load_2d(sm + SS::P, &tm_p, &bar_kp, 0, (int)(chh * 64));
+    if (outputs) tc::tma_load_2d(sm + SS::P, &tm_p, &bar_kp, 0, (int)(chh * 64));
   };
   // kFused: the prep role's flag of chunk c (bounded wait; on expiry the loads are left out
   // and the consumer's own bounded wait ends the chain).  (Reading the next chunk's flag a
@@ -835,7 +838,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     if (!tc::mbar_wait(&bar_pv, pv_phase, ws.status, kDevErrTimeoutFwd)) return;
     tc::tc_fence_after();
     tmem_ld32w(tbase, warp, 32, y);
-    if (r < p_len && un.outputs) {
+    if (r < p_len && outputs) {
 #pragma unroll
       for (int b = 0; b < 32; ++b) y[b] = d.scale * (p_eg * xq[b] + y[b]);
       st_global_bf16x32(o + ((size_t)(p_t0 + r) * Hv + j) * 128 + dv0, y);
@@ -892,7 +895,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     mma_phase ^= 1;
     tc::tc_fence_after();
     if (ok && tid == kCopyTid) {  // h_saved[chunk] rows 0..127, columns dv0..dv0+31
-      if (un.outputs) {
+      if (outputs) {
         tc::tma_store_2d(&tm_hs, sm + SS::HS, dv0, (int)(chh * 128));
         tc::bulk_commit();
       }
@@ -909,7 +912,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
         tmem_ld32w(tbase, warp, 0, x);
         if (uok) ld_halfrow_bf16(stg + SS::U, r, (dv0 >> 5) & 1, u);
 #pragma unroll
-        for (int b = 0; b < 32; ++b) u[b] = uok ? (un.zero_u ? -x[b] : u[b] - x[b]) : 0.f;
+        for (int b = 0; b < 32; ++b) u[b] = uok ? (zero_u ? -x[b] : u[b] - x[b]) : 0.f;
         st_col32_bf16(sm + SS::VNT, r, u);
 #pragma unroll
         for (int b = 0; b < 32; ++b) vn_keep[b] = u[b];
@@ -955,7 +958,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
     }
     // saved factors: Vn replaces U in the saved buffer (the backward reads Vn; each slice writes
     // only its own columns, which no other CTA reads), off the chain: after the MMA issue
-    if (ok && d.save_wy && warp < 2 && un.outputs)
+    if (ok && d.save_wy && warp < 2 && outputs)
       st_global_bf16x32(reinterpret_cast<bf16*>(ws.U) + (chh * 64 + r) * 128 + dv0, vn_keep);
     ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, mma_phase, ws.status, kDevErrTimeoutFwd));
     mma_phase ^= 1;
@@ -987,7 +990,7 @@ __device__ __forceinline__ void state_body(const CUtensorMap& tm_q, const CUtens
   if (warp == 0) tc::tmem_dealloc(tbase, 128);
 }
 
-template <bool kSingle>
+template <bool kSingle, bool kModes>
 __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_u,
@@ -996,7 +999,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_state_kernel(
   extern __shared__ unsigned char smem_raw[];
   const StateUnit un = state_unit(d, ws, cp, (int)blockIdx.x, S0, S_T);
   if (un.skip) return;  // uniform over the block, before any barrier or tensor memory
-  state_body<kSingle, false>(tm_q, tm_k, tm_w, tm_u, tm_p, tm_hs, d, o, ws, un, align1024(smem_raw));
+  state_body<kSingle, false, kModes>(tm_q, tm_k, tm_w, tm_u, tm_p, tm_hs, d, o, ws, un, align1024(smem_raw));
 }
 
 // The forward's prep and state recurrence in one cooperative launch (every CTA resident, one
@@ -1021,7 +1024,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_fwd_fused_kernel(
   __syncthreads();
   const int role = s_role;
   if (role >= 0)
-    state_body<false, true>(tm_q, tm_k, tm_w, tm_u, tm_p, tm_hs, d, o, ws,
+    state_body<false, true, false>(tm_q, tm_k, tm_w, tm_u, tm_p, tm_hs, d, o, ws,
                             state_unit(d, ws, CpArgs{}, role, S0, S_T), align1024(smem_raw));
   else
     prep_body<true>(tm_q, tm_k, tm_v, tm_w, tm_u, tm_p, tm_t, d, g, beta, ws, write_T, align1024(smem_raw));
@@ -1124,7 +1127,9 @@ cudaError_t tc_forward(const Dims& d, const FwdArgs& a, const Workspace& ws, cud
     // more CTAs than SMs: the single-buffered variant, two CTAs per SM, so they all run at once
     const bool single = units > n_sm;
     const size_t sms = (single ? StateSmem<true>::BYTES : StateSmem<false>::BYTES) + 1024;
-    auto kern = single ? tc_fwd_state_kernel<true> : tc_fwd_state_kernel<false>;
+    const bool modes = cp.pass == 1;  // only the first pass has map units
+    auto kern = single ? (modes ? tc_fwd_state_kernel<true, true> : tc_fwd_state_kernel<true, false>)
+                       : (modes ? tc_fwd_state_kernel<false, true> : tc_fwd_state_kernel<false, false>);
     set_smem_once((const void*)kern, sms);
     kern<<<(unsigned)units, kTcThreads, sms, s>>>(tq, tk, tw, tu, tp, ths, d, a.S0, a.S_T, (bf16*)a.o, ws, cp);
     stage_mark(s, stage);

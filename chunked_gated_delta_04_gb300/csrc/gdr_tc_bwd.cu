@@ -213,8 +213,10 @@ __device__ __forceinline__ WalkUnit walk_unit(const Dims& d, const Workspace& ws
 }
 
 // One walk unit (see WalkUnit).  tb: the caller's 512 TMEM columns.  Every thread of the CTA
-// (kWalkThreads) calls it.
-template <bool kPublish>
+// (kWalkThreads) calls it.  kModes: the unit may be a first-pass map (no stores, or dO = 0 from the
+// identity); without it those cases are compiled out (true walks only, as the plain chain and
+// the second pass run).
+template <bool kPublish, bool kModes>
 __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_w,
                                           const CUtensorMap& tm_p, const CUtensorMap& tm_do,
                                           const CUtensorMap& tm_dhs, const CUtensorMap& tm_dvs, const Dims& d,
@@ -229,6 +231,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
   const int nch = c_end - c_begin;
   const int t_seq = un.t_seq;
   const int L = un.L;
+  const bool stores = !kModes || un.stores, zero_do = kModes && un.zero_do, g0_eye = kModes && un.g0_eye;
   uint32_t* const status = ws.status;
   constexpr uint32_t kBit = kDevErrTimeoutBwd;
   // walk step it = 0, 1, ... is chunk c_end - 1 - it (stage it & 1); its first token, length
@@ -265,7 +268,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       GDR_DELAY(14);
       // Q, dO and P feed only the dO products: the transition walk (dO = 0) leaves them out
       // (the scaling of Q's rows and the skipped products then touch stale tiles no one reads)
-      const bool dO_tiles = !un.zero_do;
+      const bool dO_tiles = !zero_do;
       tc::mbar_arrive_expect_tx(bar, (dO_tiles ? 9 : 4) * kSlab + 256);
       tc::bulk_load(base + WS::GAM, ws.gam + chh * 64, 256, bar);
       tc::tma_load_3d(base + WS::KQ, &tm_k, bar, 0, i, tc0);
@@ -286,7 +289,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       tc::bulk_prefetch_l2(ws.gam + chh * 64, 256);
       tc::tma_prefetch_l2_3d(&tm_k, 0, i, tc0);
       tc::tma_prefetch_l2_3d(&tm_k, 64, i, tc0);
-      if (!un.zero_do) {
+      if (!zero_do) {
         tc::tma_prefetch_l2_3d(&tm_q, 0, i, tc0);
         tc::tma_prefetch_l2_3d(&tm_q, 64, i, tc0);
         tc::tma_prefetch_l2_3d(&tm_do, 0, j, tc0);
@@ -331,11 +334,11 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       unsigned char* stg = sm + st * WS::STAGE;
       if (!tc::mbar_wait(&bar_load[st], ph, status, kBit)) return false;
       tc::tc_fence_after();
-      if (!un.zero_do)
+      if (!zero_do)
         tc::gemm(accV0 + 128 * st, tc::mnmaj(stg + WS::P, kSlab), tc::mnmaj(stg + WS::DO, kSlab), 128, 4, false);
       if (!tc::mbar_wait(&bar_scaled[st], ph, status, kBit)) return false;
       tc::tc_fence_after();
-      if (!un.zero_do)
+      if (!zero_do)
         tc::gemm(accH0 + 128 * st, tc::mnmaj(stg + WS::KQ + kSlab, 2 * kSlab), tc::mnmaj(stg + WS::DO, kSlab), 128,
                  4, false);
       return true;
@@ -355,7 +358,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       GDR_DELAY(13);
       GDR_TRACE_CLK(tw1);
       tc::gemm(accV0 + 128 * st, tc::kmaj(stg + WS::KQ, 2 * kSlab), tc::mnmaj(sm + WS::DH, 16384), 128, 8,
-               !un.zero_do);
+               !zero_do);
       tc::mma_commit(&bar_vfull[st]);
       GDR_TRACE_SINCE(3, 11, tw1);
       GDR_TRACE_CLK(tw2);
@@ -365,7 +368,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       tc::tc_fence_after();
       GDR_TRACE_CLK(tw3);
       tc::gemm(accH0 + 128 * st, tc::mnmaj(stg + WS::W, kSlab), tc::mnmaj(sm + WS::DVN + st * 16384, kSlab), 128,
-               4, !un.zero_do, true);
+               4, !zero_do, true);
       tc::mma_commit(&bar_hfull[st]);
       GDR_TRACE_SINCE(3, 13, tw3);
       // the next chunk's dh'-free products
@@ -387,7 +390,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       if (!tc::mbar_wait(&bar_dh, it & 1, status, kBit)) break;
       GDR_TRACE_SINCE(3, 20, tc0_);
       GDR_DELAY(10);
-      if (un.stores) {
+      if (stores) {
         tc::tma_store_2d(&tm_dhs, sm + WS::DH, 0, (int)(chh * 128));
         tc::tma_store_2d(&tm_dhs, sm + WS::DH + 16384, 64, (int)(chh * 128));
         tc::bulk_commit();
@@ -395,7 +398,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       }
       tc::mbar_arrive(&bar_dhfree);
       if (!tc::mbar_wait(&bar_dvn[st], ph, status, kBit)) break;
-      if (un.stores) {
+      if (stores) {
         unsigned char* dvn = sm + WS::DVN + st * 16384;
         tc::tma_store_2d(&tm_dvs, dvn, 0, (int)(chh * 64));
         tc::tma_store_2d(&tm_dvs, dvn + kSlab, 64, (int)(chh * 64));
@@ -404,7 +407,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       }
       tc::mbar_arrive(&bar_dvnfree[st]);
       GDR_TRACE_CLK(tc1_);
-      if (kPublish && pub >= 0) {  // the previous step's two groups have landed
+      if (kPublish && stores && pub >= 0) {  // the previous step's two groups have landed
         tc::bulk_wait<2>();
         GDR_DELAY(11);
         publish_chunk(ws.walk_flags + (size_t)pub * Hv + j);
@@ -413,7 +416,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       pub = chunk_of(it);
     }
     tc::bulk_wait<0>();
-    if (kPublish && pub >= 0) publish_chunk(ws.walk_flags + (size_t)pub * Hv + j);
+    if (kPublish && stores && pub >= 0) publish_chunk(ws.walk_flags + (size_t)pub * Hv + j);
   } else if (tid < 256) {
     // ---------------------------------------------------------------- epilogue warps
     const int ln = (warp & 3) * 32 + lane;  // TMEM lane: token of accV (lanes 0-63), dk of accH
@@ -450,7 +453,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
     float dh[64];
 #pragma unroll
     for (int b = 0; b < 64; ++b)
-      dh[b] = un.g0_eye ? (ln == 64 * hf + b ? 1.f : 0.f)
+      dh[b] = g0_eye ? (ln == 64 * hf + b ? 1.f : 0.f)
               : un.g0   ? un.g0[un.g0_kv ? (size_t)ln * 128 + 64 * hf + b : (size_t)(64 * hf + b) * 128 + ln]
                         : 0.f;
     auto stage_dh = [&]() {  // dh' of the next step as the MMA's bf16 operand
@@ -556,8 +559,10 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
   tc::tc_fence_after();
 }
 
-// The reverse walk alone (cluster-pair gradients, or more sequences than the fused kernel's
-// order table holds): one CTA per (sequence, v-head).
+// The reverse walk alone (cluster-pair gradients, more sequences than the fused kernel's order
+// table holds, or the first context-parallel pass): one CTA per walk unit.  kPublish: counts
+// every stored chunk in ws.walk_flags for a fused kernel launched after it.
+template <bool kPublish, bool kModes>
 __global__ void __launch_bounds__(kWalkThreads, 1) tc_bwd_walk_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
@@ -573,7 +578,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tc_bwd_walk_kernel(
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  walk_body<false>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvs, d, ws, un, tmem_slot, sm);
+  walk_body<kPublish, kModes>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvs, d, ws, un, tmem_slot, sm);
   if (threadIdx.x < 32) tc::tmem_dealloc(tmem_slot, kWalkTmemCols);
 }
 
@@ -735,7 +740,7 @@ __device__ __forceinline__ bool gsync_and(bool p) { return tc::named_sync_and(1,
 // walk finishes them (last chunk of every sequence first), and a chunk's dh' and dVn
 // tiles are loaded only once the walk unit has counted it in ws.walk_flags.
 // tb: 512 TMEM columns owned by the caller.
-template <bool kGroup, bool kPair, bool kDyn>
+template <bool kGroup, bool kPair, bool kDyn, bool kCpOrder = false>
 __device__ __forceinline__ void grad_body(
     const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_do,
     const CUtensorMap& tm_w, const CUtensorMap& tm_u, const CUtensorMap& tm_dvn, const CUtensorMap& tm_dh,
@@ -799,7 +804,7 @@ __device__ __forceinline__ void grad_body(
   // kDyn: item w = q * Hv + v-head, queue position q in walk order (the index kernel lists
   // each position's chunk)
   auto chunk_of = [&](int w) {
-    if (kDyn) return idx_grad_chunk(d, ws, w / Hv);
+    if (kDyn) return kCpOrder ? idx_cp_grad_chunk(d, w / Hv) : idx_grad_chunk(d, ws, w / Hv);
     return kPair ? w / d.Hk : w / Hv;
   };
   auto vhead_of = [&](int w) { return kPair ? (w % d.Hk) * 2 + (int)rank : w % Hv; };
@@ -1403,7 +1408,7 @@ __global__ void __launch_bounds__(kGradThreads) tc_bwd_grad_kernel(
 // thread), so the increase never waits for registers that are not there.
 constexpr uint32_t kWalkRegs = 168, kGradRegs = 232, kIdleRegs = 40;
 static_assert(4 * 32 * kIdleRegs + 8 * 32 * kGradRegs == (uint32_t)kWalkThreads * kWalkRegs, "register split");
-template <bool kGroup>
+template <bool kGroup, bool kCpOrder>
 __global__ void __launch_bounds__(kWalkThreads, 1) tc_bwd_walkgrad_kernel(
     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -1414,7 +1419,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tc_bwd_walkgrad_kernel(
     const __grid_constant__ CUtensorMap tm_dq, const __grid_constant__ CUtensorMap tm_dk,
     const __grid_constant__ CUtensorMap tm_dv, Dims d, const float* __restrict__ dS_T, float* __restrict__ dS0,
     const bf16* __restrict__ beta, bf16* __restrict__ dq, bf16* __restrict__ dk, bf16* __restrict__ dv,
-    float* __restrict__ dg, bf16* __restrict__ dbeta, Workspace ws) {
+    float* __restrict__ dg, bf16* __restrict__ dbeta, Workspace ws, CpArgs cp) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = align1024(smem_raw);
   __shared__ uint32_t tmem_slot;
@@ -1422,19 +1427,22 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tc_bwd_walkgrad_kernel(
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  const int n_units = d.num_seqs * d.Hv;
+  // walk units: one per (sequence, v-head), or the second context-parallel pass's segment walks
+  // (the first pass ran before this kernel and counted its chunks in ws.walk_flags)
+  const int n_units = d.num_seqs * d.Hv * walk_units_per_chain(cp);
   if (threadIdx.x == 0) GDR_TRACE_INFO_SET(0, GDR_TRACE_NOW());
-  for (int u = (int)blockIdx.x; u < n_units; u += (int)gridDim.x)
-    walk_body<true>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvn, d, ws, walk_unit(d, ws, CpArgs{}, u, dS_T, dS0),
-                    tmem_slot, sm);
+  for (int u = (int)blockIdx.x; u < n_units; u += (int)gridDim.x) {
+    const WalkUnit un = walk_unit(d, ws, cp, u, dS_T, dS0);
+    if (!un.skip) walk_body<true, false>(tm_q, tm_k, tm_w, tm_p, tm_do, tm_dhs, tm_dvn, d, ws, un, tmem_slot, sm);
+  }
   if (threadIdx.x == 0) GDR_TRACE_INFO_SET(1, GDR_TRACE_NOW());
   if (threadIdx.x >= kGradThreads) {  // the walk's single-thread roles: registers to the gradients
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kIdleRegs) : "memory");
     return;
   }
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kGradRegs) : "memory");
-  grad_body<kGroup, false, true>(tm_q, tm_k, tm_v, tm_do, tm_w, tm_u, tm_dvn, tm_dh, tm_h, tm_t, tm_dq, tm_dk,
-                                 tm_dv, d, beta, dq, dk, dv, dg, dbeta, ws, tmem_slot, sm);
+  grad_body<kGroup, false, true, kCpOrder>(tm_q, tm_k, tm_v, tm_do, tm_w, tm_u, tm_dvn, tm_dh, tm_h, tm_t, tm_dq,
+                                           tm_dk, tm_dv, d, beta, dq, dk, dv, dg, dbeta, ws, tmem_slot, sm);
   if (threadIdx.x == 0) GDR_TRACE_INFO_SET(2, GDR_TRACE_NOW());
   if (threadIdx.x < 32) tc::tmem_dealloc(tmem_slot, 512);
 }
@@ -1495,12 +1503,31 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
   }
   // One walk unit per (sequence, v-head), over all of DV.
   Dims dd = d;
-  auto kern = d.G > 1 ? tc_bwd_walkgrad_kernel<true> : tc_bwd_walkgrad_kernel<false>;
+  const bool cp_on = d.num_seqs > 0 && d.cp_bwd > 1 && Tt > 0;
+  // the fused kernel; with context-parallel segments the instantiation whose item queue follows
+  // the segment walks
+  auto kern = d.G > 1 ? (cp_on ? tc_bwd_walkgrad_kernel<true, true> : tc_bwd_walkgrad_kernel<true, false>)
+                      : (cp_on ? tc_bwd_walkgrad_kernel<false, true> : tc_bwd_walkgrad_kernel<false, false>);
   // the fused kernel's register split assumes the block holds exactly kWalkRegs per thread; a
   // build that allocated another count runs the walk and the gradients as two launches
   cudaFuncAttributes fa{};
   const bool regs_ok = cudaFuncGetAttributes(&fa, (const void*)kern) == cudaSuccess && fa.numRegs == (int)kWalkRegs;
-  if (fused_walk_grad(d) && regs_ok && d.cp_bwd <= 1) {  // walk and gradients in one cooperative kernel
+  auto walk_launch = [&](bool publish, const CpArgs& cp, long long units, const char* stage) -> cudaError_t {
+    if (units <= 0) return cudaSuccess;
+    const size_t sm = WalkSmem::BYTES + 1024;
+    const bool modes = cp.pass == 1;  // only the first pass has map units
+    auto wk = publish ? (modes ? tc_bwd_walk_kernel<true, true> : tc_bwd_walk_kernel<true, false>)
+                      : (modes ? tc_bwd_walk_kernel<false, true> : tc_bwd_walk_kernel<false, false>);
+    set_smem_once((const void*)wk, sm);
+    wk<<<(unsigned)units, kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, dd, a.dS_T, a.dS0, ws, cp);
+    stage_mark(s, stage);
+    return cudaGetLastError();
+  };
+  const int P = d.cp_bwd;
+  const long long chains = (long long)d.num_seqs * d.Hv;
+  // walk and gradients in one cooperative kernel; with context-parallel segments (fixed length)
+  // the kernel runs the second pass's walks, after the first pass and the scan
+  if (fused_walk_grad(d) && regs_ok && (!cp_on || d.cu == nullptr)) {
     int per_sm = 0;
     const size_t smg = std::max(GradSmem::BYTES, WalkSmem::BYTES) + 1024;
     set_smem_once((const void*)kern, smg);
@@ -1508,6 +1535,14 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
       return cudaErrorInvalidConfiguration;
     e = cudaMemsetAsync(ws.walk_flags, 0, sizeof(uint32_t) * ((size_t)d.max_chunks * d.Hv + 64), s);
     if (e != cudaSuccess) return e;
+    CpArgs cp{};
+    if (cp_on) {
+      cp = CpArgs{1, P, ws.cp_X, ws.cp_M, ws.cp_R};
+      e = walk_launch(true, cp, chains * (1 + 2 * (P - 2)), "bwd_cp_maps");
+      if (e == cudaSuccess && P > 2) e = launch_cp_scan(d, ws, P, true, s);
+      if (e != cudaSuccess) return e;
+      cp.pass = 3;
+    }
     const bf16* beta = (const bf16*)a.beta;
     bf16 *dq = (bf16*)a.dq, *dk = (bf16*)a.dk, *dv = (bf16*)a.dv, *dbeta = (bf16*)a.dbeta;
     const float* dS_T = a.dS_T;
@@ -1515,7 +1550,7 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     Workspace w = ws;
     void* args[] = {&tq, &tk, &tv, &tdo, &tw, &tu, &tp, &tdvn, &tdh, &tdhs, &thf, &tt, &tdq, &tdk, &tdv, &dd,
                     (void*)&dS_T, (void*)&dS0, (void*)&beta, (void*)&dq, (void*)&dk, (void*)&dv, (void*)&dg,
-                    (void*)&dbeta, &w};
+                    (void*)&dbeta, &w, &cp};
     e = cudaLaunchCooperativeKernel((const void*)kern, dim3((unsigned)(per_sm * n_sm)), dim3(kWalkThreads), args, smg,
                                     s);
     if (e != cudaSuccess) return e;
@@ -1526,28 +1561,17 @@ cudaError_t tc_backward(const Dims& d, const BwdArgs& a, const Workspace& ws, cu
     }
     return cudaGetLastError();
   }
-  auto walk_launch = [&](const CpArgs& cp, long long units, const char* stage) -> cudaError_t {
-    if (units <= 0) return cudaSuccess;
-    const size_t sm = WalkSmem::BYTES + 1024;
-    set_smem_once((const void*)tc_bwd_walk_kernel, sm);
-    tc_bwd_walk_kernel<<<(unsigned)units, kWalkThreads, sm, s>>>(tq, tk, tw, tp, tdo, tdhs, tdvn, dd, a.dS_T, a.dS0,
-                                                                ws, cp);
-    stage_mark(s, stage);
-    return cudaGetLastError();
-  };
-  if (d.num_seqs > 0 && d.cp_bwd > 1 && Tt > 0) {
+  if (cp_on) {
     // context parallel: the last segment's walk and every middle segment's maps, the scan of the
     // boundary gradients, then segments 0 .. nseg - 2 from their true end gradients (WalkUnit)
-    const int P = d.cp_bwd;
-    const long long chains = (long long)d.num_seqs * d.Hv;
     CpArgs cp{1, P, ws.cp_X, ws.cp_M, ws.cp_R};
-    e = walk_launch(cp, chains * (1 + 2 * (P - 2)), "bwd_cp_maps");
+    e = walk_launch(false, cp, chains * (1 + 2 * (P - 2)), "bwd_cp_maps");
     if (e == cudaSuccess && P > 2) e = launch_cp_scan(d, ws, P, true, s);
     cp.pass = 3;
-    if (e == cudaSuccess) e = walk_launch(cp, chains * (P - 1), "bwd_cp_walk");
+    if (e == cudaSuccess) e = walk_launch(false, cp, chains * (P - 1), "bwd_cp_walk");
     if (e != cudaSuccess) return e;
   } else if (d.num_seqs > 0) {
-    e = walk_launch(CpArgs{}, (long long)d.num_seqs * d.Hv, "bwd_walk");
+    e = walk_launch(false, CpArgs{}, chains, "bwd_walk");
     if (e != cudaSuccess) return e;
   }
   if (d.max_chunks > 0 && Tt > 0) {
