@@ -316,9 +316,11 @@ def main():
     ap.add_argument("--no-graph", action="store_true",
                     help="time direct C-ABI calls instead of a CUDA-graph replay of the same calls")
     ap.add_argument("--cp-fwd", type=int, default=1,
-                    help="intra-card context parallelism: segments per sequence in the forward (1: off)")
+                    help="intra-card context parallelism: segments per sequence in the forward (1: off, -1: the "
+                         "library chooses)")
     ap.add_argument("--cp-bwd", type=int, default=1,
-                    help="intra-card context parallelism: segments per sequence in the backward (1: off)")
+                    help="intra-card context parallelism: segments per sequence in the backward (1: off, -1: the "
+                         "library chooses)")
     ap.add_argument("--recompute-wy", action="store_true",
                     help="the backward recomputes the chunk factors (gamma, W, U, P, T) instead of reading the "
                          "ones the forward saved")
@@ -593,7 +595,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16" if w.dtype == torch.bfloat16 else "f32",
             "data": "synthetic (seeded; see chunked_gated_delta_04_gb300/inputs.py)",
             "config": config_dict(w, inp, args.h_dtype, args.prologue, args.recompute_wy,
-                                  (args.cp_fwd, args.cp_bwd)),
+                                  gdr.gdr_debug_cp_segments(p)),
             "roofline": roofline,
             "step_roofline": {"ms": step_roof, "frac": step_roof / ms_per_step, "bound": "hbm" if
                               t_hbm_step >= t_flop_step else "tensor", "bytes": wm["bytes_fwd"] + wm["bytes_bwd"],

@@ -59,7 +59,7 @@ _STAGE_ARR = None
 EXPORTS = ["gdr_max_chunks", "gdr_saved_states_bytes", "gdr_fwd_workspace_bytes", "gdr_bwd_workspace_bytes",
            "gdr_fwd", "gdr_bwd", "gdr_workspace_status", "gdr_status_string", "gdr_path",
            "gdr_debug_set_stage_events", "gdr_debug_stage_count", "gdr_debug_stage_name",
-           "gdr_debug_launch_count", "gdr_debug_last_cuda_error", "gdr_debug_cuda_error_string", "gdr_fwd_noalloc", "gdr_noalloc_status", "gdr_debug_tc_gemm", "gdr_debug_timeout_selftest", "gdr_debug_cp_segment"]
+           "gdr_debug_launch_count", "gdr_debug_last_cuda_error", "gdr_debug_cuda_error_string", "gdr_fwd_noalloc", "gdr_noalloc_status", "gdr_debug_tc_gemm", "gdr_debug_timeout_selftest", "gdr_debug_cp_segment", "gdr_debug_cp_segments"]
 
 
 def _open(path: str):
@@ -103,6 +103,8 @@ def _open(path: str):
     lib.gdr_debug_timeout_selftest.restype = i
     lib.gdr_debug_cp_segment.argtypes = [i, i, i, i, ctypes.POINTER(ctypes.c_int)]
     lib.gdr_debug_cp_segment.restype = i
+    lib.gdr_debug_cp_segments.argtypes = [P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+    lib.gdr_debug_cp_segments.restype = i
     return lib
 
 
@@ -165,7 +167,7 @@ def make_problem(B, T, Hk, Hv, DK, DV, dtype, layout="KV", cu_seqlens=None, num_
     """Build a gdr_problem.  dtype, h_dtype (of h_saved): torch.float32/bfloat16; layout "KV"/"VK";
     prologue: bit set of GDR_PROLOGUE_* (the matching inputs are raw); save_wy: the forward keeps
     its chunk factors in the saved buffer for the backward; cp_fwd, cp_bwd: context-parallel
-    segments per sequence of each direction (1: off)."""
+    segments per sequence of each direction (1: off, GDR_CP_AUTO: the library chooses)."""
     p = gdr_problem()
     p.B, p.T, p.Hk, p.Hv, p.DK, p.DV = B, T, Hk, Hv, DK, DV
     if cu_seqlens is not None:
@@ -285,6 +287,18 @@ def gdr_debug_cp_segment(c0: int, c1: int, P: int, s: int):
     if st != 0:
         raise ValueError(f"gdr_debug_cp_segment({c0}, {c1}, {P}, {s}): invalid arguments")
     return tuple(out)
+
+
+def gdr_debug_cp_segments(p):
+    """(forward, backward) segment counts a call with problem p would use (1: none)."""
+    f, b = ctypes.c_int(0), ctypes.c_int(0)
+    st = _lib_handle().gdr_debug_cp_segments(ctypes.byref(p), ctypes.byref(f), ctypes.byref(b))
+    if st != 0:
+        raise GDRError(st, "gdr_debug_cp_segments")
+    return f.value, b.value
+
+
+GDR_CP_AUTO = -1
 
 
 def gdr_debug_launch_count() -> int:

@@ -62,6 +62,23 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Segment count of one direction's context-parallel passes (see GDR_CP_AUTO in gdr.h).
+int cp_segments(int requested, const Dims& d, bool backward) {
+  if (requested != GDR_CP_AUTO) return requested > 1 ? requested : 1;
+  int dev = 0, n_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0) {
+    (void)cudaGetLastError();  // our own query's error: no segments
+    return 1;
+  }
+  const long long chains = (long long)d.num_seqs * d.Hv;
+  if (chains <= 0 || chains * 16 > n_sm) return 1;
+  const long long nc = d.cu ? d.T_total / kChunk + 1 : (d.T + kChunk - 1) / kChunk;
+  long long P = nc / 16 < 32 ? nc / 16 : 32;
+  while (P >= 3 && (backward ? chains * (1 + 2 * (P - 2)) > n_sm : chains * (4 + 8 * (P - 2)) > 2ll * n_sm)) --P;
+  return P >= 3 ? (int)P : 1;
+}
+
 // Fills *d from *p; returns GDR_OK or the reason the problem is rejected.
 gdr_status resolve(const gdr_problem* p, Dims* d) {
   if (p == nullptr) return GDR_ERR_INVALID_ARG;
@@ -73,7 +90,8 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
   if (p->h_dtype != GDR_DTYPE_F32 && p->h_dtype != GDR_DTYPE_BF16) return GDR_ERR_INVALID_ARG;
   if (p->prologue & ~7u) return GDR_ERR_INVALID_ARG;
   if (p->save_wy != 0 && p->save_wy != 1) return GDR_ERR_INVALID_ARG;
-  if (p->cp_fwd < 0 || p->cp_fwd > kMaxCpSegments || p->cp_bwd < 0 || p->cp_bwd > kMaxCpSegments)
+  if (p->cp_fwd < GDR_CP_AUTO || p->cp_fwd > kMaxCpSegments || p->cp_bwd < GDR_CP_AUTO ||
+      p->cp_bwd > kMaxCpSegments)
     return GDR_ERR_INVALID_ARG;
   if (p->cu_seqlens != nullptr) {
     if (p->B != 1) return GDR_ERR_INVALID_ARG;
@@ -110,8 +128,8 @@ gdr_status resolve(const gdr_problem* p, Dims* d) {
   // saved chunk factors: the tensor-core path and the small-head SIMT path (gdr_simt_small.cu)
   d->save_wy = (d->path == 1 || (p->DK <= 64 && p->DV <= 64)) ? p->save_wy : 0;
   // context-parallel segments: the tensor-core path (the SIMT path runs the plain chain)
-  d->cp_fwd = d->path == 1 && p->cp_fwd > 1 ? p->cp_fwd : 1;
-  d->cp_bwd = d->path == 1 && p->cp_bwd > 1 ? p->cp_bwd : 1;
+  d->cp_fwd = d->path == 1 ? cp_segments(p->cp_fwd, *d, false) : 1;
+  d->cp_bwd = d->path == 1 ? cp_segments(p->cp_bwd, *d, true) : 1;
   return GDR_OK;
 }
 
@@ -414,6 +432,15 @@ gdr_status gdr_workspace_status(const void* workspace, gdr_stream_t stream, uint
 }
 
 int gdr_debug_last_cuda_error(void) { return g_last_cuda_error.load(std::memory_order_relaxed); }
+
+int gdr_debug_cp_segments(const gdr_problem* p, int* fwd, int* bwd) {
+  Dims d;
+  const gdr_status st = resolve(p, &d);
+  if (st != GDR_OK) return (int)st;
+  if (fwd) *fwd = d.cp_fwd;
+  if (bwd) *bwd = d.path == 1 && !tc_bwd_available() ? 1 : d.cp_bwd;
+  return 0;
+}
 
 int gdr_debug_cp_segment(int c0, int c1, int P, int s, int* out3) {
   if (P < 1 || s < 0 || c1 < c0 || out3 == nullptr) return 1;

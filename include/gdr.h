@@ -109,7 +109,8 @@ typedef struct {
                                 the tensor-core path and on the SIMT path for DK, DV <= 64,
                                 ignored (nothing saved) for larger SIMT heads. */
   int cp_fwd, cp_bwd;        /* intra-card context parallelism (FlashQLA PR #34, "Current
-                                status"), per direction: 0 or 1 = off; P in 2..64 = every
+                                status"), per direction: 0 or 1 = off; -1 = the library
+                                chooses (GDR_CP_AUTO below); P in 2..64 = every
                                 sequence is cut at chunk boundaries into min(P, its chunk
                                 count) segments of nearly equal chunk counts (the first ones
                                 one longer), which run side by side: a first pass finds
@@ -124,6 +125,14 @@ typedef struct {
                                 idle.  Honoured on the tensor-core path, ignored on the
                                 SIMT path.  Zero-initialised structs keep it off. */
 } gdr_problem;
+
+/* cp_fwd / cp_bwd = GDR_CP_AUTO: segments only when the (sequence, v-head) chains are at most
+ * 1/16 of the GPU's SM count (so the plain chains would leave most SMs idle); then the largest
+ * P <= min(32, C / 16), C = the longest sequence's chunk count (varlen: its upper bound
+ * T / 64 + 1), whose first pass fits in one wave: chains * (4 + 8 (P - 2)) <= 2 * SMs forward,
+ * chains * (1 + 2 (P - 2)) <= SMs backward; off if that P is below 3.  The choice depends only
+ * on the problem and the current device, so size queries and calls agree. */
+#define GDR_CP_AUTO (-1)
 
 /* Upper bound on the number of 64-token chunks: B * ceil(T/64) for fixed length,
  * floor(T/64) + num_seqs for varlen.  Returns 0 for an invalid problem. */

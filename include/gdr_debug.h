@@ -25,6 +25,8 @@
 #ifndef GDR_DEBUG_H_
 #define GDR_DEBUG_H_
 
+#include "gdr.h"
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -58,6 +60,11 @@ int gdr_debug_timeout_selftest(unsigned int* status, unsigned long long limit_ns
  * out3 (a segment s >= nseg is empty: {c1, c1, nseg}).  Host only; returns 0, or non-zero for
  * P < 1, s < 0, c1 < c0 or a null out3. */
 int gdr_debug_cp_segment(int c0, int c1, int P, int s, int* out3);
+
+/* The segment counts a call with problem *p would use on the current device (1: no segments;
+ * GDR_CP_AUTO resolved), forward into *fwd and backward into *bwd.  Returns 0, or a gdr_status
+ * for an invalid problem. */
+int gdr_debug_cp_segments(const gdr_problem* p, int* fwd, int* bwd);
 
 #ifdef __cplusplus
 }

@@ -89,7 +89,7 @@ def test_size_queries(lib):
     (dict(h_dtype=torch.float16), gdr.GDR_ERR_INVALID_ARG),  # h_saved is fp32 or bf16
     (dict(prologue=8), gdr.GDR_ERR_INVALID_ARG),              # unknown prologue bit
     (dict(save_wy=2), gdr.GDR_ERR_INVALID_ARG),               # save_wy is 0 or 1
-    (dict(cp_fwd=-1), gdr.GDR_ERR_INVALID_ARG),               # context-parallel segments: 0 .. 64
+    (dict(cp_fwd=-2), gdr.GDR_ERR_INVALID_ARG),               # context-parallel segments: -1 (auto), 0 .. 64
     (dict(cp_bwd=65), gdr.GDR_ERR_INVALID_ARG),
     # 2^30 token-heads but 2^24 chunk-heads: the saved states' 128-row blocks would pass 2^31
     (dict(T=1 << 27), gdr.GDR_ERR_UNSUPPORTED),
@@ -119,6 +119,11 @@ def test_context_parallel_workspace(lib):
         assert gdr.gdr_fwd_workspace_bytes(pf) == gdr.gdr_fwd_workspace_bytes(p)
         assert gdr.gdr_bwd_workspace_bytes(pb) == gdr.gdr_bwd_workspace_bytes(p)
     assert gdr.gdr_fwd_workspace_bytes(prob(cp_fwd=8)) == gdr.gdr_fwd_workspace_bytes(prob())  # SIMT shape
+    # the resolved counts: explicit values pass through on the tensor-core path, the SIMT path has none
+    if gdr.gdr_path(p) == 1:
+        assert gdr.gdr_debug_cp_segments(prob(DK=128, DV=128, cp_fwd=4, cp_bwd=0)) == (4, 1)
+    assert gdr.gdr_debug_cp_segments(prob(cp_fwd=4, cp_bwd=4)) == (1, 1)
+    assert gdr.gdr_debug_cp_segments(prob(DK=128, DV=128, cp_fwd=gdr.GDR_CP_AUTO, cp_bwd=1))[1] == 1
 
 
 def test_context_parallel_split_matches_the_oracle(lib):

@@ -11,6 +11,7 @@ sums), both state layouts, bf16 saved states, saved chunk factors and slow decay
 import pytest
 import torch
 
+import chunked_gated_delta_04_gb300 as gdr
 from chunked_gated_delta_04_gb300.inputs import make_inputs, small_workload
 from gdr_testlib import compare, reference, run_gpu, tol_for
 
@@ -68,3 +69,33 @@ def test_cp_close_to_single_chain():
             continue
         a, b = val.float(), cp[key].float()
         assert (a - b).abs().max().item() <= 2e-2 * a.abs().max().item(), key
+
+
+def _auto_rule(chains, nc, backward, n_sm):
+    """The documented GDR_CP_AUTO choice, restated."""
+    if chains * 16 > n_sm:
+        return 1
+    P = min(32, nc // 16)
+    while P >= 3 and ((chains * (1 + 2 * (P - 2)) > n_sm) if backward else (chains * (4 + 8 * (P - 2)) > 2 * n_sm)):
+        P -= 1
+    return P if P >= 3 else 1
+
+
+@pytest.mark.parametrize("B,T,Hk,Hv", [(1, 65536, 2, 2), (1, 65536, 1, 1), (1, 8192, 1, 2), (1, 65536, 16, 16),
+                                       (2, 4096, 16, 16), (1, 1000, 1, 1)])
+def test_cp_auto_choice(B, T, Hk, Hv):
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    p = gdr.make_problem(B, T, Hk, Hv, 128, 128, torch.bfloat16, cp_fwd=gdr.GDR_CP_AUTO, cp_bwd=gdr.GDR_CP_AUTO)
+    nc = (T + 63) // 64
+    assert gdr.gdr_debug_cp_segments(p) == (_auto_rule(B * Hv, nc, False, n_sm), _auto_rule(B * Hv, nc, True, n_sm))
+
+
+def test_cp_auto_matches_oracle():
+    """GDR_CP_AUTO on one short chain (4 segments of 16 chunks each way) against the oracle."""
+    w = small_workload("cp_auto", torch.bfloat16, B=1, T=4096, Hk=1, Hv=1, DK=128, DV=128)
+    inp = make_inputs(w)
+    p = gdr.make_problem(1, 4096, 1, 1, 128, 128, torch.bfloat16, cp_fwd=gdr.GDR_CP_AUTO, cp_bwd=gdr.GDR_CP_AUTO)
+    assert gdr.gdr_debug_cp_segments(p) == (4, 4)
+    res = run_gpu(inp, cp_fwd=gdr.GDR_CP_AUTO, cp_bwd=gdr.GDR_CP_AUTO)
+    torch.cuda.synchronize()
+    compare(res, reference(inp), tol_for(w.dtype))
