@@ -698,7 +698,7 @@ __global__ void __launch_bounds__(kTcThreads) tc_vn_kernel(const __grid_constant
 // Shared memory (1024-aligned tiles; later users of a tile noted after the arrow).
 struct GradSmem {
   static constexpr uint32_t KQ = 0;             // [K | Q] x 2 slabs (32 KB), to the end
-  static constexpr uint32_t DO = 32768;         // dO (16 KB) -> dk staging
+  static constexpr uint32_t DO = 32768;         // dO (16 KB); cluster pairs: -> the partner's dk half
   // O-hat = scale diag(e^gamma) dO and dVn interleaved by 64-column slab (slab s of O-hat at
   // OD + 16 KB s, of dVn 8 KB after it), so [O-hat; dVn] is one 128-row K-major operand
   // (32 KB); O-hat -> V after the first product, dVn to the WY backward
@@ -708,7 +708,7 @@ struct GradSmem {
                                                 //   h fp32 lands in H, H + 16 KB, VN and SCR
   static constexpr uint32_t VN = 147456;        // Vn~ (16 KB) -> T'
   static constexpr uint32_t W = 163840;         // Vn as loaded (16 KB) -> dv staging
-  static constexpr uint32_t UT = 180224;        // dW (16 KB)
+  static constexpr uint32_t UT = 180224;        // dW (16 KB) -> dk staging
   static constexpr uint32_t SCR = 196608;       // fp32 [64][65] scratch for row/column sums
   static constexpr uint32_t GAM = SCR + 16640;  // gamma (256 B)
   static constexpr uint32_t BYTES = GAM + 256;
@@ -719,7 +719,7 @@ struct GradSmem {
   static constexpr uint32_t T = H + 24576, DP = H, DT = H + 8192, XT = H + 16384, DAG = H + 24576;
   // fp32 h slab k (32 columns of 128 rows, 16 KB)
   static constexpr uint32_t hf32(int k) { return k < 3 ? H + (uint32_t)k * 16384 : SCR; }
-  static constexpr uint32_t TP = VN, DQS = DH, DVS = W, DKS = DO, DW = UT;
+  static constexpr uint32_t TP = VN, DQS = DH, DVS = W, DKS = UT, DW = UT;
 };
 
 constexpr int kGradThreads = 256;  // two warps per TMEM lane quarter, each on half the columns
@@ -790,8 +790,9 @@ __device__ __forceinline__ void grad_body(
   // Persistent: each CTA walks the (chunk, v-head) items w = blockIdx.x + k * gridDim.x,
   // keeping its barriers, TMEM and (warm) instruction cache across items.  The next
   // item's tiles are fetched as soon as the current item is done with their buffers
-  // (dh' and dVn after R2, W after R3, K/Q, U, h and gamma after R4, dO after the dk
-  // store), all on the next phase of bar_tma, so the loads overlap the current item.
+  // (dh', dVn and dO after R2, W after R3, K/Q, U, h and gamma after R4; with cluster pairs
+  // dO after the dk exchange, which receives into its tile), all on the next phase of
+  // bar_tma, so the loads overlap the current item.
   bool ok = true;
   uint32_t item_par = 0;  // phase parity of bar_tma / bar_tma2 for the current item
   uint32_t mma_par = 0;   // phase parity of bar_mma (five commits per item: it alternates)
@@ -1186,9 +1187,10 @@ __device__ __forceinline__ void grad_body(
       GDR_TRACE_SINCE(2, 24, tc24);
       if (cl_w >= n_items) pending = -1;
     }
-    if (pending >= 0) {
-      issue_loads(kDyn ? cl_w : wnext, kDyn ? cl_c : cnext, kLdDhDvn);
-      pending |= kLdDhDvn;
+    if (pending >= 0) {  // dO too (last read by P2), unless the dk exchange receives into its tile
+      constexpr int groups = kPair ? (int)kLdDhDvn : (int)(kLdDhDvn | kLdDo);
+      issue_loads(kDyn ? cl_w : wnext, kDyn ? cl_c : cnext, groups);
+      pending |= groups;
     }
   }
   GDR_TRACE_MARK(2, 8);
@@ -1282,7 +1284,7 @@ __device__ __forceinline__ void grad_body(
   ok = gsync_and(ok && tc::mbar_wait(&bar_mma, mma_par, ws.status, kDevErrTimeoutBwd));
   mma_par ^= 1;
   tc::tc_fence_after();
-  if (ok && tid == kCopyTid && pending >= 0) {  // every operand tile but dO (dk staging) is free
+  if (ok && tid == kCopyTid && pending >= 0) {  // every operand tile but dO (cluster pairs) is free
     issue_loads(kDyn ? cl_w : wnext, kDyn ? cl_c : cnext, kLdRest);
     pending |= kLdRest;
   }
@@ -1345,7 +1347,7 @@ __device__ __forceinline__ void grad_body(
     GDR_TRACE_CLK(tb23);
     tc::bulk_wait_read<0>();  // staging tiles read before the next item's loads
     GDR_TRACE_SINCE(2, 23, tb23);
-    if (ok && pending >= 0) {
+    if (kPair && ok && pending >= 0) {  // the dk exchange is done with the dO tile
       issue_loads(kDyn ? cl_w : wnext, kDyn ? cl_c : cnext, kLdDo);
       pending |= kLdDo;
     }
