@@ -14,6 +14,7 @@
 #include "gdr_device.cuh"
 #include "gdr_internal.h"
 #include "gdr_chunks.cuh"
+#include "gdr_instrument.cuh"
 #include "tc_primitives.cuh"
 
 namespace gdr {
@@ -56,6 +57,7 @@ __global__ void __launch_bounds__(kScanThreads) cp_scan_kernel(Dims d, Workspace
   }
   __syncthreads();
   auto issue = [&](int step) {  // M^T of step `step` into buffer step & 1 (thread 0)
+    GDR_DELAY(30);
     const float* src = ws.cp_M + base + (size_t)(s_first + dir * step) * 16384;
     float* dst = mbuf + (step & 1) * 16384;
     tc::mbar_arrive_expect_tx(&bar[step & 1], kScanMBytes);
@@ -112,6 +114,7 @@ __global__ void __launch_bounds__(kScanThreads) cp_scan_kernel(Dims d, Workspace
       v.z += p4.z;
       v.w += p4.w;
     }
+    if (warp == 1) GDR_DELAY(31);  // one warp's part of the next X late
     *reinterpret_cast<float4*>(xs + tid * kScanCols) = v;
     *reinterpret_cast<float4*>(ws.cp_X + base + (size_t)s * 16384 + (size_t)tid * 128 + col0) = v;
     __syncthreads();

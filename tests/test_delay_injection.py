@@ -13,7 +13,8 @@ sleeps are microseconds against limits of seconds: nothing here can hang or faul
 The cases cover each kernel family: the fused backward (walk + gradients in one cooperative
 launch) at the benchmark's B=2, T=4096, H=16 shape; the fused forward (few long chains);
 variable length; Hv = 2 Hk (cluster-pair gradients); Hv = 4 Hk (partials + reduce); more state
-CTAs than SMs (single-buffered forward state).
+CTAs than SMs (single-buffered forward state); context-parallel segments (first-pass maps, the
+boundary scan with its bulk copies, the fused kernel's second pass; fixed and variable length).
 """
 import pytest
 import torch
@@ -26,13 +27,15 @@ from gdr_testlib import run_gpu
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # name, B, T, Hk, Hv, seqlens, layout, save_wy
-    ("fused_bwd_b2_t4096", 2, 4096, 16, 16, None, "KV", True),
-    ("fused_fwd_few_chains", 1, 2048, 2, 2, None, "VK", True),
-    ("varlen", 1, None, 4, 4, [0, 70, 130, 1, 200, 64, 1500], "KV", False),
-    ("pair_gva", 2, 512, 2, 4, None, "KV", True),
-    ("group_gva4", 1, 300, 1, 4, None, "VK", False),
-    ("single_buffered_state", 3, 200, 13, 13, None, "KV", True),
+    # name, B, T, Hk, Hv, seqlens, layout, save_wy, context-parallel segments (fwd, bwd)
+    ("fused_bwd_b2_t4096", 2, 4096, 16, 16, None, "KV", True, (1, 1)),
+    ("fused_fwd_few_chains", 1, 2048, 2, 2, None, "VK", True, (1, 1)),
+    ("varlen", 1, None, 4, 4, [0, 70, 130, 1, 200, 64, 1500], "KV", False, (1, 1)),
+    ("pair_gva", 2, 512, 2, 4, None, "KV", True, (1, 1)),
+    ("group_gva4", 1, 300, 1, 4, None, "VK", False, (1, 1)),
+    ("single_buffered_state", 3, 200, 13, 13, None, "KV", True, (1, 1)),
+    ("cp_fixed", 1, 3000, 2, 2, None, "KV", True, (5, 7)),
+    ("cp_varlen", 1, None, 1, 2, [900, 64, 1300], "VK", False, (3, 4)),
 ]
 
 
@@ -43,17 +46,17 @@ def delay_lib():
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_delayed_roles_give_bitwise_identical_results(delay_lib, case):
-    name, B, T, Hk, Hv, lens, layout, save_wy = case
+    name, B, T, Hk, Hv, lens, layout, save_wy, (cp_f, cp_b) = case
     if lens is None:
         w = small_workload(name, torch.bfloat16, B=B, T=T, Hk=Hk, Hv=Hv, DK=128, DV=128, layout=layout)
     else:
         w = small_workload(name, torch.bfloat16, Hk=Hk, Hv=Hv, DK=128, DV=128, seqlens=lens, layout=layout)
     inp = make_inputs(w)
-    ref = run_gpu(inp, save_wy=save_wy)
+    ref = run_gpu(inp, save_wy=save_wy, cp_fwd=cp_f, cp_bwd=cp_b)
     torch.cuda.synchronize()
     with gdr.library(delay_lib):
         for _ in range(2):  # two runs: the sleeps differ between them
-            got = run_gpu(inp, save_wy=save_wy)
+            got = run_gpu(inp, save_wy=save_wy, cp_fwd=cp_f, cp_bwd=cp_b)
             torch.cuda.synchronize()
             for key, t in ref.items():
                 if t is None:
