@@ -336,6 +336,9 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tm_q, const CUtenso
   int witem = s_item[0], c = s_item[1];
   int pub = -1;  // kFused: the flag index of the previous item, not yet published
   int it = 0;    // kFused: items done (stage it & 1, phase (it >> 1) & 1)
+  // !kFused, thread 0: the item whose tiles are already loading (issued once this item's last
+  // product had read its K/Q/V tiles)
+  int prefetched = -1;
   while (witem < n_items && ok) {
   const int j = witem % Hv, i = j / d.G;
   const int4 ci = idx_chunk(d, ws, c);
@@ -357,7 +360,7 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tm_q, const CUtenso
         publish_prep(ws.fwd_flags + pub);
         pub = -1;
       }
-    } else {
+    } else if (prefetched != witem) {
       issue_loads(witem, c, 0);
     }
   }
@@ -462,10 +465,19 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tm_q, const CUtenso
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutPrep));
   GDR_TRACE_MARK(0, 4);
   tc::tc_fence_after();
-  if (ok) {  // W rows (threads 0-63) and U rows (threads 64-127) staged in the free K/Q tiles
+  // !kFused: the products are done with this item's K/Q/V tiles, so the next item's load into
+  // them now, overlapping the stores below (W and U are staged in the T' and A tiles, free too)
+  if (!kFused && ok && tid == 0) {
+    const int wn = witem + (int)gridDim.x;
+    if (wn < n_items && idx_chunk(d, ws, wn / Hv).z > 0) {
+      issue_loads(wn, wn / Hv, 0);
+      prefetched = wn;
+    }
+  }
+  if (ok) {  // W rows (threads 0-63) and U rows (threads 64-127) staged in the free T' and A tiles
     const int r = tid & 63;
     const int col = tid < 64 ? 0 : 128;
-    unsigned char* stg = kq_t + (tid < 64 ? 0 : 2 * kSlab);
+    unsigned char* stg = sm + (tid < 64 ? PrepSmem::TT : PrepSmem::A);
     float v[64];
     tmem_ld64(tbase, warp, col, v);
     st_row_bf16(stg, r, v);
@@ -477,13 +489,13 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tm_q, const CUtenso
   tc::tc_fence_before();
   __syncthreads();
   if (ok && tid == 0) {
-    tc::tma_store_2d(&tm_w, kq_t, 0, (int)(ch * 64));
-    tc::tma_store_2d(&tm_w, kq_t + kSlab, 64, (int)(ch * 64));
-    tc::tma_store_2d(&tm_u, kq_t + 2 * kSlab, 0, (int)(ch * 64));
-    tc::tma_store_2d(&tm_u, kq_t + 3 * kSlab, 64, (int)(ch * 64));
+    tc::tma_store_2d(&tm_w, sm + PrepSmem::TT, 0, (int)(ch * 64));
+    tc::tma_store_2d(&tm_w, sm + PrepSmem::TT + kSlab, 64, (int)(ch * 64));
+    tc::tma_store_2d(&tm_u, sm + PrepSmem::A, 0, (int)(ch * 64));
+    tc::tma_store_2d(&tm_u, sm + PrepSmem::A + kSlab, 64, (int)(ch * 64));
     tc::bulk_commit();
   }
-  if (tid == 0) tc::bulk_wait_read<0>();  // staging tiles read before the next item's loads
+  if (tid == 0) tc::bulk_wait_read<0>();  // staging tiles read before the next item writes them
   GDR_TRACE_MARK(0, 5);
   item_par ^= 1;
   ++it;
