@@ -155,7 +155,8 @@ def write_margins(path: str, device_name: str) -> None:
             "(every token and chunk of those heads), oracle evaluated on the exact rounded inputs. Bar:",
             "2e-2 for bf16 inputs (and for bf16 saved states), 1e-4 for fp32 inputs. Modes: `recompute` =",
             "the backward recomputes the chunk factors; `saved` = the forward keeps them (the benchmark's",
-            "mode); `h bf16` = bf16 chunk-start states. `-` = the workload has no such output.", "",
+            "mode); `h bf16` = bf16 chunk-start states; `cp f/b` = context-parallel segments per",
+            "sequence, forward / backward. `-` = the workload has no such output.", "",
             "| workload | mode | heads | " + " | ".join(MARGIN_KEYS) + " | bar |",
             "|" + "---|" * (len(MARGIN_KEYS) + 4)]
     with open(path, "w") as f:

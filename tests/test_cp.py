@@ -99,3 +99,12 @@ def test_cp_auto_matches_oracle():
     res = run_gpu(inp, cp_fwd=gdr.GDR_CP_AUTO, cp_bwd=gdr.GDR_CP_AUTO)
     torch.cuda.synchronize()
     compare(res, reference(inp), tol_for(w.dtype))
+
+
+def test_cp_with_fused_prologue():
+    """Segments with raw inputs (q/k L2 norm, logsigmoid gate, sigmoid beta inside the operator)."""
+    w = small_workload("cp_prologue", torch.bfloat16, B=1, T=900, Hk=1, Hv=2, DK=128, DV=128)
+    inp = make_inputs(w, raw=True)
+    res = run_gpu(inp, prologue=7, cp_fwd=4, cp_bwd=5, save_wy=True)
+    torch.cuda.synchronize()
+    compare(res, reference(inp, prologue=7), tol_for(w.dtype))
