@@ -35,6 +35,9 @@ CASES = [
     # slow decay (g = logsigmoid(N(2, 1)), the long-sequence workload's gates): the transitions
     # barely contract, so errors in them are not damped along the scan
     ("slow_decay_t4096_p8", dict(B=1, T=4096, Hk=1, Hv=1, layout="VK", g_shift=2.0), dict(cp_fwd=8, cp_bwd=8)),
+    # very slow decay (g = logsigmoid(N(6, 1)), about -0.16 per chunk): the state remembers
+    # across many segments, so the transitions and the scan carry most of each boundary state
+    ("long_memory_t8192_p16", dict(B=1, T=8192, Hk=1, Hv=1, g_shift=6.0), dict(cp_fwd=16, cp_bwd=16)),
 ]
 
 
