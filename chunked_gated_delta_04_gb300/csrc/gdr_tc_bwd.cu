@@ -382,6 +382,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
   } else if (tid == kWalkCopyTid) {
     // ---------------------------------------------------------------- store + publish role
     int pub = -1;  // kPublish: the previous step's chunk, whose count is still due
+    const uint64_t keep = tc::l2_policy_evict_last();
     for (int it = 0; it < nch; ++it) {
       const int st = it & 1;
       const uint32_t ph = (it >> 1) & 1;
@@ -390,9 +391,9 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       if (!tc::mbar_wait(&bar_dh, it & 1, status, kBit)) break;
       GDR_TRACE_SINCE(3, 20, tc0_);
       GDR_DELAY(10);
-      if (stores) {
-        tc::tma_store_2d(&tm_dhs, sm + WS::DH, 0, (int)(chh * 128));
-        tc::tma_store_2d(&tm_dhs, sm + WS::DH + 16384, 64, (int)(chh * 128));
+      if (stores) {  // kept in L2 for the gradient item that reads them (evict_last)
+        tc::tma_store_2d_hint(&tm_dhs, sm + WS::DH, 0, (int)(chh * 128), keep);
+        tc::tma_store_2d_hint(&tm_dhs, sm + WS::DH + 16384, 64, (int)(chh * 128), keep);
         tc::bulk_commit();
         tc::bulk_wait_read<0>();  // the dh' tile has been read: the next dh' may replace it
       }
@@ -400,8 +401,8 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       if (!tc::mbar_wait(&bar_dvn[st], ph, status, kBit)) break;
       if (stores) {
         unsigned char* dvn = sm + WS::DVN + st * 16384;
-        tc::tma_store_2d(&tm_dvs, dvn, 0, (int)(chh * 64));
-        tc::tma_store_2d(&tm_dvs, dvn + kSlab, 64, (int)(chh * 64));
+        tc::tma_store_2d_hint(&tm_dvs, dvn, 0, (int)(chh * 64), keep);
+        tc::tma_store_2d_hint(&tm_dvs, dvn + kSlab, 64, (int)(chh * 64), keep);
         tc::bulk_commit();
         tc::bulk_wait_read<0>();
       }
@@ -830,11 +831,12 @@ __device__ __forceinline__ void grad_body(
       GDR_TRACE_INFO_ADD(4, GDR_TRACE_NOW() - tf0_);
       GDR_TRACE_SINCE(2, 20, tw0);
       tc::mbar_arrive_expect_tx(bar, (d.h_bf16 ? 18 : 22) * kSlab + 256);
+      const uint64_t once = tc::l2_policy_evict_first();  // read once: released first
       for (int q4 = 0; q4 < 4; ++q4)  // dh' rows (q4 & 1) * 64.., columns (q4 >> 1) * 64..
-        tc::tma_load_2d(sm + S::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
-                        (int)(ch2 * 128 + (q4 & 1) * 64));
-      tc::tma_load_2d(sm + S::DVN, &tm_dvn, bar, 0, (int)(ch2 * 64));
-      tc::tma_load_2d(sm + S::DVN + S::OD_SLAB, &tm_dvn, bar, 64, (int)(ch2 * 64));
+        tc::tma_load_2d_hint(sm + S::DH + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_dh, bar, (q4 >> 1) * 64,
+                             (int)(ch2 * 128 + (q4 & 1) * 64), once);
+      tc::tma_load_2d_hint(sm + S::DVN, &tm_dvn, bar, 0, (int)(ch2 * 64), once);
+      tc::tma_load_2d_hint(sm + S::DVN + S::OD_SLAB, &tm_dvn, bar, 64, (int)(ch2 * 64), once);
     }
     if (groups & kLdW) {  // Vn (in U's place in memory) into W's tile, once the dv store has read it
       tc::tma_load_2d(sm + S::W, &tm_u, bar, 0, (int)(ch2 * 64));
