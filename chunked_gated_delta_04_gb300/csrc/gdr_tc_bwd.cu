@@ -261,6 +261,7 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
   if (tid == kWalkLoadTid) {
     // ---------------------------------------------------------------- load role
     const uint64_t keep = tc::l2_policy_evict_last();
+    const uint64_t keep_kq = d.G == 1 ? keep : tc::l2_policy_evict_normal();
     auto issue_loads = [&](int it) {
       const int st = it & 1, tc0 = tok0_of(it);
       const size_t chh = (size_t)chunk_of(it) * Hv + j;
@@ -272,12 +273,14 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       const bool dO_tiles = !zero_do;
       tc::mbar_arrive_expect_tx(bar, (dO_tiles ? 9 : 4) * kSlab + 256);
       tc::bulk_load(base + WS::GAM, ws.gam + chh * 64, 256, bar);
-      // q, k and dO are read again by the chunk's gradient item: kept in L2 (evict_last)
-      tc::tma_load_3d_hint(base + WS::KQ, &tm_k, bar, 0, i, tc0, keep);
-      tc::tma_load_3d_hint(base + WS::KQ + 2 * kSlab, &tm_k, bar, 64, i, tc0, keep);
+      // q, k and dO are read again by the chunk's gradient item: kept in L2 (evict_last), whose
+      // load lets them go (evict_first); q and k only with one v-head per q/k head, where that
+      // item is their last reader
+      tc::tma_load_3d_hint(base + WS::KQ, &tm_k, bar, 0, i, tc0, keep_kq);
+      tc::tma_load_3d_hint(base + WS::KQ + 2 * kSlab, &tm_k, bar, 64, i, tc0, keep_kq);
       if (dO_tiles) {
-        tc::tma_load_3d_hint(base + WS::KQ + kSlab, &tm_q, bar, 0, i, tc0, keep);
-        tc::tma_load_3d_hint(base + WS::KQ + 3 * kSlab, &tm_q, bar, 64, i, tc0, keep);
+        tc::tma_load_3d_hint(base + WS::KQ + kSlab, &tm_q, bar, 0, i, tc0, keep_kq);
+        tc::tma_load_3d_hint(base + WS::KQ + 3 * kSlab, &tm_q, bar, 64, i, tc0, keep_kq);
         tc::tma_load_3d_hint(base + WS::DO, &tm_do, bar, 0, j, tc0, keep);
         tc::tma_load_3d_hint(base + WS::DO + kSlab, &tm_do, bar, 64, j, tc0, keep);
         tc::tma_load_2d(base + WS::P, &tm_p, bar, 0, (int)(chh * 64));
@@ -846,12 +849,20 @@ __device__ __forceinline__ void grad_body(
     }
     if (groups & kLdRest) {
       tc::bulk_load(sm + S::GAM, ws.gam + ch2 * 64, 256, bar);
-      // K and Q: the walk left them in L2; with one v-head per q/k head this is their last reader
-      const uint64_t kq_pol = d.G == 1 ? tc::l2_policy_evict_first() : tc::l2_policy_evict_last();
-      tc::tma_load_3d_hint(sm + S::KQ, &tm_k, bar, 0, i2, tt, kq_pol);
-      tc::tma_load_3d_hint(sm + S::KQ + 2 * kSlab, &tm_k, bar, 64, i2, tt, kq_pol);
-      tc::tma_load_3d_hint(sm + S::KQ + kSlab, &tm_q, bar, 0, i2, tt, kq_pol);
-      tc::tma_load_3d_hint(sm + S::KQ + 3 * kSlab, &tm_q, bar, 64, i2, tt, kq_pol);
+      // K and Q: the walk left them in L2; with one v-head per q/k head this is their last
+      // reader (evict_first), else the other v-heads' items read them too (no policy)
+      if (d.G == 1) {
+        const uint64_t once = tc::l2_policy_evict_first();
+        tc::tma_load_3d_hint(sm + S::KQ, &tm_k, bar, 0, i2, tt, once);
+        tc::tma_load_3d_hint(sm + S::KQ + 2 * kSlab, &tm_k, bar, 64, i2, tt, once);
+        tc::tma_load_3d_hint(sm + S::KQ + kSlab, &tm_q, bar, 0, i2, tt, once);
+        tc::tma_load_3d_hint(sm + S::KQ + 3 * kSlab, &tm_q, bar, 64, i2, tt, once);
+      } else {
+        tc::tma_load_3d(sm + S::KQ, &tm_k, bar, 0, i2, tt);
+        tc::tma_load_3d(sm + S::KQ + 2 * kSlab, &tm_k, bar, 64, i2, tt);
+        tc::tma_load_3d(sm + S::KQ + kSlab, &tm_q, bar, 0, i2, tt);
+        tc::tma_load_3d(sm + S::KQ + 3 * kSlab, &tm_q, bar, 64, i2, tt);
+      }
       if (d.h_bf16) {  // h (bf16) straight into its operand tile, laid out like dh'
         for (int q4 = 0; q4 < 4; ++q4)
           tc::tma_load_2d(sm + S::H + (q4 >> 1) * 16384 + (q4 & 1) * kSlab, &tm_h, bar, (q4 >> 1) * 64,
