@@ -465,8 +465,9 @@ __device__ __forceinline__ void prep_body(const CUtensorMap& tm_q, const CUtenso
   ok = __syncthreads_and(ok && tc::mbar_wait(&bar_mma, 1, ws.status, kDevErrTimeoutPrep));
   GDR_TRACE_MARK(0, 4);
   tc::tc_fence_after();
-  // !kFused: the products are done with this item's K/Q/V tiles, so the next item's load into
-  // them now, overlapping the stores below (W and U are staged in the T' and A tiles, free too)
+  // !kFused: the products are done with this item's K/Q/V tiles, so the next item's tiles load
+  // into them now, overlapping the stores below (W and U are staged in the T' and A tiles, free
+  // too)
   if (!kFused && ok && tid == 0) {
     const int wn = witem + (int)gridDim.x;
     if (wn < n_items && idx_chunk(d, ws, wn / Hv).z > 0) {
