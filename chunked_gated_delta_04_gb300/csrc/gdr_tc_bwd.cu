@@ -386,7 +386,11 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
     (void)tc::mbar_wait(&bar_drain, 0, status, kBit);
   } else if (tid == kWalkCopyTid) {
     // ---------------------------------------------------------------- store + publish role
-    int pub = -1;  // kPublish: the previous step's chunk, whose count is still due
+    // kPublish: chunks stored whose counts are still due: the previous step's (pub) and, every
+    // other step, the one before (held).  The counts go out in pairs, so the GPU-scope release
+    // that orders each count after its chunk's stores is paid back to back every second step
+    // instead of once a step on the copy thread's path to the next dh' store.
+    int pub = -1, held = -1;
     const uint64_t keep = tc::l2_policy_evict_last();
     for (int it = 0; it < nch; ++it) {
       const int st = it & 1;
@@ -413,16 +417,25 @@ __device__ __forceinline__ void walk_body(const CUtensorMap& tm_q, const CUtenso
       }
       tc::mbar_arrive(&bar_dvnfree[st]);
       GDR_TRACE_CLK(tc1_);
-      if (kPublish && stores && pub >= 0) {  // the previous step's two groups have landed
-        tc::bulk_wait<2>();
-        GDR_DELAY(11);
-        publish_chunk(ws.walk_flags + (size_t)pub * Hv + j);
+      if (kPublish && stores && pub >= 0) {
+        if (held >= 0) {  // the two previous steps' groups have landed: both counts
+          tc::bulk_wait<2>();
+          GDR_DELAY(11);
+          publish_chunk(ws.walk_flags + (size_t)held * Hv + j);
+          publish_chunk(ws.walk_flags + (size_t)pub * Hv + j);
+          held = -1;
+        } else {
+          held = pub;
+        }
       }
       GDR_TRACE_SINCE(3, 21, tc1_);
       pub = chunk_of(it);
     }
     tc::bulk_wait<0>();
-    if (kPublish && stores && pub >= 0) publish_chunk(ws.walk_flags + (size_t)pub * Hv + j);
+    if (kPublish && stores) {
+      if (held >= 0) publish_chunk(ws.walk_flags + (size_t)held * Hv + j);
+      if (pub >= 0) publish_chunk(ws.walk_flags + (size_t)pub * Hv + j);
+    }
   } else if (tid < 256) {
     // ---------------------------------------------------------------- epilogue warps
     const int ln = (warp & 3) * 32 + lane;  // TMEM lane: token of accV (lanes 0-63), dk of accH
