@@ -111,3 +111,39 @@ def test_cp_with_fused_prologue():
     res = run_gpu(inp, prologue=7, cp_fwd=4, cp_bwd=5, save_wy=True)
     torch.cuda.synchronize()
     compare(res, reference(inp, prologue=7), tol_for(w.dtype))
+
+
+def _segment_scan_oracle(inp, P):
+    """The contract's outputs from the fp64 segment-scan oracle (oracle/context_parallel.py) with P
+    segments per sequence, in the layouts oracle.reference returns."""
+    import numpy as np
+
+    from oracle.context_parallel import cp_backward, cp_forward
+
+    f = lambda t: None if t is None else t.detach().double().numpy()
+    q, k, v, g, beta, dO = (f(inp[n]) for n in ("q", "k", "v", "g", "beta", "dO"))
+    B, T, Hk, DK = q.shape
+    Hv, DV = v.shape[2], v.shape[3]
+    cu = inp["cu_seqlens"].numpy() if inp["cu_seqlens"] is not None else np.arange(B + 1) * T
+    kv = inp["layout"] == "KV"
+    to_S = lambda x: None if x is None else (np.swapaxes(x, -1, -2).copy() if kv else x)
+    pk = lambda a: a.reshape(B * T, *a.shape[2:])
+    scale = 1.0 / np.sqrt(DK)
+    o, S_T, states = cp_forward(cu, Hk, Hv, scale, pk(q), pk(k), pk(v), pk(g), pk(beta), to_S(f(inp["S0"])), P)
+    dq, dk, dv, dg, dbeta, dS0 = cp_backward(cu, Hk, Hv, scale, pk(q), pk(k), pk(v), pk(g), pk(beta),
+                                             to_S(f(inp["S0"])), pk(dO), to_S(f(inp["dS_T"])), P)
+    return {"o": o.reshape(B, T, Hv, DV), "S_T": to_S(S_T), "h_saved": np.swapaxes(states, -1, -2),
+            "dq": dq.reshape(q.shape), "dk": dk.reshape(k.shape), "dv": dv.reshape(v.shape),
+            "dg": dg.reshape(B, T, Hv), "dbeta": dbeta.reshape(B, T, Hv), "dS0": to_S(dS0)}
+
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8])
+def test_cp_matches_segment_scan_oracle(P):
+    """The GPU's segment passes against the fp64 segment-scan oracle with the same segment count,
+    on ragged and empty sequences with grouped v-heads."""
+    w = small_workload("cp_vs_scan_oracle", torch.bfloat16, Hk=1, Hv=2, DK=128, DV=128,
+                       seqlens=[0, 77, 700, 1000], layout="VK")
+    inp = make_inputs(w)
+    res = run_gpu(inp, cp_fwd=P, cp_bwd=P, save_wy=True)
+    torch.cuda.synchronize()
+    compare(res, _segment_scan_oracle(inp, P), tol_for(w.dtype))
